@@ -1,0 +1,223 @@
+"""fp64 reference definitions of exact attention (test infrastructure only).
+
+All functions take numpy arrays (any float dtype; they are upcast to float64)
+in (batch, heads, seq_len, head_dim) layout.  K and V may have fewer heads
+than Q (grouped-query attention): query head h reads key/value head
+h // (H // Hkv), i.e. contiguous groups of G = H / Hkv query heads share one
+K/V head, which equals repeating each K/V head G times along the head axis.
+
+Sources (page title, section):
+  [FA]  "Flash Attention原理：分块计算与重计算，如何降低O(n^2)的显存占用"
+  [SDPA] "SDPA backend 与 FlashAttention"
+  [SEL] "PyTorch scaled dot product attention怎样选择高效注意力后端"
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+
+
+def gqa_kv_head(h: int, H: int, Hkv: int) -> int:
+    """K/V head read by query head h.  [SEL] (section on why the same code can
+    select different backends) only says the query and key/value head counts
+    must satisfy a constraint; the reading taken is Hkv divides H and
+    contiguous groups: h -> h // (H / Hkv)."""
+    if H % Hkv:
+        raise ValueError("Hkv must divide H")
+    return h // (H // Hkv)
+
+
+def _check(q, k, v):
+    if q.ndim != 4 or k.ndim != 4 or v.ndim != 4:
+        raise ValueError("expected (B, H, N, d) tensors")
+    B, H, N, d = q.shape
+    if k.shape[0] != B or v.shape[0] != B or k.shape[1] != v.shape[1]:
+        raise ValueError("batch / kv-head mismatch")
+    if k.shape[2] != v.shape[2] or k.shape[3] != d:
+        raise ValueError("key length / head_dim mismatch")
+    gqa_kv_head(0, H, k.shape[1])
+    return B, H, k.shape[1], N, k.shape[2], d
+
+
+def _scores(qh, kh, scale, causal, rows=None):
+    """S = scale * Q K^T for one head, with the causal mask applied.
+
+    [FA] §一 step 1-2 (S = Q K^T, softmax of S / sqrt(d)); the causal mask of
+    [SDPA] §3 (is_causal=True) sets S_ij = -inf for key j > query i (queries
+    and keys share positions 0..N-1).  ``rows`` selects absolute query rows.
+    """
+    if rows is None:
+        rows = np.arange(qh.shape[0])
+    S = scale * (qh[rows] @ kh.T)
+    if causal:
+        cols = np.arange(kh.shape[0])
+        S = np.where(cols[None, :] > np.asarray(rows)[:, None], -np.inf, S)
+    return S
+
+
+def softmax_rows(S):
+    """Max-subtracted softmax along the last axis ([FA] §四:
+    softmax(x_i) = exp(x_i - max x) / sum_j exp(x_j - max x)).
+    Returns (P, m, l) with m the row max and l the row sum of exp(S - m)."""
+    S = np.asarray(S, dtype=np.float64)
+    m = S.max(axis=-1, keepdims=True)
+    E = np.exp(S - m)
+    l = E.sum(axis=-1, keepdims=True)
+    return E / l, m[..., 0], l[..., 0]
+
+
+def softmax_two_block(x):
+    """The two-block merge of [FA] §四 on the last axis of x.
+
+    The last axis is split in half; each half gets its own max m1, m2 and
+    exp-sum e1, e2; the global max is m = max(m1, m2) and the global sum is
+    l = e1 * exp(m1 - m) + e2 * exp(m2 - m); both halves are then normalised
+    with the global m and l.  Works in x's own float dtype (the page's check
+    is in float32)."""
+    x = np.asarray(x)
+    mid = x.shape[-1] // 2
+    x1, x2 = x[..., :mid], x[..., mid:]
+    m1 = x1.max(axis=-1, keepdims=True)
+    m2 = x2.max(axis=-1, keepdims=True)
+    m = np.maximum(m1, m2)
+    e1 = np.exp(x1 - m1).sum(axis=-1, keepdims=True)
+    e2 = np.exp(x2 - m2).sum(axis=-1, keepdims=True)
+    l = e1 * np.exp(m1 - m) + e2 * np.exp(m2 - m)
+    return np.concatenate([np.exp(x1 - m) / l, np.exp(x2 - m) / l], axis=-1)
+
+
+def attention_forward(q, k, v, scale=None, causal=False):
+    """O = softmax(scale * Q K^T [+ causal mask]) V and lse, in float64.
+
+    [FA] §一 (standard attention: S, P and O materialised per head) with the
+    stable softmax of §四.  lse_i = m_i + ln(l_i) is the natural-log
+    logsumexp of row i of the scaled, masked scores: the single per-row
+    statistic that replaces the m and l of §五.
+    Returns O (B, H, N, d_v) and lse (B, H, N).
+    """
+    q = np.asarray(q, dtype=np.float64)
+    k = np.asarray(k, dtype=np.float64)
+    v = np.asarray(v, dtype=np.float64)
+    B, H, Hkv, N, Nk, d = _check(q, k, v)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    O = np.empty((B, H, N, v.shape[3]))
+    lse = np.empty((B, H, N))
+    for b in range(B):
+        for h in range(H):
+            hk = gqa_kv_head(h, H, Hkv)
+            S = _scores(q[b, h], k[b, hk], scale, causal)
+            P, m, l = softmax_rows(S)
+            O[b, h] = P @ v[b, hk]
+            lse[b, h] = m + np.log(l)
+    return O, lse
+
+
+def attention_forward_rows(qh, kh, vh, rows, scale, causal=False):
+    """Forward for a subset of absolute query rows of ONE head.
+
+    Same definition as ``attention_forward``; the causal mask uses the
+    absolute row indices, so sampled rows of a full-size head can be checked
+    one by one.  qh: (N, d), kh/vh: (Nk, d).  Returns O (len(rows), d_v),
+    lse (len(rows),)."""
+    qh = np.asarray(qh, dtype=np.float64)
+    kh = np.asarray(kh, dtype=np.float64)
+    vh = np.asarray(vh, dtype=np.float64)
+    rows = np.asarray(rows)
+    S = _scores(qh, kh, scale, causal, rows)
+    P, m, l = softmax_rows(S)
+    return P @ vh, m + np.log(l)
+
+
+def attention_forward_online(q, k, v, scale=None, causal=False, block=64):
+    """Forward by the blockwise online-softmax recurrence of [FA] §三-§四.
+
+    Keys/values are visited in blocks of ``block`` columns.  For each row a
+    running max m and normaliser l are kept together with the unnormalised
+    output acc; when block j arrives with local max m_j:
+        m_new = max(m, m_j)
+        acc   = acc * exp(m - m_new) + exp(S_j - m_new) V_j
+        l     = l   * exp(m - m_new) + rowsum(exp(S_j - m_new))
+    and at the end O = acc / l, lse = m + ln l.  No blocking beyond the key
+    blocks; used only to pin the two-pass = online equivalence.
+    """
+    q = np.asarray(q, dtype=np.float64)
+    k = np.asarray(k, dtype=np.float64)
+    v = np.asarray(v, dtype=np.float64)
+    B, H, Hkv, N, Nk, d = _check(q, k, v)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    O = np.empty((B, H, N, v.shape[3]))
+    lse = np.empty((B, H, N))
+    for b in range(B):
+        for h in range(H):
+            hk = gqa_kv_head(h, H, Hkv)
+            S = _scores(q[b, h], k[b, hk], scale, causal)
+            m = np.full(N, -np.inf)
+            l = np.zeros(N)
+            acc = np.zeros((N, v.shape[3]))
+            for j0 in range(0, Nk, block):
+                Sj = S[:, j0:j0 + block]
+                m_new = np.maximum(m, Sj.max(axis=1))
+                # rows whose every key so far is masked keep m = -inf
+                alive = np.isfinite(m_new)
+                shift = np.where(alive, m_new, 0.0)
+                alpha = np.where(np.isfinite(m), np.exp(m - shift), 0.0)
+                E = np.exp(Sj - shift[:, None])
+                acc = acc * alpha[:, None] + E @ v[b, hk, j0:j0 + block]
+                l = l * alpha + E.sum(axis=1)
+                m = m_new
+            O[b, h] = acc / l[:, None]
+            lse[b, h] = m + np.log(l)
+    return O, lse
+
+
+def attention_backward(q, k, v, do, scale=None, causal=False):
+    """Analytic gradients of O = softmax(scale Q K^T [+mask]) V w.r.t. Q, K, V.
+
+    The pages ([FA] §五 and FAQ Q19) say the backward recomputes P and follows
+    the chain rule without printing it; the textbook derivation is written out
+    per head with the oracle's own fp64 P:
+        dV   = P^T dO
+        dP   = dO V^T
+        D_i  = sum_j P_ij dP_ij            (softmax Jacobian-vector product)
+        dS   = P * (dP - D 1^T)            (masked entries have P = 0)
+        dQ   = scale * dS K
+        dK   = scale * dS^T Q
+    With grouped-query attention the dK, dV of a K/V head are the sums over
+    the G query heads that read it.  Returns dQ, dK, dV in float64.
+    """
+    q = np.asarray(q, dtype=np.float64)
+    k = np.asarray(k, dtype=np.float64)
+    v = np.asarray(v, dtype=np.float64)
+    do = np.asarray(do, dtype=np.float64)
+    B, H, Hkv, N, Nk, d = _check(q, k, v)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    dq = np.zeros_like(q)
+    dk = np.zeros_like(k)
+    dv = np.zeros_like(v)
+    for b in range(B):
+        for h in range(H):
+            hk = gqa_kv_head(h, H, Hkv)
+            S = _scores(q[b, h], k[b, hk], scale, causal)
+            P, _, _ = softmax_rows(S)
+            dv[b, hk] += P.T @ do[b, h]
+            dP = do[b, h] @ v[b, hk].T
+            D = (P * dP).sum(axis=1)
+            dS = P * (dP - D[:, None])
+            dq[b, h] = scale * (dS @ k[b, hk])
+            dk[b, hk] += scale * (dS.T @ q[b, h])
+    return dq, dk, dv
+
+
+def score_matrix_bytes(n: int, bytes_per_elem: int = 4) -> int:
+    """Bytes of one n x n score (or probability) matrix ([FA] §一)."""
+    return n * n * bytes_per_elem
+
+
+def row_stat_bytes(n: int, n_stats: int = 2, bytes_per_elem: int = 4) -> int:
+    """Bytes of the per-row statistics kept instead of S and P ([FA] §五:
+    m(n) and l(n))."""
+    return n * n_stats * bytes_per_elem

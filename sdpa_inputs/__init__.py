@@ -1,0 +1,125 @@
+"""Seeded synthetic inputs for exact scaled-dot-product attention.
+
+This module is shared by the CPU oracle tests, the GPU parity tests and the
+benchmark.  It holds no attention arithmetic: only the workload shapes, the
+seeded random draws and the round-to-nearest-even conversion to bf16 that
+turns each draw into exactly representable bf16 values.
+
+Workloads (all tensors in (batch, heads, seq_len, head_dim) layout, the layout
+used by the "Flash Attention原理：分块计算与重计算" page, §一, and by the
+SDPA call on "SDPA backend 与 FlashAttention", §3):
+
+  c1   B=1  H=2   Hkv=2  N=256  d=64   non-causal   seed 1
+  c2   B=4  H=16  Hkv=16 N=2048 d=128  causal       seed 2   (LLM prefill)
+  c3   B=1  H=96  Hkv=96 N=4096 d=64   non-causal   seed 3   (GPT-3 layer of §一)
+  c3c  same shape, causal                            seed 3
+  c4   B=1  H=32  Hkv=8  N=8192 d=128  causal, x0.5 seed 4   (long-context GQA)
+  c4p  same, head_dim 80 zero-padded to 96, scale 1/sqrt(80)  seed 4
+  c5   B=8  H=16  Hkv=16 N=4096 d=128  causal, fwd+bwd (dO drawn)  seed 5
+
+Every draw is numpy's PCG64 ``default_rng(seed).standard_normal(dtype=float32)``
+taken in the fixed order Q, K, V, dO, multiplied by the config's amplitude and
+then rounded to bf16 (round to nearest, ties to even).
+"""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass, replace
+
+import numpy as np
+
+
+@dataclass(frozen=True)
+class Workload:
+    name: str
+    B: int
+    H: int
+    Hkv: int
+    N: int
+    d: int
+    causal: bool
+    seed: int
+    amp: float = 1.0
+    d_draw: int | None = None      # head_dim actually drawn (zero-padded up to d)
+    with_grad: bool = False        # also draw dO
+    scale: float | None = None     # default 1/sqrt(d_draw or d)
+
+    @property
+    def softmax_scale(self) -> float:
+        if self.scale is not None:
+            return self.scale
+        return 1.0 / math.sqrt(self.d_draw or self.d)
+
+    @property
+    def G(self) -> int:
+        return self.H // self.Hkv
+
+
+WORKLOADS: dict[str, Workload] = {
+    "c1": Workload("c1", 1, 2, 2, 256, 64, False, 1),
+    "c2": Workload("c2", 4, 16, 16, 2048, 128, True, 2),
+    "c3": Workload("c3", 1, 96, 96, 4096, 64, False, 3),
+    "c3c": Workload("c3c", 1, 96, 96, 4096, 64, True, 3),
+    "c4": Workload("c4", 1, 32, 8, 8192, 128, True, 4, amp=0.5),
+    "c4p": Workload("c4p", 1, 32, 8, 8192, 96, True, 4, amp=0.5, d_draw=80),
+    "c5": Workload("c5", 8, 16, 16, 4096, 128, True, 5, with_grad=True),
+}
+
+
+def workload(name: str, **overrides) -> Workload:
+    """A named workload, optionally with fields replaced (e.g. a smaller N)."""
+    w = WORKLOADS[name]
+    return replace(w, **overrides) if overrides else w
+
+
+def round_bf16(x: np.ndarray) -> np.ndarray:
+    """Round float32 values to the nearest bf16 (ties to even); returns float32.
+
+    bf16 keeps the upper 16 bits of an IEEE float32.  Adding 0x7FFF plus the
+    lowest kept bit before truncating implements round-to-nearest-even for
+    finite inputs (the draws here are always finite).
+    """
+    u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32)
+    bias = ((u >> np.uint32(16)) & np.uint32(1)) + np.uint32(0x7FFF)
+    r = (u + bias) & np.uint32(0xFFFF0000)
+    return r.view(np.float32)
+
+
+def draw(rng: np.random.Generator, shape, amp: float) -> np.ndarray:
+    x = rng.standard_normal(size=shape, dtype=np.float32)
+    if amp != 1.0:
+        x *= np.float32(amp)
+    return round_bf16(x)
+
+
+def make_inputs(w: Workload) -> dict[str, np.ndarray]:
+    """Q, K, V (and dO when the workload has a backward pass) as float32
+    arrays whose values are exactly representable in bf16."""
+    rng = np.random.default_rng(w.seed)
+    dd = w.d_draw or w.d
+    q = draw(rng, (w.B, w.H, w.N, dd), w.amp)
+    k = draw(rng, (w.B, w.Hkv, w.N, dd), w.amp)
+    v = draw(rng, (w.B, w.Hkv, w.N, dd), w.amp)
+    out = {"q": q, "k": k, "v": v}
+    if w.with_grad:
+        out["do"] = draw(rng, (w.B, w.H, w.N, dd), 1.0)
+    if dd != w.d:
+        pad = [(0, 0)] * 3 + [(0, w.d - dd)]
+        out = {n: np.pad(a, pad) for n, a in out.items()}
+    return out
+
+
+def make_random(shape, seed: int, amp: float = 1.0) -> np.ndarray:
+    """One seeded bf16-exact float32 tensor (small parity sweeps)."""
+    return draw(np.random.default_rng(seed), shape, amp)
+
+
+def flops_forward(B: int, H: int, N: int, d: int, causal: bool) -> float:
+    """Forward work convention: 4*B*H*N^2*d, halved when causal."""
+    f = 4.0 * B * H * N * N * d
+    return f / 2 if causal else f
+
+
+def flops_backward(B: int, H: int, N: int, d: int, causal: bool) -> float:
+    """Backward work convention: 2.5x the forward."""
+    return 2.5 * flops_forward(B, H, N, d, causal)
