@@ -1,0 +1,133 @@
+/*
+ * attn.h — C ABI of a GB300 (sm_103a) library for exact scaled-dot-product
+ * attention, computed FlashAttention-style.
+ *
+ * What is computed (page "Flash Attention原理：分块计算与重计算，如何降低O(n^2)的
+ * 显存占用", §一 and §四):
+ *     S = scale * Q K^T            (n x n per head; causal: S_ij = -inf for j > i)
+ *     P = softmax(S) row-wise      (max-subtracted, exact)
+ *     O = P V
+ * The n x n matrices S and P are never written to device memory: the forward
+ * pass tiles Q, K and V through shared memory and tensor memory with a running
+ * row max and row sum (the online softmax of §四) and stores only O and one
+ * per-row statistic (§五 keeps m and l; here lse = m + ln l, natural log of
+ * the scaled, masked scores).  The backward pass recomputes P tile by tile
+ * from lse (§五, "recomputation") and returns dQ, dK, dV.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Element type: bf16 (IEEE bfloat16) for Q, K, V, O, dO, dQ, dK, dV;
+ *    float32 for lse.  Accumulation is float32.
+ *  - Layout: dense row-major (B, H, N, d) for Q, O, dO, dQ and (B, Hkv, N, d)
+ *    for K, V, dK, dV (the (batch, num_heads, seq_len, head_dim) layout of the
+ *    page above, §一); lse is (B, H, N).  Strides are implied by the shape.
+ *  - Grouped-query attention: Hkv must divide H; query head h reads K/V head
+ *    h / (H / Hkv) (contiguous groups).  Hkv == H is ordinary multi-head.
+ *  - Supported head_dim d: 64, 96, 128.  Any N >= 1.  Queries and keys share
+ *    positions 0..N-1; the causal mask hides key j from query i when j > i.
+ *  - All pointers are DEVICE pointers owned by the caller, 16-byte aligned.
+ *    The library never allocates or frees device memory and keeps no pointer
+ *    after a call returns.
+ *  - stream: a cudaStream_t (NULL = legacy default stream).  Work is enqueued
+ *    asynchronously; a return of ATTN_OK means the arguments were valid and
+ *    the kernels were launched, not that they have finished.
+ *  - Errors are returned, never hidden: there is no fallback path.  A bad
+ *    argument returns an error before anything is launched.  A device-side
+ *    wait that runs past its time limit makes the kernel stop early and
+ *    record ATTN_ERR_TIMEOUT in a device status word, which
+ *    attn_get_device_status() reports.
+ *  - Device: a GPU of compute capability 10.3 (GB300); others give
+ *    ATTN_ERR_UNSUPPORTED_DEVICE.
+ */
+#ifndef SDPA08_ATTN_H
+#define SDPA08_ATTN_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  ATTN_OK = 0,
+  ATTN_ERR_INVALID_ARG = 1,        /* null pointer, non-finite scale, bad flag   */
+  ATTN_ERR_UNSUPPORTED_SHAPE = 2,  /* d not in {64,96,128}, H % Hkv != 0, size < 1 or too large */
+  ATTN_ERR_UNSUPPORTED_DEVICE = 3, /* current device is not compute capability 10.3 */
+  ATTN_ERR_MISALIGNED = 4,         /* a pointer is not 16-byte aligned            */
+  ATTN_ERR_WORKSPACE = 5,          /* workspace missing or smaller than required  */
+  ATTN_ERR_LAUNCH = 6,             /* the CUDA launch itself failed               */
+  ATTN_ERR_TIMEOUT = 7,            /* a device-side wait ran out (reported by attn_get_device_status) */
+  ATTN_ERR_CUDA = 8                /* another CUDA runtime/driver error           */
+} attn_status_t;
+
+/*
+ * Forward pass.  Page "Flash Attention原理", §三 (tiling), §四 (online softmax),
+ * §五 (store only per-row statistics).
+ *   q    [in]  bf16 (B, H, N, d)
+ *   k, v [in]  bf16 (B, Hkv, N, d)
+ *   o    [out] bf16 (B, H, N, d)          O = softmax(scale*QK^T [+mask]) V
+ *   lse  [out] float32 (B, H, N)          ln sum_j exp(scale*q_i.k_j) over unmasked j
+ *   scale      softmax scale (1/sqrt(d) for standard attention); finite and > 0
+ *   causal     0 or 1
+ * Outputs must not overlap inputs.
+ */
+attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+                       int B, int H, int Hkv, int N, int d, float scale, int causal,
+                       void* stream);
+
+/*
+ * Bytes of device workspace attn_bwd needs for this shape: a float32 dQ
+ * accumulator and two float32 per-row vectors, each padded to a multiple of
+ * 128 rows per head.  Returns 0 for an invalid shape.
+ */
+size_t attn_bwd_workspace_size(int B, int H, int Hkv, int N, int d);
+
+/*
+ * Backward pass.  Page "Flash Attention原理", §五 (recompute P from the stored
+ * statistic instead of keeping S and P) and FAQ Q19 (gradients by the chain
+ * rule); the gradients are those of softmax-then-matmul:
+ *   dV = P^T dO,  dP = dO V^T,  dS = P * (dP - rowsum(dO * O)),
+ *   dQ = scale dS K,  dK = scale dS^T Q   (dK, dV summed over a GQA group).
+ *   q, k, v, o [in] as in attn_fwd;  lse [in] float32 (B, H, N) from attn_fwd
+ *   dout [in]  bf16 (B, H, N, d)  gradient of the loss w.r.t. O
+ *   dq   [out] bf16 (B, H, N, d);  dk, dv [out] bf16 (B, Hkv, N, d)
+ *   workspace  device buffer of at least attn_bwd_workspace_size() bytes,
+ *              owned by the caller; its contents on entry are ignored and on
+ *              return are unspecified.  It must not overlap any other argument.
+ */
+attn_status_t attn_bwd(const void* q, const void* k, const void* v, const void* o,
+                       const float* lse, const void* dout,
+                       void* dq, void* dk, void* dv,
+                       void* workspace, size_t workspace_bytes,
+                       int B, int H, int Hkv, int N, int d, float scale, int causal,
+                       void* stream);
+
+/*
+ * Synchronises `stream`, then returns (and clears) the device status word
+ * that the kernels set when a bounded wait runs out: ATTN_OK or
+ * ATTN_ERR_TIMEOUT; ATTN_ERR_CUDA if the synchronisation itself failed.
+ */
+attn_status_t attn_get_device_status(void* stream);
+
+/* Human-readable name of a status code (static storage; never NULL). */
+const char* attn_status_string(attn_status_t s);
+
+/* ABI version of this header (incremented on incompatible changes). */
+int attn_abi_version(void);
+
+/*
+ * Self-test of the bounded-wait machinery: launches one CTA whose threads
+ * wait, with a limit of `timeout_us` microseconds, on an on-chip barrier that
+ * nothing ever signals.  The kernel must give up, record ATTN_ERR_TIMEOUT
+ * and exit, leaving the context usable.  Returns ATTN_OK if launched; read
+ * the outcome with attn_get_device_status().  The pages have no counterpart;
+ * this exists so the failure-detection path can be tested without faulting
+ * or hanging a GPU.
+ */
+attn_status_t attn_selftest_wait_timeout(unsigned int timeout_us, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SDPA08_ATTN_H */

@@ -1,0 +1,164 @@
+"""Python binding of the GB300 exact-attention library (argument marshalling only).
+
+The functions ``attn_fwd``, ``attn_bwd``, ``attn_bwd_workspace_size``,
+``attn_get_device_status``, ``attn_status_string`` and
+``attn_selftest_wait_timeout`` call the C ABI of ``include/attn.h`` with raw
+device pointers.  ``forward`` and ``backward`` are conveniences that take
+torch CUDA tensors, allocate the outputs (and the backward workspace) with
+torch and call the same C ABI; they compute nothing themselves.
+
+There is no fallback: if the compiled library is missing, or the device is
+not a GB300, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import enum
+import math
+import os
+
+from .build import LIB, build  # noqa: F401  (build() is the supported way to compile)
+
+__all__ = [
+    "AttnError", "Status", "load", "attn_fwd", "attn_bwd", "attn_bwd_workspace_size",
+    "attn_get_device_status", "attn_status_string", "attn_selftest_wait_timeout",
+    "forward", "backward", "build",
+]
+
+
+class Status(enum.IntEnum):
+    OK = 0
+    INVALID_ARG = 1
+    UNSUPPORTED_SHAPE = 2
+    UNSUPPORTED_DEVICE = 3
+    MISALIGNED = 4
+    WORKSPACE = 5
+    LAUNCH = 6
+    TIMEOUT = 7
+    CUDA = 8
+
+
+class AttnError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = Status(status) if status in Status._value2member_map_ else status
+        super().__init__(f"{where}: {attn_status_string(status)}")
+
+
+_lib = None
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+
+
+def load() -> ctypes.CDLL:
+    """Load the in-tree shared library (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB):
+            raise RuntimeError(f"CUDA library not built ({LIB} missing): run __graft_entry__.build()")
+        lib = ctypes.CDLL(LIB)
+        lib.attn_fwd.argtypes = [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, ctypes.c_float, _I, _P]
+        lib.attn_fwd.restype = _I
+        lib.attn_bwd_workspace_size.argtypes = [_I, _I, _I, _I, _I]
+        lib.attn_bwd_workspace_size.restype = ctypes.c_size_t
+        lib.attn_bwd.argtypes = [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t,
+                                 _I, _I, _I, _I, _I, ctypes.c_float, _I, _P]
+        lib.attn_bwd.restype = _I
+        lib.attn_get_device_status.argtypes = [_P]
+        lib.attn_get_device_status.restype = _I
+        lib.attn_status_string.argtypes = [_I]
+        lib.attn_status_string.restype = ctypes.c_char_p
+        lib.attn_abi_version.argtypes = []
+        lib.attn_abi_version.restype = _I
+        lib.attn_selftest_wait_timeout.argtypes = [ctypes.c_uint, _P]
+        lib.attn_selftest_wait_timeout.restype = _I
+        _lib = lib
+    return _lib
+
+
+# ------------------------------------------------------------------ raw C ABI
+def attn_status_string(status: int) -> str:
+    return load().attn_status_string(int(status)).decode()
+
+
+def attn_fwd(q, k, v, o, lse, B, H, Hkv, N, d, scale, causal, stream) -> int:
+    return load().attn_fwd(q, k, v, o, lse, B, H, Hkv, N, d, scale, int(causal), stream)
+
+
+def attn_bwd_workspace_size(B, H, Hkv, N, d) -> int:
+    return load().attn_bwd_workspace_size(B, H, Hkv, N, d)
+
+
+def attn_bwd(q, k, v, o, lse, dout, dq, dk, dv, workspace, workspace_bytes,
+             B, H, Hkv, N, d, scale, causal, stream) -> int:
+    return load().attn_bwd(q, k, v, o, lse, dout, dq, dk, dv, workspace, workspace_bytes,
+                           B, H, Hkv, N, d, scale, int(causal), stream)
+
+
+def attn_get_device_status(stream=None) -> int:
+    return load().attn_get_device_status(stream)
+
+
+def attn_selftest_wait_timeout(timeout_us: int, stream=None) -> int:
+    return load().attn_selftest_wait_timeout(timeout_us, stream)
+
+
+# ------------------------------------------------------------ torch marshalling
+def _check(status: int, where: str):
+    if status != 0:
+        raise AttnError(status, where)
+
+
+def _shape(q, k, v):
+    if q.dim() != 4 or k.dim() != 4 or v.dim() != 4:
+        raise ValueError("q, k, v must be (B, H, N, d)")
+    B, H, N, d = q.shape
+    Hkv = k.shape[1]
+    if tuple(k.shape) != (B, Hkv, N, d) or tuple(v.shape) != (B, Hkv, N, d):
+        raise ValueError("k and v must be (B, Hkv, N, d) with q's B, N, d")
+    return B, H, Hkv, N, d
+
+
+def _stream_ptr(t):
+    import torch
+    return torch.cuda.current_stream(t.device).cuda_stream
+
+
+def forward(q, k, v, scale: float | None = None, causal: bool = False, out=None, lse=None):
+    """O, lse = attention(q, k, v) on the current CUDA stream.
+
+    q: bf16 (B, H, N, d); k, v: bf16 (B, Hkv, N, d); all contiguous on one
+    CUDA device.  Returns O bf16 (B, H, N, d) and lse float32 (B, H, N)."""
+    import torch
+    B, H, Hkv, N, d = _shape(q, k, v)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    for t in (q, k, v):
+        if not t.is_contiguous() or t.dtype != torch.bfloat16:
+            raise ValueError("inputs must be contiguous bf16")
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    _check(attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
+                    B, H, Hkv, N, d, scale, causal, _stream_ptr(q)), "attn_fwd")
+    return out, lse
+
+
+def backward(q, k, v, o, lse, dout, scale: float | None = None, causal: bool = False,
+             workspace=None):
+    """dQ, dK, dV of attention given the forward's O and lse and dL/dO."""
+    import torch
+    B, H, Hkv, N, d = _shape(q, k, v)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    dq = torch.empty_like(q)
+    dk = torch.empty_like(k)
+    dv = torch.empty_like(v)
+    ws_bytes = attn_bwd_workspace_size(B, H, Hkv, N, d)
+    if workspace is None:
+        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=q.device)
+    _check(attn_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                    dout.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
+                    workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+                    B, H, Hkv, N, d, scale, causal, _stream_ptr(q)), "attn_bwd")
+    return dq, dk, dv

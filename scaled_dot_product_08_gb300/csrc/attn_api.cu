@@ -1,0 +1,278 @@
+// attn_api.cu — the C ABI declared in include/attn.h: argument validation,
+// TMA tensor-map construction, device checks, the device status word and the
+// bounded-wait self-test.  No computation happens here; every step of the
+// attention path runs in the kernels of attn_fwd.cu / attn_bwd.cu.
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <initializer_list>
+#include <mutex>
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "../../include/attn.h"
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s per wait
+
+// Written by kernels when a bounded wait gives up (0 = fine).
+__device__ int g_status_word;
+
+struct DeviceInfo {
+  bool probed = false;
+  bool supported = false;
+  int* status = nullptr;  // device address of g_status_word
+};
+DeviceInfo g_dev[kMaxDevices];
+std::mutex g_dev_mu;
+
+// Probes the current device once: compute capability 10.3 and the device
+// address of the status word (cudaGetSymbolAddress, with that device current).
+attn_status_t current_device(DeviceInfo** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return ATTN_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return ATTN_ERR_UNSUPPORTED_DEVICE;
+  std::lock_guard<std::mutex> lk(g_dev_mu);
+  DeviceInfo& di = g_dev[dev];
+  if (!di.probed) {
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+      return ATTN_ERR_CUDA;
+    di.supported = (major == 10 && minor == 3);
+    if (di.supported) {
+      void* p = nullptr;
+      if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) return ATTN_ERR_CUDA;
+      di.status = static_cast<int*>(p);
+    }
+    di.probed = true;
+  }
+  if (!di.supported) return ATTN_ERR_UNSUPPORTED_DEVICE;
+  *out = &di;
+  return ATTN_OK;
+}
+
+// cuTensorMapEncodeTiled from the driver, looked up once through the runtime
+// (no link-time dependency on libcuda).
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// 3-D map over a dense bf16 (rows = B*heads, N, d) tensor: box of 64 columns
+// (128 bytes) x 128 rows x 1 head, 128-byte swizzle.  Rows past N and
+// columns past d read as zero and are never written.
+bool make_map_bf16(CUtensorMap* m, const void* ptr, int d, int N, long long heads) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)N, (cuuint64_t)heads};
+  cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)d * 2 * (cuuint64_t)N};
+  cuuint32_t box[3] = {64, 128, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Shape checks shared by forward and backward.
+attn_status_t check_shape(int B, int H, int Hkv, int N, int d) {
+  if (B < 1 || H < 1 || Hkv < 1 || N < 1) return ATTN_ERR_UNSUPPORTED_SHAPE;
+  if (d != 64 && d != 96 && d != 128) return ATTN_ERR_UNSUPPORTED_SHAPE;
+  if (H % Hkv != 0) return ATTN_ERR_UNSUPPORTED_SHAPE;
+  const long long bh = (long long)B * H;
+  const long long ntile = (N + 255) / 256;
+  if (bh > (1ll << 30) || (long long)N > (1ll << 30) || bh * ntile > 0x7fffffffll ||
+      bh * ((N + 127) / 128) > 0x7fffffffll)
+    return ATTN_ERR_UNSUPPORTED_SHAPE;
+  return ATTN_OK;
+}
+
+attn_status_t check_scale_flag(float scale, int causal) {
+  if (!std::isfinite(scale) || !(scale > 0.f)) return ATTN_ERR_INVALID_ARG;
+  if (causal != 0 && causal != 1) return ATTN_ERR_INVALID_ARG;
+  return ATTN_OK;
+}
+
+// Every pointer must be non-null and 16-byte aligned (checked on the host,
+// for all pointers, before any CUDA call) and must be device memory.
+attn_status_t check_ptrs(std::initializer_list<const void*> ps) {
+  for (const void* p : ps)
+    if (p == nullptr) return ATTN_ERR_INVALID_ARG;
+  for (const void* p : ps)
+    if (!aligned16(p)) return ATTN_ERR_MISALIGNED;
+  for (const void* p : ps) {
+    cudaPointerAttributes a;
+    if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+      cudaGetLastError();
+      return ATTN_ERR_INVALID_ARG;
+    }
+    if (a.type != cudaMemoryTypeDevice && a.type != cudaMemoryTypeManaged) return ATTN_ERR_INVALID_ARG;
+  }
+  return ATTN_OK;
+}
+
+__global__ void selftest_wait_kernel(int* status, unsigned long long limit_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    sdpa::mbar_init(sdpa::smem_u32(&bar), 1);
+    abort_flag = 0;
+    sdpa::fence_mbar_init();
+  }
+  __syncthreads();
+  const sdpa::WaitCtx wc{&abort_flag, status, limit_ns};
+  // Nothing ever arrives on `bar`: every thread must give up and return.
+  (void)sdpa::wait_bounded(wc, sdpa::smem_u32(&bar), 0);
+  __syncthreads();
+}
+
+}  // namespace
+
+#define ATTN_TRY(x)                     \
+  do {                                  \
+    attn_status_t _s = (x);             \
+    if (_s != ATTN_OK) return _s;       \
+  } while (0)
+
+extern "C" {
+
+int attn_abi_version(void) { return 1; }
+
+const char* attn_status_string(attn_status_t s) {
+  switch (s) {
+    case ATTN_OK: return "ATTN_OK";
+    case ATTN_ERR_INVALID_ARG: return "ATTN_ERR_INVALID_ARG";
+    case ATTN_ERR_UNSUPPORTED_SHAPE: return "ATTN_ERR_UNSUPPORTED_SHAPE";
+    case ATTN_ERR_UNSUPPORTED_DEVICE: return "ATTN_ERR_UNSUPPORTED_DEVICE";
+    case ATTN_ERR_MISALIGNED: return "ATTN_ERR_MISALIGNED";
+    case ATTN_ERR_WORKSPACE: return "ATTN_ERR_WORKSPACE";
+    case ATTN_ERR_LAUNCH: return "ATTN_ERR_LAUNCH";
+    case ATTN_ERR_TIMEOUT: return "ATTN_ERR_TIMEOUT";
+    case ATTN_ERR_CUDA: return "ATTN_ERR_CUDA";
+  }
+  return "ATTN_ERR_UNKNOWN";
+}
+
+attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Hkv,
+                       int N, int d, float scale, int causal, void* stream) {
+  ATTN_TRY(check_shape(B, H, Hkv, N, d));
+  ATTN_TRY(check_scale_flag(scale, causal));
+  ATTN_TRY(check_ptrs({q, k, v, o, lse}));
+  DeviceInfo* di = nullptr;
+  ATTN_TRY(current_device(&di));
+
+  CUtensorMap tq, tk, tv, to;
+  if (!make_map_bf16(&tq, q, d, N, (long long)B * H) || !make_map_bf16(&tk, k, d, N, (long long)B * Hkv) ||
+      !make_map_bf16(&tv, v, d, N, (long long)B * Hkv) || !make_map_bf16(&to, o, d, N, (long long)B * H))
+    return ATTN_ERR_CUDA;
+
+  sdpa::FwdParams p;
+  p.lse = lse;
+  p.B = B;
+  p.H = H;
+  p.Hkv = Hkv;
+  p.N = N;
+  p.G = H / Hkv;
+  p.n_mtiles = (N + 255) / 256;
+  p.nkv = (N + 127) / 128;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.status = di->status;
+  p.limit_ns = kWaitLimitNs;
+  cudaError_t e = sdpa::launch_fwd(d, causal != 0, tq, tk, tv, to, p, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return ATTN_ERR_LAUNCH;
+  return ATTN_OK;
+}
+
+size_t attn_bwd_workspace_size(int B, int H, int Hkv, int N, int d) {
+  if (check_shape(B, H, Hkv, N, d) != ATTN_OK) return 0;
+  const size_t npad = (size_t)((N + 127) / 128) * 128;
+  const size_t rows = (size_t)B * H * npad;
+  return rows * (size_t)d * 4 + rows * 4 * 2;
+}
+
+attn_status_t attn_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                       const void* dout, void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes,
+                       int B, int H, int Hkv, int N, int d, float scale, int causal, void* stream) {
+  ATTN_TRY(check_shape(B, H, Hkv, N, d));
+  ATTN_TRY(check_scale_flag(scale, causal));
+  if (workspace == nullptr || workspace_bytes < attn_bwd_workspace_size(B, H, Hkv, N, d))
+    return ATTN_ERR_WORKSPACE;
+  ATTN_TRY(check_ptrs({q, k, v, o, lse, dout, dq, dk, dv, workspace}));
+  DeviceInfo* di = nullptr;
+  ATTN_TRY(current_device(&di));
+
+  CUtensorMap tq, tk, tv, tdo, tdk, tdv;
+  if (!make_map_bf16(&tq, q, d, N, (long long)B * H) || !make_map_bf16(&tk, k, d, N, (long long)B * Hkv) ||
+      !make_map_bf16(&tv, v, d, N, (long long)B * Hkv) || !make_map_bf16(&tdo, dout, d, N, (long long)B * H) ||
+      !make_map_bf16(&tdk, dk, d, N, (long long)B * Hkv) || !make_map_bf16(&tdv, dv, d, N, (long long)B * Hkv))
+    return ATTN_ERR_CUDA;
+
+  const int npad = ((N + 127) / 128) * 128;
+  const size_t rows = (size_t)B * H * npad;
+  sdpa::BwdParams p;
+  p.o = static_cast<const uint16_t*>(o);
+  p.dout = static_cast<const uint16_t*>(dout);
+  p.lse = lse;
+  p.dq = static_cast<uint16_t*>(dq);
+  p.dq_acc = static_cast<float*>(workspace);
+  p.dvec = p.dq_acc + rows * (size_t)d;
+  p.lse2 = p.dvec + rows;
+  p.B = B;
+  p.H = H;
+  p.Hkv = Hkv;
+  p.N = N;
+  p.Npad = npad;
+  p.G = H / Hkv;
+  p.d = d;
+  p.nq = (N + 127) / 128;
+  p.scale = scale;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.status = di->status;
+  p.limit_ns = kWaitLimitNs;
+  cudaError_t e = sdpa::launch_bwd(d, causal != 0, tq, tk, tv, tdo, tdk, tdv, p, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return ATTN_ERR_LAUNCH;
+  return ATTN_OK;
+}
+
+attn_status_t attn_get_device_status(void* stream) {
+  DeviceInfo* di = nullptr;
+  ATTN_TRY(current_device(&di));
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return ATTN_ERR_CUDA;
+  int host = 0;
+  if (cudaMemcpyFromSymbol(&host, g_status_word, sizeof(int)) != cudaSuccess) return ATTN_ERR_CUDA;
+  if (host != 0) {
+    const int zero = 0;
+    if (cudaMemcpyToSymbol(g_status_word, &zero, sizeof(int)) != cudaSuccess) return ATTN_ERR_CUDA;
+  }
+  return host == 0 ? ATTN_OK : (host == sdpa::kDevTimeout ? ATTN_ERR_TIMEOUT : ATTN_ERR_CUDA);
+}
+
+attn_status_t attn_selftest_wait_timeout(unsigned int timeout_us, void* stream) {
+  DeviceInfo* di = nullptr;
+  ATTN_TRY(current_device(&di));
+  if (timeout_us == 0 || timeout_us > 5000000u) return ATTN_ERR_INVALID_ARG;
+  selftest_wait_kernel<<<1, 64, 0, static_cast<cudaStream_t>(stream)>>>(di->status,
+                                                                         (unsigned long long)timeout_us * 1000ull);
+  return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;
+}
+
+}  // extern "C"

@@ -1,0 +1,397 @@
+// attn_fwd.cu — forward pass of exact attention on sm_103a.
+//
+// Method (page "Flash Attention原理：分块计算与重计算，如何降低O(n^2)的显存占用"):
+// Q is split into 128-row tiles and K/V into 128-row tiles (§三); each local
+// score tile S_ij = Q_i K_j^T lives only in tensor memory; a running row max
+// m and row sum l are updated per tile and the old output is rescaled by
+// exp(m_old - m_new) (§四); only O and the per-row logsumexp reach global
+// memory (§五).
+//
+// GB300 mapping (one CTA per SM, 384 threads = 3 warpgroups):
+//   warps 0-3  softmax warpgroup for query tile 0 (one thread per row)
+//   warps 4-7  softmax warpgroup for query tile 1
+//   warp  8    TMA producer: Q tiles once, then K_j / V_j into a smem ring
+//   warp  9    MMA issuer (one thread): tcgen05 S = Q K^T and O += P V
+//   warps 10-11 idle
+// setmaxnreg moves registers from the producer/MMA warpgroup (72 each) to
+// the softmax warpgroups (216 each): 2*128*216 + 128*72 = 384*168, the
+// block's launch allocation.
+// Tensor memory (512 columns x 128 lanes x 32 bit):
+//   [  0,128) S0 (fp32), P0 (bf16 pairs) overwrites its first 64 columns
+//   [128,256) S1 / P1
+//   [256,256+d) O0 (fp32),  [384,384+d) O1
+// The two query tiles ping-pong: while one softmax warpgroup turns S into P,
+// the tensor core runs the other tile's P V and next Q K^T.
+//
+// Softmax details: scores are handled in base 2 (x * scale * log2 e, one FFMA
+// per element, ex2.approx).  The running max used for the exponent is only
+// raised when the tile max exceeds it by more than 8 (a factor 256), so the
+// O rescale in TMEM is rare; the result is exact either way because the final
+// normalisation uses the same max as every exponent.
+#include <cmath>
+
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace sdpa {
+
+template <int D>
+struct FwdTraits {
+  static constexpr int NB = (D + 63) / 64;           // 64-column (128-byte) blocks per row
+  static constexpr int BLOCK_BYTES = 128 * 128;      // [128 rows x 128 B]
+  static constexpr int TILE_BYTES = NB * BLOCK_BYTES;
+  static constexpr int NSTAGE = (D == 64) ? 8 : 4;   // K/V ring depth
+  static constexpr int KSTEPS = D / 16;              // K=16 steps of Q K^T
+  static constexpr int NBAR = 2 + 2 * NSTAGE + 2 + 2 + 2 + 1;
+  static constexpr int SMEM = 1024 + (2 + NSTAGE) * TILE_BYTES + NBAR * 8 + 16;
+  static constexpr int THREADS = 384;
+};
+
+template <int D, bool CAUSAL>
+__global__ void __launch_bounds__(384, 1)
+    fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+               const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
+               const FwdParams p) {
+  using T = FwdTraits<D>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* const gbase = smem_raw + (base - raw);
+
+  const uint32_t sQ = base;                          // 2 query tiles
+  const uint32_t sKV = base + 2 * T::TILE_BYTES;     // K/V ring
+  const uint32_t sBar = sKV + T::NSTAGE * T::TILE_BYTES;
+  const uint32_t bQ = sBar;                          // q_full[2]
+  const uint32_t bKVf = sBar + 8u * 2;               // kv_full[NSTAGE]
+  const uint32_t bKVe = bKVf + 8u * T::NSTAGE;       // kv_empty[NSTAGE]
+  const uint32_t bS = bKVe + 8u * T::NSTAGE;         // s_full[2]
+  const uint32_t bP = bS + 16u;                      // p_full[2]
+  const uint32_t bO = bP + 16u;                      // o_full[2]
+  const uint32_t bDrain = bO + 16u;
+  uint8_t* const misc = gbase + (sBar - base) + 8 * T::NBAR;
+  uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(misc);
+  volatile int* const abort_flag = reinterpret_cast<volatile int*>(misc + 4);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  // Work unit: head-major so the CTAs in flight share few K/V heads (L2
+  // reuse); within a head the heaviest causal query tiles go first.
+  const int bh = blockIdx.x / p.n_mtiles;
+  const int mt = p.n_mtiles - 1 - (int)(blockIdx.x % p.n_mtiles);
+  const int bhk = (bh / p.H) * p.Hkv + (bh % p.H) / p.G;
+  int n0 = p.nkv, n1 = p.nkv;  // key tiles visited by query tile 0 / 1
+  if (CAUSAL) {
+    n0 = min(2 * mt + 1, p.nkv);
+    n1 = min(2 * mt + 2, p.nkv);
+  }
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(bQ + 8u * s, 1);
+      mbar_init(bS + 8u * s, 1);
+      mbar_init(bP + 8u * s, 128);
+      mbar_init(bO + 8u * s, 1);
+    }
+    for (int i = 0; i < T::NSTAGE; ++i) {
+      mbar_init(bKVf + 8u * i, 1);
+      mbar_init(bKVe + 8u * i, 1);
+    }
+    mbar_init(bDrain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 9) {
+    tmem_alloc(smem_u32(tmem_slot), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
+  const WaitCtx wc{abort_flag, p.status, p.limit_ns};
+
+  if (warp < 8) {
+    setmaxnreg_inc<216>();
+    // ------------------------------------------------------------ softmax
+    const int s = warp >> 2;            // query tile of this warpgroup
+    const int r = threadIdx.x & 127;    // row within the tile == TMEM lane
+    const int qi = 2 * mt + s;          // global query tile index
+    const int n = s ? n1 : n0;
+    const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+    const uint32_t tS = tmem + s * 128 + lane_off;
+    const uint32_t tO = tmem + 256 + s * 128 + lane_off;
+    const uint32_t barS = bS + 8u * s, barP = bP + 8u * s, barO = bO + 8u * s;
+    const float c = p.scale_log2;
+    float m = -INFINITY, l = 0.f;
+    bool ok = true;
+
+    for (int j = 0; j < n; ++j) {
+      ok = __all_sync(0xffffffffu, wait_bounded(wc, barS, j & 1));
+      if (!ok) break;
+      tc_fence_after();
+      float x[128];
+      {
+        uint32_t ra[32], rb[32], rc[32], rd[32];
+        tmem_ld32(tS + 0, ra);
+        tmem_ld32(tS + 32, rb);
+        tmem_ld32(tS + 64, rc);
+        tmem_ld32(tS + 96, rd);
+        tmem_wait_ld();
+        reg_fence(ra);
+        reg_fence(rb);
+        reg_fence(rc);
+        reg_fence(rd);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          x[i] = __uint_as_float(ra[i]);
+          x[32 + i] = __uint_as_float(rb[i]);
+          x[64 + i] = __uint_as_float(rc[i]);
+          x[96 + i] = __uint_as_float(rd[i]);
+        }
+      }
+      if (CAUSAL) {
+        if (j == qi) {  // diagonal tile: key column i > row r is masked
+#pragma unroll
+          for (int i = 0; i < 128; ++i)
+            if (i > r) x[i] = -INFINITY;
+        }
+      } else if (j == p.nkv - 1) {  // ragged key tail
+        const int lim = p.N - j * 128;
+#pragma unroll
+        for (int i = 0; i < 128; ++i)
+          if (i >= lim) x[i] = -INFINITY;
+      }
+      float mx[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) mx[k] = x[k];
+#pragma unroll
+      for (int i = 8; i < 128; ++i) mx[i & 7] = fmaxf(mx[i & 7], x[i]);
+      const float tile_max = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                                   fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+      const float mc = tile_max * c;
+      const bool raise = mc > m + 8.0f;  // always true on the first tile
+      float alpha = 1.f;
+      if (raise) {
+        alpha = ex2(m - mc);
+        m = mc;
+      }
+      if (j > 0 && __any_sync(0xffffffffu, raise)) {
+        // O_acc <- alpha * O_acc for this warp's 32 rows (PV of tile j-1 has
+        // completed: its commit precedes S_j's).
+#pragma unroll
+        for (int cc = 0; cc < D / 32; ++cc) {
+          uint32_t o[32];
+          tmem_ld32(tO + cc * 32, o);
+          tmem_wait_ld();
+          reg_fence(o);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+          tmem_st32(tO + cc * 32, o);
+        }
+      }
+      float sum[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) sum[k] = 0.f;
+#pragma unroll
+      for (int i = 0; i < 128; ++i) {
+        x[i] = ex2(fmaf(x[i], c, -m));
+        sum[i & 7] += x[i];
+      }
+      l = l * alpha + (((sum[0] + sum[1]) + (sum[2] + sum[3])) + ((sum[4] + sum[5]) + (sum[6] + sum[7])));
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        uint32_t pk[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) pk[i] = pack_bf16(x[64 * h + 2 * i], x[64 * h + 2 * i + 1]);
+        tmem_st32(tS + 32 * h, pk);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(barP);
+    }
+
+    // ------------------------------------------------------------ epilogue
+    if (ok) ok = __all_sync(0xffffffffu, wait_bounded(wc, barO, 0));
+    const uint32_t sOut = sQ + s * T::TILE_BYTES;  // Q tile is dead once O is final
+    if (ok) {
+      tc_fence_after();
+      const float inv = 1.f / l;
+#pragma unroll
+      for (int cc = 0; cc < D / 32; ++cc) {
+        uint32_t o[32];
+        tmem_ld32(tO + cc * 32, o);
+        tmem_wait_ld();
+        reg_fence(o);
+        const int blk = (cc * 32) / 64, ch0 = ((cc * 32) % 64) / 8;
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {
+          uint32_t w[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            w[e] = pack_bf16(__uint_as_float(o[q4 * 8 + 2 * e]) * inv, __uint_as_float(o[q4 * 8 + 2 * e + 1]) * inv);
+          st_shared_v4(sOut + blk * T::BLOCK_BYTES + sw128_offset(r, ch0 + q4), w[0], w[1], w[2], w[3]);
+        }
+      }
+      fence_proxy_async_smem();
+    }
+    named_bar_sync(1 + s, 128);
+    if (ok) {
+      if (r == 0 && qi * 128 < p.N) {
+        for (int cb = 0; cb < T::NB; ++cb)
+          tma_store_3d(&tmO, sOut + cb * T::BLOCK_BYTES, cb * 64, qi * 128, bh);
+        bulk_commit();
+        bulk_wait_read_all();
+      }
+      const int row = qi * 128 + r;
+      if (row < p.N) p.lse[(size_t)bh * p.N + row] = (m + log2f(l)) * 0.69314718055994531f;
+    }
+    setmaxnreg_dec<168>();  // one register budget again for the common teardown
+  } else {
+    setmaxnreg_dec<72>();
+    if (warp == 8) {
+      // ------------------------------------------------------------ producer
+      if (lane == 0) {
+        tma_prefetch_desc(&tmQ);
+        tma_prefetch_desc(&tmK);
+        tma_prefetch_desc(&tmV);
+        for (int s = 0; s < 2; ++s) {
+          mbar_expect_tx(bQ + 8u * s, T::TILE_BYTES);
+          for (int c = 0; c < T::NB; ++c)
+            tma_load_3d(sQ + s * T::TILE_BYTES + c * T::BLOCK_BYTES, &tmQ, bQ + 8u * s, c * 64,
+                        (2 * mt + s) * 128, bh);
+        }
+        bool ok = true;
+        int t = 0;  // ring slot counter: K_j is slot 2j, V_j is slot 2j+1
+        for (int j = 0; j < n1 && ok; ++j) {
+          for (int w = 0; w < 2; ++w) {
+            const int st = t % T::NSTAGE, rd = t / T::NSTAGE;
+            if (rd > 0 && !(ok = wait_bounded(wc, bKVe + 8u * st, (rd - 1) & 1))) break;
+            mbar_expect_tx(bKVf + 8u * st, T::TILE_BYTES);
+            const CUtensorMap* m = (w == 0) ? &tmK : &tmV;
+            for (int c = 0; c < T::NB; ++c)
+              tma_load_3d(sKV + st * T::TILE_BYTES + c * T::BLOCK_BYTES, m, bKVf + 8u * st, c * 64, j * 128, bhk);
+            ++t;
+          }
+        }
+        // Every copy this thread issued has landed before the CTA may exit
+        // (immediate on the normal path; matters after an abort).
+        for (int s = 0; s < 2; ++s) wait_drain(bQ + 8u * s, 0, p.limit_ns);
+        for (int i = 0; i < T::NSTAGE && i < t; ++i) {
+          const int last = ((t - 1 - i) / T::NSTAGE) * T::NSTAGE + i;
+          wait_drain(bKVf + 8u * i, (last / T::NSTAGE) & 1, p.limit_ns);
+        }
+      }
+      __syncwarp();
+    } else if (warp == 9) {
+      // ------------------------------------------------------------ MMA issuer
+      if (lane == 0) {
+        constexpr uint32_t IQK = idesc_bf16_f32(128, 128, false, false);
+        constexpr uint32_t IPV = idesc_bf16_f32(128, D, false, true);
+        const uint32_t tS0 = tmem, tS1 = tmem + 128, tO0 = tmem + 256, tO1 = tmem + 384;
+        auto qk = [&](uint32_t dS, uint32_t q_tile, uint32_t k_tile) {
+  #pragma unroll
+          for (int kk = 0; kk < T::KSTEPS; ++kk) {
+            const uint32_t off = (kk >> 2) * T::BLOCK_BYTES + (kk & 3) * 32;
+            mma_ss(dS, sdesc_sw128(q_tile + off, 16, 1024), sdesc_sw128(k_tile + off, 16, 1024), IQK, kk > 0);
+          }
+        };
+        auto pv = [&](uint32_t dO, uint32_t p_tmem, uint32_t v_tile, bool acc) {
+  #pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            mma_ts(dO, p_tmem + kk * 8, sdesc_sw128(v_tile + kk * 2048, T::BLOCK_BYTES, 1024), IPV,
+                   (acc || kk > 0) ? 1u : 0u);
+        };
+        bool ok = wait_bounded(wc, bKVf, 0) && wait_bounded(wc, bQ, 0);
+        if (ok) {
+          tc_fence_after();
+          qk(tS0, sQ, sKV);
+          mma_commit(bS);
+          ok = wait_bounded(wc, bQ + 8u, 0);
+        }
+        if (ok) {
+          tc_fence_after();
+          qk(tS1, sQ + T::TILE_BYTES, sKV);
+          mma_commit(bS + 8u);
+          mma_commit(bKVe);  // K_0 consumed
+        }
+        int t = 1;
+        for (int j = 0; j < n1 && ok; ++j, t += 2) {
+          const int sv = t % T::NSTAGE, sk = (t + 1) % T::NSTAGE;
+          const bool next = j + 1 < n1;
+          if (!(ok = wait_bounded(wc, bKVf + 8u * sv, (t / T::NSTAGE) & 1))) break;
+          if (next && !(ok = wait_bounded(wc, bKVf + 8u * sk, ((t + 1) / T::NSTAGE) & 1))) break;
+          const uint32_t vt = sKV + sv * T::TILE_BYTES, kt = sKV + sk * T::TILE_BYTES;
+          if (j < n0) {
+            if (!(ok = wait_bounded(wc, bP, j & 1))) break;
+            tc_fence_after();
+            pv(tO0, tS0, vt, j > 0);
+            if (j + 1 < n0) {
+              qk(tS0, sQ, kt);
+              mma_commit(bS);
+            } else {
+              mma_commit(bO);
+            }
+          }
+          if (!(ok = wait_bounded(wc, bP + 8u, j & 1))) break;
+          tc_fence_after();
+          pv(tO1, tS1, vt, j > 0);
+          if (next) {
+            qk(tS1, sQ + T::TILE_BYTES, kt);
+            mma_commit(bS + 8u);
+          } else {
+            mma_commit(bO + 8u);
+          }
+          mma_commit(bKVe + 8u * sv);
+          if (next) mma_commit(bKVe + 8u * sk);
+        }
+        mma_commit(bDrain);  // fires once every MMA issued above has finished
+        wait_drain(bDrain, 0, p.limit_ns);
+      }
+      __syncwarp();
+    }
+    setmaxnreg_inc<168>();
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 9) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+size_t fwd_smem_bytes(int d) {
+  switch (d) {
+    case 64: return FwdTraits<64>::SMEM;
+    case 96: return FwdTraits<96>::SMEM;
+    case 128: return FwdTraits<128>::SMEM;
+    default: return 0;
+  }
+}
+
+template <int D, bool C>
+static cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                                const CUtensorMap& to, const FwdParams& p, cudaStream_t stream) {
+  auto kern = fwd_kernel<D, C>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, FwdTraits<D>::SMEM);
+  if (e != cudaSuccess) return e;
+  const unsigned grid = (unsigned)p.n_mtiles * (unsigned)(p.B * p.H);
+  kern<<<grid, FwdTraits<D>::THREADS, FwdTraits<D>::SMEM, stream>>>(tq, tk, tv, to, p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_fwd(int d, bool causal, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                       const CUtensorMap& to, const FwdParams& p, cudaStream_t stream) {
+  switch (d) {
+    case 64: return causal ? launch_fwd_t<64, true>(tq, tk, tv, to, p, stream)
+                           : launch_fwd_t<64, false>(tq, tk, tv, to, p, stream);
+    case 96: return causal ? launch_fwd_t<96, true>(tq, tk, tv, to, p, stream)
+                           : launch_fwd_t<96, false>(tq, tk, tv, to, p, stream);
+    case 128: return causal ? launch_fwd_t<128, true>(tq, tk, tv, to, p, stream)
+                            : launch_fwd_t<128, false>(tq, tk, tv, to, p, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace sdpa

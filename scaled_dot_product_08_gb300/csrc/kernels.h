@@ -1,0 +1,51 @@
+// kernels.h — internal launch interface between the C ABI (attn_api.cu) and
+// the kernel translation units.  Not part of the public ABI.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace sdpa {
+
+// Forward kernel arguments (tensor maps are passed separately).
+struct FwdParams {
+  float* lse;            // (B, H, N) float32
+  int B, H, Hkv, N, G;   // G = H / Hkv
+  int n_mtiles;          // ceil(N / 256): one CTA = two 128-row query tiles
+  int nkv;               // ceil(N / 128): key/value tiles
+  float scale_log2;      // scale * log2(e)
+  int* status;           // device status word
+  unsigned long long limit_ns;  // bounded-wait limit
+};
+
+// Backward arguments.
+struct BwdParams {
+  const uint16_t* o;     // (B, H, N, d) bf16
+  const uint16_t* dout;  // (B, H, N, d) bf16
+  const float* lse;      // (B, H, N)
+  uint16_t* dq;          // (B, H, N, d) bf16
+  float* dq_acc;         // (B, H, Npad, d) float32 workspace
+  float* dvec;           // (B, H, Npad) float32: D = rowsum(dO * O)
+  float* lse2;           // (B, H, Npad) float32: lse * log2(e), +inf on padding rows
+  int B, H, Hkv, N, Npad, G, d;
+  int nq;                // ceil(N / 128)
+  float scale;           // softmax scale
+  float scale_log2;      // scale * log2(e)
+  int* status;
+  unsigned long long limit_ns;
+};
+
+// Shared-memory bytes of each kernel instance (for validation and launch).
+size_t fwd_smem_bytes(int d);
+size_t bwd_smem_bytes(int d);
+
+cudaError_t launch_fwd(int d, bool causal, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                       const CUtensorMap& to, const FwdParams& p, cudaStream_t stream);
+
+cudaError_t launch_bwd(int d, bool causal, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                       const CUtensorMap& tdo, const CUtensorMap& tdk, const CUtensorMap& tdv,
+                       const BwdParams& p, cudaStream_t stream);
+
+}  // namespace sdpa

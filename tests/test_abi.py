@@ -1,0 +1,95 @@
+"""C-ABI checks that need no GPU: the library builds, loads, exports every
+function include/attn.h declares, and rejects bad arguments before touching
+the device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_functions():
+    src = open(os.path.join(ROOT, "include", "attn.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(attn_\w+)\s*\(", src)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import scaled_dot_product_08_gb300 as sdpa
+    sdpa.build()
+    return sdpa.load()
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for n in ("attn_fwd", "attn_bwd", "attn_bwd_workspace_size", "attn_get_device_status",
+              "attn_status_string"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_status_strings(lib):
+    import scaled_dot_product_08_gb300 as sdpa
+    for s in sdpa.Status:
+        assert sdpa.attn_status_string(int(s)) == "ATTN_" + ("OK" if s == 0 else "ERR_" + s.name)
+    assert sdpa.attn_status_string(99) == "ATTN_ERR_UNKNOWN"
+    assert lib.attn_abi_version() == 1
+
+
+def test_workspace_size_formula(lib):
+    import scaled_dot_product_08_gb300 as sdpa
+    # float32 dQ accumulator (B*H*Npad*d) + two float32 row vectors (B*H*Npad)
+    assert sdpa.attn_bwd_workspace_size(8, 16, 16, 4096, 128) == 8 * 16 * 4096 * (128 + 2) * 4
+    assert sdpa.attn_bwd_workspace_size(1, 2, 1, 129, 64) == 2 * 256 * (64 + 2) * 4
+    assert sdpa.attn_bwd_workspace_size(1, 3, 2, 128, 64) == 0      # H % Hkv != 0
+    assert sdpa.attn_bwd_workspace_size(1, 2, 2, 128, 80) == 0      # unsupported d
+    assert sdpa.attn_bwd_workspace_size(1, 2, 2, 0, 64) == 0
+
+
+# Argument errors are detected on the host before any CUDA call, so they can
+# be checked here without a GPU.  Fake, 16-byte aligned addresses are never
+# dereferenced because a shape error is reported first.
+FAKE = 0x10000
+
+
+@pytest.mark.parametrize("B,H,Hkv,N,d,expect", [
+    (1, 2, 2, 128, 80, 2),    # d not supported
+    (1, 2, 2, 128, 32, 2),
+    (1, 3, 2, 128, 64, 2),    # H % Hkv
+    (1, 2, 2, 0, 64, 2),      # N < 1
+    (0, 2, 2, 16, 64, 2),     # B < 1
+    (1, 2, 0, 16, 64, 2),     # Hkv < 1
+])
+def test_fwd_rejects_bad_shapes(lib, B, H, Hkv, N, d, expect):
+    import scaled_dot_product_08_gb300 as sdpa
+    st = sdpa.attn_fwd(FAKE, FAKE, FAKE, FAKE, FAKE, B, H, Hkv, N, d, 0.125, 0, None)
+    assert st == expect
+
+
+@pytest.mark.parametrize("scale,causal", [(float("nan"), 0), (float("inf"), 0), (0.0, 0), (-0.1, 1), (0.1, 2)])
+def test_fwd_rejects_bad_scale_or_flag(lib, scale, causal):
+    import scaled_dot_product_08_gb300 as sdpa
+    assert sdpa.attn_fwd(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 2, 2, 64, 64, scale, causal, None) == sdpa.Status.INVALID_ARG
+
+
+def test_fwd_rejects_null_and_misaligned(lib):
+    import scaled_dot_product_08_gb300 as sdpa
+    assert sdpa.attn_fwd(0, FAKE, FAKE, FAKE, FAKE, 1, 2, 2, 64, 64, 0.1, 0, None) == sdpa.Status.INVALID_ARG
+    assert sdpa.attn_fwd(FAKE + 8, FAKE, FAKE, FAKE, FAKE, 1, 2, 2, 64, 64, 0.1, 0, None) == sdpa.Status.MISALIGNED
+
+
+def test_bwd_rejects_bad_arguments(lib):
+    import scaled_dot_product_08_gb300 as sdpa
+    args = [FAKE] * 9
+    assert sdpa.attn_bwd(*args, FAKE, 1 << 20, 1, 2, 2, 64, 96 - 16, 0.1, 0, None) == sdpa.Status.UNSUPPORTED_SHAPE
+    assert sdpa.attn_bwd(*args, FAKE, 1 << 20, 1, 2, 2, 64, 64, float("nan"), 0, None) == sdpa.Status.INVALID_ARG
+    bad = list(args)
+    bad[6] = FAKE + 4
+    assert sdpa.attn_bwd(*bad, FAKE, 1 << 20, 1, 2, 2, 64, 64, 0.1, 0, None) == sdpa.Status.MISALIGNED
