@@ -103,6 +103,26 @@ attn_status_t attn_bwd(const void* q, const void* k, const void* v, const void* 
                        void* stream);
 
 /*
+ * The three stages attn_bwd runs, for callers that schedule (or time) them
+ * separately.  Same arguments, layouts and workspace as attn_bwd; they must
+ * run in this order on one stream with the same workspace:
+ *   attn_bwd_prep  D = rowsum(dO * O) and lse in base 2 into the workspace,
+ *                  dQ accumulator cleared                       (reads o, lse, dout)
+ *   attn_bwd_grad  recomputes P tile by tile; writes dK, dV; adds dQ into
+ *                  the workspace accumulator          (reads q, k, v, dout)
+ *   attn_bwd_dq    dQ accumulator -> bf16 dq
+ */
+attn_status_t attn_bwd_prep(const void* o, const float* lse, const void* dout,
+                            void* workspace, size_t workspace_bytes,
+                            int B, int H, int Hkv, int N, int d, void* stream);
+attn_status_t attn_bwd_grad(const void* q, const void* k, const void* v, const void* dout,
+                            void* dk, void* dv, void* workspace, size_t workspace_bytes,
+                            int B, int H, int Hkv, int N, int d, float scale, int causal,
+                            void* stream);
+attn_status_t attn_bwd_dq(void* dq, void* workspace, size_t workspace_bytes,
+                          int B, int H, int Hkv, int N, int d, void* stream);
+
+/*
  * Synchronises `stream`, then returns (and clears) the device status word
  * that the kernels set when a bounded wait runs out: ATTN_OK or
  * ATTN_ERR_TIMEOUT; ATTN_ERR_CUDA if the synchronisation itself failed.

@@ -21,6 +21,7 @@ from .build import LIB, build  # noqa: F401  (build() is the supported way to co
 
 __all__ = [
     "AttnError", "Status", "load", "attn_fwd", "attn_bwd", "attn_bwd_workspace_size",
+    "attn_bwd_prep", "attn_bwd_grad", "attn_bwd_dq",
     "attn_get_device_status", "attn_status_string", "attn_selftest_wait_timeout",
     "forward", "backward", "build",
 ]
@@ -63,6 +64,13 @@ def load() -> ctypes.CDLL:
         lib.attn_bwd.argtypes = [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t,
                                  _I, _I, _I, _I, _I, ctypes.c_float, _I, _P]
         lib.attn_bwd.restype = _I
+        lib.attn_bwd_prep.argtypes = [_P, _P, _P, _P, ctypes.c_size_t, _I, _I, _I, _I, _I, _P]
+        lib.attn_bwd_prep.restype = _I
+        lib.attn_bwd_grad.argtypes = [_P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t,
+                                      _I, _I, _I, _I, _I, ctypes.c_float, _I, _P]
+        lib.attn_bwd_grad.restype = _I
+        lib.attn_bwd_dq.argtypes = [_P, _P, ctypes.c_size_t, _I, _I, _I, _I, _I, _P]
+        lib.attn_bwd_dq.restype = _I
         lib.attn_get_device_status.argtypes = [_P]
         lib.attn_get_device_status.restype = _I
         lib.attn_status_string.argtypes = [_I]
@@ -92,6 +100,20 @@ def attn_bwd(q, k, v, o, lse, dout, dq, dk, dv, workspace, workspace_bytes,
              B, H, Hkv, N, d, scale, causal, stream) -> int:
     return load().attn_bwd(q, k, v, o, lse, dout, dq, dk, dv, workspace, workspace_bytes,
                            B, H, Hkv, N, d, scale, int(causal), stream)
+
+
+def attn_bwd_prep(o, lse, dout, workspace, workspace_bytes, B, H, Hkv, N, d, stream) -> int:
+    return load().attn_bwd_prep(o, lse, dout, workspace, workspace_bytes, B, H, Hkv, N, d, stream)
+
+
+def attn_bwd_grad(q, k, v, dout, dk, dv, workspace, workspace_bytes, B, H, Hkv, N, d, scale, causal,
+                  stream) -> int:
+    return load().attn_bwd_grad(q, k, v, dout, dk, dv, workspace, workspace_bytes, B, H, Hkv, N, d,
+                                scale, int(causal), stream)
+
+
+def attn_bwd_dq(dq, workspace, workspace_bytes, B, H, Hkv, N, d, stream) -> int:
+    return load().attn_bwd_dq(dq, workspace, workspace_bytes, B, H, Hkv, N, d, stream)
 
 
 def attn_get_device_status(stream=None) -> int:

@@ -209,48 +209,94 @@ size_t attn_bwd_workspace_size(int B, int H, int Hkv, int N, int d) {
   return rows * (size_t)d * 4 + rows * 4 * 2;
 }
 
-attn_status_t attn_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
-                       const void* dout, void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes,
-                       int B, int H, int Hkv, int N, int d, float scale, int causal, void* stream) {
+// Workspace carve-up shared by the three backward stages.
+static void bwd_params(sdpa::BwdParams* p, void* workspace, int B, int H, int Hkv, int N, int d, float scale,
+                       const DeviceInfo* di) {
+  const int npad = ((N + 127) / 128) * 128;
+  const size_t rows = (size_t)B * H * npad;
+  memset(p, 0, sizeof(*p));
+  p->dq_acc = static_cast<float*>(workspace);
+  p->dvec = p->dq_acc + rows * (size_t)d;
+  p->lse2 = p->dvec + rows;
+  p->B = B;
+  p->H = H;
+  p->Hkv = Hkv;
+  p->N = N;
+  p->Npad = npad;
+  p->G = H / Hkv;
+  p->d = d;
+  p->nq = (N + 127) / 128;
+  p->scale = scale;
+  p->scale_log2 = scale * 1.4426950408889634f;
+  p->status = di->status;
+  p->limit_ns = kWaitLimitNs;
+}
+
+static attn_status_t check_workspace(void* workspace, size_t workspace_bytes, int B, int H, int Hkv, int N, int d) {
+  if (workspace == nullptr || workspace_bytes < attn_bwd_workspace_size(B, H, Hkv, N, d)) return ATTN_ERR_WORKSPACE;
+  return ATTN_OK;
+}
+
+attn_status_t attn_bwd_prep(const void* o, const float* lse, const void* dout, void* workspace,
+                            size_t workspace_bytes, int B, int H, int Hkv, int N, int d, void* stream) {
   ATTN_TRY(check_shape(B, H, Hkv, N, d));
-  ATTN_TRY(check_scale_flag(scale, causal));
-  if (workspace == nullptr || workspace_bytes < attn_bwd_workspace_size(B, H, Hkv, N, d))
-    return ATTN_ERR_WORKSPACE;
-  ATTN_TRY(check_ptrs({q, k, v, o, lse, dout, dq, dk, dv, workspace}));
+  ATTN_TRY(check_workspace(workspace, workspace_bytes, B, H, Hkv, N, d));
+  ATTN_TRY(check_ptrs({o, lse, dout, workspace}));
   DeviceInfo* di = nullptr;
   ATTN_TRY(current_device(&di));
+  sdpa::BwdParams p;
+  bwd_params(&p, workspace, B, H, Hkv, N, d, 1.f, di);
+  p.o = static_cast<const uint16_t*>(o);
+  p.dout = static_cast<const uint16_t*>(dout);
+  p.lse = lse;
+  return sdpa::launch_bwd_prep(p, static_cast<cudaStream_t>(stream)) == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;
+}
 
+attn_status_t attn_bwd_grad(const void* q, const void* k, const void* v, const void* dout, void* dk, void* dv,
+                            void* workspace, size_t workspace_bytes, int B, int H, int Hkv, int N, int d,
+                            float scale, int causal, void* stream) {
+  ATTN_TRY(check_shape(B, H, Hkv, N, d));
+  ATTN_TRY(check_scale_flag(scale, causal));
+  ATTN_TRY(check_workspace(workspace, workspace_bytes, B, H, Hkv, N, d));
+  ATTN_TRY(check_ptrs({q, k, v, dout, dk, dv, workspace}));
+  DeviceInfo* di = nullptr;
+  ATTN_TRY(current_device(&di));
   CUtensorMap tq, tk, tv, tdo, tdk, tdv;
   if (!make_map_bf16(&tq, q, d, N, (long long)B * H) || !make_map_bf16(&tk, k, d, N, (long long)B * Hkv) ||
       !make_map_bf16(&tv, v, d, N, (long long)B * Hkv) || !make_map_bf16(&tdo, dout, d, N, (long long)B * H) ||
       !make_map_bf16(&tdk, dk, d, N, (long long)B * Hkv) || !make_map_bf16(&tdv, dv, d, N, (long long)B * Hkv))
     return ATTN_ERR_CUDA;
-
-  const int npad = ((N + 127) / 128) * 128;
-  const size_t rows = (size_t)B * H * npad;
   sdpa::BwdParams p;
-  p.o = static_cast<const uint16_t*>(o);
-  p.dout = static_cast<const uint16_t*>(dout);
-  p.lse = lse;
+  bwd_params(&p, workspace, B, H, Hkv, N, d, scale, di);
+  cudaError_t e =
+      sdpa::launch_bwd_grad(d, causal != 0, tq, tk, tv, tdo, tdk, tdv, p, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;
+}
+
+attn_status_t attn_bwd_dq(void* dq, void* workspace, size_t workspace_bytes, int B, int H, int Hkv, int N, int d,
+                          void* stream) {
+  ATTN_TRY(check_shape(B, H, Hkv, N, d));
+  ATTN_TRY(check_workspace(workspace, workspace_bytes, B, H, Hkv, N, d));
+  ATTN_TRY(check_ptrs({dq, workspace}));
+  DeviceInfo* di = nullptr;
+  ATTN_TRY(current_device(&di));
+  sdpa::BwdParams p;
+  bwd_params(&p, workspace, B, H, Hkv, N, d, 1.f, di);
   p.dq = static_cast<uint16_t*>(dq);
-  p.dq_acc = static_cast<float*>(workspace);
-  p.dvec = p.dq_acc + rows * (size_t)d;
-  p.lse2 = p.dvec + rows;
-  p.B = B;
-  p.H = H;
-  p.Hkv = Hkv;
-  p.N = N;
-  p.Npad = npad;
-  p.G = H / Hkv;
-  p.d = d;
-  p.nq = (N + 127) / 128;
-  p.scale = scale;
-  p.scale_log2 = scale * 1.4426950408889634f;
-  p.status = di->status;
-  p.limit_ns = kWaitLimitNs;
-  cudaError_t e = sdpa::launch_bwd(d, causal != 0, tq, tk, tv, tdo, tdk, tdv, p, static_cast<cudaStream_t>(stream));
-  if (e != cudaSuccess) return ATTN_ERR_LAUNCH;
-  return ATTN_OK;
+  return sdpa::launch_bwd_dq(p, static_cast<cudaStream_t>(stream)) == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;
+}
+
+attn_status_t attn_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                       const void* dout, void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes,
+                       int B, int H, int Hkv, int N, int d, float scale, int causal, void* stream) {
+  // Validate everything up front so that nothing is launched on a bad call.
+  ATTN_TRY(check_shape(B, H, Hkv, N, d));
+  ATTN_TRY(check_scale_flag(scale, causal));
+  ATTN_TRY(check_workspace(workspace, workspace_bytes, B, H, Hkv, N, d));
+  ATTN_TRY(check_ptrs({q, k, v, o, lse, dout, dq, dk, dv, workspace}));
+  ATTN_TRY(attn_bwd_prep(o, lse, dout, workspace, workspace_bytes, B, H, Hkv, N, d, stream));
+  ATTN_TRY(attn_bwd_grad(q, k, v, dout, dk, dv, workspace, workspace_bytes, B, H, Hkv, N, d, scale, causal, stream));
+  return attn_bwd_dq(dq, workspace, workspace_bytes, B, H, Hkv, N, d, stream);
 }
 
 attn_status_t attn_get_device_status(void* stream) {

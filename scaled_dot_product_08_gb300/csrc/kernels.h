@@ -44,8 +44,10 @@ size_t bwd_smem_bytes(int d);
 cudaError_t launch_fwd(int d, bool causal, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                        const CUtensorMap& to, const FwdParams& p, cudaStream_t stream);
 
-cudaError_t launch_bwd(int d, bool causal, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                       const CUtensorMap& tdo, const CUtensorMap& tdk, const CUtensorMap& tdv,
-                       const BwdParams& p, cudaStream_t stream);
+cudaError_t launch_bwd_prep(const BwdParams& p, cudaStream_t stream);
+cudaError_t launch_bwd_grad(int d, bool causal, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                            const CUtensorMap& tdo, const CUtensorMap& tdk, const CUtensorMap& tdv,
+                            const BwdParams& p, cudaStream_t stream);
+cudaError_t launch_bwd_dq(const BwdParams& p, cudaStream_t stream);
 
 }  // namespace sdpa

@@ -11,7 +11,8 @@
 namespace sdpa {
 
 // Device status word values (host maps them to attn_status_t).
-constexpr int kDevTimeout = 7;
+constexpr int kDevTimeout = 7;      // a bounded wait ran out
+constexpr int kDevMisaligned = 8;   // dynamic shared memory not 1024-byte aligned
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));

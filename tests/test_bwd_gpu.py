@@ -1,0 +1,162 @@
+"""GPU parity of the backward pass (attn_bwd through the C ABI) against the
+CPU fp64 oracle's analytic gradients on the same seeded bf16 inputs.
+
+The GPU backward consumes the GPU forward's O and lse (as a training step
+does); the reference is the pure oracle (its own fp64 P), so forward and
+backward errors are both inside the comparison."""
+import math
+
+import numpy as np
+import pytest
+
+import oracle
+from sdpa_inputs import make_inputs, make_random, workload
+from tests.parity import check_grads, dev, host, rel_fro
+
+pytestmark = pytest.mark.gpu
+
+SMALL = [
+    # B, H, Hkv, N, d
+    (1, 1, 1, 1, 64),
+    (1, 2, 2, 17, 128),
+    (1, 2, 2, 128, 64),
+    (1, 2, 1, 129, 96),
+    (2, 2, 2, 200, 128),
+    (1, 4, 2, 256, 64),
+    (1, 4, 1, 300, 128),
+    (1, 2, 2, 513, 96),
+    (1, 8, 2, 384, 64),
+    (1, 1, 1, 1000, 128),
+]
+
+
+def _run(lib, q, k, v, do, s, causal):
+    tq, tk, tv, tdo = dev(q), dev(k), dev(v), dev(do)
+    O, lse = lib.forward(tq, tk, tv, s, causal)
+    return [host(g) for g in lib.backward(tq, tk, tv, O, lse, tdo, s, causal)]
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("shape", SMALL, ids=lambda s: "B%dH%dKV%dN%dd%d" % s)
+def test_backward_small_shapes(cuda_lib, shape, causal):
+    B, H, Hkv, N, d = shape
+    seed = 5000 + N + d + H
+    q = make_random((B, H, N, d), seed)
+    k = make_random((B, Hkv, N, d), seed + 1)
+    v = make_random((B, Hkv, N, d), seed + 2)
+    do = make_random((B, H, N, d), seed + 3)
+    s = 1 / math.sqrt(d)
+    grads = _run(cuda_lib, q, k, v, do, s, causal)
+    ref = oracle.attention_backward(q, k, v, do, s, causal)
+    check_grads(grads, ref, f"{shape} causal={causal}")
+
+
+def test_backward_c5_full_size_sampled_heads(cuda_lib):
+    """The full training workload (B=8, H=16, N=4096, d=128, causal) in the
+    launch configuration the benchmark times; gradients are compared on
+    whole sampled heads (multi-head: a head's dK, dV depend on that head only)."""
+    w = workload("c5")
+    x = make_inputs(w)
+    s = w.softmax_scale
+    grads = _run(cuda_lib, x["q"], x["k"], x["v"], x["do"], s, w.causal)
+    for g in grads:
+        assert np.all(np.isfinite(g))
+    for (b, h) in [(0, 0), (3, 7), (7, 15)]:
+        sl = (slice(b, b + 1), slice(h, h + 1))
+        ref = oracle.attention_backward(x["q"][sl], x["k"][sl], x["v"][sl], x["do"][sl], s, True)
+        check_grads([g[sl] for g in grads], ref, f"c5 head ({b},{h})")
+
+
+def test_backward_gqa_group_sum_long(cuda_lib):
+    # GQA with a long sequence: dK/dV sum over the 4 query heads of a group.
+    B, H, Hkv, N, d = 1, 8, 2, 1536, 128
+    q = make_random((B, H, N, d), 71, 0.5)
+    k = make_random((B, Hkv, N, d), 72, 0.5)
+    v = make_random((B, Hkv, N, d), 73, 0.5)
+    do = make_random((B, H, N, d), 74)
+    s = 1 / math.sqrt(d)
+    grads = _run(cuda_lib, q, k, v, do, s, True)
+    ref = oracle.attention_backward(q, k, v, do, s, True)
+    check_grads(grads, ref, "gqa long")
+
+
+def test_backward_padded_head_dim(cuda_lib):
+    # head_dim 80 zero-padded to 96: gradients equal the unpadded d=80 oracle
+    # and the pad columns of dQ, dK, dV are exactly zero.
+    B, H, Hkv, N = 1, 4, 2, 333
+    q = make_random((B, H, N, 80), 81)
+    k = make_random((B, Hkv, N, 80), 82)
+    v = make_random((B, Hkv, N, 80), 83)
+    do = make_random((B, H, N, 80), 84)
+    pad = [(0, 0)] * 3 + [(0, 16)]
+    s = 1 / math.sqrt(80)
+    grads = _run(cuda_lib, np.pad(q, pad), np.pad(k, pad), np.pad(v, pad), np.pad(do, pad), s, True)
+    for g in grads:
+        assert np.all(g[..., 80:] == 0.0)
+    ref = oracle.attention_backward(q, k, v, do, s, True)
+    check_grads([g[..., :80] for g in grads], ref, "padded d=96")
+
+
+def test_backward_outputs_stay_inside_buffers_and_workspace_checks(cuda_lib):
+    import torch
+    B, H, Hkv, N, d = 1, 2, 1, 150, 64
+    q = dev(make_random((B, H, N, d), 91))
+    k = dev(make_random((B, Hkv, N, d), 92))
+    v = dev(make_random((B, Hkv, N, d), 93))
+    do = dev(make_random((B, H, N, d), 94))
+    O, lse = cuda_lib.forward(q, k, v, 0.125, True)
+    pad = 2048
+    bufs = [torch.full((2 * pad + t.numel(),), -3.0, dtype=torch.bfloat16, device="cuda") for t in (q, k, v)]
+    views = [bb[pad:pad + t.numel()].view(t.shape) for bb, t in zip(bufs, (q, k, v))]
+    ws_bytes = cuda_lib.attn_bwd_workspace_size(B, H, Hkv, N, d)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
+    S = cuda_lib.Status
+    args = [q.data_ptr(), k.data_ptr(), v.data_ptr(), O.data_ptr(), lse.data_ptr(), do.data_ptr(),
+            views[0].data_ptr(), views[1].data_ptr(), views[2].data_ptr()]
+    assert cuda_lib.attn_bwd(*args, ws.data_ptr(), ws_bytes - 16, B, H, Hkv, N, d, 0.125, 1, None) == S.WORKSPACE
+    assert cuda_lib.attn_bwd(*args, 0, ws_bytes, B, H, Hkv, N, d, 0.125, 1, None) == S.WORKSPACE
+    assert cuda_lib.attn_bwd(*args, ws.data_ptr(), ws_bytes, B, H, Hkv, N, d, 0.125, 1, None) == S.OK
+    torch.cuda.synchronize()
+    for bb in bufs:
+        assert torch.all(bb[:pad] == -3.0) and torch.all(bb[-pad:] == -3.0)
+    ref = oracle.attention_backward(host(q), host(k), host(v), host(do), 0.125, True)
+    check_grads([host(t) for t in views], ref, "views")
+    assert cuda_lib.attn_get_device_status(None) == S.OK
+
+
+def test_backward_stages_equal_the_combined_call(cuda_lib):
+    # attn_bwd_prep + attn_bwd_grad + attn_bwd_dq on one stream equal attn_bwd.
+    import torch
+    B, H, Hkv, N, d = 1, 4, 2, 260, 96
+    q = dev(make_random((B, H, N, d), 111))
+    k = dev(make_random((B, Hkv, N, d), 112))
+    v = dev(make_random((B, Hkv, N, d), 113))
+    do = dev(make_random((B, H, N, d), 114))
+    O, lse = cuda_lib.forward(q, k, v, 0.1, False)
+    ref = [host(g) for g in cuda_lib.backward(q, k, v, O, lse, do, 0.1, False)]
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ws_bytes = cuda_lib.attn_bwd_workspace_size(B, H, Hkv, N, d)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
+    sp = torch.cuda.current_stream().cuda_stream
+    assert cuda_lib.attn_bwd_prep(O.data_ptr(), lse.data_ptr(), do.data_ptr(), ws.data_ptr(), ws_bytes,
+                                  B, H, Hkv, N, d, sp) == 0
+    assert cuda_lib.attn_bwd_grad(q.data_ptr(), k.data_ptr(), v.data_ptr(), do.data_ptr(), dk.data_ptr(),
+                                  dv.data_ptr(), ws.data_ptr(), ws_bytes, B, H, Hkv, N, d, 0.1, 0, sp) == 0
+    assert cuda_lib.attn_bwd_dq(dq.data_ptr(), ws.data_ptr(), ws_bytes, B, H, Hkv, N, d, sp) == 0
+    got = [host(g) for g in (dq, dk, dv)]
+    assert np.array_equal(got[1], ref[1]) and np.array_equal(got[2], ref[2])
+    assert rel_fro(got[0], ref[0]) < 1e-2
+
+
+def test_backward_is_deterministic_in_dk_dv(cuda_lib):
+    # dK and dV accumulate in tensor memory in a fixed order: bit-identical
+    # across runs.  dQ uses float32 atomics and may differ in the last bits.
+    B, H, Hkv, N, d = 1, 4, 2, 700, 128
+    q = make_random((B, H, N, d), 101)
+    k = make_random((B, Hkv, N, d), 102)
+    v = make_random((B, Hkv, N, d), 103)
+    do = make_random((B, H, N, d), 104)
+    g1 = _run(cuda_lib, q, k, v, do, 0.1, True)
+    g2 = _run(cuda_lib, q, k, v, do, 0.1, True)
+    assert np.array_equal(g1[1], g2[1]) and np.array_equal(g1[2], g2[2])
+    assert rel_fro(g1[0], g2[0]) < 1e-2
