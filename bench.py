@@ -1,0 +1,414 @@
+#!/usr/bin/env python3
+"""Throughput of exact attention (forward + backward) on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload c5] [--impl ours|reference]
+
+One step is the whole hot path on one batch of synthetic input: the forward
+kernel (O and lse), then the backward's three kernels (prep, grad, dq).  The
+default workload is the training configuration B=8, H=16, N=4096, d=128,
+causal, forward + backward.  Inputs (seeded bf16 draws) are resident in HBM
+before timing; they total 537 MB, larger than the 129 MB L2, so no L2 flush
+is inserted between steps.
+
+Work convention: forward 4*B*H*N^2*d (halved when causal), backward 2.5x the
+forward.  ``value`` = total TFLOP/s of the timed steps (all ranks).
+
+Extra keys on the JSON line:
+  roofline      the dominant kernel's achieved rate (CUDA events on its own
+                stream, averaged over the timed steps) against the measured
+                peak in MEASURED_PEAKS.json, plus its DRAM traffic per launch
+                from the committed ncu summary (null if the kernel changed)
+  cpu_baseline  the fp64 CPU oracle timed on this host on a bounded sample
+  e2e           the same metric through the C ABI with pinned HOST buffers:
+                host->device copies of Q, K, V, dO and device->host copies of
+                O, lse, dQ, dK, dV inside the timed region
+  clocks        nvidia-smi samples taken during the timed region
+``--impl reference`` times the CPU oracle (the only other implementation of
+this path) on the same workload, one bounded sample per step.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "attention fwd/bwd TFLOPS (bf16, 1×GB300) and % of dense BF16 tensor peak"
+UNIT = "TFLOPS"
+FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--workload", default="c5")
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def workload_desc(w):
+    tail = f" (head_dim {w.d_draw} zero-padded)" if w.d_draw else ""
+    return (f"{w.name}: B={w.B} H={w.H} Hkv={w.Hkv} N={w.N} d={w.d}{tail} "
+            f"{'causal' if w.causal else 'non-causal'} {'fwd+bwd' if w.with_grad else 'fwd'}")
+
+
+def step_flops(w):
+    from sdpa_inputs import flops_backward, flops_forward
+    f = flops_forward(w.B, w.H, w.N, w.d, w.causal)
+    b = flops_backward(w.B, w.H, w.N, w.d, w.causal) if w.with_grad else 0.0
+    return f, b
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return json.load(f), "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def traffic_of(kernel, workload):
+    """DRAM bytes per launch of `kernel` on `workload` from the committed ncu
+    summary profiles/dram_traffic.txt (lines: kernel workload bytes source
+    sha1-prefix), or None if absent or taken on a different kernel source."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+    try:
+        lines = open(path).read().splitlines()
+    except OSError:
+        return None
+    for ln in lines:
+        parts = ln.split()
+        if ln.startswith("#") or len(parts) < 5 or parts[0] != kernel or parts[1] != workload:
+            continue
+        src = os.path.join(ROOT, "scaled_dot_product_08_gb300", "csrc", parts[3])
+        try:
+            digest = hashlib.sha1(open(src, "rb").read()).hexdigest()[:12]
+        except OSError:
+            return None
+        return float(parts[2]) if parts[4] == digest else None
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi samples every 100 ms while running (clocks during the timed region)."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        self.proc.terminate()
+        out, _ = self.proc.communicate(timeout=10)
+        sm, smax, power, reasons = [], [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in out.splitlines():
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+                power.append(float(f[3]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "power_w_max": max(power) if power else None, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------ CPU oracle arm
+def _oracle_head_inputs(w):
+    import numpy as np
+    from sdpa_inputs import draw
+    rng = np.random.default_rng(w.seed)
+    dd = w.d_draw or w.d
+    return [draw(rng, (1, 1, w.N, dd), a) for a in (w.amp, w.amp, w.amp, 1.0)]
+
+
+def _oracle_head_seconds(w, x):
+    """Wall time of the oracle on one whole head of the workload."""
+    import oracle
+    q, k, v, do = x
+    t0 = time.perf_counter()
+    oracle.attention_forward(q, k, v, w.softmax_scale, w.causal)
+    if w.with_grad:
+        oracle.attention_backward(q, k, v, do, w.softmax_scale, w.causal)
+    return time.perf_counter() - t0
+
+
+def _head_flops(w):
+    from sdpa_inputs import flops_backward, flops_forward
+    return flops_forward(1, 1, w.N, w.d, w.causal) + (flops_backward(1, 1, w.N, w.d, w.causal) if w.with_grad else 0)
+
+
+def _blas_threads():
+    cores = os.cpu_count()
+    try:
+        from threadpoolctl import threadpool_info
+        cores = max(i.get("num_threads", 0) for i in threadpool_info()) or cores
+    except Exception:
+        pass
+    return cores
+
+
+def cpu_baseline(w, budget_s=15.0):
+    """fp64 oracle fwd(+bwd) on whole heads of the workload, timed on this
+    host's cores (the oracle as it stands), for about `budget_s` seconds."""
+    x = _oracle_head_inputs(w)
+    done, t_total = 0, 0.0
+    while True:
+        t_total += _oracle_head_seconds(w, x)
+        done += 1
+        if t_total >= budget_s or t_total / done * (done + 1) > 2.5 * budget_s:
+            break
+    return {"value": _head_flops(w) * done / t_total / 1e12, "unit": UNIT, "cores": _blas_threads(),
+            "kind": "oracle",
+            "sample": f"{done} whole head(s) (B=1, H=1, N={w.N}, d={w.d_draw or w.d}) of {w.name}, "
+                      f"{'fwd+bwd' if w.with_grad else 'fwd'} in float64 numpy, {t_total:.1f} s"}
+
+
+def run_reference(args, w, rank, world):
+    """The reference arm: the CPU oracle, one whole head of the workload per step."""
+    if rank != 0:
+        return
+    x = _oracle_head_inputs(w)
+    for _ in range(args.warmup):
+        _oracle_head_seconds(w, x)
+    t = sum(_oracle_head_seconds(w, x) for _ in range(args.steps))
+    val = _head_flops(w) * args.steps / t / 1e12
+    sample = (f"one whole head (B=1, H=1, N={w.N}, d={w.d_draw or w.d}) of {w.name} per step, "
+              f"{'fwd+bwd' if w.with_grad else 'fwd'} in float64 numpy")
+    line = {"impl": "reference", "metric": METRIC, "value": val, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": t / args.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded N(0,1) draws rounded to bf16)",
+            "config": {"workload": workload_desc(w), "B": w.B, "H": w.H, "Hkv": w.Hkv, "N": w.N, "d": w.d,
+                       "causal": w.causal},
+            "cpu_baseline": {"value": val, "unit": UNIT, "cores": _blas_threads(), "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": val, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------ GPU arm
+def run_ours(args, w, rank, world, local_rank):
+    import torch
+    import scaled_dot_product_08_gb300 as sdpa
+    from sdpa_inputs import make_inputs
+
+    sdpa.build()
+    sdpa.load()
+    torch.cuda.set_device(local_rank)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+    x = make_inputs(w)
+    dev = lambda a: torch.from_numpy(a).to(torch.bfloat16).cuda()
+    q, k, v = dev(x["q"]), dev(x["k"]), dev(x["v"])
+    do = dev(x["do"]) if w.with_grad else None
+    B, H, Hkv, N, d = w.B, w.H, w.Hkv, w.N, w.d
+    s = w.softmax_scale
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device="cuda")
+    if w.with_grad:
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        ws_bytes = sdpa.attn_bwd_workspace_size(B, H, Hkv, N, d)
+        ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+    sp = stream.cuda_stream
+    names = ["attn_fwd"] + (["attn_bwd_prep", "attn_bwd_grad", "attn_bwd_dq"] if w.with_grad else [])
+
+    def chk(st, where):
+        if st != 0:
+            raise RuntimeError(f"{where}: {sdpa.attn_status_string(st)}")
+
+    def step(evs=None):
+        if evs is not None:
+            evs[0].record(stream)
+        chk(sdpa.attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                          B, H, Hkv, N, d, s, w.causal, sp), "attn_fwd")
+        if evs is not None:
+            evs[1].record(stream)
+        if w.with_grad:
+            chk(sdpa.attn_bwd_prep(o.data_ptr(), lse.data_ptr(), do.data_ptr(), ws.data_ptr(), ws_bytes,
+                                   B, H, Hkv, N, d, sp), "attn_bwd_prep")
+            if evs is not None:
+                evs[2].record(stream)
+            chk(sdpa.attn_bwd_grad(q.data_ptr(), k.data_ptr(), v.data_ptr(), do.data_ptr(), dk.data_ptr(),
+                                   dv.data_ptr(), ws.data_ptr(), ws_bytes, B, H, Hkv, N, d, s, w.causal, sp),
+                "attn_bwd_grad")
+            if evs is not None:
+                evs[3].record(stream)
+            chk(sdpa.attn_bwd_dq(dq.data_ptr(), ws.data_ptr(), ws_bytes, B, H, Hkv, N, d, sp), "attn_bwd_dq")
+            if evs is not None:
+                evs[4].record(stream)
+
+    def barrier():
+        torch.cuda.synchronize()
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    for _ in range(max(args.warmup, 1)):
+        step()
+    barrier()
+    st = sdpa.attn_get_device_status(None)
+    if st != 0:
+        raise RuntimeError(f"device status after warm-up: {sdpa.attn_status_string(st)}")
+
+    K = args.steps
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(names) + 1)] for _ in range(K)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    time.sleep(0.3)
+    barrier()
+    t0.record(stream)
+    for i in range(K):
+        step(evs[i])
+    t1.record(stream)
+    barrier()
+    clk = clocks.stop()
+    ms = t0.elapsed_time(t1)
+    st = sdpa.attn_get_device_status(None)
+    if st != 0:
+        raise RuntimeError(f"device status after timed steps: {sdpa.attn_status_string(st)}")
+    per_kernel = {n: sum(e[j].elapsed_time(e[j + 1]) for e in evs) / K for j, n in enumerate(names)}
+    if dist is not None:
+        t = torch.tensor([ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+
+    f_fwd, f_bwd = step_flops(w)
+    flops = f_fwd + f_bwd
+    value = world * flops * K / (ms / 1e3) / 1e12
+
+    # ---- roofline of the dominant kernel
+    peaks, peak_src = load_peaks()
+    dom = max(per_kernel, key=per_kernel.get)
+    kflops = {"attn_fwd": f_fwd, "attn_bwd_grad": f_bwd}
+    if dom in kflops:
+        achieved = kflops[dom] / (per_kernel[dom] / 1e3) / 1e12
+        peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+        roof = {"kernel": dom, "bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": achieved / peak, "peak_source": f"{peak_src} bf16 burst (cuBLAS 8192^3)",
+                "frac_of_nominal_2250": achieved / 2250.0}
+    else:
+        nbytes = {"attn_bwd_prep": 2 * B * H * N * d * 2 + B * H * N * 4 + B * H * N * (d + 2) * 4,
+                  "attn_bwd_dq": B * H * N * d * 4 + B * H * N * d * 2}[dom]
+        achieved = nbytes / (per_kernel[dom] / 1e3) / 1e9
+        peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+        roof = {"kernel": dom, "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                "frac": achieved / peak, "peak_source": f"{peak_src} copy bandwidth"}
+    roof["traffic"] = traffic_of(dom, w.name)
+
+    # ---- end to end through the C ABI with pinned host buffers
+    e2e = None
+    if not args.no_e2e:
+        hq, hk, hv = (t.cpu().pin_memory() for t in (q, k, v))
+        ins = [(q, hq), (k, hk), (v, hv)] + ([(do, do.cpu().pin_memory())] if w.with_grad else [])
+        outs = [o, lse] + ([dq, dk, dv] if w.with_grad else [])
+        houts = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in outs]
+        h2d = sum(h.numel() * h.element_size() for _, h in ins)
+        d2h = sum(h.numel() * h.element_size() for h in houts)
+        Ke = max(3, min(K, 30))
+
+        def e2e_step():
+            for dst, src in ins:
+                dst.copy_(src, non_blocking=True)
+            step()
+            for src, dst in zip(outs, houts):
+                dst.copy_(src, non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        barrier()
+        a, bev = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(Ke):
+            e2e_step()
+        bev.record(stream)
+        barrier()
+        ems = a.elapsed_time(bev)
+        if dist is not None:
+            t = torch.tensor([ems], device="cuda")
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            ems = float(t.item())
+        e2e = {"value": world * flops * Ke / (ems / 1e3) / 1e12, "unit": UNIT, "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "ms_per_step": ems / Ke, "steps": Ke}
+
+    cb = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cb = cpu_baseline(w)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": args.warmup,
+            "ms_per_step": ms / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16", "data": "synthetic (seeded N(0,1) draws rounded to bf16)",
+            "config": {"workload": workload_desc(w), "B": B, "H": H, "Hkv": Hkv, "N": N, "d": d,
+                       "causal": w.causal, "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                       "l2": "no flush: inputs (Q, K, V, dO) larger than the 129 MB L2"},
+            "fwd_tflops": f_fwd / (per_kernel["attn_fwd"] / 1e3) / 1e12,
+            "kernel_ms": per_kernel,
+            "roofline": roof, "cpu_baseline": cb, "e2e": e2e, "clocks": clk,
+            "gpu_launches": len(names) * K,
+        }
+        if w.with_grad:
+            line["bwd_tflops"] = f_bwd / (sum(per_kernel[n] for n in names[1:]) / 1e3) / 1e12
+        print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse_args()
+    from sdpa_inputs import workload
+    w = workload(args.workload)
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, w, rank, world)
+        return
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl")
+    try:
+        run_ours(args, w, rank, world, local_rank)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()
