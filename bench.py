@@ -144,6 +144,20 @@ class ClockSampler:
                 "power_w_max": max(power) if power else None, "reasons": sorted(reasons), "samples": len(sm)}
 
 
+def max_over_ranks(x: float) -> float:
+    """Max of a per-rank float over the default process group (identity when
+    torch.distributed is not initialised).  NCCL reduces on the GPU, gloo on
+    the CPU."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([float(x)], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 # ------------------------------------------------------------ CPU oracle arm
 def _oracle_head_inputs(w):
     import numpy as np
@@ -302,10 +316,7 @@ def run_ours(args, w, rank, world, local_rank):
     if st != 0:
         raise RuntimeError(f"device status after timed steps: {sdpa.attn_status_string(st)}")
     per_kernel = {n: sum(e[j].elapsed_time(e[j + 1]) for e in evs) / K for j, n in enumerate(names)}
-    if dist is not None:
-        t = torch.tensor([ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ms)
 
     f_fwd, f_bwd = step_flops(w)
     flops = f_fwd + f_bwd
@@ -358,10 +369,7 @@ def run_ours(args, w, rank, world, local_rank):
         bev.record(stream)
         barrier()
         ems = a.elapsed_time(bev)
-        if dist is not None:
-            t = torch.tensor([ems], device="cuda")
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            ems = float(t.item())
+        ems = max_over_ranks(ems)
         e2e = {"value": world * flops * Ke / (ems / 1e3) / 1e12, "unit": UNIT, "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "ms_per_step": ems / Ke, "steps": Ke}
 
