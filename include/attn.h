@@ -129,6 +129,17 @@ attn_status_t attn_bwd_dq(void* dq, void* workspace, size_t workspace_bytes,
  */
 attn_status_t attn_get_device_status(void* stream);
 
+/*
+ * Where the first bounded wait that ran out since the last call happened,
+ * for diagnosing ATTN_ERR_TIMEOUT: info[0] = (wait site << 16) | loop step,
+ * info[1] = CTA index, info[2] = thread index, info[3] = microseconds waited;
+ * all zero if no wait ran out.  Synchronises `stream`, then clears the record.
+ * Each wait is limited to 2 s, or to SDPA08_WAIT_LIMIT_MS milliseconds
+ * (1..60000) if that environment variable is set when the library is first
+ * used on a device.
+ */
+attn_status_t attn_get_timeout_info(int info[4], void* stream);
+
 /* Human-readable name of a status code (static storage; never NULL). */
 const char* attn_status_string(attn_status_t s);
 

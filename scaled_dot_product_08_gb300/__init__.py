@@ -22,7 +22,7 @@ from .build import LIB, build  # noqa: F401  (build() is the supported way to co
 __all__ = [
     "AttnError", "Status", "load", "attn_fwd", "attn_bwd", "attn_bwd_workspace_size",
     "attn_bwd_prep", "attn_bwd_grad", "attn_bwd_dq",
-    "attn_get_device_status", "attn_status_string", "attn_selftest_wait_timeout",
+    "attn_get_device_status", "attn_get_timeout_info", "attn_status_string", "attn_selftest_wait_timeout",
     "forward", "backward", "build",
 ]
 
@@ -77,6 +77,8 @@ def load() -> ctypes.CDLL:
         lib.attn_status_string.restype = ctypes.c_char_p
         lib.attn_abi_version.argtypes = []
         lib.attn_abi_version.restype = _I
+        lib.attn_get_timeout_info.argtypes = [ctypes.POINTER(ctypes.c_int), _P]
+        lib.attn_get_timeout_info.restype = _I
         lib.attn_selftest_wait_timeout.argtypes = [ctypes.c_uint, _P]
         lib.attn_selftest_wait_timeout.restype = _I
         _lib = lib
@@ -118,6 +120,13 @@ def attn_bwd_dq(dq, workspace, workspace_bytes, B, H, Hkv, N, d, stream) -> int:
 
 def attn_get_device_status(stream=None) -> int:
     return load().attn_get_device_status(stream)
+
+
+def attn_get_timeout_info(stream=None):
+    """(status, [site<<16|step, block, thread, waited_us]) of the first timed-out wait."""
+    buf = (ctypes.c_int * 4)()
+    st = load().attn_get_timeout_info(buf, stream)
+    return st, list(buf)
 
 
 def attn_selftest_wait_timeout(timeout_us: int, stream=None) -> int:

@@ -4,6 +4,7 @@
 // attention path runs in the kernels of attn_fwd.cu / attn_bwd.cu.
 #include <cmath>
 #include <cstdint>
+#include <cstdlib>
 #include <cstring>
 #include <initializer_list>
 #include <mutex>
@@ -18,15 +19,31 @@
 namespace {
 
 constexpr int kMaxDevices = 64;
-constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s per wait
 
-// Written by kernels when a bounded wait gives up (0 = fine).
+// Limit of each on-chip wait: 2 s, or SDPA08_WAIT_LIMIT_MS milliseconds
+// (1 .. 60000) when that environment variable is set at the first call.
+unsigned long long wait_limit_ns() {
+  static unsigned long long lim = [] {
+    unsigned long long v = 2000000000ull;
+    if (const char* e = std::getenv("SDPA08_WAIT_LIMIT_MS")) {
+      const long ms = std::strtol(e, nullptr, 10);
+      if (ms >= 1 && ms <= 60000) v = (unsigned long long)ms * 1000000ull;
+    }
+    return v;
+  }();
+  return lim;
+}
+
+// Written by kernels when a bounded wait gives up (0 = fine), and where the
+// first such timeout happened.
 __device__ int g_status_word;
+__device__ int g_timeout_info[4];
 
 struct DeviceInfo {
   bool probed = false;
   bool supported = false;
   int* status = nullptr;  // device address of g_status_word
+  int* info = nullptr;    // device address of g_timeout_info
 };
 DeviceInfo g_dev[kMaxDevices];
 std::mutex g_dev_mu;
@@ -49,6 +66,8 @@ attn_status_t current_device(DeviceInfo** out) {
       void* p = nullptr;
       if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) return ATTN_ERR_CUDA;
       di.status = static_cast<int*>(p);
+      if (cudaGetSymbolAddress(&p, g_timeout_info) != cudaSuccess) return ATTN_ERR_CUDA;
+      di.info = static_cast<int*>(p);
     }
     di.probed = true;
   }
@@ -130,7 +149,7 @@ attn_status_t check_ptrs(std::initializer_list<const void*> ps) {
   return ATTN_OK;
 }
 
-__global__ void selftest_wait_kernel(int* status, unsigned long long limit_ns) {
+__global__ void selftest_wait_kernel(int* status, int* info, unsigned long long limit_ns) {
   __shared__ __align__(8) uint64_t bar;
   __shared__ int abort_flag;
   if (threadIdx.x == 0) {
@@ -139,9 +158,9 @@ __global__ void selftest_wait_kernel(int* status, unsigned long long limit_ns) {
     sdpa::fence_mbar_init();
   }
   __syncthreads();
-  const sdpa::WaitCtx wc{&abort_flag, status, limit_ns};
+  const sdpa::WaitCtx wc{&abort_flag, status, limit_ns, info};
   // Nothing ever arrives on `bar`: every thread must give up and return.
-  (void)sdpa::wait_bounded(wc, sdpa::smem_u32(&bar), 0);
+  (void)sdpa::wait_bounded(wc, sdpa::smem_u32(&bar), 0, sdpa::wait_site(0x01, 0));
   __syncthreads();
 }
 
@@ -196,7 +215,8 @@ attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, flo
   p.nkv = (N + 127) / 128;
   p.scale_log2 = scale * 1.4426950408889634f;
   p.status = di->status;
-  p.limit_ns = kWaitLimitNs;
+  p.limit_ns = wait_limit_ns();
+  p.info = di->info;
   cudaError_t e = sdpa::launch_fwd(d, causal != 0, tq, tk, tv, to, p, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return ATTN_ERR_LAUNCH;
   return ATTN_OK;
@@ -229,7 +249,8 @@ static void bwd_params(sdpa::BwdParams* p, void* workspace, int B, int H, int Hk
   p->scale = scale;
   p->scale_log2 = scale * 1.4426950408889634f;
   p->status = di->status;
-  p->limit_ns = kWaitLimitNs;
+  p->limit_ns = wait_limit_ns();
+  p->info = di->info;
 }
 
 static attn_status_t check_workspace(void* workspace, size_t workspace_bytes, int B, int H, int Hkv, int N, int d) {
@@ -312,11 +333,22 @@ attn_status_t attn_get_device_status(void* stream) {
   return host == 0 ? ATTN_OK : (host == sdpa::kDevTimeout ? ATTN_ERR_TIMEOUT : ATTN_ERR_CUDA);
 }
 
+attn_status_t attn_get_timeout_info(int info[4], void* stream) {
+  if (info == nullptr) return ATTN_ERR_INVALID_ARG;
+  DeviceInfo* di = nullptr;
+  ATTN_TRY(current_device(&di));
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return ATTN_ERR_CUDA;
+  if (cudaMemcpyFromSymbol(info, g_timeout_info, 4 * sizeof(int)) != cudaSuccess) return ATTN_ERR_CUDA;
+  const int zero[4] = {0, 0, 0, 0};
+  if (cudaMemcpyToSymbol(g_timeout_info, zero, sizeof(zero)) != cudaSuccess) return ATTN_ERR_CUDA;
+  return ATTN_OK;
+}
+
 attn_status_t attn_selftest_wait_timeout(unsigned int timeout_us, void* stream) {
   DeviceInfo* di = nullptr;
   ATTN_TRY(current_device(&di));
   if (timeout_us == 0 || timeout_us > 5000000u) return ATTN_ERR_INVALID_ARG;
-  selftest_wait_kernel<<<1, 64, 0, static_cast<cudaStream_t>(stream)>>>(di->status,
+  selftest_wait_kernel<<<1, 64, 0, static_cast<cudaStream_t>(stream)>>>(di->status, di->info,
                                                                          (unsigned long long)timeout_us * 1000ull);
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;
 }

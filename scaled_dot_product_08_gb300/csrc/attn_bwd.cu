@@ -9,8 +9,8 @@
 //     dS = P * (dP - D),  dQ = scale dS K,  dK = scale dS^T Q.
 //
 // Three kernels on the caller's stream:
-//   bwd_pre     D = rowsum(dO * O) (fp32), lse2 = lse * log2(e) (+inf on the
-//               padding rows of each head), dQ accumulator := 0
+//   bwd_pre     -D = -rowsum(dO * O) (fp32), -lse2 = -lse * log2(e) (-inf on
+//               the padding rows of each head), dQ accumulator := 0
 //   bwd_main    one CTA per (key tile j, batch, K/V head); loops over the
 //               GQA group's query heads and the query tiles i (i >= j when
 //               causal).  dK_j and dV_j accumulate in tensor memory; dQ_i
@@ -38,9 +38,10 @@
 namespace sdpa {
 
 // ------------------------------------------------------------------ preprocess
-// One warp per (head, padded row).  Row i < N: D = dO_i . O_i (fp32),
-// lse2 = lse_i * log2(e).  Row i >= N: D = 0, lse2 = +inf (so P = 0 there).
-// Every row of the dQ accumulator is zeroed.
+// One warp per (head, padded row).  Row i < N: stores -D = -(dO_i . O_i)
+// (fp32) and -lse_i * log2(e).  Row i >= N: -D = 0 and -lse2 = -inf (so P = 0
+// there).  The negated values let the grad kernel form P and dP - D with one
+// packed FMA / add per pair.  Every row of the dQ accumulator is zeroed.
 __global__ void __launch_bounds__(256) bwd_pre_kernel(const BwdParams p) {
   const long long rows = (long long)p.B * p.H * p.Npad;
   const long long row = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
@@ -69,8 +70,8 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const BwdParams p) {
     for (int s = 16; s > 0; s >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, s);
   }
   if (lane == 0) {
-    p.dvec[row] = (i < p.N) ? dot : 0.f;
-    p.lse2[row] = (i < p.N) ? p.lse[(size_t)bh * p.N + i] * 1.4426950408889634f : INFINITY;
+    p.dvec[row] = (i < p.N) ? -dot : 0.f;
+    p.lse2[row] = (i < p.N) ? -p.lse[(size_t)bh * p.N + i] * 1.4426950408889634f : -INFINITY;
   }
 }
 
@@ -186,7 +187,7 @@ __global__ void __launch_bounds__(384, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
-  const WaitCtx wc{abort_flag, p.status, p.limit_ns};
+  const WaitCtx wc{abort_flag, p.status, p.limit_ns, p.info};
 
   if (warp < 4) {
     setmaxnreg_inc<232>();
@@ -194,15 +195,16 @@ __global__ void __launch_bounds__(384, 1)
     const int r = threadIdx.x;  // key row within the tile == TMEM lane
     const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
     const uint32_t tS = tmem + lane_off, tdP = tmem + 128 + lane_off;
-    const float c = p.scale_log2, sc = p.scale;
+    const float c = p.scale_log2;
+    const float2 c2 = make_float2(c, c);
     bool ok = true;
     for (int it = 0; it < total; ++it) {
       const int i = i0 + it % ni;
-      const float* vl = vec_g + (it & 1) * (T::VEC_BYTES / 4);  // lse2[128], then D[128]
+      const float* vl = vec_g + (it & 1) * (T::VEC_BYTES / 4);  // -lse2[128], then -D[128]
       // The lse2 / D vectors come from the bulk copy of this step: observe
       // its barrier (already complete by now) before reading them.
-      ok = __all_sync(0xffffffffu, wait_bounded(wc, bQf + 8u * (it & 1), (it >> 1) & 1) &&
-                                       wait_bounded(wc, bSdp, it & 1));
+      ok = __all_sync(0xffffffffu, wait_bounded(wc, bQf + 8u * (it & 1), (it >> 1) & 1, wait_site(0x11, it)) &&
+                                       wait_bounded(wc, bSdp, it & 1, wait_site(0x12, it)));
       if (!ok) break;
       tc_fence_after();
       float x[128];
@@ -230,10 +232,12 @@ __global__ void __launch_bounds__(384, 1)
 #pragma unroll
       for (int q4 = 0; q4 < 32; ++q4) {
         const float4 l4 = *reinterpret_cast<const float4*>(vl + 4 * q4);
-        x[4 * q4 + 0] = ex2(fmaf(x[4 * q4 + 0], c, -l4.x));
-        x[4 * q4 + 1] = ex2(fmaf(x[4 * q4 + 1], c, -l4.y));
-        x[4 * q4 + 2] = ex2(fmaf(x[4 * q4 + 2], c, -l4.z));
-        x[4 * q4 + 3] = ex2(fmaf(x[4 * q4 + 3], c, -l4.w));
+        const float2 t0 = ffma2(make_float2(x[4 * q4 + 0], x[4 * q4 + 1]), c2, make_float2(l4.x, l4.y));
+        const float2 t1 = ffma2(make_float2(x[4 * q4 + 2], x[4 * q4 + 3]), c2, make_float2(l4.z, l4.w));
+        x[4 * q4 + 0] = ex2(t0.x);
+        x[4 * q4 + 1] = ex2(t0.y);
+        x[4 * q4 + 2] = ex2(t1.x);
+        x[4 * q4 + 3] = ex2(t1.y);
       }
       if (CAUSAL && i == j) {
 #pragma unroll
@@ -250,8 +254,9 @@ __global__ void __launch_bounds__(384, 1)
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(bP);
-      // dS^T[r][q] = scale * P^T[r][q] * (dP^T[r][q] - D[q]) -> bf16 -> smem
-      // (128-byte swizzled rows: block q/64, 16-byte chunk (q%64)/8).
+      // dS^T[r][q] = P^T[r][q] * (dP^T[r][q] - D[q]) -> bf16 -> smem (128-byte
+      // swizzled rows: block q/64, 16-byte chunk (q%64)/8).  The softmax scale
+      // is applied later, to dK in its epilogue and to dQ in the drain.
 #pragma unroll
       for (int cc = 0; cc < 4; ++cc) {
         uint32_t g[32];
@@ -265,9 +270,10 @@ __global__ void __launch_bounds__(384, 1)
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             const int q = q4 * 8 + 2 * e;
-            const float d0 = sc * x[cc * 32 + q] * (__uint_as_float(g[q]) - Dv[q]);
-            const float d1 = sc * x[cc * 32 + q + 1] * (__uint_as_float(g[q + 1]) - Dv[q + 1]);
-            w[e] = pack_bf16(d0, d1);
+            const float2 dpd = fadd2(make_float2(__uint_as_float(g[q]), __uint_as_float(g[q + 1])),
+                                     make_float2(Dv[q], Dv[q + 1]));
+            const float2 ds = fmul2(make_float2(x[cc * 32 + q], x[cc * 32 + q + 1]), dpd);
+            w[e] = pack_bf16(ds.x, ds.y);
           }
           st_shared_v4(sDS + (cc >> 1) * T::BLOCK_BYTES + sw128_offset(r, (cc & 1) * 4 + q4), w[0], w[1], w[2],
                        w[3]);
@@ -278,7 +284,7 @@ __global__ void __launch_bounds__(384, 1)
       mbar_arrive(bDs);
     }
     // ------------------------------------------------------------ dK / dV out
-    if (ok) ok = __all_sync(0xffffffffu, wait_bounded(wc, bFin, 0));
+    if (ok) ok = __all_sync(0xffffffffu, wait_bounded(wc, bFin, 0, wait_site(0x13, total)));
     const uint32_t stage_dv = sDS, stage_dk = sQ;  // both free once every MMA is done
     if (ok) {
       tc_fence_after();
@@ -286,6 +292,7 @@ __global__ void __launch_bounds__(384, 1)
       for (int which = 0; which < 2; ++which) {
         const uint32_t src = tmem + (which ? 256u : 384u) + lane_off;
         const uint32_t dst = which ? stage_dk : stage_dv;
+        const float2 f2 = which ? make_float2(p.scale, p.scale) : make_float2(1.f, 1.f);  // dK = scale dS^T Q
 #pragma unroll
         for (int cc = 0; cc < D / 32; ++cc) {
           uint32_t o[32];
@@ -297,8 +304,11 @@ __global__ void __launch_bounds__(384, 1)
           for (int q4 = 0; q4 < 4; ++q4) {
             uint32_t w[4];
 #pragma unroll
-            for (int e = 0; e < 4; ++e)
-              w[e] = pack_bf16(__uint_as_float(o[q4 * 8 + 2 * e]), __uint_as_float(o[q4 * 8 + 2 * e + 1]));
+            for (int e = 0; e < 4; ++e) {
+              const float2 t = fmul2(make_float2(__uint_as_float(o[q4 * 8 + 2 * e]),
+                                                 __uint_as_float(o[q4 * 8 + 2 * e + 1])), f2);
+              w[e] = pack_bf16(t.x, t.y);
+            }
             st_shared_v4(dst + blk * T::BLOCK_BYTES + sw128_offset(r, ch0 + q4), w[0], w[1], w[2], w[3]);
           }
         }
@@ -320,9 +330,10 @@ __global__ void __launch_bounds__(384, 1)
     // -------------------------------------------------------------- dQ drain
     const int q = threadIdx.x - 128;  // query row within the tile == TMEM lane
     const uint32_t tQ = tmem + 128 + ((uint32_t)((warp - 4) * 32) << 16);
+    const float2 sc2 = make_float2(p.scale, p.scale);  // dQ = scale dS K
     for (int it = 0; it < total; ++it) {
       const int h = hk * p.G + it / ni, i = i0 + it % ni;
-      if (!__all_sync(0xffffffffu, wait_bounded(wc, bDqf, it & 1))) break;
+      if (!__all_sync(0xffffffffu, wait_bounded(wc, bDqf, it & 1, wait_site(0x21, it)))) break;
       tc_fence_after();
       const int row = i * 128 + q;
       float* dst = p.dq_acc + (((size_t)b * p.H + h) * p.Npad + row) * D;
@@ -334,8 +345,12 @@ __global__ void __launch_bounds__(384, 1)
         reg_fence(g);
         if (row < p.N) {
 #pragma unroll
-          for (int e = 0; e < 8; ++e)
-            red_add_v4(dst + cc * 32 + 4 * e, g[4 * e], g[4 * e + 1], g[4 * e + 2], g[4 * e + 3]);
+          for (int e = 0; e < 8; ++e) {
+            const float2 a = fmul2(make_float2(__uint_as_float(g[4 * e]), __uint_as_float(g[4 * e + 1])), sc2);
+            const float2 b2 = fmul2(make_float2(__uint_as_float(g[4 * e + 2]), __uint_as_float(g[4 * e + 3])), sc2);
+            red_add_v4(dst + cc * 32 + 4 * e, __float_as_uint(a.x), __float_as_uint(a.y), __float_as_uint(b2.x),
+                       __float_as_uint(b2.y));
+          }
         }
       }
       tc_fence_before();
@@ -357,7 +372,7 @@ __global__ void __launch_bounds__(384, 1)
         int issued = 0;
         for (int it = 0; it < total; ++it) {
           const int st = it & 1, rd = it >> 1;
-          if (rd > 0 && !wait_bounded(wc, bQe + 8u * st, (rd - 1) & 1)) break;
+          if (rd > 0 && !wait_bounded(wc, bQe + 8u * st, (rd - 1) & 1, wait_site(0x31, it))) break;
           const int h = hk * p.G + it / ni, i = i0 + it % ni;
           const int bh = b * p.H + h;
           const uint32_t bar = bQf + 8u * st;
@@ -394,25 +409,25 @@ __global__ void __launch_bounds__(384, 1)
             mma_ss(dst, sdesc_sw128(a_tile + off, 16, 1024), sdesc_sw128(b_tile + off, 16, 1024), I_SS, kk > 0);
           }
         };
-        bool ok = wait_bounded(wc, bKV, 0);
+        bool ok = wait_bounded(wc, bKV, 0, wait_site(0x41, 0));
         for (int it = 0; it < total && ok; ++it) {
           const int st = it & 1;
           const uint32_t q_t = sQ + st * T::TILE_BYTES, do_t = sdO + st * T::TILE_BYTES;
-          if (!(ok = wait_bounded(wc, bQf + 8u * st, (it >> 1) & 1))) break;
+          if (!(ok = wait_bounded(wc, bQf + 8u * st, (it >> 1) & 1, wait_site(0x42, it)))) break;
           tc_fence_after();
           mma_kk(tS, sK, q_t);  // S^T = K Q_i^T
-          if (it > 0 && !(ok = wait_bounded(wc, bDqe, (it - 1) & 1))) break;
+          if (it > 0 && !(ok = wait_bounded(wc, bDqe, (it - 1) & 1, wait_site(0x43, it)))) break;
           tc_fence_after();
           mma_kk(tdP, sV, do_t);  // dP^T = V dO_i^T
           mma_commit(bSdp);
-          if (!(ok = wait_bounded(wc, bP, it & 1))) break;
+          if (!(ok = wait_bounded(wc, bP, it & 1, wait_site(0x44, it)))) break;
           tc_fence_after();
           // dV += P^T dO_i: A = P^T (TMEM, bf16 pairs), B = dO_i (MN-major)
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)
             mma_ts(tdV, tS + kk * 8, sdesc_sw128(do_t + kk * 2048, T::BLOCK_BYTES, 1024), I_TB,
                    (it > 0 || kk > 0) ? 1u : 0u);
-          if (!(ok = wait_bounded(wc, bDs, it & 1))) break;
+          if (!(ok = wait_bounded(wc, bDs, it & 1, wait_site(0x45, it)))) break;
           tc_fence_after();
           // dK += dS^T Q_i: A = dS^T (K-major over queries), B = Q_i (MN-major)
 #pragma unroll

@@ -109,7 +109,7 @@ __global__ void __launch_bounds__(384, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
-  const WaitCtx wc{abort_flag, p.status, p.limit_ns};
+  const WaitCtx wc{abort_flag, p.status, p.limit_ns, p.info};
 
   if (warp < 8) {
     setmaxnreg_inc<216>();
@@ -127,7 +127,7 @@ __global__ void __launch_bounds__(384, 1)
     bool ok = true;
 
     for (int j = 0; j < n; ++j) {
-      ok = __all_sync(0xffffffffu, wait_bounded(wc, barS, j & 1));
+      ok = __all_sync(0xffffffffu, wait_bounded(wc, barS, j & 1, wait_site(0x51 + s, j)));
       if (!ok) break;
       tc_fence_after();
       float x[128];
@@ -162,13 +162,13 @@ __global__ void __launch_bounds__(384, 1)
         for (int i = 0; i < 128; ++i)
           if (i >= lim) x[i] = -INFINITY;
       }
+      // Row max with 3-input max: 8 independent chains over pairs of scores.
       float mx[8];
 #pragma unroll
       for (int k = 0; k < 8; ++k) mx[k] = x[k];
 #pragma unroll
-      for (int i = 8; i < 128; ++i) mx[i & 7] = fmaxf(mx[i & 7], x[i]);
-      const float tile_max = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                                   fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+      for (int i = 8; i < 128; i += 2) mx[(i >> 1) & 7] = fmax3(mx[(i >> 1) & 7], x[i], x[i + 1]);
+      const float tile_max = fmaxf(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], fmax3(mx[4], mx[5], mx[6]), mx[7]));
       const float mc = tile_max * c;
       const bool raise = mc > m + 8.0f;  // always true on the first tile
       float alpha = 1.f;
@@ -186,19 +186,30 @@ __global__ void __launch_bounds__(384, 1)
           tmem_wait_ld();
           reg_fence(o);
 #pragma unroll
-          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+          for (int i = 0; i < 32; i += 2) {
+            const float2 t = fmul2(make_float2(__uint_as_float(o[i]), __uint_as_float(o[i + 1])),
+                                   make_float2(alpha, alpha));
+            o[i] = __float_as_uint(t.x);
+            o[i + 1] = __float_as_uint(t.y);
+          }
           tmem_st32(tO + cc * 32, o);
         }
       }
-      float sum[8];
+      // p = 2^(x*c - m): one packed FMA per pair of scores, then ex2; the row
+      // sum runs in 4 packed partial sums.
+      const float2 c2 = make_float2(c, c), nm2 = make_float2(-m, -m);
+      float2 sum[4];
 #pragma unroll
-      for (int k = 0; k < 8; ++k) sum[k] = 0.f;
+      for (int k = 0; k < 4; ++k) sum[k] = make_float2(0.f, 0.f);
 #pragma unroll
-      for (int i = 0; i < 128; ++i) {
-        x[i] = ex2(fmaf(x[i], c, -m));
-        sum[i & 7] += x[i];
+      for (int i = 0; i < 128; i += 2) {
+        const float2 t = ffma2(make_float2(x[i], x[i + 1]), c2, nm2);
+        x[i] = ex2(t.x);
+        x[i + 1] = ex2(t.y);
+        sum[(i >> 1) & 3] = fadd2(sum[(i >> 1) & 3], make_float2(x[i], x[i + 1]));
       }
-      l = l * alpha + (((sum[0] + sum[1]) + (sum[2] + sum[3])) + ((sum[4] + sum[5]) + (sum[6] + sum[7])));
+      const float2 s01 = fadd2(sum[0], sum[1]), s23 = fadd2(sum[2], sum[3]);
+      l = l * alpha + ((s01.x + s23.x) + (s01.y + s23.y));
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         uint32_t pk[32];
@@ -212,7 +223,7 @@ __global__ void __launch_bounds__(384, 1)
     }
 
     // ------------------------------------------------------------ epilogue
-    if (ok) ok = __all_sync(0xffffffffu, wait_bounded(wc, barO, 0));
+    if (ok) ok = __all_sync(0xffffffffu, wait_bounded(wc, barO, 0, wait_site(0x53 + s, 0)));
     const uint32_t sOut = sQ + s * T::TILE_BYTES;  // Q tile is dead once O is final
     if (ok) {
       tc_fence_after();
@@ -266,7 +277,7 @@ __global__ void __launch_bounds__(384, 1)
         for (int j = 0; j < n1 && ok; ++j) {
           for (int w = 0; w < 2; ++w) {
             const int st = t % T::NSTAGE, rd = t / T::NSTAGE;
-            if (rd > 0 && !(ok = wait_bounded(wc, bKVe + 8u * st, (rd - 1) & 1))) break;
+            if (rd > 0 && !(ok = wait_bounded(wc, bKVe + 8u * st, (rd - 1) & 1, wait_site(0x61, t)))) break;
             mbar_expect_tx(bKVf + 8u * st, T::TILE_BYTES);
             const CUtensorMap* m = (w == 0) ? &tmK : &tmV;
             for (int c = 0; c < T::NB; ++c)
@@ -302,12 +313,12 @@ __global__ void __launch_bounds__(384, 1)
             mma_ts(dO, p_tmem + kk * 8, sdesc_sw128(v_tile + kk * 2048, T::BLOCK_BYTES, 1024), IPV,
                    (acc || kk > 0) ? 1u : 0u);
         };
-        bool ok = wait_bounded(wc, bKVf, 0) && wait_bounded(wc, bQ, 0);
+        bool ok = wait_bounded(wc, bKVf, 0, wait_site(0x71, 0)) && wait_bounded(wc, bQ, 0, wait_site(0x72, 0));
         if (ok) {
           tc_fence_after();
           qk(tS0, sQ, sKV);
           mma_commit(bS);
-          ok = wait_bounded(wc, bQ + 8u, 0);
+          ok = wait_bounded(wc, bQ + 8u, 0, wait_site(0x73, 0));
         }
         if (ok) {
           tc_fence_after();
@@ -319,11 +330,11 @@ __global__ void __launch_bounds__(384, 1)
         for (int j = 0; j < n1 && ok; ++j, t += 2) {
           const int sv = t % T::NSTAGE, sk = (t + 1) % T::NSTAGE;
           const bool next = j + 1 < n1;
-          if (!(ok = wait_bounded(wc, bKVf + 8u * sv, (t / T::NSTAGE) & 1))) break;
-          if (next && !(ok = wait_bounded(wc, bKVf + 8u * sk, ((t + 1) / T::NSTAGE) & 1))) break;
+          if (!(ok = wait_bounded(wc, bKVf + 8u * sv, (t / T::NSTAGE) & 1, wait_site(0x74, j)))) break;
+          if (next && !(ok = wait_bounded(wc, bKVf + 8u * sk, ((t + 1) / T::NSTAGE) & 1, wait_site(0x75, j)))) break;
           const uint32_t vt = sKV + sv * T::TILE_BYTES, kt = sKV + sk * T::TILE_BYTES;
           if (j < n0) {
-            if (!(ok = wait_bounded(wc, bP, j & 1))) break;
+            if (!(ok = wait_bounded(wc, bP, j & 1, wait_site(0x76, j)))) break;
             tc_fence_after();
             pv(tO0, tS0, vt, j > 0);
             if (j + 1 < n0) {
@@ -333,7 +344,7 @@ __global__ void __launch_bounds__(384, 1)
               mma_commit(bO);
             }
           }
-          if (!(ok = wait_bounded(wc, bP + 8u, j & 1))) break;
+          if (!(ok = wait_bounded(wc, bP + 8u, j & 1, wait_site(0x77, j)))) break;
           tc_fence_after();
           pv(tO1, tS1, vt, j > 0);
           if (next) {

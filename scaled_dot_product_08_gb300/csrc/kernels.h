@@ -18,6 +18,7 @@ struct FwdParams {
   float scale_log2;      // scale * log2(e)
   int* status;           // device status word
   unsigned long long limit_ns;  // bounded-wait limit
+  int* info;             // first-timeout record (4 ints)
 };
 
 // Backward arguments.
@@ -35,6 +36,7 @@ struct BwdParams {
   float scale_log2;      // scale * log2(e)
   int* status;
   unsigned long long limit_ns;
+  int* info;
 };
 
 // Shared-memory bytes of each kernel instance (for validation and launch).

@@ -57,13 +57,18 @@ struct WaitCtx {
   volatile int* abort_flag;  // shared memory
   int* status;               // global memory
   uint64_t limit_ns;
+  int* info;                 // global memory: where the first timeout happened
 };
+
+// Wait-site codes recorded with a timeout: (site << 16) | (loop step & 0xffff).
+__device__ __forceinline__ int wait_site(int site, int step) { return (site << 16) | (step & 0xffff); }
 
 // Waits for phase `parity` of `bar`.  Gives up when another role of the CTA
 // has aborted, or when `limit_ns` has passed, in which case it raises the
-// CTA abort flag and records a timeout in the status word.  Returns false
-// when the caller must stop.
-__device__ __forceinline__ bool wait_bounded(const WaitCtx& w, uint32_t bar, uint32_t parity) {
+// CTA abort flag, records a timeout in the status word and, for the first
+// timeout on the device, where it happened (site, block, thread, waited us).
+// Returns false when the caller must stop.
+__device__ __forceinline__ bool wait_bounded(const WaitCtx& w, uint32_t bar, uint32_t parity, int site = 0) {
   if (mbar_try(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   uint32_t it = 0;
@@ -73,7 +78,12 @@ __device__ __forceinline__ bool wait_bounded(const WaitCtx& w, uint32_t bar, uin
       if (*w.abort_flag) return false;
       if (globaltimer_ns() - t0 > w.limit_ns) {
         *w.abort_flag = 1;
-        atomicCAS(w.status, 0, kDevTimeout);
+        if (atomicCAS(w.status, 0, kDevTimeout) == 0 && w.info != nullptr) {
+          w.info[0] = site;
+          w.info[1] = (int)blockIdx.x;
+          w.info[2] = (int)threadIdx.x;
+          w.info[3] = (int)((globaltimer_ns() - t0) / 1000);
+        }
         return false;
       }
     }
@@ -255,6 +265,42 @@ __device__ __forceinline__ void setmaxnreg_inc() {
 template <int N>
 __device__ __forceinline__ void setmaxnreg_dec() {
   asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+
+// ------------------------------------------------- Blackwell fp32 pair math
+// Three-input maximum and packed fp32x2 FMA / add / multiply (sm_100+): one
+// instruction does the work of two (or, for max, halves a reduction chain).
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
+  float2 d;
+  asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\tmov.b64 rc, {%6, %7};\n\t"
+      "fma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+  return d;
+}
+__device__ __forceinline__ float2 fadd2(float2 a, float2 b) {
+  float2 d;
+  asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+      "add.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return d;
+}
+__device__ __forceinline__ float2 fmul2(float2 a, float2 b) {
+  float2 d;
+  asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+      "mul.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return d;
 }
 
 // ------------------------------------------------------------- misc helpers

@@ -163,6 +163,8 @@ def test_bounded_wait_times_out_and_context_survives(cuda_lib):
     S = cuda_lib.Status
     assert cuda_lib.attn_get_device_status(None) == S.OK
     assert cuda_lib.attn_selftest_wait_timeout(20000, None) == S.OK   # 20 ms limit
+    st, info = cuda_lib.attn_get_timeout_info(None)
+    assert st == S.OK and info[0] >> 16 == 0x01 and info[1] == 0 and info[3] >= 19000
     assert cuda_lib.attn_get_device_status(None) == S.TIMEOUT
     assert cuda_lib.attn_get_device_status(None) == S.OK              # cleared by the read
     # the context is still usable: a normal forward runs and is correct
