@@ -191,6 +191,7 @@ __global__ void __launch_bounds__(384, 1)
 
   if (warp < 4) {
     setmaxnreg_inc<232>();
+    reg_split_sync(384);
     // -------------------------------------------------------------- compute
     const int r = threadIdx.x;  // key row within the tile == TMEM lane
     const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
@@ -327,6 +328,7 @@ __global__ void __launch_bounds__(384, 1)
     setmaxnreg_dec<168>();
   } else if (warp < 8) {
     setmaxnreg_dec<136>();
+    reg_split_sync(384);
     // -------------------------------------------------------------- dQ drain
     const int q = threadIdx.x - 128;  // query row within the tile == TMEM lane
     const uint32_t tQ = tmem + 128 + ((uint32_t)((warp - 4) * 32) << 16);
@@ -359,6 +361,7 @@ __global__ void __launch_bounds__(384, 1)
     setmaxnreg_inc<168>();
   } else {
     setmaxnreg_dec<136>();
+    reg_split_sync(384);
     if (warp == 8) {
       // ------------------------------------------------------------ producer
       if (lane == 0) {

@@ -113,6 +113,7 @@ __global__ void __launch_bounds__(384, 1)
 
   if (warp < 8) {
     setmaxnreg_inc<216>();
+    reg_split_sync(384);
     // ------------------------------------------------------------ softmax
     const int s = warp >> 2;            // query tile of this warpgroup
     const int r = threadIdx.x & 127;    // row within the tile == TMEM lane
@@ -260,6 +261,7 @@ __global__ void __launch_bounds__(384, 1)
     setmaxnreg_dec<168>();  // one register budget again for the common teardown
   } else {
     setmaxnreg_dec<72>();
+    reg_split_sync(384);
     if (warp == 8) {
       // ------------------------------------------------------------ producer
       if (lane == 0) {

@@ -258,6 +258,12 @@ __device__ __forceinline__ void reg_fence(uint32_t (&r)[16]) { asm volatile("" :
 #undef SDPA_P8
 
 // Re-balances registers between warpgroups (all threads of a warpgroup).
+// setmaxnreg.inc waits until other warps have released registers, and it
+// waits forever if they never do.  A kernel whose idle warps give registers
+// back with dec and later take them again with inc must therefore make every
+// inc at the start complete before any warp can run its closing inc:
+// reg_split_sync() after the opening setmaxnreg of every warpgroup does that.
+constexpr uint32_t kRegSplitBarrier = 15;
 template <int N>
 __device__ __forceinline__ void setmaxnreg_inc() {
   asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
@@ -265,6 +271,10 @@ __device__ __forceinline__ void setmaxnreg_inc() {
 template <int N>
 __device__ __forceinline__ void setmaxnreg_dec() {
   asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+
+__device__ __forceinline__ void reg_split_sync(uint32_t nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(kRegSplitBarrier), "r"(nthreads) : "memory");
 }
 
 // ------------------------------------------------- Blackwell fp32 pair math
