@@ -157,6 +157,38 @@ int attn_abi_version(void);
  */
 attn_status_t attn_selftest_wait_timeout(unsigned int timeout_us, void* stream);
 
+/*
+ * attn_bwd for callers that cannot allocate device memory.  The pages have no
+ * counterpart; this is a property of the library, not of the method.
+ *
+ * Some callers have no way to provide attn_bwd's workspace: code running
+ * where cudaMalloc is not allowed (inside a custom allocator, or a runtime
+ * that owns the whole device memory pool) or a plug-in interface that passes
+ * only tensor pointers.  This entry point computes exactly what attn_bwd
+ * computes, with the same arguments minus the workspace, using instead a
+ * fixed 64 MiB scratch array compiled into the library.  It calls no
+ * cudaMalloc, cudaFree or other allocating routine.
+ *   - Limit: shapes whose attn_bwd_workspace_size() exceeds 64 MiB
+ *     (67108864 bytes) are rejected with ATTN_ERR_WORKSPACE; use attn_bwd
+ *     with a caller workspace for those.  (At d = 128 that allows
+ *     B*H*ceil(N/128)*128 <= 129,055 rows, e.g. B=1, H=16, N=8064.)
+ *   - Memory: every GPU that loads the library holds the 64 MiB until the
+ *     process exits.
+ *   - Set-up: the first call on a device looks up the array's device address
+ *     with that device current; make that first call before any stream
+ *     capture.
+ *   - Sharing: all calls use the same array, which keeps the last call's
+ *     contents (each call clears what it needs cleared).  Calls whose work
+ *     overlaps on the GPU (different streams, or different host threads
+ *     without ordering) race on the array and give wrong results; order
+ *     them on one stream.
+ */
+attn_status_t attn_bwd_noalloc(const void* q, const void* k, const void* v, const void* o,
+                               const float* lse, const void* dout,
+                               void* dq, void* dk, void* dv,
+                               int B, int H, int Hkv, int N, int d, float scale, int causal,
+                               void* stream);
+
 #ifdef __cplusplus
 }
 #endif

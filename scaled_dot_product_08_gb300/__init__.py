@@ -21,7 +21,7 @@ from .build import LIB, build  # noqa: F401  (build() is the supported way to co
 
 __all__ = [
     "AttnError", "Status", "load", "attn_fwd", "attn_bwd", "attn_bwd_workspace_size",
-    "attn_bwd_prep", "attn_bwd_grad", "attn_bwd_dq",
+    "attn_bwd_prep", "attn_bwd_grad", "attn_bwd_dq", "attn_bwd_noalloc",
     "attn_get_device_status", "attn_get_timeout_info", "attn_status_string", "attn_selftest_wait_timeout",
     "forward", "backward", "build",
 ]
@@ -77,6 +77,9 @@ def load() -> ctypes.CDLL:
         lib.attn_status_string.restype = ctypes.c_char_p
         lib.attn_abi_version.argtypes = []
         lib.attn_abi_version.restype = _I
+        lib.attn_bwd_noalloc.argtypes = [_P, _P, _P, _P, _P, _P, _P, _P, _P,
+                                         _I, _I, _I, _I, _I, ctypes.c_float, _I, _P]
+        lib.attn_bwd_noalloc.restype = _I
         lib.attn_get_timeout_info.argtypes = [ctypes.POINTER(ctypes.c_int), _P]
         lib.attn_get_timeout_info.restype = _I
         lib.attn_selftest_wait_timeout.argtypes = [ctypes.c_uint, _P]
@@ -102,6 +105,11 @@ def attn_bwd(q, k, v, o, lse, dout, dq, dk, dv, workspace, workspace_bytes,
              B, H, Hkv, N, d, scale, causal, stream) -> int:
     return load().attn_bwd(q, k, v, o, lse, dout, dq, dk, dv, workspace, workspace_bytes,
                            B, H, Hkv, N, d, scale, int(causal), stream)
+
+
+def attn_bwd_noalloc(q, k, v, o, lse, dout, dq, dk, dv, B, H, Hkv, N, d, scale, causal, stream) -> int:
+    """attn_bwd without a caller workspace (fixed 64 MiB scratch inside the library)."""
+    return load().attn_bwd_noalloc(q, k, v, o, lse, dout, dq, dk, dv, B, H, Hkv, N, d, scale, int(causal), stream)
 
 
 def attn_bwd_prep(o, lse, dout, workspace, workspace_bytes, B, H, Hkv, N, d, stream) -> int:
