@@ -110,6 +110,20 @@ bool make_map_bf16(CUtensorMap* m, const void* ptr, int d, int N, long long head
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 3-D map over the float32 dQ accumulator (rows = B*H, Npad, d): box of 32
+// columns (128 bytes) x 128 rows x 1 head, 128-byte swizzle (TMA reductions).
+bool make_map_f32_acc(CUtensorMap* m, const void* ptr, int d, int npad, long long heads) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)npad, (cuuint64_t)heads};
+  cuuint64_t strides[2] = {(cuuint64_t)d * 4, (cuuint64_t)d * 4 * (cuuint64_t)npad};
+  cuuint32_t box[3] = {32, 128, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(ptr), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 // Shape checks shared by forward and backward.
@@ -289,8 +303,10 @@ attn_status_t attn_bwd_grad(const void* q, const void* k, const void* v, const v
     return ATTN_ERR_CUDA;
   sdpa::BwdParams p;
   bwd_params(&p, workspace, B, H, Hkv, N, d, scale, di);
-  cudaError_t e =
-      sdpa::launch_bwd_grad(d, causal != 0, tq, tk, tv, tdo, tdk, tdv, p, static_cast<cudaStream_t>(stream));
+  CUtensorMap tdqa;
+  if (!make_map_f32_acc(&tdqa, p.dq_acc, d, p.Npad, (long long)B * H)) return ATTN_ERR_CUDA;
+  cudaError_t e = sdpa::launch_bwd_grad(d, causal != 0, tq, tk, tv, tdo, tdk, tdv, tdqa, p,
+                                        static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;
 }
 

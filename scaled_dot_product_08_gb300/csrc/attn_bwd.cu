@@ -15,19 +15,19 @@
 //               GQA group's query heads and the query tiles i (i >= j when
 //               causal).  dK_j and dV_j accumulate in tensor memory; dQ_i
 //               contributions are added to a float32 accumulator in global
-//               memory with vector reductions.
+//               memory with TMA bulk reductions.
 //   bwd_convert dQ accumulator -> bf16 dQ
 //
 // bwd_main warp roles (384 threads = 3 warpgroups):
 //   warps 0-3   compute: S^T -> P^T (written to TMEM as the A operand of the
 //               dV MMA), dP^T -> dS^T (written to shared memory, the A
 //               operand of the dK and dQ MMAs); dK/dV epilogue
-//   warps 4-7   dQ drain: TMEM -> red.global.add.v4.f32
+//   warps 4-7   dQ drain: TMEM -> shared memory -> TMA reduce-add
 //   warp  8     TMA producer: K_j, V_j once; Q_i, dO_i, lse2_i, D_i per step
 //   warp  9     MMA issuer (one thread)
 //   warps 10-11 idle
-// setmaxnreg: compute 232, drain 136, producer/MMA 136 registers per thread
-// (128 * (232 + 136 + 136) = 384 * 168, the launch allocation).
+// setmaxnreg: compute 240, drain 160, producer/MMA 104 registers per thread
+// (128 * (240 + 160 + 104) = 384 * 168, the launch allocation).
 // Tensor memory: [0,128) S^T / P^T, [128,256) dP^T / dQ_i, [256,256+d) dK,
 // [384,384+d) dV.  All score tiles are 128 x 128 (keys x queries).
 #include <cmath>
@@ -104,25 +104,19 @@ struct BwdTraits {
   static constexpr int KSTEPS = D / 16;
   static constexpr int DS_BYTES = 2 * BLOCK_BYTES;     // dS^T: 128 keys x 128 queries, any d
   static constexpr int VEC_BYTES = 1024;               // lse2[128] + D[128]
-  static constexpr int NBAR = 1 + 2 + 2 + 1 + 1 + 1 + 1 + 1 + 1 + 1;
+  static constexpr int NBAR = 1 + 2 + 2 + 1 + 1 + 1 + 1 + 1 + 1 + 1 + 1 + 1;
   // K, V, Q[2], dO[2], dS^T, then vectors, barriers, misc
   static constexpr int TILES_BYTES = 6 * TILE_BYTES + DS_BYTES;
   static constexpr int SMEM = TILES_BYTES + 2 * VEC_BYTES + NBAR * 8 + 16;
   static constexpr int THREADS = 384;
 };
 
-__device__ __forceinline__ void red_add_v4(float* addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
-  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(__uint_as_float(a)),
-               "f"(__uint_as_float(b)), "f"(__uint_as_float(c)), "f"(__uint_as_float(d))
-               : "memory");
-}
-
 template <int D, bool CAUSAL>
 __global__ void __launch_bounds__(384, 1)
     bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
                     const __grid_constant__ CUtensorMap tmdK, const __grid_constant__ CUtensorMap tmdV,
-                    const BwdParams p) {
+                    const __grid_constant__ CUtensorMap tmdQacc, const BwdParams p) {
   using T = BwdTraits<D>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const uint32_t base = smem_u32(smem_raw);
@@ -142,13 +136,15 @@ __global__ void __launch_bounds__(384, 1)
   const uint32_t bKV = sBar;
   const uint32_t bQf = bKV + 8;     // qdo_full[2]
   const uint32_t bQe = bQf + 16;    // qdo_empty[2]
-  const uint32_t bSdp = bQe + 16;   // S^T and dP^T ready
-  const uint32_t bP = bSdp + 8;     // P^T in TMEM (128 arrivals)
+  const uint32_t bS = bQe + 16;     // S^T ready
+  const uint32_t bP = bS + 8;       // P^T in TMEM (128 arrivals)
   const uint32_t bDs = bP + 8;      // dS^T in smem (128 arrivals)
   const uint32_t bDqf = bDs + 8;    // dQ_i in TMEM
   const uint32_t bDqe = bDqf + 8;   // dQ_i drained (128 arrivals)
   const uint32_t bFin = bDqe + 8;   // every MMA done
   const uint32_t bDrain = bFin + 8;
+  const uint32_t bDp = bDrain + 8;  // dP^T ready
+  const uint32_t bStg = bDp + 8;    // dQ_i staged in shared memory (128 arrivals)
   uint8_t* const misc = smem_raw + (sBar - base) + 8 * T::NBAR;
   uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(misc);
   volatile int* const abort_flag = reinterpret_cast<volatile int*>(misc + 4);
@@ -169,7 +165,9 @@ __global__ void __launch_bounds__(384, 1)
       mbar_init(bQf + 8u * s, 1);
       mbar_init(bQe + 8u * s, 1);
     }
-    mbar_init(bSdp, 1);
+    mbar_init(bS, 1);
+    mbar_init(bDp, 1);
+    mbar_init(bStg, 128);
     mbar_init(bP, 128);
     mbar_init(bDs, 128);
     mbar_init(bDqf, 1);
@@ -190,7 +188,7 @@ __global__ void __launch_bounds__(384, 1)
   const WaitCtx wc{abort_flag, p.status, p.limit_ns, p.info};
 
   if (warp < 4) {
-    setmaxnreg_inc<232>();
+    setmaxnreg_inc<240>();
     reg_split_sync(384);
     // -------------------------------------------------------------- compute
     const int r = threadIdx.x;  // key row within the tile == TMEM lane
@@ -205,7 +203,7 @@ __global__ void __launch_bounds__(384, 1)
       // The lse2 / D vectors come from the bulk copy of this step: observe
       // its barrier (already complete by now) before reading them.
       ok = __all_sync(0xffffffffu, wait_bounded(wc, bQf + 8u * (it & 1), (it >> 1) & 1, wait_site(0x11, it)) &&
-                                       wait_bounded(wc, bSdp, it & 1, wait_site(0x12, it)));
+                                       wait_bounded(wc, bS, it & 1, wait_site(0x12, it)));
       if (!ok) break;
       tc_fence_after();
       float x[128];
@@ -245,35 +243,53 @@ __global__ void __launch_bounds__(384, 1)
         for (int q = 0; q < 128; ++q)
           if (r > q) x[q] = 0.f;
       }
+      // P^T as bf16 pairs: written to TMEM for the dV MMA and kept in
+      // registers for dS.
+      uint32_t pa[32], pb[32];
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        uint32_t pk[32];
-#pragma unroll
-        for (int e = 0; e < 32; ++e) pk[e] = pack_bf16(x[64 * h + 2 * e], x[64 * h + 2 * e + 1]);
-        tmem_st32(tS + 32 * h, pk);
+      for (int e = 0; e < 32; ++e) {
+        pa[e] = pack_bf16(x[2 * e], x[2 * e + 1]);
+        pb[e] = pack_bf16(x[64 + 2 * e], x[64 + 2 * e + 1]);
       }
+      tmem_st32(tS, pa);
+      tmem_st32(tS + 32, pb);
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(bP);
       // dS^T[r][q] = P^T[r][q] * (dP^T[r][q] - D[q]) -> bf16 -> smem (128-byte
       // swizzled rows: block q/64, 16-byte chunk (q%64)/8).  The softmax scale
       // is applied later, to dK in its epilogue and to dQ in the drain.
+      ok = __all_sync(0xffffffffu, wait_bounded(wc, bDp, it & 1, wait_site(0x14, it)));
+      if (!ok) break;
+      tc_fence_after();
+      uint32_t g0[32], g1[32], g2[32], g3[32];
+      tmem_ld32(tdP + 0, g0);
+      tmem_ld32(tdP + 32, g1);
+      tmem_ld32(tdP + 64, g2);
+      tmem_ld32(tdP + 96, g3);
+      tmem_wait_ld();
+      reg_fence(g0);
+      reg_fence(g1);
+      reg_fence(g2);
+      reg_fence(g3);
 #pragma unroll
       for (int cc = 0; cc < 4; ++cc) {
-        uint32_t g[32];
-        tmem_ld32(tdP + cc * 32, g);
-        tmem_wait_ld();
-        reg_fence(g);
-        const float* Dv = vl + 128 + cc * 32;
+        const uint32_t* g = cc == 0 ? g0 : cc == 1 ? g1 : cc == 2 ? g2 : g3;
+        const uint32_t* pk = (cc < 2) ? pa : pb;
+        const float4* Dv = reinterpret_cast<const float4*>(vl + 128 + cc * 32);
 #pragma unroll
         for (int q4 = 0; q4 < 4; ++q4) {
           uint32_t w[4];
+          const float4 da = Dv[2 * q4], db = Dv[2 * q4 + 1];
+          const float2 dd[4] = {make_float2(da.x, da.y), make_float2(da.z, da.w), make_float2(db.x, db.y),
+                                make_float2(db.z, db.w)};
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
-            const int q = q4 * 8 + 2 * e;
-            const float2 dpd = fadd2(make_float2(__uint_as_float(g[q]), __uint_as_float(g[q + 1])),
-                                     make_float2(Dv[q], Dv[q + 1]));
-            const float2 ds = fmul2(make_float2(x[cc * 32 + q], x[cc * 32 + q + 1]), dpd);
+            const int q = q4 * 8 + 2 * e;  // column within this 32-column chunk
+            const uint32_t pp = pk[((cc & 1) * 32 + q) >> 1];
+            const float2 pf = make_float2(__uint_as_float(pp << 16), __uint_as_float(pp & 0xffff0000u));
+            const float2 dpd = fadd2(make_float2(__uint_as_float(g[q]), __uint_as_float(g[q + 1])), dd[e]);
+            const float2 ds = fmul2(pf, dpd);
             w[e] = pack_bf16(ds.x, ds.y);
           }
           st_shared_v4(sDS + (cc >> 1) * T::BLOCK_BYTES + sw128_offset(r, (cc & 1) * 4 + q4), w[0], w[1], w[2],
@@ -286,7 +302,7 @@ __global__ void __launch_bounds__(384, 1)
     }
     // ------------------------------------------------------------ dK / dV out
     if (ok) ok = __all_sync(0xffffffffu, wait_bounded(wc, bFin, 0, wait_site(0x13, total)));
-    const uint32_t stage_dv = sDS, stage_dk = sQ;  // both free once every MMA is done
+    const uint32_t stage_dv = sDS, stage_dk = sK;  // both free once every MMA is done
     if (ok) {
       tc_fence_after();
 #pragma unroll
@@ -327,40 +343,63 @@ __global__ void __launch_bounds__(384, 1)
     }
     setmaxnreg_dec<168>();
   } else if (warp < 8) {
-    setmaxnreg_dec<136>();
+    setmaxnreg_dec<160>();
     reg_split_sync(384);
     // -------------------------------------------------------------- dQ drain
     const int q = threadIdx.x - 128;  // query row within the tile == TMEM lane
     const uint32_t tQ = tmem + 128 + ((uint32_t)((warp - 4) * 32) << 16);
     const float2 sc2 = make_float2(p.scale, p.scale);  // dQ = scale dS K
+    // dQ_i goes out through the step's Q / dO shared-memory stage, which is
+    // idle once dQ_i is final (every MMA that read it has completed): fp32,
+    // boxes of 32 columns x 128 rows with the 128-byte swizzle, added into
+    // the accumulator by TMA reductions.  The stage is then handed back to
+    // the producer (qdo_empty).
+    constexpr int NBOX = D / 32;
     for (int it = 0; it < total; ++it) {
       const int h = hk * p.G + it / ni, i = i0 + it % ni;
+      const int st = it & 1;
       if (!__all_sync(0xffffffffu, wait_bounded(wc, bDqf, it & 1, wait_site(0x21, it)))) break;
       tc_fence_after();
-      const int row = i * 128 + q;
-      float* dst = p.dq_acc + (((size_t)b * p.H + h) * p.Npad + row) * D;
+      uint32_t g[NBOX][32];
 #pragma unroll
-      for (int cc = 0; cc < D / 32; ++cc) {
-        uint32_t g[32];
-        tmem_ld32(tQ + cc * 32, g);
-        tmem_wait_ld();
-        reg_fence(g);
-        if (row < p.N) {
+      for (int cc = 0; cc < NBOX; ++cc) tmem_ld32(tQ + cc * 32, g[cc]);
+      tmem_wait_ld();
 #pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            const float2 a = fmul2(make_float2(__uint_as_float(g[4 * e]), __uint_as_float(g[4 * e + 1])), sc2);
-            const float2 b2 = fmul2(make_float2(__uint_as_float(g[4 * e + 2]), __uint_as_float(g[4 * e + 3])), sc2);
-            red_add_v4(dst + cc * 32 + 4 * e, __float_as_uint(a.x), __float_as_uint(a.y), __float_as_uint(b2.x),
-                       __float_as_uint(b2.y));
-          }
+      for (int cc = 0; cc < NBOX; ++cc) reg_fence(g[cc]);
+      tc_fence_before();
+      mbar_arrive(bDqe);  // TMEM columns free for the next dP^T
+#pragma unroll
+      for (int cc = 0; cc < NBOX; ++cc) {
+        const uint32_t box = (cc < T::NB) ? sQ + st * T::TILE_BYTES + cc * T::BLOCK_BYTES
+                                          : sdO + st * T::TILE_BYTES + (cc - T::NB) * T::BLOCK_BYTES;
+#pragma unroll
+        for (int c8 = 0; c8 < 8; ++c8) {
+          const float2 a0 = fmul2(make_float2(__uint_as_float(g[cc][4 * c8]), __uint_as_float(g[cc][4 * c8 + 1])), sc2);
+          const float2 a1 = fmul2(make_float2(__uint_as_float(g[cc][4 * c8 + 2]), __uint_as_float(g[cc][4 * c8 + 3])), sc2);
+          st_shared_v4(box + sw128_offset(q, c8), __float_as_uint(a0.x), __float_as_uint(a0.y), __float_as_uint(a1.x),
+                       __float_as_uint(a1.y));
         }
       }
-      tc_fence_before();
-      mbar_arrive(bDqe);
+      fence_proxy_async_smem();
+      mbar_arrive(bStg);
+      // One thread waits (bounded) for all 128 to have staged, then reduces.
+      if (q == 0 && wait_bounded(wc, bStg, it & 1, wait_site(0x22, it))) {
+        const int bh = b * p.H + h;
+#pragma unroll
+        for (int cc = 0; cc < NBOX; ++cc) {
+          const uint32_t box = (cc < T::NB) ? sQ + st * T::TILE_BYTES + cc * T::BLOCK_BYTES
+                                            : sdO + st * T::TILE_BYTES + (cc - T::NB) * T::BLOCK_BYTES;
+          tma_reduce_add_3d(&tmdQacc, box, cc * 32, i * 128, bh);
+        }
+        bulk_commit();
+        bulk_wait_read_all();
+        mbar_arrive(bQe + 8u * st);
+      }
     }
+    if (q == 0) bulk_wait_all();  // every reduction has landed before the CTA exits
     setmaxnreg_inc<168>();
   } else {
-    setmaxnreg_dec<136>();
+    setmaxnreg_dec<104>();
     reg_split_sync(384);
     if (warp == 8) {
       // ------------------------------------------------------------ producer
@@ -412,17 +451,24 @@ __global__ void __launch_bounds__(384, 1)
             mma_ss(dst, sdesc_sw128(a_tile + off, 16, 1024), sdesc_sw128(b_tile + off, 16, 1024), I_SS, kk > 0);
           }
         };
-        bool ok = wait_bounded(wc, bKV, 0, wait_site(0x41, 0));
+        // Issue order per step i (stage st): dV(i), S^T(i+1), dK(i), dQ(i),
+        // dP^T(i+1).  S^T(i+1) overwrites P^T(i) in TMEM only after dV(i),
+        // which was issued first (MMAs from one thread run in order), so
+        // the softmax of step i+1 overlaps the dK / dQ MMAs of step i.
+        bool ok = wait_bounded(wc, bKV, 0, wait_site(0x41, 0)) &&
+                  wait_bounded(wc, bQf, 0, wait_site(0x42, 0));
+        if (ok) {
+          tc_fence_after();
+          mma_kk(tS, sK, sQ);  // S^T_0 = K Q_0^T
+          mma_commit(bS);
+          mma_kk(tdP, sV, sdO);  // dP^T_0 = V dO_0^T
+          mma_commit(bDp);
+        }
         for (int it = 0; it < total && ok; ++it) {
-          const int st = it & 1;
+          const int st = it & 1, sn = st ^ 1;
+          const bool nx = it + 1 < total;
           const uint32_t q_t = sQ + st * T::TILE_BYTES, do_t = sdO + st * T::TILE_BYTES;
-          if (!(ok = wait_bounded(wc, bQf + 8u * st, (it >> 1) & 1, wait_site(0x42, it)))) break;
-          tc_fence_after();
-          mma_kk(tS, sK, q_t);  // S^T = K Q_i^T
-          if (it > 0 && !(ok = wait_bounded(wc, bDqe, (it - 1) & 1, wait_site(0x43, it)))) break;
-          tc_fence_after();
-          mma_kk(tdP, sV, do_t);  // dP^T = V dO_i^T
-          mma_commit(bSdp);
+          const uint32_t q_n = sQ + sn * T::TILE_BYTES, do_n = sdO + sn * T::TILE_BYTES;
           if (!(ok = wait_bounded(wc, bP, it & 1, wait_site(0x44, it)))) break;
           tc_fence_after();
           // dV += P^T dO_i: A = P^T (TMEM, bf16 pairs), B = dO_i (MN-major)
@@ -430,6 +476,12 @@ __global__ void __launch_bounds__(384, 1)
           for (int kk = 0; kk < 8; ++kk)
             mma_ts(tdV, tS + kk * 8, sdesc_sw128(do_t + kk * 2048, T::BLOCK_BYTES, 1024), I_TB,
                    (it > 0 || kk > 0) ? 1u : 0u);
+          if (nx) {
+            if (!(ok = wait_bounded(wc, bQf + 8u * sn, ((it + 1) >> 1) & 1, wait_site(0x46, it)))) break;
+            tc_fence_after();
+            mma_kk(tS, sK, q_n);  // S^T_{i+1}
+            mma_commit(bS);
+          }
           if (!(ok = wait_bounded(wc, bDs, it & 1, wait_site(0x45, it)))) break;
           tc_fence_after();
           // dK += dS^T Q_i: A = dS^T (K-major over queries), B = Q_i (MN-major)
@@ -442,8 +494,13 @@ __global__ void __launch_bounds__(384, 1)
           for (int kk = 0; kk < 8; ++kk)
             mma_ss(tdP, sdesc_sw128(sDS + kk * 2048, T::BLOCK_BYTES, 1024),
                    sdesc_sw128(sK + kk * 2048, T::BLOCK_BYTES, 1024), I_MM, kk > 0 ? 1u : 0u);
-          mma_commit(bDqf);
-          mma_commit(bQe + 8u * st);
+          mma_commit(bDqf);  // the drain releases the Q / dO stage after staging dQ_i in it
+          if (nx) {
+            if (!(ok = wait_bounded(wc, bDqe, it & 1, wait_site(0x43, it)))) break;
+            tc_fence_after();
+            mma_kk(tdP, sV, do_n);  // dP^T_{i+1}
+            mma_commit(bDp);
+          }
         }
         if (ok) mma_commit(bFin);
         mma_commit(bDrain);  // fires once every MMA issued above has finished
@@ -474,12 +531,12 @@ size_t bwd_smem_bytes(int d) {
 template <int D, bool C>
 static cudaError_t launch_main_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                                  const CUtensorMap& tdo, const CUtensorMap& tdk, const CUtensorMap& tdv,
-                                 const BwdParams& p, cudaStream_t stream) {
+                                 const CUtensorMap& tdqa, const BwdParams& p, cudaStream_t stream) {
   auto kern = bwd_main_kernel<D, C>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, BwdTraits<D>::SMEM);
   if (e != cudaSuccess) return e;
   const unsigned grid = (unsigned)p.nq * (unsigned)(p.B * p.Hkv);
-  kern<<<grid, BwdTraits<D>::THREADS, BwdTraits<D>::SMEM, stream>>>(tq, tk, tv, tdo, tdk, tdv, p);
+  kern<<<grid, BwdTraits<D>::THREADS, BwdTraits<D>::SMEM, stream>>>(tq, tk, tv, tdo, tdk, tdv, tdqa, p);
   return cudaGetLastError();
 }
 
@@ -491,14 +548,14 @@ cudaError_t launch_bwd_prep(const BwdParams& p, cudaStream_t stream) {
 
 cudaError_t launch_bwd_grad(int d, bool causal, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                             const CUtensorMap& tdo, const CUtensorMap& tdk, const CUtensorMap& tdv,
-                            const BwdParams& p, cudaStream_t stream) {
+                            const CUtensorMap& tdqa, const BwdParams& p, cudaStream_t stream) {
   switch (d) {
-    case 64: return causal ? launch_main_t<64, true>(tq, tk, tv, tdo, tdk, tdv, p, stream)
-                           : launch_main_t<64, false>(tq, tk, tv, tdo, tdk, tdv, p, stream);
-    case 96: return causal ? launch_main_t<96, true>(tq, tk, tv, tdo, tdk, tdv, p, stream)
-                           : launch_main_t<96, false>(tq, tk, tv, tdo, tdk, tdv, p, stream);
-    case 128: return causal ? launch_main_t<128, true>(tq, tk, tv, tdo, tdk, tdv, p, stream)
-                            : launch_main_t<128, false>(tq, tk, tv, tdo, tdk, tdv, p, stream);
+    case 64: return causal ? launch_main_t<64, true>(tq, tk, tv, tdo, tdk, tdv, tdqa, p, stream)
+                           : launch_main_t<64, false>(tq, tk, tv, tdo, tdk, tdv, tdqa, p, stream);
+    case 96: return causal ? launch_main_t<96, true>(tq, tk, tv, tdo, tdk, tdv, tdqa, p, stream)
+                           : launch_main_t<96, false>(tq, tk, tv, tdo, tdk, tdv, tdqa, p, stream);
+    case 128: return causal ? launch_main_t<128, true>(tq, tk, tv, tdo, tdk, tdv, tdqa, p, stream)
+                            : launch_main_t<128, false>(tq, tk, tv, tdo, tdk, tdv, tdqa, p, stream);
     default: return cudaErrorInvalidValue;
   }
 }

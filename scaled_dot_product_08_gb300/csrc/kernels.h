@@ -49,7 +49,7 @@ cudaError_t launch_fwd(int d, bool causal, const CUtensorMap& tq, const CUtensor
 cudaError_t launch_bwd_prep(const BwdParams& p, cudaStream_t stream);
 cudaError_t launch_bwd_grad(int d, bool causal, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                             const CUtensorMap& tdo, const CUtensorMap& tdk, const CUtensorMap& tdv,
-                            const BwdParams& p, cudaStream_t stream);
+                            const CUtensorMap& tdqa, const BwdParams& p, cudaStream_t stream);
 cudaError_t launch_bwd_dq(const BwdParams& p, cudaStream_t stream);
 
 }  // namespace sdpa
