@@ -18,16 +18,18 @@
 //               memory with TMA bulk reductions.
 //   bwd_convert dQ accumulator -> bf16 dQ
 //
-// bwd_main warp roles (384 threads = 3 warpgroups):
-//   warps 0-3   compute: S^T -> P^T (written to TMEM as the A operand of the
-//               dV MMA), dP^T -> dS^T (written to shared memory, the A
-//               operand of the dK and dQ MMAs); dK/dV epilogue
-//   warps 4-7   dQ drain: TMEM -> shared memory -> TMA reduce-add
-//   warp  8     TMA producer: K_j, V_j once; Q_i, dO_i, lse2_i, D_i per step
-//   warp  9     MMA issuer (one thread)
-//   warps 10-11 idle
-// setmaxnreg: compute 240, drain 160, producer/MMA 104 registers per thread
-// (128 * (240 + 160 + 104) = 384 * 168, the launch allocation).
+// bwd_main warp roles (512 threads = 4 warpgroups):
+//   warps 0-7   compute, two warpgroups: warpgroup X takes query columns
+//               [64X, 64X+64) of each 128 x 128 tile (keys x queries):
+//               S^T -> P^T (to TMEM, the A operand of the dV MMA) and
+//               dP^T -> dS^T (to shared memory, the A operand of the dK and
+//               dQ MMAs); then the dV (X=0) / dK (X=1) epilogue
+//   warps 8-11  dQ drain: TMEM -> shared memory -> TMA reduce-add
+//   warp  12    TMA producer: K_j, V_j once; Q_i (+ -lse2_i, -D_i), dO_i
+//   warp  13    MMA issuer (one elected lane issues)
+//   warps 14-15 idle
+// setmaxnreg: compute 144, drain 120, producer/MMA 104 registers per thread
+// (128 * (144 + 144 + 120 + 104) = 512 * 128, the launch allocation).
 // Tensor memory: [0,128) S^T / P^T, [128,256) dP^T / dQ_i, [256,256+d) dK,
 // [384,384+d) dV.  All score tiles are 128 x 128 (keys x queries).
 #include <cmath>
@@ -103,16 +105,20 @@ struct BwdTraits {
   static constexpr int TILE_BYTES = NB * BLOCK_BYTES;  // one [128 rows x d] bf16 tile
   static constexpr int KSTEPS = D / 16;
   static constexpr int DS_BYTES = 2 * BLOCK_BYTES;     // dS^T: 128 keys x 128 queries, any d
-  static constexpr int VEC_BYTES = 1024;               // lse2[128] + D[128]
-  static constexpr int NBAR = 1 + 2 + 2 + 1 + 1 + 1 + 1 + 1 + 1 + 1 + 1 + 1;
+  static constexpr int VEC_BYTES = 1024;               // -lse2[128] + -D[128]
+  static constexpr int NBAR = 32;
   // K, V, Q[2], dO[2], dS^T, then vectors, barriers, misc
   static constexpr int TILES_BYTES = 6 * TILE_BYTES + DS_BYTES;
   static constexpr int SMEM = TILES_BYTES + 2 * VEC_BYTES + NBAR * 8 + 16;
-  static constexpr int THREADS = 384;
+  static constexpr int THREADS = 512;
+  // dQ_i leaves TMEM in two halves of head-dim columns: [0, 64) and [64, D).
+  static constexpr int DQ_B = D - 64;                  // 0 when D == 64
+  // ... and is staged in the dO stage (TILE_BYTES) in two rounds of columns.
+  static constexpr int R0 = (D == 64) ? 32 : 64;       // columns [0, R0) in round 0, [R0, D) in round 1
 };
 
 template <int D, bool CAUSAL>
-__global__ void __launch_bounds__(384, 1)
+__global__ void __launch_bounds__(512, 1)
     bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
                     const __grid_constant__ CUtensorMap tmdK, const __grid_constant__ CUtensorMap tmdV,
@@ -131,20 +137,23 @@ __global__ void __launch_bounds__(384, 1)
   const uint32_t sQ = sV + T::TILE_BYTES;            // [2]
   const uint32_t sdO = sQ + 2 * T::TILE_BYTES;       // [2]
   const uint32_t sDS = sdO + 2 * T::TILE_BYTES;      // dS^T, bf16, [keys][queries]
-  const uint32_t sVec = sDS + T::DS_BYTES;           // [2] x {lse2[128], D[128]}
+  const uint32_t sVec = sDS + T::DS_BYTES;           // [2] x {-lse2[128], -D[128]}
   const uint32_t sBar = sVec + 2 * T::VEC_BYTES;
-  const uint32_t bKV = sBar;
-  const uint32_t bQf = bKV + 8;     // qdo_full[2]
-  const uint32_t bQe = bQf + 16;    // qdo_empty[2]
-  const uint32_t bS = bQe + 16;     // S^T ready
-  const uint32_t bP = bS + 8;       // P^T in TMEM (128 arrivals)
-  const uint32_t bDs = bP + 8;      // dS^T in smem (128 arrivals)
-  const uint32_t bDqf = bDs + 8;    // dQ_i in TMEM
-  const uint32_t bDqe = bDqf + 8;   // dQ_i drained (128 arrivals)
-  const uint32_t bFin = bDqe + 8;   // every MMA done
+  const uint32_t bKV = sBar;          // K_j, V_j loaded
+  const uint32_t bQf = bKV + 8;       // [2] Q_i + vectors loaded
+  const uint32_t bQe = bQf + 16;      // [2] Q stage free (after dK_i)
+  const uint32_t bDf = bQe + 16;      // [2] dO_i loaded
+  const uint32_t bDe = bDf + 16;      // [2] dO stage free (after dQ_i left through it)
+  const uint32_t bS = bDe + 16;       // S^T ready
+  const uint32_t bP = bS + 8;         // P^T in TMEM (256 arrivals)
+  const uint32_t bDp = bP + 8;        // [2] dP^T query half ready
+  const uint32_t bDs = bDp + 16;      // dS^T in smem (256 arrivals)
+  const uint32_t bDq = bDs + 8;       // [2] dQ_i head-dim half ready
+  const uint32_t bDqe = bDq + 16;     // [2] dQ half copied out of TMEM (128 arrivals)
+  const uint32_t bStg = bDqe + 16;    // [2] dQ round staged in smem (128 arrivals)
+  const uint32_t bSfree = bStg + 16;  // dO stage free again after round 0 (1 arrival)
+  const uint32_t bFin = bSfree + 8;   // every MMA done
   const uint32_t bDrain = bFin + 8;
-  const uint32_t bDp = bDrain + 8;  // dP^T ready
-  const uint32_t bStg = bDp + 8;    // dQ_i staged in shared memory (128 arrivals)
   uint8_t* const misc = smem_raw + (sBar - base) + 8 * T::NBAR;
   uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(misc);
   volatile int* const abort_flag = reinterpret_cast<volatile int*>(misc + 4);
@@ -164,20 +173,23 @@ __global__ void __launch_bounds__(384, 1)
     for (int s = 0; s < 2; ++s) {
       mbar_init(bQf + 8u * s, 1);
       mbar_init(bQe + 8u * s, 1);
+      mbar_init(bDf + 8u * s, 1);
+      mbar_init(bDe + 8u * s, 1);
+      mbar_init(bDp + 8u * s, 1);
+      mbar_init(bDq + 8u * s, 1);
+      mbar_init(bDqe + 8u * s, 128);
+      mbar_init(bStg + 8u * s, 128);
     }
     mbar_init(bS, 1);
-    mbar_init(bDp, 1);
-    mbar_init(bStg, 128);
-    mbar_init(bP, 128);
-    mbar_init(bDs, 128);
-    mbar_init(bDqf, 1);
-    mbar_init(bDqe, 128);
+    mbar_init(bP, 256);
+    mbar_init(bDs, 256);
+    mbar_init(bSfree, 1);
     mbar_init(bFin, 1);
     mbar_init(bDrain, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == 9) {
+  if (warp == 13) {
     tmem_alloc(smem_u32(tmem_slot), 512);
     tmem_relinquish();
   }
@@ -187,49 +199,49 @@ __global__ void __launch_bounds__(384, 1)
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
   const WaitCtx wc{abort_flag, p.status, p.limit_ns, p.info};
 
-  if (warp < 4) {
-    setmaxnreg_inc<240>();
-    reg_split_sync(384);
-    // -------------------------------------------------------------- compute
-    const int r = threadIdx.x;  // key row within the tile == TMEM lane
-    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
-    const uint32_t tS = tmem + lane_off, tdP = tmem + 128 + lane_off;
+  if (warp < 8) {
+    setmaxnreg_inc<144>();
+    reg_split_sync(512);
+    // ------------------------------------------------------------ compute
+    // Warpgroup X handles query columns [64X, 64X + 64) of every score tile
+    // for all 128 key rows (thread = key row = TMEM lane).  P^T and dS^T are
+    // element-wise, so the two halves never exchange data.
+    const int X = warp >> 2;
+    const int r = threadIdx.x & 127;
+    const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+    const uint32_t tS = tmem + 64 * X + lane_off;           // S^T columns of this half
+    const uint32_t tP = tmem + 64 * X + lane_off;           // P^T (bf16 pairs), first 32 of them
+    const uint32_t tdP = tmem + 128 + 64 * X + lane_off;    // dP^T columns of this half
     const float c = p.scale_log2;
     const float2 c2 = make_float2(c, c);
     bool ok = true;
     for (int it = 0; it < total; ++it) {
       const int i = i0 + it % ni;
-      const float* vl = vec_g + (it & 1) * (T::VEC_BYTES / 4);  // -lse2[128], then -D[128]
-      // The lse2 / D vectors come from the bulk copy of this step: observe
-      // its barrier (already complete by now) before reading them.
+      const float* vl = vec_g + (it & 1) * (T::VEC_BYTES / 4) + 64 * X;  // -lse2 of this half; -D at +128
+      // The vectors come from the bulk copy of this step: observe its barrier
+      // (complete by now) before reading them.
       ok = __all_sync(0xffffffffu, wait_bounded(wc, bQf + 8u * (it & 1), (it >> 1) & 1, wait_site(0x11, it)) &&
                                        wait_bounded(wc, bS, it & 1, wait_site(0x12, it)));
       if (!ok) break;
       tc_fence_after();
-      float x[128];
+      float x[64];
       {
-        uint32_t ra[32], rb[32], rc[32], rd[32];
+        uint32_t ra[32], rb[32];
         tmem_ld32(tS + 0, ra);
         tmem_ld32(tS + 32, rb);
-        tmem_ld32(tS + 64, rc);
-        tmem_ld32(tS + 96, rd);
         tmem_wait_ld();
         reg_fence(ra);
         reg_fence(rb);
-        reg_fence(rc);
-        reg_fence(rd);
 #pragma unroll
         for (int e = 0; e < 32; ++e) {
           x[e] = __uint_as_float(ra[e]);
           x[32 + e] = __uint_as_float(rb[e]);
-          x[64 + e] = __uint_as_float(rc[e]);
-          x[96 + e] = __uint_as_float(rd[e]);
         }
       }
       // P^T[r][q] = exp2(S^T * scale * log2e - lse2[q]); masked (key > query
       // on the diagonal tile) entries are exactly 0.
 #pragma unroll
-      for (int q4 = 0; q4 < 32; ++q4) {
+      for (int q4 = 0; q4 < 16; ++q4) {
         const float4 l4 = *reinterpret_cast<const float4*>(vl + 4 * q4);
         const float2 t0 = ffma2(make_float2(x[4 * q4 + 0], x[4 * q4 + 1]), c2, make_float2(l4.x, l4.y));
         const float2 t1 = ffma2(make_float2(x[4 * q4 + 2], x[4 * q4 + 3]), c2, make_float2(l4.z, l4.w));
@@ -240,168 +252,180 @@ __global__ void __launch_bounds__(384, 1)
       }
       if (CAUSAL && i == j) {
 #pragma unroll
-        for (int q = 0; q < 128; ++q)
-          if (r > q) x[q] = 0.f;
+        for (int q = 0; q < 64; ++q)
+          if (r > 64 * X + q) x[q] = 0.f;
       }
-      // P^T as bf16 pairs: written to TMEM for the dV MMA and kept in
-      // registers for dS.
-      uint32_t pa[32], pb[32];
+      uint32_t pk[32];  // P^T as bf16 pairs: to TMEM for the dV MMA, kept for dS
 #pragma unroll
-      for (int e = 0; e < 32; ++e) {
-        pa[e] = pack_bf16(x[2 * e], x[2 * e + 1]);
-        pb[e] = pack_bf16(x[64 + 2 * e], x[64 + 2 * e + 1]);
-      }
-      tmem_st32(tS, pa);
-      tmem_st32(tS + 32, pb);
+      for (int e = 0; e < 32; ++e) pk[e] = pack_bf16(x[2 * e], x[2 * e + 1]);
+      tmem_st32(tP, pk);
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(bP);
-      // dS^T[r][q] = P^T[r][q] * (dP^T[r][q] - D[q]) -> bf16 -> smem (128-byte
-      // swizzled rows: block q/64, 16-byte chunk (q%64)/8).  The softmax scale
-      // is applied later, to dK in its epilogue and to dQ in the drain.
-      ok = __all_sync(0xffffffffu, wait_bounded(wc, bDp, it & 1, wait_site(0x14, it)));
+      // dS^T[r][q] = P^T[r][q] * (dP^T[r][q] - D[q]) -> bf16 -> smem block X
+      // (128-byte swizzled rows, 16-byte chunk q/8).  The softmax scale is
+      // applied later, to dK in its epilogue and to dQ in the drain.
+      ok = __all_sync(0xffffffffu, wait_bounded(wc, bDp + 8u * X, it & 1, wait_site(0x14, it)));
       if (!ok) break;
       tc_fence_after();
-      uint32_t g0[32], g1[32], g2[32], g3[32];
+      uint32_t g0[32], g1[32];
       tmem_ld32(tdP + 0, g0);
       tmem_ld32(tdP + 32, g1);
-      tmem_ld32(tdP + 64, g2);
-      tmem_ld32(tdP + 96, g3);
       tmem_wait_ld();
       reg_fence(g0);
       reg_fence(g1);
-      reg_fence(g2);
-      reg_fence(g3);
+      const float4* Dv = reinterpret_cast<const float4*>(vl + 128);
 #pragma unroll
-      for (int cc = 0; cc < 4; ++cc) {
-        const uint32_t* g = cc == 0 ? g0 : cc == 1 ? g1 : cc == 2 ? g2 : g3;
-        const uint32_t* pk = (cc < 2) ? pa : pb;
-        const float4* Dv = reinterpret_cast<const float4*>(vl + 128 + cc * 32);
+      for (int q8 = 0; q8 < 8; ++q8) {
+        uint32_t w[4];
+        const float4 da = Dv[2 * q8], db = Dv[2 * q8 + 1];
+        const float2 dd[4] = {make_float2(da.x, da.y), make_float2(da.z, da.w), make_float2(db.x, db.y),
+                              make_float2(db.z, db.w)};
 #pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
-          uint32_t w[4];
-          const float4 da = Dv[2 * q4], db = Dv[2 * q4 + 1];
-          const float2 dd[4] = {make_float2(da.x, da.y), make_float2(da.z, da.w), make_float2(db.x, db.y),
-                                make_float2(db.z, db.w)};
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int q = q4 * 8 + 2 * e;  // column within this 32-column chunk
-            const uint32_t pp = pk[((cc & 1) * 32 + q) >> 1];
-            const float2 pf = make_float2(__uint_as_float(pp << 16), __uint_as_float(pp & 0xffff0000u));
-            const float2 dpd = fadd2(make_float2(__uint_as_float(g[q]), __uint_as_float(g[q + 1])), dd[e]);
-            const float2 ds = fmul2(pf, dpd);
-            w[e] = pack_bf16(ds.x, ds.y);
-          }
-          st_shared_v4(sDS + (cc >> 1) * T::BLOCK_BYTES + sw128_offset(r, (cc & 1) * 4 + q4), w[0], w[1], w[2],
-                       w[3]);
+        for (int e = 0; e < 4; ++e) {
+          const int q = q8 * 8 + 2 * e;  // column within the half
+          const uint32_t gx = (q < 32) ? g0[q] : g1[q - 32];
+          const uint32_t gy = (q < 32) ? g0[q + 1] : g1[q - 31];
+          const uint32_t pp = pk[q >> 1];
+          const float2 pf = make_float2(__uint_as_float(pp << 16), __uint_as_float(pp & 0xffff0000u));
+          const float2 ds = fmul2(pf, fadd2(make_float2(__uint_as_float(gx), __uint_as_float(gy)), dd[e]));
+          w[e] = pack_bf16(ds.x, ds.y);
         }
+        st_shared_v4(sDS + X * T::BLOCK_BYTES + sw128_offset(r, q8), w[0], w[1], w[2], w[3]);
       }
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(bDs);
     }
     // ------------------------------------------------------------ dK / dV out
+    // Warpgroup 0 writes dV (staged in the dS^T tile), warpgroup 1 writes dK
+    // = scale * (dS^T Q) (staged in the K tile); both are free once every MMA
+    // has completed.
     if (ok) ok = __all_sync(0xffffffffu, wait_bounded(wc, bFin, 0, wait_site(0x13, total)));
-    const uint32_t stage_dv = sDS, stage_dk = sK;  // both free once every MMA is done
+    const uint32_t stage = X ? sK : sDS;
     if (ok) {
       tc_fence_after();
+      const uint32_t src = tmem + (X ? 256u : 384u) + lane_off;
+      const float2 f2 = X ? make_float2(p.scale, p.scale) : make_float2(1.f, 1.f);
 #pragma unroll
-      for (int which = 0; which < 2; ++which) {
-        const uint32_t src = tmem + (which ? 256u : 384u) + lane_off;
-        const uint32_t dst = which ? stage_dk : stage_dv;
-        const float2 f2 = which ? make_float2(p.scale, p.scale) : make_float2(1.f, 1.f);  // dK = scale dS^T Q
+      for (int cc = 0; cc < D / 32; ++cc) {
+        uint32_t o[32];
+        tmem_ld32(src + cc * 32, o);
+        tmem_wait_ld();
+        reg_fence(o);
+        const int blk = (cc * 32) / 64, ch0 = ((cc * 32) % 64) / 8;
 #pragma unroll
-        for (int cc = 0; cc < D / 32; ++cc) {
-          uint32_t o[32];
-          tmem_ld32(src + cc * 32, o);
-          tmem_wait_ld();
-          reg_fence(o);
-          const int blk = (cc * 32) / 64, ch0 = ((cc * 32) % 64) / 8;
+        for (int q4 = 0; q4 < 4; ++q4) {
+          uint32_t w[4];
 #pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4) {
-            uint32_t w[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const float2 t = fmul2(make_float2(__uint_as_float(o[q4 * 8 + 2 * e]),
-                                                 __uint_as_float(o[q4 * 8 + 2 * e + 1])), f2);
-              w[e] = pack_bf16(t.x, t.y);
-            }
-            st_shared_v4(dst + blk * T::BLOCK_BYTES + sw128_offset(r, ch0 + q4), w[0], w[1], w[2], w[3]);
+          for (int e = 0; e < 4; ++e) {
+            const float2 t = fmul2(make_float2(__uint_as_float(o[q4 * 8 + 2 * e]),
+                                               __uint_as_float(o[q4 * 8 + 2 * e + 1])), f2);
+            w[e] = pack_bf16(t.x, t.y);
           }
+          st_shared_v4(stage + blk * T::BLOCK_BYTES + sw128_offset(r, ch0 + q4), w[0], w[1], w[2], w[3]);
         }
       }
       fence_proxy_async_smem();
     }
-    named_bar_sync(1, 128);
+    named_bar_sync(1 + X, 128);
     if (ok && r == 0) {
-      for (int cb = 0; cb < T::NB; ++cb) {
-        tma_store_3d(&tmdV, stage_dv + cb * T::BLOCK_BYTES, cb * 64, j * 128, bhk);
-        tma_store_3d(&tmdK, stage_dk + cb * T::BLOCK_BYTES, cb * 64, j * 128, bhk);
-      }
+      for (int cb = 0; cb < T::NB; ++cb)
+        tma_store_3d(X ? &tmdK : &tmdV, stage + cb * T::BLOCK_BYTES, cb * 64, j * 128, bhk);
       bulk_commit();
       bulk_wait_read_all();
     }
-    setmaxnreg_dec<168>();
-  } else if (warp < 8) {
-    setmaxnreg_dec<160>();
-    reg_split_sync(384);
-    // -------------------------------------------------------------- dQ drain
-    const int q = threadIdx.x - 128;  // query row within the tile == TMEM lane
-    const uint32_t tQ = tmem + 128 + ((uint32_t)((warp - 4) * 32) << 16);
+    setmaxnreg_dec<128>();
+  } else if (warp < 12) {
+    setmaxnreg_dec<120>();
+    reg_split_sync(512);
+    // ------------------------------------------------------------ dQ drain
+    // dQ_i (fp32, scale applied) leaves TMEM in two head-dim halves and goes
+    // to the accumulator by TMA reductions from the step's dO stage (idle
+    // once dQ_i is final), in two rounds of columns; then the dO stage goes
+    // back to the producer.
+    const int q = threadIdx.x - 256;  // query row within the tile == TMEM lane
+    const uint32_t tQ = tmem + 128 + ((uint32_t)((warp - 8) * 32) << 16);
     const float2 sc2 = make_float2(p.scale, p.scale);  // dQ = scale dS K
-    // dQ_i goes out through the step's Q / dO shared-memory stage, which is
-    // idle once dQ_i is final (every MMA that read it has completed): fp32,
-    // boxes of 32 columns x 128 rows with the 128-byte swizzle, added into
-    // the accumulator by TMA reductions.  The stage is then handed back to
-    // the producer (qdo_empty).
-    constexpr int NBOX = D / 32;
     for (int it = 0; it < total; ++it) {
       const int h = hk * p.G + it / ni, i = i0 + it % ni;
       const int st = it & 1;
-      if (!__all_sync(0xffffffffu, wait_bounded(wc, bDqf, it & 1, wait_site(0x21, it)))) break;
+      const int bh = b * p.H + h;
+      const uint32_t stg = sdO + st * T::TILE_BYTES;
+      // half A: head-dim columns [0, 64)
+      if (!__all_sync(0xffffffffu, wait_bounded(wc, bDq, it & 1, wait_site(0x21, it)))) break;
       tc_fence_after();
-      uint32_t g[NBOX][32];
-#pragma unroll
-      for (int cc = 0; cc < NBOX; ++cc) tmem_ld32(tQ + cc * 32, g[cc]);
+      uint32_t ga[32], gb[32];
+      tmem_ld32(tQ + 0, ga);
+      tmem_ld32(tQ + 32, gb);
       tmem_wait_ld();
-#pragma unroll
-      for (int cc = 0; cc < NBOX; ++cc) reg_fence(g[cc]);
+      reg_fence(ga);
+      reg_fence(gb);
       tc_fence_before();
-      mbar_arrive(bDqe);  // TMEM columns free for the next dP^T
-#pragma unroll
-      for (int cc = 0; cc < NBOX; ++cc) {
-        const uint32_t box = (cc < T::NB) ? sQ + st * T::TILE_BYTES + cc * T::BLOCK_BYTES
-                                          : sdO + st * T::TILE_BYTES + (cc - T::NB) * T::BLOCK_BYTES;
+      mbar_arrive(bDqe);
+      // round 0: columns [0, R0) (32 or 64)
+      auto stage_box = [&](const uint32_t (&gg)[32], uint32_t box) {
 #pragma unroll
         for (int c8 = 0; c8 < 8; ++c8) {
-          const float2 a0 = fmul2(make_float2(__uint_as_float(g[cc][4 * c8]), __uint_as_float(g[cc][4 * c8 + 1])), sc2);
-          const float2 a1 = fmul2(make_float2(__uint_as_float(g[cc][4 * c8 + 2]), __uint_as_float(g[cc][4 * c8 + 3])), sc2);
+          const float2 a0 = fmul2(make_float2(__uint_as_float(gg[4 * c8]), __uint_as_float(gg[4 * c8 + 1])), sc2);
+          const float2 a1 = fmul2(make_float2(__uint_as_float(gg[4 * c8 + 2]), __uint_as_float(gg[4 * c8 + 3])), sc2);
           st_shared_v4(box + sw128_offset(q, c8), __float_as_uint(a0.x), __float_as_uint(a0.y), __float_as_uint(a1.x),
                        __float_as_uint(a1.y));
         }
-      }
+      };
+      stage_box(ga, stg);
+      if (T::R0 == 64) stage_box(gb, stg + T::BLOCK_BYTES);
       fence_proxy_async_smem();
       mbar_arrive(bStg);
-      // One thread waits (bounded) for all 128 to have staged, then reduces.
-      if (q == 0 && wait_bounded(wc, bStg, it & 1, wait_site(0x22, it))) {
-        const int bh = b * p.H + h;
-#pragma unroll
-        for (int cc = 0; cc < NBOX; ++cc) {
-          const uint32_t box = (cc < T::NB) ? sQ + st * T::TILE_BYTES + cc * T::BLOCK_BYTES
-                                            : sdO + st * T::TILE_BYTES + (cc - T::NB) * T::BLOCK_BYTES;
-          tma_reduce_add_3d(&tmdQacc, box, cc * 32, i * 128, bh);
+      bool ok0 = true;
+      if (q == 0) {
+        ok0 = wait_bounded(wc, bStg, it & 1, wait_site(0x22, it));
+        if (ok0) {
+          tma_reduce_add_3d(&tmdQacc, stg, 0, i * 128, bh);
+          if (T::R0 == 64) tma_reduce_add_3d(&tmdQacc, stg + T::BLOCK_BYTES, 32, i * 128, bh);
+          bulk_commit();
+          bulk_wait_read_all();
+          mbar_arrive(bSfree);
         }
+      }
+      // half B (D > 64): head-dim columns [64, D)
+      uint32_t gc[32], gd[32];
+      if (T::DQ_B > 0) {
+        if (!__all_sync(0xffffffffu, wait_bounded(wc, bDq + 8u, it & 1, wait_site(0x23, it)))) break;
+        tc_fence_after();
+        tmem_ld32(tQ + 64, gc);
+        if (T::DQ_B == 64) tmem_ld32(tQ + 96, gd);
+        tmem_wait_ld();
+        reg_fence(gc);
+        if (T::DQ_B == 64) reg_fence(gd);
+        tc_fence_before();
+        mbar_arrive(bDqe + 8u);
+      }
+      // round 1: columns [R0, D), after the round-0 reduction has read the stage
+      if (!__all_sync(0xffffffffu, wait_bounded(wc, bSfree, it & 1, wait_site(0x24, it)))) break;
+      if (T::DQ_B > 0) {
+        stage_box(gc, stg);
+        if (T::DQ_B == 64) stage_box(gd, stg + T::BLOCK_BYTES);
+      } else {
+        stage_box(gb, stg);
+      }
+      fence_proxy_async_smem();
+      mbar_arrive(bStg + 8u);
+      if (q == 0 && wait_bounded(wc, bStg + 8u, it & 1, wait_site(0x25, it))) {
+        tma_reduce_add_3d(&tmdQacc, stg, T::R0, i * 128, bh);
+        if (D - T::R0 == 64) tma_reduce_add_3d(&tmdQacc, stg + T::BLOCK_BYTES, T::R0 + 32, i * 128, bh);
         bulk_commit();
         bulk_wait_read_all();
-        mbar_arrive(bQe + 8u * st);
+        mbar_arrive(bDe + 8u * st);
       }
+      (void)ok0;
     }
     if (q == 0) bulk_wait_all();  // every reduction has landed before the CTA exits
-    setmaxnreg_inc<168>();
+    setmaxnreg_inc<128>();
   } else {
     setmaxnreg_dec<104>();
-    reg_split_sync(384);
-    if (warp == 8) {
+    reg_split_sync(512);
+    if (warp == 12) {
       // ------------------------------------------------------------ producer
       if (lane == 0) {
         tma_prefetch_desc(&tmQ);
@@ -411,109 +435,144 @@ __global__ void __launch_bounds__(384, 1)
           tma_load_3d(sK + cb * T::BLOCK_BYTES, &tmK, bKV, cb * 64, j * 128, bhk);
           tma_load_3d(sV + cb * T::BLOCK_BYTES, &tmV, bKV, cb * 64, j * 128, bhk);
         }
-        int issued = 0;
+        int issued_q = 0, issued_d = 0;
         for (int it = 0; it < total; ++it) {
           const int st = it & 1, rd = it >> 1;
-          if (rd > 0 && !wait_bounded(wc, bQe + 8u * st, (rd - 1) & 1, wait_site(0x31, it))) break;
           const int h = hk * p.G + it / ni, i = i0 + it % ni;
           const int bh = b * p.H + h;
-          const uint32_t bar = bQf + 8u * st;
-          mbar_expect_tx(bar, 2 * T::TILE_BYTES + T::VEC_BYTES);
-          for (int cb = 0; cb < T::NB; ++cb) {
-            tma_load_3d(sQ + st * T::TILE_BYTES + cb * T::BLOCK_BYTES, &tmQ, bar, cb * 64, i * 128, bh);
-            tma_load_3d(sdO + st * T::TILE_BYTES + cb * T::BLOCK_BYTES, &tmdO, bar, cb * 64, i * 128, bh);
-          }
+          if (rd > 0 && !wait_bounded(wc, bQe + 8u * st, (rd - 1) & 1, wait_site(0x31, it))) break;
+          const uint32_t barq = bQf + 8u * st;
+          mbar_expect_tx(barq, T::TILE_BYTES + T::VEC_BYTES);
+          for (int cb = 0; cb < T::NB; ++cb)
+            tma_load_3d(sQ + st * T::TILE_BYTES + cb * T::BLOCK_BYTES, &tmQ, barq, cb * 64, i * 128, bh);
           const size_t voff = (size_t)bh * p.Npad + (size_t)i * 128;
-          bulk_load(sVec + st * T::VEC_BYTES, p.lse2 + voff, 512, bar);
-          bulk_load(sVec + st * T::VEC_BYTES + 512, p.dvec + voff, 512, bar);
-          issued = it + 1;
+          bulk_load(sVec + st * T::VEC_BYTES, p.lse2 + voff, 512, barq);
+          bulk_load(sVec + st * T::VEC_BYTES + 512, p.dvec + voff, 512, barq);
+          issued_q = it + 1;
+          if (rd > 0 && !wait_bounded(wc, bDe + 8u * st, (rd - 1) & 1, wait_site(0x32, it))) break;
+          const uint32_t bard = bDf + 8u * st;
+          mbar_expect_tx(bard, T::TILE_BYTES);
+          for (int cb = 0; cb < T::NB; ++cb)
+            tma_load_3d(sdO + st * T::TILE_BYTES + cb * T::BLOCK_BYTES, &tmdO, bard, cb * 64, i * 128, bh);
+          issued_d = it + 1;
         }
         // Every copy issued above has landed before the CTA may exit.
         wait_drain(bKV, 0, p.limit_ns);
-        for (int st = 0; st < 2 && st < issued; ++st) {
-          const int last = ((issued - 1 - st) / 2) * 2 + st;
-          wait_drain(bQf + 8u * st, (last >> 1) & 1, p.limit_ns);
+        for (int st = 0; st < 2; ++st) {
+          if (st < issued_q) wait_drain(bQf + 8u * st, ((((issued_q - 1 - st) / 2) * 2 + st) >> 1) & 1, p.limit_ns);
+          if (st < issued_d) wait_drain(bDf + 8u * st, ((((issued_d - 1 - st) / 2) * 2 + st) >> 1) & 1, p.limit_ns);
         }
       }
       __syncwarp();
-    } else if (warp == 9) {
+    } else if (warp == 13) {
       // ------------------------------------------------------------ MMA issuer
-      if (lane == 0) {
-        constexpr uint32_t I_SS = idesc_bf16_f32(128, 128, false, false);  // S^T, dP^T
-        constexpr uint32_t I_TB = idesc_bf16_f32(128, D, false, true);     // dV (A in TMEM), dK
-        constexpr uint32_t I_MM = idesc_bf16_f32(128, D, true, true);      // dQ (A = dS, MN-major)
+      // The whole warp runs the issue loop, so descriptor arithmetic stays
+      // warp-uniform; one elected lane issues each tcgen05 instruction.
+      // Descriptors are built once and moved by constant offsets.
+      {
+        const uint32_t leader = elect_one();
+        constexpr uint32_t I_SS = idesc_bf16_f32(128, 128, false, false);   // S^T (K-major x K-major)
+        constexpr uint32_t I_DP = idesc_bf16_f32(128, 64, false, false);    // dP^T query half
+        constexpr uint32_t I_TB = idesc_bf16_f32(128, D, false, true);      // dV (A in TMEM), dK
+        constexpr uint32_t I_QA = idesc_bf16_f32(128, 64, true, true);      // dQ head-dim half A
+        constexpr uint32_t I_QB = idesc_bf16_f32(128, (D > 64 ? D - 64 : 64), true, true);  // half B
         const uint32_t tS = tmem, tdP = tmem + 128, tdK = tmem + 256, tdV = tmem + 384;
-        // D[128 x 128] = A[128 x d] * B[128 x d]^T with both K-major tiles.
-        auto mma_kk = [&](uint32_t dst, uint32_t a_tile, uint32_t b_tile) {
+        const uint64_t dKk = sdesc_sw128(sK, 16, 1024);                  // K as K-major A (S^T)
+        const uint64_t dVk = sdesc_sw128(sV, 16, 1024);                  // V as K-major A (dP^T)
+        const uint64_t dKmn = sdesc_sw128(sK, T::BLOCK_BYTES, 1024);     // K as MN-major B (dQ)
+        const uint64_t dQk0 = sdesc_sw128(sQ, 16, 1024);                 // Q stage 0, K-major B (S^T)
+        const uint64_t dQmn0 = sdesc_sw128(sQ, T::BLOCK_BYTES, 1024);    // Q stage 0, MN-major B (dK)
+        const uint64_t dOk0 = sdesc_sw128(sdO, 16, 1024);                // dO stage 0, K-major B (dP^T)
+        const uint64_t dOmn0 = sdesc_sw128(sdO, T::BLOCK_BYTES, 1024);   // dO stage 0, MN-major B (dV)
+        const uint64_t dSk = sdesc_sw128(sDS, 16, 1024);                 // dS^T as K-major A (dK)
+        const uint64_t dSmn = sdesc_sw128(sDS, T::BLOCK_BYTES, 1024);    // dS as MN-major A (dQ)
+        // D[128 x N] = A[128 x d] * B[N x d]^T with both K-major tiles.
+        auto mma_kk = [&](uint32_t dst, uint64_t ad, uint64_t bd, uint32_t idesc) {
 #pragma unroll
           for (int kk = 0; kk < T::KSTEPS; ++kk) {
             const uint32_t off = (kk >> 2) * T::BLOCK_BYTES + (kk & 3) * 32;
-            mma_ss(dst, sdesc_sw128(a_tile + off, 16, 1024), sdesc_sw128(b_tile + off, 16, 1024), I_SS, kk > 0);
+            mma_ss_p(leader, dst, sdesc_add(ad, off), sdesc_add(bd, off), idesc, kk > 0);
           }
         };
-        // Issue order per step i (stage st): dV(i), S^T(i+1), dK(i), dQ(i),
-        // dP^T(i+1).  S^T(i+1) overwrites P^T(i) in TMEM only after dV(i),
-        // which was issued first (MMAs from one thread run in order), so
-        // the softmax of step i+1 overlaps the dK / dQ MMAs of step i.
-        bool ok = wait_bounded(wc, bKV, 0, wait_site(0x41, 0)) &&
-                  wait_bounded(wc, bQf, 0, wait_site(0x42, 0));
+        auto wait_all = [&](uint32_t bar, uint32_t parity, int site) {
+          return __all_sync(0xffffffffu, wait_bounded(wc, bar, parity, site));
+        };
+        // Issue order per step i: dV(i), S^T(i+1), dK(i), dQ(i) [two halves],
+        // dP^T(i+1) [two query halves].  S^T(i+1) overwrites P^T(i) in TMEM
+        // only after dV(i), issued first (MMAs from one thread run in order).
+        bool ok = wait_all(bKV, 0, wait_site(0x41, 0)) && wait_all(bQf, 0, wait_site(0x42, 0)) &&
+                  wait_all(bDf, 0, wait_site(0x47, 0));
         if (ok) {
           tc_fence_after();
-          mma_kk(tS, sK, sQ);  // S^T_0 = K Q_0^T
-          mma_commit(bS);
-          mma_kk(tdP, sV, sdO);  // dP^T_0 = V dO_0^T
-          mma_commit(bDp);
+          mma_kk(tS, dKk, dQk0, I_SS);  // S^T_0 = K Q_0^T
+          mma_commit_p(leader, bS);
+          mma_kk(tdP, dVk, dOk0, I_DP);  // dP^T_0, queries 0-63
+          mma_commit_p(leader, bDp);
+          mma_kk(tdP + 64, dVk, sdesc_add(dOk0, 8192), I_DP);  // queries 64-127 (row 64 of each block)
+          mma_commit_p(leader, bDp + 8u);
         }
         for (int it = 0; it < total && ok; ++it) {
           const int st = it & 1, sn = st ^ 1;
           const bool nx = it + 1 < total;
-          const uint32_t q_t = sQ + st * T::TILE_BYTES, do_t = sdO + st * T::TILE_BYTES;
-          const uint32_t q_n = sQ + sn * T::TILE_BYTES, do_n = sdO + sn * T::TILE_BYTES;
-          if (!(ok = wait_bounded(wc, bP, it & 1, wait_site(0x44, it)))) break;
+          const uint32_t so = st * T::TILE_BYTES, sno = sn * T::TILE_BYTES;
+          if (!(ok = wait_all(bP, it & 1, wait_site(0x44, it)))) break;
           tc_fence_after();
-          // dV += P^T dO_i: A = P^T (TMEM, bf16 pairs), B = dO_i (MN-major)
+          // dV += P^T dO_i: A = P^T in TMEM (queries 0-63 at columns 0-31,
+          // 64-127 at columns 64-95), B = dO_i (MN-major)
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)
-            mma_ts(tdV, tS + kk * 8, sdesc_sw128(do_t + kk * 2048, T::BLOCK_BYTES, 1024), I_TB,
-                   (it > 0 || kk > 0) ? 1u : 0u);
+            mma_ts_p(leader, tdV, tS + (kk < 4 ? kk * 8 : 64 + (kk - 4) * 8), sdesc_add(dOmn0, so + kk * 2048), I_TB,
+                     (it > 0 || kk > 0) ? 1u : 0u);
           if (nx) {
-            if (!(ok = wait_bounded(wc, bQf + 8u * sn, ((it + 1) >> 1) & 1, wait_site(0x46, it)))) break;
+            if (!(ok = wait_all(bQf + 8u * sn, ((it + 1) >> 1) & 1, wait_site(0x46, it)))) break;
             tc_fence_after();
-            mma_kk(tS, sK, q_n);  // S^T_{i+1}
-            mma_commit(bS);
+            mma_kk(tS, dKk, sdesc_add(dQk0, sno), I_SS);  // S^T_{i+1}
+            mma_commit_p(leader, bS);
           }
-          if (!(ok = wait_bounded(wc, bDs, it & 1, wait_site(0x45, it)))) break;
+          if (!(ok = wait_all(bDs, it & 1, wait_site(0x45, it)))) break;
           tc_fence_after();
           // dK += dS^T Q_i: A = dS^T (K-major over queries), B = Q_i (MN-major)
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)
-            mma_ss(tdK, sdesc_sw128(sDS + (kk >> 2) * T::BLOCK_BYTES + (kk & 3) * 32, 16, 1024),
-                   sdesc_sw128(q_t + kk * 2048, T::BLOCK_BYTES, 1024), I_TB, (it > 0 || kk > 0) ? 1u : 0u);
-          // dQ_i = dS K_j: A = dS (queries contiguous: MN-major), B = K_j (MN-major)
+            mma_ss_p(leader, tdK, sdesc_add(dSk, (kk >> 2) * T::BLOCK_BYTES + (kk & 3) * 32),
+                     sdesc_add(dQmn0, so + kk * 2048), I_TB, (it > 0 || kk > 0) ? 1u : 0u);
+          mma_commit_p(leader, bQe + 8u * st);  // Q_i (and its vectors) no longer needed
+          // dQ_i = dS K_j: A = dS (queries contiguous: MN-major), B = K_j (MN-major), in two head-dim halves
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)
-            mma_ss(tdP, sdesc_sw128(sDS + kk * 2048, T::BLOCK_BYTES, 1024),
-                   sdesc_sw128(sK + kk * 2048, T::BLOCK_BYTES, 1024), I_MM, kk > 0 ? 1u : 0u);
-          mma_commit(bDqf);  // the drain releases the Q / dO stage after staging dQ_i in it
+            mma_ss_p(leader, tdP, sdesc_add(dSmn, kk * 2048), sdesc_add(dKmn, kk * 2048), I_QA, kk > 0 ? 1u : 0u);
+          mma_commit_p(leader, bDq);
+          if (T::DQ_B > 0) {
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk)
+              mma_ss_p(leader, tdP + 64, sdesc_add(dSmn, kk * 2048), sdesc_add(dKmn, T::BLOCK_BYTES + kk * 2048), I_QB,
+                       kk > 0 ? 1u : 0u);
+            mma_commit_p(leader, bDq + 8u);
+          }
           if (nx) {
-            if (!(ok = wait_bounded(wc, bDqe, it & 1, wait_site(0x43, it)))) break;
+            if (!(ok = wait_all(bDf + 8u * sn, ((it + 1) >> 1) & 1, wait_site(0x47, it)))) break;
+            if (!(ok = wait_all(bDqe, it & 1, wait_site(0x43, it)))) break;
             tc_fence_after();
-            mma_kk(tdP, sV, do_n);  // dP^T_{i+1}
-            mma_commit(bDp);
+            mma_kk(tdP, dVk, sdesc_add(dOk0, sno), I_DP);  // dP^T_{i+1}, queries 0-63
+            mma_commit_p(leader, bDp);
+            if (T::DQ_B > 0 && !(ok = wait_all(bDqe + 8u, it & 1, wait_site(0x48, it)))) break;
+            tc_fence_after();
+            mma_kk(tdP + 64, dVk, sdesc_add(dOk0, sno + 8192), I_DP);  // queries 64-127
+            mma_commit_p(leader, bDp + 8u);
           }
         }
-        if (ok) mma_commit(bFin);
-        mma_commit(bDrain);  // fires once every MMA issued above has finished
+        if (ok) mma_commit_p(leader, bFin);
+        mma_commit_p(leader, bDrain);  // fires once every MMA issued above has finished
         wait_drain(bDrain, 0, p.limit_ns);
       }
       __syncwarp();
     }
-    setmaxnreg_inc<168>();
+    setmaxnreg_inc<128>();
   }
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 9) {
+  if (warp == 13) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }

@@ -11,10 +11,11 @@
 //   warps 0-3  softmax warpgroup for query tile 0 (one thread per row)
 //   warps 4-7  softmax warpgroup for query tile 1
 //   warp  8    TMA producer: Q tiles once, then K_j / V_j into a smem ring
-//   warp  9    MMA issuer (one thread): tcgen05 S = Q K^T and O += P V
+//              (5 slots at d = 96 / 128, 8 at d = 64)
+//   warp  9    MMA issuer: tcgen05 S = Q K^T and O += P V (one elected lane issues)
 //   warps 10-11 idle
-// setmaxnreg moves registers from the producer/MMA warpgroup (72 each) to
-// the softmax warpgroups (216 each): 2*128*216 + 128*72 = 384*168, the
+// setmaxnreg moves registers from the producer/MMA warpgroup (88 each) to
+// the softmax warpgroups (208 each): 2*128*208 + 128*88 = 384*168, the
 // block's launch allocation.
 // Tensor memory (512 columns x 128 lanes x 32 bit):
 //   [  0,128) S0 (fp32), P0 (bf16 pairs) overwrites its first 64 columns
@@ -40,9 +41,9 @@ struct FwdTraits {
   static constexpr int NB = (D + 63) / 64;           // 64-column (128-byte) blocks per row
   static constexpr int BLOCK_BYTES = 128 * 128;      // [128 rows x 128 B]
   static constexpr int TILE_BYTES = NB * BLOCK_BYTES;
-  static constexpr int NSTAGE = (D == 64) ? 8 : 4;   // K/V ring depth
+  static constexpr int NSTAGE = (D == 64) ? 8 : 5;   // K/V ring depth
   static constexpr int KSTEPS = D / 16;              // K=16 steps of Q K^T
-  static constexpr int NBAR = 2 + 2 * NSTAGE + 2 + 2 + 2 + 1;
+  static constexpr int NBAR = 2 + 2 * NSTAGE + 2 + 4 + 2 + 1;
   static constexpr int SMEM = 1024 + (2 + NSTAGE) * TILE_BYTES + NBAR * 8 + 16;
   static constexpr int THREADS = 384;
 };
@@ -65,8 +66,8 @@ __global__ void __launch_bounds__(384, 1)
   const uint32_t bKVf = sBar + 8u * 2;               // kv_full[NSTAGE]
   const uint32_t bKVe = bKVf + 8u * T::NSTAGE;       // kv_empty[NSTAGE]
   const uint32_t bS = bKVe + 8u * T::NSTAGE;         // s_full[2]
-  const uint32_t bP = bS + 16u;                      // p_full[2]
-  const uint32_t bO = bP + 16u;                      // o_full[2]
+  const uint32_t bP = bS + 16u;                      // p_full[2][2] (tile, half of the keys)
+  const uint32_t bO = bP + 32u;                      // o_full[2]
   const uint32_t bDrain = bO + 16u;
   uint8_t* const misc = gbase + (sBar - base) + 8 * T::NBAR;
   uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(misc);
@@ -90,7 +91,8 @@ __global__ void __launch_bounds__(384, 1)
     for (int s = 0; s < 2; ++s) {
       mbar_init(bQ + 8u * s, 1);
       mbar_init(bS + 8u * s, 1);
-      mbar_init(bP + 8u * s, 128);
+      mbar_init(bP + 16u * s, 128);
+      mbar_init(bP + 16u * s + 8u, 128);
       mbar_init(bO + 8u * s, 1);
     }
     for (int i = 0; i < T::NSTAGE; ++i) {
@@ -112,7 +114,7 @@ __global__ void __launch_bounds__(384, 1)
   const WaitCtx wc{abort_flag, p.status, p.limit_ns, p.info};
 
   if (warp < 8) {
-    setmaxnreg_inc<216>();
+    setmaxnreg_inc<208>();
     reg_split_sync(384);
     // ------------------------------------------------------------ softmax
     const int s = warp >> 2;            // query tile of this warpgroup
@@ -122,7 +124,7 @@ __global__ void __launch_bounds__(384, 1)
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
     const uint32_t tS = tmem + s * 128 + lane_off;
     const uint32_t tO = tmem + 256 + s * 128 + lane_off;
-    const uint32_t barS = bS + 8u * s, barP = bP + 8u * s, barO = bO + 8u * s;
+    const uint32_t barS = bS + 8u * s, barP = bP + 16u * s, barO = bO + 8u * s;
     const float c = p.scale_log2;
     float m = -INFINITY, l = 0.f;
     bool ok = true;
@@ -197,30 +199,31 @@ __global__ void __launch_bounds__(384, 1)
         }
       }
       // p = 2^(x*c - m): one packed FMA per pair of scores, then ex2; the row
-      // sum runs in 4 packed partial sums.
+      // sum runs in 4 packed partial sums.  P is published in two halves of
+      // 64 keys (one barrier per half) so that the P V MMA over the first 64
+      // keys runs while the second half is computed.
       const float2 c2 = make_float2(c, c), nm2 = make_float2(-m, -m);
       float2 sum[4];
 #pragma unroll
       for (int k = 0; k < 4; ++k) sum[k] = make_float2(0.f, 0.f);
 #pragma unroll
-      for (int i = 0; i < 128; i += 2) {
-        const float2 t = ffma2(make_float2(x[i], x[i + 1]), c2, nm2);
-        x[i] = ex2(t.x);
-        x[i + 1] = ex2(t.y);
-        sum[(i >> 1) & 3] = fadd2(sum[(i >> 1) & 3], make_float2(x[i], x[i + 1]));
-      }
-      const float2 s01 = fadd2(sum[0], sum[1]), s23 = fadd2(sum[2], sum[3]);
-      l = l * alpha + ((s01.x + s23.x) + (s01.y + s23.y));
-#pragma unroll
       for (int h = 0; h < 2; ++h) {
         uint32_t pk[32];
 #pragma unroll
-        for (int i = 0; i < 32; ++i) pk[i] = pack_bf16(x[64 * h + 2 * i], x[64 * h + 2 * i + 1]);
+        for (int e = 0; e < 32; ++e) {
+          const int i = 64 * h + 2 * e;
+          const float2 t = ffma2(make_float2(x[i], x[i + 1]), c2, nm2);
+          const float2 pp = make_float2(ex2(t.x), ex2(t.y));
+          sum[e & 3] = fadd2(sum[e & 3], pp);
+          pk[e] = pack_bf16(pp.x, pp.y);
+        }
         tmem_st32(tS + 32 * h, pk);
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(barP + 8u * h);
       }
-      tmem_wait_st();
-      tc_fence_before();
-      mbar_arrive(barP);
+      const float2 s01 = fadd2(sum[0], sum[1]), s23 = fadd2(sum[2], sum[3]);
+      l = l * alpha + ((s01.x + s23.x) + (s01.y + s23.y));
     }
 
     // ------------------------------------------------------------ epilogue
@@ -260,7 +263,7 @@ __global__ void __launch_bounds__(384, 1)
     }
     setmaxnreg_dec<168>();  // one register budget again for the common teardown
   } else {
-    setmaxnreg_dec<72>();
+    setmaxnreg_dec<88>();
     reg_split_sync(384);
     if (warp == 8) {
       // ------------------------------------------------------------ producer
@@ -298,67 +301,89 @@ __global__ void __launch_bounds__(384, 1)
       __syncwarp();
     } else if (warp == 9) {
       // ------------------------------------------------------------ MMA issuer
-      if (lane == 0) {
+      // The whole warp runs the issue loop, so descriptor arithmetic stays
+      // warp-uniform; one elected lane issues each tcgen05 instruction.
+      // Descriptors are built once per tile and moved by constant offsets.
+      {
+        const uint32_t leader = elect_one();
         constexpr uint32_t IQK = idesc_bf16_f32(128, 128, false, false);
         constexpr uint32_t IPV = idesc_bf16_f32(128, D, false, true);
         const uint32_t tS0 = tmem, tS1 = tmem + 128, tO0 = tmem + 256, tO1 = tmem + 384;
-        auto qk = [&](uint32_t dS, uint32_t q_tile, uint32_t k_tile) {
-  #pragma unroll
+        const uint64_t dQ0 = sdesc_sw128(sQ, 16, 1024), dQ1 = sdesc_sw128(sQ + T::TILE_BYTES, 16, 1024);
+        const uint64_t dK0 = sdesc_sw128(sKV, 16, 1024);             // K slots (K-major)
+        const uint64_t dV0 = sdesc_sw128(sKV, T::BLOCK_BYTES, 1024);  // V slots (MN-major)
+        auto qk = [&](uint32_t dS, uint64_t qd, uint64_t kd) {
+#pragma unroll
           for (int kk = 0; kk < T::KSTEPS; ++kk) {
             const uint32_t off = (kk >> 2) * T::BLOCK_BYTES + (kk & 3) * 32;
-            mma_ss(dS, sdesc_sw128(q_tile + off, 16, 1024), sdesc_sw128(k_tile + off, 16, 1024), IQK, kk > 0);
+            mma_ss_p(leader, dS, sdesc_add(qd, off), sdesc_add(kd, off), IQK, kk > 0);
           }
         };
-        auto pv = [&](uint32_t dO, uint32_t p_tmem, uint32_t v_tile, bool acc) {
-  #pragma unroll
-          for (int kk = 0; kk < 8; ++kk)
-            mma_ts(dO, p_tmem + kk * 8, sdesc_sw128(v_tile + kk * 2048, T::BLOCK_BYTES, 1024), IPV,
-                   (acc || kk > 0) ? 1u : 0u);
+        // O += P V over keys [64h, 64h + 64) once half h of P is in TMEM.
+        auto pv_half = [&](uint32_t dO, uint32_t p_tmem, uint64_t vd, bool acc, int h) {
+#pragma unroll
+          for (int k4 = 0; k4 < 4; ++k4) {
+            const int kk = 4 * h + k4;
+            mma_ts_p(leader, dO, p_tmem + kk * 8, sdesc_add(vd, kk * 2048), IPV, (acc || kk > 0) ? 1u : 0u);
+          }
         };
-        bool ok = wait_bounded(wc, bKVf, 0, wait_site(0x71, 0)) && wait_bounded(wc, bQ, 0, wait_site(0x72, 0));
+        auto wait_all = [&](uint32_t bar, uint32_t parity, int site) {
+          return __all_sync(0xffffffffu, wait_bounded(wc, bar, parity, site));
+        };
+        bool ok = wait_all(bKVf, 0, wait_site(0x71, 0)) && wait_all(bQ, 0, wait_site(0x72, 0));
         if (ok) {
           tc_fence_after();
-          qk(tS0, sQ, sKV);
-          mma_commit(bS);
-          ok = wait_bounded(wc, bQ + 8u, 0, wait_site(0x73, 0));
+          qk(tS0, dQ0, dK0);
+          mma_commit_p(leader, bS);
+          ok = wait_all(bQ + 8u, 0, wait_site(0x73, 0));
         }
         if (ok) {
           tc_fence_after();
-          qk(tS1, sQ + T::TILE_BYTES, sKV);
-          mma_commit(bS + 8u);
-          mma_commit(bKVe);  // K_0 consumed
+          qk(tS1, dQ1, dK0);
+          mma_commit_p(leader, bS + 8u);
+          mma_commit_p(leader, bKVe);  // K_0 consumed
         }
         int t = 1;
         for (int j = 0; j < n1 && ok; ++j, t += 2) {
           const int sv = t % T::NSTAGE, sk = (t + 1) % T::NSTAGE;
           const bool next = j + 1 < n1;
-          if (!(ok = wait_bounded(wc, bKVf + 8u * sv, (t / T::NSTAGE) & 1, wait_site(0x74, j)))) break;
-          if (next && !(ok = wait_bounded(wc, bKVf + 8u * sk, ((t + 1) / T::NSTAGE) & 1, wait_site(0x75, j)))) break;
-          const uint32_t vt = sKV + sv * T::TILE_BYTES, kt = sKV + sk * T::TILE_BYTES;
+          const uint64_t vd = sdesc_add(dV0, sv * T::TILE_BYTES), kd = sdesc_add(dK0, sk * T::TILE_BYTES);
+          // V_j is needed now; K_{j+1} only for the next Q K^T.
+          if (!(ok = wait_all(bKVf + 8u * sv, (t / T::NSTAGE) & 1, wait_site(0x74, j)))) break;
           if (j < n0) {
-            if (!(ok = wait_bounded(wc, bP, j & 1, wait_site(0x76, j)))) break;
+            if (!(ok = wait_all(bP, j & 1, wait_site(0x76, j)))) break;  // keys 0-63
             tc_fence_after();
-            pv(tO0, tS0, vt, j > 0);
+            pv_half(tO0, tS0, vd, j > 0, 0);
+            if (!(ok = wait_all(bP + 8u, j & 1, wait_site(0x78, j)))) break;  // keys 64-127
+            tc_fence_after();
+            pv_half(tO0, tS0, vd, j > 0, 1);
             if (j + 1 < n0) {
-              qk(tS0, sQ, kt);
-              mma_commit(bS);
+              if (!(ok = wait_all(bKVf + 8u * sk, ((t + 1) / T::NSTAGE) & 1, wait_site(0x75, j)))) break;
+              tc_fence_after();
+              qk(tS0, dQ0, kd);
+              mma_commit_p(leader, bS);
             } else {
-              mma_commit(bO);
+              mma_commit_p(leader, bO);
             }
           }
-          if (!(ok = wait_bounded(wc, bP + 8u, j & 1, wait_site(0x77, j)))) break;
+          if (!(ok = wait_all(bP + 16u, j & 1, wait_site(0x77, j)))) break;
           tc_fence_after();
-          pv(tO1, tS1, vt, j > 0);
+          pv_half(tO1, tS1, vd, j > 0, 0);
+          if (!(ok = wait_all(bP + 24u, j & 1, wait_site(0x79, j)))) break;
+          tc_fence_after();
+          pv_half(tO1, tS1, vd, j > 0, 1);
           if (next) {
-            qk(tS1, sQ + T::TILE_BYTES, kt);
-            mma_commit(bS + 8u);
+            if (!(ok = wait_all(bKVf + 8u * sk, ((t + 1) / T::NSTAGE) & 1, wait_site(0x7a, j)))) break;
+            tc_fence_after();
+            qk(tS1, dQ1, kd);
+            mma_commit_p(leader, bS + 8u);
           } else {
-            mma_commit(bO + 8u);
+            mma_commit_p(leader, bO + 8u);
           }
-          mma_commit(bKVe + 8u * sv);
-          if (next) mma_commit(bKVe + 8u * sk);
+          mma_commit_p(leader, bKVe + 8u * sv);
+          if (next) mma_commit_p(leader, bKVe + 8u * sk);
         }
-        mma_commit(bDrain);  // fires once every MMA issued above has finished
+        mma_commit_p(leader, bDrain);  // fires once every MMA issued above has finished
         wait_drain(bDrain, 0, p.limit_ns);
       }
       __syncwarp();
