@@ -22,8 +22,8 @@
 //   warps 0-7   compute, two warpgroups: warpgroup X takes query columns
 //               [64X, 64X+64) of each 128 x 128 tile (keys x queries):
 //               S^T -> P^T (to TMEM, the A operand of the dV MMA) and
-//               dP^T -> dS^T (to shared memory, the A operand of the dK and
-//               dQ MMAs); then the dV (X=0) / dK (X=1) epilogue
+//               dP^T -> dS^T (to shared memory, the A operand of the dQ and
+//               dK MMAs); then the dV (X=0) / dK (X=1) epilogue
 //   warps 8-11  dQ drain: TMEM -> shared memory -> TMA reduce-add
 //   warp  12    TMA producer: K_j, V_j once; Q_i (+ -lse2_i, -D_i), dO_i
 //   warp  13    MMA issuer (one elected lane issues)
@@ -111,9 +111,7 @@ struct BwdTraits {
   static constexpr int TILES_BYTES = 6 * TILE_BYTES + DS_BYTES;
   static constexpr int SMEM = TILES_BYTES + 2 * VEC_BYTES + NBAR * 8 + 16;
   static constexpr int THREADS = 512;
-  // dQ_i leaves TMEM in two halves of head-dim columns: [0, 64) and [64, D).
-  static constexpr int DQ_B = D - 64;                  // 0 when D == 64
-  // ... and is staged in the dO stage (TILE_BYTES) in two rounds of columns.
+  // dQ_i is staged in the dO stage (TILE_BYTES) in two rounds of columns.
   static constexpr int R0 = (D == 64) ? 32 : 64;       // columns [0, R0) in round 0, [R0, D) in round 1
 };
 
@@ -146,10 +144,10 @@ __global__ void __launch_bounds__(512, 1)
   const uint32_t bDe = bDf + 16;      // [2] dO stage free (after dQ_i left through it)
   const uint32_t bS = bDe + 16;       // S^T ready
   const uint32_t bP = bS + 8;         // P^T in TMEM (256 arrivals)
-  const uint32_t bDp = bP + 8;        // [2] dP^T query half ready
+  const uint32_t bDp = bP + 8;        // dP^T ready
   const uint32_t bDs = bDp + 16;      // dS^T in smem (256 arrivals)
-  const uint32_t bDq = bDs + 8;       // [2] dQ_i head-dim half ready
-  const uint32_t bDqe = bDq + 16;     // [2] dQ half copied out of TMEM (128 arrivals)
+  const uint32_t bDq = bDs + 8;       // dQ_i ready in TMEM
+  const uint32_t bDqe = bDq + 16;     // dQ_i copied out of TMEM (128 arrivals)
   const uint32_t bStg = bDqe + 16;    // [2] dQ round staged in smem (128 arrivals)
   const uint32_t bSfree = bStg + 16;  // dO stage free again after round 0 (1 arrival)
   const uint32_t bFin = bSfree + 8;   // every MMA done
@@ -175,12 +173,12 @@ __global__ void __launch_bounds__(512, 1)
       mbar_init(bQe + 8u * s, 1);
       mbar_init(bDf + 8u * s, 1);
       mbar_init(bDe + 8u * s, 1);
-      mbar_init(bDp + 8u * s, 1);
-      mbar_init(bDq + 8u * s, 1);
-      mbar_init(bDqe + 8u * s, 128);
       mbar_init(bStg + 8u * s, 128);
     }
     mbar_init(bS, 1);
+    mbar_init(bDp, 1);
+    mbar_init(bDq, 1);
+    mbar_init(bDqe, 128);
     mbar_init(bP, 256);
     mbar_init(bDs, 256);
     mbar_init(bSfree, 1);
@@ -265,7 +263,7 @@ __global__ void __launch_bounds__(512, 1)
       // dS^T[r][q] = P^T[r][q] * (dP^T[r][q] - D[q]) -> bf16 -> smem block X
       // (128-byte swizzled rows, 16-byte chunk q/8).  The softmax scale is
       // applied later, to dK in its epilogue and to dQ in the drain.
-      ok = __all_sync(0xffffffffu, wait_bounded(wc, bDp + 8u * X, it & 1, wait_site(0x14, it)));
+      ok = __all_sync(0xffffffffu, wait_bounded(wc, bDp, it & 1, wait_site(0x14, it)));
       if (!ok) break;
       tc_fence_after();
       uint32_t g0[32], g1[32];
@@ -340,19 +338,30 @@ __global__ void __launch_bounds__(512, 1)
     setmaxnreg_dec<120>();
     reg_split_sync(512);
     // ------------------------------------------------------------ dQ drain
-    // dQ_i (fp32, scale applied) leaves TMEM in two head-dim halves and goes
-    // to the accumulator by TMA reductions from the step's dO stage (idle
-    // once dQ_i is final), in two rounds of columns; then the dO stage goes
-    // back to the producer.
+    // dQ_i (fp32, scale applied) goes to the accumulator by TMA reductions
+    // from the step's dO stage (idle once dQ_i is final) in two rounds of
+    // columns, [0, R0) then [R0, D).  TMEM is handed back as soon as every
+    // column of dQ_i is staged or held in registers, so the next dP^T can
+    // start while the reductions run; then the dO stage goes back to the
+    // producer.
     const int q = threadIdx.x - 256;  // query row within the tile == TMEM lane
     const uint32_t tQ = tmem + 128 + ((uint32_t)((warp - 8) * 32) << 16);
     const float2 sc2 = make_float2(p.scale, p.scale);  // dQ = scale dS K
+    // 32 columns of one row -> one 128-byte row of a [128 x 32] fp32 box.
+    auto stage_box = [&](const uint32_t (&gg)[32], uint32_t box) {
+#pragma unroll
+      for (int c8 = 0; c8 < 8; ++c8) {
+        const float2 a0 = fmul2(make_float2(__uint_as_float(gg[4 * c8]), __uint_as_float(gg[4 * c8 + 1])), sc2);
+        const float2 a1 = fmul2(make_float2(__uint_as_float(gg[4 * c8 + 2]), __uint_as_float(gg[4 * c8 + 3])), sc2);
+        st_shared_v4(box + sw128_offset(q, c8), __float_as_uint(a0.x), __float_as_uint(a0.y), __float_as_uint(a1.x),
+                     __float_as_uint(a1.y));
+      }
+    };
     for (int it = 0; it < total; ++it) {
       const int h = hk * p.G + it / ni, i = i0 + it % ni;
       const int st = it & 1;
       const int bh = b * p.H + h;
       const uint32_t stg = sdO + st * T::TILE_BYTES;
-      // half A: head-dim columns [0, 64)
       if (!__all_sync(0xffffffffu, wait_bounded(wc, bDq, it & 1, wait_site(0x21, it)))) break;
       tc_fence_after();
       uint32_t ga[32], gb[32];
@@ -361,51 +370,38 @@ __global__ void __launch_bounds__(512, 1)
       tmem_wait_ld();
       reg_fence(ga);
       reg_fence(gb);
-      tc_fence_before();
-      mbar_arrive(bDqe);
+      if (D == 64) {  // all of dQ_i is in registers
+        tc_fence_before();
+        mbar_arrive(bDqe);
+      }
       // round 0: columns [0, R0) (32 or 64)
-      auto stage_box = [&](const uint32_t (&gg)[32], uint32_t box) {
-#pragma unroll
-        for (int c8 = 0; c8 < 8; ++c8) {
-          const float2 a0 = fmul2(make_float2(__uint_as_float(gg[4 * c8]), __uint_as_float(gg[4 * c8 + 1])), sc2);
-          const float2 a1 = fmul2(make_float2(__uint_as_float(gg[4 * c8 + 2]), __uint_as_float(gg[4 * c8 + 3])), sc2);
-          st_shared_v4(box + sw128_offset(q, c8), __float_as_uint(a0.x), __float_as_uint(a0.y), __float_as_uint(a1.x),
-                       __float_as_uint(a1.y));
-        }
-      };
       stage_box(ga, stg);
       if (T::R0 == 64) stage_box(gb, stg + T::BLOCK_BYTES);
       fence_proxy_async_smem();
       mbar_arrive(bStg);
-      bool ok0 = true;
-      if (q == 0) {
-        ok0 = wait_bounded(wc, bStg, it & 1, wait_site(0x22, it));
-        if (ok0) {
-          tma_reduce_add_3d(&tmdQacc, stg, 0, i * 128, bh);
-          if (T::R0 == 64) tma_reduce_add_3d(&tmdQacc, stg + T::BLOCK_BYTES, 32, i * 128, bh);
-          bulk_commit();
-          bulk_wait_read_all();
-          mbar_arrive(bSfree);
-        }
-      }
-      // half B (D > 64): head-dim columns [64, D)
+      // columns [64, D) to registers; then TMEM is free
       uint32_t gc[32], gd[32];
-      if (T::DQ_B > 0) {
-        if (!__all_sync(0xffffffffu, wait_bounded(wc, bDq + 8u, it & 1, wait_site(0x23, it)))) break;
-        tc_fence_after();
+      if (D > 64) {
         tmem_ld32(tQ + 64, gc);
-        if (T::DQ_B == 64) tmem_ld32(tQ + 96, gd);
+        if (D == 128) tmem_ld32(tQ + 96, gd);
         tmem_wait_ld();
         reg_fence(gc);
-        if (T::DQ_B == 64) reg_fence(gd);
+        if (D == 128) reg_fence(gd);
         tc_fence_before();
-        mbar_arrive(bDqe + 8u);
+        mbar_arrive(bDqe);
+      }
+      if (q == 0 && wait_bounded(wc, bStg, it & 1, wait_site(0x22, it))) {
+        tma_reduce_add_3d(&tmdQacc, stg, 0, i * 128, bh);
+        if (T::R0 == 64) tma_reduce_add_3d(&tmdQacc, stg + T::BLOCK_BYTES, 32, i * 128, bh);
+        bulk_commit();
+        bulk_wait_read_all();
+        mbar_arrive(bSfree);
       }
       // round 1: columns [R0, D), after the round-0 reduction has read the stage
       if (!__all_sync(0xffffffffu, wait_bounded(wc, bSfree, it & 1, wait_site(0x24, it)))) break;
-      if (T::DQ_B > 0) {
+      if (D > 64) {
         stage_box(gc, stg);
-        if (T::DQ_B == 64) stage_box(gd, stg + T::BLOCK_BYTES);
+        if (D == 128) stage_box(gd, stg + T::BLOCK_BYTES);
       } else {
         stage_box(gb, stg);
       }
@@ -418,7 +414,6 @@ __global__ void __launch_bounds__(512, 1)
         bulk_wait_read_all();
         mbar_arrive(bDe + 8u * st);
       }
-      (void)ok0;
     }
     if (q == 0) bulk_wait_all();  // every reduction has landed before the CTA exits
     setmaxnreg_inc<128>();
@@ -471,11 +466,9 @@ __global__ void __launch_bounds__(512, 1)
       // Descriptors are built once and moved by constant offsets.
       {
         const uint32_t leader = elect_one();
-        constexpr uint32_t I_SS = idesc_bf16_f32(128, 128, false, false);   // S^T (K-major x K-major)
-        constexpr uint32_t I_DP = idesc_bf16_f32(128, 64, false, false);    // dP^T query half
+        constexpr uint32_t I_SS = idesc_bf16_f32(128, 128, false, false);   // S^T, dP^T (K-major x K-major)
         constexpr uint32_t I_TB = idesc_bf16_f32(128, D, false, true);      // dV (A in TMEM), dK
-        constexpr uint32_t I_QA = idesc_bf16_f32(128, 64, true, true);      // dQ head-dim half A
-        constexpr uint32_t I_QB = idesc_bf16_f32(128, (D > 64 ? D - 64 : 64), true, true);  // half B
+        constexpr uint32_t I_DQ = idesc_bf16_f32(128, D, true, true);       // dQ (both MN-major)
         const uint32_t tS = tmem, tdP = tmem + 128, tdK = tmem + 256, tdV = tmem + 384;
         const uint64_t dKk = sdesc_sw128(sK, 16, 1024);                  // K as K-major A (S^T)
         const uint64_t dVk = sdesc_sw128(sV, 16, 1024);                  // V as K-major A (dP^T)
@@ -497,19 +490,18 @@ __global__ void __launch_bounds__(512, 1)
         auto wait_all = [&](uint32_t bar, uint32_t parity, int site) {
           return __all_sync(0xffffffffu, wait_bounded(wc, bar, parity, site));
         };
-        // Issue order per step i: dV(i), S^T(i+1), dK(i), dQ(i) [two halves],
-        // dP^T(i+1) [two query halves].  S^T(i+1) overwrites P^T(i) in TMEM
-        // only after dV(i), issued first (MMAs from one thread run in order).
+        // Issue order per step i: dV(i), S^T(i+1), dQ(i), dK(i), dP^T(i+1).
+        // S^T(i+1) overwrites P^T(i) in TMEM only after dV(i), issued first
+        // (MMAs from one thread run in order); dK(i) runs while the drain
+        // empties dQ(i) out of the columns dP^T(i+1) then reuses.
         bool ok = wait_all(bKV, 0, wait_site(0x41, 0)) && wait_all(bQf, 0, wait_site(0x42, 0)) &&
                   wait_all(bDf, 0, wait_site(0x47, 0));
         if (ok) {
           tc_fence_after();
           mma_kk(tS, dKk, dQk0, I_SS);  // S^T_0 = K Q_0^T
           mma_commit_p(leader, bS);
-          mma_kk(tdP, dVk, dOk0, I_DP);  // dP^T_0, queries 0-63
+          mma_kk(tdP, dVk, dOk0, I_SS);  // dP^T_0 = V dO_0^T
           mma_commit_p(leader, bDp);
-          mma_kk(tdP + 64, dVk, sdesc_add(dOk0, 8192), I_DP);  // queries 64-127 (row 64 of each block)
-          mma_commit_p(leader, bDp + 8u);
         }
         for (int it = 0; it < total && ok; ++it) {
           const int st = it & 1, sn = st ^ 1;
@@ -531,34 +523,23 @@ __global__ void __launch_bounds__(512, 1)
           }
           if (!(ok = wait_all(bDs, it & 1, wait_site(0x45, it)))) break;
           tc_fence_after();
+          // dQ_i = dS K_j: A = dS (queries contiguous: MN-major), B = K_j (MN-major)
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            mma_ss_p(leader, tdP, sdesc_add(dSmn, kk * 2048), sdesc_add(dKmn, kk * 2048), I_DQ, kk > 0 ? 1u : 0u);
+          mma_commit_p(leader, bDq);
           // dK += dS^T Q_i: A = dS^T (K-major over queries), B = Q_i (MN-major)
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)
             mma_ss_p(leader, tdK, sdesc_add(dSk, (kk >> 2) * T::BLOCK_BYTES + (kk & 3) * 32),
                      sdesc_add(dQmn0, so + kk * 2048), I_TB, (it > 0 || kk > 0) ? 1u : 0u);
           mma_commit_p(leader, bQe + 8u * st);  // Q_i (and its vectors) no longer needed
-          // dQ_i = dS K_j: A = dS (queries contiguous: MN-major), B = K_j (MN-major), in two head-dim halves
-#pragma unroll
-          for (int kk = 0; kk < 8; ++kk)
-            mma_ss_p(leader, tdP, sdesc_add(dSmn, kk * 2048), sdesc_add(dKmn, kk * 2048), I_QA, kk > 0 ? 1u : 0u);
-          mma_commit_p(leader, bDq);
-          if (T::DQ_B > 0) {
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk)
-              mma_ss_p(leader, tdP + 64, sdesc_add(dSmn, kk * 2048), sdesc_add(dKmn, T::BLOCK_BYTES + kk * 2048), I_QB,
-                       kk > 0 ? 1u : 0u);
-            mma_commit_p(leader, bDq + 8u);
-          }
           if (nx) {
             if (!(ok = wait_all(bDf + 8u * sn, ((it + 1) >> 1) & 1, wait_site(0x47, it)))) break;
             if (!(ok = wait_all(bDqe, it & 1, wait_site(0x43, it)))) break;
             tc_fence_after();
-            mma_kk(tdP, dVk, sdesc_add(dOk0, sno), I_DP);  // dP^T_{i+1}, queries 0-63
+            mma_kk(tdP, dVk, sdesc_add(dOk0, sno), I_SS);  // dP^T_{i+1}
             mma_commit_p(leader, bDp);
-            if (T::DQ_B > 0 && !(ok = wait_all(bDqe + 8u, it & 1, wait_site(0x48, it)))) break;
-            tc_fence_after();
-            mma_kk(tdP + 64, dVk, sdesc_add(dOk0, sno + 8192), I_DP);  // queries 64-127
-            mma_commit_p(leader, bDp + 8u);
           }
         }
         if (ok) mma_commit_p(leader, bFin);
