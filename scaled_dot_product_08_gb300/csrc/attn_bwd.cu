@@ -25,9 +25,11 @@
 //               dP^T -> dS^T (to shared memory, the A operand of the dQ and
 //               dK MMAs); then the dV (X=0) / dK (X=1) epilogue
 //   warps 8-11  dQ drain: TMEM -> shared memory -> TMA reduce-add
-//   warp  12    TMA producer: K_j, V_j once; Q_i (+ -lse2_i, -D_i), dO_i
+//   warp  12    TMA producer: K_j, V_j once; Q_i (+ -lse2_i, -D_i)
 //   warp  13    MMA issuer (one elected lane issues)
-//   warps 14-15 idle
+//   warp  14    idle
+//   warp  15    TMA producer: dO_i (its own loop, so a dO stage still
+//               busy with dQ reductions never delays the next Q_i)
 // setmaxnreg: compute 144, drain 120, producer/MMA 104 registers per thread
 // (128 * (144 + 144 + 120 + 104) = 512 * 128, the launch allocation).
 // Tensor memory: [0,128) S^T / P^T, [128,256) dP^T / dQ_i, [256,256+d) dK,
@@ -421,16 +423,15 @@ __global__ void __launch_bounds__(512, 1)
     setmaxnreg_dec<104>();
     reg_split_sync(512);
     if (warp == 12) {
-      // ------------------------------------------------------------ producer
+      // ------------------------------------------------------------ producer: K, V, Q
       if (lane == 0) {
         tma_prefetch_desc(&tmQ);
-        tma_prefetch_desc(&tmdO);
         mbar_expect_tx(bKV, 2 * T::TILE_BYTES);
         for (int cb = 0; cb < T::NB; ++cb) {
           tma_load_3d(sK + cb * T::BLOCK_BYTES, &tmK, bKV, cb * 64, j * 128, bhk);
           tma_load_3d(sV + cb * T::BLOCK_BYTES, &tmV, bKV, cb * 64, j * 128, bhk);
         }
-        int issued_q = 0, issued_d = 0;
+        int issued = 0;
         for (int it = 0; it < total; ++it) {
           const int st = it & 1, rd = it >> 1;
           const int h = hk * p.G + it / ni, i = i0 + it % ni;
@@ -443,20 +444,32 @@ __global__ void __launch_bounds__(512, 1)
           const size_t voff = (size_t)bh * p.Npad + (size_t)i * 128;
           bulk_load(sVec + st * T::VEC_BYTES, p.lse2 + voff, 512, barq);
           bulk_load(sVec + st * T::VEC_BYTES + 512, p.dvec + voff, 512, barq);
-          issued_q = it + 1;
+          issued = it + 1;
+        }
+        // Every copy issued above has landed before the CTA may exit.
+        wait_drain(bKV, 0, p.limit_ns);
+        for (int st = 0; st < 2 && st < issued; ++st)
+          wait_drain(bQf + 8u * st, ((((issued - 1 - st) / 2) * 2 + st) >> 1) & 1, p.limit_ns);
+      }
+      __syncwarp();
+    } else if (warp == 15) {
+      // ------------------------------------------------------------ producer: dO
+      if (lane == 0) {
+        tma_prefetch_desc(&tmdO);
+        int issued = 0;
+        for (int it = 0; it < total; ++it) {
+          const int st = it & 1, rd = it >> 1;
+          const int h = hk * p.G + it / ni, i = i0 + it % ni;
+          const int bh = b * p.H + h;
           if (rd > 0 && !wait_bounded(wc, bDe + 8u * st, (rd - 1) & 1, wait_site(0x32, it))) break;
           const uint32_t bard = bDf + 8u * st;
           mbar_expect_tx(bard, T::TILE_BYTES);
           for (int cb = 0; cb < T::NB; ++cb)
             tma_load_3d(sdO + st * T::TILE_BYTES + cb * T::BLOCK_BYTES, &tmdO, bard, cb * 64, i * 128, bh);
-          issued_d = it + 1;
+          issued = it + 1;
         }
-        // Every copy issued above has landed before the CTA may exit.
-        wait_drain(bKV, 0, p.limit_ns);
-        for (int st = 0; st < 2; ++st) {
-          if (st < issued_q) wait_drain(bQf + 8u * st, ((((issued_q - 1 - st) / 2) * 2 + st) >> 1) & 1, p.limit_ns);
-          if (st < issued_d) wait_drain(bDf + 8u * st, ((((issued_d - 1 - st) / 2) * 2 + st) >> 1) & 1, p.limit_ns);
-        }
+        for (int st = 0; st < 2 && st < issued; ++st)
+          wait_drain(bDf + 8u * st, ((((issued - 1 - st) / 2) * 2 + st) >> 1) & 1, p.limit_ns);
       }
       __syncwarp();
     } else if (warp == 13) {
