@@ -281,7 +281,8 @@ def run_ours(args, w, rank, world, local_rank):
                 "attn_bwd_grad")
             if evs is not None:
                 evs[3].record(stream)
-            chk(sdpa.attn_bwd_dq(dq.data_ptr(), ws.data_ptr(), ws_bytes, B, H, Hkv, N, d, sp), "attn_bwd_dq")
+            chk(sdpa.attn_bwd_dq(q.data_ptr(), k.data_ptr(), v.data_ptr(), do.data_ptr(), dq.data_ptr(),
+                                 ws.data_ptr(), ws_bytes, B, H, Hkv, N, d, s, w.causal, sp), "attn_bwd_dq")
             if evs is not None:
                 evs[4].record(stream)
 
@@ -325,7 +326,11 @@ def run_ours(args, w, rank, world, local_rank):
     # ---- roofline of the dominant kernel
     peaks, peak_src = load_peaks()
     dom = max(per_kernel, key=per_kernel.get)
-    kflops = {"attn_fwd": f_fwd, "attn_bwd_grad": f_bwd}
+    # Tensor work each kernel executes, in units of one 2*B*H*N^2*d product
+    # (halved when causal): the forward runs two (QK^T, PV); the key-tile
+    # backward kernel four (S^T, dP^T, dV, dK); the query-tile kernel three
+    # (S, dP, dQ).  The step value above keeps the 2.5x-forward convention.
+    kflops = {"attn_fwd": f_fwd, "attn_bwd_grad": 2.0 * f_fwd, "attn_bwd_dq": 1.5 * f_fwd}
     if dom in kflops:
         achieved = kflops[dom] / (per_kernel[dom] / 1e3) / 1e12
         peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
@@ -333,8 +338,7 @@ def run_ours(args, w, rank, world, local_rank):
                 "frac": achieved / peak, "peak_source": f"{peak_src} bf16 burst (cuBLAS 8192^3)",
                 "frac_of_nominal_2250": achieved / 2250.0}
     else:
-        nbytes = {"attn_bwd_prep": 2 * B * H * N * d * 2 + B * H * N * 4 + B * H * N * (d + 2) * 4,
-                  "attn_bwd_dq": B * H * N * d * 4 + B * H * N * d * 2}[dom]
+        nbytes = {"attn_bwd_prep": 2 * B * H * N * d * 2 + B * H * N * 4 + B * H * N * 2 * 4}[dom]
         achieved = nbytes / (per_kernel[dom] / 1e3) / 1e9
         peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
         roof = {"kernel": dom, "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",

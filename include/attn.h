@@ -76,9 +76,10 @@ attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, flo
                        void* stream);
 
 /*
- * Bytes of device workspace attn_bwd needs for this shape: a float32 dQ
- * accumulator and two float32 per-row vectors, each padded to a multiple of
- * 128 rows per head.  Returns 0 for an invalid shape.
+ * Bytes of device workspace attn_bwd needs for this shape: two float32
+ * per-row vectors (D = rowsum(dO * O) and lse in base 2), each padded to a
+ * multiple of 128 rows per head, i.e. 8 * B * H * ceil(N/128) * 128 bytes.
+ * Returns 0 for an invalid shape.
  */
 size_t attn_bwd_workspace_size(int B, int H, int Hkv, int N, int d);
 
@@ -104,13 +105,17 @@ attn_status_t attn_bwd(const void* q, const void* k, const void* v, const void* 
 
 /*
  * The three stages attn_bwd runs, for callers that schedule (or time) them
- * separately.  Same arguments, layouts and workspace as attn_bwd; they must
- * run in this order on one stream with the same workspace:
- *   attn_bwd_prep  D = rowsum(dO * O) and lse in base 2 into the workspace,
- *                  dQ accumulator cleared                       (reads o, lse, dout)
- *   attn_bwd_grad  recomputes P tile by tile; writes dK, dV; adds dQ into
- *                  the workspace accumulator          (reads q, k, v, dout)
- *   attn_bwd_dq    dQ accumulator -> bf16 dq
+ * separately.  Same arguments, layouts and workspace as attn_bwd.  prep must
+ * complete before grad and dq start; grad and dq read the workspace but do
+ * not write it, and are independent of each other:
+ *   attn_bwd_prep  D = rowsum(dO * O) and lse in base 2 into the workspace
+ *                                                         (reads o, lse, dout)
+ *   attn_bwd_grad  one pass per key tile: recomputes P^T and dS^T tile by
+ *                  tile; writes dK, dV                  (reads q, k, v, dout)
+ *   attn_bwd_dq    one pass per query tile: recomputes P and dS tile by tile;
+ *                  writes dq                            (reads q, k, v, dout)
+ * Every output element has exactly one writer (no atomics), so the results
+ * are the same on every run.
  */
 attn_status_t attn_bwd_prep(const void* o, const float* lse, const void* dout,
                             void* workspace, size_t workspace_bytes,
@@ -119,8 +124,10 @@ attn_status_t attn_bwd_grad(const void* q, const void* k, const void* v, const v
                             void* dk, void* dv, void* workspace, size_t workspace_bytes,
                             int B, int H, int Hkv, int N, int d, float scale, int causal,
                             void* stream);
-attn_status_t attn_bwd_dq(void* dq, void* workspace, size_t workspace_bytes,
-                          int B, int H, int Hkv, int N, int d, void* stream);
+attn_status_t attn_bwd_dq(const void* q, const void* k, const void* v, const void* dout,
+                          void* dq, void* workspace, size_t workspace_bytes,
+                          int B, int H, int Hkv, int N, int d, float scale, int causal,
+                          void* stream);
 
 /*
  * Synchronises `stream`, then returns (and clears) the device status word
@@ -170,15 +177,16 @@ attn_status_t attn_selftest_wait_timeout(unsigned int timeout_us, void* stream);
  * cudaMalloc, cudaFree or other allocating routine.
  *   - Limit: shapes whose attn_bwd_workspace_size() exceeds 64 MiB
  *     (67108864 bytes) are rejected with ATTN_ERR_WORKSPACE; use attn_bwd
- *     with a caller workspace for those.  (At d = 128 that allows
- *     B*H*ceil(N/128)*128 <= 129,055 rows, e.g. B=1, H=16, N=8064.)
+ *     with a caller workspace for those.  (That allows
+ *     B*H*ceil(N/128)*128 <= 8,388,608 padded rows, e.g. B=8, H=16,
+ *     N=65536.)
  *   - Memory: every GPU that loads the library holds the 64 MiB until the
  *     process exits.
  *   - Set-up: the first call on a device looks up the array's device address
  *     with that device current; make that first call before any stream
  *     capture.
  *   - Sharing: all calls use the same array, which keeps the last call's
- *     contents (each call clears what it needs cleared).  Calls whose work
+ *     contents (each call rewrites what it reads).  Calls whose work
  *     overlaps on the GPU (different streams, or different host threads
  *     without ordering) race on the array and give wrong results; order
  *     them on one stream.

@@ -69,7 +69,7 @@ def load() -> ctypes.CDLL:
         lib.attn_bwd_grad.argtypes = [_P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t,
                                       _I, _I, _I, _I, _I, ctypes.c_float, _I, _P]
         lib.attn_bwd_grad.restype = _I
-        lib.attn_bwd_dq.argtypes = [_P, _P, ctypes.c_size_t, _I, _I, _I, _I, _I, _P]
+        lib.attn_bwd_dq.argtypes = [_P, _P, _P, _P, _P, _P, ctypes.c_size_t, _I, _I, _I, _I, _I, ctypes.c_float, _I, _P]
         lib.attn_bwd_dq.restype = _I
         lib.attn_get_device_status.argtypes = [_P]
         lib.attn_get_device_status.restype = _I
@@ -122,8 +122,8 @@ def attn_bwd_grad(q, k, v, dout, dk, dv, workspace, workspace_bytes, B, H, Hkv, 
                                 scale, int(causal), stream)
 
 
-def attn_bwd_dq(dq, workspace, workspace_bytes, B, H, Hkv, N, d, stream) -> int:
-    return load().attn_bwd_dq(dq, workspace, workspace_bytes, B, H, Hkv, N, d, stream)
+def attn_bwd_dq(q, k, v, dout, dq, workspace, workspace_bytes, B, H, Hkv, N, d, scale, causal, stream) -> int:
+    return load().attn_bwd_dq(q, k, v, dout, dq, workspace, workspace_bytes, B, H, Hkv, N, d, scale, causal, stream)
 
 
 def attn_get_device_status(stream=None) -> int:

@@ -110,20 +110,6 @@ bool make_map_bf16(CUtensorMap* m, const void* ptr, int d, int N, long long head
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// 3-D map over the float32 dQ accumulator (rows = B*H, Npad, d): box of 32
-// columns (128 bytes) x 128 rows x 1 head, 128-byte swizzle (TMA reductions).
-bool make_map_f32_acc(CUtensorMap* m, const void* ptr, int d, int npad, long long heads) {
-  EncodeTiledFn enc = encode_fn();
-  if (!enc) return false;
-  cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)npad, (cuuint64_t)heads};
-  cuuint64_t strides[2] = {(cuuint64_t)d * 4, (cuuint64_t)d * 4 * (cuuint64_t)npad};
-  cuuint32_t box[3] = {32, 128, 1};
-  cuuint32_t estr[3] = {1, 1, 1};
-  return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(ptr), dims, strides, box, estr,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 // Shape checks shared by forward and backward.
@@ -188,7 +174,7 @@ __global__ void selftest_wait_kernel(int* status, int* info, unsigned long long 
 
 extern "C" {
 
-int attn_abi_version(void) { return 1; }
+int attn_abi_version(void) { return 2; }
 
 const char* attn_status_string(attn_status_t s) {
   switch (s) {
@@ -240,17 +226,16 @@ size_t attn_bwd_workspace_size(int B, int H, int Hkv, int N, int d) {
   if (check_shape(B, H, Hkv, N, d) != ATTN_OK) return 0;
   const size_t npad = (size_t)((N + 127) / 128) * 128;
   const size_t rows = (size_t)B * H * npad;
-  return rows * (size_t)d * 4 + rows * 4 * 2;
+  return rows * 4 * 2;  // -D and -lse*log2(e) per (head, padded row), float32
 }
 
-// Workspace carve-up shared by the three backward stages.
+// Workspace carve-up shared by the three backward stages: [-D | -lse2].
 static void bwd_params(sdpa::BwdParams* p, void* workspace, int B, int H, int Hkv, int N, int d, float scale,
                        const DeviceInfo* di) {
   const int npad = ((N + 127) / 128) * 128;
   const size_t rows = (size_t)B * H * npad;
   memset(p, 0, sizeof(*p));
-  p->dq_acc = static_cast<float*>(workspace);
-  p->dvec = p->dq_acc + rows * (size_t)d;
+  p->dvec = static_cast<float*>(workspace);
   p->lse2 = p->dvec + rows;
   p->B = B;
   p->H = H;
@@ -303,24 +288,29 @@ attn_status_t attn_bwd_grad(const void* q, const void* k, const void* v, const v
     return ATTN_ERR_CUDA;
   sdpa::BwdParams p;
   bwd_params(&p, workspace, B, H, Hkv, N, d, scale, di);
-  CUtensorMap tdqa;
-  if (!make_map_f32_acc(&tdqa, p.dq_acc, d, p.Npad, (long long)B * H)) return ATTN_ERR_CUDA;
-  cudaError_t e = sdpa::launch_bwd_grad(d, causal != 0, tq, tk, tv, tdo, tdk, tdv, tdqa, p,
+  cudaError_t e = sdpa::launch_bwd_grad(d, causal != 0, tq, tk, tv, tdo, tdk, tdv, p,
                                         static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;
 }
 
-attn_status_t attn_bwd_dq(void* dq, void* workspace, size_t workspace_bytes, int B, int H, int Hkv, int N, int d,
+attn_status_t attn_bwd_dq(const void* q, const void* k, const void* v, const void* dout, void* dq, void* workspace,
+                          size_t workspace_bytes, int B, int H, int Hkv, int N, int d, float scale, int causal,
                           void* stream) {
   ATTN_TRY(check_shape(B, H, Hkv, N, d));
+  ATTN_TRY(check_scale_flag(scale, causal));
   ATTN_TRY(check_workspace(workspace, workspace_bytes, B, H, Hkv, N, d));
-  ATTN_TRY(check_ptrs({dq, workspace}));
+  ATTN_TRY(check_ptrs({q, k, v, dout, dq, workspace}));
   DeviceInfo* di = nullptr;
   ATTN_TRY(current_device(&di));
+  CUtensorMap tq, tk, tv, tdo, tdq;
+  if (!make_map_bf16(&tq, q, d, N, (long long)B * H) || !make_map_bf16(&tk, k, d, N, (long long)B * Hkv) ||
+      !make_map_bf16(&tv, v, d, N, (long long)B * Hkv) || !make_map_bf16(&tdo, dout, d, N, (long long)B * H) ||
+      !make_map_bf16(&tdq, dq, d, N, (long long)B * H))
+    return ATTN_ERR_CUDA;
   sdpa::BwdParams p;
-  bwd_params(&p, workspace, B, H, Hkv, N, d, 1.f, di);
-  p.dq = static_cast<uint16_t*>(dq);
-  return sdpa::launch_bwd_dq(p, static_cast<cudaStream_t>(stream)) == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;
+  bwd_params(&p, workspace, B, H, Hkv, N, d, scale, di);
+  cudaError_t e = sdpa::launch_bwd_dq(d, causal != 0, tq, tk, tv, tdo, tdq, p, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;
 }
 
 attn_status_t attn_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
@@ -333,7 +323,7 @@ attn_status_t attn_bwd(const void* q, const void* k, const void* v, const void* 
   ATTN_TRY(check_ptrs({q, k, v, o, lse, dout, dq, dk, dv, workspace}));
   ATTN_TRY(attn_bwd_prep(o, lse, dout, workspace, workspace_bytes, B, H, Hkv, N, d, stream));
   ATTN_TRY(attn_bwd_grad(q, k, v, dout, dk, dv, workspace, workspace_bytes, B, H, Hkv, N, d, scale, causal, stream));
-  return attn_bwd_dq(dq, workspace, workspace_bytes, B, H, Hkv, N, d, stream);
+  return attn_bwd_dq(q, k, v, dout, dq, workspace, workspace_bytes, B, H, Hkv, N, d, scale, causal, stream);
 }
 
 attn_status_t attn_get_device_status(void* stream) {

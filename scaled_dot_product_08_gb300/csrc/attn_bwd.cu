@@ -1,4 +1,4 @@
-// attn_bwd.cu — backward pass of exact attention on sm_103a.
+// attn_bwd.cu — backward pass of exact attention on sm_103a: dK and dV.
 //
 // Method (page "Flash Attention原理：分块计算与重计算，如何降低O(n^2)的显存占用",
 // §五 and FAQ Q19): the forward kept only O and the per-row logsumexp; the
@@ -9,30 +9,31 @@
 //     dS = P * (dP - D),  dQ = scale dS K,  dK = scale dS^T Q.
 //
 // Three kernels on the caller's stream:
-//   bwd_pre     -D = -rowsum(dO * O) (fp32), -lse2 = -lse * log2(e) (-inf on
-//               the padding rows of each head), dQ accumulator := 0
-//   bwd_main    one CTA per (key tile j, batch, K/V head); loops over the
-//               GQA group's query heads and the query tiles i (i >= j when
-//               causal).  dK_j and dV_j accumulate in tensor memory; dQ_i
-//               contributions are added to a float32 accumulator in global
-//               memory with TMA bulk reductions.
-//   bwd_convert dQ accumulator -> bf16 dQ
+//   bwd_pre     -D = -rowsum(dO * O) (fp32) and -lse2 = -lse * log2(e) (-inf
+//               on the padding rows of each head)
+//   bwd_main    (this file) one CTA per (key tile j, batch, K/V head); loops
+//               over the GQA group's query heads and the query tiles i (i >= j
+//               when causal); dK_j and dV_j accumulate in tensor memory and
+//               are written once
+//   bwd_dq      (attn_bwd_dq.cu) one CTA per (query tile, head); dQ in
+//               tensor memory, written once
+// Each output tile has exactly one writer: no atomics anywhere.
 //
-// bwd_main warp roles (512 threads = 4 warpgroups):
+// bwd_main warp roles (384 threads):
 //   warps 0-7   compute, two warpgroups: warpgroup X takes query columns
 //               [64X, 64X+64) of each 128 x 128 tile (keys x queries):
-//               S^T -> P^T (to TMEM, the A operand of the dV MMA) and
-//               dP^T -> dS^T (to shared memory, the A operand of the dQ and
-//               dK MMAs); then the dV (X=0) / dK (X=1) epilogue
-//   warps 8-11  dQ drain: TMEM -> shared memory -> TMA reduce-add
-//   warp  12    TMA producer: K_j, V_j once; Q_i (+ -lse2_i, -D_i)
-//   warp  13    MMA issuer (one elected lane issues)
-//   warp  14    idle
-//   warp  15    TMA producer: dO_i (its own loop, so a dO stage still
-//               busy with dQ reductions never delays the next Q_i)
-// setmaxnreg: compute 144, drain 120, producer/MMA 104 registers per thread
-// (128 * (144 + 144 + 120 + 104) = 512 * 128, the launch allocation).
-// Tensor memory: [0,128) S^T / P^T, [128,256) dP^T / dQ_i, [256,256+d) dK,
+//               S^T -> P^T (bf16 pairs over its S^T columns, the A operand of
+//               the dV MMA) and dP^T -> dS^T (bf16 pairs over its dP^T
+//               columns, the A operand of the dK MMA); then the dV (X=0) /
+//               dK (X=1) epilogue
+//   warp  8     TMA producer: K_j, V_j once; Q_i (+ -lse2_i, -D_i)
+//   warp  9     MMA issuer (one elected lane issues)
+//   warp  10    TMA producer: dO_i (its own loop, so a busy dO stage never
+//               delays the next Q_i)
+//   warp  11    idle
+// setmaxnreg: compute 200, the other warpgroup 104 registers per thread
+// (128 * (200 + 200 + 104) = 384 * 168, the launch allocation).
+// Tensor memory: [0,128) S^T / P^T, [128,256) dP^T / dS^T, [256,256+d) dK,
 // [384,384+d) dV.  All score tiles are 128 x 128 (keys x queries).
 #include <cmath>
 
@@ -44,8 +45,8 @@ namespace sdpa {
 // ------------------------------------------------------------------ preprocess
 // One warp per (head, padded row).  Row i < N: stores -D = -(dO_i . O_i)
 // (fp32) and -lse_i * log2(e).  Row i >= N: -D = 0 and -lse2 = -inf (so P = 0
-// there).  The negated values let the grad kernel form P and dP - D with one
-// packed FMA / add per pair.  Every row of the dQ accumulator is zeroed.
+// there).  The negated values let the other kernels form P and dP - D with
+// one packed FMA / add per pair.
 __global__ void __launch_bounds__(256) bwd_pre_kernel(const BwdParams p) {
   const long long rows = (long long)p.B * p.H * p.Npad;
   const long long row = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
@@ -53,8 +54,6 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const BwdParams p) {
   if (row >= rows) return;
   const long long bh = row / p.Npad;
   const int i = (int)(row % p.Npad);
-  float4* acc = reinterpret_cast<float4*>(p.dq_acc + row * p.d);
-  for (int c = lane; c < p.d / 4; c += 32) acc[c] = make_float4(0.f, 0.f, 0.f, 0.f);
   float dot = 0.f;
   if (i < p.N) {
     const size_t off = ((size_t)bh * p.N + i) * p.d;
@@ -79,26 +78,6 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const BwdParams p) {
   }
 }
 
-// ------------------------------------------------------------------ convert
-// dQ (bf16) = dQ accumulator (fp32) for the N real rows of each head.
-__global__ void __launch_bounds__(256) bwd_convert_kernel(const BwdParams p) {
-  const long long rows = (long long)p.B * p.H * p.N;
-  const long long row = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
-  const int lane = threadIdx.x & 31;
-  if (row >= rows) return;
-  const long long bh = row / p.N;
-  const int i = (int)(row % p.N);
-  const float* src = p.dq_acc + ((size_t)bh * p.Npad + i) * p.d;
-  uint16_t* dst = p.dq + (size_t)row * p.d;
-  for (int c = lane * 4; c < p.d; c += 128) {
-    const float4 a = *reinterpret_cast<const float4*>(src + c);
-    uint2 w;
-    w.x = pack_bf16(a.x, a.y);
-    w.y = pack_bf16(a.z, a.w);
-    *reinterpret_cast<uint2*>(dst + c) = w;
-  }
-}
-
 // ------------------------------------------------------------------ main
 template <int D>
 struct BwdTraits {
@@ -106,23 +85,20 @@ struct BwdTraits {
   static constexpr int BLOCK_BYTES = 128 * 128;
   static constexpr int TILE_BYTES = NB * BLOCK_BYTES;  // one [128 rows x d] bf16 tile
   static constexpr int KSTEPS = D / 16;
-  static constexpr int DS_BYTES = 2 * BLOCK_BYTES;     // dS^T: 128 keys x 128 queries, any d
   static constexpr int VEC_BYTES = 1024;               // -lse2[128] + -D[128]
-  static constexpr int NBAR = 32;
-  // K, V, Q[2], dO[2], dS^T, then vectors, barriers, misc
-  static constexpr int TILES_BYTES = 6 * TILE_BYTES + DS_BYTES;
+  static constexpr int NBAR = 16;
+  // K, V, Q[2], dO[2], then vectors, barriers, misc
+  static constexpr int TILES_BYTES = 6 * TILE_BYTES;
   static constexpr int SMEM = TILES_BYTES + 2 * VEC_BYTES + NBAR * 8 + 16;
-  static constexpr int THREADS = 512;
-  // dQ_i is staged in the dO stage (TILE_BYTES) in two rounds of columns.
-  static constexpr int R0 = (D == 64) ? 32 : 64;       // columns [0, R0) in round 0, [R0, D) in round 1
+  static constexpr int THREADS = 384;
 };
 
 template <int D, bool CAUSAL>
-__global__ void __launch_bounds__(512, 1)
+__global__ void __launch_bounds__(384, 1)
     bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
                     const __grid_constant__ CUtensorMap tmdK, const __grid_constant__ CUtensorMap tmdV,
-                    const __grid_constant__ CUtensorMap tmdQacc, const BwdParams p) {
+                    const BwdParams p) {
   using T = BwdTraits<D>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const uint32_t base = smem_u32(smem_raw);
@@ -136,24 +112,20 @@ __global__ void __launch_bounds__(512, 1)
   const uint32_t sV = sK + T::TILE_BYTES;
   const uint32_t sQ = sV + T::TILE_BYTES;            // [2]
   const uint32_t sdO = sQ + 2 * T::TILE_BYTES;       // [2]
-  const uint32_t sDS = sdO + 2 * T::TILE_BYTES;      // dS^T, bf16, [keys][queries]
-  const uint32_t sVec = sDS + T::DS_BYTES;           // [2] x {-lse2[128], -D[128]}
+  const uint32_t sVec = sdO + 2 * T::TILE_BYTES;     // [2] x {-lse2[128], -D[128]}
   const uint32_t sBar = sVec + 2 * T::VEC_BYTES;
   const uint32_t bKV = sBar;          // K_j, V_j loaded
   const uint32_t bQf = bKV + 8;       // [2] Q_i + vectors loaded
   const uint32_t bQe = bQf + 16;      // [2] Q stage free (after dK_i)
   const uint32_t bDf = bQe + 16;      // [2] dO_i loaded
-  const uint32_t bDe = bDf + 16;      // [2] dO stage free (after dQ_i left through it)
+  const uint32_t bDe = bDf + 16;      // [2] dO stage free (after dV_i)
   const uint32_t bS = bDe + 16;       // S^T ready
   const uint32_t bP = bS + 8;         // P^T in TMEM (256 arrivals)
   const uint32_t bDp = bP + 8;        // dP^T ready
-  const uint32_t bDs = bDp + 16;      // dS^T in smem (256 arrivals)
-  const uint32_t bDq = bDs + 8;       // dQ_i ready in TMEM
-  const uint32_t bDqe = bDq + 16;     // dQ_i copied out of TMEM (128 arrivals)
-  const uint32_t bStg = bDqe + 16;    // [2] dQ round staged in smem (128 arrivals)
-  const uint32_t bSfree = bStg + 16;  // dO stage free again after round 0 (1 arrival)
-  const uint32_t bFin = bSfree + 8;   // every MMA done
+  const uint32_t bDs = bDp + 8;       // dS^T in TMEM (256 arrivals)
+  const uint32_t bFin = bDs + 8;      // every MMA done
   const uint32_t bDrain = bFin + 8;
+  static_assert(1 + 2 * 4 + 6 <= 16, "barrier count");
   uint8_t* const misc = smem_raw + (sBar - base) + 8 * T::NBAR;
   uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(misc);
   volatile int* const abort_flag = reinterpret_cast<volatile int*>(misc + 4);
@@ -175,21 +147,17 @@ __global__ void __launch_bounds__(512, 1)
       mbar_init(bQe + 8u * s, 1);
       mbar_init(bDf + 8u * s, 1);
       mbar_init(bDe + 8u * s, 1);
-      mbar_init(bStg + 8u * s, 128);
     }
     mbar_init(bS, 1);
-    mbar_init(bDp, 1);
-    mbar_init(bDq, 1);
-    mbar_init(bDqe, 128);
     mbar_init(bP, 256);
+    mbar_init(bDp, 1);
     mbar_init(bDs, 256);
-    mbar_init(bSfree, 1);
     mbar_init(bFin, 1);
     mbar_init(bDrain, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == 13) {
+  if (warp == 9) {
     tmem_alloc(smem_u32(tmem_slot), 512);
     tmem_relinquish();
   }
@@ -200,8 +168,8 @@ __global__ void __launch_bounds__(512, 1)
   const WaitCtx wc{abort_flag, p.status, p.limit_ns, p.info};
 
   if (warp < 8) {
-    setmaxnreg_inc<144>();
-    reg_split_sync(512);
+    setmaxnreg_inc<200>();
+    reg_split_sync(384);
     // ------------------------------------------------------------ compute
     // Warpgroup X handles query columns [64X, 64X + 64) of every score tile
     // for all 128 key rows (thread = key row = TMEM lane).  P^T and dS^T are
@@ -211,7 +179,9 @@ __global__ void __launch_bounds__(512, 1)
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
     const uint32_t tS = tmem + 64 * X + lane_off;           // S^T columns of this half
     const uint32_t tP = tmem + 64 * X + lane_off;           // P^T (bf16 pairs), first 32 of them
-    const uint32_t tdP = tmem + 128 + 64 * X + lane_off;    // dP^T columns of this half
+    const uint32_t tdP = tmem + 128 + 64 * X + lane_off;    // dP^T columns of this half; dS^T pairs after
+    // Key rows past N (the last tile's padding) get P^T = 0.
+    const bool key_pad = j * 128 + r >= p.N;
     const float c = p.scale_log2;
     const float2 c2 = make_float2(c, c);
     bool ok = true;
@@ -239,7 +209,7 @@ __global__ void __launch_bounds__(512, 1)
         }
       }
       // P^T[r][q] = exp2(S^T * scale * log2e - lse2[q]); masked (key > query
-      // on the diagonal tile) entries are exactly 0.
+      // on the diagonal tile) entries and padding key rows are exactly 0.
 #pragma unroll
       for (int q4 = 0; q4 < 16; ++q4) {
         const float4 l4 = *reinterpret_cast<const float4*>(vl + 4 * q4);
@@ -255,6 +225,10 @@ __global__ void __launch_bounds__(512, 1)
         for (int q = 0; q < 64; ++q)
           if (r > 64 * X + q) x[q] = 0.f;
       }
+      if (key_pad) {
+#pragma unroll
+        for (int q = 0; q < 64; ++q) x[q] = 0.f;
+      }
       uint32_t pk[32];  // P^T as bf16 pairs: to TMEM for the dV MMA, kept for dS
 #pragma unroll
       for (int e = 0; e < 32; ++e) pk[e] = pack_bf16(x[2 * e], x[2 * e + 1]);
@@ -262,9 +236,9 @@ __global__ void __launch_bounds__(512, 1)
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(bP);
-      // dS^T[r][q] = P^T[r][q] * (dP^T[r][q] - D[q]) -> bf16 -> smem block X
-      // (128-byte swizzled rows, 16-byte chunk q/8).  The softmax scale is
-      // applied later, to dK in its epilogue and to dQ in the drain.
+      // dS^T[r][q] = P^T[r][q] * (dP^T[r][q] - D[q]) -> bf16 pairs over the
+      // first 32 of this half's dP^T columns.  The softmax scale is applied
+      // to dK in its epilogue.
       ok = __all_sync(0xffffffffu, wait_bounded(wc, bDp, it & 1, wait_site(0x14, it)));
       if (!ok) break;
       tc_fence_after();
@@ -275,9 +249,9 @@ __global__ void __launch_bounds__(512, 1)
       reg_fence(g0);
       reg_fence(g1);
       const float4* Dv = reinterpret_cast<const float4*>(vl + 128);
+      uint32_t w[32];
 #pragma unroll
       for (int q8 = 0; q8 < 8; ++q8) {
-        uint32_t w[4];
         const float4 da = Dv[2 * q8], db = Dv[2 * q8 + 1];
         const float2 dd[4] = {make_float2(da.x, da.y), make_float2(da.z, da.w), make_float2(db.x, db.y),
                               make_float2(db.z, db.w)};
@@ -289,20 +263,20 @@ __global__ void __launch_bounds__(512, 1)
           const uint32_t pp = pk[q >> 1];
           const float2 pf = make_float2(__uint_as_float(pp << 16), __uint_as_float(pp & 0xffff0000u));
           const float2 ds = fmul2(pf, fadd2(make_float2(__uint_as_float(gx), __uint_as_float(gy)), dd[e]));
-          w[e] = pack_bf16(ds.x, ds.y);
+          w[q >> 1] = pack_bf16(ds.x, ds.y);
         }
-        st_shared_v4(sDS + X * T::BLOCK_BYTES + sw128_offset(r, q8), w[0], w[1], w[2], w[3]);
       }
-      fence_proxy_async_smem();
+      tmem_st32(tdP, w);
+      tmem_wait_st();
       tc_fence_before();
       mbar_arrive(bDs);
     }
     // ------------------------------------------------------------ dK / dV out
-    // Warpgroup 0 writes dV (staged in the dS^T tile), warpgroup 1 writes dK
-    // = scale * (dS^T Q) (staged in the K tile); both are free once every MMA
-    // has completed.
+    // Warpgroup 0 writes dV (staged in the V tile), warpgroup 1 writes dK =
+    // scale * (dS^T Q) (staged in the K tile); both tiles are free once every
+    // MMA has completed.
     if (ok) ok = __all_sync(0xffffffffu, wait_bounded(wc, bFin, 0, wait_site(0x13, total)));
-    const uint32_t stage = X ? sK : sDS;
+    const uint32_t stage = X ? sK : sV;
     if (ok) {
       tc_fence_after();
       const uint32_t src = tmem + (X ? 256u : 384u) + lane_off;
@@ -335,94 +309,11 @@ __global__ void __launch_bounds__(512, 1)
       bulk_commit();
       bulk_wait_read_all();
     }
-    setmaxnreg_dec<128>();
-  } else if (warp < 12) {
-    setmaxnreg_dec<120>();
-    reg_split_sync(512);
-    // ------------------------------------------------------------ dQ drain
-    // dQ_i (fp32, scale applied) goes to the accumulator by TMA reductions
-    // from the step's dO stage (idle once dQ_i is final) in two rounds of
-    // columns, [0, R0) then [R0, D).  TMEM is handed back as soon as every
-    // column of dQ_i is staged or held in registers, so the next dP^T can
-    // start while the reductions run; then the dO stage goes back to the
-    // producer.
-    const int q = threadIdx.x - 256;  // query row within the tile == TMEM lane
-    const uint32_t tQ = tmem + 128 + ((uint32_t)((warp - 8) * 32) << 16);
-    const float2 sc2 = make_float2(p.scale, p.scale);  // dQ = scale dS K
-    // 32 columns of one row -> one 128-byte row of a [128 x 32] fp32 box.
-    auto stage_box = [&](const uint32_t (&gg)[32], uint32_t box) {
-#pragma unroll
-      for (int c8 = 0; c8 < 8; ++c8) {
-        const float2 a0 = fmul2(make_float2(__uint_as_float(gg[4 * c8]), __uint_as_float(gg[4 * c8 + 1])), sc2);
-        const float2 a1 = fmul2(make_float2(__uint_as_float(gg[4 * c8 + 2]), __uint_as_float(gg[4 * c8 + 3])), sc2);
-        st_shared_v4(box + sw128_offset(q, c8), __float_as_uint(a0.x), __float_as_uint(a0.y), __float_as_uint(a1.x),
-                     __float_as_uint(a1.y));
-      }
-    };
-    for (int it = 0; it < total; ++it) {
-      const int h = hk * p.G + it / ni, i = i0 + it % ni;
-      const int st = it & 1;
-      const int bh = b * p.H + h;
-      const uint32_t stg = sdO + st * T::TILE_BYTES;
-      if (!__all_sync(0xffffffffu, wait_bounded(wc, bDq, it & 1, wait_site(0x21, it)))) break;
-      tc_fence_after();
-      uint32_t ga[32], gb[32];
-      tmem_ld32(tQ + 0, ga);
-      tmem_ld32(tQ + 32, gb);
-      tmem_wait_ld();
-      reg_fence(ga);
-      reg_fence(gb);
-      if (D == 64) {  // all of dQ_i is in registers
-        tc_fence_before();
-        mbar_arrive(bDqe);
-      }
-      // round 0: columns [0, R0) (32 or 64)
-      stage_box(ga, stg);
-      if (T::R0 == 64) stage_box(gb, stg + T::BLOCK_BYTES);
-      fence_proxy_async_smem();
-      mbar_arrive(bStg);
-      // columns [64, D) to registers; then TMEM is free
-      uint32_t gc[32], gd[32];
-      if (D > 64) {
-        tmem_ld32(tQ + 64, gc);
-        if (D == 128) tmem_ld32(tQ + 96, gd);
-        tmem_wait_ld();
-        reg_fence(gc);
-        if (D == 128) reg_fence(gd);
-        tc_fence_before();
-        mbar_arrive(bDqe);
-      }
-      if (q == 0 && wait_bounded(wc, bStg, it & 1, wait_site(0x22, it))) {
-        tma_reduce_add_3d(&tmdQacc, stg, 0, i * 128, bh);
-        if (T::R0 == 64) tma_reduce_add_3d(&tmdQacc, stg + T::BLOCK_BYTES, 32, i * 128, bh);
-        bulk_commit();
-        bulk_wait_read_all();
-        mbar_arrive(bSfree);
-      }
-      // round 1: columns [R0, D), after the round-0 reduction has read the stage
-      if (!__all_sync(0xffffffffu, wait_bounded(wc, bSfree, it & 1, wait_site(0x24, it)))) break;
-      if (D > 64) {
-        stage_box(gc, stg);
-        if (D == 128) stage_box(gd, stg + T::BLOCK_BYTES);
-      } else {
-        stage_box(gb, stg);
-      }
-      fence_proxy_async_smem();
-      mbar_arrive(bStg + 8u);
-      if (q == 0 && wait_bounded(wc, bStg + 8u, it & 1, wait_site(0x25, it))) {
-        tma_reduce_add_3d(&tmdQacc, stg, T::R0, i * 128, bh);
-        if (D - T::R0 == 64) tma_reduce_add_3d(&tmdQacc, stg + T::BLOCK_BYTES, T::R0 + 32, i * 128, bh);
-        bulk_commit();
-        bulk_wait_read_all();
-        mbar_arrive(bDe + 8u * st);
-      }
-    }
-    if (q == 0) bulk_wait_all();  // every reduction has landed before the CTA exits
-    setmaxnreg_inc<128>();
+    setmaxnreg_dec<168>();
   } else {
     setmaxnreg_dec<104>();
-    reg_split_sync(512);
-    if (warp == 12) {
+    reg_split_sync(384);
+    if (warp == 8) {
       // ------------------------------------------------------------ producer: K, V, Q
       if (lane == 0) {
         tma_prefetch_desc(&tmQ);
@@ -452,7 +343,7 @@ __global__ void __launch_bounds__(512, 1)
           wait_drain(bQf + 8u * st, ((((issued - 1 - st) / 2) * 2 + st) >> 1) & 1, p.limit_ns);
       }
       __syncwarp();
-    } else if (warp == 15) {
+    } else if (warp == 10) {
       // ------------------------------------------------------------ producer: dO
       if (lane == 0) {
         tma_prefetch_desc(&tmdO);
@@ -472,7 +363,7 @@ __global__ void __launch_bounds__(512, 1)
           wait_drain(bDf + 8u * st, ((((issued - 1 - st) / 2) * 2 + st) >> 1) & 1, p.limit_ns);
       }
       __syncwarp();
-    } else if (warp == 13) {
+    } else if (warp == 9) {
       // ------------------------------------------------------------ MMA issuer
       // The whole warp runs the issue loop, so descriptor arithmetic stays
       // warp-uniform; one elected lane issues each tcgen05 instruction.
@@ -480,18 +371,14 @@ __global__ void __launch_bounds__(512, 1)
       {
         const uint32_t leader = elect_one();
         constexpr uint32_t I_SS = idesc_bf16_f32(128, 128, false, false);   // S^T, dP^T (K-major x K-major)
-        constexpr uint32_t I_TB = idesc_bf16_f32(128, D, false, true);      // dV (A in TMEM), dK
-        constexpr uint32_t I_DQ = idesc_bf16_f32(128, D, true, true);       // dQ (both MN-major)
+        constexpr uint32_t I_TB = idesc_bf16_f32(128, D, false, true);      // dV, dK (A in TMEM, B MN-major)
         const uint32_t tS = tmem, tdP = tmem + 128, tdK = tmem + 256, tdV = tmem + 384;
         const uint64_t dKk = sdesc_sw128(sK, 16, 1024);                  // K as K-major A (S^T)
         const uint64_t dVk = sdesc_sw128(sV, 16, 1024);                  // V as K-major A (dP^T)
-        const uint64_t dKmn = sdesc_sw128(sK, T::BLOCK_BYTES, 1024);     // K as MN-major B (dQ)
         const uint64_t dQk0 = sdesc_sw128(sQ, 16, 1024);                 // Q stage 0, K-major B (S^T)
         const uint64_t dQmn0 = sdesc_sw128(sQ, T::BLOCK_BYTES, 1024);    // Q stage 0, MN-major B (dK)
         const uint64_t dOk0 = sdesc_sw128(sdO, 16, 1024);                // dO stage 0, K-major B (dP^T)
         const uint64_t dOmn0 = sdesc_sw128(sdO, T::BLOCK_BYTES, 1024);   // dO stage 0, MN-major B (dV)
-        const uint64_t dSk = sdesc_sw128(sDS, 16, 1024);                 // dS^T as K-major A (dK)
-        const uint64_t dSmn = sdesc_sw128(sDS, T::BLOCK_BYTES, 1024);    // dS as MN-major A (dQ)
         // D[128 x N] = A[128 x d] * B[N x d]^T with both K-major tiles.
         auto mma_kk = [&](uint32_t dst, uint64_t ad, uint64_t bd, uint32_t idesc) {
 #pragma unroll
@@ -503,10 +390,11 @@ __global__ void __launch_bounds__(512, 1)
         auto wait_all = [&](uint32_t bar, uint32_t parity, int site) {
           return __all_sync(0xffffffffu, wait_bounded(wc, bar, parity, site));
         };
-        // Issue order per step i: dV(i), S^T(i+1), dQ(i), dK(i), dP^T(i+1).
-        // S^T(i+1) overwrites P^T(i) in TMEM only after dV(i), issued first
-        // (MMAs from one thread run in order); dK(i) runs while the drain
-        // empties dQ(i) out of the columns dP^T(i+1) then reuses.
+        // Issue order per step i: dV(i), S^T(i+1), dK(i), dP^T(i+1).  S^T(i+1)
+        // overwrites P^T(i) only after dV(i), and dP^T(i+1) overwrites dS^T(i)
+        // only after dK(i): MMAs from one thread run in order.  The A
+        // operands of dV and dK are the bf16 pairs in TMEM: queries 16kk..
+        // of K-step kk sit at column 64 (kk / 4) + 8 (kk % 4).
         bool ok = wait_all(bKV, 0, wait_site(0x41, 0)) && wait_all(bQf, 0, wait_site(0x42, 0)) &&
                   wait_all(bDf, 0, wait_site(0x47, 0));
         if (ok) {
@@ -522,12 +410,12 @@ __global__ void __launch_bounds__(512, 1)
           const uint32_t so = st * T::TILE_BYTES, sno = sn * T::TILE_BYTES;
           if (!(ok = wait_all(bP, it & 1, wait_site(0x44, it)))) break;
           tc_fence_after();
-          // dV += P^T dO_i: A = P^T in TMEM (queries 0-63 at columns 0-31,
-          // 64-127 at columns 64-95), B = dO_i (MN-major)
+          // dV += P^T dO_i: A = P^T in TMEM, B = dO_i (MN-major)
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)
-            mma_ts_p(leader, tdV, tS + (kk < 4 ? kk * 8 : 64 + (kk - 4) * 8), sdesc_add(dOmn0, so + kk * 2048), I_TB,
+            mma_ts_p(leader, tdV, tS + 64 * (kk >> 2) + 8 * (kk & 3), sdesc_add(dOmn0, so + kk * 2048), I_TB,
                      (it > 0 || kk > 0) ? 1u : 0u);
+          mma_commit_p(leader, bDe + 8u * st);  // dO_i no longer needed
           if (nx) {
             if (!(ok = wait_all(bQf + 8u * sn, ((it + 1) >> 1) & 1, wait_site(0x46, it)))) break;
             tc_fence_after();
@@ -536,20 +424,14 @@ __global__ void __launch_bounds__(512, 1)
           }
           if (!(ok = wait_all(bDs, it & 1, wait_site(0x45, it)))) break;
           tc_fence_after();
-          // dQ_i = dS K_j: A = dS (queries contiguous: MN-major), B = K_j (MN-major)
+          // dK += dS^T Q_i: A = dS^T in TMEM, B = Q_i (MN-major)
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)
-            mma_ss_p(leader, tdP, sdesc_add(dSmn, kk * 2048), sdesc_add(dKmn, kk * 2048), I_DQ, kk > 0 ? 1u : 0u);
-          mma_commit_p(leader, bDq);
-          // dK += dS^T Q_i: A = dS^T (K-major over queries), B = Q_i (MN-major)
-#pragma unroll
-          for (int kk = 0; kk < 8; ++kk)
-            mma_ss_p(leader, tdK, sdesc_add(dSk, (kk >> 2) * T::BLOCK_BYTES + (kk & 3) * 32),
-                     sdesc_add(dQmn0, so + kk * 2048), I_TB, (it > 0 || kk > 0) ? 1u : 0u);
+            mma_ts_p(leader, tdK, tdP + 64 * (kk >> 2) + 8 * (kk & 3), sdesc_add(dQmn0, so + kk * 2048), I_TB,
+                     (it > 0 || kk > 0) ? 1u : 0u);
           mma_commit_p(leader, bQe + 8u * st);  // Q_i (and its vectors) no longer needed
           if (nx) {
             if (!(ok = wait_all(bDf + 8u * sn, ((it + 1) >> 1) & 1, wait_site(0x47, it)))) break;
-            if (!(ok = wait_all(bDqe, it & 1, wait_site(0x43, it)))) break;
             tc_fence_after();
             mma_kk(tdP, dVk, sdesc_add(dOk0, sno), I_SS);  // dP^T_{i+1}
             mma_commit_p(leader, bDp);
@@ -561,12 +443,12 @@ __global__ void __launch_bounds__(512, 1)
       }
       __syncwarp();
     }
-    setmaxnreg_inc<128>();
+    setmaxnreg_inc<168>();
   }
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 13) {
+  if (warp == 9) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
@@ -584,12 +466,12 @@ size_t bwd_smem_bytes(int d) {
 template <int D, bool C>
 static cudaError_t launch_main_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                                  const CUtensorMap& tdo, const CUtensorMap& tdk, const CUtensorMap& tdv,
-                                 const CUtensorMap& tdqa, const BwdParams& p, cudaStream_t stream) {
+                                 const BwdParams& p, cudaStream_t stream) {
   auto kern = bwd_main_kernel<D, C>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, BwdTraits<D>::SMEM);
   if (e != cudaSuccess) return e;
   const unsigned grid = (unsigned)p.nq * (unsigned)(p.B * p.Hkv);
-  kern<<<grid, BwdTraits<D>::THREADS, BwdTraits<D>::SMEM, stream>>>(tq, tk, tv, tdo, tdk, tdv, tdqa, p);
+  kern<<<grid, BwdTraits<D>::THREADS, BwdTraits<D>::SMEM, stream>>>(tq, tk, tv, tdo, tdk, tdv, p);
   return cudaGetLastError();
 }
 
@@ -601,22 +483,16 @@ cudaError_t launch_bwd_prep(const BwdParams& p, cudaStream_t stream) {
 
 cudaError_t launch_bwd_grad(int d, bool causal, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                             const CUtensorMap& tdo, const CUtensorMap& tdk, const CUtensorMap& tdv,
-                            const CUtensorMap& tdqa, const BwdParams& p, cudaStream_t stream) {
+                            const BwdParams& p, cudaStream_t stream) {
   switch (d) {
-    case 64: return causal ? launch_main_t<64, true>(tq, tk, tv, tdo, tdk, tdv, tdqa, p, stream)
-                           : launch_main_t<64, false>(tq, tk, tv, tdo, tdk, tdv, tdqa, p, stream);
-    case 96: return causal ? launch_main_t<96, true>(tq, tk, tv, tdo, tdk, tdv, tdqa, p, stream)
-                           : launch_main_t<96, false>(tq, tk, tv, tdo, tdk, tdv, tdqa, p, stream);
-    case 128: return causal ? launch_main_t<128, true>(tq, tk, tv, tdo, tdk, tdv, tdqa, p, stream)
-                            : launch_main_t<128, false>(tq, tk, tv, tdo, tdk, tdv, tdqa, p, stream);
+    case 64: return causal ? launch_main_t<64, true>(tq, tk, tv, tdo, tdk, tdv, p, stream)
+                           : launch_main_t<64, false>(tq, tk, tv, tdo, tdk, tdv, p, stream);
+    case 96: return causal ? launch_main_t<96, true>(tq, tk, tv, tdo, tdk, tdv, p, stream)
+                           : launch_main_t<96, false>(tq, tk, tv, tdo, tdk, tdv, p, stream);
+    case 128: return causal ? launch_main_t<128, true>(tq, tk, tv, tdo, tdk, tdv, p, stream)
+                            : launch_main_t<128, false>(tq, tk, tv, tdo, tdk, tdv, p, stream);
     default: return cudaErrorInvalidValue;
   }
-}
-
-cudaError_t launch_bwd_dq(const BwdParams& p, cudaStream_t stream) {
-  const long long rows = (long long)p.B * p.H * p.N;
-  bwd_convert_kernel<<<(unsigned)((rows + 7) / 8), 256, 0, stream>>>(p);
-  return cudaGetLastError();
 }
 
 }  // namespace sdpa

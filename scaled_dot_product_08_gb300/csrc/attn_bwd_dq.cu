@@ -1,0 +1,383 @@
+// attn_bwd_dq.cu — dQ of exact attention on sm_103a (query-stationary).
+//
+// Method (page "Flash Attention原理：分块计算与重计算，如何降低O(n^2)的显存占用",
+// §五): for one 128-row query tile i of one head, walk the key tiles j (j <= i
+// when causal) and accumulate
+//     S  = Q_i K_j^T,   P = exp2(S * scale * log2 e - lse_i * log2 e),
+//     dP = dO_i V_j^T,  dS = P * (dP - D_i),   dQ_i += dS K_j,
+// with dQ_i in tensor memory for the whole walk and the softmax scale applied
+// once at the end.  Each dQ tile has exactly one writer: no atomics, no
+// accumulator in global memory, and the result does not depend on timing.
+//
+// Warp roles (384 threads):
+//   warps 0-7   compute, two warpgroups: warpgroup X takes key columns
+//               [64X, 64X+64) of each 128 x 128 (queries x keys) tile, one
+//               thread per query row: S -> P (registers), dP -> dS (bf16
+//               pairs back into its S columns, the A operand of the dQ MMA);
+//               then half of the dQ epilogue
+//   warp  8     TMA producer: Q_i, dO_i once; K_j (3-slot ring), V_j (2-slot)
+//   warp  9     MMA issuer (one elected lane issues)
+//   warps 10-11 idle
+// Tensor memory: S[0] [0,128), S[1] [128,256) (double-buffered, so S_{j+2}
+// is computed while step j+1 is in the softmax), dP [256,384), dQ [384,384+d).
+#include <cmath>
+
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace sdpa {
+
+template <int D>
+struct DqTraits {
+  static constexpr int NB = (D + 63) / 64;
+  static constexpr int BLOCK_BYTES = 128 * 128;
+  static constexpr int TILE_BYTES = NB * BLOCK_BYTES;  // one [128 rows x d] bf16 tile
+  static constexpr int KSTEPS = D / 16;
+  static constexpr int KS = 3, VS = 2;                 // K and V ring slots
+  static constexpr int NBAR = 18;
+  static constexpr int SMEM = 1024 + (2 + KS + VS) * TILE_BYTES + NBAR * 8 + 16;
+  static constexpr int THREADS = 384;
+};
+
+template <int D, bool CAUSAL>
+__global__ void __launch_bounds__(384, 1)
+    bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                  const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
+                  const __grid_constant__ CUtensorMap tmdQ, const BwdParams p) {
+  using T = DqTraits<D>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;  // 128-byte swizzle atoms need 1024-byte alignment
+  uint8_t* const gbase = smem_raw + (base - raw);
+
+  const uint32_t sQ = base;                          // Q_i; dQ_i staging at the end
+  const uint32_t sdO = sQ + T::TILE_BYTES;           // dO_i
+  const uint32_t sK = sdO + T::TILE_BYTES;           // [KS] K_j
+  const uint32_t sV = sK + T::KS * T::TILE_BYTES;    // [VS] V_j
+  const uint32_t sBar = sV + T::VS * T::TILE_BYTES;
+  const uint32_t bQ = sBar;                  // Q_i and dO_i loaded
+  const uint32_t bKf = bQ + 8;               // [KS] K slot full
+  const uint32_t bKe = bKf + 8 * T::KS;      // [KS] K slot free (after dQ += dS K_j)
+  const uint32_t bVf = bKe + 8 * T::KS;      // [VS] V slot full
+  const uint32_t bVe = bVf + 8 * T::VS;      // [VS] V slot free (after dP_j)
+  const uint32_t bS = bVe + 8 * T::VS;       // [2] S_j ready in buffer j & 1
+  const uint32_t bDp = bS + 16;              // dP_j ready
+  const uint32_t bDpc = bDp + 8;             // dP_j copied out of TMEM (256 arrivals)
+  const uint32_t bDs = bDpc + 8;             // dS_j in TMEM (256 arrivals)
+  const uint32_t bFin = bDs + 8;             // dQ_i final
+  const uint32_t bDrain = bFin + 8;
+  static_assert(1 + 2 * 3 + 2 * 2 + 2 + 5 == 18, "barrier count");
+  uint8_t* const misc = gbase + (sBar - base) + 8 * T::NBAR;
+  uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(misc);
+  volatile int* const abort_flag = reinterpret_cast<volatile int*>(misc + 4);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // Work unit: head-major (the CTAs in flight share K/V heads in L2); within
+  // a head the longest causal walks go first.
+  const int bh = blockIdx.x / p.nq;
+  const int i = p.nq - 1 - (int)(blockIdx.x % p.nq);  // query tile
+  const int bhk = (bh / p.H) * p.Hkv + (bh % p.H) / p.G;
+  const int n = CAUSAL ? i + 1 : p.nq;                 // key tiles visited
+
+  if (threadIdx.x == 0) {
+    mbar_init(bQ, 1);
+    for (int s = 0; s < T::KS; ++s) {
+      mbar_init(bKf + 8u * s, 1);
+      mbar_init(bKe + 8u * s, 1);
+    }
+    for (int s = 0; s < T::VS; ++s) {
+      mbar_init(bVf + 8u * s, 1);
+      mbar_init(bVe + 8u * s, 1);
+    }
+    mbar_init(bS, 1);
+    mbar_init(bS + 8u, 1);
+    mbar_init(bDp, 1);
+    mbar_init(bDpc, 256);
+    mbar_init(bDs, 256);
+    mbar_init(bFin, 1);
+    mbar_init(bDrain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 9) {
+    tmem_alloc(smem_u32(tmem_slot), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
+  const WaitCtx wc{abort_flag, p.status, p.limit_ns, p.info};
+
+  if (warp < 8) {
+    setmaxnreg_inc<200>();
+    reg_split_sync(384);
+    // ------------------------------------------------------------ compute
+    const int X = warp >> 2;
+    const int r = threadIdx.x & 127;  // query row within the tile == TMEM lane
+    const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+    const uint32_t tdP = tmem + 256 + 64 * X + lane_off;
+    const size_t vrow = (size_t)bh * p.Npad + (size_t)i * 128 + r;
+    const float l2 = p.lse2[vrow];   // -lse * log2(e); -inf on padding rows (P = 0 there)
+    const float nD = p.dvec[vrow];   // -D
+    const float2 c2 = make_float2(p.scale_log2, p.scale_log2);
+    const float2 l22 = make_float2(l2, l2), nD2 = make_float2(nD, nD);
+    bool ok = true;
+    for (int j = 0; j < n; ++j) {
+      const uint32_t tS = tmem + (j & 1) * 128 + 64 * X + lane_off;
+      ok = __all_sync(0xffffffffu, wait_bounded(wc, bS + 8u * (j & 1), (j >> 1) & 1, wait_site(0x81, j)));
+      if (!ok) break;
+      tc_fence_after();
+      float x[64];
+      {
+        uint32_t ra[32], rb[32];
+        tmem_ld32(tS + 0, ra);
+        tmem_ld32(tS + 32, rb);
+        tmem_wait_ld();
+        reg_fence(ra);
+        reg_fence(rb);
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          x[e] = __uint_as_float(ra[e]);
+          x[32 + e] = __uint_as_float(rb[e]);
+        }
+      }
+      // P[r][k] = exp2(S * scale * log2e - lse2[r]); keys past the diagonal
+      // (key > query on the diagonal tile) are exactly 0.
+#pragma unroll
+      for (int e = 0; e < 32; ++e) {
+        const float2 t = ffma2(make_float2(x[2 * e], x[2 * e + 1]), c2, l22);
+        x[2 * e] = ex2(t.x);
+        x[2 * e + 1] = ex2(t.y);
+      }
+      if (CAUSAL && j == i) {
+#pragma unroll
+        for (int k = 0; k < 64; ++k)
+          if (64 * X + k > r) x[k] = 0.f;
+      }
+      ok = __all_sync(0xffffffffu, wait_bounded(wc, bDp, j & 1, wait_site(0x82, j)));
+      if (!ok) break;
+      tc_fence_after();
+      // dS[r][k] = P * (dP - D) -> bf16 pairs over this warpgroup's S columns
+      uint32_t w[32];
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        uint32_t g[32];
+        tmem_ld32(tdP + 32 * hh, g);
+        tmem_wait_ld();
+        reg_fence(g);
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const int k = 32 * hh + 2 * e;
+          const float2 ds = fmul2(make_float2(x[k], x[k + 1]),
+                                  fadd2(make_float2(__uint_as_float(g[2 * e]), __uint_as_float(g[2 * e + 1])), nD2));
+          w[16 * hh + e] = pack_bf16(ds.x, ds.y);
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(bDpc);  // the dP columns may be overwritten
+      tmem_st32(tS, w);
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(bDs);
+    }
+    // ------------------------------------------------------------ dQ out
+    // dQ_i = scale * (sum_j dS K_j) -> bf16 -> the Q tile (dead once every
+    // MMA has completed) -> TMA store.  Warpgroup X takes the 32-column
+    // groups cc with cc % 2 == X.
+    if (ok) ok = __all_sync(0xffffffffu, wait_bounded(wc, bFin, 0, wait_site(0x83, n)));
+    if (ok) {
+      tc_fence_after();
+      const uint32_t tQd = tmem + 384 + lane_off;
+      const float2 s2 = make_float2(p.scale, p.scale);
+#pragma unroll
+      for (int cc = X; cc < D / 32; cc += 2) {
+        uint32_t o[32];
+        tmem_ld32(tQd + cc * 32, o);
+        tmem_wait_ld();
+        reg_fence(o);
+        const int blk = (cc * 32) / 64, ch0 = ((cc * 32) % 64) / 8;
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {
+          uint32_t ww[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float2 t = fmul2(make_float2(__uint_as_float(o[q4 * 8 + 2 * e]), __uint_as_float(o[q4 * 8 + 2 * e + 1])), s2);
+            ww[e] = pack_bf16(t.x, t.y);
+          }
+          st_shared_v4(sQ + blk * T::BLOCK_BYTES + sw128_offset(r, ch0 + q4), ww[0], ww[1], ww[2], ww[3]);
+        }
+      }
+      fence_proxy_async_smem();
+    }
+    named_bar_sync(1, 256);
+    if (ok && threadIdx.x == 0 && i * 128 < p.N) {
+      for (int cb = 0; cb < T::NB; ++cb) tma_store_3d(&tmdQ, sQ + cb * T::BLOCK_BYTES, cb * 64, i * 128, bh);
+      bulk_commit();
+      bulk_wait_all();
+    }
+    setmaxnreg_dec<168>();
+  } else {
+    setmaxnreg_dec<104>();
+    reg_split_sync(384);
+    if (warp == 8) {
+      // ------------------------------------------------------------ producer
+      if (lane == 0) {
+        tma_prefetch_desc(&tmK);
+        tma_prefetch_desc(&tmV);
+        mbar_expect_tx(bQ, 2 * T::TILE_BYTES);
+        for (int cb = 0; cb < T::NB; ++cb) {
+          tma_load_3d(sQ + cb * T::BLOCK_BYTES, &tmQ, bQ, cb * 64, i * 128, bh);
+          tma_load_3d(sdO + cb * T::BLOCK_BYTES, &tmdO, bQ, cb * 64, i * 128, bh);
+        }
+        int issued = 0;
+        for (int j = 0; j < n; ++j) {
+          const int ks = j % T::KS, kr = j / T::KS, vs = j % T::VS, vr = j / T::VS;
+          if (kr > 0 && !wait_bounded(wc, bKe + 8u * ks, (kr - 1) & 1, wait_site(0x91, j))) break;
+          mbar_expect_tx(bKf + 8u * ks, T::TILE_BYTES);
+          for (int cb = 0; cb < T::NB; ++cb)
+            tma_load_3d(sK + ks * T::TILE_BYTES + cb * T::BLOCK_BYTES, &tmK, bKf + 8u * ks, cb * 64, j * 128, bhk);
+          issued = 2 * j + 1;
+          if (vr > 0 && !wait_bounded(wc, bVe + 8u * vs, (vr - 1) & 1, wait_site(0x92, j))) break;
+          mbar_expect_tx(bVf + 8u * vs, T::TILE_BYTES);
+          for (int cb = 0; cb < T::NB; ++cb)
+            tma_load_3d(sV + vs * T::TILE_BYTES + cb * T::BLOCK_BYTES, &tmV, bVf + 8u * vs, cb * 64, j * 128, bhk);
+          issued = 2 * j + 2;
+        }
+        // Every copy issued above has landed before the CTA may exit.
+        wait_drain(bQ, 0, p.limit_ns);
+        const int nk = (issued + 1) / 2, nv = issued / 2;  // K_0..K_{nk-1}, V_0..V_{nv-1} issued
+        for (int s = 0; s < T::KS && s < nk; ++s) {
+          const int last = ((nk - 1 - s) / T::KS) * T::KS + s;
+          wait_drain(bKf + 8u * s, (last / T::KS) & 1, p.limit_ns);
+        }
+        for (int s = 0; s < T::VS && s < nv; ++s) {
+          const int last = ((nv - 1 - s) / T::VS) * T::VS + s;
+          wait_drain(bVf + 8u * s, (last / T::VS) & 1, p.limit_ns);
+        }
+      }
+      __syncwarp();
+    } else if (warp == 9) {
+      // ------------------------------------------------------------ MMA issuer
+      // Per step j: dP_{j+1} (once dP_j has been read), dQ += dS_j K_j,
+      // S_{j+2} into the S buffer dS_j occupied (MMAs from one thread run in
+      // order, so dQ has read dS_j first).
+      {
+        const uint32_t leader = elect_one();
+        constexpr uint32_t I_SS = idesc_bf16_f32(128, 128, false, false);  // S, dP (K-major x K-major)
+        constexpr uint32_t I_DQ = idesc_bf16_f32(128, D, false, true);     // dQ (A in TMEM, B MN-major)
+        const uint32_t tdP = tmem + 256, tdQ = tmem + 384;
+        const uint64_t dQk = sdesc_sw128(sQ, 16, 1024);                 // Q, K-major A
+        const uint64_t dOk = sdesc_sw128(sdO, 16, 1024);                // dO, K-major A
+        const uint64_t dKk0 = sdesc_sw128(sK, 16, 1024);                // K slot 0, K-major B (S)
+        const uint64_t dKmn0 = sdesc_sw128(sK, T::BLOCK_BYTES, 1024);   // K slot 0, MN-major B (dQ)
+        const uint64_t dVk0 = sdesc_sw128(sV, 16, 1024);                // V slot 0, K-major B (dP)
+        auto mma_kk = [&](uint32_t dst, uint64_t ad, uint64_t bd, uint32_t idesc) {
+#pragma unroll
+          for (int kk = 0; kk < T::KSTEPS; ++kk) {
+            const uint32_t off = (kk >> 2) * T::BLOCK_BYTES + (kk & 3) * 32;
+            mma_ss_p(leader, dst, sdesc_add(ad, off), sdesc_add(bd, off), idesc, kk > 0);
+          }
+        };
+        auto wait_all = [&](uint32_t bar, uint32_t parity, int site) {
+          return __all_sync(0xffffffffu, wait_bounded(wc, bar, parity, site));
+        };
+        bool ok = wait_all(bQ, 0, wait_site(0xa1, 0)) && wait_all(bKf, 0, wait_site(0xa2, 0)) &&
+                  wait_all(bVf, 0, wait_site(0xa3, 0));
+        if (ok) {
+          tc_fence_after();
+          mma_kk(tmem, dQk, dKk0, I_SS);  // S_0
+          mma_commit_p(leader, bS);
+          mma_kk(tdP, dOk, dVk0, I_SS);  // dP_0
+          mma_commit_p(leader, bDp);
+          mma_commit_p(leader, bVe);  // V_0 consumed
+          if (n > 1) {
+            ok = wait_all(bKf + 8u, 0, wait_site(0xa4, 1));
+            if (ok) {
+              tc_fence_after();
+              mma_kk(tmem + 128, dQk, sdesc_add(dKk0, T::TILE_BYTES), I_SS);  // S_1
+              mma_commit_p(leader, bS + 8u);
+            }
+          }
+        }
+        for (int j = 0; j < n && ok; ++j) {
+          if (j + 1 < n) {
+            const int vs = (j + 1) % T::VS;
+            if (!(ok = wait_all(bVf + 8u * vs, ((j + 1) / T::VS) & 1, wait_site(0xa5, j)))) break;
+            if (!(ok = wait_all(bDpc, j & 1, wait_site(0xa6, j)))) break;
+            tc_fence_after();
+            mma_kk(tdP, dOk, sdesc_add(dVk0, vs * T::TILE_BYTES), I_SS);  // dP_{j+1}
+            mma_commit_p(leader, bDp);
+            mma_commit_p(leader, bVe + 8u * vs);
+          }
+          if (!(ok = wait_all(bDs, j & 1, wait_site(0xa7, j)))) break;
+          tc_fence_after();
+          // dQ += dS_j K_j: A = dS in TMEM (keys 64X.. of warpgroup X at
+          // columns 64X.., bf16 pairs), B = K_j (MN-major, N = d)
+          const int ks = j % T::KS;
+          const uint32_t tS = tmem + (j & 1) * 128;
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            mma_ts_p(leader, tdQ, tS + 64 * (kk >> 2) + (kk & 3) * 8,
+                     sdesc_add(dKmn0, ks * T::TILE_BYTES + kk * 2048), I_DQ, (j > 0 || kk > 0) ? 1u : 0u);
+          mma_commit_p(leader, bKe + 8u * ks);  // K_j consumed
+          if (j + 2 < n) {
+            const int k2 = (j + 2) % T::KS;
+            if (!(ok = wait_all(bKf + 8u * k2, ((j + 2) / T::KS) & 1, wait_site(0xa8, j)))) break;
+            tc_fence_after();
+            mma_kk(tS, dQk, sdesc_add(dKk0, k2 * T::TILE_BYTES), I_SS);  // S_{j+2}
+            mma_commit_p(leader, bS + 8u * (j & 1));
+          }
+        }
+        if (ok) mma_commit_p(leader, bFin);
+        mma_commit_p(leader, bDrain);  // fires once every MMA issued above has finished
+        wait_drain(bDrain, 0, p.limit_ns);
+      }
+      __syncwarp();
+    }
+    setmaxnreg_inc<168>();
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 9) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+size_t bwd_dq_smem_bytes(int d) {
+  switch (d) {
+    case 64: return DqTraits<64>::SMEM;
+    case 96: return DqTraits<96>::SMEM;
+    case 128: return DqTraits<128>::SMEM;
+    default: return 0;
+  }
+}
+
+template <int D, bool C>
+static cudaError_t launch_dq_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                               const CUtensorMap& tdo, const CUtensorMap& tdq, const BwdParams& p,
+                               cudaStream_t stream) {
+  auto kern = bwd_dq_kernel<D, C>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, DqTraits<D>::SMEM);
+  if (e != cudaSuccess) return e;
+  const unsigned grid = (unsigned)p.nq * (unsigned)(p.B * p.H);
+  kern<<<grid, DqTraits<D>::THREADS, DqTraits<D>::SMEM, stream>>>(tq, tk, tv, tdo, tdq, p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_dq(int d, bool causal, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                          const CUtensorMap& tdo, const CUtensorMap& tdq, const BwdParams& p, cudaStream_t stream) {
+  switch (d) {
+    case 64: return causal ? launch_dq_t<64, true>(tq, tk, tv, tdo, tdq, p, stream)
+                           : launch_dq_t<64, false>(tq, tk, tv, tdo, tdq, p, stream);
+    case 96: return causal ? launch_dq_t<96, true>(tq, tk, tv, tdo, tdq, p, stream)
+                           : launch_dq_t<96, false>(tq, tk, tv, tdo, tdq, p, stream);
+    case 128: return causal ? launch_dq_t<128, true>(tq, tk, tv, tdo, tdq, p, stream)
+                            : launch_dq_t<128, false>(tq, tk, tv, tdo, tdq, p, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace sdpa

@@ -26,10 +26,8 @@ struct BwdParams {
   const uint16_t* o;     // (B, H, N, d) bf16
   const uint16_t* dout;  // (B, H, N, d) bf16
   const float* lse;      // (B, H, N)
-  uint16_t* dq;          // (B, H, N, d) bf16
-  float* dq_acc;         // (B, H, Npad, d) float32 workspace
-  float* dvec;           // (B, H, Npad) float32: D = rowsum(dO * O)
-  float* lse2;           // (B, H, Npad) float32: lse * log2(e), +inf on padding rows
+  float* dvec;           // (B, H, Npad) float32 workspace: -D = -rowsum(dO * O)
+  float* lse2;           // (B, H, Npad) float32 workspace: -lse * log2(e), -inf on padding rows
   int B, H, Hkv, N, Npad, G, d;
   int nq;                // ceil(N / 128)
   float scale;           // softmax scale
@@ -42,6 +40,7 @@ struct BwdParams {
 // Shared-memory bytes of each kernel instance (for validation and launch).
 size_t fwd_smem_bytes(int d);
 size_t bwd_smem_bytes(int d);
+size_t bwd_dq_smem_bytes(int d);
 
 cudaError_t launch_fwd(int d, bool causal, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                        const CUtensorMap& to, const FwdParams& p, cudaStream_t stream);
@@ -49,7 +48,8 @@ cudaError_t launch_fwd(int d, bool causal, const CUtensorMap& tq, const CUtensor
 cudaError_t launch_bwd_prep(const BwdParams& p, cudaStream_t stream);
 cudaError_t launch_bwd_grad(int d, bool causal, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                             const CUtensorMap& tdo, const CUtensorMap& tdk, const CUtensorMap& tdv,
-                            const CUtensorMap& tdqa, const BwdParams& p, cudaStream_t stream);
-cudaError_t launch_bwd_dq(const BwdParams& p, cudaStream_t stream);
+                            const BwdParams& p, cudaStream_t stream);
+cudaError_t launch_bwd_dq(int d, bool causal, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                          const CUtensorMap& tdo, const CUtensorMap& tdq, const BwdParams& p, cudaStream_t stream);
 
 }  // namespace sdpa

@@ -40,14 +40,14 @@ def test_status_strings(lib):
     for s in sdpa.Status:
         assert sdpa.attn_status_string(int(s)) == "ATTN_" + ("OK" if s == 0 else "ERR_" + s.name)
     assert sdpa.attn_status_string(99) == "ATTN_ERR_UNKNOWN"
-    assert lib.attn_abi_version() == 1
+    assert lib.attn_abi_version() == 2
 
 
 def test_workspace_size_formula(lib):
     import scaled_dot_product_08_gb300 as sdpa
-    # float32 dQ accumulator (B*H*Npad*d) + two float32 row vectors (B*H*Npad)
-    assert sdpa.attn_bwd_workspace_size(8, 16, 16, 4096, 128) == 8 * 16 * 4096 * (128 + 2) * 4
-    assert sdpa.attn_bwd_workspace_size(1, 2, 1, 129, 64) == 2 * 256 * (64 + 2) * 4
+    # two float32 row vectors (-D and -lse*log2 e) of B*H*Npad rows each
+    assert sdpa.attn_bwd_workspace_size(8, 16, 16, 4096, 128) == 8 * 16 * 4096 * 2 * 4
+    assert sdpa.attn_bwd_workspace_size(1, 2, 1, 129, 64) == 2 * 256 * 2 * 4
     assert sdpa.attn_bwd_workspace_size(1, 3, 2, 128, 64) == 0      # H % Hkv != 0
     assert sdpa.attn_bwd_workspace_size(1, 2, 2, 128, 80) == 0      # unsupported d
     assert sdpa.attn_bwd_workspace_size(1, 2, 2, 0, 64) == 0

@@ -142,15 +142,16 @@ def test_backward_stages_equal_the_combined_call(cuda_lib):
                                   B, H, Hkv, N, d, sp) == 0
     assert cuda_lib.attn_bwd_grad(q.data_ptr(), k.data_ptr(), v.data_ptr(), do.data_ptr(), dk.data_ptr(),
                                   dv.data_ptr(), ws.data_ptr(), ws_bytes, B, H, Hkv, N, d, 0.1, 0, sp) == 0
-    assert cuda_lib.attn_bwd_dq(dq.data_ptr(), ws.data_ptr(), ws_bytes, B, H, Hkv, N, d, sp) == 0
+    assert cuda_lib.attn_bwd_dq(q.data_ptr(), k.data_ptr(), v.data_ptr(), do.data_ptr(), dq.data_ptr(),
+                                ws.data_ptr(), ws_bytes, B, H, Hkv, N, d, 0.1, 0, sp) == 0
     got = [host(g) for g in (dq, dk, dv)]
-    assert np.array_equal(got[1], ref[1]) and np.array_equal(got[2], ref[2])
-    assert rel_fro(got[0], ref[0]) < 1e-2
+    for g, r in zip(got, ref):
+        assert np.array_equal(g, r)
 
 
-def test_backward_is_deterministic_in_dk_dv(cuda_lib):
-    # dK and dV accumulate in tensor memory in a fixed order: bit-identical
-    # across runs.  dQ uses float32 atomics and may differ in the last bits.
+def test_backward_is_deterministic(cuda_lib):
+    # dK, dV (per key tile) and dQ (per query tile) each accumulate in tensor
+    # memory in a fixed order and have one writer: bit-identical across runs.
     B, H, Hkv, N, d = 1, 4, 2, 700, 128
     q = make_random((B, H, N, d), 101)
     k = make_random((B, Hkv, N, d), 102)
@@ -158,5 +159,5 @@ def test_backward_is_deterministic_in_dk_dv(cuda_lib):
     do = make_random((B, H, N, d), 104)
     g1 = _run(cuda_lib, q, k, v, do, 0.1, True)
     g2 = _run(cuda_lib, q, k, v, do, 0.1, True)
-    assert np.array_equal(g1[1], g2[1]) and np.array_equal(g1[2], g2[2])
-    assert rel_fro(g1[0], g2[0]) < 1e-2
+    for a, b in zip(g1, g2):
+        assert np.array_equal(a, b)

@@ -52,10 +52,10 @@ def test_noalloc_backward_matches_attn_bwd_on_two_calls_in_a_row(cuda_lib):
 
 
 def test_noalloc_refuses_shapes_beyond_its_fixed_scratch(cuda_lib):
-    # B=8, H=16, N=4096, d=128 needs 272 MB of workspace, more than the 64 MiB
-    # scratch: refused before anything is read or launched.
-    assert cuda_lib.attn_bwd_workspace_size(8, 16, 16, 4096, 128) > 64 << 20
+    # B=16, H=32, N=32768, d=128 needs 128 MiB of workspace, more than the
+    # 64 MiB scratch: refused before anything is read or launched.
+    assert cuda_lib.attn_bwd_workspace_size(16, 32, 32, 32768, 128) > 64 << 20
     fake = 0x10000
     st = cuda_lib.attn_bwd_noalloc(fake, fake, fake, fake, fake, fake, fake, fake, fake,
-                                   8, 16, 16, 4096, 128, 0.1, 1, None)
+                                   16, 32, 32, 32768, 128, 0.1, 1, None)
     assert st == cuda_lib.Status.WORKSPACE
