@@ -29,6 +29,8 @@ from .sdpa import (
     attention_forward_rows,
     attention_forward_online,
     attention_backward,
+    attention_decode,
+    merge_splits,
     softmax_rows,
     softmax_two_block,
     gqa_kv_head,
@@ -41,6 +43,8 @@ __all__ = [
     "attention_forward_rows",
     "attention_forward_online",
     "attention_backward",
+    "attention_decode",
+    "merge_splits",
     "softmax_rows",
     "softmax_two_block",
     "gqa_kv_head",

@@ -40,19 +40,20 @@ def _check(q, k, v):
     return B, H, k.shape[1], N, k.shape[2], d
 
 
-def _scores(qh, kh, scale, causal, rows=None):
+def _scores(qh, kh, scale, causal, rows=None, q_offset=0):
     """S = scale * Q K^T for one head, with the causal mask applied.
 
     [FA] §一 step 1-2 (S = Q K^T, softmax of S / sqrt(d)); the causal mask of
-    [SDPA] §3 (is_causal=True) sets S_ij = -inf for key j > query i (queries
-    and keys share positions 0..N-1).  ``rows`` selects absolute query rows.
+    [SDPA] §3 (is_causal=True) sets S_ij = -inf for key j > query position
+    i.  Query row i sits at position q_offset + i (0 when queries and keys
+    share positions 0..N-1).  ``rows`` selects query rows.
     """
     if rows is None:
         rows = np.arange(qh.shape[0])
     S = scale * (qh[rows] @ kh.T)
     if causal:
         cols = np.arange(kh.shape[0])
-        S = np.where(cols[None, :] > np.asarray(rows)[:, None], -np.inf, S)
+        S = np.where(cols[None, :] > q_offset + np.asarray(rows)[:, None], -np.inf, S)
     return S
 
 
@@ -87,13 +88,15 @@ def softmax_two_block(x):
     return np.concatenate([np.exp(x1 - m) / l, np.exp(x2 - m) / l], axis=-1)
 
 
-def attention_forward(q, k, v, scale=None, causal=False):
+def attention_forward(q, k, v, scale=None, causal=False, q_offset=0):
     """O = softmax(scale * Q K^T [+ causal mask]) V and lse, in float64.
 
     [FA] §一 (standard attention: S, P and O materialised per head) with the
     stable softmax of §四.  lse_i = m_i + ln(l_i) is the natural-log
     logsumexp of row i of the scaled, masked scores: the single per-row
-    statistic that replaces the m and l of §五.
+    statistic that replaces the m and l of §五.  Query row i sits at
+    position q_offset + i for the causal mask.  A row whose keys are all
+    masked has lse = -inf and O = 0.
     Returns O (B, H, N, d_v) and lse (B, H, N).
     """
     q = np.asarray(q, dtype=np.float64)
@@ -107,10 +110,54 @@ def attention_forward(q, k, v, scale=None, causal=False):
     for b in range(B):
         for h in range(H):
             hk = gqa_kv_head(h, H, Hkv)
-            S = _scores(q[b, h], k[b, hk], scale, causal)
-            P, m, l = softmax_rows(S)
+            S = _scores(q[b, h], k[b, hk], scale, causal, q_offset=q_offset)
+            live = np.isfinite(S).any(axis=1)
+            P = np.zeros_like(S)
+            m = np.full(S.shape[0], -np.inf)
+            l = np.zeros(S.shape[0])
+            if live.any():
+                P[live], m[live], l[live] = softmax_rows(S[live])
             O[b, h] = P @ v[b, hk]
-            lse[b, h] = m + np.log(l)
+            with np.errstate(divide="ignore"):
+                lse[b, h] = m + np.log(l)
+    return O, lse
+
+
+def attention_decode(q, k, v, scale=None, causal=False):
+    """Attention of a block of Nq new queries against a cache of Nk >= Nq
+    keys/values (decode with a KV cache).
+
+    The pages place decode next to prefill ([FA] FAQ on inference, KV cache
+    and P99 decode latency) without a formula; the computation is the same
+    softmax(scale * Q K^T) V over every cached key.  Reading taken for the
+    causal mask: the new queries are the last Nq positions of the sequence,
+    so query t sits at position Nk - Nq + t and sees keys 0..Nk-Nq+t (with
+    Nq = Nk this is the ordinary causal mask).
+    Returns O (B, H, Nq, d_v) and lse (B, H, Nq)."""
+    Nq, Nk = np.shape(q)[2], np.shape(k)[2]
+    if Nq > Nk:
+        raise ValueError("decode needs Nq <= Nk")
+    return attention_forward(q, k, v, scale, causal, q_offset=Nk - Nq)
+
+
+def merge_splits(O_parts, lse_parts):
+    """Combine attention computed over disjoint key ranges ("splits").
+
+    The two-block merge of [FA] §四 for any number of blocks, on normalised
+    partial results: with lse_s the logsumexp of split s and O_s its
+    normalised output, lse = ln sum_s exp(lse_s) and
+    O = sum_s exp(lse_s - lse) O_s.  Splits with lse_s = -inf (every key
+    masked) carry weight 0.
+    O_parts: (S, ..., d), lse_parts: (S, ...).  Returns O (..., d), lse (...)."""
+    O_parts = np.asarray(O_parts, dtype=np.float64)
+    lse_parts = np.asarray(lse_parts, dtype=np.float64)
+    m = lse_parts.max(axis=0)
+    safe = np.where(np.isfinite(m), m, 0.0)
+    w = np.exp(lse_parts - safe)
+    tot = w.sum(axis=0)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        lse = np.where(tot > 0, safe + np.log(tot), -np.inf)
+        O = np.where(tot[..., None] > 0, (w[..., None] * O_parts).sum(axis=0) / np.where(tot > 0, tot, 1.0)[..., None], 0.0)
     return O, lse
 
 
