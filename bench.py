@@ -399,6 +399,119 @@ def run_ours(args, w, rank, world, local_rank):
         print(json.dumps(line), flush=True)
 
 
+def decode_bytes(w):
+    """Algorithmic HBM bytes of one decode call: read K and V of the cache
+    and Q; write O and lse (the chunk partials stay on chip or in L2)."""
+    kv = 2 * w.B * w.Hkv * w.N * w.d * 2
+    qo = 2 * w.B * w.H * w.n_queries * w.d * 2 + w.B * w.H * w.n_queries * 4
+    return kv + qo
+
+
+def run_decode(args, w, rank, world, local_rank):
+    """Decode against a resident KV cache (workloads with Nq set): one step
+    is one attn_decode call (chunk pass + merge).  The value is HBM bytes per
+    second; e2e copies the step's new queries in and O, lse out (the cache
+    stays on the device, as it does across decode steps)."""
+    import torch
+    import scaled_dot_product_08_gb300 as sdpa
+    from sdpa_inputs import make_inputs
+    import oracle
+
+    sdpa.build()
+    sdpa.load()
+    torch.cuda.set_device(local_rank)
+    x = make_inputs(w)
+    dev = lambda a: torch.from_numpy(a).to(torch.bfloat16).cuda()
+    q, k, v = dev(x["q"]), dev(x["k"]), dev(x["v"])
+    B, H, Hkv, Nq, Nk, d = w.B, w.H, w.Hkv, w.n_queries, w.N, w.d
+    s = w.softmax_scale
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, Nq), dtype=torch.float32, device="cuda")
+    ws_bytes = sdpa.attn_decode_workspace_size(B, H, Hkv, Nq, Nk, d)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+    sp = stream.cuda_stream
+
+    def step():
+        st = sdpa.attn_decode(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                              ws.data_ptr(), ws_bytes, B, H, Hkv, Nq, Nk, d, s, w.causal, sp)
+        if st != 0:
+            raise RuntimeError(f"attn_decode: {sdpa.attn_status_string(st)}")
+
+    for _ in range(max(args.warmup, 1)):
+        step()
+    torch.cuda.synchronize()
+    K = args.steps
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    time.sleep(0.3)
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(K):
+        step()
+    b.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    ms = max_over_ranks(a.elapsed_time(b))
+    st = sdpa.attn_get_device_status(None)
+    if st != 0:
+        raise RuntimeError(f"device status after timed steps: {sdpa.attn_status_string(st)}")
+    nbytes = decode_bytes(w)
+    value = world * nbytes * K / (ms / 1e3) / 1e9
+    peaks, peak_src = load_peaks()
+    peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    per_call = nbytes / (ms / K / 1e3) / 1e9
+    roof = {"kernel": "attn_decode (decode_split_kernel + decode_merge_kernel)", "bound": "hbm",
+            "achieved": per_call, "peak": peak, "unit": "GB/s", "frac": per_call / peak,
+            "peak_source": f"{peak_src} copy bandwidth", "traffic": traffic_of("attn_decode", w.name)}
+
+    e2e = None
+    if not args.no_e2e:
+        hq = q.cpu().pin_memory()
+        ho = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+        hl = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+        Ke = max(3, min(K, 50))
+        for _ in range(2):
+            q.copy_(hq, non_blocking=True); step(); ho.copy_(o, non_blocking=True); hl.copy_(lse, non_blocking=True)
+        torch.cuda.synchronize()
+        a.record(stream)
+        for _ in range(Ke):
+            q.copy_(hq, non_blocking=True); step(); ho.copy_(o, non_blocking=True); hl.copy_(lse, non_blocking=True)
+        b.record(stream)
+        torch.cuda.synchronize()
+        ems = max_over_ranks(a.elapsed_time(b))
+        e2e = {"value": world * nbytes * Ke / (ems / 1e3) / 1e9, "unit": "GB/s",
+               "h2d_bytes_per_step": hq.numel() * 2, "d2h_bytes_per_step": ho.numel() * 2 + hl.numel() * 4,
+               "ms_per_step": ems / Ke, "steps": Ke,
+               "note": "new queries in, O and lse out; the KV cache stays resident between decode steps"}
+
+    cb = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        nb = 1
+        t0 = time.perf_counter()
+        oracle.attention_decode(x["q"][:nb], x["k"][:nb], x["v"][:nb], s, w.causal)
+        dt = time.perf_counter() - t0
+        frac = nb / B
+        cb = {"value": decode_bytes(w) * frac / dt / 1e9, "unit": "GB/s", "cores": _blas_threads(), "kind": "oracle",
+              "sample": f"batch element 0 of {w.name} (all {H} heads, Nq={Nq}, Nk={Nk}) in float64 numpy, {dt:.1f} s"}
+
+    if rank == 0:
+        line = {
+            "metric": "attention decode (KV cache, split over keys) HBM bandwidth", "value": value, "unit": "GB/s",
+            "n_gpus": world, "steps": K, "warmup": args.warmup, "ms_per_step": ms / K, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded N(0,1) draws rounded to bf16)",
+            "config": {"workload": f"{w.name}: B={B} H={H} Hkv={Hkv} Nq={Nq} Nk={Nk} d={d} "
+                                   f"{'causal' if w.causal else 'non-causal'} decode",
+                       "B": B, "H": H, "Hkv": Hkv, "Nq": Nq, "Nk": Nk, "d": d, "causal": w.causal,
+                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                       "l2": "no flush: the K/V cache (%.0f MB) is larger than the 129 MB L2" % (2 * B * Hkv * Nk * d * 2 / 1e6)},
+            "roofline": roof, "cpu_baseline": cb, "e2e": e2e, "clocks": clk, "gpu_launches": 2 * K,
+        }
+        print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse_args()
     from sdpa_inputs import workload
@@ -415,7 +528,10 @@ def main():
         torch.cuda.set_device(local_rank)
         dist.init_process_group("nccl")
     try:
-        run_ours(args, w, rank, world, local_rank)
+        if w.Nq is not None:
+            run_decode(args, w, rank, world, local_rank)
+        else:
+            run_ours(args, w, rank, world, local_rank)
     finally:
         if world > 1:
             import torch.distributed as dist

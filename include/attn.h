@@ -130,6 +130,32 @@ attn_status_t attn_bwd_dq(const void* q, const void* k, const void* v, const voi
                           void* stream);
 
 /*
+ * Decode: attention of Nq new queries per head against a cache of Nk keys
+ * and values (a KV cache), computed in key chunks that are merged by their
+ * logsumexp.  Page "Flash Attention原理", FAQ on inference (the KV cache moves
+ * the work into decode steps, profiled apart from prefill); the merge is the
+ * two-block merge of §四 applied to any number of chunks.
+ *   q    [in]  bf16 (B, H, Nq, d)     the new queries
+ *   k, v [in]  bf16 (B, Hkv, Nk, d)   the cache; every position is valid
+ *   o    [out] bf16 (B, H, Nq, d)     softmax(scale * q K^T [+ mask]) V
+ *   lse  [out] float32 (B, H, Nq)     natural-log logsumexp of each query's
+ *                                     scaled, masked scores
+ *   causal     0: each query sees all Nk keys.  1: query t (0-based) of the
+ *              block sits at position Nk - Nq + t, i.e. the new tokens end
+ *              the sequence, and sees keys 0 .. Nk - Nq + t.
+ *   workspace  device buffer of at least attn_decode_workspace_size() bytes,
+ *              owned by the caller; its contents on entry are ignored.
+ * Limits: 1 <= Nq <= Nk; (H / Hkv) * Nq <= 64 query rows per K/V head;
+ * d in {64, 96, 128}.  Two kernels run on `stream` (chunk pass, merge); the
+ * chunk count depends only on the shape.  Bound by the HBM read of K and V.
+ */
+size_t attn_decode_workspace_size(int B, int H, int Hkv, int Nq, int Nk, int d);
+attn_status_t attn_decode(const void* q, const void* k, const void* v, void* o, float* lse,
+                          void* workspace, size_t workspace_bytes,
+                          int B, int H, int Hkv, int Nq, int Nk, int d, float scale, int causal,
+                          void* stream);
+
+/*
  * Synchronises `stream`, then returns (and clears) the device status word
  * that the kernels set when a bounded wait runs out: ATTN_OK or
  * ATTN_ERR_TIMEOUT; ATTN_ERR_CUDA if the synchronisation itself failed.

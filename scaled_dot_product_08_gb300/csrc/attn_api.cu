@@ -2,6 +2,7 @@
 // TMA tensor-map construction, device checks, the device status word and the
 // bounded-wait self-test.  No computation happens here; every step of the
 // attention path runs in the kernels of attn_fwd.cu / attn_bwd.cu.
+#include <algorithm>
 #include <cmath>
 #include <cstdint>
 #include <cstdlib>
@@ -324,6 +325,72 @@ attn_status_t attn_bwd(const void* q, const void* k, const void* v, const void* 
   ATTN_TRY(attn_bwd_prep(o, lse, dout, workspace, workspace_bytes, B, H, Hkv, N, d, stream));
   ATTN_TRY(attn_bwd_grad(q, k, v, dout, dk, dv, workspace, workspace_bytes, B, H, Hkv, N, d, scale, causal, stream));
   return attn_bwd_dq(q, k, v, dout, dq, workspace, workspace_bytes, B, H, Hkv, N, d, scale, causal, stream);
+}
+
+// Key chunks of the decode kernel, a pure function of the shape (so the
+// workspace size needs no device query): chunks of whole 128-key tiles, at
+// most four tiles each, and enough chunks for ~1024 CTAs over B * Hkv when
+// the cache is short.
+static void decode_plan(int B, int Hkv, int Nk, int* nsplit, int* split_keys) {
+  const int tiles = (Nk + 127) / 128;
+  const long long bh = (long long)B * Hkv;
+  const long long want = std::max<long long>((tiles + 3) / 4, (1024 + bh - 1) / bh);
+  const int ns0 = (int)std::min<long long>(tiles, want);
+  const int per = (tiles + ns0 - 1) / ns0;  // tiles per chunk
+  *nsplit = (tiles + per - 1) / per;
+  *split_keys = per * 128;
+}
+
+static attn_status_t check_decode_shape(int B, int H, int Hkv, int Nq, int Nk, int d) {
+  if (B < 1 || H < 1 || Hkv < 1 || Nq < 1 || Nk < 1 || Nq > Nk) return ATTN_ERR_UNSUPPORTED_SHAPE;
+  if (d != 64 && d != 96 && d != 128) return ATTN_ERR_UNSUPPORTED_SHAPE;
+  if (H % Hkv != 0 || (long long)(H / Hkv) * Nq > sdpa::kDecMaxRows) return ATTN_ERR_UNSUPPORTED_SHAPE;
+  if ((long long)B * H * Nq > (1ll << 31) / 8 || (long long)B * Hkv > 65535) return ATTN_ERR_UNSUPPORTED_SHAPE;
+  return ATTN_OK;
+}
+
+size_t attn_decode_workspace_size(int B, int H, int Hkv, int Nq, int Nk, int d) {
+  if (check_decode_shape(B, H, Hkv, Nq, Nk, d) != ATTN_OK) return 0;
+  int nsplit = 0, split_keys = 0;
+  decode_plan(B, Hkv, Nk, &nsplit, &split_keys);
+  const size_t rows = (size_t)B * H * Nq * (size_t)nsplit;
+  return rows * (size_t)d * 4 + rows * 4;  // partial O, then partial lse
+}
+
+attn_status_t attn_decode(const void* q, const void* k, const void* v, void* o, float* lse, void* workspace,
+                          size_t workspace_bytes, int B, int H, int Hkv, int Nq, int Nk, int d, float scale,
+                          int causal, void* stream) {
+  ATTN_TRY(check_decode_shape(B, H, Hkv, Nq, Nk, d));
+  ATTN_TRY(check_scale_flag(scale, causal));
+  if (workspace == nullptr || workspace_bytes < attn_decode_workspace_size(B, H, Hkv, Nq, Nk, d))
+    return ATTN_ERR_WORKSPACE;
+  ATTN_TRY(check_ptrs({q, k, v, o, lse, workspace}));
+  DeviceInfo* di = nullptr;
+  ATTN_TRY(current_device(&di));
+  CUtensorMap tk, tv;
+  if (!make_map_bf16(&tk, k, d, Nk, (long long)B * Hkv) || !make_map_bf16(&tv, v, d, Nk, (long long)B * Hkv))
+    return ATTN_ERR_CUDA;
+  sdpa::DecParams p;
+  memset(&p, 0, sizeof(p));
+  decode_plan(B, Hkv, Nk, &p.nsplit, &p.split_keys);
+  const size_t rows = (size_t)B * H * Nq * (size_t)p.nsplit;
+  p.q = static_cast<const uint16_t*>(q);
+  p.o = static_cast<uint16_t*>(o);
+  p.lse = lse;
+  p.o_part = static_cast<float*>(workspace);
+  p.lse_part = p.o_part + rows * (size_t)d;
+  p.B = B;
+  p.H = H;
+  p.Hkv = Hkv;
+  p.G = H / Hkv;
+  p.Nq = Nq;
+  p.Nk = Nk;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.status = di->status;
+  p.limit_ns = wait_limit_ns();
+  p.info = di->info;
+  cudaError_t e = sdpa::launch_decode(d, causal != 0, tk, tv, p, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;
 }
 
 attn_status_t attn_get_device_status(void* stream) {

@@ -37,10 +37,27 @@ struct BwdParams {
   int* info;
 };
 
+// Decode (split over the keys) arguments.
+constexpr int kDecMaxRows = 64;  // G * Nq query rows per K/V head
+struct DecParams {
+  const uint16_t* q;     // (B, H, Nq, d) bf16
+  uint16_t* o;           // (B, H, Nq, d) bf16
+  float* lse;            // (B, H, Nq)
+  float* o_part;         // (B, H, Nq, nsplit, d) float32 workspace
+  float* lse_part;       // (B, H, Nq, nsplit) float32 workspace
+  int B, H, Hkv, G, Nq, Nk;
+  int nsplit, split_keys;  // key chunks: [s * split_keys, min(Nk, (s + 1) * split_keys))
+  float scale_log2;
+  int* status;
+  unsigned long long limit_ns;
+  int* info;
+};
+
 // Shared-memory bytes of each kernel instance (for validation and launch).
 size_t fwd_smem_bytes(int d);
 size_t bwd_smem_bytes(int d);
 size_t bwd_dq_smem_bytes(int d);
+size_t decode_smem_bytes(int d);
 
 cudaError_t launch_fwd(int d, bool causal, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                        const CUtensorMap& to, const FwdParams& p, cudaStream_t stream);
@@ -51,5 +68,7 @@ cudaError_t launch_bwd_grad(int d, bool causal, const CUtensorMap& tq, const CUt
                             const BwdParams& p, cudaStream_t stream);
 cudaError_t launch_bwd_dq(int d, bool causal, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                           const CUtensorMap& tdo, const CUtensorMap& tdq, const BwdParams& p, cudaStream_t stream);
+cudaError_t launch_decode(int d, bool causal, const CUtensorMap& tk, const CUtensorMap& tv, const DecParams& p,
+                          cudaStream_t stream);
 
 }  // namespace sdpa

@@ -17,6 +17,14 @@ SDPA call on "SDPA backend 与 FlashAttention", §3):
   c4p  same, head_dim 80 zero-padded to 96, scale 1/sqrt(80)  seed 4
   c5   B=8  H=16  Hkv=16 N=4096 d=128  causal, fwd+bwd (dO drawn)  seed 5
 
+Decode workloads (Nq new queries per head against a cache of N keys/values;
+the pages' FAQ on inference with a KV cache, decode profiled apart from
+prefill; the cache length and group size are those of a long-context GQA
+model):
+
+  dec1 B=8  H=64  Hkv=8  Nq=1 N=32768 d=128  non-causal  seed 6
+  dec4 same shape, Nq=4 new tokens (a speculative block), causal  seed 7
+
 Every draw is numpy's PCG64 ``default_rng(seed).standard_normal(dtype=float32)``
 taken in the fixed order Q, K, V, dO, multiplied by the config's amplitude and
 then rounded to bf16 (round to nearest, ties to even).
@@ -43,6 +51,7 @@ class Workload:
     d_draw: int | None = None      # head_dim actually drawn (zero-padded up to d)
     with_grad: bool = False        # also draw dO
     scale: float | None = None     # default 1/sqrt(d_draw or d)
+    Nq: int | None = None          # decode: new queries per head (None: Nq = N)
 
     @property
     def softmax_scale(self) -> float:
@@ -54,6 +63,10 @@ class Workload:
     def G(self) -> int:
         return self.H // self.Hkv
 
+    @property
+    def n_queries(self) -> int:
+        return self.Nq if self.Nq is not None else self.N
+
 
 WORKLOADS: dict[str, Workload] = {
     "c1": Workload("c1", 1, 2, 2, 256, 64, False, 1),
@@ -63,6 +76,8 @@ WORKLOADS: dict[str, Workload] = {
     "c4": Workload("c4", 1, 32, 8, 8192, 128, True, 4, amp=0.5),
     "c4p": Workload("c4p", 1, 32, 8, 8192, 96, True, 4, amp=0.5, d_draw=80),
     "c5": Workload("c5", 8, 16, 16, 4096, 128, True, 5, with_grad=True),
+    "dec1": Workload("dec1", 8, 64, 8, 32768, 128, False, 6, Nq=1),
+    "dec4": Workload("dec4", 8, 64, 8, 32768, 128, True, 7, Nq=4),
 }
 
 
@@ -97,12 +112,12 @@ def make_inputs(w: Workload) -> dict[str, np.ndarray]:
     arrays whose values are exactly representable in bf16."""
     rng = np.random.default_rng(w.seed)
     dd = w.d_draw or w.d
-    q = draw(rng, (w.B, w.H, w.N, dd), w.amp)
+    q = draw(rng, (w.B, w.H, w.n_queries, dd), w.amp)
     k = draw(rng, (w.B, w.Hkv, w.N, dd), w.amp)
     v = draw(rng, (w.B, w.Hkv, w.N, dd), w.amp)
     out = {"q": q, "k": k, "v": v}
     if w.with_grad:
-        out["do"] = draw(rng, (w.B, w.H, w.N, dd), 1.0)
+        out["do"] = draw(rng, (w.B, w.H, w.n_queries, dd), 1.0)
     if dd != w.d:
         pad = [(0, 0)] * 3 + [(0, w.d - dd)]
         out = {n: np.pad(a, pad) for n, a in out.items()}

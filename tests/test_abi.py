@@ -93,3 +93,39 @@ def test_bwd_rejects_bad_arguments(lib):
     bad = list(args)
     bad[6] = FAKE + 4
     assert sdpa.attn_bwd(*bad, FAKE, 1 << 20, 1, 2, 2, 64, 64, 0.1, 0, None) == sdpa.Status.MISALIGNED
+
+
+def _decode_chunks(B, Hkv, Nk):
+    # The documented chunk plan: whole 128-key tiles, at most 4 per chunk,
+    # and at least ceil(1024 / (B * Hkv)) chunks while tiles last.
+    tiles = -(-Nk // 128)
+    want = max(-(-tiles // 4), -(-1024 // (B * Hkv)))
+    ns0 = min(tiles, want)
+    per = -(-tiles // ns0)
+    return -(-tiles // per)
+
+
+@pytest.mark.parametrize("B,H,Hkv,Nq,Nk,d", [(8, 32, 8, 1, 32768, 128), (1, 8, 8, 4, 4096, 64),
+                                             (2, 16, 2, 2, 1000, 96), (1, 1, 1, 1, 1, 128)])
+def test_decode_workspace_size_formula(lib, B, H, Hkv, Nq, Nk, d):
+    import scaled_dot_product_08_gb300 as sdpa
+    ns = _decode_chunks(B, Hkv, Nk)
+    assert sdpa.attn_decode_workspace_size(B, H, Hkv, Nq, Nk, d) == B * H * Nq * ns * (d + 1) * 4
+
+
+def test_decode_rejects_bad_arguments(lib):
+    import scaled_dot_product_08_gb300 as sdpa
+    S = sdpa.Status
+    f = lambda *a: sdpa.attn_decode(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1 << 30, *a)
+    assert f(1, 8, 8, 5, 4, 128, 0.1, 0, None) == S.UNSUPPORTED_SHAPE      # Nq > Nk
+    assert f(1, 8, 8, 0, 4, 128, 0.1, 0, None) == S.UNSUPPORTED_SHAPE      # Nq < 1
+    assert f(1, 64, 1, 2, 64, 128, 0.1, 0, None) == S.UNSUPPORTED_SHAPE    # G * Nq = 128 > 64
+    assert f(1, 8, 3, 1, 64, 128, 0.1, 0, None) == S.UNSUPPORTED_SHAPE     # Hkv does not divide H
+    assert f(1, 8, 8, 1, 64, 80, 0.1, 0, None) == S.UNSUPPORTED_SHAPE      # d
+    assert f(1, 8, 8, 1, 64, 128, float("inf"), 0, None) == S.INVALID_ARG
+    assert f(1, 8, 8, 1, 64, 128, 0.1, 2, None) == S.INVALID_ARG
+    assert sdpa.attn_decode(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 16, 1, 8, 8, 1, 64, 128, 0.1, 0, None) == S.WORKSPACE
+    assert sdpa.attn_decode(FAKE, FAKE, FAKE, FAKE, FAKE, 0, 1 << 30, 1, 8, 8, 1, 64, 128, 0.1, 0, None) == S.WORKSPACE
+    assert sdpa.attn_decode(FAKE + 4, FAKE, FAKE, FAKE, FAKE, FAKE, 1 << 30, 1, 8, 8, 1, 64, 128, 0.1, 0,
+                            None) == S.MISALIGNED
+    assert sdpa.attn_decode_workspace_size(1, 8, 8, 5, 4, 128) == 0
