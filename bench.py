@@ -209,9 +209,40 @@ def cpu_baseline(w, budget_s=15.0):
                       f"{'fwd+bwd' if w.with_grad else 'fwd'} in float64 numpy, {t_total:.1f} s"}
 
 
+def run_reference_decode(args, w):
+    """The reference arm for a decode workload: the CPU oracle's decode on
+    batch element 0 (all heads, the whole cache) per step, in HBM-equivalent
+    bytes per second of the GPU arm's metric."""
+    import oracle
+    from sdpa_inputs import make_inputs
+    x = make_inputs(w)
+    q, k, v = x["q"][:1], x["k"][:1], x["v"][:1]
+    run = lambda: oracle.attention_decode(q, k, v, w.softmax_scale, w.causal)
+    for _ in range(args.warmup):
+        run()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        run()
+    t = time.perf_counter() - t0
+    val = decode_bytes(w) / w.B * args.steps / t / 1e9
+    sample = f"batch element 0 of {w.name} (all {w.H} heads, Nq={w.n_queries}, Nk={w.N}) per step, float64 numpy"
+    line = {"impl": "reference", "metric": "attention decode (KV cache, split over keys) HBM bandwidth",
+            "value": val, "unit": "GB/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": t / args.steps * 1e3, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f64", "data": "synthetic (seeded N(0,1) draws rounded to bf16)",
+            "config": {"workload": f"{w.name}: B={w.B} H={w.H} Hkv={w.Hkv} Nq={w.n_queries} Nk={w.N} d={w.d} "
+                                   f"{'causal' if w.causal else 'non-causal'} decode"},
+            "cpu_baseline": {"value": val, "unit": "GB/s", "cores": _blas_threads(), "kind": "oracle", "sample": sample},
+            "e2e": {"value": val, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
 def run_reference(args, w, rank, world):
     """The reference arm: the CPU oracle, one whole head of the workload per step."""
     if rank != 0:
+        return
+    if w.Nq is not None:
+        run_reference_decode(args, w)
         return
     x = _oracle_head_inputs(w)
     for _ in range(args.warmup):

@@ -145,7 +145,7 @@ attn_status_t attn_bwd_dq(const void* q, const void* k, const void* v, const voi
  *              the sequence, and sees keys 0 .. Nk - Nq + t.
  *   workspace  device buffer of at least attn_decode_workspace_size() bytes,
  *              owned by the caller; its contents on entry are ignored.
- * Limits: 1 <= Nq <= Nk; (H / Hkv) * Nq <= 64 query rows per K/V head;
+ * Limits: 1 <= Nq <= Nk; (H / Hkv) * Nq <= 128 query rows per K/V head;
  * d in {64, 96, 128}.  Two kernels run on `stream` (chunk pass, merge); the
  * chunk count depends only on the shape.  Bound by the HBM read of K and V.
  */

@@ -328,13 +328,13 @@ attn_status_t attn_bwd(const void* q, const void* k, const void* v, const void* 
 }
 
 // Key chunks of the decode kernel, a pure function of the shape (so the
-// workspace size needs no device query): chunks of whole 128-key tiles, at
-// most four tiles each, and enough chunks for ~1024 CTAs over B * Hkv when
-// the cache is short.
+// workspace size needs no device query): chunks of whole 128-key tiles,
+// about 1216 CTAs in all (four waves of two CTAs on each of 152 SMs) when
+// the cache is long enough.
 static void decode_plan(int B, int Hkv, int Nk, int* nsplit, int* split_keys) {
   const int tiles = (Nk + 127) / 128;
   const long long bh = (long long)B * Hkv;
-  const long long want = std::max<long long>((tiles + 3) / 4, (1024 + bh - 1) / bh);
+  const long long want = (1216 + bh - 1) / bh;
   const int ns0 = (int)std::min<long long>(tiles, want);
   const int per = (tiles + ns0 - 1) / ns0;  // tiles per chunk
   *nsplit = (tiles + per - 1) / per;
@@ -367,8 +367,9 @@ attn_status_t attn_decode(const void* q, const void* k, const void* v, void* o, 
   ATTN_TRY(check_ptrs({q, k, v, o, lse, workspace}));
   DeviceInfo* di = nullptr;
   ATTN_TRY(current_device(&di));
-  CUtensorMap tk, tv;
-  if (!make_map_bf16(&tk, k, d, Nk, (long long)B * Hkv) || !make_map_bf16(&tv, v, d, Nk, (long long)B * Hkv))
+  CUtensorMap tq, tk, tv;  // q as one (B*H*Nq) x d matrix: a K/V head's query rows are contiguous
+  if (!make_map_bf16(&tq, q, d, B * H * Nq, 1) || !make_map_bf16(&tk, k, d, Nk, (long long)B * Hkv) ||
+      !make_map_bf16(&tv, v, d, Nk, (long long)B * Hkv))
     return ATTN_ERR_CUDA;
   sdpa::DecParams p;
   memset(&p, 0, sizeof(p));
@@ -389,7 +390,7 @@ attn_status_t attn_decode(const void* q, const void* k, const void* v, void* o, 
   p.status = di->status;
   p.limit_ns = wait_limit_ns();
   p.info = di->info;
-  cudaError_t e = sdpa::launch_decode(d, causal != 0, tk, tv, p, static_cast<cudaStream_t>(stream));
+  cudaError_t e = sdpa::launch_decode(d, causal != 0, tq, tk, tv, p, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;
 }
 

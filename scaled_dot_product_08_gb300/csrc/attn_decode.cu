@@ -9,29 +9,34 @@
 // Causal: query t of the block sits at position Nk - Nq + t (the new tokens
 // end the sequence) and sees keys 0 .. Nk - Nq + t.
 //
-// The work reads every cached key and value once and does 4d flops per key
-// and query row, so for the few query rows of a decode step it is bound by
-// HBM bandwidth, not by the tensor cores: the arithmetic runs on the FMA
-// pipes and the design effort goes into streaming K/V at full bandwidth.
+// A decode step reads every cached key and value once for the R = G * Nq
+// query rows of their K/V head (the head's G query heads times the Nq new
+// tokens), so it is bound by HBM bandwidth.  The two contractions are still
+// dense (R x 128 keys x d per tile), and running them on the tensor cores
+// keeps the instruction stream short enough for the SM to stream K/V at full
+// bandwidth (an FMA-pipe version of this kernel issued ~3,400 warp
+// instructions per 64 KB tile and reached ~20% of HBM bandwidth).
 //
 // Two kernels on the caller's stream:
-//   decode_split  one CTA per (key chunk, batch * K/V head), 256 threads.
-//                 The R = G * Nq query rows of a K/V head (its G query heads
-//                 times the Nq new tokens) share every K/V tile the CTA
-//                 loads.  Thread 0 streams 128-key K and V tiles by TMA
-//                 into a 2-stage ring (128-byte swizzle, so 16-byte reads of
-//                 consecutive rows hit distinct banks); per tile:
-//                   scores   one key per thread, R/2 query rows each, fp32 FMA
-//                            against Q rows pre-scaled by scale * log2(e)
-//                   softmax  one warp per query row: tile max, running max,
-//                            rescale factor, exp2, row sum (online, §四)
-//                   P V      each thread owns (query row, 8 columns) pairs for
-//                            a subset of the tile's keys; partial sums stay in
-//                            registers across tiles and are combined once
-//                 and writes its chunk's normalised O and lse (natural log;
-//                 -inf with O = 0 when every key of the chunk is masked).
-//   decode_merge  one warp per (batch, head, query): the lse-weighted merge
+//   decode_split  one CTA per (key chunk, batch * K/V head), 192 threads,
+//                 two CTAs per SM (97 KB shared memory, 256 TMEM columns
+//                 each), so one CTA's loads overlap the other's work:
+//                   warps 0-3  softmax, one thread per query row (TMEM lane);
+//                              rows >= R (up to 128 rows per K/V head are
+//                              live) are padding and only keep the phases
+//                   warp 4     TMA producer: the group's 128 query rows
+//                              (rows >= R are whatever follows; their
+//                              results are never read), then K_j, V_j
+//                   warp 5     MMA issuer (one elected lane issues)
+//                 Per 128-key tile j: S = Q K_j^T (TMEM, M = 128 query rows,
+//                 N = 128 keys), online softmax in base 2 with a lazily
+//                 raised running max (as in the forward kernel), P as bf16
+//                 pairs over S, O += P V_j (A = P in TMEM).  The chunk's
+//                 normalised O and its lse go to the workspace (lse = -inf,
+//                 O = 0 when no key of the chunk is visible to the row).
+//   decode_merge  one CTA per (batch, head, query): the lse-weighted merge
 //                 of the chunks -> O (bf16) and lse.
+// Tensor memory (256 columns per CTA): S / P [0,128), O [128,128+d).
 #include <cmath>
 
 #include "kernels.h"
@@ -41,305 +46,302 @@ namespace sdpa {
 
 namespace {
 
-constexpr int kDecThreads = 256;
-constexpr int kDecTileKeys = 128;
+constexpr int kDecThreads = 192;
 
 template <int D>
 struct DecTraits {
   static constexpr int NB = (D + 63) / 64;
-  static constexpr int BLOCK_BYTES = 128 * 128;        // [128 keys x 64 columns] bf16, swizzled
-  static constexpr int TILE_BYTES = NB * BLOCK_BYTES;  // one [128 keys x d] tile
-  static constexpr int STAGE_BYTES = 2 * TILE_BYTES;   // K and V
-  static constexpr int QS_BYTES = kDecMaxRows * D * 4; // Q rows, fp32, pre-scaled
-  static constexpr int PS_BYTES = kDecMaxRows * kDecTileKeys * 4;  // P of one tile, fp32
-  static constexpr int STAT_BYTES = kDecMaxRows * 4 * 3;           // m, l, alpha per row
-  static constexpr int SMEM = 1024 + 2 * STAGE_BYTES + QS_BYTES + PS_BYTES + STAT_BYTES + 64;
-  // (query row, 8-column group) pairs each thread accumulates in P V
-  static constexpr int MAX_PAIRS = (kDecMaxRows * (D / 8) + kDecThreads - 1) / kDecThreads;
+  static constexpr int BLOCK_BYTES = 128 * 128;        // [128 rows x 64 columns] bf16, swizzled
+  static constexpr int TILE_BYTES = NB * BLOCK_BYTES;  // one [128 rows x d] tile
+  static constexpr int KSTEPS = D / 16;
+  static constexpr int NBAR = 10;
+  static constexpr int SMEM = 1024 + 3 * TILE_BYTES + NBAR * 8 + 16;  // Q, K, V
 };
-
-// Column group c8 (8 bf16 columns) of row `row` of a swizzled [128 x d] tile.
-__device__ __forceinline__ uint32_t dec_chunk(uint32_t tile, int row, int c8) {
-  return tile + (uint32_t)(c8 >> 3) * (128u * 128u) + (uint32_t)row * 128u + ((uint32_t)((c8 & 7) ^ (row & 7)) << 4);
-}
-
-__device__ __forceinline__ uint4 lds128(uint32_t addr) {
-  uint4 v;
-  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
-  return v;
-}
-
-__device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
-__device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 
 }  // namespace
 
 template <int D, bool CAUSAL>
-__global__ void __launch_bounds__(kDecThreads, 1)
-    decode_split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
-                        const DecParams p) {
+__global__ void __launch_bounds__(kDecThreads, 2)
+    decode_split_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                        const __grid_constant__ CUtensorMap tmV, const DecParams p) {
   using T = DecTraits<D>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* const gbase = smem_raw + (base - raw);
-  const uint32_t sStage = base;                              // [2] {K tile, V tile}
-  float* const q_s = reinterpret_cast<float*>(gbase + 2 * T::STAGE_BYTES);            // [R][D]
-  float* const p_s = reinterpret_cast<float*>(gbase + 2 * T::STAGE_BYTES + T::QS_BYTES);  // [R][128]
-  float* const m_s = reinterpret_cast<float*>(gbase + 2 * T::STAGE_BYTES + T::QS_BYTES + T::PS_BYTES);
-  float* const l_s = m_s + kDecMaxRows;
-  float* const a_s = l_s + kDecMaxRows;
-  const uint32_t sBar = smem_u32(a_s + kDecMaxRows);
-  const uint32_t bFull = (sBar + 7u) & ~7u;                  // [2] stage loaded
-  volatile int* const abort_flag = reinterpret_cast<volatile int*>(gbase + (bFull - base) + 16);
+  const uint32_t sQ = base, sK = sQ + T::TILE_BYTES, sV = sK + T::TILE_BYTES;
+  const uint32_t sBar = sV + T::TILE_BYTES;
+  const uint32_t bQ = sBar;          // Q loaded
+  const uint32_t bKf = bQ + 8;       // K_j loaded (phase j)
+  const uint32_t bKe = bKf + 8;      // K slot free: S_j done (phase j)
+  const uint32_t bVf = bKe + 8;      // V_j loaded
+  const uint32_t bVe = bVf + 8;      // V slot free: P V_j done
+  const uint32_t bS = bVe + 8;       // S_j ready (phase j)
+  const uint32_t bP = bS + 8;        // P_j in TMEM (128 arrivals)
+  const uint32_t bO = bP + 8;        // the chunk's last P V done
+  const uint32_t bDrain = bO + 8;
+  uint8_t* const misc = gbase + (sBar - base) + 8 * T::NBAR;
+  uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(misc);
+  volatile int* const abort_flag = reinterpret_cast<volatile int*>(misc + 4);
 
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int split = blockIdx.x, bhk = blockIdx.y;
   const int b = bhk / p.Hkv, hk = bhk % p.Hkv;
-  const int R = p.G * p.Nq;                                  // query rows of this K/V head
+  const int R = p.G * p.Nq;                    // live query rows
+  const int qrow0 = (b * p.H + hk * p.G) * p.Nq;  // first query row of the group in (B*H*Nq, d)
   const int key0 = split * p.split_keys;
   const int key1 = min(p.Nk, key0 + p.split_keys);
-  const int ntiles = (key1 - key0 + kDecTileKeys - 1) / kDecTileKeys;
+  const int n = (key1 - key0 + 127) / 128;     // key tiles of this chunk
 
-  if (tid == 0) {
-    mbar_init(bFull, 1);
-    mbar_init(bFull + 8u, 1);
+  if (threadIdx.x == 0) {
+    mbar_init(bQ, 1);
+    mbar_init(bKf, 1);
+    mbar_init(bKe, 1);
+    mbar_init(bVf, 1);
+    mbar_init(bVe, 1);
+    mbar_init(bS, 1);
+    mbar_init(bP, 128);
+    mbar_init(bO, 1);
+    mbar_init(bDrain, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
-  // Q rows of the group, fp32, pre-scaled into the base-2 domain.
-  for (int e = tid; e < R * (D / 8); e += kDecThreads) {
-    const int r = e / (D / 8), c8 = e % (D / 8);
-    const int h = hk * p.G + r / p.Nq, t = r % p.Nq;
-    const uint4 w = *reinterpret_cast<const uint4*>(p.q + (((size_t)b * p.H + h) * p.Nq + t) * D + c8 * 8);
-    float* dst = q_s + r * D + c8 * 8;
-    const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      dst[2 * k] = bf_lo(ws[k]) * p.scale_log2;
-      dst[2 * k + 1] = bf_hi(ws[k]) * p.scale_log2;
-    }
+  if (warp == 5) {
+    tmem_alloc(smem_u32(tmem_slot), 256);
+    tmem_relinquish();
   }
-  for (int r = tid; r < kDecMaxRows; r += kDecThreads) {
-    m_s[r] = -INFINITY;
-    l_s[r] = 0.f;
-  }
+  tc_fence_before();
   __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
   const WaitCtx wc{abort_flag, p.status, p.limit_ns, p.info};
 
-  auto issue = [&](int tile) {  // thread 0: K and V of `tile` into stage tile & 1
-    const uint32_t st = sStage + (uint32_t)(tile & 1) * T::STAGE_BYTES, bar = bFull + 8u * (tile & 1);
-    fence_proxy_async_smem();
-    mbar_expect_tx(bar, T::STAGE_BYTES);
-    const int row = key0 + tile * kDecTileKeys;
-    for (int cb = 0; cb < T::NB; ++cb) {
-      tma_load_3d(st + cb * T::BLOCK_BYTES, &tmK, bar, cb * 64, row, bhk);
-      tma_load_3d(st + T::TILE_BYTES + cb * T::BLOCK_BYTES, &tmV, bar, cb * 64, row, bhk);
+  if (warp < 4) {
+    // ------------------------------------------------------------ softmax
+    const int r = threadIdx.x;            // query row == TMEM lane
+    const bool live = r < R;
+    const bool warp_live = warp * 32 < R;  // rows >= R only keep the phases
+    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+    const uint32_t tS = tmem + lane_off, tO = tmem + 128 + lane_off;
+    const float c = p.scale_log2;
+    // One past the last key this row may see: the chunk end, and for causal
+    // rows position Nk - Nq + t (plus one).
+    const int vis_end = CAUSAL ? min(key1, p.Nk - p.Nq + (live ? r % p.Nq : 0) + 1) : key1;
+    float m = -INFINITY, l = 0.f;  // running max (scaled, base 2), running sum
+    bool ok = true;
+    for (int j = 0; j < n; ++j) {
+      ok = __all_sync(0xffffffffu, wait_bounded(wc, bS, j & 1, wait_site(0xc1, j)));
+      if (!ok) break;
+      tc_fence_after();
+      if (warp_live) {
+        const int kt = key0 + j * 128;                      // key of column 0
+        const int lim = vis_end - kt;                       // columns >= lim are masked
+        // Pass 1: row max over the tile (two loads of 64 columns).
+        float mx = -INFINITY;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          uint32_t xa[32], xb[32];
+          tmem_ld32(tS + 64 * h, xa);
+          tmem_ld32(tS + 64 * h + 32, xb);
+          tmem_wait_ld();
+          reg_fence(xa);
+          reg_fence(xb);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const int ca = 64 * h + i, cb = 64 * h + 32 + i;
+            mx = fmax3(mx, ca < lim ? __uint_as_float(xa[i]) : -INFINITY, cb < lim ? __uint_as_float(xb[i]) : -INFINITY);
+          }
+        }
+        const float mc = mx * c;
+        float alpha = 1.f;
+        if (mc > m + 8.0f) {  // raise the running max (always on the first live tile)
+          alpha = (m == -INFINITY) ? 0.f : ex2(m - mc);
+          m = mc;
+        }
+        if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+          // O <- alpha O for this warp's rows (P V_{j-1} finished before S_j).
+#pragma unroll
+          for (int cc = 0; cc < D / 32; ++cc) {
+            uint32_t o[32];
+            tmem_ld32(tO + cc * 32, o);
+            tmem_wait_ld();
+            reg_fence(o);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+            tmem_st32(tO + cc * 32, o);
+          }
+        }
+        // Pass 2: p = 2^(s*c - m) (0 where masked or while no key is visible)
+        // as bf16 pairs over the first 64 columns of S, a quarter at a time:
+        // quarter q reads S columns 32q .. 32q+31 and writes packed columns
+        // 16q .. 16q+15, which earlier quarters have already read.
+        const float mm = (m == -INFINITY) ? 0.f : m;
+        float sum = 0.f;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          uint32_t xa[32], pk[16];
+          tmem_ld32(tS + 32 * q, xa);
+          tmem_wait_ld();
+          reg_fence(xa);
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const int i = 32 * q + 2 * e;
+            const float p0 = (i < lim) ? ex2(__uint_as_float(xa[2 * e]) * c - mm) : 0.f;
+            const float p1 = (i + 1 < lim) ? ex2(__uint_as_float(xa[2 * e + 1]) * c - mm) : 0.f;
+            sum += p0 + p1;
+            pk[e] = pack_bf16(p0, p1);
+          }
+          tmem_st16(tS + 16 * q, pk);
+        }
+        tmem_wait_st();
+        l = l * alpha + sum;
+      }
+      tc_fence_before();
+      mbar_arrive(bP);
     }
-  };
-  int issued = 0;
-  if (tid == 0) {
-    tma_prefetch_desc(&tmK);
-    tma_prefetch_desc(&tmV);
-    for (; issued < ntiles && issued < 2; ++issued) issue(issued);
-  }
-
-  // P V ownership: pairs (row r, column group c8) in row-major order; with
-  // fewer pairs than threads, the tile's keys are dealt to `kg` groups.
-  const int npairs = R * (D / 8);
-  const int kg = npairs >= kDecThreads ? 1 : min(16, kDecThreads / npairs);
-  const int grp = npairs >= kDecThreads ? 0 : tid / npairs;
-  const bool pv_active = npairs >= kDecThreads || tid < npairs * kg;
-  float acc[T::MAX_PAIRS][8];
+    // ------------------------------------------------------------ chunk out
+    if (ok) ok = __all_sync(0xffffffffu, wait_bounded(wc, bO, 0, wait_site(0xc2, n)));
+    if (ok && warp_live) {
+      tc_fence_after();
+      const size_t row = (size_t)qrow0 + r;  // == ((b * H + h) * Nq + t) for live rows
+      const float inv = l > 0.f ? 1.f / l : 0.f;
 #pragma unroll
-  for (int u = 0; u < T::MAX_PAIRS; ++u)
+      for (int cc = 0; cc < D / 32; ++cc) {
+        uint32_t o[32];
+        tmem_ld32(tO + cc * 32, o);
+        tmem_wait_ld();
+        reg_fence(o);
+        if (live) {
+          float4* dst = reinterpret_cast<float4*>(p.o_part + (row * p.nsplit + split) * D + cc * 32);
 #pragma unroll
-    for (int c = 0; c < 8; ++c) acc[u][c] = 0.f;
-
-  bool ok = true;
-  for (int tile = 0; tile < ntiles; ++tile) {
-    const uint32_t st = sStage + (uint32_t)(tile & 1) * T::STAGE_BYTES;
-    ok = __syncthreads_and(wait_bounded(wc, bFull + 8u * (tile & 1), (tile >> 1) & 1, wait_site(0xb1, tile)));
-    if (!ok) break;
-    const int kt0 = key0 + tile * kDecTileKeys;  // first key of the tile
-    // ---- scores: key jj = tid % 128, rows rh, rh + 2, ...
+          for (int i = 0; i < 8; ++i)
+            dst[i] = make_float4(__uint_as_float(o[4 * i]) * inv, __uint_as_float(o[4 * i + 1]) * inv,
+                                 __uint_as_float(o[4 * i + 2]) * inv, __uint_as_float(o[4 * i + 3]) * inv);
+        }
+      }
+      if (live)
+        p.lse_part[row * p.nsplit + split] = l > 0.f ? (m + log2f(l)) * 0.69314718055994531f : -INFINITY;
+    }
+  } else if (warp == 4) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      tma_prefetch_desc(&tmK);
+      tma_prefetch_desc(&tmV);
+      mbar_expect_tx(bQ, T::TILE_BYTES);
+      for (int cb = 0; cb < T::NB; ++cb) tma_load_3d(sQ + cb * T::BLOCK_BYTES, &tmQ, bQ, cb * 64, qrow0, 0);
+      int nk = 0, nv = 0;
+      for (int j = 0; j < n; ++j) {
+        if (j > 0 && !wait_bounded(wc, bKe, (j - 1) & 1, wait_site(0xd1, j))) break;
+        mbar_expect_tx(bKf, T::TILE_BYTES);
+        for (int cb = 0; cb < T::NB; ++cb)
+          tma_load_3d(sK + cb * T::BLOCK_BYTES, &tmK, bKf, cb * 64, key0 + j * 128, bhk);
+        nk = j + 1;
+        if (j > 0 && !wait_bounded(wc, bVe, (j - 1) & 1, wait_site(0xd2, j))) break;
+        mbar_expect_tx(bVf, T::TILE_BYTES);
+        for (int cb = 0; cb < T::NB; ++cb)
+          tma_load_3d(sV + cb * T::BLOCK_BYTES, &tmV, bVf, cb * 64, key0 + j * 128, bhk);
+        nv = j + 1;
+      }
+      // Every copy issued above has landed before the CTA may exit.
+      wait_drain(bQ, 0, p.limit_ns);
+      if (nk > 0) wait_drain(bKf, (nk - 1) & 1, p.limit_ns);
+      if (nv > 0) wait_drain(bVf, (nv - 1) & 1, p.limit_ns);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ MMA issuer
     {
-      const int jj = tid & (kDecTileKeys - 1), rh = tid >> 7;
-      const int key = kt0 + jj;
-      const bool key_ok = key < key1;
-      for (int r0 = rh; r0 < R; r0 += 16) {  // up to 8 rows per pass
-        float s[8];
+      const uint32_t leader = elect_one();
+      constexpr uint32_t IQK = idesc_bf16_f32(128, 128, false, false);  // S = Q K^T (K-major x K-major)
+      constexpr uint32_t IPV = idesc_bf16_f32(128, D, false, true);     // O += P V (A in TMEM, B MN-major)
+      const uint32_t tS = tmem, tO = tmem + 128;
+      const uint64_t dQ = sdesc_sw128(sQ, 16, 1024);
+      const uint64_t dK = sdesc_sw128(sK, 16, 1024);
+      const uint64_t dV = sdesc_sw128(sV, T::BLOCK_BYTES, 1024);
+      auto wait_all = [&](uint32_t bar, uint32_t parity, int site) {
+        return __all_sync(0xffffffffu, wait_bounded(wc, bar, parity, site));
+      };
+      bool ok = wait_all(bQ, 0, wait_site(0xe1, 0));
+      for (int j = 0; j < n && ok; ++j) {
+        if (!(ok = wait_all(bKf, j & 1, wait_site(0xe2, j)))) break;
+        tc_fence_after();
 #pragma unroll
-        for (int u = 0; u < 8; ++u) s[u] = 0.f;
-#pragma unroll 4
-        for (int c8 = 0; c8 < D / 8; ++c8) {
-          const uint4 kw = lds128(dec_chunk(st, jj, c8));
-          const float kf[8] = {bf_lo(kw.x), bf_hi(kw.x), bf_lo(kw.y), bf_hi(kw.y),
-                               bf_lo(kw.z), bf_hi(kw.z), bf_lo(kw.w), bf_hi(kw.w)};
-#pragma unroll
-          for (int u = 0; u < 8; ++u) {
-            const int r = r0 + 2 * u;
-            if (r < R) {
-              const float4 qa = *reinterpret_cast<const float4*>(q_s + r * D + c8 * 8);
-              const float4 qb = *reinterpret_cast<const float4*>(q_s + r * D + c8 * 8 + 4);
-              s[u] = fmaf(qa.x, kf[0], s[u]);
-              s[u] = fmaf(qa.y, kf[1], s[u]);
-              s[u] = fmaf(qa.z, kf[2], s[u]);
-              s[u] = fmaf(qa.w, kf[3], s[u]);
-              s[u] = fmaf(qb.x, kf[4], s[u]);
-              s[u] = fmaf(qb.y, kf[5], s[u]);
-              s[u] = fmaf(qb.z, kf[6], s[u]);
-              s[u] = fmaf(qb.w, kf[7], s[u]);
-            }
-          }
+        for (int kk = 0; kk < T::KSTEPS; ++kk) {
+          const uint32_t off = (kk >> 2) * T::BLOCK_BYTES + (kk & 3) * 32;
+          mma_ss_p(leader, tS, sdesc_add(dQ, off), sdesc_add(dK, off), IQK, kk > 0);
         }
+        mma_commit_p(leader, bS);
+        mma_commit_p(leader, bKe);  // K_j consumed
+        if (!(ok = wait_all(bP, j & 1, wait_site(0xe3, j)))) break;
+        if (!(ok = wait_all(bVf, j & 1, wait_site(0xe4, j)))) break;
+        tc_fence_after();
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          const int r = r0 + 2 * u;
-          if (r < R) {
-            bool live = key_ok;
-            if (CAUSAL) live = live && key <= p.Nk - p.Nq + r % p.Nq;
-            p_s[r * kDecTileKeys + jj] = live ? s[u] : -INFINITY;
-          }
-        }
+        for (int kk = 0; kk < 8; ++kk)
+          mma_ts_p(leader, tO, tS + kk * 8, sdesc_add(dV, kk * 2048), IPV, (j > 0 || kk > 0) ? 1u : 0u);
+        mma_commit_p(leader, bVe);  // V_j consumed (and P_j read)
       }
+      if (ok) mma_commit_p(leader, bO);
+      mma_commit_p(leader, bDrain);  // fires once every MMA issued above has finished
+      wait_drain(bDrain, 0, p.limit_ns);
     }
-    __syncthreads();
-    // ---- online softmax: one warp per row
-    for (int r = warp; r < R; r += kDecThreads / 32) {
-      float* row = p_s + r * kDecTileKeys;
-      float v4[4];
-#pragma unroll
-      for (int k = 0; k < 4; ++k) v4[k] = row[lane + 32 * k];
-      float mx = fmaxf(fmaxf(v4[0], v4[1]), fmaxf(v4[2], v4[3]));
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-      const float m_old = m_s[r];
-      const float m_new = fmaxf(m_old, mx);
-      // Rows with no live key so far keep m = -inf: every p is then 0.
-      const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
-      float sum = 0.f;
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const float e = ex2(v4[k] - m_use);
-        row[lane + 32 * k] = e;
-        sum += e;
-      }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-      if (lane == 0) {
-        const float alpha = (m_old == -INFINITY) ? 0.f : ex2(m_old - m_use);
-        a_s[r] = alpha;
-        l_s[r] = l_s[r] * alpha + sum;
-        m_s[r] = m_new;
-      }
-    }
-    __syncthreads();
-    // ---- P V
-    if (pv_active) {
-#pragma unroll
-      for (int u = 0; u < T::MAX_PAIRS; ++u) {
-        const int pair = (npairs >= kDecThreads) ? tid + u * kDecThreads : tid % npairs;
-        if ((npairs >= kDecThreads && pair < npairs) || (npairs < kDecThreads && u == 0)) {
-          const int r = pair / (D / 8), c8 = pair % (D / 8);
-          const float alpha = a_s[r];
-#pragma unroll
-          for (int c = 0; c < 8; ++c) acc[u][c] *= alpha;
-          const float* prow = p_s + r * kDecTileKeys;
-#pragma unroll 4
-          for (int jj = grp; jj < kDecTileKeys; jj += kg) {
-            const float pv = prow[jj];
-            const uint4 vw = lds128(dec_chunk(st + T::TILE_BYTES, jj, c8));
-            acc[u][0] = fmaf(pv, bf_lo(vw.x), acc[u][0]);
-            acc[u][1] = fmaf(pv, bf_hi(vw.x), acc[u][1]);
-            acc[u][2] = fmaf(pv, bf_lo(vw.y), acc[u][2]);
-            acc[u][3] = fmaf(pv, bf_hi(vw.y), acc[u][3]);
-            acc[u][4] = fmaf(pv, bf_lo(vw.z), acc[u][4]);
-            acc[u][5] = fmaf(pv, bf_hi(vw.z), acc[u][5]);
-            acc[u][6] = fmaf(pv, bf_lo(vw.w), acc[u][6]);
-            acc[u][7] = fmaf(pv, bf_hi(vw.w), acc[u][7]);
-          }
-        }
-      }
-    }
-    __syncthreads();  // stage tile & 1 and p_s are free again
-    if (tid == 0 && issued < ntiles) issue(issued++);
+    __syncwarp();
   }
-  if (tid == 0) {  // nothing of ours may still be landing in shared memory at exit
-    // Tiles before the one the loop stopped at were consumed; at most the
-    // last two issued can still be in flight.
-    for (int t = issued - 2 > 0 ? issued - 2 : 0; t < issued; ++t)
-      wait_drain(bFull + 8u * (t & 1), (t >> 1) & 1, p.limit_ns);
-  }
-  if (!ok) return;
-  // ---- combine the key groups' partial sums (through p_s), normalise, store
-  float* const red = p_s;  // [kg][npairs][8] when kg > 1
-  if (kg > 1) {
-    if (pv_active) {
-#pragma unroll
-      for (int c = 0; c < 8; ++c) red[(grp * npairs + (tid % npairs)) * 8 + c] = acc[0][c];
-    }
-    __syncthreads();
-  }
-  for (int u = 0; u < T::MAX_PAIRS; ++u) {
-    const int pair = (npairs >= kDecThreads) ? tid + u * kDecThreads : tid;
-    if (pair >= npairs || (npairs < kDecThreads && u > 0)) break;
-    const int r = pair / (D / 8), c8 = pair % (D / 8);
-    float o[8];
-#pragma unroll
-    for (int c = 0; c < 8; ++c) o[c] = (kg > 1) ? 0.f : acc[u][c];
-    if (kg > 1)
-      for (int g2 = 0; g2 < kg; ++g2)
-#pragma unroll
-        for (int c = 0; c < 8; ++c) o[c] += red[(g2 * npairs + pair) * 8 + c];
-    const float l = l_s[r];
-    const float inv = l > 0.f ? 1.f / l : 0.f;
-    const int h = hk * p.G + r / p.Nq, t = r % p.Nq;
-    const size_t row = ((size_t)b * p.H + h) * p.Nq + t;
-    float4* dst = reinterpret_cast<float4*>(p.o_part + (row * p.nsplit + split) * D + c8 * 8);
-    dst[0] = make_float4(o[0] * inv, o[1] * inv, o[2] * inv, o[3] * inv);
-    dst[1] = make_float4(o[4] * inv, o[5] * inv, o[6] * inv, o[7] * inv);
-    if (c8 == 0)
-      p.lse_part[row * p.nsplit + split] = l > 0.f ? (m_s[r] + log2f(l)) * 0.69314718055994531f : -INFINITY;
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 5) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 256);
   }
 }
 
-// One warp per (batch, head, query): O = sum_s w_s O_s / sum_s w_s with
-// w_s = exp(lse_s - max lse); lse = max + ln sum w (-inf, O = 0 if no split
-// saw a live key).
+// One CTA of 128 threads per (batch, head, query) row: O = sum_s w_s O_s /
+// sum_s w_s with w_s = exp(lse_s - max lse); lse = max + ln sum w (-inf and
+// O = 0 if no chunk saw a visible key).  The chunks are dealt to the four
+// warps so that a row with many chunks is read by many loads in flight;
+// the warps' sums are combined in shared memory.  Lane l holds columns l,
+// l + 32, ... (coalesced scalar loads, aligned for every d).
 template <int D>
-__global__ void __launch_bounds__(256) decode_merge_kernel(const DecParams p) {
-  const long long rows = (long long)p.B * p.H * p.Nq;
-  const long long row = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
-  const int lane = threadIdx.x & 31;
-  if (row >= rows) return;
+__global__ void __launch_bounds__(128) decode_merge_kernel(const DecParams p) {
+  __shared__ float red[4][D];
+  __shared__ float wsum[4];
+  __shared__ float wmax[4];
+  const long long row = blockIdx.x;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const float* lp = p.lse_part + row * p.nsplit;
   float mx = -INFINITY;
-  for (int s = lane; s < p.nsplit; s += 32) mx = fmaxf(mx, lp[s]);
+  for (int s = threadIdx.x; s < p.nsplit; s += 128) mx = fmaxf(mx, lp[s]);
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-  constexpr int C = D / 32;  // columns per lane
+  if (lane == 0) wmax[warp] = mx;
+  __syncthreads();
+  mx = fmaxf(fmaxf(wmax[0], wmax[1]), fmaxf(wmax[2], wmax[3]));
+  constexpr int C = D / 32;  // columns per lane: lane + 32 c (coalesced scalar loads)
   float acc[C];
 #pragma unroll
   for (int c = 0; c < C; ++c) acc[c] = 0.f;
   float tot = 0.f;
   if (mx != -INFINITY) {
-    for (int s = 0; s < p.nsplit; ++s) {
+#pragma unroll 4
+    for (int s = warp; s < p.nsplit; s += 4) {
       const float w = __expf(lp[s] - mx);
       tot += w;
-      const float* op = p.o_part + (row * p.nsplit + s) * D;
+      const float* op = p.o_part + (row * p.nsplit + s) * D + lane;
 #pragma unroll
-      for (int c = 0; c < C; ++c) acc[c] = fmaf(w, op[lane + 32 * c], acc[c]);
+      for (int c = 0; c < C; ++c) acc[c] = fmaf(w, op[32 * c], acc[c]);
     }
   }
-  const float inv = tot > 0.f ? 1.f / tot : 0.f;
-  uint16_t* out = p.o + row * D;
 #pragma unroll
-  for (int c = 0; c < C; ++c) {
-    const float v = acc[c] * inv;
-    out[lane + 32 * c] = (uint16_t)(pack_bf16(v, 0.f) & 0xffffu);
+  for (int c = 0; c < C; ++c) red[warp][lane + 32 * c] = acc[c];
+  if (lane == 0) wsum[warp] = tot;
+  __syncthreads();
+  const float all = (wsum[0] + wsum[1]) + (wsum[2] + wsum[3]);
+  const float inv = all > 0.f ? 1.f / all : 0.f;
+  for (int c = threadIdx.x; c < D; c += 128) {
+    const float v = ((red[0][c] + red[1][c]) + (red[2][c] + red[3][c])) * inv;
+    p.o[row * D + c] = (uint16_t)(pack_bf16(v, 0.f) & 0xffffu);
   }
-  if (lane == 0) p.lse[row] = tot > 0.f ? mx + logf(tot) : -INFINITY;
+  if (threadIdx.x == 0) p.lse[row] = all > 0.f ? mx + logf(all) : -INFINITY;
 }
 
 size_t decode_smem_bytes(int d) {
@@ -352,25 +354,27 @@ size_t decode_smem_bytes(int d) {
 }
 
 template <int D, bool C>
-static cudaError_t launch_decode_t(const CUtensorMap& tk, const CUtensorMap& tv, const DecParams& p,
-                                   cudaStream_t stream) {
+static cudaError_t launch_decode_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                                   const DecParams& p, cudaStream_t stream) {
   auto kern = decode_split_kernel<D, C>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, DecTraits<D>::SMEM);
   if (e != cudaSuccess) return e;
-  kern<<<dim3((unsigned)p.nsplit, (unsigned)(p.B * p.Hkv)), kDecThreads, DecTraits<D>::SMEM, stream>>>(tk, tv, p);
+  kern<<<dim3((unsigned)p.nsplit, (unsigned)(p.B * p.Hkv)), kDecThreads, DecTraits<D>::SMEM, stream>>>(tq, tk, tv, p);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   const long long rows = (long long)p.B * p.H * p.Nq;
-  decode_merge_kernel<D><<<(unsigned)((rows + 7) / 8), 256, 0, stream>>>(p);
+  decode_merge_kernel<D><<<(unsigned)rows, 128, 0, stream>>>(p);
   return cudaGetLastError();
 }
 
-cudaError_t launch_decode(int d, bool causal, const CUtensorMap& tk, const CUtensorMap& tv, const DecParams& p,
-                          cudaStream_t stream) {
+cudaError_t launch_decode(int d, bool causal, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                          const DecParams& p, cudaStream_t stream) {
   switch (d) {
-    case 64: return causal ? launch_decode_t<64, true>(tk, tv, p, stream) : launch_decode_t<64, false>(tk, tv, p, stream);
-    case 96: return causal ? launch_decode_t<96, true>(tk, tv, p, stream) : launch_decode_t<96, false>(tk, tv, p, stream);
-    case 128: return causal ? launch_decode_t<128, true>(tk, tv, p, stream)
-                            : launch_decode_t<128, false>(tk, tv, p, stream);
+    case 64: return causal ? launch_decode_t<64, true>(tq, tk, tv, p, stream)
+                           : launch_decode_t<64, false>(tq, tk, tv, p, stream);
+    case 96: return causal ? launch_decode_t<96, true>(tq, tk, tv, p, stream)
+                           : launch_decode_t<96, false>(tq, tk, tv, p, stream);
+    case 128: return causal ? launch_decode_t<128, true>(tq, tk, tv, p, stream)
+                            : launch_decode_t<128, false>(tq, tk, tv, p, stream);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -38,7 +38,7 @@ struct BwdParams {
 };
 
 // Decode (split over the keys) arguments.
-constexpr int kDecMaxRows = 64;  // G * Nq query rows per K/V head
+constexpr int kDecMaxRows = 128;  // G * Nq query rows per K/V head (one 128-row MMA tile)
 struct DecParams {
   const uint16_t* q;     // (B, H, Nq, d) bf16
   uint16_t* o;           // (B, H, Nq, d) bf16
@@ -68,7 +68,7 @@ cudaError_t launch_bwd_grad(int d, bool causal, const CUtensorMap& tq, const CUt
                             const BwdParams& p, cudaStream_t stream);
 cudaError_t launch_bwd_dq(int d, bool causal, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                           const CUtensorMap& tdo, const CUtensorMap& tdq, const BwdParams& p, cudaStream_t stream);
-cudaError_t launch_decode(int d, bool causal, const CUtensorMap& tk, const CUtensorMap& tv, const DecParams& p,
-                          cudaStream_t stream);
+cudaError_t launch_decode(int d, bool causal, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                          const DecParams& p, cudaStream_t stream);
 
 }  // namespace sdpa

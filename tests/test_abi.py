@@ -96,10 +96,10 @@ def test_bwd_rejects_bad_arguments(lib):
 
 
 def _decode_chunks(B, Hkv, Nk):
-    # The documented chunk plan: whole 128-key tiles, at most 4 per chunk,
-    # and at least ceil(1024 / (B * Hkv)) chunks while tiles last.
+    # The documented chunk plan: whole 128-key tiles, about 1216 CTAs in all
+    # (ceil(1216 / (B * Hkv)) chunks while tiles last).
     tiles = -(-Nk // 128)
-    want = max(-(-tiles // 4), -(-1024 // (B * Hkv)))
+    want = -(-1216 // (B * Hkv))
     ns0 = min(tiles, want)
     per = -(-tiles // ns0)
     return -(-tiles // per)
@@ -119,7 +119,7 @@ def test_decode_rejects_bad_arguments(lib):
     f = lambda *a: sdpa.attn_decode(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1 << 30, *a)
     assert f(1, 8, 8, 5, 4, 128, 0.1, 0, None) == S.UNSUPPORTED_SHAPE      # Nq > Nk
     assert f(1, 8, 8, 0, 4, 128, 0.1, 0, None) == S.UNSUPPORTED_SHAPE      # Nq < 1
-    assert f(1, 64, 1, 2, 64, 128, 0.1, 0, None) == S.UNSUPPORTED_SHAPE    # G * Nq = 128 > 64
+    assert f(1, 64, 1, 3, 64, 128, 0.1, 0, None) == S.UNSUPPORTED_SHAPE    # G * Nq = 192 > 128
     assert f(1, 8, 3, 1, 64, 128, 0.1, 0, None) == S.UNSUPPORTED_SHAPE     # Hkv does not divide H
     assert f(1, 8, 8, 1, 64, 80, 0.1, 0, None) == S.UNSUPPORTED_SHAPE      # d
     assert f(1, 8, 8, 1, 64, 128, float("inf"), 0, None) == S.INVALID_ARG

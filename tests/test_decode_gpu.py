@@ -37,7 +37,8 @@ SHAPES = [
     (2, 8, 8, 1, 300, 128),     # MHA decode, ragged last tile
     (1, 32, 8, 1, 4096, 128),   # GQA 4:1
     (2, 16, 2, 4, 1000, 96),    # G*Nq = 32 rows, speculative block of 4
-    (1, 64, 8, 8, 777, 64),     # G*Nq = 64 rows (the limit)
+    (1, 64, 8, 8, 777, 64),     # G*Nq = 64 rows
+    (1, 64, 4, 8, 1500, 128),   # G*Nq = 128 rows (the limit)
     (3, 4, 1, 3, 129, 128),     # MQA, one key past a tile
     (1, 8, 4, 2, 5000, 128),    # many chunks
 ]
@@ -54,7 +55,7 @@ def test_decode_matches_oracle(cuda_lib, shape, causal):
 def test_decode_equal_lengths_causal_matches_forward(cuda_lib):
     # With Nq = Nk the decode alignment is the ordinary causal mask: decode
     # equals the forward kernel's result within the output tolerances.
-    B, H, Hkv, N, d = 1, 4, 2, 31, 64     # G * Nq = 62 rows: within the 64-row limit
+    B, H, Hkv, N, d = 1, 4, 2, 60, 64     # G * Nq = 120 rows: within the 128-row limit
     q = dev(make_random((B, H, N, d), 301))
     k = dev(make_random((B, Hkv, N, d), 302))
     v = dev(make_random((B, Hkv, N, d), 303))
