@@ -76,6 +76,23 @@ attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, flo
                        void* stream);
 
 /*
+ * Forward with Nq query rows and Nk key/value rows per head (cross
+ * attention; chunked prefill of Nq new tokens against a cache of Nk).  The
+ * SDPA call of page "SDPA backend 与 FlashAttention" (§3) takes query and key
+ * sequences of their own lengths; the pages fix no causal alignment for
+ * Nq != Nk, and the one taken is that of a block of new tokens ending the
+ * sequence: query row i sits at position Nk - Nq + i and sees keys
+ * 0 .. Nk - Nq + i (top-left and bottom-right agree when Nq == Nk).
+ *   q, o [in/out] bf16 (B, H, Nq, d);  k, v [in] bf16 (B, Hkv, Nk, d)
+ *   lse  [out] float32 (B, H, Nq)
+ * causal requires Nq <= Nk (otherwise ATTN_ERR_UNSUPPORTED_SHAPE).
+ * attn_fwd(..., N, ...) is attn_fwd_cross(..., N, N, ...).
+ */
+attn_status_t attn_fwd_cross(const void* q, const void* k, const void* v, void* o, float* lse,
+                             int B, int H, int Hkv, int Nq, int Nk, int d, float scale, int causal,
+                             void* stream);
+
+/*
  * Bytes of device workspace attn_bwd needs for this shape: two float32
  * per-row vectors (D = rowsum(dO * O) and lse in base 2), each padded to a
  * multiple of 128 rows per head, i.e. 8 * B * H * ceil(N/128) * 128 bytes.

@@ -23,8 +23,8 @@ __all__ = [
     "AttnError", "Status", "load", "attn_fwd", "attn_bwd", "attn_bwd_workspace_size",
     "attn_bwd_prep", "attn_bwd_grad", "attn_bwd_dq", "attn_bwd_noalloc",
     "attn_get_device_status", "attn_get_timeout_info", "attn_status_string", "attn_selftest_wait_timeout",
-    "attn_decode", "attn_decode_workspace_size",
-    "forward", "backward", "decode", "build",
+    "attn_decode", "attn_decode_workspace_size", "attn_fwd_cross",
+    "forward", "forward_cross", "backward", "decode", "build",
 ]
 
 
@@ -76,6 +76,8 @@ def load() -> ctypes.CDLL:
         lib.attn_get_device_status.restype = _I
         lib.attn_status_string.argtypes = [_I]
         lib.attn_status_string.restype = ctypes.c_char_p
+        lib.attn_fwd_cross.argtypes = [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, ctypes.c_float, _I, _P]
+        lib.attn_fwd_cross.restype = _I
         lib.attn_decode_workspace_size.argtypes = [_I, _I, _I, _I, _I, _I]
         lib.attn_decode_workspace_size.restype = ctypes.c_size_t
         lib.attn_decode.argtypes = [_P, _P, _P, _P, _P, _P, ctypes.c_size_t, _I, _I, _I, _I, _I, _I,
@@ -130,6 +132,10 @@ def attn_bwd_grad(q, k, v, dout, dk, dv, workspace, workspace_bytes, B, H, Hkv, 
 
 def attn_bwd_dq(q, k, v, dout, dq, workspace, workspace_bytes, B, H, Hkv, N, d, scale, causal, stream) -> int:
     return load().attn_bwd_dq(q, k, v, dout, dq, workspace, workspace_bytes, B, H, Hkv, N, d, scale, causal, stream)
+
+
+def attn_fwd_cross(q, k, v, o, lse, B, H, Hkv, Nq, Nk, d, scale, causal, stream) -> int:
+    return load().attn_fwd_cross(q, k, v, o, lse, B, H, Hkv, Nq, Nk, d, scale, causal, stream)
 
 
 def attn_decode_workspace_size(B, H, Hkv, Nq, Nk, d) -> int:
@@ -243,4 +249,28 @@ def decode(q, k, v, scale: float | None = None, causal: bool = False, workspace=
     _check(attn_decode(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
                        workspace.data_ptr(), workspace.numel() * workspace.element_size(),
                        B, H, Hkv, Nq, Nk, d, scale, causal, _stream_ptr(q)), "attn_decode")
+    return o, lse
+
+
+def forward_cross(q, k, v, scale: float | None = None, causal: bool = False):
+    """O, lse of Nq queries against Nk keys/values per head.
+
+    q: bf16 (B, H, Nq, d); k, v: bf16 (B, Hkv, Nk, d); causal: query row i
+    sits at position Nk - Nq + i (needs Nq <= Nk)."""
+    import torch
+    if q.dim() != 4 or k.dim() != 4 or v.dim() != 4:
+        raise ValueError("q, k, v must be 4-D")
+    B, H, Nq, d = q.shape
+    Hkv, Nk = k.shape[1], k.shape[2]
+    if tuple(k.shape) != (B, Hkv, Nk, d) or tuple(v.shape) != (B, Hkv, Nk, d):
+        raise ValueError("k and v must be (B, Hkv, Nk, d) with q's B and d")
+    for t in (q, k, v):
+        if not t.is_contiguous() or t.dtype != torch.bfloat16:
+            raise ValueError("inputs must be contiguous bf16")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device)
+    _check(attn_fwd_cross(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                          B, H, Hkv, Nq, Nk, d, scale, causal, _stream_ptr(q)), "attn_fwd_cross")
     return o, lse

@@ -192,17 +192,21 @@ const char* attn_status_string(attn_status_t s) {
   return "ATTN_ERR_UNKNOWN";
 }
 
-attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Hkv,
-                       int N, int d, float scale, int causal, void* stream) {
-  ATTN_TRY(check_shape(B, H, Hkv, N, d));
+// Forward over Nq query rows and Nk key rows per head (Nq == Nk for
+// attn_fwd); causal rows sit at positions Nk - Nq + i.
+static attn_status_t fwd_common(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                                int Hkv, int Nq, int Nk, int d, float scale, int causal, void* stream) {
+  ATTN_TRY(check_shape(B, H, Hkv, Nq, d));
+  ATTN_TRY(check_shape(B, H, Hkv, Nk, d));
   ATTN_TRY(check_scale_flag(scale, causal));
+  if (causal && Nq > Nk) return ATTN_ERR_UNSUPPORTED_SHAPE;  // a causal row would see no key
   ATTN_TRY(check_ptrs({q, k, v, o, lse}));
   DeviceInfo* di = nullptr;
   ATTN_TRY(current_device(&di));
 
   CUtensorMap tq, tk, tv, to;
-  if (!make_map_bf16(&tq, q, d, N, (long long)B * H) || !make_map_bf16(&tk, k, d, N, (long long)B * Hkv) ||
-      !make_map_bf16(&tv, v, d, N, (long long)B * Hkv) || !make_map_bf16(&to, o, d, N, (long long)B * H))
+  if (!make_map_bf16(&tq, q, d, Nq, (long long)B * H) || !make_map_bf16(&tk, k, d, Nk, (long long)B * Hkv) ||
+      !make_map_bf16(&tv, v, d, Nk, (long long)B * Hkv) || !make_map_bf16(&to, o, d, Nq, (long long)B * H))
     return ATTN_ERR_CUDA;
 
   sdpa::FwdParams p;
@@ -210,10 +214,12 @@ attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, flo
   p.B = B;
   p.H = H;
   p.Hkv = Hkv;
-  p.N = N;
   p.G = H / Hkv;
-  p.n_mtiles = (N + 255) / 256;
-  p.nkv = (N + 127) / 128;
+  p.Nq = Nq;
+  p.Nk = Nk;
+  p.koff = causal ? Nk - Nq : 0;
+  p.n_mtiles = (Nq + 255) / 256;
+  p.nkv = (Nk + 127) / 128;
   p.scale_log2 = scale * 1.4426950408889634f;
   p.status = di->status;
   p.limit_ns = wait_limit_ns();
@@ -221,6 +227,16 @@ attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, flo
   cudaError_t e = sdpa::launch_fwd(d, causal != 0, tq, tk, tv, to, p, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return ATTN_ERR_LAUNCH;
   return ATTN_OK;
+}
+
+attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Hkv,
+                       int N, int d, float scale, int causal, void* stream) {
+  return fwd_common(q, k, v, o, lse, B, H, Hkv, N, N, d, scale, causal, stream);
+}
+
+attn_status_t attn_fwd_cross(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                             int Hkv, int Nq, int Nk, int d, float scale, int causal, void* stream) {
+  return fwd_common(q, k, v, o, lse, B, H, Hkv, Nq, Nk, d, scale, causal, stream);
 }
 
 size_t attn_bwd_workspace_size(int B, int H, int Hkv, int N, int d) {

@@ -82,9 +82,9 @@ __global__ void __launch_bounds__(384, 1)
   const int mt = p.n_mtiles - 1 - (int)(blockIdx.x % p.n_mtiles);
   const int bhk = (bh / p.H) * p.Hkv + (bh % p.H) / p.G;
   int n0 = p.nkv, n1 = p.nkv;  // key tiles visited by query tile 0 / 1
-  if (CAUSAL) {
-    n0 = min(2 * mt + 1, p.nkv);
-    n1 = min(2 * mt + 2, p.nkv);
+  if (CAUSAL) {  // up to the tile holding the last row's last visible key, koff + 128 qi + 127
+    n0 = min((p.koff + 256 * mt + 127) / 128 + 1, p.nkv);
+    n1 = min((p.koff + 256 * mt + 255) / 128 + 1, p.nkv);
   }
 
   if (threadIdx.x == 0) {
@@ -153,17 +153,17 @@ __global__ void __launch_bounds__(384, 1)
           x[96 + i] = __uint_as_float(rd[i]);
         }
       }
-      if (CAUSAL) {
-        if (j == qi) {  // diagonal tile: key column i > row r is masked
+      {
+        // Columns at or past `lim` are invisible to row r: keys past Nk, and
+        // for causal rows keys past position koff + 128 qi + r.  Only the
+        // diagonal and the ragged last tile have any.
+        int lim = p.Nk - j * 128;
+        if (CAUSAL) lim = min(lim, p.koff + qi * 128 + r + 1 - j * 128);
+        if (__any_sync(0xffffffffu, lim < 128)) {
 #pragma unroll
           for (int i = 0; i < 128; ++i)
-            if (i > r) x[i] = -INFINITY;
+            if (i >= lim) x[i] = -INFINITY;
         }
-      } else if (j == p.nkv - 1) {  // ragged key tail
-        const int lim = p.N - j * 128;
-#pragma unroll
-        for (int i = 0; i < 128; ++i)
-          if (i >= lim) x[i] = -INFINITY;
       }
       // Row max with 3-input max: 8 independent chains over pairs of scores.
       float mx[8];
@@ -252,14 +252,14 @@ __global__ void __launch_bounds__(384, 1)
     }
     named_bar_sync(1 + s, 128);
     if (ok) {
-      if (r == 0 && qi * 128 < p.N) {
+      if (r == 0 && qi * 128 < p.Nq) {
         for (int cb = 0; cb < T::NB; ++cb)
           tma_store_3d(&tmO, sOut + cb * T::BLOCK_BYTES, cb * 64, qi * 128, bh);
         bulk_commit();
         bulk_wait_read_all();
       }
       const int row = qi * 128 + r;
-      if (row < p.N) p.lse[(size_t)bh * p.N + row] = (m + log2f(l)) * 0.69314718055994531f;
+      if (row < p.Nq) p.lse[(size_t)bh * p.Nq + row] = (m + log2f(l)) * 0.69314718055994531f;
     }
     setmaxnreg_dec<168>();  // one register budget again for the common teardown
   } else {

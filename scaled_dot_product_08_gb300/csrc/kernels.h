@@ -11,10 +11,12 @@ namespace sdpa {
 
 // Forward kernel arguments (tensor maps are passed separately).
 struct FwdParams {
-  float* lse;            // (B, H, N) float32
-  int B, H, Hkv, N, G;   // G = H / Hkv
-  int n_mtiles;          // ceil(N / 256): one CTA = two 128-row query tiles
-  int nkv;               // ceil(N / 128): key/value tiles
+  float* lse;            // (B, H, Nq) float32
+  int B, H, Hkv, G;      // G = H / Hkv
+  int Nq, Nk;            // query rows, key/value rows per head
+  int koff;              // causal: query row i sits at position koff + i (Nk - Nq)
+  int n_mtiles;          // ceil(Nq / 256): one CTA = two 128-row query tiles
+  int nkv;               // ceil(Nk / 128): key/value tiles
   float scale_log2;      // scale * log2(e)
   int* status;           // device status word
   unsigned long long limit_ns;  // bounded-wait limit

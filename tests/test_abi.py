@@ -129,3 +129,14 @@ def test_decode_rejects_bad_arguments(lib):
     assert sdpa.attn_decode(FAKE + 4, FAKE, FAKE, FAKE, FAKE, FAKE, 1 << 30, 1, 8, 8, 1, 64, 128, 0.1, 0,
                             None) == S.MISALIGNED
     assert sdpa.attn_decode_workspace_size(1, 8, 8, 5, 4, 128) == 0
+
+
+def test_fwd_cross_rejects_bad_arguments(lib):
+    import scaled_dot_product_08_gb300 as sdpa
+    S = sdpa.Status
+    f = lambda *a: sdpa.attn_fwd_cross(FAKE, FAKE, FAKE, FAKE, FAKE, *a)
+    assert f(1, 2, 2, 300, 200, 128, 0.1, 1, None) == S.UNSUPPORTED_SHAPE   # causal with Nq > Nk
+    assert f(1, 2, 2, 0, 200, 128, 0.1, 0, None) == S.UNSUPPORTED_SHAPE     # Nq < 1
+    assert f(1, 2, 2, 10, 0, 128, 0.1, 0, None) == S.UNSUPPORTED_SHAPE      # Nk < 1
+    assert f(1, 2, 2, 10, 20, 80, 0.1, 0, None) == S.UNSUPPORTED_SHAPE      # d
+    assert f(1, 2, 2, 10, 20, 128, -1.0, 0, None) == S.INVALID_ARG
