@@ -30,6 +30,7 @@ from .sdpa import (
     attention_forward_online,
     attention_backward,
     attention_decode,
+    attention_cross_backward,
     merge_splits,
     softmax_rows,
     softmax_two_block,
@@ -44,6 +45,7 @@ __all__ = [
     "attention_forward_online",
     "attention_backward",
     "attention_decode",
+    "attention_cross_backward",
     "merge_splits",
     "softmax_rows",
     "softmax_two_block",

@@ -140,6 +140,16 @@ def attention_decode(q, k, v, scale=None, causal=False):
     return attention_forward(q, k, v, scale, causal, q_offset=Nk - Nq)
 
 
+def attention_cross_backward(q, k, v, do, scale=None, causal=False):
+    """Gradients of the Nq-query, Nk-key attention of ``attention_decode``
+    (same causal reading: query t at position Nk - Nq + t), by the chain rule
+    of ``attention_backward``.  Returns dQ (B, H, Nq, d), dK, dV (B, Hkv, Nk, d)."""
+    Nq, Nk = np.shape(q)[2], np.shape(k)[2]
+    if causal and Nq > Nk:
+        raise ValueError("causal cross attention needs Nq <= Nk")
+    return attention_backward(q, k, v, do, scale, causal, q_offset=Nk - Nq)
+
+
 def merge_splits(O_parts, lse_parts):
     """Combine attention computed over disjoint key ranges ("splits").
 
@@ -220,7 +230,7 @@ def attention_forward_online(q, k, v, scale=None, causal=False, block=64):
     return O, lse
 
 
-def attention_backward(q, k, v, do, scale=None, causal=False):
+def attention_backward(q, k, v, do, scale=None, causal=False, q_offset=0):
     """Analytic gradients of O = softmax(scale Q K^T [+mask]) V w.r.t. Q, K, V.
 
     The pages ([FA] §五 and FAQ Q19) say the backward recomputes P and follows
@@ -233,7 +243,10 @@ def attention_backward(q, k, v, do, scale=None, causal=False):
         dQ   = scale * dS K
         dK   = scale * dS^T Q
     With grouped-query attention the dK, dV of a K/V head are the sums over
-    the G query heads that read it.  Returns dQ, dK, dV in float64.
+    the G query heads that read it.  Query row i sits at position
+    q_offset + i for the causal mask, as in ``attention_forward``; a row that
+    sees no key has P = 0 and so contributes nothing.  Returns dQ, dK, dV in
+    float64.
     """
     q = np.asarray(q, dtype=np.float64)
     k = np.asarray(k, dtype=np.float64)
@@ -248,8 +261,11 @@ def attention_backward(q, k, v, do, scale=None, causal=False):
     for b in range(B):
         for h in range(H):
             hk = gqa_kv_head(h, H, Hkv)
-            S = _scores(q[b, h], k[b, hk], scale, causal)
-            P, _, _ = softmax_rows(S)
+            S = _scores(q[b, h], k[b, hk], scale, causal, q_offset=q_offset)
+            live = np.isfinite(S).any(axis=1)
+            P = np.zeros_like(S)
+            if live.any():
+                P[live] = softmax_rows(S[live])[0]
             dv[b, hk] += P.T @ do[b, h]
             dP = do[b, h] @ v[b, hk].T
             D = (P * dP).sum(axis=1)
