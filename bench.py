@@ -8,7 +8,9 @@ kernel (O and lse), then the backward's three kernels (prep, grad, dq).  The
 default workload is the training configuration B=8, H=16, N=4096, d=128,
 causal, forward + backward.  Inputs (seeded bf16 draws) are resident in HBM
 before timing; they total 537 MB, larger than the 129 MB L2, so no L2 flush
-is inserted between steps.
+is inserted between steps.  Workloads whose inputs are below twice the L2
+write a 258 MB buffer before every timed step instead, and their step time
+is then the sum of the per-step CUDA-event durations (flush excluded).
 
 Work convention: forward 4*B*H*N^2*d (halved when causal), backward 2.5x the
 forward.  ``value`` = total TFLOP/s of the timed steps (all ranks).
@@ -42,6 +44,7 @@ sys.path.insert(0, ROOT)
 
 METRIC = "attention fwd/bwd TFLOPS (bf16, 1×GB300) and % of dense BF16 tensor peak"
 UNIT = "TFLOPS"
+L2_BYTES = 129_000_000
 FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}
 
 
@@ -58,13 +61,20 @@ def parse_args():
 
 
 def workload_desc(w):
+    if w.kind == "cross":
+        what = "fwd+bwd (encoder-decoder cross attention)" if w.with_grad else "fwd (chunked prefill)"
+        return (f"{w.name}: B={w.B} H={w.H} Hkv={w.Hkv} Nq={w.n_queries} Nk={w.N} d={w.d} "
+                f"{'causal' if w.causal else 'non-causal'} {what}")
     tail = f" (head_dim {w.d_draw} zero-padded)" if w.d_draw else ""
     return (f"{w.name}: B={w.B} H={w.H} Hkv={w.Hkv} N={w.N} d={w.d}{tail} "
             f"{'causal' if w.causal else 'non-causal'} {'fwd+bwd' if w.with_grad else 'fwd'}")
 
 
 def step_flops(w):
-    from sdpa_inputs import flops_backward, flops_forward
+    from sdpa_inputs import flops_backward, flops_cross, flops_forward
+    if w.kind == "cross":
+        f = flops_cross(w.B, w.H, w.n_queries, w.N, w.d, w.causal)
+        return f, (2.5 * f if w.with_grad else 0.0)
     f = flops_forward(w.B, w.H, w.N, w.d, w.causal)
     b = flops_backward(w.B, w.H, w.N, w.d, w.causal) if w.with_grad else 0.0
     return f, b
@@ -164,7 +174,8 @@ def _oracle_head_inputs(w):
     from sdpa_inputs import draw
     rng = np.random.default_rng(w.seed)
     dd = w.d_draw or w.d
-    return [draw(rng, (1, 1, w.N, dd), a) for a in (w.amp, w.amp, w.amp, 1.0)]
+    shapes = [(1, 1, w.n_queries, dd), (1, 1, w.N, dd), (1, 1, w.N, dd), (1, 1, w.n_queries, dd)]
+    return [draw(rng, sh, a) for sh, a in zip(shapes, (w.amp, w.amp, w.amp, 1.0))]
 
 
 def _oracle_head_seconds(w, x):
@@ -172,15 +183,24 @@ def _oracle_head_seconds(w, x):
     import oracle
     q, k, v, do = x
     t0 = time.perf_counter()
-    oracle.attention_forward(q, k, v, w.softmax_scale, w.causal)
+    off = (w.N - w.n_queries) if (w.kind == "cross" and w.causal) else 0
+    oracle.attention_forward(q, k, v, w.softmax_scale, w.causal, q_offset=off)
     if w.with_grad:
-        oracle.attention_backward(q, k, v, do, w.softmax_scale, w.causal)
+        oracle.attention_backward(q, k, v, do, w.softmax_scale, w.causal, q_offset=off)
     return time.perf_counter() - t0
 
 
 def _head_flops(w):
     from sdpa_inputs import flops_backward, flops_forward
+    if w.kind == "cross":
+        from sdpa_inputs import flops_cross
+        return flops_cross(1, 1, w.n_queries, w.N, w.d, w.causal) * (3.5 if w.with_grad else 1.0)
     return flops_forward(1, 1, w.N, w.d, w.causal) + (flops_backward(1, 1, w.N, w.d, w.causal) if w.with_grad else 0)
+
+
+def _head_dims(w):
+    n = f"Nq={w.n_queries}, Nk={w.N}" if w.kind == "cross" else f"N={w.N}"
+    return f"{n}, d={w.d_draw or w.d}"
 
 
 def _blas_threads():
@@ -205,7 +225,7 @@ def cpu_baseline(w, budget_s=15.0):
             break
     return {"value": _head_flops(w) * done / t_total / 1e12, "unit": UNIT, "cores": _blas_threads(),
             "kind": "oracle",
-            "sample": f"{done} whole head(s) (B=1, H=1, N={w.N}, d={w.d_draw or w.d}) of {w.name}, "
+            "sample": f"{done} whole head(s) (B=1, H=1, {_head_dims(w)}) of {w.name}, "
                       f"{'fwd+bwd' if w.with_grad else 'fwd'} in float64 numpy, {t_total:.1f} s"}
 
 
@@ -241,7 +261,7 @@ def run_reference(args, w, rank, world):
     """The reference arm: the CPU oracle, one whole head of the workload per step."""
     if rank != 0:
         return
-    if w.Nq is not None:
+    if w.kind == "decode":
         run_reference_decode(args, w)
         return
     x = _oracle_head_inputs(w)
@@ -249,7 +269,7 @@ def run_reference(args, w, rank, world):
         _oracle_head_seconds(w, x)
     t = sum(_oracle_head_seconds(w, x) for _ in range(args.steps))
     val = _head_flops(w) * args.steps / t / 1e12
-    sample = (f"one whole head (B=1, H=1, N={w.N}, d={w.d_draw or w.d}) of {w.name} per step, "
+    sample = (f"one whole head (B=1, H=1, {_head_dims(w)}) of {w.name} per step, "
               f"{'fwd+bwd' if w.with_grad else 'fwd'} in float64 numpy")
     line = {"impl": "reference", "metric": METRIC, "value": val, "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": t / args.steps * 1e3,
@@ -282,10 +302,11 @@ def run_ours(args, w, rank, world, local_rank):
     B, H, Hkv, N, d = w.B, w.H, w.Hkv, w.N, w.d
     s = w.softmax_scale
     o = torch.empty_like(q)
-    lse = torch.empty((B, H, N), dtype=torch.float32, device="cuda")
+    Nq = w.n_queries
+    lse = torch.empty((B, H, Nq), dtype=torch.float32, device="cuda")
     if w.with_grad:
         dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-        ws_bytes = sdpa.attn_bwd_workspace_size(B, H, Hkv, N, d)
+        ws_bytes = sdpa.attn_bwd_workspace_size(B, H, Hkv, Nq, d)
         ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
     stream = torch.cuda.current_stream()
     sp = stream.cuda_stream
@@ -298,22 +319,36 @@ def run_ours(args, w, rank, world, local_rank):
     def step(evs=None):
         if evs is not None:
             evs[0].record(stream)
-        chk(sdpa.attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
-                          B, H, Hkv, N, d, s, w.causal, sp), "attn_fwd")
+        if w.kind == "cross":
+            chk(sdpa.attn_fwd_cross(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                                    B, H, Hkv, Nq, N, d, s, w.causal, sp), "attn_fwd_cross")
+        else:
+            chk(sdpa.attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                              B, H, Hkv, N, d, s, w.causal, sp), "attn_fwd")
         if evs is not None:
             evs[1].record(stream)
         if w.with_grad:
             chk(sdpa.attn_bwd_prep(o.data_ptr(), lse.data_ptr(), do.data_ptr(), ws.data_ptr(), ws_bytes,
-                                   B, H, Hkv, N, d, sp), "attn_bwd_prep")
+                                   B, H, Hkv, Nq, d, sp), "attn_bwd_prep")
             if evs is not None:
                 evs[2].record(stream)
-            chk(sdpa.attn_bwd_grad(q.data_ptr(), k.data_ptr(), v.data_ptr(), do.data_ptr(), dk.data_ptr(),
-                                   dv.data_ptr(), ws.data_ptr(), ws_bytes, B, H, Hkv, N, d, s, w.causal, sp),
-                "attn_bwd_grad")
+            if w.kind == "cross":
+                chk(sdpa.attn_bwd_grad_cross(q.data_ptr(), k.data_ptr(), v.data_ptr(), do.data_ptr(),
+                                             dk.data_ptr(), dv.data_ptr(), ws.data_ptr(), ws_bytes,
+                                             B, H, Hkv, Nq, N, d, s, w.causal, sp), "attn_bwd_grad_cross")
+            else:
+                chk(sdpa.attn_bwd_grad(q.data_ptr(), k.data_ptr(), v.data_ptr(), do.data_ptr(), dk.data_ptr(),
+                                       dv.data_ptr(), ws.data_ptr(), ws_bytes, B, H, Hkv, N, d, s, w.causal, sp),
+                    "attn_bwd_grad")
             if evs is not None:
                 evs[3].record(stream)
-            chk(sdpa.attn_bwd_dq(q.data_ptr(), k.data_ptr(), v.data_ptr(), do.data_ptr(), dq.data_ptr(),
-                                 ws.data_ptr(), ws_bytes, B, H, Hkv, N, d, s, w.causal, sp), "attn_bwd_dq")
+            if w.kind == "cross":
+                chk(sdpa.attn_bwd_dq_cross(q.data_ptr(), k.data_ptr(), v.data_ptr(), do.data_ptr(),
+                                           dq.data_ptr(), ws.data_ptr(), ws_bytes,
+                                           B, H, Hkv, Nq, N, d, s, w.causal, sp), "attn_bwd_dq_cross")
+            else:
+                chk(sdpa.attn_bwd_dq(q.data_ptr(), k.data_ptr(), v.data_ptr(), do.data_ptr(), dq.data_ptr(),
+                                     ws.data_ptr(), ws_bytes, B, H, Hkv, N, d, s, w.causal, sp), "attn_bwd_dq")
             if evs is not None:
                 evs[4].record(stream)
 
@@ -322,6 +357,10 @@ def run_ours(args, w, rank, world, local_rank):
         if dist is not None:
             dist.barrier()
         torch.cuda.synchronize()
+
+    # Inputs below twice the L2: evict them before every timed step.
+    in_bytes = sum(t.numel() * t.element_size() for t in (q, k, v) + ((do,) if w.with_grad else ()))
+    flush = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device="cuda") if in_bytes < 2 * L2_BYTES else None
 
     for _ in range(max(args.warmup, 1)):
         step()
@@ -339,16 +378,27 @@ def run_ours(args, w, rank, world, local_rank):
     barrier()
     t0.record(stream)
     for i in range(K):
+        if flush is not None:
+            flush.zero_()
         step(evs[i])
     t1.record(stream)
     barrier()
     clk = clocks.stop()
-    ms = t0.elapsed_time(t1)
+    ms_region = t0.elapsed_time(t1)
     st = sdpa.attn_get_device_status(None)
     if st != 0:
         raise RuntimeError(f"device status after timed steps: {sdpa.attn_status_string(st)}")
     per_kernel = {n: sum(e[j].elapsed_time(e[j + 1]) for e in evs) / K for j, n in enumerate(names)}
+    # With a flush between steps the step time is the sum of the per-step
+    # event spans (first kernel's start to last kernel's end).
+    ms = sum(e[0].elapsed_time(e[-1]) for e in evs) if flush is not None else ms_region
     ms = max_over_ranks(ms)
+    ms_region = max_over_ranks(ms_region)
+    if flush is not None:
+        l2_note = (f"flush: a {2 * L2_BYTES / 1e6:.0f} MB buffer is written before each timed step "
+                   f"(inputs {in_bytes / 1e6:.0f} MB); step time = sum of per-step event spans")
+    else:
+        l2_note = f"no flush: inputs ({in_bytes / 1e6:.0f} MB) larger than twice the 129 MB L2"
 
     f_fwd, f_bwd = step_flops(w)
     flops = f_fwd + f_bwd
@@ -369,7 +419,7 @@ def run_ours(args, w, rank, world, local_rank):
                 "frac": achieved / peak, "peak_source": f"{peak_src} bf16 burst (cuBLAS 8192^3)",
                 "frac_of_nominal_2250": achieved / 2250.0}
     else:
-        nbytes = {"attn_bwd_prep": 2 * B * H * N * d * 2 + B * H * N * 4 + B * H * N * 2 * 4}[dom]
+        nbytes = {"attn_bwd_prep": 2 * B * H * Nq * d * 2 + B * H * Nq * 4 + B * H * Nq * 2 * 4}[dom]
         achieved = nbytes / (per_kernel[dom] / 1e3) / 1e9
         peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
         roof = {"kernel": dom, "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
@@ -419,7 +469,8 @@ def run_ours(args, w, rank, world, local_rank):
             "dtype": "bf16", "data": "synthetic (seeded N(0,1) draws rounded to bf16)",
             "config": {"workload": workload_desc(w), "B": B, "H": H, "Hkv": Hkv, "N": N, "d": d,
                        "causal": w.causal, "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-                       "l2": "no flush: inputs (Q, K, V, dO) larger than the 129 MB L2"},
+                       "l2": l2_note},
+            "ms_timed_region": ms_region / K,
             "fwd_tflops": f_fwd / (per_kernel["attn_fwd"] / 1e3) / 1e12,
             "kernel_ms": per_kernel,
             "roofline": roof, "cpu_baseline": cb, "e2e": e2e, "clocks": clk,
@@ -563,7 +614,7 @@ def main():
         torch.cuda.set_device(local_rank)
         dist.init_process_group("nccl")
     try:
-        if w.Nq is not None:
+        if w.kind == "decode":
             run_decode(args, w, rank, world, local_rank)
         else:
             run_ours(args, w, rank, world, local_rank)

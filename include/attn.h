@@ -147,6 +147,40 @@ attn_status_t attn_bwd_dq(const void* q, const void* k, const void* v, const voi
                           void* stream);
 
 /*
+ * Backward of attn_fwd_cross: Nq query rows, Nk key/value rows per head,
+ * the same causal alignment (query row i sees keys 0 .. Nk - Nq + i) and the
+ * same gradients as attn_bwd.
+ *   q, o, dout [in] bf16 (B, H, Nq, d);  lse [in] float32 (B, H, Nq)
+ *   k, v [in] bf16 (B, Hkv, Nk, d)
+ *   dq [out] bf16 (B, H, Nq, d);  dk, dv [out] bf16 (B, Hkv, Nk, d)
+ *   workspace  at least attn_bwd_workspace_size(B, H, Hkv, Nq, d) bytes
+ * causal requires Nq <= Nk (otherwise ATTN_ERR_UNSUPPORTED_SHAPE).  Nothing
+ * is launched when any check fails.  attn_bwd(..., N, ...) is
+ * attn_bwd_cross(..., N, N, ...).
+ */
+attn_status_t attn_bwd_cross(const void* q, const void* k, const void* v, const void* o,
+                             const float* lse, const void* dout,
+                             void* dq, void* dk, void* dv,
+                             void* workspace, size_t workspace_bytes,
+                             int B, int H, int Hkv, int Nq, int Nk, int d, float scale, int causal,
+                             void* stream);
+
+/*
+ * The grad and dq stages of attn_bwd_cross, for callers that schedule them
+ * separately (the prep stage is attn_bwd_prep with N = Nq).  Arguments and
+ * ordering rules as for attn_bwd_grad / attn_bwd_dq, with the shapes of
+ * attn_bwd_cross.
+ */
+attn_status_t attn_bwd_grad_cross(const void* q, const void* k, const void* v, const void* dout,
+                                  void* dk, void* dv, void* workspace, size_t workspace_bytes,
+                                  int B, int H, int Hkv, int Nq, int Nk, int d, float scale, int causal,
+                                  void* stream);
+attn_status_t attn_bwd_dq_cross(const void* q, const void* k, const void* v, const void* dout,
+                                void* dq, void* workspace, size_t workspace_bytes,
+                                int B, int H, int Hkv, int Nq, int Nk, int d, float scale, int causal,
+                                void* stream);
+
+/*
  * Decode: attention of Nq new queries per head against a cache of Nk keys
  * and values (a KV cache), computed in key chunks that are merged by their
  * logsumexp.  Page "Flash Attention原理", FAQ on inference (the KV cache moves

@@ -23,8 +23,9 @@ __all__ = [
     "AttnError", "Status", "load", "attn_fwd", "attn_bwd", "attn_bwd_workspace_size",
     "attn_bwd_prep", "attn_bwd_grad", "attn_bwd_dq", "attn_bwd_noalloc",
     "attn_get_device_status", "attn_get_timeout_info", "attn_status_string", "attn_selftest_wait_timeout",
-    "attn_decode", "attn_decode_workspace_size", "attn_fwd_cross",
-    "forward", "forward_cross", "backward", "decode", "build",
+    "attn_decode", "attn_decode_workspace_size", "attn_fwd_cross", "attn_bwd_cross",
+    "attn_bwd_grad_cross", "attn_bwd_dq_cross",
+    "forward", "forward_cross", "backward", "backward_cross", "decode", "build",
 ]
 
 
@@ -78,6 +79,15 @@ def load() -> ctypes.CDLL:
         lib.attn_status_string.restype = ctypes.c_char_p
         lib.attn_fwd_cross.argtypes = [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, ctypes.c_float, _I, _P]
         lib.attn_fwd_cross.restype = _I
+        lib.attn_bwd_cross.argtypes = [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t,
+                                       _I, _I, _I, _I, _I, _I, ctypes.c_float, _I, _P]
+        lib.attn_bwd_cross.restype = _I
+        lib.attn_bwd_grad_cross.argtypes = [_P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t,
+                                            _I, _I, _I, _I, _I, _I, ctypes.c_float, _I, _P]
+        lib.attn_bwd_grad_cross.restype = _I
+        lib.attn_bwd_dq_cross.argtypes = [_P, _P, _P, _P, _P, _P, ctypes.c_size_t,
+                                          _I, _I, _I, _I, _I, _I, ctypes.c_float, _I, _P]
+        lib.attn_bwd_dq_cross.restype = _I
         lib.attn_decode_workspace_size.argtypes = [_I, _I, _I, _I, _I, _I]
         lib.attn_decode_workspace_size.restype = ctypes.c_size_t
         lib.attn_decode.argtypes = [_P, _P, _P, _P, _P, _P, ctypes.c_size_t, _I, _I, _I, _I, _I, _I,
@@ -136,6 +146,24 @@ def attn_bwd_dq(q, k, v, dout, dq, workspace, workspace_bytes, B, H, Hkv, N, d, 
 
 def attn_fwd_cross(q, k, v, o, lse, B, H, Hkv, Nq, Nk, d, scale, causal, stream) -> int:
     return load().attn_fwd_cross(q, k, v, o, lse, B, H, Hkv, Nq, Nk, d, scale, causal, stream)
+
+
+def attn_bwd_cross(q, k, v, o, lse, dout, dq, dk, dv, workspace, workspace_bytes,
+                   B, H, Hkv, Nq, Nk, d, scale, causal, stream) -> int:
+    return load().attn_bwd_cross(q, k, v, o, lse, dout, dq, dk, dv, workspace, workspace_bytes,
+                                 B, H, Hkv, Nq, Nk, d, scale, causal, stream)
+
+
+def attn_bwd_grad_cross(q, k, v, dout, dk, dv, workspace, workspace_bytes, B, H, Hkv, Nq, Nk, d, scale,
+                        causal, stream) -> int:
+    return load().attn_bwd_grad_cross(q, k, v, dout, dk, dv, workspace, workspace_bytes, B, H, Hkv, Nq, Nk, d,
+                                      scale, causal, stream)
+
+
+def attn_bwd_dq_cross(q, k, v, dout, dq, workspace, workspace_bytes, B, H, Hkv, Nq, Nk, d, scale, causal,
+                      stream) -> int:
+    return load().attn_bwd_dq_cross(q, k, v, dout, dq, workspace, workspace_bytes, B, H, Hkv, Nq, Nk, d,
+                                    scale, causal, stream)
 
 
 def attn_decode_workspace_size(B, H, Hkv, Nq, Nk, d) -> int:
@@ -274,3 +302,36 @@ def forward_cross(q, k, v, scale: float | None = None, causal: bool = False):
     _check(attn_fwd_cross(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
                           B, H, Hkv, Nq, Nk, d, scale, causal, _stream_ptr(q)), "attn_fwd_cross")
     return o, lse
+
+
+def backward_cross(q, k, v, o, lse, dout, scale: float | None = None, causal: bool = False,
+                   workspace=None):
+    """dQ, dK, dV of forward_cross given its O and lse and dL/dO.
+
+    q, o, dout: bf16 (B, H, Nq, d); k, v: bf16 (B, Hkv, Nk, d); lse float32
+    (B, H, Nq); causal alignment as in forward_cross."""
+    import torch
+    if q.dim() != 4 or k.dim() != 4 or v.dim() != 4:
+        raise ValueError("q, k, v must be 4-D")
+    B, H, Nq, d = q.shape
+    Hkv, Nk = k.shape[1], k.shape[2]
+    if tuple(k.shape) != (B, Hkv, Nk, d) or tuple(v.shape) != (B, Hkv, Nk, d):
+        raise ValueError("k and v must be (B, Hkv, Nk, d) with q's B and d")
+    if tuple(o.shape) != tuple(q.shape) or tuple(dout.shape) != tuple(q.shape):
+        raise ValueError("o and dout must have q's shape")
+    for t in (q, k, v, o, dout):
+        if not t.is_contiguous() or t.dtype != torch.bfloat16:
+            raise ValueError("inputs must be contiguous bf16")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    dq = torch.empty_like(q)
+    dk = torch.empty_like(k)
+    dv = torch.empty_like(v)
+    ws_bytes = attn_bwd_workspace_size(B, H, Hkv, Nq, d)
+    if workspace is None:
+        workspace = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=q.device)
+    _check(attn_bwd_cross(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                          dout.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
+                          workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+                          B, H, Hkv, Nq, Nk, d, scale, causal, _stream_ptr(q)), "attn_bwd_cross")
+    return dq, dk, dv

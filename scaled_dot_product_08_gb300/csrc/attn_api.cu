@@ -246,10 +246,12 @@ size_t attn_bwd_workspace_size(int B, int H, int Hkv, int N, int d) {
   return rows * 4 * 2;  // -D and -lse*log2(e) per (head, padded row), float32
 }
 
-// Workspace carve-up shared by the three backward stages: [-D | -lse2].
-static void bwd_params(sdpa::BwdParams* p, void* workspace, int B, int H, int Hkv, int N, int d, float scale,
-                       const DeviceInfo* di) {
-  const int npad = ((N + 127) / 128) * 128;
+// Workspace carve-up shared by the three backward stages: [-D | -lse2], one
+// float per (head, padded query row).  Nq query rows, Nk key rows; causal
+// query row i sits at position Nk - Nq + i.
+static void bwd_params(sdpa::BwdParams* p, void* workspace, int B, int H, int Hkv, int Nq, int Nk, int d,
+                       float scale, int causal, const DeviceInfo* di) {
+  const int npad = ((Nq + 127) / 128) * 128;
   const size_t rows = (size_t)B * H * npad;
   memset(p, 0, sizeof(*p));
   p->dvec = static_cast<float*>(workspace);
@@ -257,11 +259,14 @@ static void bwd_params(sdpa::BwdParams* p, void* workspace, int B, int H, int Hk
   p->B = B;
   p->H = H;
   p->Hkv = Hkv;
-  p->N = N;
+  p->N = Nq;
   p->Npad = npad;
   p->G = H / Hkv;
   p->d = d;
-  p->nq = (N + 127) / 128;
+  p->nq = (Nq + 127) / 128;
+  p->Nk = Nk;
+  p->nkv = (Nk + 127) / 128;
+  p->koff = causal ? Nk - Nq : 0;
   p->scale = scale;
   p->scale_log2 = scale * 1.4426950408889634f;
   p->status = di->status;
@@ -274,73 +279,123 @@ static attn_status_t check_workspace(void* workspace, size_t workspace_bytes, in
   return ATTN_OK;
 }
 
-attn_status_t attn_bwd_prep(const void* o, const float* lse, const void* dout, void* workspace,
-                            size_t workspace_bytes, int B, int H, int Hkv, int N, int d, void* stream) {
-  ATTN_TRY(check_shape(B, H, Hkv, N, d));
-  ATTN_TRY(check_workspace(workspace, workspace_bytes, B, H, Hkv, N, d));
+static attn_status_t check_bwd_shape(int B, int H, int Hkv, int Nq, int Nk, int d, int causal) {
+  ATTN_TRY(check_shape(B, H, Hkv, Nq, d));
+  ATTN_TRY(check_shape(B, H, Hkv, Nk, d));
+  if (causal == 1 && Nq > Nk) return ATTN_ERR_UNSUPPORTED_SHAPE;  // a causal row would see no key
+  return ATTN_OK;
+}
+
+static attn_status_t bwd_prep_x(const void* o, const float* lse, const void* dout, void* workspace,
+                                size_t workspace_bytes, int B, int H, int Hkv, int Nq, int d, void* stream) {
+  ATTN_TRY(check_shape(B, H, Hkv, Nq, d));
+  ATTN_TRY(check_workspace(workspace, workspace_bytes, B, H, Hkv, Nq, d));
   ATTN_TRY(check_ptrs({o, lse, dout, workspace}));
   DeviceInfo* di = nullptr;
   ATTN_TRY(current_device(&di));
   sdpa::BwdParams p;
-  bwd_params(&p, workspace, B, H, Hkv, N, d, 1.f, di);
+  bwd_params(&p, workspace, B, H, Hkv, Nq, Nq, d, 1.f, 0, di);
   p.o = static_cast<const uint16_t*>(o);
   p.dout = static_cast<const uint16_t*>(dout);
   p.lse = lse;
   return sdpa::launch_bwd_prep(p, static_cast<cudaStream_t>(stream)) == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;
 }
 
-attn_status_t attn_bwd_grad(const void* q, const void* k, const void* v, const void* dout, void* dk, void* dv,
-                            void* workspace, size_t workspace_bytes, int B, int H, int Hkv, int N, int d,
-                            float scale, int causal, void* stream) {
-  ATTN_TRY(check_shape(B, H, Hkv, N, d));
+static attn_status_t bwd_grad_x(const void* q, const void* k, const void* v, const void* dout, void* dk, void* dv,
+                                void* workspace, size_t workspace_bytes, int B, int H, int Hkv, int Nq, int Nk, int d,
+                                float scale, int causal, void* stream) {
   ATTN_TRY(check_scale_flag(scale, causal));
-  ATTN_TRY(check_workspace(workspace, workspace_bytes, B, H, Hkv, N, d));
+  ATTN_TRY(check_bwd_shape(B, H, Hkv, Nq, Nk, d, causal));
+  ATTN_TRY(check_workspace(workspace, workspace_bytes, B, H, Hkv, Nq, d));
   ATTN_TRY(check_ptrs({q, k, v, dout, dk, dv, workspace}));
   DeviceInfo* di = nullptr;
   ATTN_TRY(current_device(&di));
   CUtensorMap tq, tk, tv, tdo, tdk, tdv;
-  if (!make_map_bf16(&tq, q, d, N, (long long)B * H) || !make_map_bf16(&tk, k, d, N, (long long)B * Hkv) ||
-      !make_map_bf16(&tv, v, d, N, (long long)B * Hkv) || !make_map_bf16(&tdo, dout, d, N, (long long)B * H) ||
-      !make_map_bf16(&tdk, dk, d, N, (long long)B * Hkv) || !make_map_bf16(&tdv, dv, d, N, (long long)B * Hkv))
+  if (!make_map_bf16(&tq, q, d, Nq, (long long)B * H) || !make_map_bf16(&tk, k, d, Nk, (long long)B * Hkv) ||
+      !make_map_bf16(&tv, v, d, Nk, (long long)B * Hkv) || !make_map_bf16(&tdo, dout, d, Nq, (long long)B * H) ||
+      !make_map_bf16(&tdk, dk, d, Nk, (long long)B * Hkv) || !make_map_bf16(&tdv, dv, d, Nk, (long long)B * Hkv))
     return ATTN_ERR_CUDA;
   sdpa::BwdParams p;
-  bwd_params(&p, workspace, B, H, Hkv, N, d, scale, di);
+  bwd_params(&p, workspace, B, H, Hkv, Nq, Nk, d, scale, causal, di);
   cudaError_t e = sdpa::launch_bwd_grad(d, causal != 0, tq, tk, tv, tdo, tdk, tdv, p,
                                         static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;
 }
 
-attn_status_t attn_bwd_dq(const void* q, const void* k, const void* v, const void* dout, void* dq, void* workspace,
-                          size_t workspace_bytes, int B, int H, int Hkv, int N, int d, float scale, int causal,
-                          void* stream) {
-  ATTN_TRY(check_shape(B, H, Hkv, N, d));
+static attn_status_t bwd_dq_x(const void* q, const void* k, const void* v, const void* dout, void* dq, void* workspace,
+                              size_t workspace_bytes, int B, int H, int Hkv, int Nq, int Nk, int d, float scale,
+                              int causal, void* stream) {
   ATTN_TRY(check_scale_flag(scale, causal));
-  ATTN_TRY(check_workspace(workspace, workspace_bytes, B, H, Hkv, N, d));
+  ATTN_TRY(check_bwd_shape(B, H, Hkv, Nq, Nk, d, causal));
+  ATTN_TRY(check_workspace(workspace, workspace_bytes, B, H, Hkv, Nq, d));
   ATTN_TRY(check_ptrs({q, k, v, dout, dq, workspace}));
   DeviceInfo* di = nullptr;
   ATTN_TRY(current_device(&di));
   CUtensorMap tq, tk, tv, tdo, tdq;
-  if (!make_map_bf16(&tq, q, d, N, (long long)B * H) || !make_map_bf16(&tk, k, d, N, (long long)B * Hkv) ||
-      !make_map_bf16(&tv, v, d, N, (long long)B * Hkv) || !make_map_bf16(&tdo, dout, d, N, (long long)B * H) ||
-      !make_map_bf16(&tdq, dq, d, N, (long long)B * H))
+  if (!make_map_bf16(&tq, q, d, Nq, (long long)B * H) || !make_map_bf16(&tk, k, d, Nk, (long long)B * Hkv) ||
+      !make_map_bf16(&tv, v, d, Nk, (long long)B * Hkv) || !make_map_bf16(&tdo, dout, d, Nq, (long long)B * H) ||
+      !make_map_bf16(&tdq, dq, d, Nq, (long long)B * H))
     return ATTN_ERR_CUDA;
   sdpa::BwdParams p;
-  bwd_params(&p, workspace, B, H, Hkv, N, d, scale, di);
+  bwd_params(&p, workspace, B, H, Hkv, Nq, Nk, d, scale, causal, di);
   cudaError_t e = sdpa::launch_bwd_dq(d, causal != 0, tq, tk, tv, tdo, tdq, p, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;
+}
+
+static attn_status_t bwd_all(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                             const void* dout, void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes,
+                             int B, int H, int Hkv, int Nq, int Nk, int d, float scale, int causal, void* stream) {
+  // Validate everything up front so that nothing is launched on a bad call.
+  ATTN_TRY(check_scale_flag(scale, causal));
+  ATTN_TRY(check_bwd_shape(B, H, Hkv, Nq, Nk, d, causal));
+  ATTN_TRY(check_workspace(workspace, workspace_bytes, B, H, Hkv, Nq, d));
+  ATTN_TRY(check_ptrs({q, k, v, o, lse, dout, dq, dk, dv, workspace}));
+  ATTN_TRY(bwd_prep_x(o, lse, dout, workspace, workspace_bytes, B, H, Hkv, Nq, d, stream));
+  ATTN_TRY(bwd_grad_x(q, k, v, dout, dk, dv, workspace, workspace_bytes, B, H, Hkv, Nq, Nk, d, scale, causal, stream));
+  return bwd_dq_x(q, k, v, dout, dq, workspace, workspace_bytes, B, H, Hkv, Nq, Nk, d, scale, causal, stream);
+}
+
+attn_status_t attn_bwd_prep(const void* o, const float* lse, const void* dout, void* workspace,
+                            size_t workspace_bytes, int B, int H, int Hkv, int N, int d, void* stream) {
+  return bwd_prep_x(o, lse, dout, workspace, workspace_bytes, B, H, Hkv, N, d, stream);
+}
+
+attn_status_t attn_bwd_grad(const void* q, const void* k, const void* v, const void* dout, void* dk, void* dv,
+                            void* workspace, size_t workspace_bytes, int B, int H, int Hkv, int N, int d,
+                            float scale, int causal, void* stream) {
+  return bwd_grad_x(q, k, v, dout, dk, dv, workspace, workspace_bytes, B, H, Hkv, N, N, d, scale, causal, stream);
+}
+
+attn_status_t attn_bwd_dq(const void* q, const void* k, const void* v, const void* dout, void* dq, void* workspace,
+                          size_t workspace_bytes, int B, int H, int Hkv, int N, int d, float scale, int causal,
+                          void* stream) {
+  return bwd_dq_x(q, k, v, dout, dq, workspace, workspace_bytes, B, H, Hkv, N, N, d, scale, causal, stream);
 }
 
 attn_status_t attn_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
                        const void* dout, void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes,
                        int B, int H, int Hkv, int N, int d, float scale, int causal, void* stream) {
-  // Validate everything up front so that nothing is launched on a bad call.
-  ATTN_TRY(check_shape(B, H, Hkv, N, d));
-  ATTN_TRY(check_scale_flag(scale, causal));
-  ATTN_TRY(check_workspace(workspace, workspace_bytes, B, H, Hkv, N, d));
-  ATTN_TRY(check_ptrs({q, k, v, o, lse, dout, dq, dk, dv, workspace}));
-  ATTN_TRY(attn_bwd_prep(o, lse, dout, workspace, workspace_bytes, B, H, Hkv, N, d, stream));
-  ATTN_TRY(attn_bwd_grad(q, k, v, dout, dk, dv, workspace, workspace_bytes, B, H, Hkv, N, d, scale, causal, stream));
-  return attn_bwd_dq(q, k, v, dout, dq, workspace, workspace_bytes, B, H, Hkv, N, d, scale, causal, stream);
+  return bwd_all(q, k, v, o, lse, dout, dq, dk, dv, workspace, workspace_bytes, B, H, Hkv, N, N, d, scale, causal,
+                 stream);
+}
+
+attn_status_t attn_bwd_grad_cross(const void* q, const void* k, const void* v, const void* dout, void* dk, void* dv,
+                                  void* workspace, size_t workspace_bytes, int B, int H, int Hkv, int Nq, int Nk,
+                                  int d, float scale, int causal, void* stream) {
+  return bwd_grad_x(q, k, v, dout, dk, dv, workspace, workspace_bytes, B, H, Hkv, Nq, Nk, d, scale, causal, stream);
+}
+
+attn_status_t attn_bwd_dq_cross(const void* q, const void* k, const void* v, const void* dout, void* dq,
+                                void* workspace, size_t workspace_bytes, int B, int H, int Hkv, int Nq, int Nk,
+                                int d, float scale, int causal, void* stream) {
+  return bwd_dq_x(q, k, v, dout, dq, workspace, workspace_bytes, B, H, Hkv, Nq, Nk, d, scale, causal, stream);
+}
+
+attn_status_t attn_bwd_cross(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                             const void* dout, void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes,
+                             int B, int H, int Hkv, int Nq, int Nk, int d, float scale, int causal, void* stream) {
+  return bwd_all(q, k, v, o, lse, dout, dq, dk, dv, workspace, workspace_bytes, B, H, Hkv, Nq, Nk, d, scale, causal,
+                 stream);
 }
 
 // Key chunks of the decode kernel, a pure function of the shape (so the

@@ -132,11 +132,12 @@ __global__ void __launch_bounds__(384, 1)
   const float* const vec_g = reinterpret_cast<const float*>(smem_raw + (sVec - base));
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int nkv = p.nq;
+  const int nkv = p.nkv;
   const int bhk = blockIdx.x / nkv;           // b * Hkv + hk
   const int j = blockIdx.x % nkv;             // key tile (0 = most causal work)
   const int b = bhk / p.Hkv, hk = bhk % p.Hkv;
-  const int i0 = CAUSAL ? j : 0;
+  // Causal: the first query tile with a row at position >= 128 j.
+  const int i0 = CAUSAL ? max(0, (j * 128 - p.koff) / 128) : 0;
   const int ni = p.nq - i0;                   // query tiles per head
   const int total = p.G * ni;                 // steps: (head in group) x (query tile)
 
@@ -181,7 +182,7 @@ __global__ void __launch_bounds__(384, 1)
     const uint32_t tP = tmem + 64 * X + lane_off;           // P^T (bf16 pairs), first 32 of them
     const uint32_t tdP = tmem + 128 + 64 * X + lane_off;    // dP^T columns of this half; dS^T pairs after
     // Key rows past N (the last tile's padding) get P^T = 0.
-    const bool key_pad = j * 128 + r >= p.N;
+    const bool key_pad = j * 128 + r >= p.Nk;
     const float c = p.scale_log2;
     const float2 c2 = make_float2(c, c);
     bool ok = true;
@@ -220,10 +221,15 @@ __global__ void __launch_bounds__(384, 1)
         x[4 * q4 + 2] = ex2(t1.x);
         x[4 * q4 + 3] = ex2(t1.y);
       }
-      if (CAUSAL && i == j) {
+      if (CAUSAL) {
+        // Key 128 j + r is invisible to query columns below qmin (query
+        // position koff + 128 i + 64 X + q < key).
+        const int qmin = 128 * (j - i) + r - p.koff - 64 * X;
+        if (__any_sync(0xffffffffu, qmin > 0)) {
 #pragma unroll
-        for (int q = 0; q < 64; ++q)
-          if (r > 64 * X + q) x[q] = 0.f;
+          for (int q = 0; q < 64; ++q)
+            if (q < qmin) x[q] = 0.f;
+        }
       }
       if (key_pad) {
 #pragma unroll
@@ -470,7 +476,7 @@ static cudaError_t launch_main_t(const CUtensorMap& tq, const CUtensorMap& tk, c
   auto kern = bwd_main_kernel<D, C>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, BwdTraits<D>::SMEM);
   if (e != cudaSuccess) return e;
-  const unsigned grid = (unsigned)p.nq * (unsigned)(p.B * p.Hkv);
+  const unsigned grid = (unsigned)p.nkv * (unsigned)(p.B * p.Hkv);
   kern<<<grid, BwdTraits<D>::THREADS, BwdTraits<D>::SMEM, stream>>>(tq, tk, tv, tdo, tdk, tdv, p);
   return cudaGetLastError();
 }

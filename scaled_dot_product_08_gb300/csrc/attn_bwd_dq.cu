@@ -77,7 +77,9 @@ __global__ void __launch_bounds__(384, 1)
   const int bh = blockIdx.x / p.nq;
   const int i = p.nq - 1 - (int)(blockIdx.x % p.nq);  // query tile
   const int bhk = (bh / p.H) * p.Hkv + (bh % p.H) / p.G;
-  const int n = CAUSAL ? i + 1 : p.nq;                 // key tiles visited
+  // Key tiles visited: causal, up to the tile holding the last row's last
+  // visible key koff + 128 i + 127.
+  const int n = CAUSAL ? min(p.nkv, (p.koff + i * 128 + 127) / 128 + 1) : p.nkv;
 
   if (threadIdx.x == 0) {
     mbar_init(bQ, 1);
@@ -142,18 +144,24 @@ __global__ void __launch_bounds__(384, 1)
           x[32 + e] = __uint_as_float(rb[e]);
         }
       }
-      // P[r][k] = exp2(S * scale * log2e - lse2[r]); keys past the diagonal
-      // (key > query on the diagonal tile) are exactly 0.
+      // P[r][k] = exp2(S * scale * log2e - lse2[r]); invisible keys (past
+      // the row's causal position, or past Nk) are exactly 0.
 #pragma unroll
       for (int e = 0; e < 32; ++e) {
         const float2 t = ffma2(make_float2(x[2 * e], x[2 * e + 1]), c2, l22);
         x[2 * e] = ex2(t.x);
         x[2 * e + 1] = ex2(t.y);
       }
-      if (CAUSAL && j == i) {
+      {
+        // Key columns at or past lim are invisible to row r: keys past Nk,
+        // and for causal rows keys past position koff + 128 i + r.
+        int lim = p.Nk - j * 128 - 64 * X;
+        if (CAUSAL) lim = min(lim, p.koff + 128 * (i - j) + r - 64 * X + 1);
+        if (__any_sync(0xffffffffu, lim < 64)) {
 #pragma unroll
-        for (int k = 0; k < 64; ++k)
-          if (64 * X + k > r) x[k] = 0.f;
+          for (int k = 0; k < 64; ++k)
+            if (k >= lim) x[k] = 0.f;
+        }
       }
       ok = __all_sync(0xffffffffu, wait_bounded(wc, bDp, j & 1, wait_site(0x82, j)));
       if (!ok) break;

@@ -30,8 +30,10 @@ struct BwdParams {
   const float* lse;      // (B, H, N)
   float* dvec;           // (B, H, Npad) float32 workspace: -D = -rowsum(dO * O)
   float* lse2;           // (B, H, Npad) float32 workspace: -lse * log2(e), -inf on padding rows
-  int B, H, Hkv, N, Npad, G, d;
-  int nq;                // ceil(N / 128)
+  int B, H, Hkv, N, Npad, G, d;  // N: query rows per head (Npad: rounded up to 128)
+  int nq;                // ceil(N / 128): query tiles
+  int Nk, nkv;           // key/value rows per head, ceil(Nk / 128) key tiles
+  int koff;              // causal: query row i sits at position koff + i (Nk - N)
   float scale;           // softmax scale
   float scale_log2;      // scale * log2(e)
   int* status;

@@ -25,6 +25,15 @@ model):
   dec1 B=8  H=64  Hkv=8  Nq=1 N=32768 d=128  non-causal  seed 6
   dec4 same shape, Nq=4 new tokens (a speculative block), causal  seed 7
 
+Chunked prefill (Nq new queries per head against N keys, the tiled forward):
+
+  cp1  B=1  H=32  Hkv=8  Nq=2048 N=16384 d=128  causal   seed 8
+
+Encoder-decoder cross attention (Nq decoder queries against N encoder keys,
+no mask), forward + backward:
+
+  cx   B=8  H=16  Hkv=16 Nq=2048 N=4096  d=128  non-causal  seed 9
+
 Every draw is numpy's PCG64 ``default_rng(seed).standard_normal(dtype=float32)``
 taken in the fixed order Q, K, V, dO, multiplied by the config's amplitude and
 then rounded to bf16 (round to nearest, ties to even).
@@ -51,7 +60,8 @@ class Workload:
     d_draw: int | None = None      # head_dim actually drawn (zero-padded up to d)
     with_grad: bool = False        # also draw dO
     scale: float | None = None     # default 1/sqrt(d_draw or d)
-    Nq: int | None = None          # decode: new queries per head (None: Nq = N)
+    Nq: int | None = None          # decode / cross: query rows per head (None: Nq = N)
+    kind: str = "full"             # "full" (Nq = N), "decode" (attn_decode), "cross" (attn_fwd_cross)
 
     @property
     def softmax_scale(self) -> float:
@@ -76,8 +86,10 @@ WORKLOADS: dict[str, Workload] = {
     "c4": Workload("c4", 1, 32, 8, 8192, 128, True, 4, amp=0.5),
     "c4p": Workload("c4p", 1, 32, 8, 8192, 96, True, 4, amp=0.5, d_draw=80),
     "c5": Workload("c5", 8, 16, 16, 4096, 128, True, 5, with_grad=True),
-    "dec1": Workload("dec1", 8, 64, 8, 32768, 128, False, 6, Nq=1),
-    "dec4": Workload("dec4", 8, 64, 8, 32768, 128, True, 7, Nq=4),
+    "dec1": Workload("dec1", 8, 64, 8, 32768, 128, False, 6, Nq=1, kind="decode"),
+    "dec4": Workload("dec4", 8, 64, 8, 32768, 128, True, 7, Nq=4, kind="decode"),
+    "cp1": Workload("cp1", 1, 32, 8, 16384, 128, True, 8, Nq=2048, kind="cross"),
+    "cx": Workload("cx", 8, 16, 16, 4096, 128, False, 9, with_grad=True, Nq=2048, kind="cross"),
 }
 
 
@@ -127,6 +139,14 @@ def make_inputs(w: Workload) -> dict[str, np.ndarray]:
 def make_random(shape, seed: int, amp: float = 1.0) -> np.ndarray:
     """One seeded bf16-exact float32 tensor (small parity sweeps)."""
     return draw(np.random.default_rng(seed), shape, amp)
+
+
+def flops_cross(B: int, H: int, Nq: int, Nk: int, d: int, causal: bool) -> float:
+    """Forward work of Nq queries against Nk keys: 4*B*H*d per visible
+    (query, key) pair; causal rows sit at positions Nk - Nq + i, and the
+    square Nq x Nq corner is counted halved as in the Nq = Nk convention."""
+    pairs = Nq * (Nk - Nq) + Nq * Nq / 2 if causal else Nq * Nk
+    return 4.0 * B * H * d * pairs
 
 
 def flops_forward(B: int, H: int, N: int, d: int, causal: bool) -> float:

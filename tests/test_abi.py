@@ -140,3 +140,37 @@ def test_fwd_cross_rejects_bad_arguments(lib):
     assert f(1, 2, 2, 10, 0, 128, 0.1, 0, None) == S.UNSUPPORTED_SHAPE      # Nk < 1
     assert f(1, 2, 2, 10, 20, 80, 0.1, 0, None) == S.UNSUPPORTED_SHAPE      # d
     assert f(1, 2, 2, 10, 20, 128, -1.0, 0, None) == S.INVALID_ARG
+
+
+def test_bwd_cross_rejects_bad_arguments(lib):
+    import scaled_dot_product_08_gb300 as sdpa
+    S = sdpa.Status
+    ws = sdpa.attn_bwd_workspace_size(1, 2, 2, 300, 128)
+
+    def f(Nq, Nk, d, scale, causal, wsb=ws, w=FAKE, q=FAKE):
+        return sdpa.attn_bwd_cross(q, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, w, wsb,
+                                   1, 2, 2, Nq, Nk, d, scale, causal, None)
+    assert f(300, 200, 128, 0.1, 1) == S.UNSUPPORTED_SHAPE   # causal with Nq > Nk
+    assert f(0, 200, 128, 0.1, 0) == S.UNSUPPORTED_SHAPE     # Nq < 1
+    assert f(10, 0, 128, 0.1, 0) == S.UNSUPPORTED_SHAPE      # Nk < 1
+    assert f(10, 20, 80, 0.1, 0) == S.UNSUPPORTED_SHAPE      # d
+    assert f(10, 20, 128, -1.0, 0) == S.INVALID_ARG
+    assert f(10, 20, 128, 0.1, 2) == S.INVALID_ARG
+    # the workspace is sized by the query rows
+    assert f(300, 400, 128, 0.1, 1, wsb=ws - 1) == S.WORKSPACE
+    assert f(300, 400, 128, 0.1, 1, w=0) == S.WORKSPACE
+    assert f(300, 400, 128, 0.1, 1, q=FAKE + 2) == S.MISALIGNED
+
+
+def test_bwd_cross_stages_reject_bad_arguments(lib):
+    import scaled_dot_product_08_gb300 as sdpa
+    S = sdpa.Status
+    ws = sdpa.attn_bwd_workspace_size(1, 2, 2, 300, 128)
+    g = lambda Nq, Nk, causal: sdpa.attn_bwd_grad_cross(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, ws,
+                                                        1, 2, 2, Nq, Nk, 128, 0.1, causal, None)
+    q = lambda Nq, Nk, causal: sdpa.attn_bwd_dq_cross(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, ws,
+                                                      1, 2, 2, Nq, Nk, 128, 0.1, causal, None)
+    for f in (g, q):
+        assert f(300, 200, 1) == S.UNSUPPORTED_SHAPE
+        assert f(300, 0, 0) == S.UNSUPPORTED_SHAPE
+        assert f(385, 400, 0) == S.WORKSPACE      # workspace sized for 300 (padded: 384) query rows
