@@ -31,6 +31,8 @@ from .sdpa import (
     attention_backward,
     attention_decode,
     attention_cross_backward,
+    attention_varlen_forward,
+    attention_varlen_backward,
     merge_splits,
     softmax_rows,
     softmax_two_block,
@@ -46,6 +48,8 @@ __all__ = [
     "attention_backward",
     "attention_decode",
     "attention_cross_backward",
+    "attention_varlen_forward",
+    "attention_varlen_backward",
     "merge_splits",
     "softmax_rows",
     "softmax_two_block",

@@ -275,6 +275,77 @@ def attention_backward(q, k, v, do, scale=None, causal=False, q_offset=0):
     return dq, dk, dv
 
 
+def _varlen_bounds(cu, total):
+    cu = [int(x) for x in np.asarray(cu).reshape(-1)]
+    if len(cu) < 1 or cu[0] != 0 or cu[-1] != total or any(b < a for a, b in zip(cu, cu[1:])):
+        raise ValueError("cu_seqlens must start at 0, be non-decreasing and end at the packed length")
+    return cu
+
+
+def attention_varlen_forward(q, k, v, cu_q, cu_k, scale=None, causal=False):
+    """Attention over a packed batch of variable-length sequences.
+
+    [FA] FAQ Q10: several sequences of different lengths are packed into one
+    batch and delimited by cumulative offsets (cu_seqlens), so that no padding
+    is computed.  Layout read here: q (total_q, H, d), k and v (total_k, Hkv,
+    d), the sequences one after another; sequence b owns query rows
+    cu_q[b] .. cu_q[b+1]-1 and key rows cu_k[b] .. cu_k[b+1]-1 and attends
+    only within itself.  Causal: per sequence, query row i sits at position
+    Nk_b - Nq_b + i (the alignment of ``attention_decode``).  A row that sees
+    no key has O = 0 and lse = -inf.
+    Returns O (total_q, H, d_v) and lse (H, total_q)."""
+    q = np.asarray(q, dtype=np.float64)
+    k = np.asarray(k, dtype=np.float64)
+    v = np.asarray(v, dtype=np.float64)
+    cq = _varlen_bounds(cu_q, q.shape[0])
+    ck = _varlen_bounds(cu_k, k.shape[0])
+    if len(cq) != len(ck):
+        raise ValueError("cu_seqlens_q and cu_seqlens_k describe different batch sizes")
+    H = q.shape[1]
+    O = np.zeros((q.shape[0], H, v.shape[2]))
+    lse = np.full((H, q.shape[0]), -np.inf)
+    for b in range(len(cq) - 1):
+        q0, q1, k0, k1 = cq[b], cq[b + 1], ck[b], ck[b + 1]
+        if q1 == q0:
+            continue
+        qb = q[q0:q1].transpose(1, 0, 2)[None]
+        kb = k[k0:k1].transpose(1, 0, 2)[None]
+        vb = v[k0:k1].transpose(1, 0, 2)[None]
+        off = (k1 - k0) - (q1 - q0) if causal else 0
+        Ob, lb = attention_forward(qb, kb, vb, scale, causal, q_offset=off)
+        O[q0:q1] = Ob[0].transpose(1, 0, 2)
+        lse[:, q0:q1] = lb[0]
+    return O, lse
+
+
+def attention_varlen_backward(q, k, v, do, cu_q, cu_k, scale=None, causal=False):
+    """Gradients of ``attention_varlen_forward``: per sequence, the chain rule
+    of ``attention_backward`` with that sequence's causal offset.  Returns
+    dQ (total_q, H, d), dK and dV (total_k, Hkv, d); keys of a sequence with
+    no query rows get zero gradients."""
+    q = np.asarray(q, dtype=np.float64)
+    k = np.asarray(k, dtype=np.float64)
+    v = np.asarray(v, dtype=np.float64)
+    do = np.asarray(do, dtype=np.float64)
+    cq = _varlen_bounds(cu_q, q.shape[0])
+    ck = _varlen_bounds(cu_k, k.shape[0])
+    if len(cq) != len(ck):
+        raise ValueError("cu_seqlens_q and cu_seqlens_k describe different batch sizes")
+    dq, dk, dv = np.zeros_like(q), np.zeros_like(k), np.zeros_like(v)
+    for b in range(len(cq) - 1):
+        q0, q1, k0, k1 = cq[b], cq[b + 1], ck[b], ck[b + 1]
+        if q1 == q0 or k1 == k0:
+            continue
+        t = lambda x, a, c: x[a:c].transpose(1, 0, 2)[None]
+        off = (k1 - k0) - (q1 - q0) if causal else 0
+        g = attention_backward(t(q, q0, q1), t(k, k0, k1), t(v, k0, k1), t(do, q0, q1), scale, causal,
+                               q_offset=off)
+        dq[q0:q1] = g[0][0].transpose(1, 0, 2)
+        dk[k0:k1] = g[1][0].transpose(1, 0, 2)
+        dv[k0:k1] = g[2][0].transpose(1, 0, 2)
+    return dq, dk, dv
+
+
 def score_matrix_bytes(n: int, bytes_per_elem: int = 4) -> int:
     """Bytes of one n x n score (or probability) matrix ([FA] §一)."""
     return n * n * bytes_per_elem
