@@ -181,6 +181,57 @@ attn_status_t attn_bwd_dq_cross(const void* q, const void* k, const void* v, con
                                 void* stream);
 
 /*
+ * Packed variable-length batch.  Page "Flash Attention原理", FAQ Q10:
+ * sequences of different lengths are packed into one batch, delimited by
+ * cumulative offsets (cu_seqlens), so no padding is computed.  Sequence b
+ * owns query rows cu_seqlens_q[b] .. cu_seqlens_q[b+1]-1 and key rows
+ * cu_seqlens_k[b] .. cu_seqlens_k[b+1]-1 and attends only within itself.
+ *   q, o   [in/out] bf16 (total_q, H, d)   packed, token-major
+ *   k, v   [in]     bf16 (total_k, Hkv, d)
+ *   lse    [out]    float32 (H, total_q)
+ *   cu_seqlens_q, cu_seqlens_k  [in] DEVICE int32 arrays of B + 1 offsets:
+ *          0 = cu[0] <= cu[1] <= ... <= cu[B] = total (4-byte aligned)
+ *   max_seqlen_q, max_seqlen_k  upper bounds of the sequence lengths (they
+ *          size the launch)
+ * Causal: per sequence, query row i sits at position Nk_b - Nq_b + i and
+ * sees keys 0 .. Nk_b - Nq_b + i.  Sequences may be empty, and Nq_b > Nk_b
+ * is allowed: a row that sees no key gets O = 0 and lse = -inf (the result
+ * of softmax over an empty set taken as zero weight everywhere).
+ * The offsets are read on the device: inconsistent ones (decreasing, past
+ * total, or longer than the stated maximum) skip the affected sequences and
+ * make attn_get_device_status() return ATTN_ERR_INVALID_ARG.  Requires
+ * total_q, total_k >= 1 and H * d * 128 < 2^32.
+ */
+attn_status_t attn_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse,
+                              const int* cu_seqlens_q, const int* cu_seqlens_k,
+                              int B, int H, int Hkv, int total_q, int total_k,
+                              int max_seqlen_q, int max_seqlen_k, int d, float scale, int causal,
+                              void* stream);
+
+/*
+ * Bytes of device workspace attn_bwd_varlen needs: two float32 row vectors
+ * per head, each sequence's rows in a 16-byte aligned region padded to a
+ * multiple of 128, i.e. 8 * H * (round_up(total_q + 132 * B, 4) + 128).
+ * Returns 0 for an invalid shape.
+ */
+size_t attn_bwd_varlen_workspace_size(int B, int H, int Hkv, int total_q, int d);
+
+/*
+ * Backward of attn_fwd_varlen: the gradients of attn_bwd per sequence, in
+ * the packed layouts of attn_fwd_varlen (dq like q, dk / dv like k / v).
+ * Keys that no query sees (an empty query sequence) get dK = dV = 0; rows
+ * that saw no key get dQ = 0.  Same offset checks as attn_fwd_varlen.
+ */
+attn_status_t attn_bwd_varlen(const void* q, const void* k, const void* v, const void* o,
+                              const float* lse, const void* dout,
+                              void* dq, void* dk, void* dv,
+                              const int* cu_seqlens_q, const int* cu_seqlens_k,
+                              void* workspace, size_t workspace_bytes,
+                              int B, int H, int Hkv, int total_q, int total_k,
+                              int max_seqlen_q, int max_seqlen_k, int d, float scale, int causal,
+                              void* stream);
+
+/*
  * Decode: attention of Nq new queries per head against a cache of Nk keys
  * and values (a KV cache), computed in key chunks that are merged by their
  * logsumexp.  Page "Flash Attention原理", FAQ on inference (the KV cache moves

@@ -24,7 +24,8 @@ __all__ = [
     "attn_bwd_prep", "attn_bwd_grad", "attn_bwd_dq", "attn_bwd_noalloc",
     "attn_get_device_status", "attn_get_timeout_info", "attn_status_string", "attn_selftest_wait_timeout",
     "attn_decode", "attn_decode_workspace_size", "attn_fwd_cross", "attn_bwd_cross",
-    "attn_bwd_grad_cross", "attn_bwd_dq_cross",
+    "attn_bwd_grad_cross", "attn_bwd_dq_cross", "attn_fwd_varlen", "attn_bwd_varlen",
+    "attn_bwd_varlen_workspace_size", "forward_varlen", "backward_varlen",
     "forward", "forward_cross", "backward", "backward_cross", "decode", "build",
 ]
 
@@ -88,6 +89,14 @@ def load() -> ctypes.CDLL:
         lib.attn_bwd_dq_cross.argtypes = [_P, _P, _P, _P, _P, _P, ctypes.c_size_t,
                                           _I, _I, _I, _I, _I, _I, ctypes.c_float, _I, _P]
         lib.attn_bwd_dq_cross.restype = _I
+        lib.attn_fwd_varlen.argtypes = [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I,
+                                        ctypes.c_float, _I, _P]
+        lib.attn_fwd_varlen.restype = _I
+        lib.attn_bwd_varlen_workspace_size.argtypes = [_I, _I, _I, _I, _I]
+        lib.attn_bwd_varlen_workspace_size.restype = ctypes.c_size_t
+        lib.attn_bwd_varlen.argtypes = [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t,
+                                        _I, _I, _I, _I, _I, _I, _I, _I, ctypes.c_float, _I, _P]
+        lib.attn_bwd_varlen.restype = _I
         lib.attn_decode_workspace_size.argtypes = [_I, _I, _I, _I, _I, _I]
         lib.attn_decode_workspace_size.restype = ctypes.c_size_t
         lib.attn_decode.argtypes = [_P, _P, _P, _P, _P, _P, ctypes.c_size_t, _I, _I, _I, _I, _I, _I,
@@ -164,6 +173,22 @@ def attn_bwd_dq_cross(q, k, v, dout, dq, workspace, workspace_bytes, B, H, Hkv, 
                       stream) -> int:
     return load().attn_bwd_dq_cross(q, k, v, dout, dq, workspace, workspace_bytes, B, H, Hkv, Nq, Nk, d,
                                     scale, causal, stream)
+
+
+def attn_fwd_varlen(q, k, v, o, lse, cu_q, cu_k, B, H, Hkv, total_q, total_k, max_q, max_k, d, scale, causal,
+                    stream) -> int:
+    return load().attn_fwd_varlen(q, k, v, o, lse, cu_q, cu_k, B, H, Hkv, total_q, total_k, max_q, max_k, d,
+                                  scale, causal, stream)
+
+
+def attn_bwd_varlen_workspace_size(B, H, Hkv, total_q, d) -> int:
+    return load().attn_bwd_varlen_workspace_size(B, H, Hkv, total_q, d)
+
+
+def attn_bwd_varlen(q, k, v, o, lse, dout, dq, dk, dv, cu_q, cu_k, workspace, workspace_bytes, B, H, Hkv,
+                    total_q, total_k, max_q, max_k, d, scale, causal, stream) -> int:
+    return load().attn_bwd_varlen(q, k, v, o, lse, dout, dq, dk, dv, cu_q, cu_k, workspace, workspace_bytes,
+                                  B, H, Hkv, total_q, total_k, max_q, max_k, d, scale, causal, stream)
 
 
 def attn_decode_workspace_size(B, H, Hkv, Nq, Nk, d) -> int:
@@ -334,4 +359,66 @@ def backward_cross(q, k, v, o, lse, dout, scale: float | None = None, causal: bo
                           dout.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
                           workspace.data_ptr(), workspace.numel() * workspace.element_size(),
                           B, H, Hkv, Nq, Nk, d, scale, causal, _stream_ptr(q)), "attn_bwd_cross")
+    return dq, dk, dv
+
+
+def _varlen_args(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k):
+    import torch
+    if q.dim() != 3 or k.dim() != 3 or v.dim() != 3:
+        raise ValueError("packed q, k, v must be (total, heads, d)")
+    total_q, H, d = q.shape
+    total_k, Hkv = k.shape[0], k.shape[1]
+    if tuple(v.shape) != tuple(k.shape) or k.shape[2] != d:
+        raise ValueError("k and v must be (total_k, Hkv, d) with q's d")
+    for t in (q, k, v):
+        if not t.is_contiguous() or t.dtype != torch.bfloat16:
+            raise ValueError("inputs must be contiguous bf16")
+    for c in (cu_seqlens_q, cu_seqlens_k):
+        if c.dtype != torch.int32 or c.dim() != 1 or not c.is_cuda or not c.is_contiguous():
+            raise ValueError("cu_seqlens must be contiguous int32 CUDA vectors")
+    if cu_seqlens_q.numel() != cu_seqlens_k.numel() or cu_seqlens_q.numel() < 2:
+        raise ValueError("cu_seqlens_q and cu_seqlens_k must both hold B + 1 offsets")
+    B = cu_seqlens_q.numel() - 1
+    return B, H, Hkv, total_q, total_k, d, int(max_seqlen_q), int(max_seqlen_k)
+
+
+def forward_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k, scale: float | None = None,
+                   causal: bool = False):
+    """O, lse of a packed variable-length batch.
+
+    q: bf16 (total_q, H, d); k, v: bf16 (total_k, Hkv, d); cu_seqlens_*:
+    int32 CUDA vectors of B + 1 offsets.  Returns O (total_q, H, d) and lse
+    float32 (H, total_q)."""
+    import torch
+    B, H, Hkv, total_q, total_k, d, mq, mk = _varlen_args(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q,
+                                                           max_seqlen_k)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    o = torch.empty_like(q)
+    lse = torch.empty((H, total_q), dtype=torch.float32, device=q.device)
+    _check(attn_fwd_varlen(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                           cu_seqlens_q.data_ptr(), cu_seqlens_k.data_ptr(), B, H, Hkv, total_q, total_k, mq, mk, d,
+                           scale, causal, _stream_ptr(q)), "attn_fwd_varlen")
+    return o, lse
+
+
+def backward_varlen(q, k, v, o, lse, dout, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k,
+                    scale: float | None = None, causal: bool = False, workspace=None):
+    """dQ, dK, dV of forward_varlen (packed layouts as its inputs)."""
+    import torch
+    B, H, Hkv, total_q, total_k, d, mq, mk = _varlen_args(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q,
+                                                           max_seqlen_k)
+    if tuple(o.shape) != tuple(q.shape) or tuple(dout.shape) != tuple(q.shape):
+        raise ValueError("o and dout must have q's shape")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ws_bytes = attn_bwd_varlen_workspace_size(B, H, Hkv, total_q, d)
+    if workspace is None:
+        workspace = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=q.device)
+    _check(attn_bwd_varlen(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), dout.data_ptr(),
+                           dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), cu_seqlens_q.data_ptr(),
+                           cu_seqlens_k.data_ptr(), workspace.data_ptr(),
+                           workspace.numel() * workspace.element_size(), B, H, Hkv, total_q, total_k, mq, mk, d,
+                           scale, causal, _stream_ptr(q)), "attn_bwd_varlen")
     return dq, dk, dv

@@ -17,6 +17,12 @@
 #include "kernels.h"
 #include "ptx.cuh"
 
+#define ATTN_TRY_INNER(x)               \
+  do {                                  \
+    attn_status_t _s = (x);             \
+    if (_s != ATTN_OK) return _s;       \
+  } while (0)
+
 namespace {
 
 constexpr int kMaxDevices = 64;
@@ -111,6 +117,22 @@ bool make_map_bf16(CUtensorMap* m, const void* ptr, int d, int N, long long head
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 3-D map over a packed (total, heads, d) bf16 tensor (sequences one after
+// another, token-major): dims (d, total, heads), so a box of 128 rows x 1
+// head is 128 consecutive tokens of one head, and the kernels address it
+// exactly like the dense map (row, plane = head).
+bool make_map_bf16_packed(CUtensorMap* m, const void* ptr, int d, long long total, int heads) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)total, (cuuint64_t)heads};
+  cuuint64_t strides[2] = {(cuuint64_t)heads * d * 2, (cuuint64_t)d * 2};
+  cuuint32_t box[3] = {64, 128, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 // Shape checks shared by forward and backward.
@@ -147,6 +169,37 @@ attn_status_t check_ptrs(std::initializer_list<const void*> ps) {
     }
     if (a.type != cudaMemoryTypeDevice && a.type != cudaMemoryTypeManaged) return ATTN_ERR_INVALID_ARG;
   }
+  return ATTN_OK;
+}
+
+// cu_seqlens arrays: non-null, int32-aligned device memory.
+attn_status_t check_offsets_ptrs(const int* a, const int* b) {
+  for (const int* p : {a, b}) {
+    if (p == nullptr) return ATTN_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(p) & 3u) return ATTN_ERR_MISALIGNED;
+  }
+  for (const int* p : {a, b}) {
+    cudaPointerAttributes at;
+    if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+      cudaGetLastError();
+      return ATTN_ERR_INVALID_ARG;
+    }
+    if (at.type != cudaMemoryTypeDevice && at.type != cudaMemoryTypeManaged) return ATTN_ERR_INVALID_ARG;
+  }
+  return ATTN_OK;
+}
+
+// Shape checks of a packed batch: B sequences of at most max_q query and
+// max_k key rows, total_q / total_k rows in all.
+attn_status_t check_varlen_shape(int B, int H, int Hkv, int total_q, int total_k, int max_q, int max_k, int d) {
+  ATTN_TRY_INNER(check_shape(B, H, Hkv, max_q, d));
+  ATTN_TRY_INNER(check_shape(B, H, Hkv, max_k, d));
+  if (total_q < 1 || total_k < 1) return ATTN_ERR_UNSUPPORTED_SHAPE;
+  if ((long long)total_q > (long long)B * max_q || (long long)total_k > (long long)B * max_k)
+    return ATTN_ERR_UNSUPPORTED_SHAPE;  // some sequence would be longer than its maximum
+  if ((long long)total_q * H > (1ll << 31) || (long long)total_k * Hkv > (1ll << 31)) return ATTN_ERR_UNSUPPORTED_SHAPE;
+  if ((long long)H * d * 128 >= (1ll << 32)) return ATTN_ERR_UNSUPPORTED_SHAPE;  // 32-bit tile row offsets
+  if (sdpa::varlen_vec_stride(total_q, B) >= (1ll << 31)) return ATTN_ERR_UNSUPPORTED_SHAPE;
   return ATTN_OK;
 }
 
@@ -210,6 +263,7 @@ static attn_status_t fwd_common(const void* q, const void* k, const void* v, voi
     return ATTN_ERR_CUDA;
 
   sdpa::FwdParams p;
+  memset(&p, 0, sizeof(p));
   p.lse = lse;
   p.B = B;
   p.H = H;
@@ -237,6 +291,46 @@ attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, flo
 attn_status_t attn_fwd_cross(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
                              int Hkv, int Nq, int Nk, int d, float scale, int causal, void* stream) {
   return fwd_common(q, k, v, o, lse, B, H, Hkv, Nq, Nk, d, scale, causal, stream);
+}
+
+attn_status_t attn_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse,
+                              const int* cu_seqlens_q, const int* cu_seqlens_k, int B, int H, int Hkv, int total_q,
+                              int total_k, int max_seqlen_q, int max_seqlen_k, int d, float scale, int causal,
+                              void* stream) {
+  ATTN_TRY(check_varlen_shape(B, H, Hkv, total_q, total_k, max_seqlen_q, max_seqlen_k, d));
+  ATTN_TRY(check_scale_flag(scale, causal));
+  ATTN_TRY(check_ptrs({q, k, v, o, lse}));
+  ATTN_TRY(check_offsets_ptrs(cu_seqlens_q, cu_seqlens_k));
+  DeviceInfo* di = nullptr;
+  ATTN_TRY(current_device(&di));
+
+  CUtensorMap tq, tk, tv, to;
+  if (!make_map_bf16_packed(&tq, q, d, total_q, H) || !make_map_bf16_packed(&tk, k, d, total_k, Hkv) ||
+      !make_map_bf16_packed(&tv, v, d, total_k, Hkv) || !make_map_bf16_packed(&to, o, d, total_q, H))
+    return ATTN_ERR_CUDA;
+
+  sdpa::FwdParams p;
+  memset(&p, 0, sizeof(p));
+  p.lse = lse;
+  p.B = B;
+  p.H = H;
+  p.Hkv = Hkv;
+  p.G = H / Hkv;
+  p.Nq = max_seqlen_q;
+  p.Nk = max_seqlen_k;
+  p.n_mtiles = (max_seqlen_q + 255) / 256;
+  p.nkv = (max_seqlen_k + 127) / 128;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.status = di->status;
+  p.limit_ns = wait_limit_ns();
+  p.info = di->info;
+  p.vl.cu_q = cu_seqlens_q;
+  p.vl.cu_k = cu_seqlens_k;
+  p.vl.total_q = total_q;
+  p.vl.total_k = total_k;
+  p.o = static_cast<uint16_t*>(o);
+  cudaError_t e = sdpa::launch_fwd(d, causal != 0, tq, tk, tv, to, p, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;
 }
 
 size_t attn_bwd_workspace_size(int B, int H, int Hkv, int N, int d) {
@@ -398,6 +492,66 @@ attn_status_t attn_bwd_cross(const void* q, const void* k, const void* v, const 
                  stream);
 }
 
+size_t attn_bwd_varlen_workspace_size(int B, int H, int Hkv, int total_q, int d) {
+  if (check_shape(B, H, Hkv, 1, d) != ATTN_OK || total_q < 1) return 0;
+  return (size_t)H * (size_t)sdpa::varlen_vec_stride(total_q, B) * 4 * 2;  // -D and -lse2 per head, float32
+}
+
+attn_status_t attn_bwd_varlen(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                              const void* dout, void* dq, void* dk, void* dv, const int* cu_seqlens_q,
+                              const int* cu_seqlens_k, void* workspace, size_t workspace_bytes, int B, int H,
+                              int Hkv, int total_q, int total_k, int max_seqlen_q, int max_seqlen_k, int d,
+                              float scale, int causal, void* stream) {
+  ATTN_TRY(check_varlen_shape(B, H, Hkv, total_q, total_k, max_seqlen_q, max_seqlen_k, d));
+  ATTN_TRY(check_scale_flag(scale, causal));
+  if (workspace == nullptr || workspace_bytes < attn_bwd_varlen_workspace_size(B, H, Hkv, total_q, d))
+    return ATTN_ERR_WORKSPACE;
+  ATTN_TRY(check_ptrs({q, k, v, o, lse, dout, dq, dk, dv, workspace}));
+  ATTN_TRY(check_offsets_ptrs(cu_seqlens_q, cu_seqlens_k));
+  DeviceInfo* di = nullptr;
+  ATTN_TRY(current_device(&di));
+  CUtensorMap tq, tk, tv, tdo, tdq, tdk, tdv;
+  if (!make_map_bf16_packed(&tq, q, d, total_q, H) || !make_map_bf16_packed(&tk, k, d, total_k, Hkv) ||
+      !make_map_bf16_packed(&tv, v, d, total_k, Hkv) || !make_map_bf16_packed(&tdo, dout, d, total_q, H) ||
+      !make_map_bf16_packed(&tdq, dq, d, total_q, H) || !make_map_bf16_packed(&tdk, dk, d, total_k, Hkv) ||
+      !make_map_bf16_packed(&tdv, dv, d, total_k, Hkv))
+    return ATTN_ERR_CUDA;
+  sdpa::BwdParams p;
+  memset(&p, 0, sizeof(p));
+  p.o = static_cast<const uint16_t*>(o);
+  p.dout = static_cast<const uint16_t*>(dout);
+  p.lse = lse;
+  p.vec_stride = (int)sdpa::varlen_vec_stride(total_q, B);
+  p.dvec = static_cast<float*>(workspace);
+  p.lse2 = p.dvec + (size_t)H * p.vec_stride;
+  p.B = B;
+  p.H = H;
+  p.Hkv = Hkv;
+  p.N = max_seqlen_q;
+  p.G = H / Hkv;
+  p.d = d;
+  p.nq = (max_seqlen_q + 127) / 128;
+  p.Nk = max_seqlen_k;
+  p.nkv = (max_seqlen_k + 127) / 128;
+  p.scale = scale;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.status = di->status;
+  p.limit_ns = wait_limit_ns();
+  p.info = di->info;
+  p.vl.cu_q = cu_seqlens_q;
+  p.vl.cu_k = cu_seqlens_k;
+  p.vl.total_q = total_q;
+  p.vl.total_k = total_k;
+  p.dq = static_cast<uint16_t*>(dq);
+  p.dk = static_cast<uint16_t*>(dk);
+  p.dv = static_cast<uint16_t*>(dv);
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (sdpa::launch_bwd_prep(p, st) != cudaSuccess) return ATTN_ERR_LAUNCH;
+  if (sdpa::launch_bwd_grad(d, causal != 0, tq, tk, tv, tdo, tdk, tdv, p, st) != cudaSuccess) return ATTN_ERR_LAUNCH;
+  if (sdpa::launch_bwd_dq(d, causal != 0, tq, tk, tv, tdo, tdq, p, st) != cudaSuccess) return ATTN_ERR_LAUNCH;
+  return ATTN_OK;
+}
+
 // Key chunks of the decode kernel, a pure function of the shape (so the
 // workspace size needs no device query): chunks of whole 128-key tiles,
 // about 1216 CTAs in all (four waves of two CTAs on each of 152 SMs) when
@@ -475,7 +629,10 @@ attn_status_t attn_get_device_status(void* stream) {
     const int zero = 0;
     if (cudaMemcpyToSymbol(g_status_word, &zero, sizeof(int)) != cudaSuccess) return ATTN_ERR_CUDA;
   }
-  return host == 0 ? ATTN_OK : (host == sdpa::kDevTimeout ? ATTN_ERR_TIMEOUT : ATTN_ERR_CUDA);
+  if (host == 0) return ATTN_OK;
+  if (host == sdpa::kDevTimeout) return ATTN_ERR_TIMEOUT;
+  if (host == sdpa::kDevBadSeqlens) return ATTN_ERR_INVALID_ARG;
+  return ATTN_ERR_CUDA;
 }
 
 attn_status_t attn_get_timeout_info(int info[4], void* stream) {

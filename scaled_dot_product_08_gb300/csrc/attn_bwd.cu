@@ -30,7 +30,7 @@
 //   warp  9     MMA issuer (one elected lane issues)
 //   warp  10    TMA producer: dO_i (its own loop, so a busy dO stage never
 //               delays the next Q_i)
-//   warp  11    idle
+//   warp  11    stores the last, partial dK / dV tile of a packed sequence
 // setmaxnreg: compute 200, the other warpgroup 104 registers per thread
 // (128 * (200 + 200 + 104) = 384 * 168, the launch allocation).
 // Tensor memory: [0,128) S^T / P^T, [128,256) dP^T / dS^T, [256,256+d) dK,
@@ -78,6 +78,51 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const BwdParams p) {
   }
 }
 
+// Packed batch: one CTA of 8 warps per (128-row tile of a sequence, head);
+// warp w takes rows w, w + 8, ... of the tile and writes them into the
+// sequence's aligned region of the workspace (rows past Nq: -D = 0 and
+// -lse2 = -inf).  A row that saw no key (lse = -inf) also gets -lse2 = -inf,
+// so P = 0 on it.
+__global__ void __launch_bounds__(256) bwd_pre_varlen_kernel(const BwdParams p) {
+  const int t = (int)(blockIdx.x % p.nq);
+  const int bh = (int)(blockIdx.x / p.nq);
+  const int b = bh / p.H, h = bh % p.H;
+  const SeqView sq = seq_view(p.vl, b, p.N, p.Nk);
+  if (!sq.ok) {
+    if (threadIdx.x == 0) atomicCAS(p.status, 0, kDevBadSeqlens);
+    return;
+  }
+  if (128 * t >= sq.nq) return;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const size_t vbase = (size_t)h * p.vec_stride + (size_t)varlen_vec_offset(sq.q0, b) + 128 * (size_t)t;
+  for (int k = warp; k < 128; k += 8) {
+    const int i = 128 * t + k;
+    float dot = 0.f, l = -INFINITY;
+    if (i < sq.nq) {
+      const size_t off = ((size_t)(sq.q0 + i) * p.H + h) * p.d;
+      if (lane * 8 < p.d) {
+        const uint4 o = *reinterpret_cast<const uint4*>(p.o + off + lane * 8);
+        const uint4 g = *reinterpret_cast<const uint4*>(p.dout + off + lane * 8);
+        const uint32_t ow[4] = {o.x, o.y, o.z, o.w}, gw[4] = {g.x, g.y, g.z, g.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float2 of = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&ow[e]));
+          const float2 gf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&gw[e]));
+          dot = fmaf(of.x, gf.x, dot);
+          dot = fmaf(of.y, gf.y, dot);
+        }
+      }
+#pragma unroll
+      for (int s = 16; s > 0; s >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, s);
+      l = p.lse[(size_t)h * p.vl.total_q + sq.q0 + i];
+    }
+    if (lane == 0) {
+      p.dvec[vbase + k] = -dot;
+      p.lse2[vbase + k] = (l == -INFINITY) ? -INFINITY : -l * 1.4426950408889634f;
+    }
+  }
+}
+
 // ------------------------------------------------------------------ main
 template <int D>
 struct BwdTraits {
@@ -89,7 +134,7 @@ struct BwdTraits {
   static constexpr int NBAR = 16;
   // K, V, Q[2], dO[2], then vectors, barriers, misc
   static constexpr int TILES_BYTES = 6 * TILE_BYTES;
-  static constexpr int SMEM = TILES_BYTES + 2 * VEC_BYTES + NBAR * 8 + 16;
+  static constexpr int SMEM = TILES_BYTES + 2 * VEC_BYTES + NBAR * 8 + 32;
   static constexpr int THREADS = 384;
 };
 
@@ -129,6 +174,9 @@ __global__ void __launch_bounds__(384, 1)
   uint8_t* const misc = smem_raw + (sBar - base) + 8 * T::NBAR;
   uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(misc);
   volatile int* const abort_flag = reinterpret_cast<volatile int*>(misc + 4);
+  // This CTA's sequence {q0, nq, k0, nk}, read back where needed rather than
+  // held in registers across the main loops.
+  volatile int* const seq_s = reinterpret_cast<volatile int*>(misc + 8);
   const float* const vec_g = reinterpret_cast<const float*>(smem_raw + (sVec - base));
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -136,9 +184,39 @@ __global__ void __launch_bounds__(384, 1)
   const int bhk = blockIdx.x / nkv;           // b * Hkv + hk
   const int j = blockIdx.x % nkv;             // key tile (0 = most causal work)
   const int b = bhk / p.Hkv, hk = bhk % p.Hkv;
-  // Causal: the first query tile with a row at position >= 128 j.
-  const int i0 = CAUSAL ? max(0, (j * 128 - p.koff) / 128) : 0;
-  const int ni = p.nq - i0;                   // query tiles per head
+  const bool varlen = p.vl.cu_q != nullptr;
+  // Tensor-map plane of K/V: b * Hkv + hk for the dense batch, the head for a
+  // packed one (maps over (total, heads)); Q/dO planes likewise per head.
+  const int kplane = varlen ? hk : bhk;
+  int i0, ni;  // first query tile, query tiles per head
+  {
+    const SeqView sq = seq_view(p.vl, b, p.N, p.Nk);
+    if (!sq.ok) {
+      if (threadIdx.x == 0) atomicCAS(p.status, 0, kDevBadSeqlens);
+      return;
+    }
+    if (128 * j >= sq.nk) return;  // past the end of a shorter packed sequence
+    // Causal: the first query tile with a row at position >= 128 j, query
+    // row i at position koff + i, koff = Nk - Nq.
+    i0 = CAUSAL ? max(0, (j * 128 - (sq.nk - sq.nq)) / 128) : 0;
+    ni = (sq.nq + 127) / 128 - i0;
+    if (ni <= 0) {
+      // No query attends to these keys (a packed sequence without queries):
+      // dK = dV = 0.
+      const uint32_t rs = (uint32_t)(p.Hkv * D);
+      const long long off = ((long long)sq.k0 + 128 * j) * rs + (long long)hk * D;
+      zero_rows2_bf16<D>(p.dk + off, p.dv + off, rs, min(128, sq.nk - 128 * j));
+      return;
+    }
+    if (threadIdx.x == 0) {
+      seq_s[0] = sq.q0;
+      seq_s[1] = sq.nq;
+      seq_s[2] = sq.k0;
+      seq_s[3] = sq.nk;
+      seq_s[4] = kplane;
+      seq_s[5] = hk;
+    }
+  }
   const int total = p.G * ni;                 // steps: (head in group) x (query tile)
 
   if (threadIdx.x == 0) {
@@ -181,8 +259,13 @@ __global__ void __launch_bounds__(384, 1)
     const uint32_t tS = tmem + 64 * X + lane_off;           // S^T columns of this half
     const uint32_t tP = tmem + 64 * X + lane_off;           // P^T (bf16 pairs), first 32 of them
     const uint32_t tdP = tmem + 128 + 64 * X + lane_off;    // dP^T columns of this half; dS^T pairs after
-    // Key rows past N (the last tile's padding) get P^T = 0.
-    const bool key_pad = j * 128 + r >= p.Nk;
+    // Query column q of tile i cannot see key row 128 j + r when
+    // q < qmin0 - 128 i: every column for key rows past Nk (the last tile's
+    // padding), and for causal rows the queries at positions koff + 128 i +
+    // 64 X + q below the key.
+    const int qmin0 = (j * 128 + r >= seq_s[3]) ? (1 << 30)
+                      : CAUSAL                  ? 128 * j + r - (seq_s[3] - seq_s[1]) - 64 * X
+                                                : -(1 << 30);
     const float c = p.scale_log2;
     const float2 c2 = make_float2(c, c);
     bool ok = true;
@@ -221,19 +304,13 @@ __global__ void __launch_bounds__(384, 1)
         x[4 * q4 + 2] = ex2(t1.x);
         x[4 * q4 + 3] = ex2(t1.y);
       }
-      if (CAUSAL) {
-        // Key 128 j + r is invisible to query columns below qmin (query
-        // position koff + 128 i + 64 X + q < key).
-        const int qmin = 128 * (j - i) + r - p.koff - 64 * X;
+      {
+        const int qmin = qmin0 - 128 * i;
         if (__any_sync(0xffffffffu, qmin > 0)) {
 #pragma unroll
           for (int q = 0; q < 64; ++q)
             if (q < qmin) x[q] = 0.f;
         }
-      }
-      if (key_pad) {
-#pragma unroll
-        for (int q = 0; q < 64; ++q) x[q] = 0.f;
       }
       uint32_t pk[32];  // P^T as bf16 pairs: to TMEM for the dV MMA, kept for dS
 #pragma unroll
@@ -309,11 +386,20 @@ __global__ void __launch_bounds__(384, 1)
       fence_proxy_async_smem();
     }
     named_bar_sync(1 + X, 128);
-    if (ok && r == 0) {
-      for (int cb = 0; cb < T::NB; ++cb)
-        tma_store_3d(X ? &tmdK : &tmdV, stage + cb * T::BLOCK_BYTES, cb * 64, j * 128, bhk);
-      bulk_commit();
-      bulk_wait_read_all();
+    // The dense batch clips the box at Nk.  In a packed batch the rows past
+    // the sequence belong to the next one, so warp 11 stores a partial tile
+    // row by row (barrier 3: both warpgroups' staging is complete).
+    const int valid = seq_s[3] - 128 * (int)(blockIdx.x % p.nkv);
+    if (valid >= 128 || p.vl.cu_q == nullptr) {
+      if (ok && r == 0) {
+        for (int cb = 0; cb < T::NB; ++cb)
+          tma_store_3d(X ? &tmdK : &tmdV, stage + cb * T::BLOCK_BYTES, cb * 64,
+                       seq_s[2] + 128 * (int)(blockIdx.x % p.nkv), seq_s[4]);
+        bulk_commit();
+        bulk_wait_read_all();
+      }
+    } else {
+      named_bar_arrive(3, 256 + 32);
     }
     setmaxnreg_dec<168>();
   } else {
@@ -322,23 +408,28 @@ __global__ void __launch_bounds__(384, 1)
     if (warp == 8) {
       // ------------------------------------------------------------ producer: K, V, Q
       if (lane == 0) {
+        const int q0 = seq_s[0], k0 = seq_s[2];
+        // Row vectors: (b * H + h) * Npad for the dense batch; the sequence's
+        // aligned region of head h for a packed one.
+        const size_t vseq = varlen ? (size_t)varlen_vec_offset(q0, b) : 0;
         tma_prefetch_desc(&tmQ);
         mbar_expect_tx(bKV, 2 * T::TILE_BYTES);
         for (int cb = 0; cb < T::NB; ++cb) {
-          tma_load_3d(sK + cb * T::BLOCK_BYTES, &tmK, bKV, cb * 64, j * 128, bhk);
-          tma_load_3d(sV + cb * T::BLOCK_BYTES, &tmV, bKV, cb * 64, j * 128, bhk);
+          tma_load_3d(sK + cb * T::BLOCK_BYTES, &tmK, bKV, cb * 64, k0 + j * 128, kplane);
+          tma_load_3d(sV + cb * T::BLOCK_BYTES, &tmV, bKV, cb * 64, k0 + j * 128, kplane);
         }
         int issued = 0;
         for (int it = 0; it < total; ++it) {
           const int st = it & 1, rd = it >> 1;
           const int h = hk * p.G + it / ni, i = i0 + it % ni;
           const int bh = b * p.H + h;
+          const int qplane = varlen ? h : bh;
           if (rd > 0 && !wait_bounded(wc, bQe + 8u * st, (rd - 1) & 1, wait_site(0x31, it))) break;
           const uint32_t barq = bQf + 8u * st;
           mbar_expect_tx(barq, T::TILE_BYTES + T::VEC_BYTES);
           for (int cb = 0; cb < T::NB; ++cb)
-            tma_load_3d(sQ + st * T::TILE_BYTES + cb * T::BLOCK_BYTES, &tmQ, barq, cb * 64, i * 128, bh);
-          const size_t voff = (size_t)bh * p.Npad + (size_t)i * 128;
+            tma_load_3d(sQ + st * T::TILE_BYTES + cb * T::BLOCK_BYTES, &tmQ, barq, cb * 64, q0 + i * 128, qplane);
+          const size_t voff = (varlen ? (size_t)h * p.vec_stride + vseq : (size_t)bh * p.Npad) + (size_t)i * 128;
           bulk_load(sVec + st * T::VEC_BYTES, p.lse2 + voff, 512, barq);
           bulk_load(sVec + st * T::VEC_BYTES + 512, p.dvec + voff, 512, barq);
           issued = it + 1;
@@ -349,20 +440,33 @@ __global__ void __launch_bounds__(384, 1)
           wait_drain(bQf + 8u * st, ((((issued - 1 - st) / 2) * 2 + st) >> 1) & 1, p.limit_ns);
       }
       __syncwarp();
+    } else if (warp == 11) {
+      // ------------------------------------------------------------ partial dK / dV tile (packed batch)
+      const int valid = seq_s[3] - 128 * j;
+      if (p.vl.cu_q != nullptr && valid < 128) {
+        named_bar_sync(3, 256 + 32);
+        if (*abort_flag == 0) {  // staging is complete unless a wait gave up
+          const uint32_t rs = (uint32_t)(p.Hkv * D);
+          const long long off = ((long long)seq_s[2] + 128 * j) * rs + (long long)hk * D;
+          store_rows_sw128<D>(sV, p.dv + off, rs, valid, lane, 32);
+          store_rows_sw128<D>(sK, p.dk + off, rs, valid, lane, 32);
+        }
+      }
     } else if (warp == 10) {
       // ------------------------------------------------------------ producer: dO
       if (lane == 0) {
+        const int q0 = seq_s[0];
         tma_prefetch_desc(&tmdO);
         int issued = 0;
         for (int it = 0; it < total; ++it) {
           const int st = it & 1, rd = it >> 1;
           const int h = hk * p.G + it / ni, i = i0 + it % ni;
-          const int bh = b * p.H + h;
+          const int qplane = varlen ? h : b * p.H + h;
           if (rd > 0 && !wait_bounded(wc, bDe + 8u * st, (rd - 1) & 1, wait_site(0x32, it))) break;
           const uint32_t bard = bDf + 8u * st;
           mbar_expect_tx(bard, T::TILE_BYTES);
           for (int cb = 0; cb < T::NB; ++cb)
-            tma_load_3d(sdO + st * T::TILE_BYTES + cb * T::BLOCK_BYTES, &tmdO, bard, cb * 64, i * 128, bh);
+            tma_load_3d(sdO + st * T::TILE_BYTES + cb * T::BLOCK_BYTES, &tmdO, bard, cb * 64, q0 + i * 128, qplane);
           issued = it + 1;
         }
         for (int st = 0; st < 2 && st < issued; ++st)
@@ -482,8 +586,12 @@ static cudaError_t launch_main_t(const CUtensorMap& tq, const CUtensorMap& tk, c
 }
 
 cudaError_t launch_bwd_prep(const BwdParams& p, cudaStream_t stream) {
-  const long long rows = (long long)p.B * p.H * p.Npad;
-  bwd_pre_kernel<<<(unsigned)((rows + 7) / 8), 256, 0, stream>>>(p);
+  if (p.vl.cu_q != nullptr) {
+    bwd_pre_varlen_kernel<<<(unsigned)p.nq * (unsigned)(p.B * p.H), 256, 0, stream>>>(p);
+  } else {
+    const long long rows = (long long)p.B * p.H * p.Npad;
+    bwd_pre_kernel<<<(unsigned)((rows + 7) / 8), 256, 0, stream>>>(p);
+  }
   return cudaGetLastError();
 }
 

@@ -1,8 +1,8 @@
 // attn_bwd_dq.cu — dQ of exact attention on sm_103a (query-stationary).
 //
 // Method (page "Flash Attention原理：分块计算与重计算，如何降低O(n^2)的显存占用",
-// §五): for one 128-row query tile i of one head, walk the key tiles j (j <= i
-// when causal) and accumulate
+// §五): for one 128-row query tile i of one head, walk the key tiles j (up to
+// the last one a row of the tile sees, when causal) and accumulate
 //     S  = Q_i K_j^T,   P = exp2(S * scale * log2 e - lse_i * log2 e),
 //     dP = dO_i V_j^T,  dS = P * (dP - D_i),   dQ_i += dS K_j,
 // with dQ_i in tensor memory for the whole walk and the softmax scale applied
@@ -35,7 +35,7 @@ struct DqTraits {
   static constexpr int KSTEPS = D / 16;
   static constexpr int KS = 3, VS = 2;                 // K and V ring slots
   static constexpr int NBAR = 18;
-  static constexpr int SMEM = 1024 + (2 + KS + VS) * TILE_BYTES + NBAR * 8 + 16;
+  static constexpr int SMEM = 1024 + (2 + KS + VS) * TILE_BYTES + NBAR * 8 + 32;
   static constexpr int THREADS = 384;
 };
 
@@ -70,16 +70,46 @@ __global__ void __launch_bounds__(384, 1)
   uint8_t* const misc = gbase + (sBar - base) + 8 * T::NBAR;
   uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(misc);
   volatile int* const abort_flag = reinterpret_cast<volatile int*>(misc + 4);
+  // This CTA's sequence {q0, nq, k0, nk}, read back where needed rather than
+  // held in registers across the main loops.
+  volatile int* const seq_s = reinterpret_cast<volatile int*>(misc + 8);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // Work unit: head-major (the CTAs in flight share K/V heads in L2); within
   // a head the longest causal walks go first.
   const int bh = blockIdx.x / p.nq;
   const int i = p.nq - 1 - (int)(blockIdx.x % p.nq);  // query tile
-  const int bhk = (bh / p.H) * p.Hkv + (bh % p.H) / p.G;
-  // Key tiles visited: causal, up to the tile holding the last row's last
-  // visible key koff + 128 i + 127.
-  const int n = CAUSAL ? min(p.nkv, (p.koff + i * 128 + 127) / 128 + 1) : p.nkv;
+  const int b = bh / p.H, h = bh % p.H;
+  const int bhk = b * p.Hkv + h / p.G;
+  const bool varlen = p.vl.cu_q != nullptr;
+  // Tensor-map planes: b * heads + head for the dense batch, the head for a
+  // packed one (maps over (total, heads)).
+  const int qplane = varlen ? h : bh, kplane = varlen ? h / p.G : bhk;
+  int n;  // key tiles visited
+  {
+    const SeqView sq = seq_view(p.vl, b, p.N, p.Nk);
+    if (!sq.ok) {
+      if (threadIdx.x == 0) atomicCAS(p.status, 0, kDevBadSeqlens);
+      return;
+    }
+    if (128 * i >= sq.nq) return;  // past the end of a shorter packed sequence
+    // Causal: up to the tile holding the last row's last visible key,
+    // koff + 128 i + 127 (query row r at position koff + r, koff = Nk - Nq).
+    const int nkv = (sq.nk + 127) / 128;
+    n = CAUSAL ? min(nkv, (sq.nk - sq.nq + i * 128 + 127) / 128 + 1) : nkv;
+    if (n <= 0) {
+      // No row of the tile sees a key (packed batches only): dQ = 0.
+      const uint32_t rs = (uint32_t)(p.H * D);
+      zero_rows_bf16<D>(p.dq + ((long long)sq.q0 + 128 * i) * rs + (long long)h * D, rs, min(128, sq.nq - 128 * i));
+      return;
+    }
+    if (threadIdx.x == 0) {
+      seq_s[0] = sq.q0;
+      seq_s[1] = sq.nq;
+      seq_s[2] = sq.k0;
+      seq_s[3] = sq.nk;
+    }
+  }
 
   if (threadIdx.x == 0) {
     mbar_init(bQ, 1);
@@ -119,11 +149,15 @@ __global__ void __launch_bounds__(384, 1)
     const int r = threadIdx.x & 127;  // query row within the tile == TMEM lane
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
     const uint32_t tdP = tmem + 256 + 64 * X + lane_off;
-    const size_t vrow = (size_t)bh * p.Npad + (size_t)i * 128 + r;
+    const size_t vrow = (varlen ? (size_t)h * p.vec_stride + (size_t)varlen_vec_offset(seq_s[0], b)
+                                : (size_t)bh * p.Npad) + (size_t)i * 128 + r;
     const float l2 = p.lse2[vrow];   // -lse * log2(e); -inf on padding rows (P = 0 there)
     const float nD = p.dvec[vrow];   // -D
     const float2 c2 = make_float2(p.scale_log2, p.scale_log2);
     const float2 l22 = make_float2(l2, l2), nD2 = make_float2(nD, nD);
+    // Key columns at or past lim0 - 128 j of key tile j are invisible to row
+    // r: keys past Nk, and for causal rows keys past position koff + 128 i + r.
+    const int lim0 = (CAUSAL ? min(seq_s[3], seq_s[3] - seq_s[1] + 128 * i + r + 1) : seq_s[3]) - 64 * X;
     bool ok = true;
     for (int j = 0; j < n; ++j) {
       const uint32_t tS = tmem + (j & 1) * 128 + 64 * X + lane_off;
@@ -153,10 +187,7 @@ __global__ void __launch_bounds__(384, 1)
         x[2 * e + 1] = ex2(t.y);
       }
       {
-        // Key columns at or past lim are invisible to row r: keys past Nk,
-        // and for causal rows keys past position koff + 128 i + r.
-        int lim = p.Nk - j * 128 - 64 * X;
-        if (CAUSAL) lim = min(lim, p.koff + 128 * (i - j) + r - 64 * X + 1);
+        const int lim = lim0 - 128 * j;
         if (__any_sync(0xffffffffu, lim < 64)) {
 #pragma unroll
           for (int k = 0; k < 64; ++k)
@@ -219,10 +250,22 @@ __global__ void __launch_bounds__(384, 1)
       fence_proxy_async_smem();
     }
     named_bar_sync(1, 256);
-    if (ok && threadIdx.x == 0 && i * 128 < p.N) {
-      for (int cb = 0; cb < T::NB; ++cb) tma_store_3d(&tmdQ, sQ + cb * T::BLOCK_BYTES, cb * 64, i * 128, bh);
-      bulk_commit();
-      bulk_wait_all();
+    if (ok) {
+      // The dense batch clips the box at Nq; in a packed batch the rows past
+      // the sequence belong to the next one, so a partial tile is stored row
+      // by row instead.
+      const int q0 = seq_s[0], valid = seq_s[1] - 128 * i;
+      if (valid >= 128 || !varlen) {
+        if (threadIdx.x == 0) {
+          for (int cb = 0; cb < T::NB; ++cb)
+            tma_store_3d(&tmdQ, sQ + cb * T::BLOCK_BYTES, cb * 64, q0 + i * 128, qplane);
+          bulk_commit();
+          bulk_wait_all();
+        }
+      } else {
+        const uint32_t rs = (uint32_t)(p.H * D);
+        store_rows_sw128<D>(sQ, p.dq + ((long long)q0 + 128 * i) * rs + (long long)h * D, rs, valid, threadIdx.x, 256);
+      }
     }
     setmaxnreg_dec<168>();
   } else {
@@ -231,12 +274,13 @@ __global__ void __launch_bounds__(384, 1)
     if (warp == 8) {
       // ------------------------------------------------------------ producer
       if (lane == 0) {
+        const int q0 = seq_s[0], k0 = seq_s[2];
         tma_prefetch_desc(&tmK);
         tma_prefetch_desc(&tmV);
         mbar_expect_tx(bQ, 2 * T::TILE_BYTES);
         for (int cb = 0; cb < T::NB; ++cb) {
-          tma_load_3d(sQ + cb * T::BLOCK_BYTES, &tmQ, bQ, cb * 64, i * 128, bh);
-          tma_load_3d(sdO + cb * T::BLOCK_BYTES, &tmdO, bQ, cb * 64, i * 128, bh);
+          tma_load_3d(sQ + cb * T::BLOCK_BYTES, &tmQ, bQ, cb * 64, q0 + i * 128, qplane);
+          tma_load_3d(sdO + cb * T::BLOCK_BYTES, &tmdO, bQ, cb * 64, q0 + i * 128, qplane);
         }
         int issued = 0;
         for (int j = 0; j < n; ++j) {
@@ -244,12 +288,14 @@ __global__ void __launch_bounds__(384, 1)
           if (kr > 0 && !wait_bounded(wc, bKe + 8u * ks, (kr - 1) & 1, wait_site(0x91, j))) break;
           mbar_expect_tx(bKf + 8u * ks, T::TILE_BYTES);
           for (int cb = 0; cb < T::NB; ++cb)
-            tma_load_3d(sK + ks * T::TILE_BYTES + cb * T::BLOCK_BYTES, &tmK, bKf + 8u * ks, cb * 64, j * 128, bhk);
+            tma_load_3d(sK + ks * T::TILE_BYTES + cb * T::BLOCK_BYTES, &tmK, bKf + 8u * ks, cb * 64, k0 + j * 128,
+                        kplane);
           issued = 2 * j + 1;
           if (vr > 0 && !wait_bounded(wc, bVe + 8u * vs, (vr - 1) & 1, wait_site(0x92, j))) break;
           mbar_expect_tx(bVf + 8u * vs, T::TILE_BYTES);
           for (int cb = 0; cb < T::NB; ++cb)
-            tma_load_3d(sV + vs * T::TILE_BYTES + cb * T::BLOCK_BYTES, &tmV, bVf + 8u * vs, cb * 64, j * 128, bhk);
+            tma_load_3d(sV + vs * T::TILE_BYTES + cb * T::BLOCK_BYTES, &tmV, bVf + 8u * vs, cb * 64, k0 + j * 128,
+                        kplane);
           issued = 2 * j + 2;
         }
         // Every copy issued above has landed before the CTA may exit.

@@ -44,7 +44,7 @@ struct FwdTraits {
   static constexpr int NSTAGE = (D == 64) ? 8 : 5;   // K/V ring depth
   static constexpr int KSTEPS = D / 16;              // K=16 steps of Q K^T
   static constexpr int NBAR = 2 + 2 * NSTAGE + 2 + 4 + 2 + 1;
-  static constexpr int SMEM = 1024 + (2 + NSTAGE) * TILE_BYTES + NBAR * 8 + 16;
+  static constexpr int SMEM = 1024 + (2 + NSTAGE) * TILE_BYTES + NBAR * 8 + 32;
   static constexpr int THREADS = 384;
 };
 
@@ -72,6 +72,10 @@ __global__ void __launch_bounds__(384, 1)
   uint8_t* const misc = gbase + (sBar - base) + 8 * T::NBAR;
   uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(misc);
   volatile int* const abort_flag = reinterpret_cast<volatile int*>(misc + 4);
+  // This CTA's sequence {q0, nq, k0, nk} and its query plane and head, read
+  // back by each role where needed rather than held in registers across the
+  // main loops.
+  volatile int* const seq_s = reinterpret_cast<volatile int*>(misc + 8);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -80,12 +84,36 @@ __global__ void __launch_bounds__(384, 1)
   // reuse); within a head the heaviest causal query tiles go first.
   const int bh = blockIdx.x / p.n_mtiles;
   const int mt = p.n_mtiles - 1 - (int)(blockIdx.x % p.n_mtiles);
-  const int bhk = (bh / p.H) * p.Hkv + (bh % p.H) / p.G;
-  int n0 = p.nkv, n1 = p.nkv;  // key tiles visited by query tile 0 / 1
-  if (CAUSAL) {  // up to the tile holding the last row's last visible key, koff + 128 qi + 127
-    n0 = min((p.koff + 256 * mt + 127) / 128 + 1, p.nkv);
-    n1 = min((p.koff + 256 * mt + 255) / 128 + 1, p.nkv);
+  const int b = bh / p.H, h = bh % p.H;
+  const int bhk = b * p.Hkv + h / p.G;
+  // This CTA's sequence: the whole (b, h) plane, or rows of a packed batch
+  // (tensor maps over (total, heads): the plane is the head).
+  const bool varlen = p.vl.cu_q != nullptr;
+  {
+    const SeqView sq = seq_view(p.vl, b, p.Nq, p.Nk);
+    if (!sq.ok) {
+      if (threadIdx.x == 0 && mt == 0) atomicCAS(p.status, 0, kDevBadSeqlens);
+      return;
+    }
+    if (256 * mt >= sq.nq) return;  // past the end of a shorter packed sequence
+    if (threadIdx.x == 0) {
+      seq_s[0] = sq.q0;
+      seq_s[1] = sq.nq;
+      seq_s[2] = sq.k0;
+      seq_s[3] = sq.nk;
+      seq_s[4] = varlen ? h : bh;  // query plane of the tensor maps
+      seq_s[5] = h;
+    }
   }
+  // Key tiles visited by query tile s of this CTA (at least one: a row that
+  // sees no key still runs one fully masked tile).  Causal: up to the tile
+  // holding the last row's last visible key, koff + 128 qi + 127, with query
+  // row i at position koff + i, koff = Nk - Nq.
+  auto key_tiles = [&](int s) {
+    const int nq = seq_s[1], nk = seq_s[3];
+    const int nkv = max(1, (nk + 127) / 128);
+    return CAUSAL ? max(1, min((nk - nq + 256 * mt + 128 * s + 127) / 128 + 1, nkv)) : nkv;
+  };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < 2; ++s) {
@@ -120,7 +148,10 @@ __global__ void __launch_bounds__(384, 1)
     const int s = warp >> 2;            // query tile of this warpgroup
     const int r = threadIdx.x & 127;    // row within the tile == TMEM lane
     const int qi = 2 * mt + s;          // global query tile index
-    const int n = s ? n1 : n0;
+    const int n = key_tiles(s);
+    // Columns at or past lim0 - 128 j of key tile j are invisible to row r:
+    // keys past Nk, and for causal rows keys past position koff + 128 qi + r.
+    const int lim0 = CAUSAL ? min(seq_s[3], seq_s[3] - seq_s[1] + qi * 128 + r + 1) : seq_s[3];
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
     const uint32_t tS = tmem + s * 128 + lane_off;
     const uint32_t tO = tmem + 256 + s * 128 + lane_off;
@@ -154,11 +185,8 @@ __global__ void __launch_bounds__(384, 1)
         }
       }
       {
-        // Columns at or past `lim` are invisible to row r: keys past Nk, and
-        // for causal rows keys past position koff + 128 qi + r.  Only the
-        // diagonal and the ragged last tile have any.
-        int lim = p.Nk - j * 128;
-        if (CAUSAL) lim = min(lim, p.koff + qi * 128 + r + 1 - j * 128);
+        // Only the diagonal and the ragged last tile have masked columns.
+        const int lim = lim0 - j * 128;
         if (__any_sync(0xffffffffu, lim < 128)) {
 #pragma unroll
           for (int i = 0; i < 128; ++i)
@@ -202,7 +230,10 @@ __global__ void __launch_bounds__(384, 1)
       // sum runs in 4 packed partial sums.  P is published in two halves of
       // 64 keys (one barrier per half) so that the P V MMA over the first 64
       // keys runs while the second half is computed.
-      const float2 c2 = make_float2(c, c), nm2 = make_float2(-m, -m);
+      // A row that has seen no key yet (m = -inf: only in packed batches)
+      // takes exponent base 0, so its masked scores give p = 0, not NaN.
+      const float mu = (m == -INFINITY) ? 0.f : m;
+      const float2 c2 = make_float2(c, c), nm2 = make_float2(-mu, -mu);
       float2 sum[4];
 #pragma unroll
       for (int k = 0; k < 4; ++k) sum[k] = make_float2(0.f, 0.f);
@@ -231,7 +262,7 @@ __global__ void __launch_bounds__(384, 1)
     const uint32_t sOut = sQ + s * T::TILE_BYTES;  // Q tile is dead once O is final
     if (ok) {
       tc_fence_after();
-      const float inv = 1.f / l;
+      const float inv = l > 0.f ? 1.f / l : 0.f;  // a row that saw no key: O = 0, lse = -inf
 #pragma unroll
       for (int cc = 0; cc < D / 32; ++cc) {
         uint32_t o[32];
@@ -252,14 +283,28 @@ __global__ void __launch_bounds__(384, 1)
     }
     named_bar_sync(1 + s, 128);
     if (ok) {
-      if (r == 0 && qi * 128 < p.Nq) {
-        for (int cb = 0; cb < T::NB; ++cb)
-          tma_store_3d(&tmO, sOut + cb * T::BLOCK_BYTES, cb * 64, qi * 128, bh);
-        bulk_commit();
-        bulk_wait_read_all();
+      // The dense batch clips the box at Nq; in a packed batch the rows past
+      // the sequence belong to the next one, so a partial tile is stored row
+      // by row instead.
+      const int q0 = seq_s[0], nq = seq_s[1], qplane = seq_s[4], hh = seq_s[5];
+      const bool packed = p.vl.cu_q != nullptr;
+      const int valid = nq - qi * 128;
+      if (valid >= 128 || (!packed && valid > 0)) {
+        if (r == 0) {
+          for (int cb = 0; cb < T::NB; ++cb)
+            tma_store_3d(&tmO, sOut + cb * T::BLOCK_BYTES, cb * 64, q0 + qi * 128, qplane);
+          bulk_commit();
+          bulk_wait_read_all();
+        }
+      } else if (valid > 0) {
+        const uint32_t rs = (uint32_t)(p.H * D);
+        store_rows_sw128<D>(sOut, p.o + ((long long)q0 + qi * 128) * rs + (long long)hh * D, rs, valid, r, 128);
       }
       const int row = qi * 128 + r;
-      if (row < p.Nq) p.lse[(size_t)bh * p.Nq + row] = (m + log2f(l)) * 0.69314718055994531f;
+      // lse: (H, total_q) for a packed batch, (B, H, Nq) otherwise; the
+      // query plane is the head there and b * H + h here.
+      const size_t lbase = packed ? (size_t)qplane * p.vl.total_q + q0 : (size_t)qplane * p.Nq;
+      if (row < nq) p.lse[lbase + row] = (m + log2f(l)) * 0.69314718055994531f;
     }
     setmaxnreg_dec<168>();  // one register budget again for the common teardown
   } else {
@@ -268,6 +313,8 @@ __global__ void __launch_bounds__(384, 1)
     if (warp == 8) {
       // ------------------------------------------------------------ producer
       if (lane == 0) {
+        const int q0 = seq_s[0], k0 = seq_s[2], n1 = key_tiles(1);
+        const int qplane = seq_s[4], kplane = varlen ? seq_s[5] / p.G : bhk;
         tma_prefetch_desc(&tmQ);
         tma_prefetch_desc(&tmK);
         tma_prefetch_desc(&tmV);
@@ -275,7 +322,7 @@ __global__ void __launch_bounds__(384, 1)
           mbar_expect_tx(bQ + 8u * s, T::TILE_BYTES);
           for (int c = 0; c < T::NB; ++c)
             tma_load_3d(sQ + s * T::TILE_BYTES + c * T::BLOCK_BYTES, &tmQ, bQ + 8u * s, c * 64,
-                        (2 * mt + s) * 128, bh);
+                        q0 + (2 * mt + s) * 128, qplane);
         }
         bool ok = true;
         int t = 0;  // ring slot counter: K_j is slot 2j, V_j is slot 2j+1
@@ -286,7 +333,8 @@ __global__ void __launch_bounds__(384, 1)
             mbar_expect_tx(bKVf + 8u * st, T::TILE_BYTES);
             const CUtensorMap* m = (w == 0) ? &tmK : &tmV;
             for (int c = 0; c < T::NB; ++c)
-              tma_load_3d(sKV + st * T::TILE_BYTES + c * T::BLOCK_BYTES, m, bKVf + 8u * st, c * 64, j * 128, bhk);
+              tma_load_3d(sKV + st * T::TILE_BYTES + c * T::BLOCK_BYTES, m, bKVf + 8u * st, c * 64,
+                          k0 + j * 128, kplane);
             ++t;
           }
         }
@@ -305,6 +353,7 @@ __global__ void __launch_bounds__(384, 1)
       // warp-uniform; one elected lane issues each tcgen05 instruction.
       // Descriptors are built once per tile and moved by constant offsets.
       {
+        const int n0 = key_tiles(0), n1 = key_tiles(1);
         const uint32_t leader = elect_one();
         constexpr uint32_t IQK = idesc_bf16_f32(128, 128, false, false);
         constexpr uint32_t IPV = idesc_bf16_f32(128, D, false, true);

@@ -9,6 +9,15 @@
 
 namespace sdpa {
 
+// Packed variable-length batch (cu_seqlens): sequence b owns query rows
+// cu_q[b] .. cu_q[b+1]-1 and key rows cu_k[b] .. cu_k[b+1]-1 of a
+// (total, heads, d) tensor.  cu_q == nullptr: the dense (B, heads, N, d) batch.
+struct VarlenArgs {
+  const int* cu_q;
+  const int* cu_k;
+  int total_q, total_k;  // packed rows (the bound every offset is checked against)
+};
+
 // Forward kernel arguments (tensor maps are passed separately).
 struct FwdParams {
   float* lse;            // (B, H, Nq) float32
@@ -21,6 +30,8 @@ struct FwdParams {
   int* status;           // device status word
   unsigned long long limit_ns;  // bounded-wait limit
   int* info;             // first-timeout record (4 ints)
+  VarlenArgs vl;         // varlen: Nq / Nk above are the longest sequences
+  uint16_t* o;           // varlen: O base, for the rows of a sequence's last tile
 };
 
 // Backward arguments.
@@ -39,6 +50,11 @@ struct BwdParams {
   int* status;
   unsigned long long limit_ns;
   int* info;
+  VarlenArgs vl;         // varlen: N / Nk above are the longest sequences
+  int vec_stride;        // varlen: workspace floats per head (see varlen_vec_offset)
+  uint16_t* dq;          // varlen: output bases, for the rows of a sequence's last tile
+  uint16_t* dk;
+  uint16_t* dv;
 };
 
 // Decode (split over the keys) arguments.
@@ -56,6 +72,43 @@ struct DecParams {
   unsigned long long limit_ns;
   int* info;
 };
+
+// Device status value for cu_seqlens that are out of range (a sequence longer
+// than the stated maximum, decreasing offsets, or past the packed length).
+constexpr int kDevBadSeqlens = 9;
+
+// Varlen backward workspace: per head, sequence b's row vectors start at
+// float offset varlen_vec_offset(cu_q[b], b) (16-byte aligned) and span
+// ceil(Nq_b / 128) * 128 floats, the rows past Nq_b holding the padding
+// values.  Regions of consecutive sequences never overlap; every region ends
+// below varlen_vec_stride(total_q, B) floats.
+__host__ __device__ inline long long varlen_vec_offset(long long q0, long long b) {
+  return ((q0 + 132 * b) + 3) / 4 * 4;
+}
+__host__ __device__ inline long long varlen_vec_stride(long long total_q, long long B) {
+  return varlen_vec_offset(total_q, B) + 128;
+}
+
+#ifdef __CUDACC__
+// One sequence of a (possibly packed) batch as a kernel sees it.
+struct SeqView {
+  int q0, nq;  // first query row in the tensor map, query rows
+  int k0, nk;  // first key row, key rows
+  bool ok;     // offsets consistent with the packed lengths and maxima
+};
+__device__ __forceinline__ SeqView seq_view(const VarlenArgs& vl, int b, int Nq, int Nk) {
+  SeqView v{0, Nq, 0, Nk, true};
+  if (vl.cu_q != nullptr) {
+    v.q0 = vl.cu_q[b];
+    v.nq = vl.cu_q[b + 1] - v.q0;
+    v.k0 = vl.cu_k[b];
+    v.nk = vl.cu_k[b + 1] - v.k0;
+    v.ok = v.q0 >= 0 && v.nq >= 0 && v.nq <= Nq && v.q0 <= vl.total_q - v.nq && v.k0 >= 0 && v.nk >= 0 &&
+           v.nk <= Nk && v.k0 <= vl.total_k - v.nk;
+  }
+  return v;
+}
+#endif
 
 // Shared-memory bytes of each kernel instance (for validation and launch).
 size_t fwd_smem_bytes(int d);

@@ -373,6 +373,9 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
+__device__ __forceinline__ void named_bar_arrive(uint32_t id, uint32_t nthreads) {
+  asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
   asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
                : "memory");
@@ -389,6 +392,52 @@ __device__ __forceinline__ float4 ld_shared_v4f(uint32_t addr) {
 // 128-byte rows stored with the 128-byte swizzle (chunk index XOR row%8).
 __device__ __forceinline__ uint32_t sw128_offset(uint32_t row, uint32_t chunk) {
   return row * 128u + ((chunk ^ (row & 7u)) << 4);
+}
+__device__ __forceinline__ uint4 ld_shared_v4u(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(addr)
+               : "memory");
+  return v;
+}
+
+// Rows [0, nrows) of a [128 x D] bf16 tile staged in shared memory with the
+// 128-byte swizzle (blocks of [128 rows x 64 columns], 16 KB apart) go to
+// global memory with plain 16-byte stores: row r to dst + r * row_stride
+// elements.  For tiles whose remaining rows belong to someone else (the last
+// tile of a packed sequence), where a TMA store of the whole box would write
+// them.  Thread t of nt takes chunks t, t + nt, ...  128 * row_stride must
+// fit in 32 bits (the host checks heads * d * 128 < 2^32).
+// Rows [0, nrows) of a [rows x D] bf16 tile (row stride row_stride
+// elements) set to zero by the whole CTA.  Out of line: it runs only for
+// outputs that nothing attends to (in packed batches), and inlined it would
+// take registers from the kernels' main loops.
+template <int D>
+__device__ __noinline__ void zero_rows_bf16(uint16_t* dst, uint32_t row_stride, int nrows) {
+  for (int c = threadIdx.x; c < nrows * (D / 8); c += blockDim.x)
+    *reinterpret_cast<uint4*>(dst + ((uint32_t)(c / (D / 8)) * row_stride + (c % (D / 8)) * 8)) = make_uint4(0, 0, 0, 0);
+}
+// The same for two tiles with one row layout (dK and dV).
+template <int D>
+__device__ __noinline__ void zero_rows2_bf16(uint16_t* a, uint16_t* b, uint32_t row_stride, int nrows) {
+  for (int c = threadIdx.x; c < nrows * (D / 8); c += blockDim.x) {
+    const uint32_t e = (uint32_t)(c / (D / 8)) * row_stride + (c % (D / 8)) * 8;
+    *reinterpret_cast<uint4*>(a + e) = make_uint4(0, 0, 0, 0);
+    *reinterpret_cast<uint4*>(b + e) = make_uint4(0, 0, 0, 0);
+  }
+}
+
+template <int D>
+__device__ __forceinline__ void store_rows_sw128(uint32_t stage, uint16_t* dst, uint32_t row_stride, int nrows,
+                                                 int t, int nt) {
+  constexpr uint32_t CH = D / 8;  // 16-byte chunks per row
+#pragma unroll 1
+  for (int c = t; c < nrows * (int)CH; c += nt) {
+    const uint32_t row = (uint32_t)c / CH, ch = (uint32_t)c % CH;
+    const uint4 v = ld_shared_v4u(stage + (ch >> 3) * 16384u + sw128_offset(row, ch & 7));
+    *reinterpret_cast<uint4*>(dst + (row * row_stride + ch * 8)) = v;
+  }
 }
 
 }  // namespace sdpa

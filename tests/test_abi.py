@@ -174,3 +174,24 @@ def test_bwd_cross_stages_reject_bad_arguments(lib):
         assert f(300, 200, 1) == S.UNSUPPORTED_SHAPE
         assert f(300, 0, 0) == S.UNSUPPORTED_SHAPE
         assert f(385, 400, 0) == S.WORKSPACE      # workspace sized for 300 (padded: 384) query rows
+
+
+def test_varlen_rejects_bad_arguments(lib):
+    import scaled_dot_product_08_gb300 as sdpa
+    S = sdpa.Status
+    f = lambda B, tq, tk, mq, mk, d=128, scale=0.1, causal=0: sdpa.attn_fwd_varlen(
+        FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, B, 4, 2, tq, tk, mq, mk, d, scale, causal, None)
+    assert f(2, 0, 10, 8, 8) == S.UNSUPPORTED_SHAPE        # no query rows
+    assert f(2, 10, 0, 8, 8) == S.UNSUPPORTED_SHAPE        # no key rows
+    assert f(2, 17, 10, 8, 8) == S.UNSUPPORTED_SHAPE       # total_q > B * max_seqlen_q
+    assert f(2, 10, 10, 0, 8) == S.UNSUPPORTED_SHAPE       # max_seqlen_q < 1
+    assert f(2, 10, 10, 8, 8, d=80) == S.UNSUPPORTED_SHAPE
+    assert f(2, 10, 10, 8, 8, scale=float("nan")) == S.INVALID_ARG
+    assert f(2, 10, 10, 8, 8, causal=3) == S.INVALID_ARG
+    ws = sdpa.attn_bwd_varlen_workspace_size(2, 4, 2, 10, 128)
+    assert ws == 4 * 8 * (((10 + 264 + 3) // 4) * 4 + 128)
+    assert sdpa.attn_bwd_varlen_workspace_size(2, 4, 2, 0, 128) == 0
+    g = lambda wsb, w=FAKE: sdpa.attn_bwd_varlen(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE,
+                                                 w, wsb, 2, 4, 2, 10, 10, 8, 8, 128, 0.1, 1, None)
+    assert g(ws - 1) == S.WORKSPACE
+    assert g(ws, w=0) == S.WORKSPACE
