@@ -61,6 +61,12 @@ def parse_args():
 
 
 def workload_desc(w):
+    if w.kind == "varlen":
+        from sdpa_inputs import varlen_lengths
+        lens = varlen_lengths(w)
+        return (f"{w.name}: packed batch of {len(lens)} sequences ({'+'.join(map(str, lens))} = {w.N} tokens, "
+                f"lengths uniform in [{w.len_range[0]}, {w.len_range[1]}]) H={w.H} Hkv={w.Hkv} d={w.d} "
+                f"{'causal' if w.causal else 'non-causal'} {'fwd+bwd' if w.with_grad else 'fwd'}")
     if w.kind == "cross":
         what = "fwd+bwd (encoder-decoder cross attention)" if w.with_grad else "fwd (chunked prefill)"
         return (f"{w.name}: B={w.B} H={w.H} Hkv={w.Hkv} Nq={w.n_queries} Nk={w.N} d={w.d} "
@@ -72,6 +78,10 @@ def workload_desc(w):
 
 def step_flops(w):
     from sdpa_inputs import flops_backward, flops_cross, flops_forward
+    if w.kind == "varlen":
+        from sdpa_inputs import flops_varlen, varlen_lengths
+        f = flops_varlen(varlen_lengths(w), w.H, w.d, w.causal)
+        return f, (2.5 * f if w.with_grad else 0.0)
     if w.kind == "cross":
         f = flops_cross(w.B, w.H, w.n_queries, w.N, w.d, w.causal)
         return f, (2.5 * f if w.with_grad else 0.0)
@@ -169,12 +179,23 @@ def max_over_ranks(x: float) -> float:
 
 
 # ------------------------------------------------------------ CPU oracle arm
+def _oracle_lengths(w):
+    """(query rows, key rows) of the oracle's per-step sample: one head of
+    the workload; for a packed batch one head of its first sequence."""
+    if w.kind == "varlen":
+        from sdpa_inputs import varlen_lengths
+        n = varlen_lengths(w)[0]
+        return n, n
+    return w.n_queries, w.N
+
+
 def _oracle_head_inputs(w):
     import numpy as np
     from sdpa_inputs import draw
     rng = np.random.default_rng(w.seed)
     dd = w.d_draw or w.d
-    shapes = [(1, 1, w.n_queries, dd), (1, 1, w.N, dd), (1, 1, w.N, dd), (1, 1, w.n_queries, dd)]
+    nq, nk = _oracle_lengths(w)
+    shapes = [(1, 1, nq, dd), (1, 1, nk, dd), (1, 1, nk, dd), (1, 1, nq, dd)]
     return [draw(rng, sh, a) for sh, a in zip(shapes, (w.amp, w.amp, w.amp, 1.0))]
 
 
@@ -192,6 +213,9 @@ def _oracle_head_seconds(w, x):
 
 def _head_flops(w):
     from sdpa_inputs import flops_backward, flops_forward
+    if w.kind == "varlen":
+        n = _oracle_lengths(w)[0]
+        return flops_forward(1, 1, n, w.d, w.causal) * (3.5 if w.with_grad else 1.0)
     if w.kind == "cross":
         from sdpa_inputs import flops_cross
         return flops_cross(1, 1, w.n_queries, w.N, w.d, w.causal) * (3.5 if w.with_grad else 1.0)
@@ -199,6 +223,8 @@ def _head_flops(w):
 
 
 def _head_dims(w):
+    if w.kind == "varlen":
+        return f"N={_oracle_lengths(w)[0]} (its first sequence), d={w.d}"
     n = f"Nq={w.n_queries}, Nk={w.N}" if w.kind == "cross" else f"N={w.N}"
     return f"{n}, d={w.d_draw or w.d}"
 
@@ -295,18 +321,31 @@ def run_ours(args, w, rank, world, local_rank):
     dist = None
     if world > 1:
         import torch.distributed as dist
-    x = make_inputs(w)
     dev = lambda a: torch.from_numpy(a).to(torch.bfloat16).cuda()
-    q, k, v = dev(x["q"]), dev(x["k"]), dev(x["v"])
-    do = dev(x["do"]) if w.with_grad else None
     B, H, Hkv, N, d = w.B, w.H, w.Hkv, w.N, w.d
     s = w.softmax_scale
-    o = torch.empty_like(q)
     Nq = w.n_queries
-    lse = torch.empty((B, H, Nq), dtype=torch.float32, device="cuda")
+    extra_in = []  # further device inputs of a step (cu_seqlens)
+    if w.kind == "varlen":
+        from sdpa_inputs import make_varlen_inputs
+        x = make_varlen_inputs(w)
+        cu = torch.from_numpy(x["cu"]).cuda()
+        extra_in = [cu]
+        nseq, maxlen = len(x["lengths"]), int(x["lengths"].max())
+        lse_shape = (H, N)
+    else:
+        x = make_inputs(w)
+        lse_shape = (B, H, Nq)
+    q, k, v = dev(x["q"]), dev(x["k"]), dev(x["v"])
+    do = dev(x["do"]) if w.with_grad else None
+    o = torch.empty_like(q)
+    lse = torch.empty(lse_shape, dtype=torch.float32, device="cuda")
     if w.with_grad:
         dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-        ws_bytes = sdpa.attn_bwd_workspace_size(B, H, Hkv, Nq, d)
+        if w.kind == "varlen":
+            ws_bytes = sdpa.attn_bwd_varlen_workspace_size(nseq, H, Hkv, N, d)
+        else:
+            ws_bytes = sdpa.attn_bwd_workspace_size(B, H, Hkv, Nq, d)
         ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
     stream = torch.cuda.current_stream()
     sp = stream.cuda_stream
@@ -316,41 +355,47 @@ def run_ours(args, w, rank, world, local_rank):
         if st != 0:
             raise RuntimeError(f"{where}: {sdpa.attn_status_string(st)}")
 
-    def step(evs=None):
-        if evs is not None:
-            evs[0].record(stream)
-        if w.kind == "cross":
-            chk(sdpa.attn_fwd_cross(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
-                                    B, H, Hkv, Nq, N, d, s, w.causal, sp), "attn_fwd_cross")
-        else:
-            chk(sdpa.attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
-                              B, H, Hkv, N, d, s, w.causal, sp), "attn_fwd")
-        if evs is not None:
-            evs[1].record(stream)
+    P = lambda t: t.data_ptr()
+    # One callable per kernel of the step, in order (names above).
+    if w.kind == "varlen":
+        def vstage(mask):
+            return lambda: chk(sdpa.attn_bwd_varlen_stages(
+                P(q), P(k), P(v), P(o), P(lse), P(do), P(dq), P(dk), P(dv), P(cu), P(cu), P(ws), ws_bytes,
+                nseq, H, Hkv, N, N, maxlen, maxlen, d, s, w.causal, mask, sp), "attn_bwd_varlen_stages")
+        launches = [lambda: chk(sdpa.attn_fwd_varlen(P(q), P(k), P(v), P(o), P(lse), P(cu), P(cu), nseq, H, Hkv,
+                                                     N, N, maxlen, maxlen, d, s, w.causal, sp), "attn_fwd_varlen")]
         if w.with_grad:
-            chk(sdpa.attn_bwd_prep(o.data_ptr(), lse.data_ptr(), do.data_ptr(), ws.data_ptr(), ws_bytes,
-                                   B, H, Hkv, Nq, d, sp), "attn_bwd_prep")
+            launches += [vstage(1), vstage(2), vstage(4)]
+    elif w.kind == "cross":
+        launches = [lambda: chk(sdpa.attn_fwd_cross(P(q), P(k), P(v), P(o), P(lse), B, H, Hkv, Nq, N, d, s,
+                                                    w.causal, sp), "attn_fwd_cross")]
+        if w.with_grad:
+            launches += [
+                lambda: chk(sdpa.attn_bwd_prep(P(o), P(lse), P(do), P(ws), ws_bytes, B, H, Hkv, Nq, d, sp),
+                            "attn_bwd_prep"),
+                lambda: chk(sdpa.attn_bwd_grad_cross(P(q), P(k), P(v), P(do), P(dk), P(dv), P(ws), ws_bytes,
+                                                     B, H, Hkv, Nq, N, d, s, w.causal, sp), "attn_bwd_grad_cross"),
+                lambda: chk(sdpa.attn_bwd_dq_cross(P(q), P(k), P(v), P(do), P(dq), P(ws), ws_bytes,
+                                                   B, H, Hkv, Nq, N, d, s, w.causal, sp), "attn_bwd_dq_cross")]
+    else:
+        launches = [lambda: chk(sdpa.attn_fwd(P(q), P(k), P(v), P(o), P(lse), B, H, Hkv, N, d, s, w.causal, sp),
+                                "attn_fwd")]
+        if w.with_grad:
+            launches += [
+                lambda: chk(sdpa.attn_bwd_prep(P(o), P(lse), P(do), P(ws), ws_bytes, B, H, Hkv, N, d, sp),
+                            "attn_bwd_prep"),
+                lambda: chk(sdpa.attn_bwd_grad(P(q), P(k), P(v), P(do), P(dk), P(dv), P(ws), ws_bytes,
+                                               B, H, Hkv, N, d, s, w.causal, sp), "attn_bwd_grad"),
+                lambda: chk(sdpa.attn_bwd_dq(P(q), P(k), P(v), P(do), P(dq), P(ws), ws_bytes,
+                                             B, H, Hkv, N, d, s, w.causal, sp), "attn_bwd_dq")]
+
+    def step(evs=None):
+        for idx, launch in enumerate(launches):
             if evs is not None:
-                evs[2].record(stream)
-            if w.kind == "cross":
-                chk(sdpa.attn_bwd_grad_cross(q.data_ptr(), k.data_ptr(), v.data_ptr(), do.data_ptr(),
-                                             dk.data_ptr(), dv.data_ptr(), ws.data_ptr(), ws_bytes,
-                                             B, H, Hkv, Nq, N, d, s, w.causal, sp), "attn_bwd_grad_cross")
-            else:
-                chk(sdpa.attn_bwd_grad(q.data_ptr(), k.data_ptr(), v.data_ptr(), do.data_ptr(), dk.data_ptr(),
-                                       dv.data_ptr(), ws.data_ptr(), ws_bytes, B, H, Hkv, N, d, s, w.causal, sp),
-                    "attn_bwd_grad")
-            if evs is not None:
-                evs[3].record(stream)
-            if w.kind == "cross":
-                chk(sdpa.attn_bwd_dq_cross(q.data_ptr(), k.data_ptr(), v.data_ptr(), do.data_ptr(),
-                                           dq.data_ptr(), ws.data_ptr(), ws_bytes,
-                                           B, H, Hkv, Nq, N, d, s, w.causal, sp), "attn_bwd_dq_cross")
-            else:
-                chk(sdpa.attn_bwd_dq(q.data_ptr(), k.data_ptr(), v.data_ptr(), do.data_ptr(), dq.data_ptr(),
-                                     ws.data_ptr(), ws_bytes, B, H, Hkv, N, d, s, w.causal, sp), "attn_bwd_dq")
-            if evs is not None:
-                evs[4].record(stream)
+                evs[idx].record(stream)
+            launch()
+        if evs is not None:
+            evs[len(launches)].record(stream)
 
     def barrier():
         torch.cuda.synchronize()
@@ -431,6 +476,7 @@ def run_ours(args, w, rank, world, local_rank):
     if not args.no_e2e:
         hq, hk, hv = (t.cpu().pin_memory() for t in (q, k, v))
         ins = [(q, hq), (k, hk), (v, hv)] + ([(do, do.cpu().pin_memory())] if w.with_grad else [])
+        ins += [(t, t.cpu().pin_memory()) for t in extra_in]
         outs = [o, lse] + ([dq, dk, dv] if w.with_grad else [])
         houts = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in outs]
         h2d = sum(h.numel() * h.element_size() for _, h in ins)

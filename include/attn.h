@@ -232,6 +232,23 @@ attn_status_t attn_bwd_varlen(const void* q, const void* k, const void* v, const
                               void* stream);
 
 /*
+ * The stages of attn_bwd_varlen, for callers that schedule (or time) them
+ * separately: `stages` is a non-zero OR of 1 (prep: D and lse in base 2 into
+ * the workspace), 2 (grad: dK, dV) and 4 (dq: dQ), run in that order.  The
+ * ordering rules of attn_bwd_prep / _grad / _dq apply: prep completes before
+ * grad or dq starts.  Other arguments as attn_bwd_varlen (all pointers are
+ * checked whether or not the stage reads them).
+ */
+attn_status_t attn_bwd_varlen_stages(const void* q, const void* k, const void* v, const void* o,
+                                     const float* lse, const void* dout,
+                                     void* dq, void* dk, void* dv,
+                                     const int* cu_seqlens_q, const int* cu_seqlens_k,
+                                     void* workspace, size_t workspace_bytes,
+                                     int B, int H, int Hkv, int total_q, int total_k,
+                                     int max_seqlen_q, int max_seqlen_k, int d, float scale, int causal,
+                                     unsigned stages, void* stream);
+
+/*
  * Decode: attention of Nq new queries per head against a cache of Nk keys
  * and values (a KV cache), computed in key chunks that are merged by their
  * logsumexp.  Page "Flash Attention原理", FAQ on inference (the KV cache moves

@@ -25,7 +25,7 @@ __all__ = [
     "attn_get_device_status", "attn_get_timeout_info", "attn_status_string", "attn_selftest_wait_timeout",
     "attn_decode", "attn_decode_workspace_size", "attn_fwd_cross", "attn_bwd_cross",
     "attn_bwd_grad_cross", "attn_bwd_dq_cross", "attn_fwd_varlen", "attn_bwd_varlen",
-    "attn_bwd_varlen_workspace_size", "forward_varlen", "backward_varlen",
+    "attn_bwd_varlen_workspace_size", "attn_bwd_varlen_stages", "forward_varlen", "backward_varlen",
     "forward", "forward_cross", "backward", "backward_cross", "decode", "build",
 ]
 
@@ -97,6 +97,10 @@ def load() -> ctypes.CDLL:
         lib.attn_bwd_varlen.argtypes = [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t,
                                         _I, _I, _I, _I, _I, _I, _I, _I, ctypes.c_float, _I, _P]
         lib.attn_bwd_varlen.restype = _I
+        lib.attn_bwd_varlen_stages.argtypes = [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t,
+                                               _I, _I, _I, _I, _I, _I, _I, _I, ctypes.c_float, _I, ctypes.c_uint,
+                                               _P]
+        lib.attn_bwd_varlen_stages.restype = _I
         lib.attn_decode_workspace_size.argtypes = [_I, _I, _I, _I, _I, _I]
         lib.attn_decode_workspace_size.restype = ctypes.c_size_t
         lib.attn_decode.argtypes = [_P, _P, _P, _P, _P, _P, ctypes.c_size_t, _I, _I, _I, _I, _I, _I,
@@ -189,6 +193,13 @@ def attn_bwd_varlen(q, k, v, o, lse, dout, dq, dk, dv, cu_q, cu_k, workspace, wo
                     total_q, total_k, max_q, max_k, d, scale, causal, stream) -> int:
     return load().attn_bwd_varlen(q, k, v, o, lse, dout, dq, dk, dv, cu_q, cu_k, workspace, workspace_bytes,
                                   B, H, Hkv, total_q, total_k, max_q, max_k, d, scale, causal, stream)
+
+
+def attn_bwd_varlen_stages(q, k, v, o, lse, dout, dq, dk, dv, cu_q, cu_k, workspace, workspace_bytes, B, H, Hkv,
+                           total_q, total_k, max_q, max_k, d, scale, causal, stages, stream) -> int:
+    return load().attn_bwd_varlen_stages(q, k, v, o, lse, dout, dq, dk, dv, cu_q, cu_k, workspace, workspace_bytes,
+                                         B, H, Hkv, total_q, total_k, max_q, max_k, d, scale, causal, stages,
+                                         stream)
 
 
 def attn_decode_workspace_size(B, H, Hkv, Nq, Nk, d) -> int:

@@ -497,26 +497,33 @@ size_t attn_bwd_varlen_workspace_size(int B, int H, int Hkv, int total_q, int d)
   return (size_t)H * (size_t)sdpa::varlen_vec_stride(total_q, B) * 4 * 2;  // -D and -lse2 per head, float32
 }
 
-attn_status_t attn_bwd_varlen(const void* q, const void* k, const void* v, const void* o, const float* lse,
-                              const void* dout, void* dq, void* dk, void* dv, const int* cu_seqlens_q,
-                              const int* cu_seqlens_k, void* workspace, size_t workspace_bytes, int B, int H,
-                              int Hkv, int total_q, int total_k, int max_seqlen_q, int max_seqlen_k, int d,
-                              float scale, int causal, void* stream) {
-  ATTN_TRY(check_varlen_shape(B, H, Hkv, total_q, total_k, max_seqlen_q, max_seqlen_k, d));
+// Everything the three varlen backward stages share: validation, tensor
+// maps and kernel arguments.  Maps for arguments a stage does not use are
+// built over placeholders that stay valid (they are never read).
+struct VarlenBwd {
+  CUtensorMap tq, tk, tv, tdo, tdq, tdk, tdv;
+  sdpa::BwdParams p;
+};
+
+static attn_status_t varlen_bwd_setup(VarlenBwd* w, const void* q, const void* k, const void* v, const void* o,
+                                      const float* lse, const void* dout, void* dq, void* dk, void* dv,
+                                      const int* cu_q, const int* cu_k, void* workspace, size_t workspace_bytes,
+                                      int B, int H, int Hkv, int total_q, int total_k, int max_q, int max_k, int d,
+                                      float scale, int causal) {
+  ATTN_TRY(check_varlen_shape(B, H, Hkv, total_q, total_k, max_q, max_k, d));
   ATTN_TRY(check_scale_flag(scale, causal));
   if (workspace == nullptr || workspace_bytes < attn_bwd_varlen_workspace_size(B, H, Hkv, total_q, d))
     return ATTN_ERR_WORKSPACE;
   ATTN_TRY(check_ptrs({q, k, v, o, lse, dout, dq, dk, dv, workspace}));
-  ATTN_TRY(check_offsets_ptrs(cu_seqlens_q, cu_seqlens_k));
+  ATTN_TRY(check_offsets_ptrs(cu_q, cu_k));
   DeviceInfo* di = nullptr;
   ATTN_TRY(current_device(&di));
-  CUtensorMap tq, tk, tv, tdo, tdq, tdk, tdv;
-  if (!make_map_bf16_packed(&tq, q, d, total_q, H) || !make_map_bf16_packed(&tk, k, d, total_k, Hkv) ||
-      !make_map_bf16_packed(&tv, v, d, total_k, Hkv) || !make_map_bf16_packed(&tdo, dout, d, total_q, H) ||
-      !make_map_bf16_packed(&tdq, dq, d, total_q, H) || !make_map_bf16_packed(&tdk, dk, d, total_k, Hkv) ||
-      !make_map_bf16_packed(&tdv, dv, d, total_k, Hkv))
+  if (!make_map_bf16_packed(&w->tq, q, d, total_q, H) || !make_map_bf16_packed(&w->tk, k, d, total_k, Hkv) ||
+      !make_map_bf16_packed(&w->tv, v, d, total_k, Hkv) || !make_map_bf16_packed(&w->tdo, dout, d, total_q, H) ||
+      !make_map_bf16_packed(&w->tdq, dq, d, total_q, H) || !make_map_bf16_packed(&w->tdk, dk, d, total_k, Hkv) ||
+      !make_map_bf16_packed(&w->tdv, dv, d, total_k, Hkv))
     return ATTN_ERR_CUDA;
-  sdpa::BwdParams p;
+  sdpa::BwdParams& p = w->p;
   memset(&p, 0, sizeof(p));
   p.o = static_cast<const uint16_t*>(o);
   p.dout = static_cast<const uint16_t*>(dout);
@@ -527,29 +534,65 @@ attn_status_t attn_bwd_varlen(const void* q, const void* k, const void* v, const
   p.B = B;
   p.H = H;
   p.Hkv = Hkv;
-  p.N = max_seqlen_q;
+  p.N = max_q;
   p.G = H / Hkv;
   p.d = d;
-  p.nq = (max_seqlen_q + 127) / 128;
-  p.Nk = max_seqlen_k;
-  p.nkv = (max_seqlen_k + 127) / 128;
+  p.nq = (max_q + 127) / 128;
+  p.Nk = max_k;
+  p.nkv = (max_k + 127) / 128;
   p.scale = scale;
   p.scale_log2 = scale * 1.4426950408889634f;
   p.status = di->status;
   p.limit_ns = wait_limit_ns();
   p.info = di->info;
-  p.vl.cu_q = cu_seqlens_q;
-  p.vl.cu_k = cu_seqlens_k;
+  p.vl.cu_q = cu_q;
+  p.vl.cu_k = cu_k;
   p.vl.total_q = total_q;
   p.vl.total_k = total_k;
   p.dq = static_cast<uint16_t*>(dq);
   p.dk = static_cast<uint16_t*>(dk);
   p.dv = static_cast<uint16_t*>(dv);
-  const cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (sdpa::launch_bwd_prep(p, st) != cudaSuccess) return ATTN_ERR_LAUNCH;
-  if (sdpa::launch_bwd_grad(d, causal != 0, tq, tk, tv, tdo, tdk, tdv, p, st) != cudaSuccess) return ATTN_ERR_LAUNCH;
-  if (sdpa::launch_bwd_dq(d, causal != 0, tq, tk, tv, tdo, tdq, p, st) != cudaSuccess) return ATTN_ERR_LAUNCH;
   return ATTN_OK;
+}
+
+enum : unsigned { kStagePrep = 1, kStageGrad = 2, kStageDq = 4 };
+
+static attn_status_t varlen_bwd_run(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                                    const void* dout, void* dq, void* dk, void* dv, const int* cu_q, const int* cu_k,
+                                    void* workspace, size_t workspace_bytes, int B, int H, int Hkv, int total_q,
+                                    int total_k, int max_q, int max_k, int d, float scale, int causal, void* stream,
+                                    unsigned stages) {
+  VarlenBwd w;
+  ATTN_TRY(varlen_bwd_setup(&w, q, k, v, o, lse, dout, dq, dk, dv, cu_q, cu_k, workspace, workspace_bytes, B, H,
+                            Hkv, total_q, total_k, max_q, max_k, d, scale, causal));
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if ((stages & kStagePrep) && sdpa::launch_bwd_prep(w.p, st) != cudaSuccess) return ATTN_ERR_LAUNCH;
+  if ((stages & kStageGrad) &&
+      sdpa::launch_bwd_grad(d, causal != 0, w.tq, w.tk, w.tv, w.tdo, w.tdk, w.tdv, w.p, st) != cudaSuccess)
+    return ATTN_ERR_LAUNCH;
+  if ((stages & kStageDq) && sdpa::launch_bwd_dq(d, causal != 0, w.tq, w.tk, w.tv, w.tdo, w.tdq, w.p, st) != cudaSuccess)
+    return ATTN_ERR_LAUNCH;
+  return ATTN_OK;
+}
+
+attn_status_t attn_bwd_varlen(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                              const void* dout, void* dq, void* dk, void* dv, const int* cu_seqlens_q,
+                              const int* cu_seqlens_k, void* workspace, size_t workspace_bytes, int B, int H,
+                              int Hkv, int total_q, int total_k, int max_seqlen_q, int max_seqlen_k, int d,
+                              float scale, int causal, void* stream) {
+  return varlen_bwd_run(q, k, v, o, lse, dout, dq, dk, dv, cu_seqlens_q, cu_seqlens_k, workspace, workspace_bytes,
+                        B, H, Hkv, total_q, total_k, max_seqlen_q, max_seqlen_k, d, scale, causal, stream,
+                        kStagePrep | kStageGrad | kStageDq);
+}
+
+attn_status_t attn_bwd_varlen_stages(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                                     const void* dout, void* dq, void* dk, void* dv, const int* cu_seqlens_q,
+                                     const int* cu_seqlens_k, void* workspace, size_t workspace_bytes, int B, int H,
+                                     int Hkv, int total_q, int total_k, int max_seqlen_q, int max_seqlen_k, int d,
+                                     float scale, int causal, unsigned stages, void* stream) {
+  if (stages == 0 || (stages & ~7u) != 0) return ATTN_ERR_INVALID_ARG;
+  return varlen_bwd_run(q, k, v, o, lse, dout, dq, dk, dv, cu_seqlens_q, cu_seqlens_k, workspace, workspace_bytes,
+                        B, H, Hkv, total_q, total_k, max_seqlen_q, max_seqlen_k, d, scale, causal, stream, stages);
 }
 
 // Key chunks of the decode kernel, a pure function of the shape (so the

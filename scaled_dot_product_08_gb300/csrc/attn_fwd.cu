@@ -13,7 +13,7 @@
 //   warp  8    TMA producer: Q tiles once, then K_j / V_j into a smem ring
 //              (5 slots at d = 96 / 128, 8 at d = 64)
 //   warp  9    MMA issuer: tcgen05 S = Q K^T and O += P V (one elected lane issues)
-//   warps 10-11 idle
+//   warps 10-11 store the last, partial O tile of a packed sequence row by row
 // setmaxnreg moves registers from the producer/MMA warpgroup (88 each) to
 // the softmax warpgroups (208 each): 2*128*208 + 128*88 = 384*168, the
 // block's launch allocation.
@@ -157,7 +157,11 @@ __global__ void __launch_bounds__(384, 1)
     const uint32_t tO = tmem + 256 + s * 128 + lane_off;
     const uint32_t barS = bS + 8u * s, barP = bP + 16u * s, barO = bO + 8u * s;
     const float c = p.scale_log2;
-    float m = -INFINITY, l = 0.f;
+    // The running max starts at -1e30 rather than -inf: a row that has seen
+    // only masked keys so far (packed batches) then gets p = 2^(-inf) = 0 for
+    // them instead of 2^(-inf + inf) = NaN, and the first visible key still
+    // raises the max (alpha = 2^(-1e30 - m) = 0).
+    float m = -1e30f, l = 0.f;
     bool ok = true;
 
     for (int j = 0; j < n; ++j) {
@@ -230,10 +234,7 @@ __global__ void __launch_bounds__(384, 1)
       // sum runs in 4 packed partial sums.  P is published in two halves of
       // 64 keys (one barrier per half) so that the P V MMA over the first 64
       // keys runs while the second half is computed.
-      // A row that has seen no key yet (m = -inf: only in packed batches)
-      // takes exponent base 0, so its masked scores give p = 0, not NaN.
-      const float mu = (m == -INFINITY) ? 0.f : m;
-      const float2 c2 = make_float2(c, c), nm2 = make_float2(-mu, -mu);
+      const float2 c2 = make_float2(c, c), nm2 = make_float2(-m, -m);
       float2 sum[4];
 #pragma unroll
       for (int k = 0; k < 4; ++k) sum[k] = make_float2(0.f, 0.f);
@@ -282,24 +283,30 @@ __global__ void __launch_bounds__(384, 1)
       fence_proxy_async_smem();
     }
     named_bar_sync(1 + s, 128);
-    if (ok) {
-      // The dense batch clips the box at Nq; in a packed batch the rows past
-      // the sequence belong to the next one, so a partial tile is stored row
-      // by row instead.
-      const int q0 = seq_s[0], nq = seq_s[1], qplane = seq_s[4], hh = seq_s[5];
+    {
+      // The dense batch clips the box at Nq.  In a packed batch the rows past
+      // the sequence belong to the next one, so warp 10 + s stores a partial
+      // tile row by row once the staging is complete (barrier 3 + s).
+      const int q0 = seq_s[0], nq = seq_s[1], qplane = seq_s[4];
       const bool packed = p.vl.cu_q != nullptr;
       const int valid = nq - qi * 128;
       if (valid >= 128 || (!packed && valid > 0)) {
-        if (r == 0) {
+        if (ok && r == 0) {
           for (int cb = 0; cb < T::NB; ++cb)
             tma_store_3d(&tmO, sOut + cb * T::BLOCK_BYTES, cb * 64, q0 + qi * 128, qplane);
           bulk_commit();
           bulk_wait_read_all();
         }
       } else if (valid > 0) {
-        const uint32_t rs = (uint32_t)(p.H * D);
-        store_rows_sw128<D>(sOut, p.o + ((long long)q0 + qi * 128) * rs + (long long)hh * D, rs, valid, r, 128);
+        if (s == 0)
+          named_bar_arrive_c<3, 128 + 32>();
+        else
+          named_bar_arrive_c<4, 128 + 32>();
       }
+    }
+    if (ok) {
+      const int q0 = seq_s[0], nq = seq_s[1], qplane = seq_s[4];
+      const bool packed = p.vl.cu_q != nullptr;
       const int row = qi * 128 + r;
       // lse: (H, total_q) for a packed batch, (B, H, Nq) otherwise; the
       // query plane is the head there and b * H + h here.
@@ -347,6 +354,22 @@ __global__ void __launch_bounds__(384, 1)
         }
       }
       __syncwarp();
+    } else if (warp >= 10) {
+      // ------------------------------------------------------------ partial O tile (packed batch)
+      const int s = warp - 10;
+      const int valid = seq_s[1] - (2 * mt + s) * 128;
+      if (p.vl.cu_q != nullptr && valid > 0 && valid < 128) {
+        if (s == 0)
+          named_bar_sync_c<3, 128 + 32>();
+        else
+          named_bar_sync_c<4, 128 + 32>();
+        if (*abort_flag == 0) {  // the staging is complete unless a wait gave up
+          const uint32_t rs = (uint32_t)(p.H * D);
+          store_rows_sw128<D>(sQ + s * T::TILE_BYTES,
+                              p.o + ((long long)seq_s[0] + (2 * mt + s) * 128) * rs + (long long)seq_s[5] * D, rs,
+                              valid, lane, 32);
+        }
+      }
     } else if (warp == 9) {
       // ------------------------------------------------------------ MMA issuer
       // The whole warp runs the issue loop, so descriptor arithmetic stays

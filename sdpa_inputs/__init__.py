@@ -34,6 +34,16 @@ no mask), forward + backward:
 
   cx   B=8  H=16  Hkv=16 Nq=2048 N=4096  d=128  non-causal  seed 9
 
+Packed variable-length batch (the pages' FAQ on variable lengths: sequences
+of different lengths packed into one batch by cumulative offsets), forward +
+backward, self-attention (the same lengths for queries and keys):
+
+  vl1  32768 tokens, H=16 Hkv=16 d=128, causal, seed 10; sequence lengths
+       drawn uniformly from [128, 8192] (numpy default_rng(10).integers,
+       inclusive) until they reach 32768 tokens, the last one cut to fit.
+       Tensors are packed token-major: (total, heads, d).  The draws of Q,
+       K, V, dO use default_rng(seed + 1000) in that order.
+
 Every draw is numpy's PCG64 ``default_rng(seed).standard_normal(dtype=float32)``
 taken in the fixed order Q, K, V, dO, multiplied by the config's amplitude and
 then rounded to bf16 (round to nearest, ties to even).
@@ -61,7 +71,9 @@ class Workload:
     with_grad: bool = False        # also draw dO
     scale: float | None = None     # default 1/sqrt(d_draw or d)
     Nq: int | None = None          # decode / cross: query rows per head (None: Nq = N)
-    kind: str = "full"             # "full" (Nq = N), "decode" (attn_decode), "cross" (attn_fwd_cross)
+    kind: str = "full"             # "full" (Nq = N), "decode" (attn_decode), "cross" (attn_fwd_cross),
+                                   # "varlen" (attn_fwd_varlen: N = total tokens, B = 1)
+    len_range: tuple[int, int] | None = None  # varlen: sequence lengths drawn from [lo, hi]
 
     @property
     def softmax_scale(self) -> float:
@@ -90,7 +102,36 @@ WORKLOADS: dict[str, Workload] = {
     "dec4": Workload("dec4", 8, 64, 8, 32768, 128, True, 7, Nq=4, kind="decode"),
     "cp1": Workload("cp1", 1, 32, 8, 16384, 128, True, 8, Nq=2048, kind="cross"),
     "cx": Workload("cx", 8, 16, 16, 4096, 128, False, 9, with_grad=True, Nq=2048, kind="cross"),
+    "vl1": Workload("vl1", 1, 16, 16, 32768, 128, True, 10, with_grad=True, kind="varlen", len_range=(128, 8192)),
 }
+
+
+def varlen_lengths(w: Workload) -> list[int]:
+    """Sequence lengths of a packed workload: uniform integers in
+    w.len_range (inclusive) from default_rng(w.seed) until they cover w.N
+    tokens; the last one is cut so that they sum to exactly w.N."""
+    lo, hi = w.len_range
+    rng = np.random.default_rng(w.seed)
+    out, tot = [], 0
+    while tot < w.N:
+        n = int(rng.integers(lo, hi, endpoint=True))
+        n = min(n, w.N - tot)
+        out.append(n)
+        tot += n
+    return out
+
+
+def make_varlen_inputs(w: Workload) -> dict[str, np.ndarray]:
+    """Packed (total, heads, d) Q, K, V, dO of a varlen workload and its
+    int32 cumulative offsets cu (B + 1 entries)."""
+    lens = varlen_lengths(w)
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    rng = np.random.default_rng(w.seed + 1000)
+    out = {"q": draw(rng, (w.N, w.H, w.d), w.amp), "k": draw(rng, (w.N, w.Hkv, w.d), w.amp),
+           "v": draw(rng, (w.N, w.Hkv, w.d), w.amp), "cu": cu, "lengths": np.array(lens)}
+    if w.with_grad:
+        out["do"] = draw(rng, (w.N, w.H, w.d), 1.0)
+    return out
 
 
 def workload(name: str, **overrides) -> Workload:
@@ -147,6 +188,12 @@ def flops_cross(B: int, H: int, Nq: int, Nk: int, d: int, causal: bool) -> float
     square Nq x Nq corner is counted halved as in the Nq = Nk convention."""
     pairs = Nq * (Nk - Nq) + Nq * Nq / 2 if causal else Nq * Nk
     return 4.0 * B * H * d * pairs
+
+
+def flops_varlen(lengths, H: int, d: int, causal: bool) -> float:
+    """Forward work of a packed self-attention batch: the forward convention
+    summed over its sequences."""
+    return sum(flops_forward(1, H, int(n), d, causal) for n in lengths)
 
 
 def flops_forward(B: int, H: int, N: int, d: int, causal: bool) -> float:

@@ -149,3 +149,28 @@ def test_inconsistent_offsets_are_reported(cuda_lib):
         assert cuda_lib.attn_get_device_status(None) == cuda_lib.Status.INVALID_ARG
     # the status word is cleared by the read
     assert cuda_lib.attn_get_device_status(None) == cuda_lib.Status.OK
+
+
+def test_varlen_stages_equal_the_combined_call(cuda_lib):
+    import torch
+    lq = [300, 17, 700]
+    H, Hkv, d = 4, 2, 128
+    q, k, v, do, cu_q, cu_k = _packed(lq, lq, H, Hkv, d, 36001)
+    tq, tk, tv, tdo = dev(q), dev(k), dev(v), dev(do)
+    cq = _cu(cu_q)
+    O, lse = cuda_lib.forward_varlen(tq, tk, tv, cq, cq, 700, 700, 0.1, True)
+    want = [host(g) for g in cuda_lib.backward_varlen(tq, tk, tv, O, lse, tdo, cq, cq, 700, 700, 0.1, True)]
+    ws_bytes = cuda_lib.attn_bwd_varlen_workspace_size(3, H, Hkv, int(cu_q[-1]), d)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
+    dq, dk, dv = torch.empty_like(tq), torch.empty_like(tk), torch.empty_like(tv)
+    sp = torch.cuda.current_stream().cuda_stream
+    P = lambda t: t.data_ptr()
+    for stages in (1, 2, 4):
+        assert cuda_lib.attn_bwd_varlen_stages(P(tq), P(tk), P(tv), P(O), P(lse), P(tdo), P(dq), P(dk), P(dv),
+                                               P(cq), P(cq), P(ws), ws_bytes, 3, H, Hkv, int(cu_q[-1]),
+                                               int(cu_q[-1]), 700, 700, d, 0.1, 1, stages, sp) == 0
+    for got, w in zip((dq, dk, dv), want):
+        assert np.array_equal(host(got), w)
+    assert cuda_lib.attn_bwd_varlen_stages(P(tq), P(tk), P(tv), P(O), P(lse), P(tdo), P(dq), P(dk), P(dv),
+                                           P(cq), P(cq), P(ws), ws_bytes, 3, H, Hkv, int(cu_q[-1]),
+                                           int(cu_q[-1]), 700, 700, d, 0.1, 1, 8, sp) == cuda_lib.Status.INVALID_ARG
