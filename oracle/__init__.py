@@ -33,6 +33,9 @@ from .sdpa import (
     attention_cross_backward,
     attention_varlen_forward,
     attention_varlen_backward,
+    attention_masked_forward,
+    attention_masked_backward,
+    visibility,
     merge_splits,
     softmax_rows,
     softmax_two_block,
@@ -50,6 +53,9 @@ __all__ = [
     "attention_cross_backward",
     "attention_varlen_forward",
     "attention_varlen_backward",
+    "attention_masked_forward",
+    "attention_masked_backward",
+    "visibility",
     "merge_splits",
     "softmax_rows",
     "softmax_two_block",

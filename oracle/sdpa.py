@@ -57,6 +57,107 @@ def _scores(qh, kh, scale, causal, rows=None, q_offset=0):
     return S
 
 
+def visibility(Nq, Nk, causal=False, q_offset=0, window=None, key_length=None, mask=None):
+    """Boolean (Nq, Nk) matrix: may query row i attend to key j?
+
+    Query row i sits at position q_offset + i.  The conditions combine by
+    AND ([SDPA] §3: is_causal, and attn_mask with True = take part):
+      causal      j <= q_offset + i
+      window      (wl, wr): j >= q_offset + i - wl when wl >= 0 and
+                  j <= q_offset + i + wr when wr >= 0 (a sliding window, the
+                  [PROF] section on changing the architecture: cost n * w
+                  instead of n^2); -1 leaves that side open
+      key_length  j < key_length (a padding mask: the keys past a batch
+                  element's length are padding)
+      mask        an explicit boolean (Nq, Nk) matrix ([FA] FAQ Q11).
+    """
+    i = q_offset + np.arange(Nq)[:, None]
+    j = np.arange(Nk)[None, :]
+    vis = np.ones((Nq, Nk), dtype=bool)
+    if causal:
+        vis &= j <= i
+    if window is not None:
+        wl, wr = window
+        if wl >= 0:
+            vis &= j >= i - wl
+        if wr >= 0:
+            vis &= j <= i + wr
+    if key_length is not None:
+        vis &= j < key_length
+    if mask is not None:
+        vis &= np.asarray(mask, dtype=bool)
+    return vis
+
+
+def _mask_plane(mask, b, h):
+    """The (Nq, Nk) plane of a (Bm, Hm, Nq, Nk) boolean mask that batch b,
+    head h reads (Bm, Hm of 1 broadcast)."""
+    if mask is None:
+        return None
+    m = np.asarray(mask, dtype=bool)
+    return m[b if m.shape[0] > 1 else 0, h if m.shape[1] > 1 else 0]
+
+
+def attention_masked_forward(q, k, v, scale=None, causal=False, window=None, key_lengths=None, mask=None):
+    """Attention under any combination of the masks of ``visibility``, with
+    query row i at position Nk - Nq + i (the alignment of
+    ``attention_decode``; i itself when Nq = Nk).  key_lengths: (B,) ints or
+    None; mask: boolean (Bm, Hm, Nq, Nk), Bm in {1, B}, Hm in {1, H}, or
+    None.  Rows that see no key: O = 0, lse = -inf.
+    Returns O (B, H, Nq, d_v) and lse (B, H, Nq)."""
+    q = np.asarray(q, dtype=np.float64)
+    k = np.asarray(k, dtype=np.float64)
+    v = np.asarray(v, dtype=np.float64)
+    B, H, Hkv, Nq, Nk, d = _check(q, k, v)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    O = np.zeros((B, H, Nq, v.shape[3]))
+    lse = np.full((B, H, Nq), -np.inf)
+    for b in range(B):
+        for h in range(H):
+            hk = gqa_kv_head(h, H, Hkv)
+            vis = visibility(Nq, Nk, causal, Nk - Nq, window,
+                             None if key_lengths is None else int(key_lengths[b]), _mask_plane(mask, b, h))
+            S = np.where(vis, scale * (q[b, h] @ k[b, hk].T), -np.inf)
+            live = vis.any(axis=1)
+            if live.any():
+                P, m, l = softmax_rows(S[live])
+                O[b, h][live] = P @ v[b, hk]
+                lse[b, h][live] = m + np.log(l)
+    return O, lse
+
+
+def attention_masked_backward(q, k, v, do, scale=None, causal=False, window=None, key_lengths=None, mask=None):
+    """Gradients of ``attention_masked_forward`` by the chain rule of
+    ``attention_backward`` (masked entries have P = 0; rows that see no key
+    contribute nothing).  Returns dQ, dK, dV in float64."""
+    q = np.asarray(q, dtype=np.float64)
+    k = np.asarray(k, dtype=np.float64)
+    v = np.asarray(v, dtype=np.float64)
+    do = np.asarray(do, dtype=np.float64)
+    B, H, Hkv, Nq, Nk, d = _check(q, k, v)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    dq, dk, dv = np.zeros_like(q), np.zeros_like(k), np.zeros_like(v)
+    for b in range(B):
+        for h in range(H):
+            hk = gqa_kv_head(h, H, Hkv)
+            vis = visibility(Nq, Nk, causal, Nk - Nq, window,
+                             None if key_lengths is None else int(key_lengths[b]), _mask_plane(mask, b, h))
+            S = np.where(vis, scale * (q[b, h] @ k[b, hk].T), -np.inf)
+            live = vis.any(axis=1)
+            P = np.zeros_like(S)
+            if live.any():
+                P[live] = softmax_rows(S[live])[0]
+            dv[b, hk] += P.T @ do[b, h]
+            dP = do[b, h] @ v[b, hk].T
+            D = (P * dP).sum(axis=1)
+            dS = P * (dP - D[:, None])
+            dq[b, h] = scale * (dS @ k[b, hk])
+            dk[b, hk] += scale * (dS.T @ q[b, h])
+    return dq, dk, dv
+
+
 def softmax_rows(S):
     """Max-subtracted softmax along the last axis ([FA] §四:
     softmax(x_i) = exp(x_i - max x) / sum_j exp(x_j - max x)).
