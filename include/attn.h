@@ -181,6 +181,71 @@ attn_status_t attn_bwd_dq_cross(const void* q, const void* k, const void* v, con
                                 void* stream);
 
 /*
+ * Masks beyond is_causal (page "SDPA backend 与 FlashAttention" §3: the
+ * boolean attn_mask of the SDPA call; "Flash Attention原理" FAQ Q11: padding
+ * and arbitrary boolean masks handled inside the kernel).  Query row i sits
+ * at position pos = Nk - Nq + i (i itself when Nq == Nk); key j takes part in
+ * row i when all of these hold:
+ *   causal (the call's flag)     j <= pos
+ *   window_left  >= 0            j >= pos - window_left
+ *   window_right >= 0            j <= pos + window_right   (a sliding window)
+ *   key_lengths != NULL          j < key_lengths[b]        (padding mask;
+ *                                values are clamped to [0, Nk])
+ *   mask != NULL                 mask[b'][h'][i][j] != 0, with b' = b (or 0
+ *                                when mask_batch == 1), h' = h (or 0 when
+ *                                mask_heads == 1)
+ * -1 leaves a window side open.  A row no key passes gets O = 0, lse = -inf
+ * and dQ = 0; keys no row sees get dK = dV = 0.
+ *   key_lengths  DEVICE int32 (B), 4-byte aligned, or NULL
+ *   mask         DEVICE bytes (mask_batch, mask_heads, Nq, Nk), dense
+ *                row-major, any alignment, or NULL
+ */
+typedef struct {
+  int window_left;
+  int window_right;
+  const int* key_lengths;
+  const unsigned char* mask;
+  int mask_batch;   /* 1 or B */
+  int mask_heads;   /* 1 or H */
+} attn_mask_t;
+
+/*
+ * Workspace bytes of attn_fwd_masked (backward = 0) or attn_bwd_masked
+ * (backward = 1): the bit-packed mask (one bit per (query, key), plus its
+ * transpose for the backward) and, for the backward, attn_bwd's row vectors.
+ * 0 when the forward needs none (no boolean mask) or the shape is invalid.
+ */
+size_t attn_masked_workspace_size(int B, int H, int Hkv, int Nq, int Nk, int d, const attn_mask_t* mask,
+                                  int backward);
+
+/*
+ * Forward and backward under the masks above; layouts as attn_fwd_cross /
+ * attn_bwd_cross (Nq query rows, Nk key rows; Nq == Nk for self-attention).
+ * Unlike attn_fwd_cross, causal with Nq > Nk is accepted (the first rows see
+ * no key).  The workspace is owned by the caller (at least
+ * attn_masked_workspace_size bytes, 16-byte aligned; NULL allowed when that
+ * size is 0).  attn_bwd_masked_stages runs a subset of the backward's
+ * stages, as attn_bwd_varlen_stages (1: prep and mask packing, 2: dK / dV,
+ * 4: dQ).
+ */
+attn_status_t attn_fwd_masked(const void* q, const void* k, const void* v, void* o, float* lse,
+                              int B, int H, int Hkv, int Nq, int Nk, int d, float scale, int causal,
+                              const attn_mask_t* mask, void* workspace, size_t workspace_bytes,
+                              void* stream);
+attn_status_t attn_bwd_masked(const void* q, const void* k, const void* v, const void* o,
+                              const float* lse, const void* dout,
+                              void* dq, void* dk, void* dv,
+                              int B, int H, int Hkv, int Nq, int Nk, int d, float scale, int causal,
+                              const attn_mask_t* mask, void* workspace, size_t workspace_bytes,
+                              void* stream);
+attn_status_t attn_bwd_masked_stages(const void* q, const void* k, const void* v, const void* o,
+                                     const float* lse, const void* dout,
+                                     void* dq, void* dk, void* dv,
+                                     int B, int H, int Hkv, int Nq, int Nk, int d, float scale, int causal,
+                                     const attn_mask_t* mask, void* workspace, size_t workspace_bytes,
+                                     unsigned stages, void* stream);
+
+/*
  * Packed variable-length batch.  Page "Flash Attention原理", FAQ Q10:
  * sequences of different lengths are packed into one batch, delimited by
  * cumulative offsets (cu_seqlens), so no padding is computed.  Sequence b

@@ -26,6 +26,8 @@ __all__ = [
     "attn_decode", "attn_decode_workspace_size", "attn_fwd_cross", "attn_bwd_cross",
     "attn_bwd_grad_cross", "attn_bwd_dq_cross", "attn_fwd_varlen", "attn_bwd_varlen",
     "attn_bwd_varlen_workspace_size", "attn_bwd_varlen_stages", "forward_varlen", "backward_varlen",
+    "AttnMask", "attn_masked_workspace_size", "attn_fwd_masked", "attn_bwd_masked", "attn_bwd_masked_stages",
+    "forward_masked", "backward_masked",
     "forward", "forward_cross", "backward", "backward_cross", "decode", "build",
 ]
 
@@ -40,6 +42,13 @@ class Status(enum.IntEnum):
     LAUNCH = 6
     TIMEOUT = 7
     CUDA = 8
+
+
+class AttnMask(ctypes.Structure):
+    """attn_mask_t of include/attn.h (device pointers as integers, 0 = none)."""
+    _fields_ = [("window_left", ctypes.c_int), ("window_right", ctypes.c_int),
+                ("key_lengths", ctypes.c_void_p), ("mask", ctypes.c_void_p),
+                ("mask_batch", ctypes.c_int), ("mask_heads", ctypes.c_int)]
 
 
 class AttnError(RuntimeError):
@@ -101,6 +110,18 @@ def load() -> ctypes.CDLL:
                                                _I, _I, _I, _I, _I, _I, _I, _I, ctypes.c_float, _I, ctypes.c_uint,
                                                _P]
         lib.attn_bwd_varlen_stages.restype = _I
+        _M = ctypes.POINTER(AttnMask)
+        lib.attn_masked_workspace_size.argtypes = [_I, _I, _I, _I, _I, _I, _M, _I]
+        lib.attn_masked_workspace_size.restype = ctypes.c_size_t
+        lib.attn_fwd_masked.argtypes = [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, ctypes.c_float, _I, _M, _P,
+                                        ctypes.c_size_t, _P]
+        lib.attn_fwd_masked.restype = _I
+        lib.attn_bwd_masked.argtypes = [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, ctypes.c_float, _I,
+                                        _M, _P, ctypes.c_size_t, _P]
+        lib.attn_bwd_masked.restype = _I
+        lib.attn_bwd_masked_stages.argtypes = [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I,
+                                               ctypes.c_float, _I, _M, _P, ctypes.c_size_t, ctypes.c_uint, _P]
+        lib.attn_bwd_masked_stages.restype = _I
         lib.attn_decode_workspace_size.argtypes = [_I, _I, _I, _I, _I, _I]
         lib.attn_decode_workspace_size.restype = ctypes.c_size_t
         lib.attn_decode.argtypes = [_P, _P, _P, _P, _P, _P, ctypes.c_size_t, _I, _I, _I, _I, _I, _I,
@@ -200,6 +221,28 @@ def attn_bwd_varlen_stages(q, k, v, o, lse, dout, dq, dk, dv, cu_q, cu_k, worksp
     return load().attn_bwd_varlen_stages(q, k, v, o, lse, dout, dq, dk, dv, cu_q, cu_k, workspace, workspace_bytes,
                                          B, H, Hkv, total_q, total_k, max_q, max_k, d, scale, causal, stages,
                                          stream)
+
+
+def attn_masked_workspace_size(B, H, Hkv, Nq, Nk, d, mask: AttnMask, backward) -> int:
+    return load().attn_masked_workspace_size(B, H, Hkv, Nq, Nk, d, ctypes.byref(mask), int(backward))
+
+
+def attn_fwd_masked(q, k, v, o, lse, B, H, Hkv, Nq, Nk, d, scale, causal, mask: AttnMask, workspace,
+                    workspace_bytes, stream) -> int:
+    return load().attn_fwd_masked(q, k, v, o, lse, B, H, Hkv, Nq, Nk, d, scale, causal, ctypes.byref(mask),
+                                  workspace, workspace_bytes, stream)
+
+
+def attn_bwd_masked(q, k, v, o, lse, dout, dq, dk, dv, B, H, Hkv, Nq, Nk, d, scale, causal, mask: AttnMask,
+                    workspace, workspace_bytes, stream) -> int:
+    return load().attn_bwd_masked(q, k, v, o, lse, dout, dq, dk, dv, B, H, Hkv, Nq, Nk, d, scale, causal,
+                                  ctypes.byref(mask), workspace, workspace_bytes, stream)
+
+
+def attn_bwd_masked_stages(q, k, v, o, lse, dout, dq, dk, dv, B, H, Hkv, Nq, Nk, d, scale, causal, mask: AttnMask,
+                           workspace, workspace_bytes, stages, stream) -> int:
+    return load().attn_bwd_masked_stages(q, k, v, o, lse, dout, dq, dk, dv, B, H, Hkv, Nq, Nk, d, scale, causal,
+                                         ctypes.byref(mask), workspace, workspace_bytes, stages, stream)
 
 
 def attn_decode_workspace_size(B, H, Hkv, Nq, Nk, d) -> int:
@@ -432,4 +475,75 @@ def backward_varlen(q, k, v, o, lse, dout, cu_seqlens_q, cu_seqlens_k, max_seqle
                            cu_seqlens_k.data_ptr(), workspace.data_ptr(),
                            workspace.numel() * workspace.element_size(), B, H, Hkv, total_q, total_k, mq, mk, d,
                            scale, causal, _stream_ptr(q)), "attn_bwd_varlen")
+    return dq, dk, dv
+
+
+def make_mask(window=None, key_lengths=None, mask=None, B=1, H=1) -> AttnMask:
+    """AttnMask from Python values: window (left, right) with -1 for an open
+    side, key_lengths an int32 CUDA vector (B,), mask a bool / uint8 CUDA
+    tensor (1 or B, 1 or H, Nq, Nk).  The tensors must stay alive while the
+    calls that use the AttnMask run."""
+    import torch
+    wl, wr = window if window is not None else (-1, -1)
+    m = AttnMask(int(wl), int(wr), 0, 0, 1, 1)
+    if key_lengths is not None:
+        if key_lengths.dtype != torch.int32 or not key_lengths.is_cuda or not key_lengths.is_contiguous():
+            raise ValueError("key_lengths must be a contiguous int32 CUDA vector")
+        m.key_lengths = key_lengths.data_ptr()
+    if mask is not None:
+        if mask.dim() != 4 or mask.dtype not in (torch.bool, torch.uint8) or not mask.is_cuda:
+            raise ValueError("mask must be a 4-D bool / uint8 CUDA tensor")
+        if not mask.is_contiguous():
+            raise ValueError("mask must be contiguous")
+        m.mask = mask.data_ptr()
+        m.mask_batch, m.mask_heads = int(mask.shape[0]), int(mask.shape[1])
+    return m
+
+
+def _masked_shapes(q, k, v):
+    import torch
+    if q.dim() != 4 or k.dim() != 4 or v.dim() != 4:
+        raise ValueError("q, k, v must be 4-D")
+    B, H, Nq, d = q.shape
+    Hkv, Nk = k.shape[1], k.shape[2]
+    if tuple(k.shape) != (B, Hkv, Nk, d) or tuple(v.shape) != (B, Hkv, Nk, d):
+        raise ValueError("k and v must be (B, Hkv, Nk, d) with q's B and d")
+    for t in (q, k, v):
+        if not t.is_contiguous() or t.dtype != torch.bfloat16:
+            raise ValueError("inputs must be contiguous bf16")
+    return B, H, Hkv, Nq, Nk, d
+
+
+def forward_masked(q, k, v, scale: float | None = None, causal: bool = False, window=None, key_lengths=None,
+                   mask=None):
+    """O, lse under a sliding window / key lengths / boolean mask (see
+    include/attn.h, attn_mask_t); q (B, H, Nq, d), k, v (B, Hkv, Nk, d)."""
+    import torch
+    B, H, Hkv, Nq, Nk, d = _masked_shapes(q, k, v)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    m = make_mask(window, key_lengths, mask, B, H)
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device)
+    wsb = attn_masked_workspace_size(B, H, Hkv, Nq, Nk, d, m, 0)
+    ws = torch.empty(max(wsb, 16), dtype=torch.uint8, device=q.device)
+    _check(attn_fwd_masked(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), B, H, Hkv, Nq, Nk,
+                           d, scale, causal, m, ws.data_ptr(), ws.numel(), _stream_ptr(q)), "attn_fwd_masked")
+    return o, lse
+
+
+def backward_masked(q, k, v, o, lse, dout, scale: float | None = None, causal: bool = False, window=None,
+                    key_lengths=None, mask=None):
+    """dQ, dK, dV of forward_masked with the same masks."""
+    import torch
+    B, H, Hkv, Nq, Nk, d = _masked_shapes(q, k, v)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    m = make_mask(window, key_lengths, mask, B, H)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    wsb = attn_masked_workspace_size(B, H, Hkv, Nq, Nk, d, m, 1)
+    ws = torch.empty(max(wsb, 16), dtype=torch.uint8, device=q.device)
+    _check(attn_bwd_masked(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), dout.data_ptr(),
+                           dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, Hkv, Nq, Nk, d, scale, causal, m,
+                           ws.data_ptr(), ws.numel(), _stream_ptr(q)), "attn_bwd_masked")
     return dq, dk, dv

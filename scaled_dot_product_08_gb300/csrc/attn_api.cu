@@ -411,6 +411,8 @@ static attn_status_t bwd_grad_x(const void* q, const void* k, const void* v, con
     return ATTN_ERR_CUDA;
   sdpa::BwdParams p;
   bwd_params(&p, workspace, B, H, Hkv, Nq, Nk, d, scale, causal, di);
+  p.dk = static_cast<uint16_t*>(dk);
+  p.dv = static_cast<uint16_t*>(dv);
   cudaError_t e = sdpa::launch_bwd_grad(d, causal != 0, tq, tk, tv, tdo, tdk, tdv, p,
                                         static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;
@@ -432,6 +434,7 @@ static attn_status_t bwd_dq_x(const void* q, const void* k, const void* v, const
     return ATTN_ERR_CUDA;
   sdpa::BwdParams p;
   bwd_params(&p, workspace, B, H, Hkv, Nq, Nk, d, scale, causal, di);
+  p.dq = static_cast<uint16_t*>(dq);
   cudaError_t e = sdpa::launch_bwd_dq(d, causal != 0, tq, tk, tv, tdo, tdq, p, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;
 }
@@ -593,6 +596,182 @@ attn_status_t attn_bwd_varlen_stages(const void* q, const void* k, const void* v
   if (stages == 0 || (stages & ~7u) != 0) return ATTN_ERR_INVALID_ARG;
   return varlen_bwd_run(q, k, v, o, lse, dout, dq, dk, dv, cu_seqlens_q, cu_seqlens_k, workspace, workspace_bytes,
                         B, H, Hkv, total_q, total_k, max_seqlen_q, max_seqlen_k, d, scale, causal, stream, stages);
+}
+
+// ------------------------------------------------------------------ masks
+// Bit-array geometry of a mask (see MaskArgs): words per query row and per
+// key row, planes, and the byte sizes of the two arrays.
+struct MaskGeom {
+  int words, words_t, planes;
+  size_t bits_bytes, bits_t_bytes;
+};
+
+static MaskGeom mask_geom(int Nq, int Nk, const attn_mask_t* m) {
+  MaskGeom g{((Nk + 127) / 128) * 4, ((Nq + 127) / 128) * 4, 0, 0, 0};
+  if (m != nullptr && m->mask != nullptr) {
+    g.planes = m->mask_batch * m->mask_heads;
+    g.bits_bytes = (size_t)g.planes * Nq * g.words * 4;
+    g.bits_t_bytes = (size_t)g.planes * Nk * g.words_t * 4;
+  }
+  return g;
+}
+
+static attn_status_t check_mask(int B, int H, int Nq, int Nk, const attn_mask_t* m) {
+  if (m == nullptr) return ATTN_ERR_INVALID_ARG;
+  if (m->window_left < -1 || m->window_right < -1) return ATTN_ERR_INVALID_ARG;
+  if (m->key_lengths != nullptr) {
+    if (reinterpret_cast<uintptr_t>(m->key_lengths) & 3u) return ATTN_ERR_MISALIGNED;
+  }
+  if (m->mask != nullptr) {
+    if ((m->mask_batch != 1 && m->mask_batch != B) || (m->mask_heads != 1 && m->mask_heads != H))
+      return ATTN_ERR_INVALID_ARG;
+    const MaskGeom g = mask_geom(Nq, Nk, m);
+    // The kernels index the bit arrays with 32-bit word indices.
+    if ((long long)g.planes * Nq * g.words >= 0xffffffffll || (long long)g.planes * Nk * g.words_t >= 0xffffffffll)
+      return ATTN_ERR_UNSUPPORTED_SHAPE;
+  }
+  return ATTN_OK;
+}
+
+static attn_status_t check_mask_ptrs(const attn_mask_t* m) {
+  for (const void* p : {static_cast<const void*>(m->key_lengths), static_cast<const void*>(m->mask)}) {
+    if (p == nullptr) continue;
+    cudaPointerAttributes at;
+    if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+      cudaGetLastError();
+      return ATTN_ERR_INVALID_ARG;
+    }
+    if (at.type != cudaMemoryTypeDevice && at.type != cudaMemoryTypeManaged) return ATTN_ERR_INVALID_ARG;
+  }
+  return ATTN_OK;
+}
+
+// Kernel mask arguments; the bit arrays (when there is a mask) at `bits` and
+// `bits_t` inside the caller's workspace.  Causal enters as wr = 0.
+static sdpa::MaskArgs mask_args(const attn_mask_t* m, int Nq, int Nk, int causal, uint32_t* bits, uint32_t* bits_t) {
+  const MaskGeom g = mask_geom(Nq, Nk, m);
+  sdpa::MaskArgs a;
+  a.wl = m->window_left;
+  a.wr = causal ? 0 : m->window_right;
+  a.key_len = m->key_lengths;
+  a.bits = m->mask != nullptr ? bits : nullptr;
+  a.bits_t = m->mask != nullptr ? bits_t : nullptr;
+  a.words = g.words;
+  a.words_t = g.words_t;
+  a.mask_b = m->mask != nullptr ? m->mask_batch : 1;
+  a.mask_h = m->mask != nullptr ? m->mask_heads : 1;
+  return a;
+}
+
+size_t attn_masked_workspace_size(int B, int H, int Hkv, int Nq, int Nk, int d, const attn_mask_t* mask,
+                                  int backward) {
+  if (check_shape(B, H, Hkv, Nq, d) != ATTN_OK || check_shape(B, H, Hkv, Nk, d) != ATTN_OK ||
+      check_mask(B, H, Nq, Nk, mask) != ATTN_OK)
+    return 0;
+  const MaskGeom g = mask_geom(Nq, Nk, mask);
+  if (!backward) return g.bits_bytes;
+  return attn_bwd_workspace_size(B, H, Hkv, Nq, d) + g.bits_bytes + g.bits_t_bytes;
+}
+
+attn_status_t attn_fwd_masked(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                              int Hkv, int Nq, int Nk, int d, float scale, int causal, const attn_mask_t* mask,
+                              void* workspace, size_t workspace_bytes, void* stream) {
+  ATTN_TRY(check_shape(B, H, Hkv, Nq, d));
+  ATTN_TRY(check_shape(B, H, Hkv, Nk, d));
+  ATTN_TRY(check_scale_flag(scale, causal));
+  ATTN_TRY(check_mask(B, H, Nq, Nk, mask));
+  const MaskGeom g = mask_geom(Nq, Nk, mask);
+  if (g.bits_bytes > 0 && (workspace == nullptr || workspace_bytes < g.bits_bytes)) return ATTN_ERR_WORKSPACE;
+  ATTN_TRY(check_ptrs({q, k, v, o, lse}));
+  if (g.bits_bytes > 0) ATTN_TRY(check_ptrs({workspace}));
+  ATTN_TRY(check_mask_ptrs(mask));
+  DeviceInfo* di = nullptr;
+  ATTN_TRY(current_device(&di));
+  CUtensorMap tq, tk, tv, to;
+  if (!make_map_bf16(&tq, q, d, Nq, (long long)B * H) || !make_map_bf16(&tk, k, d, Nk, (long long)B * Hkv) ||
+      !make_map_bf16(&tv, v, d, Nk, (long long)B * Hkv) || !make_map_bf16(&to, o, d, Nq, (long long)B * H))
+    return ATTN_ERR_CUDA;
+  sdpa::FwdParams p;
+  memset(&p, 0, sizeof(p));
+  p.lse = lse;
+  p.B = B;
+  p.H = H;
+  p.Hkv = Hkv;
+  p.G = H / Hkv;
+  p.Nq = Nq;
+  p.Nk = Nk;
+  p.n_mtiles = (Nq + 255) / 256;
+  p.nkv = (Nk + 127) / 128;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.status = di->status;
+  p.limit_ns = wait_limit_ns();
+  p.info = di->info;
+  uint32_t* bits = static_cast<uint32_t*>(workspace);
+  p.mk = mask_args(mask, Nq, Nk, causal, bits, nullptr);
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (mask->mask != nullptr &&
+      sdpa::launch_mask_pack(static_cast<const uint8_t*>(mask->mask), mask->mask_batch, mask->mask_heads, Nq, Nk,
+                             bits, g.words, nullptr, 0, st) != cudaSuccess)
+    return ATTN_ERR_LAUNCH;
+  return sdpa::launch_fwd(d, false, tq, tk, tv, to, p, st, true) == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;
+}
+
+attn_status_t attn_bwd_masked_stages(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                                     const void* dout, void* dq, void* dk, void* dv, int B, int H, int Hkv, int Nq,
+                                     int Nk, int d, float scale, int causal, const attn_mask_t* mask, void* workspace,
+                                     size_t workspace_bytes, unsigned stages, void* stream) {
+  if (stages == 0 || (stages & ~7u) != 0) return ATTN_ERR_INVALID_ARG;
+  ATTN_TRY(check_shape(B, H, Hkv, Nq, d));
+  ATTN_TRY(check_shape(B, H, Hkv, Nk, d));
+  ATTN_TRY(check_scale_flag(scale, causal));
+  ATTN_TRY(check_mask(B, H, Nq, Nk, mask));
+  const size_t need = attn_masked_workspace_size(B, H, Hkv, Nq, Nk, d, mask, 1);
+  if (workspace == nullptr || workspace_bytes < need) return ATTN_ERR_WORKSPACE;
+  ATTN_TRY(check_ptrs({q, k, v, o, lse, dout, dq, dk, dv, workspace}));
+  ATTN_TRY(check_mask_ptrs(mask));
+  DeviceInfo* di = nullptr;
+  ATTN_TRY(current_device(&di));
+  CUtensorMap tq, tk, tv, tdo, tdq, tdk, tdv;
+  if (!make_map_bf16(&tq, q, d, Nq, (long long)B * H) || !make_map_bf16(&tk, k, d, Nk, (long long)B * Hkv) ||
+      !make_map_bf16(&tv, v, d, Nk, (long long)B * Hkv) || !make_map_bf16(&tdo, dout, d, Nq, (long long)B * H) ||
+      !make_map_bf16(&tdq, dq, d, Nq, (long long)B * H) || !make_map_bf16(&tdk, dk, d, Nk, (long long)B * Hkv) ||
+      !make_map_bf16(&tdv, dv, d, Nk, (long long)B * Hkv))
+    return ATTN_ERR_CUDA;
+  // Workspace: [row vectors | row bits | transposed bits].
+  const MaskGeom g = mask_geom(Nq, Nk, mask);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  uint32_t* bits = reinterpret_cast<uint32_t*>(ws + attn_bwd_workspace_size(B, H, Hkv, Nq, d));
+  uint32_t* bits_t = reinterpret_cast<uint32_t*>(reinterpret_cast<uint8_t*>(bits) + g.bits_bytes);
+  sdpa::BwdParams p;
+  bwd_params(&p, workspace, B, H, Hkv, Nq, Nk, d, scale, causal, di);
+  p.o = static_cast<const uint16_t*>(o);
+  p.dout = static_cast<const uint16_t*>(dout);
+  p.lse = lse;
+  p.mk = mask_args(mask, Nq, Nk, causal, bits, bits_t);
+  p.dq = static_cast<uint16_t*>(dq);  // outputs whose tiles nothing attends to are zeroed in place
+  p.dk = static_cast<uint16_t*>(dk);
+  p.dv = static_cast<uint16_t*>(dv);
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (stages & 1u) {
+    if (sdpa::launch_bwd_prep(p, st) != cudaSuccess) return ATTN_ERR_LAUNCH;
+    if (mask->mask != nullptr &&
+        sdpa::launch_mask_pack(static_cast<const uint8_t*>(mask->mask), mask->mask_batch, mask->mask_heads, Nq, Nk,
+                               bits, g.words, bits_t, g.words_t, st) != cudaSuccess)
+      return ATTN_ERR_LAUNCH;
+  }
+  if ((stages & 2u) && sdpa::launch_bwd_grad(d, false, tq, tk, tv, tdo, tdk, tdv, p, st, true) != cudaSuccess)
+    return ATTN_ERR_LAUNCH;
+  if ((stages & 4u) && sdpa::launch_bwd_dq(d, false, tq, tk, tv, tdo, tdq, p, st, true) != cudaSuccess)
+    return ATTN_ERR_LAUNCH;
+  return ATTN_OK;
+}
+
+attn_status_t attn_bwd_masked(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                              const void* dout, void* dq, void* dk, void* dv, int B, int H, int Hkv, int Nq, int Nk,
+                              int d, float scale, int causal, const attn_mask_t* mask, void* workspace,
+                              size_t workspace_bytes, void* stream) {
+  return attn_bwd_masked_stages(q, k, v, o, lse, dout, dq, dk, dv, B, H, Hkv, Nq, Nk, d, scale, causal, mask,
+                                workspace, workspace_bytes, 7u, stream);
 }
 
 // Key chunks of the decode kernel, a pure function of the shape (so the

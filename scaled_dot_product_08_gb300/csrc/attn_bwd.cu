@@ -73,8 +73,11 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const BwdParams p) {
     for (int s = 16; s > 0; s >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, s);
   }
   if (lane == 0) {
+    // A row that saw no key (lse = -inf, masked calls only) also gets
+    // -lse2 = -inf, so P = 0 on it.
+    const float l = (i < p.N) ? p.lse[(size_t)bh * p.N + i] : -INFINITY;
     p.dvec[row] = (i < p.N) ? -dot : 0.f;
-    p.lse2[row] = (i < p.N) ? -p.lse[(size_t)bh * p.N + i] * 1.4426950408889634f : -INFINITY;
+    p.lse2[row] = (l == -INFINITY) ? -INFINITY : -l * 1.4426950408889634f;
   }
 }
 
@@ -134,11 +137,12 @@ struct BwdTraits {
   static constexpr int NBAR = 16;
   // K, V, Q[2], dO[2], then vectors, barriers, misc
   static constexpr int TILES_BYTES = 6 * TILE_BYTES;
-  static constexpr int SMEM = TILES_BYTES + 2 * VEC_BYTES + NBAR * 8 + 32;
+  static constexpr int SMEM = TILES_BYTES + 2 * VEC_BYTES + NBAR * 8 + 48;
   static constexpr int THREADS = 384;
 };
 
-template <int D, bool CAUSAL>
+// MASKED: the instance that applies p.mk (causal enters as wr = 0).
+template <int D, bool CAUSAL, bool MASKED>
 __global__ void __launch_bounds__(384, 1)
     bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
@@ -198,13 +202,28 @@ __global__ void __launch_bounds__(384, 1)
     if (128 * j >= sq.nk) return;  // past the end of a shorter packed sequence
     // Causal: the first query tile with a row at position >= 128 j, query
     // row i at position koff + i, koff = Nk - Nq.
-    i0 = CAUSAL ? max(0, (j * 128 - (sq.nk - sq.nq)) / 128) : 0;
-    ni = (sq.nq + 127) / 128 - i0;
+    const int koff = sq.nk - sq.nq;
+    int nke = sq.nk;  // keys past this are invisible
+    if (MASKED) {
+      // The query tiles whose rows reach key tile j: positions from
+      // 128 j - wr (wr >= 0) to 128 j + 127 + wl (wl >= 0).
+      if (p.mk.key_len != nullptr) nke = max(0, min(nke, p.mk.key_len[b]));
+      const int nqt = (sq.nq + 127) / 128;
+      i0 = p.mk.wr >= 0 ? max(0, floor_div128(128 * j - p.mk.wr - koff)) : 0;
+      int iend = p.mk.wl >= 0 ? min(nqt, floor_div128(128 * j + 127 + p.mk.wl - koff) + 1) : nqt;
+      if (128 * j >= nke) iend = i0;  // the whole tile is past the key length
+      ni = iend - i0;
+    } else {
+      i0 = CAUSAL ? max(0, (j * 128 - koff) / 128) : 0;
+      ni = (sq.nq + 127) / 128 - i0;
+    }
     if (ni <= 0) {
-      // No query attends to these keys (a packed sequence without queries):
-      // dK = dV = 0.
-      const uint32_t rs = (uint32_t)(p.Hkv * D);
-      const long long off = ((long long)sq.k0 + 128 * j) * rs + (long long)hk * D;
+      // No query attends to these keys (a packed sequence without queries,
+      // or keys every mask hides): dK = dV = 0.
+      // Packed: (total, Hkv, d) rows; dense: the (b, hk) plane of (B, Hkv, Nk, d).
+      const uint32_t rs = varlen ? (uint32_t)(p.Hkv * D) : (uint32_t)D;
+      const long long off = varlen ? ((long long)sq.k0 + 128 * j) * rs + (long long)hk * D
+                                   : ((long long)bhk * p.Nk + 128 * j) * D;
       zero_rows2_bf16<D>(p.dk + off, p.dv + off, rs, min(128, sq.nk - 128 * j));
       return;
     }
@@ -215,6 +234,8 @@ __global__ void __launch_bounds__(384, 1)
       seq_s[3] = sq.nk;
       seq_s[4] = kplane;
       seq_s[5] = hk;
+      seq_s[6] = nke;
+      if (MASKED) seq_s[7] = (p.mk.mask_b > 1 ? b : 0) * p.mk.mask_h;  // mask plane base of this batch element
     }
   }
   const int total = p.G * ni;                 // steps: (head in group) x (query tile)
@@ -263,9 +284,11 @@ __global__ void __launch_bounds__(384, 1)
     // q < qmin0 - 128 i: every column for key rows past Nk (the last tile's
     // padding), and for causal rows the queries at positions koff + 128 i +
     // 64 X + q below the key.
-    const int qmin0 = (j * 128 + r >= seq_s[3]) ? (1 << 30)
-                      : CAUSAL                  ? 128 * j + r - (seq_s[3] - seq_s[1]) - 64 * X
-                                                : -(1 << 30);
+    // (The masked instance computes its bounds per step, below.)
+    const int qmin0 = MASKED                    ? 0
+                      : (j * 128 + r >= seq_s[3]) ? (1 << 30)
+                      : CAUSAL                    ? 128 * j + r - (seq_s[3] - seq_s[1]) - 64 * X
+                                                  : -(1 << 30);
     const float c = p.scale_log2;
     const float2 c2 = make_float2(c, c);
     bool ok = true;
@@ -304,7 +327,28 @@ __global__ void __launch_bounds__(384, 1)
         x[4 * q4 + 2] = ex2(t1.x);
         x[4 * q4 + 3] = ex2(t1.y);
       }
-      {
+      if (MASKED) {
+        // Masked instance: query column q is also hidden when q > qmax (the
+        // window's left edge seen from the key: positions above key + wl),
+        // when the key is past the key length, and when its bit is clear.
+        // Recomputed per step from shared memory and the indices rather than
+        // held in registers across the loop.
+        const int kk = 128 * (int)(blockIdx.x % p.nkv) + r, koff = seq_s[3] - seq_s[1];
+        const int qmin = (kk >= seq_s[6] ? (1 << 30) : p.mk.wr >= 0 ? kk - p.mk.wr - koff - 64 * X : -(1 << 30)) - 128 * i;
+        const int qmax = (p.mk.wl >= 0 ? kk + p.mk.wl - koff - 64 * X : (1 << 30)) - 128 * i;
+        uint2 bt = make_uint2(~0u, ~0u);
+        if (p.mk.bits_t != nullptr && kk < p.Nk) {
+          const int h = seq_s[5] * p.G + it / ni;  // query head of this step
+          const uint32_t plane = (uint32_t)seq_s[7] + (p.mk.mask_h > 1 ? (uint32_t)h : 0u);
+          const uint32_t w = (plane * (uint32_t)p.Nk + (uint32_t)kk) * (uint32_t)p.mk.words_t + 2u * X + 4u * i;
+          bt = *reinterpret_cast<const uint2*>(p.mk.bits_t + w);
+        }
+        if (__any_sync(0xffffffffu, qmin > 0 || qmax < 63 || (bt.x & bt.y) != ~0u)) {
+#pragma unroll
+          for (int q = 0; q < 64; ++q)
+            if (q < qmin || q > qmax || !((((q < 32) ? bt.x : bt.y) >> (q & 31)) & 1u)) x[q] = 0.f;
+        }
+      } else {
         const int qmin = qmin0 - 128 * i;
         if (__any_sync(0xffffffffu, qmin > 0)) {
 #pragma unroll
@@ -573,11 +617,11 @@ size_t bwd_smem_bytes(int d) {
   }
 }
 
-template <int D, bool C>
+template <int D, bool C, bool M = false>
 static cudaError_t launch_main_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                                  const CUtensorMap& tdo, const CUtensorMap& tdk, const CUtensorMap& tdv,
                                  const BwdParams& p, cudaStream_t stream) {
-  auto kern = bwd_main_kernel<D, C>;
+  auto kern = bwd_main_kernel<D, C, M>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, BwdTraits<D>::SMEM);
   if (e != cudaSuccess) return e;
   const unsigned grid = (unsigned)p.nkv * (unsigned)(p.B * p.Hkv);
@@ -597,7 +641,15 @@ cudaError_t launch_bwd_prep(const BwdParams& p, cudaStream_t stream) {
 
 cudaError_t launch_bwd_grad(int d, bool causal, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                             const CUtensorMap& tdo, const CUtensorMap& tdk, const CUtensorMap& tdv,
-                            const BwdParams& p, cudaStream_t stream) {
+                            const BwdParams& p, cudaStream_t stream, bool masked) {
+  if (masked) {
+    switch (d) {
+      case 64: return launch_main_t<64, false, true>(tq, tk, tv, tdo, tdk, tdv, p, stream);
+      case 96: return launch_main_t<96, false, true>(tq, tk, tv, tdo, tdk, tdv, p, stream);
+      case 128: return launch_main_t<128, false, true>(tq, tk, tv, tdo, tdk, tdv, p, stream);
+      default: return cudaErrorInvalidValue;
+    }
+  }
   switch (d) {
     case 64: return causal ? launch_main_t<64, true>(tq, tk, tv, tdo, tdk, tdv, p, stream)
                            : launch_main_t<64, false>(tq, tk, tv, tdo, tdk, tdv, p, stream);

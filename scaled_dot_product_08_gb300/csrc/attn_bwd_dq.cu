@@ -35,11 +35,12 @@ struct DqTraits {
   static constexpr int KSTEPS = D / 16;
   static constexpr int KS = 3, VS = 2;                 // K and V ring slots
   static constexpr int NBAR = 18;
-  static constexpr int SMEM = 1024 + (2 + KS + VS) * TILE_BYTES + NBAR * 8 + 32;
+  static constexpr int SMEM = 1024 + (2 + KS + VS) * TILE_BYTES + NBAR * 8 + 48;
   static constexpr int THREADS = 384;
 };
 
-template <int D, bool CAUSAL>
+// MASKED: the instance that applies p.mk (causal enters as wr = 0).
+template <int D, bool CAUSAL, bool MASKED>
 __global__ void __launch_bounds__(384, 1)
     bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
@@ -70,8 +71,9 @@ __global__ void __launch_bounds__(384, 1)
   uint8_t* const misc = gbase + (sBar - base) + 8 * T::NBAR;
   uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(misc);
   volatile int* const abort_flag = reinterpret_cast<volatile int*>(misc + 4);
-  // This CTA's sequence {q0, nq, k0, nk}, read back where needed rather than
-  // held in registers across the main loops.
+  // This CTA's sequence {q0, nq, k0, nk}, first key tile, visible key count
+  // and mask plane, read back where needed rather than held in registers
+  // across the main loops.
   volatile int* const seq_s = reinterpret_cast<volatile int*>(misc + 8);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -95,12 +97,26 @@ __global__ void __launch_bounds__(384, 1)
     if (128 * i >= sq.nq) return;  // past the end of a shorter packed sequence
     // Causal: up to the tile holding the last row's last visible key,
     // koff + 128 i + 127 (query row r at position koff + r, koff = Nk - Nq).
-    const int nkv = (sq.nk + 127) / 128;
-    n = CAUSAL ? min(nkv, (sq.nk - sq.nq + i * 128 + 127) / 128 + 1) : nkv;
+    const int nkv = (sq.nk + 127) / 128, koff = sq.nk - sq.nq;
+    int jlo = 0, nke = sq.nk;
+    if (MASKED) {
+      // Key tiles from the first row's window start to the last row's
+      // last visible key.
+      if (p.mk.key_len != nullptr) nke = max(0, min(nke, p.mk.key_len[b]));
+      int hi = nke;
+      if (p.mk.wr >= 0) hi = min(hi, koff + 128 * i + 127 + p.mk.wr + 1);
+      if (p.mk.wl >= 0) jlo = max(0, floor_div128(koff + 128 * i - p.mk.wl));
+      n = min(nkv, (max(hi, 0) + 127) / 128) - jlo;
+    } else {
+      n = CAUSAL ? min(nkv, (koff + i * 128 + 127) / 128 + 1) : nkv;
+    }
     if (n <= 0) {
-      // No row of the tile sees a key (packed batches only): dQ = 0.
-      const uint32_t rs = (uint32_t)(p.H * D);
-      zero_rows_bf16<D>(p.dq + ((long long)sq.q0 + 128 * i) * rs + (long long)h * D, rs, min(128, sq.nq - 128 * i));
+      // No row of the tile sees a key (packed batches, masks): dQ = 0.
+      // Packed: (total, H, d) rows; dense: the (b, h) plane of (B, H, Nq, d).
+      const uint32_t rs = varlen ? (uint32_t)(p.H * D) : (uint32_t)D;
+      uint16_t* dst = varlen ? p.dq + ((long long)sq.q0 + 128 * i) * rs + (long long)h * D
+                             : p.dq + ((long long)bh * p.N + 128 * i) * D;
+      zero_rows_bf16<D>(dst, rs, min(128, sq.nq - 128 * i));
       return;
     }
     if (threadIdx.x == 0) {
@@ -108,6 +124,9 @@ __global__ void __launch_bounds__(384, 1)
       seq_s[1] = sq.nq;
       seq_s[2] = sq.k0;
       seq_s[3] = sq.nk;
+      seq_s[4] = jlo;
+      seq_s[5] = nke;
+      if (MASKED) seq_s[6] = mask_plane(p.mk, b, h);
     }
   }
 
@@ -155,12 +174,30 @@ __global__ void __launch_bounds__(384, 1)
     const float nD = p.dvec[vrow];   // -D
     const float2 c2 = make_float2(p.scale_log2, p.scale_log2);
     const float2 l22 = make_float2(l2, l2), nD2 = make_float2(nD, nD);
-    // Key columns at or past lim0 - 128 j of key tile j are invisible to row
-    // r: keys past Nk, and for causal rows keys past position koff + 128 i + r.
-    const int lim0 = (CAUSAL ? min(seq_s[3], seq_s[3] - seq_s[1] + 128 * i + r + 1) : seq_s[3]) - 64 * X;
+    // Key columns at or past lim0 - 128 j of the j-th visited key tile are
+    // invisible to row r: keys past Nk, and for causal rows keys past
+    // position koff + 128 i + r.  Masked instance: the key length and the
+    // window's right edge bound lim0; columns below lom0 - 128 j (the
+    // window's left edge) and those whose bit is clear are hidden too.
+    int lim0, lom0 = 0;
+    uint32_t rowbits = 0xffffffffu;  // word index of this row's bits (all ones: none)
+    if (MASKED) {
+      const int pos = seq_s[3] - seq_s[1] + 128 * i + r, jlo = seq_s[4];
+      int hi = seq_s[5];
+      if (p.mk.wr >= 0) hi = min(hi, pos + p.mk.wr + 1);
+      lim0 = hi - 128 * jlo - 64 * X;
+      lom0 = (p.mk.wl >= 0 ? pos - p.mk.wl : -(1 << 30)) - 128 * jlo - 64 * X;
+      if (p.mk.bits != nullptr && 128 * i + r < p.N)
+        rowbits = ((uint32_t)seq_s[6] * (uint32_t)p.N + (uint32_t)(128 * i + r)) * (uint32_t)p.mk.words +
+                  4u * jlo + 2u * X;
+    } else {
+      lim0 = (CAUSAL ? min(seq_s[3], seq_s[3] - seq_s[1] + 128 * i + r + 1) : seq_s[3]) - 64 * X;
+    }
     bool ok = true;
     for (int j = 0; j < n; ++j) {
       const uint32_t tS = tmem + (j & 1) * 128 + 64 * X + lane_off;
+      uint2 bt = make_uint2(~0u, ~0u);
+      if (MASKED && rowbits != 0xffffffffu) bt = *reinterpret_cast<const uint2*>(p.mk.bits + rowbits + 4u * j);
       ok = __all_sync(0xffffffffu, wait_bounded(wc, bS + 8u * (j & 1), (j >> 1) & 1, wait_site(0x81, j)));
       if (!ok) break;
       tc_fence_after();
@@ -186,7 +223,14 @@ __global__ void __launch_bounds__(384, 1)
         x[2 * e] = ex2(t.x);
         x[2 * e + 1] = ex2(t.y);
       }
-      {
+      if (MASKED) {
+        const int lim = lim0 - 128 * j, lom = lom0 - 128 * j;
+        if (__any_sync(0xffffffffu, lim < 64 || lom > 0 || (bt.x & bt.y) != ~0u)) {
+#pragma unroll
+          for (int k = 0; k < 64; ++k)
+            if (k >= lim || k < lom || !((((k < 32) ? bt.x : bt.y) >> (k & 31)) & 1u)) x[k] = 0.f;
+        }
+      } else {
         const int lim = lim0 - 128 * j;
         if (__any_sync(0xffffffffu, lim < 64)) {
 #pragma unroll
@@ -274,7 +318,7 @@ __global__ void __launch_bounds__(384, 1)
     if (warp == 8) {
       // ------------------------------------------------------------ producer
       if (lane == 0) {
-        const int q0 = seq_s[0], k0 = seq_s[2];
+        const int q0 = seq_s[0], k0 = seq_s[2] + 128 * seq_s[4];  // from the first visited key tile
         tma_prefetch_desc(&tmK);
         tma_prefetch_desc(&tmV);
         mbar_expect_tx(bQ, 2 * T::TILE_BYTES);
@@ -409,11 +453,11 @@ size_t bwd_dq_smem_bytes(int d) {
   }
 }
 
-template <int D, bool C>
+template <int D, bool C, bool M = false>
 static cudaError_t launch_dq_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                                const CUtensorMap& tdo, const CUtensorMap& tdq, const BwdParams& p,
                                cudaStream_t stream) {
-  auto kern = bwd_dq_kernel<D, C>;
+  auto kern = bwd_dq_kernel<D, C, M>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, DqTraits<D>::SMEM);
   if (e != cudaSuccess) return e;
   const unsigned grid = (unsigned)p.nq * (unsigned)(p.B * p.H);
@@ -422,7 +466,16 @@ static cudaError_t launch_dq_t(const CUtensorMap& tq, const CUtensorMap& tk, con
 }
 
 cudaError_t launch_bwd_dq(int d, bool causal, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                          const CUtensorMap& tdo, const CUtensorMap& tdq, const BwdParams& p, cudaStream_t stream) {
+                          const CUtensorMap& tdo, const CUtensorMap& tdq, const BwdParams& p, cudaStream_t stream,
+                          bool masked) {
+  if (masked) {
+    switch (d) {
+      case 64: return launch_dq_t<64, false, true>(tq, tk, tv, tdo, tdq, p, stream);
+      case 96: return launch_dq_t<96, false, true>(tq, tk, tv, tdo, tdq, p, stream);
+      case 128: return launch_dq_t<128, false, true>(tq, tk, tv, tdo, tdq, p, stream);
+      default: return cudaErrorInvalidValue;
+    }
+  }
   switch (d) {
     case 64: return causal ? launch_dq_t<64, true>(tq, tk, tv, tdo, tdq, p, stream)
                            : launch_dq_t<64, false>(tq, tk, tv, tdo, tdq, p, stream);

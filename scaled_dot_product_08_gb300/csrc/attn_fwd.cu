@@ -44,11 +44,13 @@ struct FwdTraits {
   static constexpr int NSTAGE = (D == 64) ? 8 : 5;   // K/V ring depth
   static constexpr int KSTEPS = D / 16;              // K=16 steps of Q K^T
   static constexpr int NBAR = 2 + 2 * NSTAGE + 2 + 4 + 2 + 1;
-  static constexpr int SMEM = 1024 + (2 + NSTAGE) * TILE_BYTES + NBAR * 8 + 32;
+  static constexpr int SMEM = 1024 + (2 + NSTAGE) * TILE_BYTES + NBAR * 8 + 48;
   static constexpr int THREADS = 384;
 };
 
-template <int D, bool CAUSAL>
+// MASKED: the instance that applies p.mk (sliding window, key lengths, a
+// bit mask), with causal entering as wr = 0; CAUSAL is then false.
+template <int D, bool CAUSAL, bool MASKED>
 __global__ void __launch_bounds__(384, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
@@ -72,9 +74,9 @@ __global__ void __launch_bounds__(384, 1)
   uint8_t* const misc = gbase + (sBar - base) + 8 * T::NBAR;
   uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(misc);
   volatile int* const abort_flag = reinterpret_cast<volatile int*>(misc + 4);
-  // This CTA's sequence {q0, nq, k0, nk} and its query plane and head, read
-  // back by each role where needed rather than held in registers across the
-  // main loops.
+  // This CTA's sequence {q0, nq, k0, nk}, its query plane and head, its
+  // first key tile and (masked) its visible key count, read back by each
+  // role where needed rather than held in registers across the main loops.
   volatile int* const seq_s = reinterpret_cast<volatile int*>(misc + 8);
 
   const int warp = threadIdx.x >> 5;
@@ -103,15 +105,30 @@ __global__ void __launch_bounds__(384, 1)
       seq_s[3] = sq.nk;
       seq_s[4] = varlen ? h : bh;  // query plane of the tensor maps
       seq_s[5] = h;
+      int js = 0, nke = sq.nk;
+      if (MASKED) {
+        // Keys below the first row's window never take part: start there.
+        if (p.mk.wl >= 0) js = min(max(0, sq.nk - sq.nq + 256 * mt - p.mk.wl) / 128, max(0, (sq.nk - 1) / 128));
+        if (p.mk.key_len != nullptr) nke = max(0, min(nke, p.mk.key_len[b]));
+      }
+      seq_s[6] = js;   // first key tile
+      seq_s[7] = nke;  // keys past this are invisible
     }
   }
-  // Key tiles visited by query tile s of this CTA (at least one: a row that
-  // sees no key still runs one fully masked tile).  Causal: up to the tile
-  // holding the last row's last visible key, koff + 128 qi + 127, with query
-  // row i at position koff + i, koff = Nk - Nq.
+  // One past the last key tile visited by query tile s of this CTA (at
+  // least one tile from the first: a row that sees no key still runs one
+  // fully masked tile).  Causal / windowed: up to the tile holding the last
+  // row's last visible key, with query row i at position koff + i,
+  // koff = Nk - Nq.
   auto key_tiles = [&](int s) {
     const int nq = seq_s[1], nk = seq_s[3];
     const int nkv = max(1, (nk + 127) / 128);
+    if (MASKED) {
+      const int last = nk - nq + 256 * mt + 128 * s + 127;  // position of the tile's last row
+      int hi = seq_s[7];
+      if (p.mk.wr >= 0) hi = min(hi, last + p.mk.wr + 1);
+      return max(seq_s[6] + 1, min((hi + 127) / 128, nkv));
+    }
     return CAUSAL ? max(1, min((nk - nq + 256 * mt + 128 * s + 127) / 128 + 1, nkv)) : nkv;
   };
 
@@ -148,10 +165,29 @@ __global__ void __launch_bounds__(384, 1)
     const int s = warp >> 2;            // query tile of this warpgroup
     const int r = threadIdx.x & 127;    // row within the tile == TMEM lane
     const int qi = 2 * mt + s;          // global query tile index
-    const int n = key_tiles(s);
-    // Columns at or past lim0 - 128 j of key tile j are invisible to row r:
-    // keys past Nk, and for causal rows keys past position koff + 128 qi + r.
-    const int lim0 = CAUSAL ? min(seq_s[3], seq_s[3] - seq_s[1] + qi * 128 + r + 1) : seq_s[3];
+    // Key tiles js .. js + n - 1 (js = 0 unless a window starts later).
+    const int js = MASKED ? seq_s[6] : 0;
+    const int n = key_tiles(s) - js;
+    // Columns at or past lim0 - 128 j of the j-th visited key tile are
+    // invisible to row r: keys past Nk, and for causal rows keys past
+    // position koff + 128 qi + r.  Masked instance: also columns below
+    // lom0 - 128 j (the window's left edge), keys past the key length, the
+    // window's right edge, and the columns whose bit is clear.
+    int lim0, lom0 = 0;
+    // Word index of this row's bits in p.mk.bits (all ones: none); the host
+    // keeps every index of the bit array below 2^32 - 1.
+    uint32_t rowbits = 0xffffffffu;
+    if (MASKED) {
+      const int pos = seq_s[3] - seq_s[1] + qi * 128 + r;
+      int hi = seq_s[7];
+      if (p.mk.wr >= 0) hi = min(hi, pos + p.mk.wr + 1);
+      lim0 = hi - 128 * js;
+      lom0 = (p.mk.wl >= 0 ? pos - p.mk.wl : -(1 << 30)) - 128 * js;
+      if (p.mk.bits != nullptr && qi * 128 + r < p.Nq)
+        rowbits = ((uint32_t)mask_plane(p.mk, b, h) * (uint32_t)p.Nq + (uint32_t)(qi * 128 + r)) * (uint32_t)p.mk.words + 4u * js;
+    } else {
+      lim0 = CAUSAL ? min(seq_s[3], seq_s[3] - seq_s[1] + qi * 128 + r + 1) : seq_s[3];
+    }
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
     const uint32_t tS = tmem + s * 128 + lane_off;
     const uint32_t tO = tmem + 256 + s * 128 + lane_off;
@@ -165,6 +201,8 @@ __global__ void __launch_bounds__(384, 1)
     bool ok = true;
 
     for (int j = 0; j < n; ++j) {
+      uint4 b4 = make_uint4(~0u, ~0u, ~0u, ~0u);
+      if (MASKED && rowbits != 0xffffffffu) b4 = *reinterpret_cast<const uint4*>(p.mk.bits + rowbits + 4u * j);
       ok = __all_sync(0xffffffffu, wait_bounded(wc, barS, j & 1, wait_site(0x51 + s, j)));
       if (!ok) break;
       tc_fence_after();
@@ -188,7 +226,16 @@ __global__ void __launch_bounds__(384, 1)
           x[96 + i] = __uint_as_float(rd[i]);
         }
       }
-      {
+      if (MASKED) {
+        const int lim = lim0 - j * 128, lom = lom0 - j * 128;
+        const bool all_bits = (b4.x & b4.y & b4.z & b4.w) == ~0u;
+        if (__any_sync(0xffffffffu, lim < 128 || lom > 0 || !all_bits)) {
+          const uint32_t bw[4] = {b4.x, b4.y, b4.z, b4.w};
+#pragma unroll
+          for (int i = 0; i < 128; ++i)
+            if (i >= lim || i < lom || !((bw[i >> 5] >> (i & 31)) & 1u)) x[i] = -INFINITY;
+        }
+      } else {
         // Only the diagonal and the ragged last tile have masked columns.
         const int lim = lim0 - j * 128;
         if (__any_sync(0xffffffffu, lim < 128)) {
@@ -320,7 +367,8 @@ __global__ void __launch_bounds__(384, 1)
     if (warp == 8) {
       // ------------------------------------------------------------ producer
       if (lane == 0) {
-        const int q0 = seq_s[0], k0 = seq_s[2], n1 = key_tiles(1);
+        const int js = MASKED ? seq_s[6] : 0;
+        const int q0 = seq_s[0], k0 = seq_s[2] + 128 * js, n1 = key_tiles(1) - js;
         const int qplane = seq_s[4], kplane = varlen ? seq_s[5] / p.G : bhk;
         tma_prefetch_desc(&tmQ);
         tma_prefetch_desc(&tmK);
@@ -376,7 +424,8 @@ __global__ void __launch_bounds__(384, 1)
       // warp-uniform; one elected lane issues each tcgen05 instruction.
       // Descriptors are built once per tile and moved by constant offsets.
       {
-        const int n0 = key_tiles(0), n1 = key_tiles(1);
+        const int js = MASKED ? seq_s[6] : 0;
+        const int n0 = key_tiles(0) - js, n1 = key_tiles(1) - js;  // tiles visited from js on
         const uint32_t leader = elect_one();
         constexpr uint32_t IQK = idesc_bf16_f32(128, 128, false, false);
         constexpr uint32_t IPV = idesc_bf16_f32(128, D, false, true);
@@ -480,10 +529,10 @@ size_t fwd_smem_bytes(int d) {
   }
 }
 
-template <int D, bool C>
+template <int D, bool C, bool M = false>
 static cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                                 const CUtensorMap& to, const FwdParams& p, cudaStream_t stream) {
-  auto kern = fwd_kernel<D, C>;
+  auto kern = fwd_kernel<D, C, M>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, FwdTraits<D>::SMEM);
   if (e != cudaSuccess) return e;
   const unsigned grid = (unsigned)p.n_mtiles * (unsigned)(p.B * p.H);
@@ -492,7 +541,15 @@ static cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, co
 }
 
 cudaError_t launch_fwd(int d, bool causal, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                       const CUtensorMap& to, const FwdParams& p, cudaStream_t stream) {
+                       const CUtensorMap& to, const FwdParams& p, cudaStream_t stream, bool masked) {
+  if (masked) {
+    switch (d) {
+      case 64: return launch_fwd_t<64, false, true>(tq, tk, tv, to, p, stream);
+      case 96: return launch_fwd_t<96, false, true>(tq, tk, tv, to, p, stream);
+      case 128: return launch_fwd_t<128, false, true>(tq, tk, tv, to, p, stream);
+      default: return cudaErrorInvalidValue;
+    }
+  }
   switch (d) {
     case 64: return causal ? launch_fwd_t<64, true>(tq, tk, tv, to, p, stream)
                            : launch_fwd_t<64, false>(tq, tk, tv, to, p, stream);

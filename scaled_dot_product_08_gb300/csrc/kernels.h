@@ -18,6 +18,23 @@ struct VarlenArgs {
   int total_q, total_k;  // packed rows (the bound every offset is checked against)
 };
 
+// Masks beyond causal (the masked kernel instances only).  Query row i sits
+// at position Nk - Nq + i; key j is visible to it when
+//   j >= pos - wl (wl >= 0),  j <= pos + wr (wr >= 0; causal sets wr = 0),
+//   j < key_len[b] (key_len != nullptr),  and its bit is set (bits != nullptr).
+// bits: (planes, Nq, words) uint32, bit j % 32 of word j / 32 of a query row;
+// bits_t: (planes, Nk, words_t), bit i % 32 of word i / 32 of a key row;
+// words / words_t are multiples of 4 (one 16-byte group per 128 columns).
+// plane = (mask_b > 1 ? b : 0) * mask_h + (mask_h > 1 ? h : 0).
+struct MaskArgs {
+  int wl, wr;
+  const int* key_len;
+  const uint32_t* bits;
+  const uint32_t* bits_t;
+  int words, words_t;
+  int mask_b, mask_h;
+};
+
 // Forward kernel arguments (tensor maps are passed separately).
 struct FwdParams {
   float* lse;            // (B, H, Nq) float32
@@ -32,6 +49,7 @@ struct FwdParams {
   int* info;             // first-timeout record (4 ints)
   VarlenArgs vl;         // varlen: Nq / Nk above are the longest sequences
   uint16_t* o;           // varlen: O base, for the rows of a sequence's last tile
+  MaskArgs mk;           // masked instances only
 };
 
 // Backward arguments.
@@ -55,6 +73,7 @@ struct BwdParams {
   uint16_t* dq;          // varlen: output bases, for the rows of a sequence's last tile
   uint16_t* dk;
   uint16_t* dv;
+  MaskArgs mk;           // masked instances only
 };
 
 // Decode (split over the keys) arguments.
@@ -90,6 +109,14 @@ __host__ __device__ inline long long varlen_vec_stride(long long total_q, long l
 }
 
 #ifdef __CUDACC__
+// floor(a / 128) for any sign of a.
+__device__ __forceinline__ int floor_div128(int a) { return a >= 0 ? a / 128 : -((127 - a) / 128); }
+
+// Mask plane of batch b, head h.
+__device__ __forceinline__ int mask_plane(const MaskArgs& mk, int b, int h) {
+  return (mk.mask_b > 1 ? b : 0) * mk.mask_h + (mk.mask_h > 1 ? h : 0);
+}
+
 // One sequence of a (possibly packed) batch as a kernel sees it.
 struct SeqView {
   int q0, nq;  // first query row in the tensor map, query rows
@@ -116,15 +143,21 @@ size_t bwd_smem_bytes(int d);
 size_t bwd_dq_smem_bytes(int d);
 size_t decode_smem_bytes(int d);
 
+// masked: the instance that applies p.mk (causal then enters as wr = 0).
 cudaError_t launch_fwd(int d, bool causal, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                       const CUtensorMap& to, const FwdParams& p, cudaStream_t stream);
+                       const CUtensorMap& to, const FwdParams& p, cudaStream_t stream, bool masked = false);
 
 cudaError_t launch_bwd_prep(const BwdParams& p, cudaStream_t stream);
 cudaError_t launch_bwd_grad(int d, bool causal, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                             const CUtensorMap& tdo, const CUtensorMap& tdk, const CUtensorMap& tdv,
-                            const BwdParams& p, cudaStream_t stream);
+                            const BwdParams& p, cudaStream_t stream, bool masked = false);
 cudaError_t launch_bwd_dq(int d, bool causal, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                          const CUtensorMap& tdo, const CUtensorMap& tdq, const BwdParams& p, cudaStream_t stream);
+                          const CUtensorMap& tdo, const CUtensorMap& tdq, const BwdParams& p, cudaStream_t stream,
+                          bool masked = false);
+// Packs a boolean (mask_b, mask_h, Nq, Nk) byte mask into the row and
+// transposed bit layouts of MaskArgs (bits_t may be null: row bits only).
+cudaError_t launch_mask_pack(const uint8_t* mask, int mask_b, int mask_h, int Nq, int Nk, uint32_t* bits,
+                             int words, uint32_t* bits_t, int words_t, cudaStream_t stream);
 cudaError_t launch_decode(int d, bool causal, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                           const DecParams& p, cudaStream_t stream);
 

@@ -195,3 +195,28 @@ def test_varlen_rejects_bad_arguments(lib):
                                                  w, wsb, 2, 4, 2, 10, 10, 8, 8, 128, 0.1, 1, None)
     assert g(ws - 1) == S.WORKSPACE
     assert g(ws, w=0) == S.WORKSPACE
+
+
+def test_masked_rejects_bad_arguments(lib):
+    import scaled_dot_product_08_gb300 as sdpa
+    S = sdpa.Status
+    M = lambda wl=-1, wr=-1, kl=0, m=0, mb=1, mh=1: sdpa.AttnMask(wl, wr, kl, m, mb, mh)
+    f = lambda mask, ws=FAKE, wsb=1 << 20, causal=0: sdpa.attn_fwd_masked(
+        FAKE, FAKE, FAKE, FAKE, FAKE, 2, 4, 2, 100, 300, 128, 0.1, causal, mask, ws, wsb, None)
+    assert f(M(wl=-2)) == S.INVALID_ARG
+    assert f(M(wr=-3)) == S.INVALID_ARG
+    assert f(M(kl=FAKE + 2)) == S.MISALIGNED                 # key lengths are int32
+    assert f(M(m=FAKE, mb=3)) == S.INVALID_ARG               # mask batch must be 1 or B
+    assert f(M(m=FAKE, mh=2)) == S.INVALID_ARG               # mask heads must be 1 or H
+    need = sdpa.attn_masked_workspace_size(2, 4, 2, 100, 300, 128, M(m=FAKE, mb=2), 0)
+    assert need == 2 * 100 * 12 * 4                          # one bit per (query, key), 16-byte groups
+    assert f(M(m=FAKE, mb=2), wsb=need - 1) == S.WORKSPACE
+    assert f(M(m=FAKE, mb=2), ws=0) == S.WORKSPACE
+    assert sdpa.attn_masked_workspace_size(2, 4, 2, 100, 300, 128, M(), 0) == 0
+    assert sdpa.attn_masked_workspace_size(2, 4, 2, 100, 300, 128, M(), 1) == sdpa.attn_bwd_workspace_size(
+        2, 4, 2, 100, 128)
+    g = lambda stages, wsb=1 << 20: sdpa.attn_bwd_masked_stages(
+        FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 2, 4, 2, 100, 300, 128, 0.1, 0, M(), FAKE, wsb,
+        stages, None)
+    assert g(0) == S.INVALID_ARG and g(8) == S.INVALID_ARG
+    assert g(7, wsb=16) == S.WORKSPACE

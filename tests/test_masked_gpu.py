@@ -1,0 +1,134 @@
+"""GPU parity of the masked path (attn_fwd_masked / attn_bwd_masked through
+the C ABI: sliding windows, per-batch key lengths, boolean masks and their
+combinations) against the fp64 oracle on seeded bf16 inputs.  The backward
+consumes the GPU forward's O and lse."""
+import math
+
+import numpy as np
+import pytest
+
+import oracle
+from sdpa_inputs import make_random
+from tests.parity import LSE_MAX_ABS, O_MAX_ABS, O_MEAN_ABS, check_grads, dev, host
+
+pytestmark = pytest.mark.gpu
+
+
+def _problem(B, H, Hkv, Nq, Nk, d, seed):
+    return (make_random((B, H, Nq, d), seed), make_random((B, Hkv, Nk, d), seed + 1),
+            make_random((B, Hkv, Nk, d), seed + 2), make_random((B, H, Nq, d), seed + 3))
+
+
+def _t(a, dtype):
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(a)).to(dtype).cuda()
+
+
+def _check_forward(O, lse, Or, lr, what):
+    live = np.isfinite(lr)
+    assert np.all(np.isneginf(lse[~live])), what
+    assert np.all(O[~live] == 0), what
+    err = np.abs(O[live] - Or[live])
+    assert err.max() <= O_MAX_ABS and err.mean() <= O_MEAN_ABS, f"{what}: O err {err.max():.3e} / {err.mean():.3e}"
+    assert np.abs(lse[live] - lr[live]).max() <= LSE_MAX_ABS, what
+
+
+def _run(lib, shape, causal, window=None, key_lengths=None, mask=None, seed=40000):
+    import torch
+    B, H, Hkv, Nq, Nk, d = shape
+    q, k, v, do = _problem(B, H, Hkv, Nq, Nk, d, seed)
+    s = 1 / math.sqrt(d)
+    kl = _t(np.asarray(key_lengths, dtype=np.int32), torch.int32) if key_lengths is not None else None
+    mk = _t(mask.astype(np.uint8), torch.uint8) if mask is not None else None
+    tq, tk, tv, tdo = dev(q), dev(k), dev(v), dev(do)
+    O, lse = lib.forward_masked(tq, tk, tv, s, causal, window, kl, mk)
+    g = lib.backward_masked(tq, tk, tv, O, lse, tdo, s, causal, window, kl, mk)
+    assert lib.attn_get_device_status(None) == lib.Status.OK
+    Or, lr = oracle.attention_masked_forward(q, k, v, s, causal, window, key_lengths, mask)
+    ref = oracle.attention_masked_backward(q, k, v, do, s, causal, window, key_lengths, mask)
+    return host(O), host(lse), [host(x) for x in g], Or, lr, ref
+
+
+CASES = [
+    # (B, H, Hkv, Nq, Nk, d), causal, window, key_lengths, mask kind
+    ((1, 4, 2, 700, 700, 128), True, (100, -1), None, None),       # causal sliding window
+    ((1, 2, 2, 513, 513, 64), False, (64, 200), None, None),       # two-sided window
+    ((2, 2, 1, 640, 640, 128), True, (300, -1), None, None),       # window spanning tiles
+    ((3, 2, 2, 700, 700, 128), False, None, [700, 129, 1], None),  # padding by key length
+    ((3, 2, 2, 700, 700, 96), True, None, [650, 300, 1], None),
+    ((2, 4, 2, 300, 300, 96), False, None, None, "batch"),          # random boolean mask per batch element
+    ((2, 4, 4, 260, 260, 128), True, None, None, "full"),           # per (batch, head), with causal
+    ((1, 2, 1, 384, 384, 64), False, None, None, "shared"),
+    ((2, 2, 2, 512, 512, 128), False, None, None, "documents"),     # block-diagonal document mask
+    ((2, 4, 2, 200, 600, 128), True, (250, -1), [600, 450], "batch"),  # all of it, Nq < Nk
+    ((1, 2, 2, 300, 150, 64), True, None, None, None),              # causal with Nq > Nk: rows without keys
+]
+
+
+def _mask(kind, B, H, Nq, Nk, seed):
+    rng = np.random.default_rng(seed)
+    if kind is None:
+        return None
+    if kind == "documents":
+        m = np.zeros((B, 1, Nq, Nk), dtype=bool)
+        for b in range(B):
+            cuts = np.sort(rng.choice(np.arange(1, Nq), size=4, replace=False))
+            edges = [0, *cuts.tolist(), Nq]
+            for a, e in zip(edges, edges[1:]):
+                m[b, 0, a:e, a:e] = True
+        return m
+    shape = {"batch": (B, 1, Nq, Nk), "full": (B, H, Nq, Nk), "shared": (1, 1, Nq, Nk)}[kind]
+    return rng.random(shape) < 0.7
+
+
+@pytest.mark.parametrize("case", CASES, ids=lambda c: "B%dH%dKV%dQ%dK%dd%d" % c[0] + f"_c{int(c[1])}_w{c[2]}_kl{c[3] is not None}_{c[4]}")
+def test_masked_matches_oracle(cuda_lib, case):
+    shape, causal, window, kl, kind = case
+    B, H, Hkv, Nq, Nk, d = shape
+    mask = _mask(kind, B, H, Nq, Nk, 41000 + Nq)
+    O, lse, g, Or, lr, ref = _run(cuda_lib, shape, causal, window, kl, mask, seed=42000 + Nq + Nk)
+    _check_forward(O, lse, Or, lr, str(case))
+    check_grads(g, ref, str(case))
+
+
+def test_rows_without_keys_are_zero(cuda_lib):
+    B, H, Hkv, N, d = 1, 2, 2, 256, 128
+    mask = np.ones((1, 1, N, N), dtype=bool)
+    mask[0, 0, [0, 5, 130, 255]] = False
+    O, lse, g, Or, lr, ref = _run(cuda_lib, (B, H, Hkv, N, N, d), False, None, None, mask, seed=43000)
+    for r in (0, 5, 130, 255):
+        assert np.all(O[:, :, r] == 0) and np.all(np.isneginf(lse[:, :, r])) and np.all(g[0][:, :, r] == 0)
+    _check_forward(O, lse, Or, lr, "dead rows")
+    check_grads(g, ref, "dead rows")
+
+
+def test_keys_nobody_sees_get_zero_gradients(cuda_lib):
+    # Key length 100 of 600: keys 100.. are padding for every query.
+    shape = (1, 2, 2, 300, 600, 128)
+    O, lse, g, Or, lr, ref = _run(cuda_lib, shape, False, None, [100], None, seed=44000)
+    assert np.all(g[1][:, :, 100:] == 0) and np.all(g[2][:, :, 100:] == 0)
+    check_grads(g, ref, "padding keys")
+
+
+def test_plain_causal_through_the_masked_path_is_the_dense_result(cuda_lib):
+    # No window, no lengths, no mask: the masked instance visits the same
+    # tiles and masks the same entries as the dense causal kernels.
+    B, H, Hkv, N, d = 2, 4, 2, 777, 128
+    q, k, v, do = (dev(x) for x in _problem(B, H, Hkv, N, N, d, 45000))
+    for causal in (False, True):
+        Od, ld = cuda_lib.forward(q, k, v, 0.1, causal)
+        gd = cuda_lib.backward(q, k, v, Od, ld, do, 0.1, causal)
+        Om, lm = cuda_lib.forward_masked(q, k, v, 0.1, causal)
+        gm = cuda_lib.backward_masked(q, k, v, Om, lm, do, 0.1, causal)
+        assert np.array_equal(host(Om), host(Od)) and np.array_equal(host(lm), host(ld))
+        for a, b in zip(gm, gd):
+            assert np.array_equal(host(a), host(b))
+
+
+def test_masked_backward_is_deterministic(cuda_lib):
+    shape = (2, 4, 2, 300, 300, 96)
+    mask = _mask("batch", 2, 4, 300, 300, 46000)
+    a = _run(cuda_lib, shape, True, (120, -1), [300, 200], mask, seed=46001)[2]
+    b = _run(cuda_lib, shape, True, (120, -1), [300, 200], mask, seed=46001)[2]
+    for x, y in zip(a, b):
+        assert np.array_equal(x, y)
