@@ -61,6 +61,11 @@ def parse_args():
 
 
 def workload_desc(w):
+    if w.kind == "masked":
+        what = (f"sliding window (left {w.window[0]}, right {w.window[1]})" if w.window is not None
+                else f"prefix-LM boolean mask (prefix {w.prefix})")
+        return (f"{w.name}: B={w.B} H={w.H} Hkv={w.Hkv} N={w.N} d={w.d} {'causal ' if w.causal else ''}{what} "
+                f"{'fwd+bwd' if w.with_grad else 'fwd'}; FLOPs count the visible (query, key) pairs")
     if w.kind == "varlen":
         from sdpa_inputs import varlen_lengths
         lens = varlen_lengths(w)
@@ -78,6 +83,10 @@ def workload_desc(w):
 
 def step_flops(w):
     from sdpa_inputs import flops_backward, flops_cross, flops_forward
+    if w.kind == "masked":
+        from sdpa_inputs import flops_masked
+        f = flops_masked(w)
+        return f, (2.5 * f if w.with_grad else 0.0)
     if w.kind == "varlen":
         from sdpa_inputs import flops_varlen, varlen_lengths
         f = flops_varlen(varlen_lengths(w), w.H, w.d, w.causal)
@@ -203,6 +212,14 @@ def _oracle_head_seconds(w, x):
     """Wall time of the oracle on one whole head of the workload."""
     import oracle
     q, k, v, do = x
+    if w.kind == "masked":
+        from sdpa_inputs import prefix_lm_mask
+        mask = prefix_lm_mask(w.N, w.prefix) if w.prefix is not None else None
+        t0 = time.perf_counter()
+        oracle.attention_masked_forward(q, k, v, w.softmax_scale, w.causal, w.window, None, mask)
+        if w.with_grad:
+            oracle.attention_masked_backward(q, k, v, do, w.softmax_scale, w.causal, w.window, None, mask)
+        return time.perf_counter() - t0
     t0 = time.perf_counter()
     off = (w.N - w.n_queries) if (w.kind == "cross" and w.causal) else 0
     oracle.attention_forward(q, k, v, w.softmax_scale, w.causal, q_offset=off)
@@ -213,6 +230,9 @@ def _oracle_head_seconds(w, x):
 
 def _head_flops(w):
     from sdpa_inputs import flops_backward, flops_forward
+    if w.kind == "masked":
+        from sdpa_inputs import visible_pairs
+        return 4.0 * w.d * visible_pairs(w) * (3.5 if w.with_grad else 1.0)
     if w.kind == "varlen":
         n = _oracle_lengths(w)[0]
         return flops_forward(1, 1, n, w.d, w.causal) * (3.5 if w.with_grad else 1.0)
@@ -336,6 +356,17 @@ def run_ours(args, w, rank, world, local_rank):
     else:
         x = make_inputs(w)
         lse_shape = (B, H, Nq)
+    mask_spec = None
+    if w.kind == "masked":
+        from sdpa_inputs import prefix_lm_mask
+        mask_t = None
+        if w.prefix is not None:
+            mask_t = torch.from_numpy(prefix_lm_mask(N, w.prefix).astype("uint8")).cuda()
+            extra_in = [mask_t]
+        mask_spec = sdpa.make_mask(w.window, None, mask_t, B, H)
+        mws_f = sdpa.attn_masked_workspace_size(B, H, Hkv, Nq, N, d, mask_spec, 0)
+        mws_b = sdpa.attn_masked_workspace_size(B, H, Hkv, Nq, N, d, mask_spec, 1)
+        mws = torch.empty(max(mws_f, mws_b, 16), dtype=torch.uint8, device="cuda")
     q, k, v = dev(x["q"]), dev(x["k"]), dev(x["v"])
     do = dev(x["do"]) if w.with_grad else None
     o = torch.empty_like(q)
@@ -366,6 +397,15 @@ def run_ours(args, w, rank, world, local_rank):
                                                      N, N, maxlen, maxlen, d, s, w.causal, sp), "attn_fwd_varlen")]
         if w.with_grad:
             launches += [vstage(1), vstage(2), vstage(4)]
+    elif w.kind == "masked":
+        def mstage(mask):
+            return lambda: chk(sdpa.attn_bwd_masked_stages(
+                P(q), P(k), P(v), P(o), P(lse), P(do), P(dq), P(dk), P(dv), B, H, Hkv, Nq, N, d, s, w.causal,
+                mask_spec, P(mws), mws.numel(), mask, sp), "attn_bwd_masked_stages")
+        launches = [lambda: chk(sdpa.attn_fwd_masked(P(q), P(k), P(v), P(o), P(lse), B, H, Hkv, Nq, N, d, s, w.causal,
+                                                     mask_spec, P(mws), mws.numel(), sp), "attn_fwd_masked")]
+        if w.with_grad:
+            launches += [mstage(1), mstage(2), mstage(4)]
     elif w.kind == "cross":
         launches = [lambda: chk(sdpa.attn_fwd_cross(P(q), P(k), P(v), P(o), P(lse), B, H, Hkv, Nq, N, d, s,
                                                     w.causal, sp), "attn_fwd_cross")]
@@ -388,6 +428,12 @@ def run_ours(args, w, rank, world, local_rank):
                                                B, H, Hkv, N, d, s, w.causal, sp), "attn_bwd_grad"),
                 lambda: chk(sdpa.attn_bwd_dq(P(q), P(k), P(v), P(do), P(dq), P(ws), ws_bytes,
                                              B, H, Hkv, N, d, s, w.causal, sp), "attn_bwd_dq")]
+
+    # Kernels per step: one per call, plus the mask packing inside the masked
+    # forward and backward-prep calls when there is a boolean mask.
+    kernels_per_step = len(launches) + (2 if w.kind == "masked" and w.prefix is not None else 0)
+    if w.kind == "masked" and w.prefix is not None and not w.with_grad:
+        kernels_per_step -= 1
 
     def step(evs=None):
         for idx, launch in enumerate(launches):
@@ -520,7 +566,7 @@ def run_ours(args, w, rank, world, local_rank):
             "fwd_tflops": f_fwd / (per_kernel["attn_fwd"] / 1e3) / 1e12,
             "kernel_ms": per_kernel,
             "roofline": roof, "cpu_baseline": cb, "e2e": e2e, "clocks": clk,
-            "gpu_launches": len(names) * K,
+            "gpu_launches": kernels_per_step * K,
         }
         if w.with_grad:
             line["bwd_tflops"] = f_bwd / (sum(per_kernel[n] for n in names[1:]) / 1e3) / 1e12

@@ -44,6 +44,13 @@ backward, self-attention (the same lengths for queries and keys):
        Tensors are packed token-major: (total, heads, d).  The draws of Q,
        K, V, dO use default_rng(seed + 1000) in that order.
 
+Masked workloads (attn_fwd_masked / attn_bwd_masked), forward + backward:
+
+  sw1  B=1  H=32  Hkv=8  N=16384 d=128  causal sliding window of 4096 keys
+       (window_left 4095): the [PROF] page's window attention, n * w work
+  pl1  B=8  H=16  Hkv=16 N=4096  d=128  prefix-LM boolean mask, one plane for
+       all (b, h): key j visible to query i when j < 1024 or j <= i
+
 Every draw is numpy's PCG64 ``default_rng(seed).standard_normal(dtype=float32)``
 taken in the fixed order Q, K, V, dO, multiplied by the config's amplitude and
 then rounded to bf16 (round to nearest, ties to even).
@@ -74,6 +81,8 @@ class Workload:
     kind: str = "full"             # "full" (Nq = N), "decode" (attn_decode), "cross" (attn_fwd_cross),
                                    # "varlen" (attn_fwd_varlen: N = total tokens, B = 1)
     len_range: tuple[int, int] | None = None  # varlen: sequence lengths drawn from [lo, hi]
+    window: tuple[int, int] | None = None     # masked: (left, right), -1 = open
+    prefix: int | None = None                 # masked: prefix-LM boolean mask with this prefix
 
     @property
     def softmax_scale(self) -> float:
@@ -103,7 +112,36 @@ WORKLOADS: dict[str, Workload] = {
     "cp1": Workload("cp1", 1, 32, 8, 16384, 128, True, 8, Nq=2048, kind="cross"),
     "cx": Workload("cx", 8, 16, 16, 4096, 128, False, 9, with_grad=True, Nq=2048, kind="cross"),
     "vl1": Workload("vl1", 1, 16, 16, 32768, 128, True, 10, with_grad=True, kind="varlen", len_range=(128, 8192)),
+    "sw1": Workload("sw1", 1, 32, 8, 16384, 128, True, 11, with_grad=True, kind="masked", window=(4095, -1)),
+    "pl1": Workload("pl1", 8, 16, 16, 4096, 128, False, 12, with_grad=True, kind="masked", prefix=1024),
 }
+
+
+def prefix_lm_mask(N: int, prefix: int) -> np.ndarray:
+    """Boolean (1, 1, N, N) prefix-LM mask: key j is visible to query i when
+    j < prefix (the bidirectional prefix) or j <= i (causal after it)."""
+    i = np.arange(N)[:, None]
+    j = np.arange(N)[None, :]
+    return ((j < prefix) | (j <= i))[None, None]
+
+
+def visible_pairs(w: Workload) -> int:
+    """(query, key) pairs a masked self-attention workload computes, per
+    (batch, head): the exact count, by closed form."""
+    N = w.N
+    if w.prefix is not None:
+        P = w.prefix
+        return P * P + sum(i + 1 for i in range(P, N))
+    wl = w.window[0] if w.window is not None else -1
+    if w.causal:
+        return sum(min(i + 1, wl + 1) if wl >= 0 else i + 1 for i in range(N))
+    raise ValueError("no closed form for this mask")
+
+
+def flops_masked(w: Workload) -> float:
+    """Forward work of a masked workload: 4 * d per visible (query, key)
+    pair and head (the convention of flops_forward with the exact count)."""
+    return 4.0 * w.B * w.H * w.d * visible_pairs(w)
 
 
 def varlen_lengths(w: Workload) -> list[int]:
