@@ -603,15 +603,16 @@ attn_status_t attn_bwd_varlen_stages(const void* q, const void* k, const void* v
 // key row, planes, and the byte sizes of the two arrays.
 struct MaskGeom {
   int words, words_t, planes;
-  size_t bits_bytes, bits_t_bytes;
+  size_t bits_bytes, bits_t_bytes, flags_bytes;
 };
 
 static MaskGeom mask_geom(int Nq, int Nk, const attn_mask_t* m) {
-  MaskGeom g{((Nk + 127) / 128) * 4, ((Nq + 127) / 128) * 4, 0, 0, 0};
+  MaskGeom g{((Nk + 127) / 128) * 4, ((Nq + 127) / 128) * 4, 0, 0, 0, 0};
   if (m != nullptr && m->mask != nullptr) {
     g.planes = m->mask_batch * m->mask_heads;
     g.bits_bytes = (size_t)g.planes * Nq * g.words * 4;
     g.bits_t_bytes = (size_t)g.planes * Nk * g.words_t * 4;
+    g.flags_bytes = ((size_t)g.planes * (g.words_t / 4) * (g.words / 4) + 15) / 16 * 16;
   }
   return g;
 }
@@ -648,9 +649,13 @@ static attn_status_t check_mask_ptrs(const attn_mask_t* m) {
 
 // Kernel mask arguments; the bit arrays (when there is a mask) at `bits` and
 // `bits_t` inside the caller's workspace.  Causal enters as wr = 0.
-static sdpa::MaskArgs mask_args(const attn_mask_t* m, int Nq, int Nk, int causal, uint32_t* bits, uint32_t* bits_t) {
+static sdpa::MaskArgs mask_args(const attn_mask_t* m, int Nq, int Nk, int causal, uint32_t* bits, uint32_t* bits_t,
+                                uint8_t* flags) {
   const MaskGeom g = mask_geom(Nq, Nk, m);
   sdpa::MaskArgs a;
+  a.flags = m->mask != nullptr ? flags : nullptr;
+  a.ftq = g.words_t / 4;
+  a.ftk = g.words / 4;
   a.wl = m->window_left;
   a.wr = causal ? 0 : m->window_right;
   a.key_len = m->key_lengths;
@@ -669,8 +674,8 @@ size_t attn_masked_workspace_size(int B, int H, int Hkv, int Nq, int Nk, int d, 
       check_mask(B, H, Nq, Nk, mask) != ATTN_OK)
     return 0;
   const MaskGeom g = mask_geom(Nq, Nk, mask);
-  if (!backward) return g.bits_bytes;
-  return attn_bwd_workspace_size(B, H, Hkv, Nq, d) + g.bits_bytes + g.bits_t_bytes;
+  if (!backward) return g.bits_bytes + g.flags_bytes;
+  return attn_bwd_workspace_size(B, H, Hkv, Nq, d) + g.bits_bytes + g.bits_t_bytes + g.flags_bytes;
 }
 
 attn_status_t attn_fwd_masked(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
@@ -681,7 +686,8 @@ attn_status_t attn_fwd_masked(const void* q, const void* k, const void* v, void*
   ATTN_TRY(check_scale_flag(scale, causal));
   ATTN_TRY(check_mask(B, H, Nq, Nk, mask));
   const MaskGeom g = mask_geom(Nq, Nk, mask);
-  if (g.bits_bytes > 0 && (workspace == nullptr || workspace_bytes < g.bits_bytes)) return ATTN_ERR_WORKSPACE;
+  if (g.bits_bytes > 0 && (workspace == nullptr || workspace_bytes < g.bits_bytes + g.flags_bytes))
+    return ATTN_ERR_WORKSPACE;
   ATTN_TRY(check_ptrs({q, k, v, o, lse}));
   if (g.bits_bytes > 0) ATTN_TRY(check_ptrs({workspace}));
   ATTN_TRY(check_mask_ptrs(mask));
@@ -706,12 +712,14 @@ attn_status_t attn_fwd_masked(const void* q, const void* k, const void* v, void*
   p.status = di->status;
   p.limit_ns = wait_limit_ns();
   p.info = di->info;
+  // Workspace: [row bits | tile flags].
   uint32_t* bits = static_cast<uint32_t*>(workspace);
-  p.mk = mask_args(mask, Nq, Nk, causal, bits, nullptr);
+  uint8_t* flags = static_cast<uint8_t*>(workspace) + g.bits_bytes;
+  p.mk = mask_args(mask, Nq, Nk, causal, bits, nullptr, flags);
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (mask->mask != nullptr &&
       sdpa::launch_mask_pack(static_cast<const uint8_t*>(mask->mask), mask->mask_batch, mask->mask_heads, Nq, Nk,
-                             bits, g.words, nullptr, 0, st) != cudaSuccess)
+                             bits, g.words, nullptr, 0, flags, st) != cudaSuccess)
     return ATTN_ERR_LAUNCH;
   return sdpa::launch_fwd(d, false, tq, tk, tv, to, p, st, true) == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;
 }
@@ -737,17 +745,18 @@ attn_status_t attn_bwd_masked_stages(const void* q, const void* k, const void* v
       !make_map_bf16(&tdq, dq, d, Nq, (long long)B * H) || !make_map_bf16(&tdk, dk, d, Nk, (long long)B * Hkv) ||
       !make_map_bf16(&tdv, dv, d, Nk, (long long)B * Hkv))
     return ATTN_ERR_CUDA;
-  // Workspace: [row vectors | row bits | transposed bits].
+  // Workspace: [row vectors | row bits | transposed bits | tile flags].
   const MaskGeom g = mask_geom(Nq, Nk, mask);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   uint32_t* bits = reinterpret_cast<uint32_t*>(ws + attn_bwd_workspace_size(B, H, Hkv, Nq, d));
   uint32_t* bits_t = reinterpret_cast<uint32_t*>(reinterpret_cast<uint8_t*>(bits) + g.bits_bytes);
+  uint8_t* flags = reinterpret_cast<uint8_t*>(bits_t) + g.bits_t_bytes;
   sdpa::BwdParams p;
   bwd_params(&p, workspace, B, H, Hkv, Nq, Nk, d, scale, causal, di);
   p.o = static_cast<const uint16_t*>(o);
   p.dout = static_cast<const uint16_t*>(dout);
   p.lse = lse;
-  p.mk = mask_args(mask, Nq, Nk, causal, bits, bits_t);
+  p.mk = mask_args(mask, Nq, Nk, causal, bits, bits_t, flags);
   p.dq = static_cast<uint16_t*>(dq);  // outputs whose tiles nothing attends to are zeroed in place
   p.dk = static_cast<uint16_t*>(dk);
   p.dv = static_cast<uint16_t*>(dv);
@@ -756,7 +765,7 @@ attn_status_t attn_bwd_masked_stages(const void* q, const void* k, const void* v
     if (sdpa::launch_bwd_prep(p, st) != cudaSuccess) return ATTN_ERR_LAUNCH;
     if (mask->mask != nullptr &&
         sdpa::launch_mask_pack(static_cast<const uint8_t*>(mask->mask), mask->mask_batch, mask->mask_heads, Nq, Nk,
-                               bits, g.words, bits_t, g.words_t, st) != cudaSuccess)
+                               bits, g.words, bits_t, g.words_t, flags, st) != cudaSuccess)
       return ATTN_ERR_LAUNCH;
   }
   if ((stages & 2u) && sdpa::launch_bwd_grad(d, false, tq, tk, tv, tdo, tdk, tdv, p, st, true) != cudaSuccess)

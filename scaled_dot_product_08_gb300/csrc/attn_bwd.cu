@@ -137,7 +137,8 @@ struct BwdTraits {
   static constexpr int NBAR = 16;
   // K, V, Q[2], dO[2], then vectors, barriers, misc
   static constexpr int TILES_BYTES = 6 * TILE_BYTES;
-  static constexpr int SMEM = TILES_BYTES + 2 * VEC_BYTES + NBAR * 8 + 48;
+  static constexpr int MISC = 64;                      // tmem slot, abort flag, per-CTA values
+  static constexpr int SMEM = TILES_BYTES + 2 * VEC_BYTES + NBAR * 8 + MISC + 4 * kMaxStepList;
   static constexpr int THREADS = 384;
 };
 
@@ -181,6 +182,9 @@ __global__ void __launch_bounds__(384, 1)
   // This CTA's sequence {q0, nq, k0, nk}, read back where needed rather than
   // held in registers across the main loops.
   volatile int* const seq_s = reinterpret_cast<volatile int*>(misc + 8);
+  // Masked instance with a tile mask: the (head in group, query tile) steps
+  // this CTA runs, as (g << 16) | (i - i0).
+  volatile uint32_t* const step_list = reinterpret_cast<volatile uint32_t*>(misc + T::MISC);
   const float* const vec_g = reinterpret_cast<const float*>(smem_raw + (sVec - base));
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -238,7 +242,54 @@ __global__ void __launch_bounds__(384, 1)
       if (MASKED) seq_s[7] = (p.mk.mask_b > 1 ? b : 0) * p.mk.mask_h;  // mask plane base of this batch element
     }
   }
-  const int total = p.G * ni;                 // steps: (head in group) x (query tile)
+  // Tile skipping (masked instance with tile flags): warp 0 lists the steps
+  // whose 128 x 128 tile has a visible entry.  seq_s[8] = 1 when the list is
+  // in use, seq_s[9] its length.  No step at all: dK = dV = 0.
+  if (MASKED) {
+    if (warp == 0) {
+      int use = 0, cnt = 0;
+      if (p.mk.flags != nullptr && p.G * ni <= kMaxStepList) {
+        use = 1;
+        for (int base = 0; base < p.G * ni; base += 32) {
+          const int it = base + lane;
+          bool act = false;
+          uint32_t e = 0;
+          if (it < p.G * ni) {
+            const int g = it / ni, i = i0 + it % ni;
+            act = p.mk.flags[((size_t)mask_plane(p.mk, b, hk * p.G + g) * p.mk.ftq + i) * p.mk.ftk + j] != 0;
+            e = ((uint32_t)g << 16) | (uint32_t)(it % ni);
+          }
+          const unsigned bal = __ballot_sync(0xffffffffu, act);
+          if (act) step_list[cnt + __popc(bal & ((1u << lane) - 1u))] = e;
+          cnt += __popc(bal);
+        }
+      }
+      if (lane == 0) {
+        seq_s[8] = use;
+        seq_s[9] = cnt;
+      }
+    }
+    __syncthreads();
+    if (seq_s[8] && seq_s[9] == 0) {
+      const uint32_t rs = varlen ? (uint32_t)(p.Hkv * D) : (uint32_t)D;
+      const long long off = varlen ? ((long long)seq_s[2] + 128 * j) * rs + (long long)hk * D
+                                   : ((long long)bhk * p.Nk + 128 * j) * D;
+      zero_rows2_bf16<D>(p.dk + off, p.dv + off, rs, min(128, seq_s[3] - 128 * j));
+      return;
+    }
+  }
+  const int total = (MASKED && seq_s[8]) ? seq_s[9] : p.G * ni;  // steps: (head in group) x (query tile)
+  // Head in group and query tile of step it.
+  auto step_at = [&](int it, int& g, int& i) {
+    if (MASKED && seq_s[8]) {
+      const uint32_t e = step_list[it];
+      g = (int)(e >> 16);
+      i = i0 + (int)(e & 0xffffu);
+    } else {
+      g = it / ni;
+      i = i0 + it % ni;
+    }
+  };
 
   if (threadIdx.x == 0) {
     mbar_init(bKV, 1);
@@ -293,7 +344,8 @@ __global__ void __launch_bounds__(384, 1)
     const float2 c2 = make_float2(c, c);
     bool ok = true;
     for (int it = 0; it < total; ++it) {
-      const int i = i0 + it % ni;
+      int g, i;
+      step_at(it, g, i);
       const float* vl = vec_g + (it & 1) * (T::VEC_BYTES / 4) + 64 * X;  // -lse2 of this half; -D at +128
       // The vectors come from the bulk copy of this step: observe its barrier
       // (complete by now) before reading them.
@@ -338,7 +390,7 @@ __global__ void __launch_bounds__(384, 1)
         const int qmax = (p.mk.wl >= 0 ? kk + p.mk.wl - koff - 64 * X : (1 << 30)) - 128 * i;
         uint2 bt = make_uint2(~0u, ~0u);
         if (p.mk.bits_t != nullptr && kk < p.Nk) {
-          const int h = seq_s[5] * p.G + it / ni;  // query head of this step
+          const int h = seq_s[5] * p.G + g;  // query head of this step
           const uint32_t plane = (uint32_t)seq_s[7] + (p.mk.mask_h > 1 ? (uint32_t)h : 0u);
           const uint32_t w = (plane * (uint32_t)p.Nk + (uint32_t)kk) * (uint32_t)p.mk.words_t + 2u * X + 4u * i;
           bt = *reinterpret_cast<const uint2*>(p.mk.bits_t + w);
@@ -465,7 +517,9 @@ __global__ void __launch_bounds__(384, 1)
         int issued = 0;
         for (int it = 0; it < total; ++it) {
           const int st = it & 1, rd = it >> 1;
-          const int h = hk * p.G + it / ni, i = i0 + it % ni;
+          int g, i;
+          step_at(it, g, i);
+          const int h = hk * p.G + g;
           const int bh = b * p.H + h;
           const int qplane = varlen ? h : bh;
           if (rd > 0 && !wait_bounded(wc, bQe + 8u * st, (rd - 1) & 1, wait_site(0x31, it))) break;
@@ -504,7 +558,9 @@ __global__ void __launch_bounds__(384, 1)
         int issued = 0;
         for (int it = 0; it < total; ++it) {
           const int st = it & 1, rd = it >> 1;
-          const int h = hk * p.G + it / ni, i = i0 + it % ni;
+          int g, i;
+          step_at(it, g, i);
+          const int h = hk * p.G + g;
           const int qplane = varlen ? h : b * p.H + h;
           if (rd > 0 && !wait_bounded(wc, bDe + 8u * st, (rd - 1) & 1, wait_site(0x32, it))) break;
           const uint32_t bard = bDf + 8u * st;

@@ -35,7 +35,8 @@ struct DqTraits {
   static constexpr int KSTEPS = D / 16;
   static constexpr int KS = 3, VS = 2;                 // K and V ring slots
   static constexpr int NBAR = 18;
-  static constexpr int SMEM = 1024 + (2 + KS + VS) * TILE_BYTES + NBAR * 8 + 48;
+  static constexpr int MISC = 64;                      // tmem slot, abort flag, per-CTA values
+  static constexpr int SMEM = 1024 + (2 + KS + VS) * TILE_BYTES + NBAR * 8 + MISC + 2 * kMaxTileList;
   static constexpr int THREADS = 384;
 };
 
@@ -75,6 +76,9 @@ __global__ void __launch_bounds__(384, 1)
   // and mask plane, read back where needed rather than held in registers
   // across the main loops.
   volatile int* const seq_s = reinterpret_cast<volatile int*>(misc + 8);
+  // Masked instance with a tile mask: the key tiles this CTA visits, in
+  // order, relative to its first key tile jlo.
+  volatile uint16_t* const tile_list = reinterpret_cast<volatile uint16_t*>(misc + T::MISC);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // Work unit: head-major (the CTAs in flight share K/V heads in L2); within
@@ -129,6 +133,44 @@ __global__ void __launch_bounds__(384, 1)
       if (MASKED) seq_s[6] = mask_plane(p.mk, b, h);
     }
   }
+  // Tile skipping (masked instance with tile flags): warp 0 lists the key
+  // tiles of [jlo, jlo + n) whose tile with this query tile has a visible
+  // entry; seq_s[7] = 1 when the list is in use, seq_s[8] its length.  No
+  // tile at all: dQ = 0.
+  if (MASKED) {
+    if (warp == 0) {
+      __syncwarp();
+      int use = 0, cnt = 0;
+      if (p.mk.flags != nullptr && n <= kMaxTileList) {
+        use = 1;
+        const uint8_t* f = p.mk.flags + ((size_t)seq_s[6] * p.mk.ftq + i) * p.mk.ftk + seq_s[4];
+        for (int base = 0; base < n; base += 32) {
+          const int jj = base + lane;
+          const bool act = jj < n && f[jj] != 0;
+          const unsigned bal = __ballot_sync(0xffffffffu, act);
+          if (act) tile_list[cnt + __popc(bal & ((1u << lane) - 1u))] = (uint16_t)jj;
+          cnt += __popc(bal);
+        }
+      }
+      if (lane == 0) {
+        seq_s[7] = use;
+        seq_s[8] = cnt;
+      }
+    }
+    __syncthreads();
+    if (seq_s[7]) {
+      n = seq_s[8];
+      if (n == 0) {
+        const uint32_t rs = varlen ? (uint32_t)(p.H * D) : (uint32_t)D;
+        uint16_t* dst = varlen ? p.dq + ((long long)seq_s[0] + 128 * i) * rs + (long long)h * D
+                               : p.dq + ((long long)bh * p.N + 128 * i) * D;
+        zero_rows_bf16<D>(dst, rs, min(128, seq_s[1] - 128 * i));
+        return;
+      }
+    }
+  }
+  // The j-th visited key tile, relative to jlo.
+  auto tile_at = [&](int jj) -> int { return (MASKED && seq_s[7]) ? (int)tile_list[jj] : jj; };
 
   if (threadIdx.x == 0) {
     mbar_init(bQ, 1);
@@ -197,7 +239,8 @@ __global__ void __launch_bounds__(384, 1)
     for (int j = 0; j < n; ++j) {
       const uint32_t tS = tmem + (j & 1) * 128 + 64 * X + lane_off;
       uint2 bt = make_uint2(~0u, ~0u);
-      if (MASKED && rowbits != 0xffffffffu) bt = *reinterpret_cast<const uint2*>(p.mk.bits + rowbits + 4u * j);
+      const int jt = MASKED ? tile_at(j) : j;  // key tile relative to jlo
+      if (MASKED && rowbits != 0xffffffffu) bt = *reinterpret_cast<const uint2*>(p.mk.bits + rowbits + 4u * jt);
       ok = __all_sync(0xffffffffu, wait_bounded(wc, bS + 8u * (j & 1), (j >> 1) & 1, wait_site(0x81, j)));
       if (!ok) break;
       tc_fence_after();
@@ -224,7 +267,7 @@ __global__ void __launch_bounds__(384, 1)
         x[2 * e + 1] = ex2(t.y);
       }
       if (MASKED) {
-        const int lim = lim0 - 128 * j, lom = lom0 - 128 * j;
+        const int lim = lim0 - 128 * jt, lom = lom0 - 128 * jt;
         if (__any_sync(0xffffffffu, lim < 64 || lom > 0 || (bt.x & bt.y) != ~0u)) {
 #pragma unroll
           for (int k = 0; k < 64; ++k)
@@ -332,14 +375,14 @@ __global__ void __launch_bounds__(384, 1)
           if (kr > 0 && !wait_bounded(wc, bKe + 8u * ks, (kr - 1) & 1, wait_site(0x91, j))) break;
           mbar_expect_tx(bKf + 8u * ks, T::TILE_BYTES);
           for (int cb = 0; cb < T::NB; ++cb)
-            tma_load_3d(sK + ks * T::TILE_BYTES + cb * T::BLOCK_BYTES, &tmK, bKf + 8u * ks, cb * 64, k0 + j * 128,
-                        kplane);
+            tma_load_3d(sK + ks * T::TILE_BYTES + cb * T::BLOCK_BYTES, &tmK, bKf + 8u * ks, cb * 64,
+                        k0 + tile_at(j) * 128, kplane);
           issued = 2 * j + 1;
           if (vr > 0 && !wait_bounded(wc, bVe + 8u * vs, (vr - 1) & 1, wait_site(0x92, j))) break;
           mbar_expect_tx(bVf + 8u * vs, T::TILE_BYTES);
           for (int cb = 0; cb < T::NB; ++cb)
-            tma_load_3d(sV + vs * T::TILE_BYTES + cb * T::BLOCK_BYTES, &tmV, bVf + 8u * vs, cb * 64, k0 + j * 128,
-                        kplane);
+            tma_load_3d(sV + vs * T::TILE_BYTES + cb * T::BLOCK_BYTES, &tmV, bVf + 8u * vs, cb * 64,
+                        k0 + tile_at(j) * 128, kplane);
           issued = 2 * j + 2;
         }
         // Every copy issued above has landed before the CTA may exit.

@@ -44,7 +44,8 @@ struct FwdTraits {
   static constexpr int NSTAGE = (D == 64) ? 8 : 5;   // K/V ring depth
   static constexpr int KSTEPS = D / 16;              // K=16 steps of Q K^T
   static constexpr int NBAR = 2 + 2 * NSTAGE + 2 + 4 + 2 + 1;
-  static constexpr int SMEM = 1024 + (2 + NSTAGE) * TILE_BYTES + NBAR * 8 + 48;
+  static constexpr int MISC = 64;                    // tmem slot, abort flag, per-CTA sequence values
+  static constexpr int SMEM = 1024 + (2 + NSTAGE) * TILE_BYTES + NBAR * 8 + MISC + 2 * kMaxTileList;
   static constexpr int THREADS = 384;
 };
 
@@ -78,6 +79,9 @@ __global__ void __launch_bounds__(384, 1)
   // first key tile and (masked) its visible key count, read back by each
   // role where needed rather than held in registers across the main loops.
   volatile int* const seq_s = reinterpret_cast<volatile int*>(misc + 8);
+  // Masked instance with a tile mask: the key tiles this CTA visits, in
+  // order, relative to its first key tile js.
+  volatile uint16_t* const tile_list = reinterpret_cast<volatile uint16_t*>(misc + T::MISC);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -131,6 +135,47 @@ __global__ void __launch_bounds__(384, 1)
     }
     return CAUSAL ? max(1, min((nk - nq + 256 * mt + 128 * s + 127) / 128 + 1, nkv)) : nkv;
   };
+  // Tile skipping (masked instance with tile flags): warp 0 lists the key
+  // tiles of [js, key_tiles(1)) in which either query tile has a visible
+  // entry; tile js is always listed, so that both query tiles visit at least
+  // one tile.  seq_s[8] / seq_s[9]: list entries below key_tiles(0) / in all;
+  // seq_s[10] = 1 when the list is in use.
+  if (MASKED && warp == 0) {
+    __syncwarp();
+    int use = 0;
+    if (p.mk.flags != nullptr) {
+      const int js = seq_s[6], e0 = key_tiles(0), e1 = key_tiles(1);
+      if (e1 - js <= kMaxTileList) {
+        use = 1;
+        const uint8_t* f = p.mk.flags + ((size_t)mask_plane(p.mk, b, h) * p.mk.ftq + 2 * mt) * p.mk.ftk;
+        const bool has1 = 2 * mt + 1 < p.mk.ftq;
+        int cnt = 0, cnt0 = 0;
+        for (int base = js; base < e1; base += 32) {
+          const int jt = base + lane;
+          bool act = false;
+          if (jt < e1) act = jt == js || f[jt] != 0 || (has1 && f[p.mk.ftk + jt] != 0);
+          const unsigned bal = __ballot_sync(0xffffffffu, act);
+          if (act) tile_list[cnt + __popc(bal & ((1u << lane) - 1u))] = (uint16_t)(jt - js);  // < kMaxTileList
+          cnt += __popc(bal);
+          cnt0 += __popc(__ballot_sync(0xffffffffu, act && jt < e0));
+        }
+        if (lane == 0) {
+          seq_s[8] = cnt0;
+          seq_s[9] = cnt;
+        }
+      }
+    }
+    if (lane == 0) seq_s[10] = use;
+  }
+  // Tiles visited by query tile s, and the absolute index of the jj-th one.
+  auto ntiles = [&](int s) -> int {
+    if (MASKED && seq_s[10]) return s ? seq_s[9] : seq_s[8];
+    return key_tiles(s) - (MASKED ? seq_s[6] : 0);
+  };
+  auto tile_at = [&](int jj) -> int {
+    if (MASKED && seq_s[10]) return seq_s[6] + tile_list[jj];
+    return (MASKED ? seq_s[6] : 0) + jj;
+  };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < 2; ++s) {
@@ -165,9 +210,9 @@ __global__ void __launch_bounds__(384, 1)
     const int s = warp >> 2;            // query tile of this warpgroup
     const int r = threadIdx.x & 127;    // row within the tile == TMEM lane
     const int qi = 2 * mt + s;          // global query tile index
-    // Key tiles js .. js + n - 1 (js = 0 unless a window starts later).
-    const int js = MASKED ? seq_s[6] : 0;
-    const int n = key_tiles(s) - js;
+    // Key tiles tile_at(0 .. n - 1): 0 .. n - 1 unless a window starts later
+    // or a tile mask skips some.
+    const int n = ntiles(s);
     // Columns at or past lim0 - 128 j of the j-th visited key tile are
     // invisible to row r: keys past Nk, and for causal rows keys past
     // position koff + 128 qi + r.  Masked instance: also columns below
@@ -181,10 +226,10 @@ __global__ void __launch_bounds__(384, 1)
       const int pos = seq_s[3] - seq_s[1] + qi * 128 + r;
       int hi = seq_s[7];
       if (p.mk.wr >= 0) hi = min(hi, pos + p.mk.wr + 1);
-      lim0 = hi - 128 * js;
-      lom0 = (p.mk.wl >= 0 ? pos - p.mk.wl : -(1 << 30)) - 128 * js;
+      lim0 = hi;
+      lom0 = p.mk.wl >= 0 ? pos - p.mk.wl : -(1 << 30);
       if (p.mk.bits != nullptr && qi * 128 + r < p.Nq)
-        rowbits = ((uint32_t)mask_plane(p.mk, b, h) * (uint32_t)p.Nq + (uint32_t)(qi * 128 + r)) * (uint32_t)p.mk.words + 4u * js;
+        rowbits = ((uint32_t)mask_plane(p.mk, b, h) * (uint32_t)p.Nq + (uint32_t)(qi * 128 + r)) * (uint32_t)p.mk.words;
     } else {
       lim0 = CAUSAL ? min(seq_s[3], seq_s[3] - seq_s[1] + qi * 128 + r + 1) : seq_s[3];
     }
@@ -202,7 +247,8 @@ __global__ void __launch_bounds__(384, 1)
 
     for (int j = 0; j < n; ++j) {
       uint4 b4 = make_uint4(~0u, ~0u, ~0u, ~0u);
-      if (MASKED && rowbits != 0xffffffffu) b4 = *reinterpret_cast<const uint4*>(p.mk.bits + rowbits + 4u * j);
+      const int jt = MASKED ? tile_at(j) : j;  // absolute key tile
+      if (MASKED && rowbits != 0xffffffffu) b4 = *reinterpret_cast<const uint4*>(p.mk.bits + rowbits + 4u * jt);
       ok = __all_sync(0xffffffffu, wait_bounded(wc, barS, j & 1, wait_site(0x51 + s, j)));
       if (!ok) break;
       tc_fence_after();
@@ -227,7 +273,7 @@ __global__ void __launch_bounds__(384, 1)
         }
       }
       if (MASKED) {
-        const int lim = lim0 - j * 128, lom = lom0 - j * 128;
+        const int lim = lim0 - jt * 128, lom = lom0 - jt * 128;
         const bool all_bits = (b4.x & b4.y & b4.z & b4.w) == ~0u;
         if (__any_sync(0xffffffffu, lim < 128 || lom > 0 || !all_bits)) {
           const uint32_t bw[4] = {b4.x, b4.y, b4.z, b4.w};
@@ -367,8 +413,7 @@ __global__ void __launch_bounds__(384, 1)
     if (warp == 8) {
       // ------------------------------------------------------------ producer
       if (lane == 0) {
-        const int js = MASKED ? seq_s[6] : 0;
-        const int q0 = seq_s[0], k0 = seq_s[2] + 128 * js, n1 = key_tiles(1) - js;
+        const int q0 = seq_s[0], k0 = seq_s[2], n1 = ntiles(1);
         const int qplane = seq_s[4], kplane = varlen ? seq_s[5] / p.G : bhk;
         tma_prefetch_desc(&tmQ);
         tma_prefetch_desc(&tmK);
@@ -389,7 +434,7 @@ __global__ void __launch_bounds__(384, 1)
             const CUtensorMap* m = (w == 0) ? &tmK : &tmV;
             for (int c = 0; c < T::NB; ++c)
               tma_load_3d(sKV + st * T::TILE_BYTES + c * T::BLOCK_BYTES, m, bKVf + 8u * st, c * 64,
-                          k0 + j * 128, kplane);
+                          k0 + tile_at(j) * 128, kplane);
             ++t;
           }
         }
@@ -424,8 +469,7 @@ __global__ void __launch_bounds__(384, 1)
       // warp-uniform; one elected lane issues each tcgen05 instruction.
       // Descriptors are built once per tile and moved by constant offsets.
       {
-        const int js = MASKED ? seq_s[6] : 0;
-        const int n0 = key_tiles(0) - js, n1 = key_tiles(1) - js;  // tiles visited from js on
+        const int n0 = ntiles(0), n1 = ntiles(1);  // tiles visited by query tile 0 / 1
         const uint32_t leader = elect_one();
         constexpr uint32_t IQK = idesc_bf16_f32(128, 128, false, false);
         constexpr uint32_t IPV = idesc_bf16_f32(128, D, false, true);

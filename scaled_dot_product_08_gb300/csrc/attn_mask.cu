@@ -10,7 +10,9 @@
 // and transposed bits (bit i % 32 of word i / 32 of a key row) for the
 // dK/dV kernel, whose threads own key rows.  A 128 x 128 tile of bits is
 // 2 KB against 16 KB of mask bytes, so the kernels read an eighth of the
-// mask per pass, with one 16- or 8-byte load per row and tile.
+// mask per pass, with one 16- or 8-byte load per row and tile.  One byte per
+// 128 x 128 tile classifies it (nothing visible / some / all), so that the
+// kernels skip the tiles a sparse mask (documents, prefix-LM) hides.
 #include "kernels.h"
 #include "ptx.cuh"
 
@@ -27,8 +29,10 @@ constexpr int kPitch = 132;  // shared row pitch in bytes: column reads spread o
 // column for the transposed bits.
 __global__ void __launch_bounds__(256) mask_pack_kernel(const uint8_t* __restrict__ mask, int Nq, int Nk,
                                                         uint32_t* __restrict__ bits, int words,
-                                                        uint32_t* __restrict__ bits_t, int words_t) {
+                                                        uint32_t* __restrict__ bits_t, int words_t,
+                                                        uint8_t* __restrict__ flags) {
   __shared__ uint8_t tile[kTile * kPitch];
+  __shared__ int any_vis, all_vis;
   const int nqt = (Nq + kTile - 1) / kTile, nkt = (Nk + kTile - 1) / kTile;
   const int kt = (int)(blockIdx.x % nkt);
   const int qt = (int)((blockIdx.x / nkt) % nqt);
@@ -39,12 +43,33 @@ __global__ void __launch_bounds__(256) mask_pack_kernel(const uint8_t* __restric
     const int qi = qt * kTile + r, kj = kt * kTile + c;
     tile[r * kPitch + c] = (qi < Nq && kj < Nk) ? (src[(size_t)qi * Nk + kj] != 0) : 0;
   }
+  if (threadIdx.x == 0) {
+    any_vis = 0;
+    all_vis = 1;
+  }
   __syncthreads();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+  // Columns of word w that exist (keys < Nk).
+  const int kvalid = min(kTile, Nk - kt * kTile);
+  bool any = false, all = true;
   for (int rw = warp; rw < kTile * 4; rw += nw) {
     const int r = rw >> 2, w = rw & 3;
     const uint32_t word = __ballot_sync(0xffffffffu, tile[r * kPitch + 32 * w + lane] != 0);
-    if (lane == 0 && qt * kTile + r < Nq) bits[((size_t)plane * Nq + qt * kTile + r) * words + kt * 4 + w] = word;
+    if (qt * kTile + r < Nq) {
+      const int nb = min(32, max(0, kvalid - 32 * w));
+      const uint32_t valid = nb == 32 ? 0xffffffffu : ((1u << nb) - 1u);
+      any |= (word & valid) != 0;
+      all &= (word & valid) == valid;
+      if (lane == 0) bits[((size_t)plane * Nq + qt * kTile + r) * words + kt * 4 + w] = word;
+    }
+  }
+  if (flags != nullptr) {
+    // The tile's class for skipping: 0 = nothing visible, 1 = some, 2 = all.
+    if (lane == 0 && any) atomicOr(&any_vis, 1);
+    if (lane == 0 && !all) atomicAnd(&all_vis, 0);
+    __syncthreads();
+    if (threadIdx.x == 0)
+      flags[((size_t)plane * nqt + qt) * nkt + kt] = (uint8_t)(any_vis == 0 ? 0 : (all_vis ? 2 : 1));
   }
   if (bits_t != nullptr) {
     for (int cw = warp; cw < kTile * 4; cw += nw) {
@@ -59,10 +84,10 @@ __global__ void __launch_bounds__(256) mask_pack_kernel(const uint8_t* __restric
 }  // namespace
 
 cudaError_t launch_mask_pack(const uint8_t* mask, int mask_b, int mask_h, int Nq, int Nk, uint32_t* bits, int words,
-                             uint32_t* bits_t, int words_t, cudaStream_t stream) {
+                             uint32_t* bits_t, int words_t, uint8_t* flags, cudaStream_t stream) {
   const unsigned tiles = (unsigned)((Nq + kTile - 1) / kTile) * (unsigned)((Nk + kTile - 1) / kTile);
   mask_pack_kernel<<<tiles * (unsigned)(mask_b * mask_h), 256, 0, stream>>>(mask, Nq, Nk, bits, words, bits_t,
-                                                                            words_t);
+                                                                            words_t, flags);
   return cudaGetLastError();
 }
 

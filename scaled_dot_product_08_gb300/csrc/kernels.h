@@ -26,6 +26,8 @@ struct VarlenArgs {
 // bits_t: (planes, Nk, words_t), bit i % 32 of word i / 32 of a key row;
 // words / words_t are multiples of 4 (one 16-byte group per 128 columns).
 // plane = (mask_b > 1 ? b : 0) * mask_h + (mask_h > 1 ? h : 0).
+// flags: (planes, ceil(Nq/128), ceil(Nk/128)) bytes, one per 128 x 128 tile:
+// 0 = no visible entry (the tile is skipped), 1 = some, 2 = all.
 struct MaskArgs {
   int wl, wr;
   const int* key_len;
@@ -33,7 +35,16 @@ struct MaskArgs {
   const uint32_t* bits_t;
   int words, words_t;
   int mask_b, mask_h;
+  const uint8_t* flags;
+  int ftq, ftk;  // query and key tiles per plane in flags
 };
+
+// Most key tiles a masked forward / dQ CTA can list for skipping (its
+// shared-memory list of uint16 tile indices), and most (head, query tile)
+// steps a masked dK / dV CTA can list (uint32 entries).  Beyond these the
+// kernels visit every tile of their range without skipping.
+constexpr int kMaxTileList = 880;
+constexpr int kMaxStepList = 8192;
 
 // Forward kernel arguments (tensor maps are passed separately).
 struct FwdParams {
@@ -157,7 +168,7 @@ cudaError_t launch_bwd_dq(int d, bool causal, const CUtensorMap& tq, const CUten
 // Packs a boolean (mask_b, mask_h, Nq, Nk) byte mask into the row and
 // transposed bit layouts of MaskArgs (bits_t may be null: row bits only).
 cudaError_t launch_mask_pack(const uint8_t* mask, int mask_b, int mask_h, int Nq, int Nk, uint32_t* bits,
-                             int words, uint32_t* bits_t, int words_t, cudaStream_t stream);
+                             int words, uint32_t* bits_t, int words_t, uint8_t* flags, cudaStream_t stream);
 cudaError_t launch_decode(int d, bool causal, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                           const DecParams& p, cudaStream_t stream);
 

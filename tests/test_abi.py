@@ -209,7 +209,7 @@ def test_masked_rejects_bad_arguments(lib):
     assert f(M(m=FAKE, mb=3)) == S.INVALID_ARG               # mask batch must be 1 or B
     assert f(M(m=FAKE, mh=2)) == S.INVALID_ARG               # mask heads must be 1 or H
     need = sdpa.attn_masked_workspace_size(2, 4, 2, 100, 300, 128, M(m=FAKE, mb=2), 0)
-    assert need == 2 * 100 * 12 * 4                          # one bit per (query, key), 16-byte groups
+    assert need == 2 * 100 * 12 * 4 + 16                     # one bit per (query, key) + tile flags
     assert f(M(m=FAKE, mb=2), wsb=need - 1) == S.WORKSPACE
     assert f(M(m=FAKE, mb=2), ws=0) == S.WORKSPACE
     assert sdpa.attn_masked_workspace_size(2, 4, 2, 100, 300, 128, M(), 0) == 0

@@ -62,6 +62,9 @@ CASES = [
     ((2, 2, 2, 512, 512, 128), False, None, None, "documents"),     # block-diagonal document mask
     ((2, 4, 2, 200, 600, 128), True, (250, -1), [600, 450], "batch"),  # all of it, Nq < Nk
     ((1, 2, 2, 300, 150, 64), True, None, None, None),              # causal with Nq > Nk: rows without keys
+    ((1, 4, 2, 1536, 1536, 128), False, None, None, "doc3"),        # 3 documents: most tiles skipped
+    ((2, 2, 2, 1024, 1024, 128), False, None, None, "prefix"),      # prefix-LM
+    ((1, 2, 1, 1000, 1000, 96), True, (200, -1), None, "doc3"),     # documents, causal, window
 ]
 
 
@@ -77,6 +80,16 @@ def _mask(kind, B, H, Nq, Nk, seed):
             for a, e in zip(edges, edges[1:]):
                 m[b, 0, a:e, a:e] = True
         return m
+    if kind == "doc3":  # three documents of uneven lengths, one plane for all (b, h)
+        m = np.zeros((1, 1, Nq, Nk), dtype=bool)
+        edges = [0, Nq // 5, (3 * Nq) // 5, Nq]
+        for a, e in zip(edges, edges[1:]):
+            m[0, 0, a:e, a:e] = True
+        return m
+    if kind == "prefix":  # prefix-LM over the first quarter
+        i = np.arange(Nq)[:, None]
+        j = np.arange(Nk)[None, :]
+        return ((j < Nk // 4) | (j <= i))[None, None]
     shape = {"batch": (B, 1, Nq, Nk), "full": (B, H, Nq, Nk), "shared": (1, 1, Nq, Nk)}[kind]
     return rng.random(shape) < 0.7
 
