@@ -77,6 +77,8 @@ def workload_desc(w):
         return (f"{w.name}: B={w.B} H={w.H} Hkv={w.Hkv} Nq={w.n_queries} Nk={w.N} d={w.d} "
                 f"{'causal' if w.causal else 'non-causal'} {what}")
     tail = f" (head_dim {w.d_draw} zero-padded)" if w.d_draw else ""
+    if w.kind == "fp8":
+        tail += " e4m3 inputs (per-tensor scales)"
     return (f"{w.name}: B={w.B} H={w.H} Hkv={w.Hkv} N={w.N} d={w.d}{tail} "
             f"{'causal' if w.causal else 'non-causal'} {'fwd+bwd' if w.with_grad else 'fwd'}")
 
@@ -356,6 +358,10 @@ def run_ours(args, w, rank, world, local_rank):
     else:
         x = make_inputs(w)
         lse_shape = (B, H, Nq)
+    fp8 = None
+    if w.kind == "fp8":
+        from sdpa_inputs import quantize_e4m3
+        fp8 = [quantize_e4m3(x[n]) for n in ("q", "k", "v")]  # (bytes, scale) each
     mask_spec = None
     if w.kind == "masked":
         from sdpa_inputs import prefix_lm_mask
@@ -367,9 +373,13 @@ def run_ours(args, w, rank, world, local_rank):
         mws_f = sdpa.attn_masked_workspace_size(B, H, Hkv, Nq, N, d, mask_spec, 0)
         mws_b = sdpa.attn_masked_workspace_size(B, H, Hkv, Nq, N, d, mask_spec, 1)
         mws = torch.empty(max(mws_f, mws_b, 16), dtype=torch.uint8, device="cuda")
-    q, k, v = dev(x["q"]), dev(x["k"]), dev(x["v"])
+    if fp8 is not None:
+        q, k, v = (torch.from_numpy(b).cuda() for b, _ in fp8)
+        o = torch.empty(q.shape, dtype=torch.bfloat16, device="cuda")
+    else:
+        q, k, v = dev(x["q"]), dev(x["k"]), dev(x["v"])
+        o = torch.empty_like(q)
     do = dev(x["do"]) if w.with_grad else None
-    o = torch.empty_like(q)
     lse = torch.empty(lse_shape, dtype=torch.float32, device="cuda")
     if w.with_grad:
         dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
@@ -397,6 +407,10 @@ def run_ours(args, w, rank, world, local_rank):
                                                      N, N, maxlen, maxlen, d, s, w.causal, sp), "attn_fwd_varlen")]
         if w.with_grad:
             launches += [vstage(1), vstage(2), vstage(4)]
+    elif w.kind == "fp8":
+        (_, qsc), (_, ksc), (_, vsc) = fp8
+        launches = [lambda: chk(sdpa.attn_fwd_fp8(P(q), P(k), P(v), P(o), P(lse), B, H, Hkv, Nq, N, d, s, qsc, ksc,
+                                                  vsc, w.causal, sp), "attn_fwd_fp8")]
     elif w.kind == "masked":
         def mstage(mask):
             return lambda: chk(sdpa.attn_bwd_masked_stages(
@@ -506,9 +520,11 @@ def run_ours(args, w, rank, world, local_rank):
     if dom in kflops:
         achieved = kflops[dom] / (per_kernel[dom] / 1e3) / 1e12
         peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+        src, nominal = f"{peak_src} bf16 burst (cuBLAS 8192^3)", 2250.0
+        if w.kind == "fp8":  # the FP8 peak: the measured bf16 burst times the nominal ratio 4.5 / 2.25
+            peak, src, nominal = 2.0 * peak, f"2 x {peak_src} bf16 burst (nominal fp8 / bf16 ratio 4.5 / 2.25)", 4500.0
         roof = {"kernel": dom, "bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                "frac": achieved / peak, "peak_source": f"{peak_src} bf16 burst (cuBLAS 8192^3)",
-                "frac_of_nominal_2250": achieved / 2250.0}
+                "frac": achieved / peak, "peak_source": src, f"frac_of_nominal_{int(nominal)}": achieved / nominal}
     else:
         nbytes = {"attn_bwd_prep": 2 * B * H * Nq * d * 2 + B * H * Nq * 4 + B * H * Nq * 2 * 4}[dom]
         achieved = nbytes / (per_kernel[dom] / 1e3) / 1e9
@@ -558,7 +574,9 @@ def run_ours(args, w, rank, world, local_rank):
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": args.warmup,
             "ms_per_step": ms / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": "bf16", "data": "synthetic (seeded N(0,1) draws rounded to bf16)",
+            "dtype": "e4m3 (fp32 accumulate, bf16 O)" if w.kind == "fp8" else "bf16",
+            "data": ("synthetic (seeded N(0,1) draws, quantised per tensor to e4m3)" if w.kind == "fp8"
+                     else "synthetic (seeded N(0,1) draws rounded to bf16)"),
             "config": {"workload": workload_desc(w), "B": B, "H": H, "Hkv": Hkv, "N": N, "d": d,
                        "causal": w.causal, "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                        "l2": l2_note},

@@ -27,7 +27,7 @@ __all__ = [
     "attn_bwd_grad_cross", "attn_bwd_dq_cross", "attn_fwd_varlen", "attn_bwd_varlen",
     "attn_bwd_varlen_workspace_size", "attn_bwd_varlen_stages", "forward_varlen", "backward_varlen",
     "AttnMask", "attn_masked_workspace_size", "attn_fwd_masked", "attn_bwd_masked", "attn_bwd_masked_stages",
-    "forward_masked", "backward_masked",
+    "forward_masked", "backward_masked", "attn_fwd_fp8", "forward_fp8",
     "forward", "forward_cross", "backward", "backward_cross", "decode", "build",
 ]
 
@@ -110,6 +110,9 @@ def load() -> ctypes.CDLL:
                                                _I, _I, _I, _I, _I, _I, _I, _I, ctypes.c_float, _I, ctypes.c_uint,
                                                _P]
         lib.attn_bwd_varlen_stages.restype = _I
+        _F = ctypes.c_float
+        lib.attn_fwd_fp8.argtypes = [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _F, _F, _F, _I, _P]
+        lib.attn_fwd_fp8.restype = _I
         _M = ctypes.POINTER(AttnMask)
         lib.attn_masked_workspace_size.argtypes = [_I, _I, _I, _I, _I, _I, _M, _I]
         lib.attn_masked_workspace_size.restype = ctypes.c_size_t
@@ -221,6 +224,11 @@ def attn_bwd_varlen_stages(q, k, v, o, lse, dout, dq, dk, dv, cu_q, cu_k, worksp
     return load().attn_bwd_varlen_stages(q, k, v, o, lse, dout, dq, dk, dv, cu_q, cu_k, workspace, workspace_bytes,
                                          B, H, Hkv, total_q, total_k, max_q, max_k, d, scale, causal, stages,
                                          stream)
+
+
+def attn_fwd_fp8(q, k, v, o, lse, B, H, Hkv, Nq, Nk, d, scale, q_scale, k_scale, v_scale, causal, stream) -> int:
+    return load().attn_fwd_fp8(q, k, v, o, lse, B, H, Hkv, Nq, Nk, d, scale, q_scale, k_scale, v_scale, causal,
+                               stream)
 
 
 def attn_masked_workspace_size(B, H, Hkv, Nq, Nk, d, mask: AttnMask, backward) -> int:
@@ -547,3 +555,25 @@ def backward_masked(q, k, v, o, lse, dout, scale: float | None = None, causal: b
                            dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, Hkv, Nq, Nk, d, scale, causal, m,
                            ws.data_ptr(), ws.numel(), _stream_ptr(q)), "attn_bwd_masked")
     return dq, dk, dv
+
+
+def forward_fp8(q8, k8, v8, q_scale: float, k_scale: float, v_scale: float, scale: float | None = None,
+                causal: bool = False):
+    """O (bf16), lse of attention on e4m3 inputs: q8 (B, H, Nq, 128), k8, v8
+    (B, Hkv, Nk, 128) uint8 CUDA tensors holding e4m3 bytes, each with its
+    dequantisation factor."""
+    import torch
+    for t in (q8, k8, v8):
+        if t.dim() != 4 or t.dtype != torch.uint8 or not t.is_contiguous() or not t.is_cuda:
+            raise ValueError("q8, k8, v8 must be contiguous 4-D uint8 CUDA tensors of e4m3 bytes")
+    B, H, Nq, d = q8.shape
+    Hkv, Nk = k8.shape[1], k8.shape[2]
+    if tuple(k8.shape) != (B, Hkv, Nk, d) or tuple(v8.shape) != (B, Hkv, Nk, d):
+        raise ValueError("k8 and v8 must be (B, Hkv, Nk, d) with q8's B and d")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    o = torch.empty((B, H, Nq, d), dtype=torch.bfloat16, device=q8.device)
+    lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q8.device)
+    _check(attn_fwd_fp8(q8.data_ptr(), k8.data_ptr(), v8.data_ptr(), o.data_ptr(), lse.data_ptr(), B, H, Hkv, Nq, Nk,
+                        d, scale, q_scale, k_scale, v_scale, causal, _stream_ptr(q8)), "attn_fwd_fp8")
+    return o, lse

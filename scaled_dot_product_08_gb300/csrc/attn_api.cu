@@ -133,6 +133,20 @@ bool make_map_bf16_packed(CUtensorMap* m, const void* ptr, int d, long long tota
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 3-D map over a dense e4m3 (rows = B*heads, N, 128) byte tensor: box of 128
+// bytes x 128 rows x 1 head (one 128-byte swizzle block).
+bool make_map_e4m3(CUtensorMap* m, const void* ptr, int N, long long heads) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {128, (cuuint64_t)N, (cuuint64_t)heads};
+  cuuint64_t strides[2] = {128, 128 * (cuuint64_t)N};
+  cuuint32_t box[3] = {128, 128, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(ptr), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 // Shape checks shared by forward and backward.
@@ -596,6 +610,48 @@ attn_status_t attn_bwd_varlen_stages(const void* q, const void* k, const void* v
   if (stages == 0 || (stages & ~7u) != 0) return ATTN_ERR_INVALID_ARG;
   return varlen_bwd_run(q, k, v, o, lse, dout, dq, dk, dv, cu_seqlens_q, cu_seqlens_k, workspace, workspace_bytes,
                         B, H, Hkv, total_q, total_k, max_seqlen_q, max_seqlen_k, d, scale, causal, stream, stages);
+}
+
+// ------------------------------------------------------------------ FP8
+attn_status_t attn_fwd_fp8(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Hkv,
+                           int Nq, int Nk, int d, float scale, float q_scale, float k_scale, float v_scale, int causal,
+                           void* stream) {
+  ATTN_TRY(check_shape(B, H, Hkv, Nq, d));
+  ATTN_TRY(check_shape(B, H, Hkv, Nk, d));
+  if (d != 128) return ATTN_ERR_UNSUPPORTED_SHAPE;
+  ATTN_TRY(check_scale_flag(scale, causal));
+  for (float f : {q_scale, k_scale, v_scale})
+    if (!std::isfinite(f) || !(f > 0.f)) return ATTN_ERR_INVALID_ARG;
+  if (!std::isfinite(scale * q_scale * k_scale * 1.4426950408889634f)) return ATTN_ERR_INVALID_ARG;
+  if (causal && Nq > Nk) return ATTN_ERR_UNSUPPORTED_SHAPE;
+  ATTN_TRY(check_ptrs({q, k, v, o, lse}));
+  DeviceInfo* di = nullptr;
+  ATTN_TRY(current_device(&di));
+  CUtensorMap tq, tk, tv;
+  if (!make_map_e4m3(&tq, q, Nq, (long long)B * H) || !make_map_e4m3(&tk, k, Nk, (long long)B * Hkv) ||
+      !make_map_e4m3(&tv, v, Nk, (long long)B * Hkv))
+    return ATTN_ERR_CUDA;
+  sdpa::FwdParams p;
+  memset(&p, 0, sizeof(p));
+  p.lse = lse;
+  p.B = B;
+  p.H = H;
+  p.Hkv = Hkv;
+  p.G = H / Hkv;
+  p.Nq = Nq;
+  p.Nk = Nk;
+  p.koff = causal ? Nk - Nq : 0;
+  p.n_mtiles = (Nq + 255) / 256;
+  p.nkv = (Nk + 127) / 128;
+  p.scale_log2 = scale * q_scale * k_scale * 1.4426950408889634f;
+  p.o_scale = v_scale;
+  p.o = static_cast<uint16_t*>(o);
+  p.status = di->status;
+  p.limit_ns = wait_limit_ns();
+  p.info = di->info;
+  return sdpa::launch_fwd_fp8(causal != 0, tq, tk, tv, p, static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? ATTN_OK
+             : ATTN_ERR_LAUNCH;
 }
 
 // ------------------------------------------------------------------ masks

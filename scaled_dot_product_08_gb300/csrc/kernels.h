@@ -59,8 +59,9 @@ struct FwdParams {
   unsigned long long limit_ns;  // bounded-wait limit
   int* info;             // first-timeout record (4 ints)
   VarlenArgs vl;         // varlen: Nq / Nk above are the longest sequences
-  uint16_t* o;           // varlen: O base, for the rows of a sequence's last tile
+  uint16_t* o;           // varlen: O base, for the rows of a sequence's last tile; FP8: O base
   MaskArgs mk;           // masked instances only
+  float o_scale;         // FP8: V's dequantisation factor, applied to O
 };
 
 // Backward arguments.
@@ -157,6 +158,11 @@ size_t decode_smem_bytes(int d);
 // masked: the instance that applies p.mk (causal then enters as wr = 0).
 cudaError_t launch_fwd(int d, bool causal, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                        const CUtensorMap& to, const FwdParams& p, cudaStream_t stream, bool masked = false);
+
+// FP8 (e4m3) forward, head_dim 128, dense (B, H, N, 128) e4m3 Q, K, V (maps
+// of bytes), O bf16 through p.o; p.scale_log2 carries q_scale * k_scale.
+cudaError_t launch_fwd_fp8(bool causal, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                           const FwdParams& p, cudaStream_t stream);
 
 cudaError_t launch_bwd_prep(const BwdParams& p, cudaStream_t stream);
 cudaError_t launch_bwd_grad(int d, bool causal, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,

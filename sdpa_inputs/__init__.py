@@ -44,6 +44,9 @@ backward, self-attention (the same lengths for queries and keys):
        Tensors are packed token-major: (total, heads, d).  The draws of Q,
        K, V, dO use default_rng(seed + 1000) in that order.
 
+FP8 forward (attn_fwd_fp8): c4f8 is c4's draw (seed 4, x0.5) quantised per
+tensor to e4m3 (quantize_e4m3: scale = amax / 448).
+
 Masked workloads (attn_fwd_masked / attn_bwd_masked), forward + backward:
 
   sw1  B=1  H=32  Hkv=8  N=16384 d=128  causal sliding window of 4096 keys
@@ -79,7 +82,8 @@ class Workload:
     scale: float | None = None     # default 1/sqrt(d_draw or d)
     Nq: int | None = None          # decode / cross: query rows per head (None: Nq = N)
     kind: str = "full"             # "full" (Nq = N), "decode" (attn_decode), "cross" (attn_fwd_cross),
-                                   # "varlen" (attn_fwd_varlen: N = total tokens, B = 1)
+                                   # "varlen" (attn_fwd_varlen: N = total tokens, B = 1), "masked",
+                                   # "fp8" (attn_fwd_fp8 on e4m3 inputs)
     len_range: tuple[int, int] | None = None  # varlen: sequence lengths drawn from [lo, hi]
     window: tuple[int, int] | None = None     # masked: (left, right), -1 = open
     prefix: int | None = None                 # masked: prefix-LM boolean mask with this prefix
@@ -112,6 +116,7 @@ WORKLOADS: dict[str, Workload] = {
     "cp1": Workload("cp1", 1, 32, 8, 16384, 128, True, 8, Nq=2048, kind="cross"),
     "cx": Workload("cx", 8, 16, 16, 4096, 128, False, 9, with_grad=True, Nq=2048, kind="cross"),
     "vl1": Workload("vl1", 1, 16, 16, 32768, 128, True, 10, with_grad=True, kind="varlen", len_range=(128, 8192)),
+    "c4f8": Workload("c4f8", 1, 32, 8, 8192, 128, True, 4, amp=0.5, kind="fp8"),
     "sw1": Workload("sw1", 1, 32, 8, 16384, 128, True, 11, with_grad=True, kind="masked", window=(4095, -1)),
     "pl1": Workload("pl1", 8, 16, 16, 4096, 128, False, 12, with_grad=True, kind="masked", prefix=1024),
 }
@@ -243,3 +248,53 @@ def flops_forward(B: int, H: int, N: int, d: int, causal: bool) -> float:
 def flops_backward(B: int, H: int, N: int, d: int, causal: bool) -> float:
     """Backward work convention: 2.5x the forward."""
     return 2.5 * flops_forward(B, H, N, d, causal)
+
+
+# ---------------------------------------------------------------- e4m3 inputs
+# FP8 e4m3 (the "fn" variant: 1 sign bit, 4 exponent bits with bias 7, 3
+# mantissa bits, no infinities, S.1111.111 is NaN, largest value 448,
+# subnormals m / 8 * 2^-6).  Input preparation only: the FP8 forward takes
+# e4m3 tensors with one dequantisation factor each.
+E4M3_MAX = 448.0
+
+
+def e4m3_encode(x: np.ndarray) -> np.ndarray:
+    """float -> e4m3 bytes: round to nearest, ties to even, saturating at
+    +-448 (finite inputs)."""
+    x = np.asarray(x, dtype=np.float64)
+    sign = (np.signbit(x)).astype(np.uint8) << 7
+    a = np.minimum(np.abs(x), E4M3_MAX)
+    with np.errstate(divide="ignore"):
+        e = np.floor(np.log2(np.where(a > 0, a, 1.0)))
+    e = np.clip(e, -6, 8)                       # -6: the subnormal binade shares the smallest exponent
+    q = a / np.exp2(e - 3)                      # significand in units of the last place: [8, 16) or [0, 8)
+    qr = np.round(q)                            # numpy rounds half to even
+    carry = qr >= 16
+    e = np.where(carry, e + 1, e)
+    qr = np.where(carry, 8, qr)
+    over = (e > 8) | ((e == 8) & (qr > 14))     # beyond 448 = 1.75 * 2^8: saturate
+    e = np.where(over, 8, e)
+    qr = np.where(over, 14, qr)
+    normal = qr >= 8
+    code = np.where(normal, ((e + 7).astype(np.int64) << 3) | (qr.astype(np.int64) - 8), qr.astype(np.int64))
+    return (code.astype(np.uint8) | sign).astype(np.uint8)
+
+
+def e4m3_decode(b: np.ndarray) -> np.ndarray:
+    """e4m3 bytes -> float64 (NaN for S.1111.111)."""
+    b = np.asarray(b, dtype=np.uint8).astype(np.int64)
+    s = np.where(b & 0x80, -1.0, 1.0)
+    E = (b >> 3) & 0xF
+    M = b & 0x7
+    val = np.where(E == 0, M * 2.0 ** -9, (8 + M) * np.exp2(E - 10.0))
+    val = np.where((E == 15) & (M == 7), np.nan, val)
+    return s * val
+
+
+def quantize_e4m3(x: np.ndarray):
+    """Per-tensor e4m3 quantisation: scale = amax / 448, bytes = e4m3(x /
+    scale).  Returns (bytes, scale); the tensor the FP8 path computes with is
+    e4m3_decode(bytes) * scale."""
+    amax = float(np.max(np.abs(x)))
+    scale = np.float32(amax / E4M3_MAX if amax > 0 else 1.0)
+    return e4m3_encode(np.asarray(x, dtype=np.float64) / float(scale)), float(scale)

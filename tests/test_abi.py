@@ -220,3 +220,16 @@ def test_masked_rejects_bad_arguments(lib):
         stages, None)
     assert g(0) == S.INVALID_ARG and g(8) == S.INVALID_ARG
     assert g(7, wsb=16) == S.WORKSPACE
+
+
+def test_fp8_rejects_bad_arguments(lib):
+    import scaled_dot_product_08_gb300 as sdpa
+    S = sdpa.Status
+    f = lambda d=128, scale=0.1, qs=1.0, ks=1.0, vs=1.0, causal=0, Nq=100, Nk=200: sdpa.attn_fwd_fp8(
+        FAKE, FAKE, FAKE, FAKE, FAKE, 1, 4, 2, Nq, Nk, d, scale, qs, ks, vs, causal, None)
+    assert f(d=64) == S.UNSUPPORTED_SHAPE
+    assert f(qs=0.0) == S.INVALID_ARG
+    assert f(vs=float("inf")) == S.INVALID_ARG
+    assert f(ks=-1.0) == S.INVALID_ARG
+    assert f(scale=float("nan")) == S.INVALID_ARG
+    assert f(causal=1, Nq=300, Nk=200) == S.UNSUPPORTED_SHAPE
