@@ -43,41 +43,60 @@
 namespace sdpa {
 
 // ------------------------------------------------------------------ preprocess
-// One warp per (head, padded row).  Row i < N: stores -D = -(dO_i . O_i)
-// (fp32) and -lse_i * log2(e).  Row i >= N: -D = 0 and -lse2 = -inf (so P = 0
+// Row i < N of each (head, padded row) gets -D = -(dO_i . O_i) (fp32) and
+// -lse_i * log2(e); rows i >= N get -D = 0 and -lse2 = -inf (so P = 0
 // there).  The negated values let the other kernels form P and dP - D with
-// one packed FMA / add per pair.
+// one packed FMA / add per pair.  A row that saw no key (lse = -inf, masked
+// calls only) also gets -lse2 = -inf, so P = 0 on it.
+// HBM-bound (reads O and dO once): LPR lanes take one row, 16 bytes of O and
+// dO each, so a warp covers 32 / LPR rows per pass, and every thread issues
+// the loads of all its PRE_IT passes before it uses any of them.
+constexpr int PRE_IT = 4;
+
+template <int LPR>
 __global__ void __launch_bounds__(256) bwd_pre_kernel(const BwdParams p) {
+  constexpr int RPW = 32 / LPR;  // rows per warp and pass
   const long long rows = (long long)p.B * p.H * p.Npad;
-  const long long row = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
-  const int lane = threadIdx.x & 31;
-  if (row >= rows) return;
-  const long long bh = row / p.Npad;
-  const int i = (int)(row % p.Npad);
-  float dot = 0.f;
-  if (i < p.N) {
-    const size_t off = ((size_t)bh * p.N + i) * p.d;
-    if (lane * 8 < p.d) {
-      const uint4 o = *reinterpret_cast<const uint4*>(p.o + off + lane * 8);
-      const uint4 g = *reinterpret_cast<const uint4*>(p.dout + off + lane * 8);
-      const uint32_t ow[4] = {o.x, o.y, o.z, o.w}, gw[4] = {g.x, g.y, g.z, g.w};
+  const int lane = threadIdx.x & 31, sub = lane / LPR, c = lane % LPR;
+  const long long row0 = ((long long)blockIdx.x * 8 + (threadIdx.x >> 5)) * (RPW * PRE_IT);
+  if (row0 >= rows) return;
+  // A warp's RPW * PRE_IT (8 or 16) rows lie in one head: Npad is a multiple
+  // of 128.  One division per thread.
+  const long long bh = row0 / p.Npad;
+  const int i0 = (int)(row0 - bh * p.Npad) + sub;
+  const size_t base = ((size_t)bh * p.N) * p.d + c * 8;
+  uint4 o[PRE_IT], g[PRE_IT];
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const float2 of = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&ow[e]));
-        const float2 gf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&gw[e]));
-        dot = fmaf(of.x, gf.x, dot);
-        dot = fmaf(of.y, gf.y, dot);
-      }
+  for (int it = 0; it < PRE_IT; ++it) {
+    const int i = i0 + it * RPW;
+    o[it] = make_uint4(0, 0, 0, 0);
+    g[it] = make_uint4(0, 0, 0, 0);
+    if (i < p.N && c * 8 < p.d) {
+      const size_t off = base + (size_t)i * p.d;
+      o[it] = *reinterpret_cast<const uint4*>(p.o + off);
+      g[it] = *reinterpret_cast<const uint4*>(p.dout + off);
+    }
+  }
+#pragma unroll
+  for (int it = 0; it < PRE_IT; ++it) {
+    const uint32_t ow[4] = {o[it].x, o[it].y, o[it].z, o[it].w}, gw[4] = {g[it].x, g[it].y, g[it].z, g[it].w};
+    float dot = 0.f;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float2 of = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&ow[e]));
+      const float2 gf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&gw[e]));
+      dot = fmaf(of.x, gf.x, dot);
+      dot = fmaf(of.y, gf.y, dot);
     }
 #pragma unroll
-    for (int s = 16; s > 0; s >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, s);
-  }
-  if (lane == 0) {
-    // A row that saw no key (lse = -inf, masked calls only) also gets
-    // -lse2 = -inf, so P = 0 on it.
-    const float l = (i < p.N) ? p.lse[(size_t)bh * p.N + i] : -INFINITY;
-    p.dvec[row] = (i < p.N) ? -dot : 0.f;
-    p.lse2[row] = (l == -INFINITY) ? -INFINITY : -l * 1.4426950408889634f;
+    for (int s = LPR / 2; s > 0; s >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, s);
+    const long long row = row0 + it * RPW + sub;
+    const int i = i0 + it * RPW;
+    if (c == 0 && row < rows) {
+      const float l = (i < p.N) ? p.lse[(size_t)bh * p.N + i] : -INFINITY;
+      p.dvec[row] = (i < p.N) ? -dot : 0.f;
+      p.lse2[row] = (l == -INFINITY) ? -INFINITY : -l * 1.4426950408889634f;
+    }
   }
 }
 
@@ -689,8 +708,15 @@ cudaError_t launch_bwd_prep(const BwdParams& p, cudaStream_t stream) {
   if (p.vl.cu_q != nullptr) {
     bwd_pre_varlen_kernel<<<(unsigned)p.nq * (unsigned)(p.B * p.H), 256, 0, stream>>>(p);
   } else {
+    // 16 lanes per row for d = 96, 128 (12 of them busy at 96), 8 for d = 64.
     const long long rows = (long long)p.B * p.H * p.Npad;
-    bwd_pre_kernel<<<(unsigned)((rows + 7) / 8), 256, 0, stream>>>(p);
+    if (p.d == 64) {
+      const long long per_block = 8LL * (32 / 8) * PRE_IT;
+      bwd_pre_kernel<8><<<(unsigned)((rows + per_block - 1) / per_block), 256, 0, stream>>>(p);
+    } else {
+      const long long per_block = 8LL * (32 / 16) * PRE_IT;
+      bwd_pre_kernel<16><<<(unsigned)((rows + per_block - 1) / per_block), 256, 0, stream>>>(p);
+    }
   }
   return cudaGetLastError();
 }
