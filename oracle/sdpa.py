@@ -272,18 +272,18 @@ def merge_splits(O_parts, lse_parts):
     return O, lse
 
 
-def attention_forward_rows(qh, kh, vh, rows, scale, causal=False):
+def attention_forward_rows(qh, kh, vh, rows, scale, causal=False, q_offset=0):
     """Forward for a subset of absolute query rows of ONE head.
 
     Same definition as ``attention_forward``; the causal mask uses the
-    absolute row indices, so sampled rows of a full-size head can be checked
-    one by one.  qh: (N, d), kh/vh: (Nk, d).  Returns O (len(rows), d_v),
-    lse (len(rows),)."""
+    absolute row indices (query row i at position q_offset + i), so sampled
+    rows of a full-size head can be checked one by one.  qh: (N, d), kh/vh:
+    (Nk, d).  Returns O (len(rows), d_v), lse (len(rows),)."""
     qh = np.asarray(qh, dtype=np.float64)
     kh = np.asarray(kh, dtype=np.float64)
     vh = np.asarray(vh, dtype=np.float64)
     rows = np.asarray(rows)
-    S = _scores(qh, kh, scale, causal, rows)
+    S = _scores(qh, kh, scale, causal, rows, q_offset=q_offset)
     P, m, l = softmax_rows(S)
     return P @ vh, m + np.log(l)
 

@@ -186,6 +186,13 @@ def test_rows_variant_matches_full():
         Or, lr = oracle.attention_forward_rows(q[0, 0], k[0, 0], v[0, 0], rows, 0.2, causal)
         np.testing.assert_allclose(Or, O[0, 0, rows], rtol=0, atol=1e-14)
         np.testing.assert_allclose(lr, lse[0, 0, rows], rtol=0, atol=1e-14)
+    # with the rows placed later in the key sequence (query i at position 30 + i)
+    qs = q[:, :, :40]
+    O, lse = oracle.attention_forward(qs, k, v, 0.2, True, q_offset=30)
+    rows = np.array([0, 7, 39])
+    Or, lr = oracle.attention_forward_rows(qs[0, 0], k[0, 0], v[0, 0], rows, 0.2, True, q_offset=30)
+    np.testing.assert_allclose(Or, O[0, 0, rows], rtol=0, atol=1e-14)
+    np.testing.assert_allclose(lr, lse[0, 0, rows], rtol=0, atol=1e-14)
 
 
 # --------------------------------------------------------------- backward pins
