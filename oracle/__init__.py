@@ -30,6 +30,7 @@ from .sdpa import (
     attention_forward_online,
     attention_backward,
     attention_decode,
+    attention_decode_paged,
     attention_cross_backward,
     attention_varlen_forward,
     attention_varlen_backward,
@@ -50,6 +51,7 @@ __all__ = [
     "attention_forward_online",
     "attention_backward",
     "attention_decode",
+    "attention_decode_paged",
     "attention_cross_backward",
     "attention_varlen_forward",
     "attention_varlen_backward",

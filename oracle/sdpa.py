@@ -251,6 +251,31 @@ def attention_cross_backward(q, k, v, do, scale=None, causal=False):
     return attention_backward(q, k, v, do, scale, causal, q_offset=Nk - Nq)
 
 
+def attention_decode_paged(q, k_cache, v_cache, block_table, seq_lens, scale=None, causal=False):
+    """Decode against a paged KV cache ([FA] FAQ Q12-Q13: the KV cache with
+    PagedAttention, the cache kept in fixed-size pages found through a block
+    table).  Batch element b's cached keys are the first seq_lens[b] tokens
+    of its pages block_table[b, 0], block_table[b, 1], ..., in that order;
+    k_cache, v_cache: (num_pages, page_size, Hkv, d).  The keys are gathered
+    into one sequence per batch element and ``attention_decode`` applies.
+    Returns O (B, H, Nq, d_v) and lse (B, H, Nq)."""
+    q = np.asarray(q, dtype=np.float64)
+    k_cache = np.asarray(k_cache, dtype=np.float64)
+    v_cache = np.asarray(v_cache, dtype=np.float64)
+    B, H, Nq, _ = q.shape
+    ps = k_cache.shape[1]
+    O = np.zeros((B, H, Nq, v_cache.shape[3]))
+    lse = np.full((B, H, Nq), -np.inf)
+    for b in range(B):
+        L = int(seq_lens[b])
+        npg = -(-L // ps)
+        pages = [int(x) for x in np.asarray(block_table)[b, :npg]]
+        kb = k_cache[pages].reshape(npg * ps, *k_cache.shape[2:])[:L].transpose(1, 0, 2)[None]
+        vb = v_cache[pages].reshape(npg * ps, *v_cache.shape[2:])[:L].transpose(1, 0, 2)[None]
+        O[b:b + 1], lse[b:b + 1] = attention_decode(q[b:b + 1], kb, vb, scale, causal)
+    return O, lse
+
+
 def merge_splits(O_parts, lse_parts):
     """Combine attention computed over disjoint key ranges ("splits").
 

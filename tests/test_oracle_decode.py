@@ -138,3 +138,53 @@ def test_planted_merge_mistake_is_caught():
     assert np.abs(wrong - O_full).max() > 1e-3
     right, _ = oracle.merge_splits([p[0] for p in parts], [p[1] for p in parts])
     assert np.abs(right - O_full).max() < 1e-13
+
+
+# ----------------------------------------------------------------- paged cache
+def _paged(k, v, page_size, order, max_pages):
+    """Store contiguous (B, Hkv, N, d) K / V into a page pool: logical page i
+    of batch element b goes to physical page order[b * max_pages + i]."""
+    B, Hkv, N, d = k.shape
+    num_pages = B * max_pages
+    kc = np.zeros((num_pages, page_size, Hkv, d))
+    vc = np.zeros((num_pages, page_size, Hkv, d))
+    table = np.full((B, max_pages), -1, dtype=np.int64)
+    for b in range(B):
+        for i in range(-(-N // page_size)):
+            phys = order[b * max_pages + i]
+            table[b, i] = phys
+            seg = slice(i * page_size, min(N, (i + 1) * page_size))
+            n = seg.stop - seg.start
+            kc[phys, :n] = k[b, :, seg].transpose(1, 0, 2)
+            vc[phys, :n] = v[b, :, seg].transpose(1, 0, 2)
+    return kc, vc, table
+
+
+@pytest.mark.parametrize("page_size", [4, 16])
+@pytest.mark.parametrize("causal", [False, True])
+def test_paged_decode_equals_contiguous_decode(page_size, causal):
+    B, H, Hkv, Nq, N, d = 3, 4, 2, 2, 37, 8
+    q, k, v = _qkv(B, H, Hkv, Nq, N, d, 70)
+    max_pages = -(-N // page_size) + 2
+    order = np.random.default_rng(71).permutation(B * max_pages)   # pages scattered over the pool
+    kc, vc, table = _paged(k, v, page_size, order, max_pages)
+    lens = np.array([N, 23, 5])
+    O, lse = oracle.attention_decode_paged(q, kc, vc, table, lens, 0.3, causal)
+    for b in range(B):
+        L = lens[b]
+        Or, lr = oracle.attention_decode(q[b:b + 1], k[b:b + 1, :, :L], v[b:b + 1, :, :L], 0.3, causal)
+        np.testing.assert_allclose(O[b], Or[0], rtol=0, atol=1e-13)
+        np.testing.assert_allclose(lse[b], lr[0], rtol=0, atol=1e-13)
+
+
+def test_planted_page_order_mistake_is_caught():
+    # Reading logical page i from physical page i (ignoring the table) is a
+    # plausible mistake; with scattered pages it changes the result.
+    B, H, Hkv, Nq, N, d, ps = 1, 2, 1, 1, 32, 4, 8
+    q, k, v = _qkv(B, H, Hkv, Nq, N, d, 80)
+    order = np.array([3, 0, 2, 1])
+    kc, vc, table = _paged(k, v, ps, order, 4)
+    right, _ = oracle.attention_decode_paged(q, kc, vc, table, [N], 0.5)
+    wrong, _ = oracle.attention_decode_paged(q, kc, vc, np.arange(4)[None], [N], 0.5)
+    ref, _ = oracle.attention_decode(q, k, v, 0.5)
+    assert np.abs(right - ref).max() < 1e-13 and np.abs(wrong - ref).max() > 1e-3
