@@ -179,12 +179,14 @@ def test_paged_decode_equals_contiguous_decode(page_size, causal):
 
 def test_planted_page_order_mistake_is_caught():
     # Reading logical page i from physical page i (ignoring the table) is a
-    # plausible mistake; with scattered pages it changes the result.
-    B, H, Hkv, Nq, N, d, ps = 1, 2, 1, 1, 32, 4, 8
+    # plausible mistake; with scattered pages and a ragged, causal block (so
+    # that the order decides which keys each query sees) it changes the
+    # result.  (Without a mask the key order would not matter.)
+    B, H, Hkv, Nq, N, d, ps = 1, 2, 1, 4, 30, 4, 8
     q, k, v = _qkv(B, H, Hkv, Nq, N, d, 80)
     order = np.array([3, 0, 2, 1])
     kc, vc, table = _paged(k, v, ps, order, 4)
-    right, _ = oracle.attention_decode_paged(q, kc, vc, table, [N], 0.5)
-    wrong, _ = oracle.attention_decode_paged(q, kc, vc, np.arange(4)[None], [N], 0.5)
-    ref, _ = oracle.attention_decode(q, k, v, 0.5)
+    right, _ = oracle.attention_decode_paged(q, kc, vc, table, [N], 0.5, True)
+    wrong, _ = oracle.attention_decode_paged(q, kc, vc, np.arange(4)[None], [N], 0.5, True)
+    ref, _ = oracle.attention_decode(q, k, v, 0.5, True)
     assert np.abs(right - ref).max() < 1e-13 and np.abs(wrong - ref).max() > 1e-3
