@@ -181,6 +181,34 @@ attn_status_t attn_bwd_dq_cross(const void* q, const void* k, const void* v, con
                                 void* stream);
 
 /*
+ * Decode against a paged KV cache.  Page "Flash Attention原理", FAQ Q12 and
+ * Q13: at inference the KV cache is combined with PagedAttention, which
+ * keeps each sequence's cached keys and values in fixed-size pages found
+ * through a block table.  The attention is attn_decode's, over the cached
+ * keys of each batch element:
+ *   k_cache, v_cache [in] bf16 (num_pages, page_size, Hkv, d): physical
+ *            pages of page_size tokens, heads interleaved per token
+ *   block_table [in] DEVICE int32 (B, max_pages): logical page i of batch
+ *            element b is physical page block_table[b * max_pages + i];
+ *            entries past a sequence's last page are never read
+ *   seq_lens [in] DEVICE int32 (B): cached keys of each batch element
+ *            (the Nk of attn_decode, the new tokens included), at most
+ *            page_size * max_pages
+ *   q, o, lse, workspace, scale, causal as attn_decode (causal: query t of
+ *            batch element b at position seq_lens[b] - Nq + t)
+ * page_size: a multiple of 16 that divides 128, or a multiple of 128.
+ * Table entries a sequence needs that are out of [0, num_pages), or lengths
+ * past the capacity, are read as zero keys and make
+ * attn_get_device_status() return ATTN_ERR_INVALID_ARG.
+ */
+size_t attn_decode_paged_workspace_size(int B, int H, int Hkv, int Nq, int page_size, int max_pages, int d);
+attn_status_t attn_decode_paged(const void* q, const void* k_cache, const void* v_cache, void* o, float* lse,
+                                const int* block_table, const int* seq_lens,
+                                void* workspace, size_t workspace_bytes,
+                                int B, int H, int Hkv, int Nq, int page_size, int num_pages, int max_pages,
+                                int d, float scale, int causal, void* stream);
+
+/*
  * Forward with FP8 (e4m3) tensor-core products, head_dim 128.  Page "Flash
  * Attention原理" (§六 and FAQ Q8: FlashAttention-3 runs attention on FP8
  * tensor cores).  Q, K and V are e4m3 (1 sign, 4 exponent bits with bias 7,

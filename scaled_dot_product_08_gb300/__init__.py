@@ -28,6 +28,7 @@ __all__ = [
     "attn_bwd_varlen_workspace_size", "attn_bwd_varlen_stages", "forward_varlen", "backward_varlen",
     "AttnMask", "attn_masked_workspace_size", "attn_fwd_masked", "attn_bwd_masked", "attn_bwd_masked_stages",
     "forward_masked", "backward_masked", "attn_fwd_fp8", "forward_fp8",
+    "attn_decode_paged", "attn_decode_paged_workspace_size", "decode_paged",
     "forward", "forward_cross", "backward", "backward_cross", "decode", "build",
 ]
 
@@ -110,6 +111,11 @@ def load() -> ctypes.CDLL:
                                                _I, _I, _I, _I, _I, _I, _I, _I, ctypes.c_float, _I, ctypes.c_uint,
                                                _P]
         lib.attn_bwd_varlen_stages.restype = _I
+        lib.attn_decode_paged_workspace_size.argtypes = [_I, _I, _I, _I, _I, _I, _I]
+        lib.attn_decode_paged_workspace_size.restype = ctypes.c_size_t
+        lib.attn_decode_paged.argtypes = [_P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _I, _I, _I, _I, _I, _I, _I,
+                                          _I, ctypes.c_float, _I, _P]
+        lib.attn_decode_paged.restype = _I
         _F = ctypes.c_float
         lib.attn_fwd_fp8.argtypes = [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _F, _F, _F, _I, _P]
         lib.attn_fwd_fp8.restype = _I
@@ -229,6 +235,16 @@ def attn_bwd_varlen_stages(q, k, v, o, lse, dout, dq, dk, dv, cu_q, cu_k, worksp
 def attn_fwd_fp8(q, k, v, o, lse, B, H, Hkv, Nq, Nk, d, scale, q_scale, k_scale, v_scale, causal, stream) -> int:
     return load().attn_fwd_fp8(q, k, v, o, lse, B, H, Hkv, Nq, Nk, d, scale, q_scale, k_scale, v_scale, causal,
                                stream)
+
+
+def attn_decode_paged_workspace_size(B, H, Hkv, Nq, page_size, max_pages, d) -> int:
+    return load().attn_decode_paged_workspace_size(B, H, Hkv, Nq, page_size, max_pages, d)
+
+
+def attn_decode_paged(q, k_cache, v_cache, o, lse, block_table, seq_lens, workspace, workspace_bytes, B, H, Hkv, Nq,
+                      page_size, num_pages, max_pages, d, scale, causal, stream) -> int:
+    return load().attn_decode_paged(q, k_cache, v_cache, o, lse, block_table, seq_lens, workspace, workspace_bytes,
+                                    B, H, Hkv, Nq, page_size, num_pages, max_pages, d, scale, causal, stream)
 
 
 def attn_masked_workspace_size(B, H, Hkv, Nq, Nk, d, mask: AttnMask, backward) -> int:
@@ -576,4 +592,41 @@ def forward_fp8(q8, k8, v8, q_scale: float, k_scale: float, v_scale: float, scal
     lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q8.device)
     _check(attn_fwd_fp8(q8.data_ptr(), k8.data_ptr(), v8.data_ptr(), o.data_ptr(), lse.data_ptr(), B, H, Hkv, Nq, Nk,
                         d, scale, q_scale, k_scale, v_scale, causal, _stream_ptr(q8)), "attn_fwd_fp8")
+    return o, lse
+
+
+def decode_paged(q, k_cache, v_cache, block_table, seq_lens, scale: float | None = None, causal: bool = False,
+                 workspace=None):
+    """O, lse of Nq new queries per head against a paged KV cache.
+
+    q: bf16 (B, H, Nq, d); k_cache, v_cache: bf16 (num_pages, page_size,
+    Hkv, d); block_table: int32 CUDA (B, max_pages); seq_lens: int32 CUDA
+    (B,)."""
+    import torch
+    if q.dim() != 4 or k_cache.dim() != 4 or tuple(v_cache.shape) != tuple(k_cache.shape):
+        raise ValueError("q must be (B, H, Nq, d), k_cache and v_cache (num_pages, page_size, Hkv, d)")
+    B, H, Nq, d = q.shape
+    num_pages, page_size, Hkv = k_cache.shape[0], k_cache.shape[1], k_cache.shape[2]
+    if k_cache.shape[3] != d:
+        raise ValueError("the cache's head_dim must be q's")
+    for t in (q, k_cache, v_cache):
+        if not t.is_contiguous() or t.dtype != torch.bfloat16:
+            raise ValueError("q and the caches must be contiguous bf16")
+    for t in (block_table, seq_lens):
+        if t.dtype != torch.int32 or not t.is_cuda or not t.is_contiguous():
+            raise ValueError("block_table and seq_lens must be contiguous int32 CUDA tensors")
+    if block_table.dim() != 2 or block_table.shape[0] != B or tuple(seq_lens.shape) != (B,):
+        raise ValueError("block_table must be (B, max_pages) and seq_lens (B,)")
+    max_pages = block_table.shape[1]
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device)
+    wsb = attn_decode_paged_workspace_size(B, H, Hkv, Nq, page_size, max_pages, d)
+    if workspace is None:
+        workspace = torch.empty(max(wsb, 16), dtype=torch.uint8, device=q.device)
+    _check(attn_decode_paged(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                             block_table.data_ptr(), seq_lens.data_ptr(), workspace.data_ptr(),
+                             workspace.numel() * workspace.element_size(), B, H, Hkv, Nq, page_size, num_pages,
+                             max_pages, d, scale, causal, _stream_ptr(q)), "attn_decode_paged")
     return o, lse

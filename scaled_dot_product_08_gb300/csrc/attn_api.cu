@@ -906,6 +906,81 @@ attn_status_t attn_decode(const void* q, const void* k, const void* v, void* o, 
   return e == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;
 }
 
+// ------------------------------------------------------------------ paged decode
+static attn_status_t check_paged(int B, int page_size, int num_pages, int max_pages) {
+  if (page_size < 16 || page_size % 16 != 0) return ATTN_ERR_UNSUPPORTED_SHAPE;
+  if (page_size < 128 ? (128 % page_size != 0) : (page_size % 128 != 0)) return ATTN_ERR_UNSUPPORTED_SHAPE;
+  if (num_pages < 1 || max_pages < 1) return ATTN_ERR_UNSUPPORTED_SHAPE;
+  if ((long long)page_size * max_pages > (1ll << 30) || (long long)B * max_pages > (1ll << 31))
+    return ATTN_ERR_UNSUPPORTED_SHAPE;
+  return ATTN_OK;
+}
+
+size_t attn_decode_paged_workspace_size(int B, int H, int Hkv, int Nq, int page_size, int max_pages, int d) {
+  if (check_paged(B, page_size, 1, max_pages) != ATTN_OK) return 0;
+  return attn_decode_workspace_size(B, H, Hkv, Nq, page_size * max_pages, d);
+}
+
+attn_status_t attn_decode_paged(const void* q, const void* k_cache, const void* v_cache, void* o, float* lse,
+                                const int* block_table, const int* seq_lens, void* workspace,
+                                size_t workspace_bytes, int B, int H, int Hkv, int Nq, int page_size, int num_pages,
+                                int max_pages, int d, float scale, int causal, void* stream) {
+  ATTN_TRY(check_paged(B, page_size, num_pages, max_pages));
+  const int Nk = page_size * max_pages;  // the most keys a sequence can hold
+  ATTN_TRY(check_decode_shape(B, H, Hkv, Nq, Nk, d));
+  ATTN_TRY(check_scale_flag(scale, causal));
+  if (workspace == nullptr || workspace_bytes < attn_decode_workspace_size(B, H, Hkv, Nq, Nk, d))
+    return ATTN_ERR_WORKSPACE;
+  ATTN_TRY(check_ptrs({q, k_cache, v_cache, o, lse, workspace}));
+  ATTN_TRY(check_offsets_ptrs(block_table, seq_lens));
+  DeviceInfo* di = nullptr;
+  ATTN_TRY(current_device(&di));
+  // Cache maps: 4-D over (d, Hkv, page_size, num_pages), box 64 x 1 x
+  // min(page_size, 128) x 1 (one page's tokens of one head).
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return ATTN_ERR_CUDA;
+  CUtensorMap tq, tk, tv;
+  if (!make_map_bf16(&tq, q, d, B * H * Nq, 1)) return ATTN_ERR_CUDA;
+  const int box_rows = std::min(page_size, 128);
+  for (int t = 0; t < 2; ++t) {
+    cuuint64_t dims[4] = {(cuuint64_t)d, (cuuint64_t)Hkv, (cuuint64_t)page_size, (cuuint64_t)num_pages};
+    cuuint64_t strides[3] = {(cuuint64_t)d * 2, (cuuint64_t)Hkv * d * 2, (cuuint64_t)page_size * Hkv * d * 2};
+    cuuint32_t box[4] = {64, 1, (cuuint32_t)box_rows, 1};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    if (enc(t == 0 ? &tk : &tv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(t == 0 ? k_cache : v_cache),
+            dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return ATTN_ERR_CUDA;
+  }
+  sdpa::DecParams p;
+  memset(&p, 0, sizeof(p));
+  decode_plan(B, Hkv, Nk, &p.nsplit, &p.split_keys);
+  const size_t rows = (size_t)B * H * Nq * (size_t)p.nsplit;
+  p.q = static_cast<const uint16_t*>(q);
+  p.o = static_cast<uint16_t*>(o);
+  p.lse = lse;
+  p.o_part = static_cast<float*>(workspace);
+  p.lse_part = p.o_part + rows * (size_t)d;
+  p.B = B;
+  p.H = H;
+  p.Hkv = Hkv;
+  p.G = H / Hkv;
+  p.Nq = Nq;
+  p.Nk = Nk;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.status = di->status;
+  p.limit_ns = wait_limit_ns();
+  p.info = di->info;
+  p.block_table = block_table;
+  p.seq_lens = seq_lens;
+  p.page_size = page_size;
+  p.max_pages = max_pages;
+  p.num_pages = num_pages;
+  p.box_rows = box_rows;
+  cudaError_t e = sdpa::launch_decode(d, causal != 0, tq, tk, tv, p, static_cast<cudaStream_t>(stream), true);
+  return e == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;
+}
+
 attn_status_t attn_get_device_status(void* stream) {
   DeviceInfo* di = nullptr;
   ATTN_TRY(current_device(&di));

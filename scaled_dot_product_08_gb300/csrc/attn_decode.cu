@@ -60,7 +60,11 @@ struct DecTraits {
 
 }  // namespace
 
-template <int D, bool CAUSAL>
+// PAGED: the cache is paged (DecParams' page fields): per-sequence key
+// counts, tiles gathered from the block table, and the rows of a last tile
+// past the sequence zeroed before the P V product (their cache slots may
+// hold anything, and 0 * NaN is NaN).
+template <int D, bool CAUSAL, bool PAGED>
 __global__ void __launch_bounds__(kDecThreads, 2)
     decode_split_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                         const __grid_constant__ CUtensorMap tmV, const DecParams p) {
@@ -89,9 +93,19 @@ __global__ void __launch_bounds__(kDecThreads, 2)
   const int b = bhk / p.Hkv, hk = bhk % p.Hkv;
   const int R = p.G * p.Nq;                    // live query rows
   const int qrow0 = (b * p.H + hk * p.G) * p.Nq;  // first query row of the group in (B*H*Nq, d)
+  // Cached keys of this batch element: Nk, or its sequence length (paged;
+  // a length past the table's capacity is an error, reported and clamped).
+  int nkb = p.Nk;
+  if (PAGED) {
+    nkb = p.seq_lens[b];
+    if (nkb < 0 || nkb > p.Nk) {
+      if (threadIdx.x == 0 && split == 0) atomicCAS(p.status, 0, kDevBadSeqlens);
+      nkb = max(0, min(nkb, p.Nk));
+    }
+  }
   const int key0 = split * p.split_keys;
-  const int key1 = min(p.Nk, key0 + p.split_keys);
-  const int n = (key1 - key0 + 127) / 128;     // key tiles of this chunk
+  const int key1 = min(nkb, key0 + p.split_keys);
+  const int n = max(0, (key1 - key0 + 127) / 128);  // key tiles of this chunk (0: a chunk past the sequence)
 
   if (threadIdx.x == 0) {
     mbar_init(bQ, 1);
@@ -126,7 +140,7 @@ __global__ void __launch_bounds__(kDecThreads, 2)
     const float c = p.scale_log2;
     // One past the last key this row may see: the chunk end, and for causal
     // rows position Nk - Nq + t (plus one).
-    const int vis_end = CAUSAL ? min(key1, p.Nk - p.Nq + (live ? r % p.Nq : 0) + 1) : key1;
+    const int vis_end = CAUSAL ? min(key1, nkb - p.Nq + (live ? r % p.Nq : 0) + 1) : key1;
     float m = -INFINITY, l = 0.f;  // running max (scaled, base 2), running sum
     bool ok = true;
     for (int j = 0; j < n; ++j) {
@@ -212,11 +226,15 @@ __global__ void __launch_bounds__(kDecThreads, 2)
         tmem_wait_ld();
         reg_fence(o);
         if (live) {
+          // A row that saw no key of the chunk writes zeros, not 0 * O: a
+          // chunk with no key tile at all (paged: past its sequence) never
+          // ran a P V product, and its O columns hold whatever was there.
           float4* dst = reinterpret_cast<float4*>(p.o_part + (row * p.nsplit + split) * D + cc * 32);
 #pragma unroll
           for (int i = 0; i < 8; ++i)
-            dst[i] = make_float4(__uint_as_float(o[4 * i]) * inv, __uint_as_float(o[4 * i + 1]) * inv,
-                                 __uint_as_float(o[4 * i + 2]) * inv, __uint_as_float(o[4 * i + 3]) * inv);
+            dst[i] = l > 0.f ? make_float4(__uint_as_float(o[4 * i]) * inv, __uint_as_float(o[4 * i + 1]) * inv,
+                                           __uint_as_float(o[4 * i + 2]) * inv, __uint_as_float(o[4 * i + 3]) * inv)
+                             : make_float4(0.f, 0.f, 0.f, 0.f);
         }
       }
       if (live)
@@ -230,16 +248,39 @@ __global__ void __launch_bounds__(kDecThreads, 2)
       mbar_expect_tx(bQ, T::TILE_BYTES);
       for (int cb = 0; cb < T::NB; ++cb) tma_load_3d(sQ + cb * T::BLOCK_BYTES, &tmQ, bQ, cb * 64, qrow0, 0);
       int nk = 0, nv = 0;
+      // One 128-key tile into [128 rows x d] at dst: a plain box, or (paged)
+      // 128 / box_rows boxes, each box_rows tokens of one physical page.
+      // Pages past the sequence, or table entries out of range, load from
+      // page num_pages: out of the map's bounds, so the box reads as zeros
+      // (an out-of-range entry the sequence needs is also reported).
+      auto load_tile = [&](uint32_t dst, const CUtensorMap* m, uint32_t bar, int key) {
+        if constexpr (!PAGED) {
+          for (int cb = 0; cb < T::NB; ++cb) tma_load_3d(dst + cb * T::BLOCK_BYTES, m, bar, cb * 64, key, bhk);
+        } else {
+          for (int piece = 0; piece < 128 / p.box_rows; ++piece) {
+            const int kp = key + piece * p.box_rows;
+            const int lp = kp / p.page_size, off = kp % p.page_size;
+            int page = p.num_pages;
+            if (kp < nkb) {
+              page = p.block_table[(size_t)b * p.max_pages + lp];
+              if (page < 0 || page >= p.num_pages) {
+                atomicCAS(p.status, 0, kDevBadSeqlens);
+                page = p.num_pages;
+              }
+            }
+            for (int cb = 0; cb < T::NB; ++cb)
+              tma_load_4d(dst + cb * T::BLOCK_BYTES + piece * p.box_rows * 128, m, bar, cb * 64, hk, off, page);
+          }
+        }
+      };
       for (int j = 0; j < n; ++j) {
         if (j > 0 && !wait_bounded(wc, bKe, (j - 1) & 1, wait_site(0xd1, j))) break;
         mbar_expect_tx(bKf, T::TILE_BYTES);
-        for (int cb = 0; cb < T::NB; ++cb)
-          tma_load_3d(sK + cb * T::BLOCK_BYTES, &tmK, bKf, cb * 64, key0 + j * 128, bhk);
+        load_tile(sK, &tmK, bKf, key0 + j * 128);
         nk = j + 1;
         if (j > 0 && !wait_bounded(wc, bVe, (j - 1) & 1, wait_site(0xd2, j))) break;
         mbar_expect_tx(bVf, T::TILE_BYTES);
-        for (int cb = 0; cb < T::NB; ++cb)
-          tma_load_3d(sV + cb * T::BLOCK_BYTES, &tmV, bVf, cb * 64, key0 + j * 128, bhk);
+        load_tile(sV, &tmV, bVf, key0 + j * 128);
         nv = j + 1;
       }
       // Every copy issued above has landed before the CTA may exit.
@@ -274,6 +315,19 @@ __global__ void __launch_bounds__(kDecThreads, 2)
         mma_commit_p(leader, bKe);  // K_j consumed
         if (!(ok = wait_all(bP, j & 1, wait_site(0xe3, j)))) break;
         if (!(ok = wait_all(bVf, j & 1, wait_site(0xe4, j)))) break;
+        if (PAGED) {
+          // Rows of V past the sequence (the tail of its last page) hold
+          // whatever the cache slot holds: zero them, P is 0 there.
+          const int valid = nkb - (key0 + j * 128);
+          if (valid < 128) {
+            for (int e = lane; e < (128 - valid) * 8 * T::NB; e += 32) {
+              const int row = valid + e / (8 * T::NB), cb = (e / 8) % T::NB, ch = e % 8;
+              st_shared_v4(sV + cb * T::BLOCK_BYTES + row * 128 + ch * 16, 0u, 0u, 0u, 0u);
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+          }
+        }
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
@@ -353,10 +407,10 @@ size_t decode_smem_bytes(int d) {
   }
 }
 
-template <int D, bool C>
+template <int D, bool C, bool PG = false>
 static cudaError_t launch_decode_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                                    const DecParams& p, cudaStream_t stream) {
-  auto kern = decode_split_kernel<D, C>;
+  auto kern = decode_split_kernel<D, C, PG>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, DecTraits<D>::SMEM);
   if (e != cudaSuccess) return e;
   kern<<<dim3((unsigned)p.nsplit, (unsigned)(p.B * p.Hkv)), kDecThreads, DecTraits<D>::SMEM, stream>>>(tq, tk, tv, p);
@@ -367,7 +421,18 @@ static cudaError_t launch_decode_t(const CUtensorMap& tq, const CUtensorMap& tk,
 }
 
 cudaError_t launch_decode(int d, bool causal, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                          const DecParams& p, cudaStream_t stream) {
+                          const DecParams& p, cudaStream_t stream, bool paged) {
+  if (paged) {
+    switch (d) {
+      case 64: return causal ? launch_decode_t<64, true, true>(tq, tk, tv, p, stream)
+                             : launch_decode_t<64, false, true>(tq, tk, tv, p, stream);
+      case 96: return causal ? launch_decode_t<96, true, true>(tq, tk, tv, p, stream)
+                             : launch_decode_t<96, false, true>(tq, tk, tv, p, stream);
+      case 128: return causal ? launch_decode_t<128, true, true>(tq, tk, tv, p, stream)
+                              : launch_decode_t<128, false, true>(tq, tk, tv, p, stream);
+      default: return cudaErrorInvalidValue;
+    }
+  }
   switch (d) {
     case 64: return causal ? launch_decode_t<64, true>(tq, tk, tv, p, stream)
                            : launch_decode_t<64, false>(tq, tk, tv, p, stream);

@@ -102,6 +102,13 @@ struct DecParams {
   int* status;
   unsigned long long limit_ns;
   int* info;
+  // Paged KV cache (the paged instance): K / V as (num_pages, page_size, Hkv,
+  // d), batch element b's logical page i in physical page block_table[b *
+  // max_pages + i], seq_lens[b] cached keys; a 128-key tile is loaded as
+  // 128 / box_rows boxes of box_rows = min(page_size, 128) tokens.
+  const int* block_table;
+  const int* seq_lens;
+  int page_size, max_pages, num_pages, box_rows;
 };
 
 // Device status value for cu_seqlens that are out of range (a sequence longer
@@ -175,7 +182,8 @@ cudaError_t launch_bwd_dq(int d, bool causal, const CUtensorMap& tq, const CUten
 // transposed bit layouts of MaskArgs (bits_t may be null: row bits only).
 cudaError_t launch_mask_pack(const uint8_t* mask, int mask_b, int mask_h, int Nq, int Nk, uint32_t* bits,
                              int words, uint32_t* bits_t, int words_t, uint8_t* flags, cudaStream_t stream);
+// paged: tk / tv are 4-D maps over (d, Hkv, page_size, num_pages).
 cudaError_t launch_decode(int d, bool causal, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                          const DecParams& p, cudaStream_t stream);
+                          const DecParams& p, cudaStream_t stream, bool paged = false);
 
 }  // namespace sdpa

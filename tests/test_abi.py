@@ -233,3 +233,20 @@ def test_fp8_rejects_bad_arguments(lib):
     assert f(ks=-1.0) == S.INVALID_ARG
     assert f(scale=float("nan")) == S.INVALID_ARG
     assert f(causal=1, Nq=300, Nk=200) == S.UNSUPPORTED_SHAPE
+
+
+def test_decode_paged_rejects_bad_arguments(lib):
+    import scaled_dot_product_08_gb300 as sdpa
+    S = sdpa.Status
+    ws = sdpa.attn_decode_paged_workspace_size(2, 8, 2, 1, 16, 64, 128)
+    assert ws == sdpa.attn_decode_workspace_size(2, 8, 2, 1, 16 * 64, 128)
+    f = lambda ps=16, npg=10, mp=64, d=128, wsb=ws, causal=0: sdpa.attn_decode_paged(
+        FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, wsb, 2, 8, 2, 1, ps, npg, mp, d, 0.1, causal, None)
+    assert f(ps=48) == S.UNSUPPORTED_SHAPE     # neither divides 128 nor a multiple of it
+    assert f(ps=100) == S.UNSUPPORTED_SHAPE
+    assert f(ps=8) == S.UNSUPPORTED_SHAPE
+    assert f(npg=0) == S.UNSUPPORTED_SHAPE
+    assert f(mp=0) == S.UNSUPPORTED_SHAPE
+    assert f(d=80) == S.UNSUPPORTED_SHAPE
+    assert f(wsb=ws - 1) == S.WORKSPACE
+    assert sdpa.attn_decode_paged_workspace_size(2, 8, 2, 1, 48, 64, 128) == 0
