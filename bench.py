@@ -614,19 +614,34 @@ def run_decode(args, w, rank, world, local_rank):
     torch.cuda.set_device(local_rank)
     x = make_inputs(w)
     dev = lambda a: torch.from_numpy(a).to(torch.bfloat16).cuda()
-    q, k, v = dev(x["q"]), dev(x["k"]), dev(x["v"])
     B, H, Hkv, Nq, Nk, d = w.B, w.H, w.Hkv, w.n_queries, w.N, w.d
     s = w.softmax_scale
+    q = dev(x["q"])
+    if w.page_size:
+        from sdpa_inputs import paged_layout
+        kc, vc, table = paged_layout(w, x["k"], x["v"])
+        k, v = dev(kc), dev(vc)
+        tbl = torch.from_numpy(table).cuda()
+        lens = torch.full((B,), Nk, dtype=torch.int32, device="cuda")
+        num_pages, max_pages = kc.shape[0], table.shape[1]
+        ws_bytes = sdpa.attn_decode_paged_workspace_size(B, H, Hkv, Nq, w.page_size, max_pages, d)
+    else:
+        k, v = dev(x["k"]), dev(x["v"])
+        ws_bytes = sdpa.attn_decode_workspace_size(B, H, Hkv, Nq, Nk, d)
     o = torch.empty_like(q)
     lse = torch.empty((B, H, Nq), dtype=torch.float32, device="cuda")
-    ws_bytes = sdpa.attn_decode_workspace_size(B, H, Hkv, Nq, Nk, d)
     ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
     stream = torch.cuda.current_stream()
     sp = stream.cuda_stream
 
     def step():
-        st = sdpa.attn_decode(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
-                              ws.data_ptr(), ws_bytes, B, H, Hkv, Nq, Nk, d, s, w.causal, sp)
+        if w.page_size:
+            st = sdpa.attn_decode_paged(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                                        tbl.data_ptr(), lens.data_ptr(), ws.data_ptr(), ws_bytes, B, H, Hkv, Nq,
+                                        w.page_size, num_pages, max_pages, d, s, w.causal, sp)
+        else:
+            st = sdpa.attn_decode(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                                  ws.data_ptr(), ws_bytes, B, H, Hkv, Nq, Nk, d, s, w.causal, sp)
         if st != 0:
             raise RuntimeError(f"attn_decode: {sdpa.attn_status_string(st)}")
 
@@ -654,7 +669,8 @@ def run_decode(args, w, rank, world, local_rank):
     peaks, peak_src = load_peaks()
     peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
     per_call = nbytes / (ms / K / 1e3) / 1e9
-    roof = {"kernel": "attn_decode (decode_split_kernel + decode_merge_kernel)", "bound": "hbm",
+    roof = {"kernel": ("attn_decode_paged" if w.page_size else "attn_decode") +
+                      " (decode_split_kernel + decode_merge_kernel)", "bound": "hbm",
             "achieved": per_call, "peak": peak, "unit": "GB/s", "frac": per_call / peak,
             "peak_source": f"{peak_src} copy bandwidth", "traffic": traffic_of("attn_decode", w.name)}
 
@@ -699,7 +715,9 @@ def run_decode(args, w, rank, world, local_rank):
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic (seeded N(0,1) draws rounded to bf16)",
             "config": {"workload": f"{w.name}: B={B} H={H} Hkv={Hkv} Nq={Nq} Nk={Nk} d={d} "
-                                   f"{'causal' if w.causal else 'non-causal'} decode",
+                                   f"{'causal' if w.causal else 'non-causal'} decode"
+                                   + (f", cache in {w.page_size}-token pages scattered over the pool"
+                                      if w.page_size else ""),
                        "B": B, "H": H, "Hkv": Hkv, "Nq": Nq, "Nk": Nk, "d": d, "causal": w.causal,
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                        "l2": "no flush: the K/V cache (%.0f MB) is larger than the 129 MB L2" % (2 * B * Hkv * Nk * d * 2 / 1e6)},

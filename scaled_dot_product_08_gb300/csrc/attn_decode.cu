@@ -242,48 +242,62 @@ __global__ void __launch_bounds__(kDecThreads, 2)
     }
   } else if (warp == 4) {
     // ------------------------------------------------------------ producer
+    // Lane 0 waits for the free slots and arms the barriers; the K / V boxes
+    // of a tile are issued by the warp's lanes (paged: lane i fetches the
+    // i-th piece's page from the block table and loads it, so the table
+    // lookups of a tile overlap instead of following one another).
     if (lane == 0) {
       tma_prefetch_desc(&tmK);
       tma_prefetch_desc(&tmV);
       mbar_expect_tx(bQ, T::TILE_BYTES);
       for (int cb = 0; cb < T::NB; ++cb) tma_load_3d(sQ + cb * T::BLOCK_BYTES, &tmQ, bQ, cb * 64, qrow0, 0);
-      int nk = 0, nv = 0;
-      // One 128-key tile into [128 rows x d] at dst: a plain box, or (paged)
-      // 128 / box_rows boxes, each box_rows tokens of one physical page.
-      // Pages past the sequence, or table entries out of range, load from
-      // page num_pages: out of the map's bounds, so the box reads as zeros
-      // (an out-of-range entry the sequence needs is also reported).
-      auto load_tile = [&](uint32_t dst, const CUtensorMap* m, uint32_t bar, int key) {
-        if constexpr (!PAGED) {
+    }
+    int nk = 0, nv = 0;
+    // One 128-key tile into [128 rows x d] at dst: a plain box, or (paged)
+    // 128 / box_rows boxes, each box_rows tokens of one physical page.
+    // Pages past the sequence, or table entries out of range, load from page
+    // num_pages: out of the map's bounds, so the box reads as zeros (an
+    // out-of-range entry the sequence needs is also reported).
+    auto load_tile = [&](uint32_t dst, const CUtensorMap* m, uint32_t bar, int key) {
+      if constexpr (!PAGED) {
+        if (lane == 0)
           for (int cb = 0; cb < T::NB; ++cb) tma_load_3d(dst + cb * T::BLOCK_BYTES, m, bar, cb * 64, key, bhk);
-        } else {
-          for (int piece = 0; piece < 128 / p.box_rows; ++piece) {
-            const int kp = key + piece * p.box_rows;
-            const int lp = kp / p.page_size, off = kp % p.page_size;
-            int page = p.num_pages;
-            if (kp < nkb) {
-              page = p.block_table[(size_t)b * p.max_pages + lp];
-              if (page < 0 || page >= p.num_pages) {
-                atomicCAS(p.status, 0, kDevBadSeqlens);
-                page = p.num_pages;
-              }
+      } else {
+        for (int piece = lane; piece < 128 / p.box_rows; piece += 32) {
+          const int kp = key + piece * p.box_rows;
+          const int lp = kp / p.page_size, off = kp % p.page_size;
+          int page = p.num_pages;
+          if (kp < nkb) {
+            page = p.block_table[(size_t)b * p.max_pages + lp];
+            if (page < 0 || page >= p.num_pages) {
+              atomicCAS(p.status, 0, kDevBadSeqlens);
+              page = p.num_pages;
             }
-            for (int cb = 0; cb < T::NB; ++cb)
-              tma_load_4d(dst + cb * T::BLOCK_BYTES + piece * p.box_rows * 128, m, bar, cb * 64, hk, off, page);
           }
+          for (int cb = 0; cb < T::NB; ++cb)
+            tma_load_4d(dst + cb * T::BLOCK_BYTES + piece * p.box_rows * 128, m, bar, cb * 64, hk, off, page);
         }
-      };
-      for (int j = 0; j < n; ++j) {
-        if (j > 0 && !wait_bounded(wc, bKe, (j - 1) & 1, wait_site(0xd1, j))) break;
-        mbar_expect_tx(bKf, T::TILE_BYTES);
-        load_tile(sK, &tmK, bKf, key0 + j * 128);
-        nk = j + 1;
-        if (j > 0 && !wait_bounded(wc, bVe, (j - 1) & 1, wait_site(0xd2, j))) break;
-        mbar_expect_tx(bVf, T::TILE_BYTES);
-        load_tile(sV, &tmV, bVf, key0 + j * 128);
-        nv = j + 1;
       }
-      // Every copy issued above has landed before the CTA may exit.
+    };
+    for (int j = 0; j < n; ++j) {
+      bool ok = true;
+      if (lane == 0) {
+        ok = j == 0 || wait_bounded(wc, bKe, (j - 1) & 1, wait_site(0xd1, j));
+        if (ok) mbar_expect_tx(bKf, T::TILE_BYTES);
+      }
+      if (!__shfl_sync(0xffffffffu, ok, 0)) break;  // the barrier is armed before any box is issued
+      load_tile(sK, &tmK, bKf, key0 + j * 128);
+      nk = j + 1;
+      if (lane == 0) {
+        ok = j == 0 || wait_bounded(wc, bVe, (j - 1) & 1, wait_site(0xd2, j));
+        if (ok) mbar_expect_tx(bVf, T::TILE_BYTES);
+      }
+      if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+      load_tile(sV, &tmV, bVf, key0 + j * 128);
+      nv = j + 1;
+    }
+    // Every copy issued above has landed before the CTA may exit.
+    if (lane == 0) {
       wait_drain(bQ, 0, p.limit_ns);
       if (nk > 0) wait_drain(bKf, (nk - 1) & 1, p.limit_ns);
       if (nv > 0) wait_drain(bVf, (nv - 1) & 1, p.limit_ns);

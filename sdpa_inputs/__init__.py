@@ -24,6 +24,9 @@ model):
 
   dec1 B=8  H=64  Hkv=8  Nq=1 N=32768 d=128  non-causal  seed 6
   dec4 same shape, Nq=4 new tokens (a speculative block), causal  seed 7
+  dec1p dec1's draw with the cache in a pool of 16-token pages (the page
+       size vLLM uses by default), each sequence's pages scattered over the
+       pool by paged_layout (default_rng(seed + 2000).permutation)
 
 Chunked prefill (Nq new queries per head against N keys, the tiled forward):
 
@@ -87,6 +90,7 @@ class Workload:
     len_range: tuple[int, int] | None = None  # varlen: sequence lengths drawn from [lo, hi]
     window: tuple[int, int] | None = None     # masked: (left, right), -1 = open
     prefix: int | None = None                 # masked: prefix-LM boolean mask with this prefix
+    page_size: int | None = None              # decode: the cache kept in pages of this many tokens
 
     @property
     def softmax_scale(self) -> float:
@@ -113,6 +117,7 @@ WORKLOADS: dict[str, Workload] = {
     "c5": Workload("c5", 8, 16, 16, 4096, 128, True, 5, with_grad=True),
     "dec1": Workload("dec1", 8, 64, 8, 32768, 128, False, 6, Nq=1, kind="decode"),
     "dec4": Workload("dec4", 8, 64, 8, 32768, 128, True, 7, Nq=4, kind="decode"),
+    "dec1p": Workload("dec1p", 8, 64, 8, 32768, 128, False, 6, Nq=1, kind="decode", page_size=16),
     "cp1": Workload("cp1", 1, 32, 8, 16384, 128, True, 8, Nq=2048, kind="cross"),
     "cx": Workload("cx", 8, 16, 16, 4096, 128, False, 9, with_grad=True, Nq=2048, kind="cross"),
     "vl1": Workload("vl1", 1, 16, 16, 32768, 128, True, 10, with_grad=True, kind="varlen", len_range=(128, 8192)),
@@ -298,3 +303,26 @@ def quantize_e4m3(x: np.ndarray):
     amax = float(np.max(np.abs(x)))
     scale = np.float32(amax / E4M3_MAX if amax > 0 else 1.0)
     return e4m3_encode(np.asarray(x, dtype=np.float64) / float(scale)), float(scale)
+
+
+def paged_layout(w: Workload, k: np.ndarray, v: np.ndarray):
+    """A decode workload's contiguous (B, Hkv, N, d) cache stored in a page
+    pool of w.page_size-token pages: (num_pages, page_size, Hkv, d) K and V
+    and the (B, max_pages) int32 block table, each sequence's logical pages
+    at physical pages default_rng(w.seed + 2000).permutation(num_pages)."""
+    B, Hkv, N, d = k.shape
+    ps = w.page_size
+    max_pages = -(-N // ps)
+    num_pages = B * max_pages
+    order = np.random.default_rng(w.seed + 2000).permutation(num_pages)
+    table = order.reshape(B, max_pages).astype(np.int32)
+    kc = np.zeros((num_pages, ps, Hkv, d), dtype=k.dtype)
+    vc = np.zeros((num_pages, ps, Hkv, d), dtype=v.dtype)
+    for b in range(B):
+        kp = np.zeros((max_pages * ps, Hkv, d), dtype=k.dtype)
+        vp = np.zeros((max_pages * ps, Hkv, d), dtype=v.dtype)
+        kp[:N] = k[b].transpose(1, 0, 2)
+        vp[:N] = v[b].transpose(1, 0, 2)
+        kc[table[b]] = kp.reshape(max_pages, ps, Hkv, d)
+        vc[table[b]] = vp.reshape(max_pages, ps, Hkv, d)
+    return kc, vc, table
