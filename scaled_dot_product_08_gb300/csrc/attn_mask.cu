@@ -21,27 +21,49 @@ namespace sdpa {
 namespace {
 
 constexpr int kTile = 128;
-constexpr int kPitch = 132;  // shared row pitch in bytes: column reads spread over the banks
+constexpr int kPitchW = 33;  // shared row pitch in 32-bit words: row-wise and column-wise reads spread over the banks
 
 // One CTA per (plane, 128-row query tile, 128-column key tile).  The tile's
-// bytes go through shared memory; each 32-bit word is then one warp ballot
-// (lane l supplies element 32 w + l), over a row for the row bits and over a
-// column for the transposed bits.
+// bytes go through shared memory.  A row word (32 keys of one query row) is
+// built by one thread from eight 4-byte reads: __vsetne4 turns each byte
+// into 0 / 1 and one multiply gathers the four into a nibble.  A transposed
+// word (32 query rows of one key) is a warp ballot, lane l holding row
+// 32 w + l; each lane reads four keys at once, so one read feeds four
+// ballots.
 __global__ void __launch_bounds__(256) mask_pack_kernel(const uint8_t* __restrict__ mask, int Nq, int Nk,
                                                         uint32_t* __restrict__ bits, int words,
                                                         uint32_t* __restrict__ bits_t, int words_t,
                                                         uint8_t* __restrict__ flags) {
-  __shared__ uint8_t tile[kTile * kPitch];
+  __shared__ uint32_t tile_w[kTile * kPitchW];
   __shared__ int any_vis, all_vis;
+  uint8_t* tile = reinterpret_cast<uint8_t*>(tile_w);
+  constexpr int kPitch = 4 * kPitchW;
   const int nqt = (Nq + kTile - 1) / kTile, nkt = (Nk + kTile - 1) / kTile;
   const int kt = (int)(blockIdx.x % nkt);
   const int qt = (int)((blockIdx.x / nkt) % nqt);
   const int plane = (int)(blockIdx.x / ((unsigned)nkt * nqt));
   const uint8_t* src = mask + (size_t)plane * Nq * Nk;
-  for (int e = threadIdx.x; e < kTile * kTile; e += blockDim.x) {
-    const int r = e / kTile, c = e % kTile;
-    const int qi = qt * kTile + r, kj = kt * kTile + c;
-    tile[r * kPitch + c] = (qi < Nq && kj < Nk) ? (src[(size_t)qi * Nk + kj] != 0) : 0;
+  if ((Nk & 15) == 0 && (reinterpret_cast<uintptr_t>(mask) & 15) == 0) {
+    // 16 bytes per load (rows start 16-byte aligned); four 4-byte stores
+    // into the padded shared rows.  Bytes keep their values: only their
+    // being nonzero is read below.
+    for (int e = threadIdx.x; e < kTile * kTile / 16; e += blockDim.x) {
+      const int r = e / (kTile / 16), c16 = e % (kTile / 16);
+      const int qi = qt * kTile + r, kj = kt * kTile + c16 * 16;
+      uint4 v = make_uint4(0, 0, 0, 0);
+      if (qi < Nq && kj < Nk) v = *reinterpret_cast<const uint4*>(src + (size_t)qi * Nk + kj);
+      uint32_t* dst = tile_w + r * kPitchW + c16 * 4;
+      dst[0] = v.x;
+      dst[1] = v.y;
+      dst[2] = v.z;
+      dst[3] = v.w;
+    }
+  } else {
+    for (int e = threadIdx.x; e < kTile * kTile; e += blockDim.x) {
+      const int r = e / kTile, c = e % kTile;
+      const int qi = qt * kTile + r, kj = kt * kTile + c;
+      tile[r * kPitch + c] = (qi < Nq && kj < Nk) ? (src[(size_t)qi * Nk + kj] != 0) : 0;
+    }
   }
   if (threadIdx.x == 0) {
     any_vis = 0;
@@ -49,22 +71,34 @@ __global__ void __launch_bounds__(256) mask_pack_kernel(const uint8_t* __restric
   }
   __syncthreads();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
-  // Columns of word w that exist (keys < Nk).
-  const int kvalid = min(kTile, Nk - kt * kTile);
+  const int kvalid = min(kTile, Nk - kt * kTile);  // key columns that exist
+  const int qvalid = min(kTile, Nq - qt * kTile);  // query rows that exist
   bool any = false, all = true;
-  for (int rw = warp; rw < kTile * 4; rw += nw) {
-    const int r = rw >> 2, w = rw & 3;
-    const uint32_t word = __ballot_sync(0xffffffffu, tile[r * kPitch + 32 * w + lane] != 0);
-    if (qt * kTile + r < Nq) {
+  // Row words: thread e handles (row e / 4, word e % 4), every thread the
+  // same number of times.
+  for (int e = threadIdx.x; e < kTile * 4; e += blockDim.x) {
+    const int r = e >> 2, w = e & 3;
+    const uint32_t* rw = tile_w + r * kPitchW + 8 * w;
+    uint32_t word = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      // bytes b0..b3 of nz are 0 / 1; the product puts b_k at bit 24 + k
+      // and every cross term below bit 24 or above bit 31
+      const uint32_t nz = __vsetne4(rw[i], 0u);
+      word |= ((nz * 0x01020408u) >> 24) << (4 * i);
+    }
+    if (r < qvalid) {
       const int nb = min(32, max(0, kvalid - 32 * w));
       const uint32_t valid = nb == 32 ? 0xffffffffu : ((1u << nb) - 1u);
       any |= (word & valid) != 0;
       all &= (word & valid) == valid;
-      if (lane == 0) bits[((size_t)plane * Nq + qt * kTile + r) * words + kt * 4 + w] = word;
+      bits[((size_t)plane * Nq + qt * kTile + r) * words + kt * 4 + w] = word;
     }
   }
   if (flags != nullptr) {
     // The tile's class for skipping: 0 = nothing visible, 1 = some, 2 = all.
+    any = __any_sync(0xffffffffu, any);
+    all = __all_sync(0xffffffffu, all);
     if (lane == 0 && any) atomicOr(&any_vis, 1);
     if (lane == 0 && !all) atomicAnd(&all_vis, 0);
     __syncthreads();
@@ -72,11 +106,19 @@ __global__ void __launch_bounds__(256) mask_pack_kernel(const uint8_t* __restric
       flags[((size_t)plane * nqt + qt) * nkt + kt] = (uint8_t)(any_vis == 0 ? 0 : (all_vis ? 2 : 1));
   }
   if (bits_t != nullptr) {
-    for (int cw = warp; cw < kTile * 4; cw += nw) {
-      const int c = cw >> 2, w = cw & 3;
-      const uint32_t word = __ballot_sync(0xffffffffu, tile[(32 * w + lane) * kPitch + c] != 0);
-      if (lane == 0 && kt * kTile + c < Nk)
-        bits_t[((size_t)plane * Nk + kt * kTile + c) * words_t + qt * 4 + w] = word;
+    // (row block w, keys 4 g .. 4 g + 3): four transposed words per item.
+    for (int wg = warp; wg < 4 * (kTile / 4); wg += nw) {
+      const int w = wg / (kTile / 4), g = wg % (kTile / 4);
+      const uint32_t nz = __vsetne4(tile_w[(32 * w + lane) * kPitchW + g], 0u);
+      uint32_t mine = 0;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const uint32_t word = __ballot_sync(0xffffffffu, (nz >> (8 * k)) & 1u);
+        if (lane == k) mine = word;
+      }
+      const int c = 4 * g + lane;
+      if (lane < 4 && kt * kTile + c < Nk)
+        bits_t[((size_t)plane * Nk + kt * kTile + c) * words_t + qt * 4 + w] = mine;
     }
   }
 }

@@ -145,3 +145,30 @@ def test_masked_backward_is_deterministic(cuda_lib):
     b = _run(cuda_lib, shape, True, (120, -1), [300, 200], mask, seed=46001)[2]
     for x, y in zip(a, b):
         assert np.array_equal(x, y)
+
+
+def test_mask_bytes_nonzero_values_and_unaligned_base(cuda_lib):
+    # Any nonzero byte marks a visible key, whether the packer reads the rows
+    # 16 bytes at a time (Nk a multiple of 16, base 16-byte aligned) or byte
+    # by byte (base one byte past the allocation's start): both give the
+    # result of the same mask as 0 / 1 bytes.
+    import torch
+    B, H, Hkv, N, d = 1, 2, 2, 512, 64
+    q, k, v, do = (dev(x) for x in _problem(B, H, Hkv, N, N, d, 47000))
+    mask = _mask("batch", B, H, N, N, 47001)
+    codes = np.where(mask, np.random.default_rng(47002).integers(1, 256, mask.shape), 0).astype(np.uint8)
+    ref = _t(mask.astype(np.uint8), torch.uint8)
+    aligned = _t(codes, torch.uint8)
+    buf = torch.zeros(codes.size + 1, dtype=torch.uint8, device="cuda")
+    shifted = buf[1:].view(codes.shape)
+    shifted.copy_(aligned)
+    assert shifted.data_ptr() % 16 == 1
+    O0, l0 = cuda_lib.forward_masked(q, k, v, 0.125, False, None, None, ref)
+    g0 = cuda_lib.backward_masked(q, k, v, O0, l0, do, 0.125, False, None, None, ref)
+    for m in (aligned, shifted):
+        O1, l1 = cuda_lib.forward_masked(q, k, v, 0.125, False, None, None, m)
+        g1 = cuda_lib.backward_masked(q, k, v, O1, l1, do, 0.125, False, None, None, m)
+        assert np.array_equal(host(O1), host(O0)) and np.array_equal(host(l1), host(l0))
+        for a, b in zip(g1, g0):
+            assert np.array_equal(host(a), host(b))
+    assert cuda_lib.attn_get_device_status(None) == cuda_lib.Status.OK
