@@ -4,7 +4,8 @@
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload c5] [--impl ours|reference]
 
 One step is the whole hot path on one batch of synthetic input: the forward
-kernel (O and lse), then the backward's three kernels (prep, grad, dq).  The
+kernel (O and lse), then the backward's two kernels: dQ (which also forms
+each row's D = rowsum(dO * O) and lse in base 2) and dK / dV.  The
 default workload is the training configuration B=8, H=16, N=4096, d=128,
 causal, forward + backward.  Inputs (seeded bf16 draws) are resident in HBM
 before timing; they total 537 MB, larger than the 129 MB L2, so no L2 flush
@@ -390,7 +391,9 @@ def run_ours(args, w, rank, world, local_rank):
         ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
     stream = torch.cuda.current_stream()
     sp = stream.cuda_stream
-    names = ["attn_fwd"] + (["attn_bwd_prep", "attn_bwd_grad", "attn_bwd_dq"] if w.with_grad else [])
+    # The backward: dQ (forming the row vectors D and lse in base 2 on the way),
+    # then dK / dV from those vectors.
+    names = ["attn_fwd"] + (["attn_bwd_dq", "attn_bwd_grad"] if w.with_grad else [])
 
     def chk(st, where):
         if st != 0:
@@ -406,7 +409,7 @@ def run_ours(args, w, rank, world, local_rank):
         launches = [lambda: chk(sdpa.attn_fwd_varlen(P(q), P(k), P(v), P(o), P(lse), P(cu), P(cu), nseq, H, Hkv,
                                                      N, N, maxlen, maxlen, d, s, w.causal, sp), "attn_fwd_varlen")]
         if w.with_grad:
-            launches += [vstage(1), vstage(2), vstage(4)]
+            launches += [vstage(8), vstage(2)]
     elif w.kind == "fp8":
         (_, qsc), (_, ksc), (_, vsc) = fp8
         launches = [lambda: chk(sdpa.attn_fwd_fp8(P(q), P(k), P(v), P(o), P(lse), B, H, Hkv, Nq, N, d, s, qsc, ksc,
@@ -419,32 +422,28 @@ def run_ours(args, w, rank, world, local_rank):
         launches = [lambda: chk(sdpa.attn_fwd_masked(P(q), P(k), P(v), P(o), P(lse), B, H, Hkv, Nq, N, d, s, w.causal,
                                                      mask_spec, P(mws), mws.numel(), sp), "attn_fwd_masked")]
         if w.with_grad:
-            launches += [mstage(1), mstage(2), mstage(4)]
+            launches += [mstage(8), mstage(2)]
     elif w.kind == "cross":
         launches = [lambda: chk(sdpa.attn_fwd_cross(P(q), P(k), P(v), P(o), P(lse), B, H, Hkv, Nq, N, d, s,
                                                     w.causal, sp), "attn_fwd_cross")]
         if w.with_grad:
             launches += [
-                lambda: chk(sdpa.attn_bwd_prep(P(o), P(lse), P(do), P(ws), ws_bytes, B, H, Hkv, Nq, d, sp),
-                            "attn_bwd_prep"),
+                lambda: chk(sdpa.attn_bwd_dq_rows(P(q), P(k), P(v), P(o), P(lse), P(do), P(dq), P(ws), ws_bytes,
+                                                  B, H, Hkv, Nq, N, d, s, w.causal, sp), "attn_bwd_dq_rows"),
                 lambda: chk(sdpa.attn_bwd_grad_cross(P(q), P(k), P(v), P(do), P(dk), P(dv), P(ws), ws_bytes,
-                                                     B, H, Hkv, Nq, N, d, s, w.causal, sp), "attn_bwd_grad_cross"),
-                lambda: chk(sdpa.attn_bwd_dq_cross(P(q), P(k), P(v), P(do), P(dq), P(ws), ws_bytes,
-                                                   B, H, Hkv, Nq, N, d, s, w.causal, sp), "attn_bwd_dq_cross")]
+                                                     B, H, Hkv, Nq, N, d, s, w.causal, sp), "attn_bwd_grad_cross")]
     else:
         launches = [lambda: chk(sdpa.attn_fwd(P(q), P(k), P(v), P(o), P(lse), B, H, Hkv, N, d, s, w.causal, sp),
                                 "attn_fwd")]
         if w.with_grad:
             launches += [
-                lambda: chk(sdpa.attn_bwd_prep(P(o), P(lse), P(do), P(ws), ws_bytes, B, H, Hkv, N, d, sp),
-                            "attn_bwd_prep"),
+                lambda: chk(sdpa.attn_bwd_dq_rows(P(q), P(k), P(v), P(o), P(lse), P(do), P(dq), P(ws), ws_bytes,
+                                                  B, H, Hkv, N, N, d, s, w.causal, sp), "attn_bwd_dq_rows"),
                 lambda: chk(sdpa.attn_bwd_grad(P(q), P(k), P(v), P(do), P(dk), P(dv), P(ws), ws_bytes,
-                                               B, H, Hkv, N, d, s, w.causal, sp), "attn_bwd_grad"),
-                lambda: chk(sdpa.attn_bwd_dq(P(q), P(k), P(v), P(do), P(dq), P(ws), ws_bytes,
-                                             B, H, Hkv, N, d, s, w.causal, sp), "attn_bwd_dq")]
+                                               B, H, Hkv, N, d, s, w.causal, sp), "attn_bwd_grad")]
 
     # Kernels per step: one per call, plus the mask packing inside the masked
-    # forward and backward-prep calls when there is a boolean mask.
+    # forward and first backward calls when there is a boolean mask.
     kernels_per_step = len(launches) + (2 if w.kind == "masked" and w.prefix is not None else 0)
     if w.kind == "masked" and w.prefix is not None and not w.with_grad:
         kernels_per_step -= 1
@@ -517,20 +516,13 @@ def run_ours(args, w, rank, world, local_rank):
     # backward kernel four (S^T, dP^T, dV, dK); the query-tile kernel three
     # (S, dP, dQ).  The step value above keeps the 2.5x-forward convention.
     kflops = {"attn_fwd": f_fwd, "attn_bwd_grad": 2.0 * f_fwd, "attn_bwd_dq": 1.5 * f_fwd}
-    if dom in kflops:
-        achieved = kflops[dom] / (per_kernel[dom] / 1e3) / 1e12
-        peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
-        src, nominal = f"{peak_src} bf16 burst (cuBLAS 8192^3)", 2250.0
-        if w.kind == "fp8":  # the FP8 peak: the measured bf16 burst times the nominal ratio 4.5 / 2.25
-            peak, src, nominal = 2.0 * peak, f"2 x {peak_src} bf16 burst (nominal fp8 / bf16 ratio 4.5 / 2.25)", 4500.0
-        roof = {"kernel": dom, "bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                "frac": achieved / peak, "peak_source": src, f"frac_of_nominal_{int(nominal)}": achieved / nominal}
-    else:
-        nbytes = {"attn_bwd_prep": 2 * B * H * Nq * d * 2 + B * H * Nq * 4 + B * H * Nq * 2 * 4}[dom]
-        achieved = nbytes / (per_kernel[dom] / 1e3) / 1e9
-        peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
-        roof = {"kernel": dom, "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                "frac": achieved / peak, "peak_source": f"{peak_src} copy bandwidth"}
+    achieved = kflops[dom] / (per_kernel[dom] / 1e3) / 1e12
+    peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    src, nominal = f"{peak_src} bf16 burst (cuBLAS 8192^3)", 2250.0
+    if w.kind == "fp8":  # the FP8 peak: the measured bf16 burst times the nominal ratio 4.5 / 2.25
+        peak, src, nominal = 2.0 * peak, f"2 x {peak_src} bf16 burst (nominal fp8 / bf16 ratio 4.5 / 2.25)", 4500.0
+    roof = {"kernel": dom, "bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+            "frac": achieved / peak, "peak_source": src, f"frac_of_nominal_{int(nominal)}": achieved / nominal}
     roof["traffic"] = traffic_of(dom, w.name)
 
     # ---- end to end through the C ABI with pinned host buffers

@@ -121,18 +121,27 @@ attn_status_t attn_bwd(const void* q, const void* k, const void* v, const void* 
                        void* stream);
 
 /*
- * The three stages attn_bwd runs, for callers that schedule (or time) them
- * separately.  Same arguments, layouts and workspace as attn_bwd.  prep must
- * complete before grad and dq start; grad and dq read the workspace but do
- * not write it, and are independent of each other:
- *   attn_bwd_prep  D = rowsum(dO * O) and lse in base 2 into the workspace
- *                                                         (reads o, lse, dout)
- *   attn_bwd_grad  one pass per key tile: recomputes P^T and dS^T tile by
- *                  tile; writes dK, dV                  (reads q, k, v, dout)
- *   attn_bwd_dq    one pass per query tile: recomputes P and dS tile by tile;
- *                  writes dq                            (reads q, k, v, dout)
+ * The stages of the backward, for callers that schedule (or time) them
+ * separately.  Same arguments, layouts and workspace as attn_bwd.  The
+ * workspace's row vectors (D = rowsum(dO * O) and lse in base 2) must be
+ * complete before grad or dq starts:
+ *   attn_bwd_prep     the row vectors into the workspace  (reads o, lse, dout)
+ *   attn_bwd_grad     one pass per key tile: recomputes P^T and dS^T tile by
+ *                     tile; writes dK, dV; reads the row vectors
+ *                                                       (reads q, k, v, dout)
+ *   attn_bwd_dq       one pass per query tile: recomputes P and dS tile by
+ *                     tile; writes dq; reads the row vectors
+ *                                                       (reads q, k, v, dout)
+ *   attn_bwd_dq_rows  attn_bwd_dq that forms each query tile's row vectors
+ *                     itself (from o, lse, dout) and writes them into the
+ *                     workspace: it replaces prep + dq, and grad runs after
+ *                     it.  attn_bwd is attn_bwd_dq_rows then attn_bwd_grad.
+ *                     Nq query rows and Nk key rows (Nq == Nk for attn_bwd's
+ *                     shapes; attn_bwd_cross's otherwise); workspace of
+ *                     attn_bwd_workspace_size(B, H, Hkv, Nq, d) bytes.
  * Every output element has exactly one writer (no atomics), so the results
- * are the same on every run.
+ * are the same on every run; D summed by prep and by dq_rows may differ in
+ * its last bits (another order of the same float32 additions).
  */
 attn_status_t attn_bwd_prep(const void* o, const float* lse, const void* dout,
                             void* workspace, size_t workspace_bytes,
@@ -145,6 +154,11 @@ attn_status_t attn_bwd_dq(const void* q, const void* k, const void* v, const voi
                           void* dq, void* workspace, size_t workspace_bytes,
                           int B, int H, int Hkv, int N, int d, float scale, int causal,
                           void* stream);
+attn_status_t attn_bwd_dq_rows(const void* q, const void* k, const void* v, const void* o,
+                               const float* lse, const void* dout, void* dq,
+                               void* workspace, size_t workspace_bytes,
+                               int B, int H, int Hkv, int Nq, int Nk, int d, float scale, int causal,
+                               void* stream);
 
 /*
  * Backward of attn_fwd_cross: Nq query rows, Nk key/value rows per head,
@@ -167,9 +181,9 @@ attn_status_t attn_bwd_cross(const void* q, const void* k, const void* v, const 
 
 /*
  * The grad and dq stages of attn_bwd_cross, for callers that schedule them
- * separately (the prep stage is attn_bwd_prep with N = Nq).  Arguments and
- * ordering rules as for attn_bwd_grad / attn_bwd_dq, with the shapes of
- * attn_bwd_cross.
+ * separately (the prep stage is attn_bwd_prep with N = Nq; attn_bwd_dq_rows
+ * takes Nq and Nk itself).  Arguments and ordering rules as for
+ * attn_bwd_grad / attn_bwd_dq, with the shapes of attn_bwd_cross.
  */
 attn_status_t attn_bwd_grad_cross(const void* q, const void* k, const void* v, const void* dout,
                                   void* dk, void* dv, void* workspace, size_t workspace_bytes,
@@ -272,8 +286,9 @@ size_t attn_masked_workspace_size(int B, int H, int Hkv, int Nq, int Nk, int d, 
  * no key).  The workspace is owned by the caller (at least
  * attn_masked_workspace_size bytes, 16-byte aligned; NULL allowed when that
  * size is 0).  attn_bwd_masked_stages runs a subset of the backward's
- * stages, as attn_bwd_varlen_stages (1: prep and mask packing, 2: dK / dV,
- * 4: dQ).
+ * stages, as attn_bwd_varlen_stages (1: prep and mask packing, 8: dQ with
+ * the row vectors and mask packing, 2: dK / dV, 4: dQ); attn_bwd_masked runs
+ * 8 then 2.
  */
 attn_status_t attn_fwd_masked(const void* q, const void* k, const void* v, void* o, float* lse,
                               int B, int H, int Hkv, int Nq, int Nk, int d, float scale, int causal,
@@ -346,10 +361,13 @@ attn_status_t attn_bwd_varlen(const void* q, const void* k, const void* v, const
 /*
  * The stages of attn_bwd_varlen, for callers that schedule (or time) them
  * separately: `stages` is a non-zero OR of 1 (prep: D and lse in base 2 into
- * the workspace), 2 (grad: dK, dV) and 4 (dq: dQ), run in that order.  The
- * ordering rules of attn_bwd_prep / _grad / _dq apply: prep completes before
- * grad or dq starts.  Other arguments as attn_bwd_varlen (all pointers are
- * checked whether or not the stage reads them).
+ * the workspace), 8 (dq_rows: dQ, forming and writing those row vectors),
+ * 2 (grad: dK, dV) and 4 (dq: dQ from the row vectors), run in that order;
+ * other bits are ATTN_ERR_INVALID_ARG.  The ordering rules of attn_bwd_prep /
+ * _grad / _dq / _dq_rows apply: the row vectors are complete before grad or
+ * dq starts.  attn_bwd_varlen runs 8 then 2.  Other arguments as
+ * attn_bwd_varlen (all pointers are checked whether or not the stage reads
+ * them).
  */
 attn_status_t attn_bwd_varlen_stages(const void* q, const void* k, const void* v, const void* o,
                                      const float* lse, const void* dout,

@@ -21,7 +21,7 @@ from .build import LIB, build  # noqa: F401  (build() is the supported way to co
 
 __all__ = [
     "AttnError", "Status", "load", "attn_fwd", "attn_bwd", "attn_bwd_workspace_size",
-    "attn_bwd_prep", "attn_bwd_grad", "attn_bwd_dq", "attn_bwd_noalloc",
+    "attn_bwd_prep", "attn_bwd_grad", "attn_bwd_dq", "attn_bwd_dq_rows", "attn_bwd_noalloc",
     "attn_get_device_status", "attn_get_timeout_info", "attn_status_string", "attn_selftest_wait_timeout",
     "attn_decode", "attn_decode_workspace_size", "attn_fwd_cross", "attn_bwd_cross",
     "attn_bwd_grad_cross", "attn_bwd_dq_cross", "attn_fwd_varlen", "attn_bwd_varlen",
@@ -99,6 +99,9 @@ def load() -> ctypes.CDLL:
         lib.attn_bwd_dq_cross.argtypes = [_P, _P, _P, _P, _P, _P, ctypes.c_size_t,
                                           _I, _I, _I, _I, _I, _I, ctypes.c_float, _I, _P]
         lib.attn_bwd_dq_cross.restype = _I
+        lib.attn_bwd_dq_rows.argtypes = [_P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t,
+                                         _I, _I, _I, _I, _I, _I, ctypes.c_float, _I, _P]
+        lib.attn_bwd_dq_rows.restype = _I
         lib.attn_fwd_varlen.argtypes = [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I,
                                         ctypes.c_float, _I, _P]
         lib.attn_fwd_varlen.restype = _I
@@ -185,6 +188,12 @@ def attn_bwd_grad(q, k, v, dout, dk, dv, workspace, workspace_bytes, B, H, Hkv, 
 
 def attn_bwd_dq(q, k, v, dout, dq, workspace, workspace_bytes, B, H, Hkv, N, d, scale, causal, stream) -> int:
     return load().attn_bwd_dq(q, k, v, dout, dq, workspace, workspace_bytes, B, H, Hkv, N, d, scale, causal, stream)
+
+
+def attn_bwd_dq_rows(q, k, v, o, lse, dout, dq, workspace, workspace_bytes, B, H, Hkv, Nq, Nk, d, scale, causal,
+                     stream) -> int:
+    return load().attn_bwd_dq_rows(q, k, v, o, lse, dout, dq, workspace, workspace_bytes, B, H, Hkv, Nq, Nk, d,
+                                   scale, int(causal), stream)
 
 
 def attn_fwd_cross(q, k, v, o, lse, B, H, Hkv, Nq, Nk, d, scale, causal, stream) -> int:

@@ -449,7 +449,33 @@ static attn_status_t bwd_dq_x(const void* q, const void* k, const void* v, const
   sdpa::BwdParams p;
   bwd_params(&p, workspace, B, H, Hkv, Nq, Nk, d, scale, causal, di);
   p.dq = static_cast<uint16_t*>(dq);
-  cudaError_t e = sdpa::launch_bwd_dq(d, causal != 0, tq, tk, tv, tdo, tdq, p, static_cast<cudaStream_t>(stream));
+  cudaError_t e =
+      sdpa::launch_bwd_dq(d, causal != 0, tq, tk, tv, tdo, tdq, tq, p, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;
+}
+
+// The dQ stage that forms and writes the row vectors itself (from o, lse,
+// dout): replaces prep + dq, and grad runs after it.
+static attn_status_t bwd_dq_rows_x(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                                   const void* dout, void* dq, void* workspace, size_t workspace_bytes, int B, int H,
+                                   int Hkv, int Nq, int Nk, int d, float scale, int causal, void* stream) {
+  ATTN_TRY(check_scale_flag(scale, causal));
+  ATTN_TRY(check_bwd_shape(B, H, Hkv, Nq, Nk, d, causal));
+  ATTN_TRY(check_workspace(workspace, workspace_bytes, B, H, Hkv, Nq, d));
+  ATTN_TRY(check_ptrs({q, k, v, o, lse, dout, dq, workspace}));
+  DeviceInfo* di = nullptr;
+  ATTN_TRY(current_device(&di));
+  CUtensorMap tq, tk, tv, tdo, tdq, to;
+  if (!make_map_bf16(&tq, q, d, Nq, (long long)B * H) || !make_map_bf16(&tk, k, d, Nk, (long long)B * Hkv) ||
+      !make_map_bf16(&tv, v, d, Nk, (long long)B * Hkv) || !make_map_bf16(&tdo, dout, d, Nq, (long long)B * H) ||
+      !make_map_bf16(&tdq, dq, d, Nq, (long long)B * H) || !make_map_bf16(&to, o, d, Nq, (long long)B * H))
+    return ATTN_ERR_CUDA;
+  sdpa::BwdParams p;
+  bwd_params(&p, workspace, B, H, Hkv, Nq, Nk, d, scale, causal, di);
+  p.dq = static_cast<uint16_t*>(dq);
+  p.lse = lse;
+  p.rows_in_dq = 1;
+  cudaError_t e = sdpa::launch_bwd_dq(d, causal != 0, tq, tk, tv, tdo, tdq, to, p, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;
 }
 
@@ -461,9 +487,9 @@ static attn_status_t bwd_all(const void* q, const void* k, const void* v, const 
   ATTN_TRY(check_bwd_shape(B, H, Hkv, Nq, Nk, d, causal));
   ATTN_TRY(check_workspace(workspace, workspace_bytes, B, H, Hkv, Nq, d));
   ATTN_TRY(check_ptrs({q, k, v, o, lse, dout, dq, dk, dv, workspace}));
-  ATTN_TRY(bwd_prep_x(o, lse, dout, workspace, workspace_bytes, B, H, Hkv, Nq, d, stream));
-  ATTN_TRY(bwd_grad_x(q, k, v, dout, dk, dv, workspace, workspace_bytes, B, H, Hkv, Nq, Nk, d, scale, causal, stream));
-  return bwd_dq_x(q, k, v, dout, dq, workspace, workspace_bytes, B, H, Hkv, Nq, Nk, d, scale, causal, stream);
+  ATTN_TRY(bwd_dq_rows_x(q, k, v, o, lse, dout, dq, workspace, workspace_bytes, B, H, Hkv, Nq, Nk, d, scale, causal,
+                         stream));
+  return bwd_grad_x(q, k, v, dout, dk, dv, workspace, workspace_bytes, B, H, Hkv, Nq, Nk, d, scale, causal, stream);
 }
 
 attn_status_t attn_bwd_prep(const void* o, const float* lse, const void* dout, void* workspace,
@@ -481,6 +507,13 @@ attn_status_t attn_bwd_dq(const void* q, const void* k, const void* v, const voi
                           size_t workspace_bytes, int B, int H, int Hkv, int N, int d, float scale, int causal,
                           void* stream) {
   return bwd_dq_x(q, k, v, dout, dq, workspace, workspace_bytes, B, H, Hkv, N, N, d, scale, causal, stream);
+}
+
+attn_status_t attn_bwd_dq_rows(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                               const void* dout, void* dq, void* workspace, size_t workspace_bytes, int B, int H,
+                               int Hkv, int Nq, int Nk, int d, float scale, int causal, void* stream) {
+  return bwd_dq_rows_x(q, k, v, o, lse, dout, dq, workspace, workspace_bytes, B, H, Hkv, Nq, Nk, d, scale, causal,
+                       stream);
 }
 
 attn_status_t attn_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
@@ -518,7 +551,7 @@ size_t attn_bwd_varlen_workspace_size(int B, int H, int Hkv, int total_q, int d)
 // maps and kernel arguments.  Maps for arguments a stage does not use are
 // built over placeholders that stay valid (they are never read).
 struct VarlenBwd {
-  CUtensorMap tq, tk, tv, tdo, tdq, tdk, tdv;
+  CUtensorMap tq, tk, tv, tdo, tdq, tdk, tdv, to;
   sdpa::BwdParams p;
 };
 
@@ -538,7 +571,7 @@ static attn_status_t varlen_bwd_setup(VarlenBwd* w, const void* q, const void* k
   if (!make_map_bf16_packed(&w->tq, q, d, total_q, H) || !make_map_bf16_packed(&w->tk, k, d, total_k, Hkv) ||
       !make_map_bf16_packed(&w->tv, v, d, total_k, Hkv) || !make_map_bf16_packed(&w->tdo, dout, d, total_q, H) ||
       !make_map_bf16_packed(&w->tdq, dq, d, total_q, H) || !make_map_bf16_packed(&w->tdk, dk, d, total_k, Hkv) ||
-      !make_map_bf16_packed(&w->tdv, dv, d, total_k, Hkv))
+      !make_map_bf16_packed(&w->tdv, dv, d, total_k, Hkv) || !make_map_bf16_packed(&w->to, o, d, total_q, H))
     return ATTN_ERR_CUDA;
   sdpa::BwdParams& p = w->p;
   memset(&p, 0, sizeof(p));
@@ -572,7 +605,7 @@ static attn_status_t varlen_bwd_setup(VarlenBwd* w, const void* q, const void* k
   return ATTN_OK;
 }
 
-enum : unsigned { kStagePrep = 1, kStageGrad = 2, kStageDq = 4 };
+enum : unsigned { kStagePrep = 1, kStageGrad = 2, kStageDq = 4, kStageDqRows = 8, kStagesAll = 15 };
 
 static attn_status_t varlen_bwd_run(const void* q, const void* k, const void* v, const void* o, const float* lse,
                                     const void* dout, void* dq, void* dk, void* dv, const int* cu_q, const int* cu_k,
@@ -584,10 +617,17 @@ static attn_status_t varlen_bwd_run(const void* q, const void* k, const void* v,
                             Hkv, total_q, total_k, max_q, max_k, d, scale, causal));
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
   if ((stages & kStagePrep) && sdpa::launch_bwd_prep(w.p, st) != cudaSuccess) return ATTN_ERR_LAUNCH;
+  if (stages & kStageDqRows) {
+    sdpa::BwdParams pr = w.p;
+    pr.rows_in_dq = 1;
+    if (sdpa::launch_bwd_dq(d, causal != 0, w.tq, w.tk, w.tv, w.tdo, w.tdq, w.to, pr, st) != cudaSuccess)
+      return ATTN_ERR_LAUNCH;
+  }
   if ((stages & kStageGrad) &&
       sdpa::launch_bwd_grad(d, causal != 0, w.tq, w.tk, w.tv, w.tdo, w.tdk, w.tdv, w.p, st) != cudaSuccess)
     return ATTN_ERR_LAUNCH;
-  if ((stages & kStageDq) && sdpa::launch_bwd_dq(d, causal != 0, w.tq, w.tk, w.tv, w.tdo, w.tdq, w.p, st) != cudaSuccess)
+  if ((stages & kStageDq) &&
+      sdpa::launch_bwd_dq(d, causal != 0, w.tq, w.tk, w.tv, w.tdo, w.tdq, w.to, w.p, st) != cudaSuccess)
     return ATTN_ERR_LAUNCH;
   return ATTN_OK;
 }
@@ -599,7 +639,7 @@ attn_status_t attn_bwd_varlen(const void* q, const void* k, const void* v, const
                               float scale, int causal, void* stream) {
   return varlen_bwd_run(q, k, v, o, lse, dout, dq, dk, dv, cu_seqlens_q, cu_seqlens_k, workspace, workspace_bytes,
                         B, H, Hkv, total_q, total_k, max_seqlen_q, max_seqlen_k, d, scale, causal, stream,
-                        kStagePrep | kStageGrad | kStageDq);
+                        kStageDqRows | kStageGrad);
 }
 
 attn_status_t attn_bwd_varlen_stages(const void* q, const void* k, const void* v, const void* o, const float* lse,
@@ -607,7 +647,7 @@ attn_status_t attn_bwd_varlen_stages(const void* q, const void* k, const void* v
                                      const int* cu_seqlens_k, void* workspace, size_t workspace_bytes, int B, int H,
                                      int Hkv, int total_q, int total_k, int max_seqlen_q, int max_seqlen_k, int d,
                                      float scale, int causal, unsigned stages, void* stream) {
-  if (stages == 0 || (stages & ~7u) != 0) return ATTN_ERR_INVALID_ARG;
+  if (stages == 0 || (stages & ~kStagesAll) != 0) return ATTN_ERR_INVALID_ARG;
   return varlen_bwd_run(q, k, v, o, lse, dout, dq, dk, dv, cu_seqlens_q, cu_seqlens_k, workspace, workspace_bytes,
                         B, H, Hkv, total_q, total_k, max_seqlen_q, max_seqlen_k, d, scale, causal, stream, stages);
 }
@@ -784,7 +824,7 @@ attn_status_t attn_bwd_masked_stages(const void* q, const void* k, const void* v
                                      const void* dout, void* dq, void* dk, void* dv, int B, int H, int Hkv, int Nq,
                                      int Nk, int d, float scale, int causal, const attn_mask_t* mask, void* workspace,
                                      size_t workspace_bytes, unsigned stages, void* stream) {
-  if (stages == 0 || (stages & ~7u) != 0) return ATTN_ERR_INVALID_ARG;
+  if (stages == 0 || (stages & ~kStagesAll) != 0) return ATTN_ERR_INVALID_ARG;
   ATTN_TRY(check_shape(B, H, Hkv, Nq, d));
   ATTN_TRY(check_shape(B, H, Hkv, Nk, d));
   ATTN_TRY(check_scale_flag(scale, causal));
@@ -795,11 +835,11 @@ attn_status_t attn_bwd_masked_stages(const void* q, const void* k, const void* v
   ATTN_TRY(check_mask_ptrs(mask));
   DeviceInfo* di = nullptr;
   ATTN_TRY(current_device(&di));
-  CUtensorMap tq, tk, tv, tdo, tdq, tdk, tdv;
+  CUtensorMap tq, tk, tv, tdo, tdq, tdk, tdv, to;
   if (!make_map_bf16(&tq, q, d, Nq, (long long)B * H) || !make_map_bf16(&tk, k, d, Nk, (long long)B * Hkv) ||
       !make_map_bf16(&tv, v, d, Nk, (long long)B * Hkv) || !make_map_bf16(&tdo, dout, d, Nq, (long long)B * H) ||
       !make_map_bf16(&tdq, dq, d, Nq, (long long)B * H) || !make_map_bf16(&tdk, dk, d, Nk, (long long)B * Hkv) ||
-      !make_map_bf16(&tdv, dv, d, Nk, (long long)B * Hkv))
+      !make_map_bf16(&tdv, dv, d, Nk, (long long)B * Hkv) || !make_map_bf16(&to, o, d, Nq, (long long)B * H))
     return ATTN_ERR_CUDA;
   // Workspace: [row vectors | row bits | transposed bits | tile flags].
   const MaskGeom g = mask_geom(Nq, Nk, mask);
@@ -817,16 +857,20 @@ attn_status_t attn_bwd_masked_stages(const void* q, const void* k, const void* v
   p.dk = static_cast<uint16_t*>(dk);
   p.dv = static_cast<uint16_t*>(dv);
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (stages & 1u) {
-    if (sdpa::launch_bwd_prep(p, st) != cudaSuccess) return ATTN_ERR_LAUNCH;
-    if (mask->mask != nullptr &&
-        sdpa::launch_mask_pack(static_cast<const uint8_t*>(mask->mask), mask->mask_batch, mask->mask_heads, Nq, Nk,
-                               bits, g.words, bits_t, g.words_t, flags, st) != cudaSuccess)
-      return ATTN_ERR_LAUNCH;
-  }
-  if ((stages & 2u) && sdpa::launch_bwd_grad(d, false, tq, tk, tv, tdo, tdk, tdv, p, st, true) != cudaSuccess)
+  // The mask is packed once, by the first of stages 1 and 8 that runs.
+  if ((stages & (kStagePrep | kStageDqRows)) && mask->mask != nullptr &&
+      sdpa::launch_mask_pack(static_cast<const uint8_t*>(mask->mask), mask->mask_batch, mask->mask_heads, Nq, Nk,
+                             bits, g.words, bits_t, g.words_t, flags, st) != cudaSuccess)
     return ATTN_ERR_LAUNCH;
-  if ((stages & 4u) && sdpa::launch_bwd_dq(d, false, tq, tk, tv, tdo, tdq, p, st, true) != cudaSuccess)
+  if ((stages & kStagePrep) && sdpa::launch_bwd_prep(p, st) != cudaSuccess) return ATTN_ERR_LAUNCH;
+  if (stages & kStageDqRows) {
+    sdpa::BwdParams pr = p;
+    pr.rows_in_dq = 1;
+    if (sdpa::launch_bwd_dq(d, false, tq, tk, tv, tdo, tdq, to, pr, st, true) != cudaSuccess) return ATTN_ERR_LAUNCH;
+  }
+  if ((stages & kStageGrad) && sdpa::launch_bwd_grad(d, false, tq, tk, tv, tdo, tdk, tdv, p, st, true) != cudaSuccess)
+    return ATTN_ERR_LAUNCH;
+  if ((stages & kStageDq) && sdpa::launch_bwd_dq(d, false, tq, tk, tv, tdo, tdq, to, p, st, true) != cudaSuccess)
     return ATTN_ERR_LAUNCH;
   return ATTN_OK;
 }
@@ -836,7 +880,7 @@ attn_status_t attn_bwd_masked(const void* q, const void* k, const void* v, const
                               int d, float scale, int causal, const attn_mask_t* mask, void* workspace,
                               size_t workspace_bytes, void* stream) {
   return attn_bwd_masked_stages(q, k, v, o, lse, dout, dq, dk, dv, B, H, Hkv, Nq, Nk, d, scale, causal, mask,
-                                workspace, workspace_bytes, 7u, stream);
+                                workspace, workspace_bytes, kStageDqRows | kStageGrad, stream);
 }
 
 // Key chunks of the decode kernel, a pure function of the shape (so the

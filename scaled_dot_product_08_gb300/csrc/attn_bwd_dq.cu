@@ -15,7 +15,11 @@
 //               thread per query row: S -> P (registers), dP -> dS (bf16
 //               pairs back into its S columns, the A operand of the dQ MMA);
 //               then half of the dQ epilogue
-//   warp  8     TMA producer: Q_i, dO_i once; K_j (3-slot ring), V_j (2-slot)
+//   warp  8     TMA producer: Q_i, dO_i once; K_j (3-slot ring), V_j (2-slot);
+//               with p.rows_in_dq, O_i once into K slot 2 before K_2
+//               (the compute threads then form D_i = rowsum(dO_i * O_i) and
+//               lse_i in base 2, use them, and write them for the dK/dV
+//               kernel; otherwise they read them from the workspace)
 //   warp  9     MMA issuer (one elected lane issues)
 //   warps 10-11 idle
 // Tensor memory: S[0] [0,128), S[1] [128,256) (double-buffered, so S_{j+2}
@@ -34,18 +38,29 @@ struct DqTraits {
   static constexpr int TILE_BYTES = NB * BLOCK_BYTES;  // one [128 rows x d] bf16 tile
   static constexpr int KSTEPS = D / 16;
   static constexpr int KS = 3, VS = 2;                 // K and V ring slots
-  static constexpr int NBAR = 18;
+  static constexpr int NBAR = 20;
   static constexpr int MISC = 64;                      // tmem slot, abort flag, per-CTA values
   static constexpr int SMEM = 1024 + (2 + KS + VS) * TILE_BYTES + NBAR * 8 + MISC + 2 * kMaxTileList;
   static constexpr int THREADS = 384;
 };
+
+// A query tile none of whose rows sees a key: its rows' vectors for the
+// dK/dV kernel, -lse2 = -inf (P = 0) and -D = 0, one thread per row.
+__device__ __noinline__ void no_key_vectors(const BwdParams& p, bool varlen, int q0, int b, int bh, int h, int i) {
+  if (threadIdx.x >= 128) return;
+  const size_t vrow = (varlen ? (size_t)h * p.vec_stride + (size_t)varlen_vec_offset(q0, b) : (size_t)bh * p.Npad) +
+                      (size_t)i * 128 + threadIdx.x;
+  p.dvec[vrow] = 0.f;
+  p.lse2[vrow] = -INFINITY;
+}
 
 // MASKED: the instance that applies p.mk (causal enters as wr = 0).
 template <int D, bool CAUSAL, bool MASKED>
 __global__ void __launch_bounds__(384, 1)
     bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
-                  const __grid_constant__ CUtensorMap tmdQ, const BwdParams p) {
+                  const __grid_constant__ CUtensorMap tmdQ, const __grid_constant__ CUtensorMap tmO,
+                  const BwdParams p) {
   using T = DqTraits<D>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -68,7 +83,9 @@ __global__ void __launch_bounds__(384, 1)
   const uint32_t bDs = bDpc + 8;             // dS_j in TMEM (256 arrivals)
   const uint32_t bFin = bDs + 8;             // dQ_i final
   const uint32_t bDrain = bFin + 8;
-  static_assert(1 + 2 * 3 + 2 * 2 + 2 + 5 == 18, "barrier count");
+  const uint32_t bO = bDrain + 8;            // O_i loaded into K slot 2 (row vectors formed here)
+  const uint32_t bOc = bO + 8;               // O_i read (256 arrivals): K slot 2 free for K_2
+  static_assert(1 + 2 * 3 + 2 * 2 + 2 + 5 + 2 == 20, "barrier count");
   uint8_t* const misc = gbase + (sBar - base) + 8 * T::NBAR;
   uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(misc);
   volatile int* const abort_flag = reinterpret_cast<volatile int*>(misc + 4);
@@ -117,6 +134,7 @@ __global__ void __launch_bounds__(384, 1)
     if (n <= 0) {
       // No row of the tile sees a key (packed batches, masks): dQ = 0.
       // Packed: (total, H, d) rows; dense: the (b, h) plane of (B, H, Nq, d).
+      if (p.rows_in_dq) no_key_vectors(p, varlen, sq.q0, b, bh, h, i);
       const uint32_t rs = varlen ? (uint32_t)(p.H * D) : (uint32_t)D;
       uint16_t* dst = varlen ? p.dq + ((long long)sq.q0 + 128 * i) * rs + (long long)h * D
                              : p.dq + ((long long)bh * p.N + 128 * i) * D;
@@ -161,6 +179,7 @@ __global__ void __launch_bounds__(384, 1)
     if (seq_s[7]) {
       n = seq_s[8];
       if (n == 0) {
+        if (p.rows_in_dq) no_key_vectors(p, varlen, seq_s[0], b, bh, h, i);
         const uint32_t rs = varlen ? (uint32_t)(p.H * D) : (uint32_t)D;
         uint16_t* dst = varlen ? p.dq + ((long long)seq_s[0] + 128 * i) * rs + (long long)h * D
                                : p.dq + ((long long)bh * p.N + 128 * i) * D;
@@ -189,6 +208,8 @@ __global__ void __launch_bounds__(384, 1)
     mbar_init(bDs, 256);
     mbar_init(bFin, 1);
     mbar_init(bDrain, 1);
+    mbar_init(bO, 1);
+    mbar_init(bOc, 256);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -212,8 +233,56 @@ __global__ void __launch_bounds__(384, 1)
     const uint32_t tdP = tmem + 256 + 64 * X + lane_off;
     const size_t vrow = (varlen ? (size_t)h * p.vec_stride + (size_t)varlen_vec_offset(seq_s[0], b)
                                 : (size_t)bh * p.Npad) + (size_t)i * 128 + r;
-    const float l2 = p.lse2[vrow];   // -lse * log2(e); -inf on padding rows (P = 0 there)
-    const float nD = p.dvec[vrow];   // -D
+    float l2, nD;  // -lse * log2(e) (-inf on padding rows: P = 0 there) and -D
+    bool rows_ok = true;
+    if (p.rows_in_dq) {
+      // This kernel forms its rows' vectors itself and writes them for the
+      // dK/dV kernel: O_i arrives by TMA in K slot 2 (free until K_2), dO_i
+      // is already in shared memory.  Warpgroup X sums its half of the
+      // columns, [X d / 2, (X + 1) d / 2), of dO_r * O_r; the halves meet
+      // through tensor-memory columns 384 + X of lane r (dQ columns, which no
+      // MMA writes before every thread has passed dS_0).  Every compute
+      // thread reaches the barriers below, whatever the waits return.
+      rows_ok = __all_sync(0xffffffffu, wait_bounded(wc, bQ, 0, wait_site(0x84, 0)) &&
+                                            wait_bounded(wc, bO, 0, wait_site(0x85, 0)));
+      const int row = 128 * i + r;
+      float part = 0.f, l = -INFINITY;
+      if (rows_ok && row < seq_s[1]) {
+        l = varlen ? p.lse[(size_t)h * p.vl.total_q + seq_s[0] + row] : p.lse[(size_t)bh * p.N + row];
+        const uint32_t sO = sK + 2 * T::TILE_BYTES;
+#pragma unroll
+        for (int cc = X * (D / 16); cc < (X + 1) * (D / 16); ++cc) {
+          const uint32_t off = (uint32_t)(cc >> 3) * T::BLOCK_BYTES + sw128_offset(r, cc & 7);
+          const uint4 a = ld_shared_v4u(sO + off), g = ld_shared_v4u(sdO + off);
+          const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, gw[4] = {g.x, g.y, g.z, g.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float2 af = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&aw[e]));
+            const float2 gf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&gw[e]));
+            part = fmaf(af.x, gf.x, part);
+            part = fmaf(af.y, gf.y, part);
+          }
+        }
+      }
+      mbar_arrive(bOc);  // O_i read: the producer may load K_2 over it
+      tmem_st1(tmem + 384 + X + lane_off, __float_as_uint(part));
+      tmem_wait_st();
+      tc_fence_before();
+      named_bar_sync_c<2, 256>();
+      tc_fence_after();
+      uint32_t other = tmem_ld1(tmem + 384 + (1 - X) + lane_off);
+      tmem_wait_ld();
+      asm volatile("" : "+r"(other));
+      nD = row < seq_s[1] ? -(part + __uint_as_float(other)) : 0.f;
+      l2 = (l == -INFINITY) ? -INFINITY : -l * 1.4426950408889634f;
+      if (X == 0 && rows_ok) {
+        p.dvec[vrow] = nD;
+        p.lse2[vrow] = l2;
+      }
+    } else {
+      l2 = p.lse2[vrow];
+      nD = p.dvec[vrow];
+    }
     const float2 c2 = make_float2(p.scale_log2, p.scale_log2);
     const float2 l22 = make_float2(l2, l2), nD2 = make_float2(nD, nD);
     // Key columns at or past lim0 - 128 j of the j-th visited key tile are
@@ -235,8 +304,8 @@ __global__ void __launch_bounds__(384, 1)
     } else {
       lim0 = (CAUSAL ? min(seq_s[3], seq_s[3] - seq_s[1] + 128 * i + r + 1) : seq_s[3]) - 64 * X;
     }
-    bool ok = true;
-    for (int j = 0; j < n; ++j) {
+    bool ok = rows_ok;
+    for (int j = 0; j < n && ok; ++j) {
       const uint32_t tS = tmem + (j & 1) * 128 + 64 * X + lane_off;
       uint2 bt = make_uint2(~0u, ~0u);
       const int jt = MASKED ? tile_at(j) : j;  // key tile relative to jlo
@@ -370,9 +439,11 @@ __global__ void __launch_bounds__(384, 1)
           tma_load_3d(sdO + cb * T::BLOCK_BYTES, &tmdO, bQ, cb * 64, q0 + i * 128, qplane);
         }
         int issued = 0;
+        bool o_issued = false;
         for (int j = 0; j < n; ++j) {
           const int ks = j % T::KS, kr = j / T::KS, vs = j % T::VS, vr = j / T::VS;
           if (kr > 0 && !wait_bounded(wc, bKe + 8u * ks, (kr - 1) & 1, wait_site(0x91, j))) break;
+          if (o_issued && j == 2 && !wait_bounded(wc, bOc, 0, wait_site(0x93, j))) break;
           mbar_expect_tx(bKf + 8u * ks, T::TILE_BYTES);
           for (int cb = 0; cb < T::NB; ++cb)
             tma_load_3d(sK + ks * T::TILE_BYTES + cb * T::BLOCK_BYTES, &tmK, bKf + 8u * ks, cb * 64,
@@ -384,9 +455,17 @@ __global__ void __launch_bounds__(384, 1)
             tma_load_3d(sV + vs * T::TILE_BYTES + cb * T::BLOCK_BYTES, &tmV, bVf + 8u * vs, cb * 64,
                         k0 + tile_at(j) * 128, kplane);
           issued = 2 * j + 2;
+          if (j == 0 && p.rows_in_dq) {
+            // O_i for the row vectors, after the tiles of the first step
+            mbar_expect_tx(bO, T::TILE_BYTES);
+            for (int cb = 0; cb < T::NB; ++cb)
+              tma_load_3d(sK + 2 * T::TILE_BYTES + cb * T::BLOCK_BYTES, &tmO, bO, cb * 64, q0 + i * 128, qplane);
+            o_issued = true;
+          }
         }
         // Every copy issued above has landed before the CTA may exit.
         wait_drain(bQ, 0, p.limit_ns);
+        if (o_issued) wait_drain(bO, 0, p.limit_ns);
         const int nk = (issued + 1) / 2, nv = issued / 2;  // K_0..K_{nk-1}, V_0..V_{nv-1} issued
         for (int s = 0; s < T::KS && s < nk; ++s) {
           const int last = ((nk - 1 - s) / T::KS) * T::KS + s;
@@ -498,34 +577,34 @@ size_t bwd_dq_smem_bytes(int d) {
 
 template <int D, bool C, bool M = false>
 static cudaError_t launch_dq_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                               const CUtensorMap& tdo, const CUtensorMap& tdq, const BwdParams& p,
-                               cudaStream_t stream) {
+                               const CUtensorMap& tdo, const CUtensorMap& tdq, const CUtensorMap& to,
+                               const BwdParams& p, cudaStream_t stream) {
   auto kern = bwd_dq_kernel<D, C, M>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, DqTraits<D>::SMEM);
   if (e != cudaSuccess) return e;
   const unsigned grid = (unsigned)p.nq * (unsigned)(p.B * p.H);
-  kern<<<grid, DqTraits<D>::THREADS, DqTraits<D>::SMEM, stream>>>(tq, tk, tv, tdo, tdq, p);
+  kern<<<grid, DqTraits<D>::THREADS, DqTraits<D>::SMEM, stream>>>(tq, tk, tv, tdo, tdq, to, p);
   return cudaGetLastError();
 }
 
 cudaError_t launch_bwd_dq(int d, bool causal, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                          const CUtensorMap& tdo, const CUtensorMap& tdq, const BwdParams& p, cudaStream_t stream,
-                          bool masked) {
+                          const CUtensorMap& tdo, const CUtensorMap& tdq, const CUtensorMap& to, const BwdParams& p,
+                          cudaStream_t stream, bool masked) {
   if (masked) {
     switch (d) {
-      case 64: return launch_dq_t<64, false, true>(tq, tk, tv, tdo, tdq, p, stream);
-      case 96: return launch_dq_t<96, false, true>(tq, tk, tv, tdo, tdq, p, stream);
-      case 128: return launch_dq_t<128, false, true>(tq, tk, tv, tdo, tdq, p, stream);
+      case 64: return launch_dq_t<64, false, true>(tq, tk, tv, tdo, tdq, to, p, stream);
+      case 96: return launch_dq_t<96, false, true>(tq, tk, tv, tdo, tdq, to, p, stream);
+      case 128: return launch_dq_t<128, false, true>(tq, tk, tv, tdo, tdq, to, p, stream);
       default: return cudaErrorInvalidValue;
     }
   }
   switch (d) {
-    case 64: return causal ? launch_dq_t<64, true>(tq, tk, tv, tdo, tdq, p, stream)
-                           : launch_dq_t<64, false>(tq, tk, tv, tdo, tdq, p, stream);
-    case 96: return causal ? launch_dq_t<96, true>(tq, tk, tv, tdo, tdq, p, stream)
-                           : launch_dq_t<96, false>(tq, tk, tv, tdo, tdq, p, stream);
-    case 128: return causal ? launch_dq_t<128, true>(tq, tk, tv, tdo, tdq, p, stream)
-                            : launch_dq_t<128, false>(tq, tk, tv, tdo, tdq, p, stream);
+    case 64: return causal ? launch_dq_t<64, true>(tq, tk, tv, tdo, tdq, to, p, stream)
+                           : launch_dq_t<64, false>(tq, tk, tv, tdo, tdq, to, p, stream);
+    case 96: return causal ? launch_dq_t<96, true>(tq, tk, tv, tdo, tdq, to, p, stream)
+                           : launch_dq_t<96, false>(tq, tk, tv, tdo, tdq, to, p, stream);
+    case 128: return causal ? launch_dq_t<128, true>(tq, tk, tv, tdo, tdq, to, p, stream)
+                            : launch_dq_t<128, false>(tq, tk, tv, tdo, tdq, to, p, stream);
     default: return cudaErrorInvalidValue;
   }
 }

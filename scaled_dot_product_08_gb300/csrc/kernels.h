@@ -71,6 +71,7 @@ struct BwdParams {
   const float* lse;      // (B, H, N)
   float* dvec;           // (B, H, Npad) float32 workspace: -D = -rowsum(dO * O)
   float* lse2;           // (B, H, Npad) float32 workspace: -lse * log2(e), -inf on padding rows
+  int rows_in_dq;        // 1: the dQ kernel forms -D and -lse2 from o, dout, lse and writes them
   int B, H, Hkv, N, Npad, G, d;  // N: query rows per head (Npad: rounded up to 128)
   int nq;                // ceil(N / 128): query tiles
   int Nk, nkv;           // key/value rows per head, ceil(Nk / 128) key tiles
@@ -175,9 +176,10 @@ cudaError_t launch_bwd_prep(const BwdParams& p, cudaStream_t stream);
 cudaError_t launch_bwd_grad(int d, bool causal, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                             const CUtensorMap& tdo, const CUtensorMap& tdk, const CUtensorMap& tdv,
                             const BwdParams& p, cudaStream_t stream, bool masked = false);
+// `to` (a map over O laid out as Q) is read only when p.rows_in_dq is set.
 cudaError_t launch_bwd_dq(int d, bool causal, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                          const CUtensorMap& tdo, const CUtensorMap& tdq, const BwdParams& p, cudaStream_t stream,
-                          bool masked = false);
+                          const CUtensorMap& tdo, const CUtensorMap& tdq, const CUtensorMap& to, const BwdParams& p,
+                          cudaStream_t stream, bool masked = false);
 // Packs a boolean (mask_b, mask_h, Nq, Nk) byte mask into the row and
 // transposed bit layouts of MaskArgs (bits_t may be null: row bits only).
 cudaError_t launch_mask_pack(const uint8_t* mask, int mask_b, int mask_h, int Nq, int Nk, uint32_t* bits,

@@ -11,7 +11,7 @@ import pytest
 
 import oracle
 from sdpa_inputs import make_inputs, make_random, workload
-from tests.parity import check_grads, dev, host, rel_fro
+from tests.parity import check_same_but_rounding, check_grads, dev, host, rel_fro
 
 pytestmark = pytest.mark.gpu
 
@@ -125,7 +125,9 @@ def test_backward_outputs_stay_inside_buffers_and_workspace_checks(cuda_lib):
 
 
 def test_backward_stages_equal_the_combined_call(cuda_lib):
-    # attn_bwd_prep + attn_bwd_grad + attn_bwd_dq on one stream equal attn_bwd.
+    # attn_bwd_dq_rows + attn_bwd_grad on one stream are attn_bwd, bit for
+    # bit; attn_bwd_prep + attn_bwd_grad + attn_bwd_dq differ only by the
+    # order of D's float32 additions, and both write the same row vectors.
     import torch
     B, H, Hkv, N, d = 1, 4, 2, 260, 96
     q = dev(make_random((B, H, N, d), 111))
@@ -134,19 +136,36 @@ def test_backward_stages_equal_the_combined_call(cuda_lib):
     do = dev(make_random((B, H, N, d), 114))
     O, lse = cuda_lib.forward(q, k, v, 0.1, False)
     ref = [host(g) for g in cuda_lib.backward(q, k, v, O, lse, do, 0.1, False)]
-    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     ws_bytes = cuda_lib.attn_bwd_workspace_size(B, H, Hkv, N, d)
-    ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
     sp = torch.cuda.current_stream().cuda_stream
-    assert cuda_lib.attn_bwd_prep(O.data_ptr(), lse.data_ptr(), do.data_ptr(), ws.data_ptr(), ws_bytes,
-                                  B, H, Hkv, N, d, sp) == 0
-    assert cuda_lib.attn_bwd_grad(q.data_ptr(), k.data_ptr(), v.data_ptr(), do.data_ptr(), dk.data_ptr(),
-                                  dv.data_ptr(), ws.data_ptr(), ws_bytes, B, H, Hkv, N, d, 0.1, 0, sp) == 0
-    assert cuda_lib.attn_bwd_dq(q.data_ptr(), k.data_ptr(), v.data_ptr(), do.data_ptr(), dq.data_ptr(),
-                                ws.data_ptr(), ws_bytes, B, H, Hkv, N, d, 0.1, 0, sp) == 0
-    got = [host(g) for g in (dq, dk, dv)]
-    for g, r in zip(got, ref):
-        assert np.array_equal(g, r)
+    P = lambda t: t.data_ptr()
+    vecs = []
+    for order in ("rows", "prep"):
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        ws = torch.full((ws_bytes // 4,), float("nan"), dtype=torch.float32, device="cuda")
+        if order == "rows":
+            assert cuda_lib.attn_bwd_dq_rows(P(q), P(k), P(v), P(O), P(lse), P(do), P(dq), P(ws), ws_bytes,
+                                             B, H, Hkv, N, N, d, 0.1, 0, sp) == 0
+            assert cuda_lib.attn_bwd_grad(P(q), P(k), P(v), P(do), P(dk), P(dv), P(ws), ws_bytes,
+                                          B, H, Hkv, N, d, 0.1, 0, sp) == 0
+        else:
+            assert cuda_lib.attn_bwd_prep(P(O), P(lse), P(do), P(ws), ws_bytes, B, H, Hkv, N, d, sp) == 0
+            assert cuda_lib.attn_bwd_grad(P(q), P(k), P(v), P(do), P(dk), P(dv), P(ws), ws_bytes,
+                                          B, H, Hkv, N, d, 0.1, 0, sp) == 0
+            assert cuda_lib.attn_bwd_dq(P(q), P(k), P(v), P(do), P(dq), P(ws), ws_bytes,
+                                        B, H, Hkv, N, d, 0.1, 0, sp) == 0
+        got = [host(g) for g in (dq, dk, dv)]
+        if order == "rows":
+            for g, r in zip(got, ref):
+                assert np.array_equal(g, r)
+        else:
+            check_same_but_rounding(got, ref, "prep + grad + dq")
+        vecs.append(ws.cpu().numpy().reshape(2, B * H, -1))
+    # -D close, -lse2 identical; the padding rows (260..383) -D = 0, -lse2 = -inf
+    assert np.allclose(vecs[0][0], vecs[1][0], rtol=1e-5, atol=1e-6)
+    assert np.array_equal(vecs[0][1], vecs[1][1])
+    for vv in vecs:
+        assert np.all(vv[0][:, N:] == 0) and np.all(np.isneginf(vv[1][:, N:]))
 
 
 def test_backward_is_deterministic(cuda_lib):

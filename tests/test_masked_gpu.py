@@ -172,3 +172,39 @@ def test_mask_bytes_nonzero_values_and_unaligned_base(cuda_lib):
         for a, b in zip(g1, g0):
             assert np.array_equal(host(a), host(b))
     assert cuda_lib.attn_get_device_status(None) == cuda_lib.Status.OK
+
+
+def test_masked_stage_orders(cuda_lib):
+    # Stages 8 then 2 (dQ forming the row vectors and packing the mask, then
+    # dK / dV) are attn_bwd_masked bit for bit; 1, 2, 4 (prep and packing,
+    # dK / dV, dQ) differ only in D's rounding.  Other stage words are
+    # refused.
+    import torch
+    from tests.parity import check_same_but_rounding
+    B, H, Hkv, N, d = 2, 4, 2, 384, 128
+    q, k, v, do = (dev(x) for x in _problem(B, H, Hkv, N, N, d, 48000))
+    mask = _mask("documents", B, H, N, N, 48001)
+    tm = _t(mask.astype(np.uint8), torch.uint8)
+    O, lse = cuda_lib.forward_masked(q, k, v, 0.1, True, (200, -1), None, tm)
+    want = [host(g) for g in cuda_lib.backward_masked(q, k, v, O, lse, do, 0.1, True, (200, -1), None, tm)]
+    m = cuda_lib.make_mask((200, -1), None, tm, B, H)
+    wsb = cuda_lib.attn_masked_workspace_size(B, H, Hkv, N, N, d, m, 1)
+    ws = torch.empty(wsb, dtype=torch.uint8, device="cuda")
+    sp = torch.cuda.current_stream().cuda_stream
+    P = lambda t: t.data_ptr()
+    for order in ((8, 2), (1, 2, 4)):
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        for st in order:
+            assert cuda_lib.attn_bwd_masked_stages(P(q), P(k), P(v), P(O), P(lse), P(do), P(dq), P(dk), P(dv),
+                                                   B, H, Hkv, N, N, d, 0.1, 1, m, P(ws), wsb, st, sp) == 0
+        got = [host(g) for g in (dq, dk, dv)]
+        if order == (8, 2):
+            for g, w in zip(got, want):
+                assert np.array_equal(g, w)
+        else:
+            check_same_but_rounding(got, want, "masked stages 1, 2, 4")
+    for bad in (0, 16):
+        assert cuda_lib.attn_bwd_masked_stages(P(q), P(k), P(v), P(O), P(lse), P(do), P(dq), P(dk), P(dv),
+                                               B, H, Hkv, N, N, d, 0.1, 1, m, P(ws), wsb, bad,
+                                               sp) == cuda_lib.Status.INVALID_ARG
+    assert cuda_lib.attn_get_device_status(None) == cuda_lib.Status.OK
