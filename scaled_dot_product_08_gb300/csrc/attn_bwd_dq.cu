@@ -243,12 +243,15 @@ __global__ void __launch_bounds__(384, 1)
       // through tensor-memory columns 384 + X of lane r (dQ columns, which no
       // MMA writes before every thread has passed dS_0).  Every compute
       // thread reaches the barriers below, whatever the waits return.
+      const int row = 128 * i + r;
+      // the row's lse first: its load overlaps the waits below
+      const float l = row < seq_s[1] ? (varlen ? p.lse[(size_t)h * p.vl.total_q + seq_s[0] + row]
+                                               : p.lse[(size_t)bh * p.N + row])
+                                     : -INFINITY;
       rows_ok = __all_sync(0xffffffffu, wait_bounded(wc, bQ, 0, wait_site(0x84, 0)) &&
                                             wait_bounded(wc, bO, 0, wait_site(0x85, 0)));
-      const int row = 128 * i + r;
-      float part = 0.f, l = -INFINITY;
+      float part = 0.f;
       if (rows_ok && row < seq_s[1]) {
-        l = varlen ? p.lse[(size_t)h * p.vl.total_q + seq_s[0] + row] : p.lse[(size_t)bh * p.N + row];
         const uint32_t sO = sK + 2 * T::TILE_BYTES;
 #pragma unroll
         for (int cc = X * (D / 16); cc < (X + 1) * (D / 16); ++cc) {
@@ -438,8 +441,15 @@ __global__ void __launch_bounds__(384, 1)
           tma_load_3d(sQ + cb * T::BLOCK_BYTES, &tmQ, bQ, cb * 64, q0 + i * 128, qplane);
           tma_load_3d(sdO + cb * T::BLOCK_BYTES, &tmdO, bQ, cb * 64, q0 + i * 128, qplane);
         }
+        // O_i for the row vectors, right after Q_i and dO_i: the compute
+        // threads form them while K_0 and V_0 arrive and S_0 is computed.
+        const bool o_issued = p.rows_in_dq != 0;
+        if (o_issued) {
+          mbar_expect_tx(bO, T::TILE_BYTES);
+          for (int cb = 0; cb < T::NB; ++cb)
+            tma_load_3d(sK + 2 * T::TILE_BYTES + cb * T::BLOCK_BYTES, &tmO, bO, cb * 64, q0 + i * 128, qplane);
+        }
         int issued = 0;
-        bool o_issued = false;
         for (int j = 0; j < n; ++j) {
           const int ks = j % T::KS, kr = j / T::KS, vs = j % T::VS, vr = j / T::VS;
           if (kr > 0 && !wait_bounded(wc, bKe + 8u * ks, (kr - 1) & 1, wait_site(0x91, j))) break;
@@ -455,13 +465,6 @@ __global__ void __launch_bounds__(384, 1)
             tma_load_3d(sV + vs * T::TILE_BYTES + cb * T::BLOCK_BYTES, &tmV, bVf + 8u * vs, cb * 64,
                         k0 + tile_at(j) * 128, kplane);
           issued = 2 * j + 2;
-          if (j == 0 && p.rows_in_dq) {
-            // O_i for the row vectors, after the tiles of the first step
-            mbar_expect_tx(bO, T::TILE_BYTES);
-            for (int cb = 0; cb < T::NB; ++cb)
-              tma_load_3d(sK + 2 * T::TILE_BYTES + cb * T::BLOCK_BYTES, &tmO, bO, cb * 64, q0 + i * 128, qplane);
-            o_issued = true;
-          }
         }
         // Every copy issued above has landed before the CTA may exit.
         wait_drain(bQ, 0, p.limit_ns);
