@@ -24,7 +24,9 @@ Extra keys on the JSON line:
   cpu_baseline  the fp64 CPU oracle timed on this host on a bounded sample
   e2e           the same metric through the C ABI with pinned HOST buffers:
                 host->device copies of Q, K, V, dO and device->host copies of
-                O, lse, dQ, dK, dV inside the timed region
+                O, lse, dQ, dK, dV inside the timed region, every step,
+                pipelined with the compute (two buffer slots, two copy
+                streams)
   clocks        nvidia-smi samples taken during the timed region
 ``--impl reference`` times the CPU oracle (the only other implementation of
 this path) on the same workload, one bounded sample per step.
@@ -333,6 +335,78 @@ def run_reference(args, w, rank, world):
 
 
 # ------------------------------------------------------------ GPU arm
+def run_e2e(torch, sdpa, w, bufs, make_launches, stream, barrier, max_over_ranks, world, flops, Ke):
+    """The step end to end from pinned host memory: every step copies its
+    inputs host -> device and its outputs (O, lse and, with a backward, dQ,
+    dK, dV) device -> host inside the timed region.  The copies are
+    pipelined as a data loader would: two slots of device buffers, step i+1's
+    inputs going in on one stream and step i-1's outputs coming out on
+    another while step i computes on the launching stream."""
+    in_keys = ["q", "k", "v"] + (["do"] if w.with_grad else [])
+    in_keys += [n for n in ("cu", "mask_t") if bufs[n] is not None]
+    out_keys = ["o", "lse"] + (["dq", "dk", "dv"] if w.with_grad else [])
+    second = {n: (torch.empty_like(t) if t is not None and n not in ("mask_spec",) else t) for n, t in bufs.items()}
+    if bufs["mask_t"] is not None:
+        second["mask_spec"] = sdpa.make_mask(w.window, None, second["mask_t"], w.B, w.H)
+    slots = [bufs, second]
+    launches = [make_launches(b) for b in slots]
+    host_in = {n: bufs[n].cpu().pin_memory() for n in in_keys}
+    host_out = [{n: torch.empty(b[n].shape, dtype=b[n].dtype).pin_memory() for n in out_keys} for b in slots]
+    h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+    d2h = sum(t.numel() * t.element_size() for t in host_out[0].values())
+    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+    ev_in = [torch.cuda.Event() for _ in slots]     # slot's inputs are on the device
+    ev_done = [torch.cuda.Event() for _ in slots]   # slot's step has computed
+    ev_out = [torch.cuda.Event() for _ in slots]    # slot's outputs are on the host
+
+    def copy_in(i):
+        sl = slots[i % 2]
+        with torch.cuda.stream(s_in):
+            if i >= 2:
+                s_in.wait_event(ev_done[i % 2])  # step i - 2 has finished reading the slot
+            for n in in_keys:
+                sl[n].copy_(host_in[n], non_blocking=True)
+            ev_in[i % 2].record(s_in)
+
+    def run(nsteps, start=None, end=None):
+        if start is not None:
+            start.record(stream)
+            s_in.wait_event(start)
+        copy_in(0)
+        for i in range(nsteps):
+            if i + 1 < nsteps:
+                copy_in(i + 1)
+            stream.wait_event(ev_in[i % 2])
+            if i >= 2:
+                stream.wait_event(ev_out[i % 2])  # step i - 2's outputs have left the slot
+            for launch in launches[i % 2]:
+                launch()
+            ev_done[i % 2].record(stream)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(ev_done[i % 2])
+                for n in out_keys:
+                    host_out[i % 2][n].copy_(slots[i % 2][n], non_blocking=True)
+                ev_out[i % 2].record(s_out)
+        stream.wait_event(ev_out[(nsteps - 1) % 2])
+        stream.wait_event(ev_out[nsteps % 2])
+        if end is not None:
+            end.record(stream)
+
+    run(2)
+    barrier()
+    a, bev = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    run(Ke, a, bev)
+    barrier()
+    ems = max_over_ranks(a.elapsed_time(bev))
+    st = sdpa.attn_get_device_status(None)
+    if st != 0:
+        raise RuntimeError(f"device status after the end-to-end steps: {sdpa.attn_status_string(st)}")
+    return {"value": world * flops * Ke / (ems / 1e3) / 1e12, "unit": UNIT, "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "ms_per_step": ems / Ke, "steps": Ke,
+            "note": "inputs in and outputs (O, lse, and dQ, dK, dV with a backward) out every step, pipelined "
+                    "with the compute over two buffer slots and two copy streams"}
+
+
 def run_ours(args, w, rank, world, local_rank):
     import torch
     import scaled_dot_product_08_gb300 as sdpa
@@ -348,12 +422,10 @@ def run_ours(args, w, rank, world, local_rank):
     B, H, Hkv, N, d = w.B, w.H, w.Hkv, w.N, w.d
     s = w.softmax_scale
     Nq = w.n_queries
-    extra_in = []  # further device inputs of a step (cu_seqlens)
     if w.kind == "varlen":
         from sdpa_inputs import make_varlen_inputs
         x = make_varlen_inputs(w)
         cu = torch.from_numpy(x["cu"]).cuda()
-        extra_in = [cu]
         nseq, maxlen = len(x["lengths"]), int(x["lengths"].max())
         lse_shape = (H, N)
     else:
@@ -369,7 +441,6 @@ def run_ours(args, w, rank, world, local_rank):
         mask_t = None
         if w.prefix is not None:
             mask_t = torch.from_numpy(prefix_lm_mask(N, w.prefix).astype("uint8")).cuda()
-            extra_in = [mask_t]
         mask_spec = sdpa.make_mask(w.window, None, mask_t, B, H)
         mws_f = sdpa.attn_masked_workspace_size(B, H, Hkv, Nq, N, d, mask_spec, 0)
         mws_b = sdpa.attn_masked_workspace_size(B, H, Hkv, Nq, N, d, mask_spec, 1)
@@ -400,47 +471,61 @@ def run_ours(args, w, rank, world, local_rank):
             raise RuntimeError(f"{where}: {sdpa.attn_status_string(st)}")
 
     P = lambda t: t.data_ptr()
-    # One callable per kernel of the step, in order (names above).
-    if w.kind == "varlen":
-        def vstage(mask):
-            return lambda: chk(sdpa.attn_bwd_varlen_stages(
-                P(q), P(k), P(v), P(o), P(lse), P(do), P(dq), P(dk), P(dv), P(cu), P(cu), P(ws), ws_bytes,
-                nseq, H, Hkv, N, N, maxlen, maxlen, d, s, w.causal, mask, sp), "attn_bwd_varlen_stages")
-        launches = [lambda: chk(sdpa.attn_fwd_varlen(P(q), P(k), P(v), P(o), P(lse), P(cu), P(cu), nseq, H, Hkv,
-                                                     N, N, maxlen, maxlen, d, s, w.causal, sp), "attn_fwd_varlen")]
-        if w.with_grad:
-            launches += [vstage(8), vstage(2)]
-    elif w.kind == "fp8":
-        (_, qsc), (_, ksc), (_, vsc) = fp8
-        launches = [lambda: chk(sdpa.attn_fwd_fp8(P(q), P(k), P(v), P(o), P(lse), B, H, Hkv, Nq, N, d, s, qsc, ksc,
-                                                  vsc, w.causal, sp), "attn_fwd_fp8")]
-    elif w.kind == "masked":
-        def mstage(mask):
-            return lambda: chk(sdpa.attn_bwd_masked_stages(
-                P(q), P(k), P(v), P(o), P(lse), P(do), P(dq), P(dk), P(dv), B, H, Hkv, Nq, N, d, s, w.causal,
-                mask_spec, P(mws), mws.numel(), mask, sp), "attn_bwd_masked_stages")
-        launches = [lambda: chk(sdpa.attn_fwd_masked(P(q), P(k), P(v), P(o), P(lse), B, H, Hkv, Nq, N, d, s, w.causal,
-                                                     mask_spec, P(mws), mws.numel(), sp), "attn_fwd_masked")]
-        if w.with_grad:
-            launches += [mstage(8), mstage(2)]
-    elif w.kind == "cross":
-        launches = [lambda: chk(sdpa.attn_fwd_cross(P(q), P(k), P(v), P(o), P(lse), B, H, Hkv, Nq, N, d, s,
-                                                    w.causal, sp), "attn_fwd_cross")]
-        if w.with_grad:
-            launches += [
-                lambda: chk(sdpa.attn_bwd_dq_rows(P(q), P(k), P(v), P(o), P(lse), P(do), P(dq), P(ws), ws_bytes,
-                                                  B, H, Hkv, Nq, N, d, s, w.causal, sp), "attn_bwd_dq_rows"),
-                lambda: chk(sdpa.attn_bwd_grad_cross(P(q), P(k), P(v), P(do), P(dk), P(dv), P(ws), ws_bytes,
-                                                     B, H, Hkv, Nq, N, d, s, w.causal, sp), "attn_bwd_grad_cross")]
-    else:
-        launches = [lambda: chk(sdpa.attn_fwd(P(q), P(k), P(v), P(o), P(lse), B, H, Hkv, N, d, s, w.causal, sp),
-                                "attn_fwd")]
-        if w.with_grad:
-            launches += [
-                lambda: chk(sdpa.attn_bwd_dq_rows(P(q), P(k), P(v), P(o), P(lse), P(do), P(dq), P(ws), ws_bytes,
-                                                  B, H, Hkv, N, N, d, s, w.causal, sp), "attn_bwd_dq_rows"),
-                lambda: chk(sdpa.attn_bwd_grad(P(q), P(k), P(v), P(do), P(dk), P(dv), P(ws), ws_bytes,
-                                               B, H, Hkv, N, d, s, w.causal, sp), "attn_bwd_grad")]
+
+    def make_launches(bf):
+        """One callable per kernel of the step, in order (names above), on the
+        device buffers of `bf` (inputs, outputs, mask)."""
+        ptr = lambda n: bf[n].data_ptr() if bf[n] is not None else 0
+        pq, pk, pv, po, pl = (ptr(n) for n in ("q", "k", "v", "o", "lse"))
+        pdo, pdq, pdk, pdv, pcu = (ptr(n) for n in ("do", "dq", "dk", "dv", "cu"))
+        mspec = bf["mask_spec"]
+        if w.kind == "varlen":
+            def vstage(mask):
+                return lambda: chk(sdpa.attn_bwd_varlen_stages(
+                    pq, pk, pv, po, pl, pdo, pdq, pdk, pdv, pcu, pcu, P(ws), ws_bytes,
+                    nseq, H, Hkv, N, N, maxlen, maxlen, d, s, w.causal, mask, sp), "attn_bwd_varlen_stages")
+            launches = [lambda: chk(sdpa.attn_fwd_varlen(pq, pk, pv, po, pl, pcu, pcu, nseq, H, Hkv,
+                                                         N, N, maxlen, maxlen, d, s, w.causal, sp), "attn_fwd_varlen")]
+            if w.with_grad:
+                launches += [vstage(8), vstage(2)]
+        elif w.kind == "fp8":
+            (_, qsc), (_, ksc), (_, vsc) = fp8
+            launches = [lambda: chk(sdpa.attn_fwd_fp8(pq, pk, pv, po, pl, B, H, Hkv, Nq, N, d, s, qsc, ksc,
+                                                      vsc, w.causal, sp), "attn_fwd_fp8")]
+        elif w.kind == "masked":
+            def mstage(mask):
+                return lambda: chk(sdpa.attn_bwd_masked_stages(
+                    pq, pk, pv, po, pl, pdo, pdq, pdk, pdv, B, H, Hkv, Nq, N, d, s, w.causal,
+                    mspec, P(mws), mws.numel(), mask, sp), "attn_bwd_masked_stages")
+            launches = [lambda: chk(sdpa.attn_fwd_masked(pq, pk, pv, po, pl, B, H, Hkv, Nq, N, d, s, w.causal,
+                                                         mspec, P(mws), mws.numel(), sp), "attn_fwd_masked")]
+            if w.with_grad:
+                launches += [mstage(8), mstage(2)]
+        elif w.kind == "cross":
+            launches = [lambda: chk(sdpa.attn_fwd_cross(pq, pk, pv, po, pl, B, H, Hkv, Nq, N, d, s,
+                                                        w.causal, sp), "attn_fwd_cross")]
+            if w.with_grad:
+                launches += [
+                    lambda: chk(sdpa.attn_bwd_dq_rows(pq, pk, pv, po, pl, pdo, pdq, P(ws), ws_bytes,
+                                                      B, H, Hkv, Nq, N, d, s, w.causal, sp), "attn_bwd_dq_rows"),
+                    lambda: chk(sdpa.attn_bwd_grad_cross(pq, pk, pv, pdo, pdk, pdv, P(ws), ws_bytes,
+                                                         B, H, Hkv, Nq, N, d, s, w.causal, sp), "attn_bwd_grad_cross")]
+        else:
+            launches = [lambda: chk(sdpa.attn_fwd(pq, pk, pv, po, pl, B, H, Hkv, N, d, s, w.causal, sp),
+                                    "attn_fwd")]
+            if w.with_grad:
+                launches += [
+                    lambda: chk(sdpa.attn_bwd_dq_rows(pq, pk, pv, po, pl, pdo, pdq, P(ws), ws_bytes,
+                                                      B, H, Hkv, N, N, d, s, w.causal, sp), "attn_bwd_dq_rows"),
+                    lambda: chk(sdpa.attn_bwd_grad(pq, pk, pv, pdo, pdk, pdv, P(ws), ws_bytes,
+                                                   B, H, Hkv, N, d, s, w.causal, sp), "attn_bwd_grad")]
+        return launches
+
+    bufs = {"q": q, "k": k, "v": v, "o": o, "lse": lse, "do": do, "dq": dq if w.with_grad else None,
+            "dk": dk if w.with_grad else None, "dv": dv if w.with_grad else None,
+            "cu": cu if w.kind == "varlen" else None, "mask_t": mask_t if w.kind == "masked" else None,
+            "mask_spec": mask_spec}
+    launches = make_launches(bufs)
 
     # Kernels per step: one per call, plus the mask packing inside the masked
     # forward and first backward calls when there is a boolean mask.
@@ -528,35 +613,8 @@ def run_ours(args, w, rank, world, local_rank):
     # ---- end to end through the C ABI with pinned host buffers
     e2e = None
     if not args.no_e2e:
-        hq, hk, hv = (t.cpu().pin_memory() for t in (q, k, v))
-        ins = [(q, hq), (k, hk), (v, hv)] + ([(do, do.cpu().pin_memory())] if w.with_grad else [])
-        ins += [(t, t.cpu().pin_memory()) for t in extra_in]
-        outs = [o, lse] + ([dq, dk, dv] if w.with_grad else [])
-        houts = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in outs]
-        h2d = sum(h.numel() * h.element_size() for _, h in ins)
-        d2h = sum(h.numel() * h.element_size() for h in houts)
-        Ke = max(3, min(K, 30))
-
-        def e2e_step():
-            for dst, src in ins:
-                dst.copy_(src, non_blocking=True)
-            step()
-            for src, dst in zip(outs, houts):
-                dst.copy_(src, non_blocking=True)
-
-        for _ in range(2):
-            e2e_step()
-        barrier()
-        a, bev = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        for _ in range(Ke):
-            e2e_step()
-        bev.record(stream)
-        barrier()
-        ems = a.elapsed_time(bev)
-        ems = max_over_ranks(ems)
-        e2e = {"value": world * flops * Ke / (ems / 1e3) / 1e12, "unit": UNIT, "h2d_bytes_per_step": h2d,
-               "d2h_bytes_per_step": d2h, "ms_per_step": ems / Ke, "steps": Ke}
+        e2e = run_e2e(torch, sdpa, w, bufs, make_launches, stream, barrier, max_over_ranks, world, flops,
+                      max(3, min(K, 30)))
 
     cb = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
