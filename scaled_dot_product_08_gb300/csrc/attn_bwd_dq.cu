@@ -419,7 +419,7 @@ __global__ void __launch_bounds__(384, 1)
           for (int cb = 0; cb < T::NB; ++cb)
             tma_store_3d(&tmdQ, sQ + cb * T::BLOCK_BYTES, cb * 64, q0 + i * 128, qplane);
           bulk_commit();
-          bulk_wait_all();
+          bulk_wait_read_all();  // the tile has been read out of shared memory
         }
       } else {
         const uint32_t rs = (uint32_t)(p.H * D);

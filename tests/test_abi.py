@@ -176,6 +176,25 @@ def test_bwd_cross_stages_reject_bad_arguments(lib):
         assert f(385, 400, 0) == S.WORKSPACE      # workspace sized for 300 (padded: 384) query rows
 
 
+def test_bwd_dq_rows_rejects_bad_arguments(lib):
+    # attn_bwd_dq_rows also reads o and lse: both are checked like the rest.
+    import scaled_dot_product_08_gb300 as sdpa
+    S = sdpa.Status
+    ws = sdpa.attn_bwd_workspace_size(1, 2, 2, 300, 128)
+
+    def f(Nq=300, Nk=400, causal=0, wsb=ws, o=FAKE, lse=FAKE, scale=0.1, d=128):
+        return sdpa.attn_bwd_dq_rows(FAKE, FAKE, FAKE, o, lse, FAKE, FAKE, FAKE, wsb, 1, 2, 2, Nq, Nk, d, scale,
+                                     causal, None)
+    assert f(Nq=300, Nk=200, causal=1) == S.UNSUPPORTED_SHAPE   # a causal row would see no key
+    assert f(d=80) == S.UNSUPPORTED_SHAPE
+    assert f(scale=float("inf")) == S.INVALID_ARG
+    assert f(causal=2) == S.INVALID_ARG
+    assert f(wsb=ws - 1) == S.WORKSPACE
+    assert f(o=0) == S.INVALID_ARG
+    assert f(lse=0) == S.INVALID_ARG
+    assert f(o=FAKE + 2) == S.MISALIGNED
+
+
 def test_varlen_rejects_bad_arguments(lib):
     import scaled_dot_product_08_gb300 as sdpa
     S = sdpa.Status
