@@ -98,13 +98,34 @@ def _mask_plane(mask, b, h):
     return m[b if m.shape[0] > 1 else 0, h if m.shape[1] > 1 else 0]
 
 
-def attention_masked_forward(q, k, v, scale=None, causal=False, window=None, key_lengths=None, mask=None):
+def _masked_scores(q, k, scale, vis, bias):
+    """scale * q k^T, plus the additive mask when there is one, with the
+    invisible entries at -inf."""
+    S = scale * (q @ k.T)
+    if bias is not None:
+        S = S + bias
+    return np.where(vis, S, -np.inf)
+
+
+def _bias_plane(bias, b, h):
+    """The (Nq, Nk) float64 plane of a (Bb, Hb, Nq, Nk) additive mask that
+    batch b, head h adds (Bb, Hb of 1 broadcast)."""
+    if bias is None:
+        return None
+    a = np.asarray(bias, dtype=np.float64)
+    return a[b if a.shape[0] > 1 else 0, h if a.shape[1] > 1 else 0]
+
+
+def attention_masked_forward(q, k, v, scale=None, causal=False, window=None, key_lengths=None, mask=None,
+                             bias=None):
     """Attention under any combination of the masks of ``visibility``, with
     query row i at position Nk - Nq + i (the alignment of
     ``attention_decode``; i itself when Nq = Nk).  key_lengths: (B,) ints or
     None; mask: boolean (Bm, Hm, Nq, Nk), Bm in {1, B}, Hm in {1, H}, or
-    None.  Rows that see no key: O = 0, lse = -inf.
-    Returns O (B, H, Nq, d_v) and lse (B, H, Nq)."""
+    None; bias: an additive float mask of the same broadcasting shape, added
+    to the scaled scores before the softmax (SDPA's float attn_mask; finite
+    or -inf entries, -inf hiding the key), or None.  Rows that see no key:
+    O = 0, lse = -inf.  Returns O (B, H, Nq, d_v) and lse (B, H, Nq)."""
     q = np.asarray(q, dtype=np.float64)
     k = np.asarray(k, dtype=np.float64)
     v = np.asarray(v, dtype=np.float64)
@@ -118,8 +139,8 @@ def attention_masked_forward(q, k, v, scale=None, causal=False, window=None, key
             hk = gqa_kv_head(h, H, Hkv)
             vis = visibility(Nq, Nk, causal, Nk - Nq, window,
                              None if key_lengths is None else int(key_lengths[b]), _mask_plane(mask, b, h))
-            S = np.where(vis, scale * (q[b, h] @ k[b, hk].T), -np.inf)
-            live = vis.any(axis=1)
+            S = _masked_scores(q[b, h], k[b, hk], scale, vis, _bias_plane(bias, b, h))
+            live = np.isfinite(S).any(axis=1)
             if live.any():
                 P, m, l = softmax_rows(S[live])
                 O[b, h][live] = P @ v[b, hk]
@@ -127,10 +148,12 @@ def attention_masked_forward(q, k, v, scale=None, causal=False, window=None, key
     return O, lse
 
 
-def attention_masked_backward(q, k, v, do, scale=None, causal=False, window=None, key_lengths=None, mask=None):
+def attention_masked_backward(q, k, v, do, scale=None, causal=False, window=None, key_lengths=None, mask=None,
+                              bias=None):
     """Gradients of ``attention_masked_forward`` by the chain rule of
     ``attention_backward`` (masked entries have P = 0; rows that see no key
-    contribute nothing).  Returns dQ, dK, dV in float64."""
+    contribute nothing; the additive mask enters through P only and gets no
+    gradient).  Returns dQ, dK, dV in float64."""
     q = np.asarray(q, dtype=np.float64)
     k = np.asarray(k, dtype=np.float64)
     v = np.asarray(v, dtype=np.float64)
@@ -144,8 +167,8 @@ def attention_masked_backward(q, k, v, do, scale=None, causal=False, window=None
             hk = gqa_kv_head(h, H, Hkv)
             vis = visibility(Nq, Nk, causal, Nk - Nq, window,
                              None if key_lengths is None else int(key_lengths[b]), _mask_plane(mask, b, h))
-            S = np.where(vis, scale * (q[b, h] @ k[b, hk].T), -np.inf)
-            live = vis.any(axis=1)
+            S = _masked_scores(q[b, h], k[b, hk], scale, vis, _bias_plane(bias, b, h))
+            live = np.isfinite(S).any(axis=1)
             P = np.zeros_like(S)
             if live.any():
                 P[live] = softmax_rows(S[live])[0]
