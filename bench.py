@@ -66,7 +66,8 @@ def parse_args():
 def workload_desc(w):
     if w.kind == "masked":
         what = (f"sliding window (left {w.window[0]}, right {w.window[1]})" if w.window is not None
-                else f"prefix-LM boolean mask (prefix {w.prefix})")
+                else f"prefix-LM boolean mask (prefix {w.prefix})" if w.prefix is not None
+                else f"additive float32 mask -{w.bias_slope:g}*|i-j| shared by all heads")
         return (f"{w.name}: B={w.B} H={w.H} Hkv={w.Hkv} N={w.N} d={w.d} {'causal ' if w.causal else ''}{what} "
                 f"{'fwd+bwd' if w.with_grad else 'fwd'}; FLOPs count the visible (query, key) pairs")
     if w.kind == "varlen":
@@ -218,12 +219,13 @@ def _oracle_head_seconds(w, x):
     import oracle
     q, k, v, do = x
     if w.kind == "masked":
-        from sdpa_inputs import prefix_lm_mask
+        from sdpa_inputs import distance_bias, prefix_lm_mask
         mask = prefix_lm_mask(w.N, w.prefix) if w.prefix is not None else None
+        bias = distance_bias(w.N, w.bias_slope) if w.bias_slope is not None else None
         t0 = time.perf_counter()
-        oracle.attention_masked_forward(q, k, v, w.softmax_scale, w.causal, w.window, None, mask)
+        oracle.attention_masked_forward(q, k, v, w.softmax_scale, w.causal, w.window, None, mask, bias)
         if w.with_grad:
-            oracle.attention_masked_backward(q, k, v, do, w.softmax_scale, w.causal, w.window, None, mask)
+            oracle.attention_masked_backward(q, k, v, do, w.softmax_scale, w.causal, w.window, None, mask, bias)
         return time.perf_counter() - t0
     t0 = time.perf_counter()
     off = (w.N - w.n_queries) if (w.kind == "cross" and w.causal) else 0
@@ -343,11 +345,11 @@ def run_e2e(torch, sdpa, w, bufs, make_launches, stream, barrier, max_over_ranks
     inputs going in on one stream and step i-1's outputs coming out on
     another while step i computes on the launching stream."""
     in_keys = ["q", "k", "v"] + (["do"] if w.with_grad else [])
-    in_keys += [n for n in ("cu", "mask_t") if bufs[n] is not None]
+    in_keys += [n for n in ("cu", "mask_t", "bias_t") if bufs[n] is not None]
     out_keys = ["o", "lse"] + (["dq", "dk", "dv"] if w.with_grad else [])
     second = {n: (torch.empty_like(t) if t is not None and n not in ("mask_spec",) else t) for n, t in bufs.items()}
-    if bufs["mask_t"] is not None:
-        second["mask_spec"] = sdpa.make_mask(w.window, None, second["mask_t"], w.B, w.H)
+    if bufs["mask_spec"] is not None:
+        second["mask_spec"] = sdpa.make_mask(w.window, None, second["mask_t"], w.B, w.H, second["bias_t"])
     slots = [bufs, second]
     launches = [make_launches(b) for b in slots]
     host_in = {n: bufs[n].cpu().pin_memory() for n in in_keys}
@@ -437,11 +439,13 @@ def run_ours(args, w, rank, world, local_rank):
         fp8 = [quantize_e4m3(x[n]) for n in ("q", "k", "v")]  # (bytes, scale) each
     mask_spec = None
     if w.kind == "masked":
-        from sdpa_inputs import prefix_lm_mask
-        mask_t = None
+        from sdpa_inputs import distance_bias, prefix_lm_mask
+        mask_t = bias_t = None
         if w.prefix is not None:
             mask_t = torch.from_numpy(prefix_lm_mask(N, w.prefix).astype("uint8")).cuda()
-        mask_spec = sdpa.make_mask(w.window, None, mask_t, B, H)
+        if w.bias_slope is not None:
+            bias_t = torch.from_numpy(distance_bias(N, w.bias_slope)).cuda()
+        mask_spec = sdpa.make_mask(w.window, None, mask_t, B, H, bias_t)
         mws_f = sdpa.attn_masked_workspace_size(B, H, Hkv, Nq, N, d, mask_spec, 0)
         mws_b = sdpa.attn_masked_workspace_size(B, H, Hkv, Nq, N, d, mask_spec, 1)
         mws = torch.empty(max(mws_f, mws_b, 16), dtype=torch.uint8, device="cuda")
@@ -524,14 +528,17 @@ def run_ours(args, w, rank, world, local_rank):
     bufs = {"q": q, "k": k, "v": v, "o": o, "lse": lse, "do": do, "dq": dq if w.with_grad else None,
             "dk": dk if w.with_grad else None, "dv": dv if w.with_grad else None,
             "cu": cu if w.kind == "varlen" else None, "mask_t": mask_t if w.kind == "masked" else None,
-            "mask_spec": mask_spec}
+            "bias_t": bias_t if w.kind == "masked" else None, "mask_spec": mask_spec}
     launches = make_launches(bufs)
 
     # Kernels per step: one per call, plus the mask packing inside the masked
-    # forward and first backward calls when there is a boolean mask.
-    kernels_per_step = len(launches) + (2 if w.kind == "masked" and w.prefix is not None else 0)
-    if w.kind == "masked" and w.prefix is not None and not w.with_grad:
-        kernels_per_step -= 1
+    # forward and first backward calls when there is a boolean mask, and the
+    # additive mask's transpose inside the first backward call.
+    kernels_per_step = len(launches)
+    if w.kind == "masked" and w.prefix is not None:
+        kernels_per_step += 2 if w.with_grad else 1
+    if w.kind == "masked" and w.bias_slope is not None and w.with_grad:
+        kernels_per_step += 1
 
     def step(evs=None):
         for idx, launch in enumerate(launches):

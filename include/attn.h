@@ -255,11 +255,20 @@ attn_status_t attn_fwd_fp8(const void* q, const void* k, const void* v, void* o,
  *   mask != NULL                 mask[b'][h'][i][j] != 0, with b' = b (or 0
  *                                when mask_batch == 1), h' = h (or 0 when
  *                                mask_heads == 1)
- * -1 leaves a window side open.  A row no key passes gets O = 0, lse = -inf
- * and dQ = 0; keys no row sees get dK = dV = 0.
+ * -1 leaves a window side open.  An additive mask (SDPA's float attn_mask)
+ * adds bias[b''][h''][i][j] (broadcast over bias_batch, bias_heads as for
+ * mask) to the scaled score of every (i, j) the conditions above keep:
+ * softmax over j of scale * q_i . k_j + bias[i][j].  Its entries are finite
+ * or -inf (-inf hides the key); +inf and NaN are not allowed.  The bias gets
+ * no gradient.  A row no key passes (or whose bias is -inf at every key it
+ * may see) gets O = 0, lse = -inf and dQ = 0; keys no row sees get
+ * dK = dV = 0.
  *   key_lengths  DEVICE int32 (B), 4-byte aligned, or NULL
  *   mask         DEVICE bytes (mask_batch, mask_heads, Nq, Nk), dense
  *                row-major, any alignment, or NULL
+ *   bias         DEVICE float32 (bias_batch, bias_heads, Nq, Nk), dense
+ *                row-major, 4-byte aligned, or NULL (bias_batch and
+ *                bias_heads are then ignored)
  */
 typedef struct {
   int window_left;
@@ -268,6 +277,9 @@ typedef struct {
   const unsigned char* mask;
   int mask_batch;   /* 1 or B */
   int mask_heads;   /* 1 or H */
+  const float* bias;
+  int bias_batch;   /* 1 or B */
+  int bias_heads;   /* 1 or H */
 } attn_mask_t;
 
 /*

@@ -49,7 +49,8 @@ class AttnMask(ctypes.Structure):
     """attn_mask_t of include/attn.h (device pointers as integers, 0 = none)."""
     _fields_ = [("window_left", ctypes.c_int), ("window_right", ctypes.c_int),
                 ("key_lengths", ctypes.c_void_p), ("mask", ctypes.c_void_p),
-                ("mask_batch", ctypes.c_int), ("mask_heads", ctypes.c_int)]
+                ("mask_batch", ctypes.c_int), ("mask_heads", ctypes.c_int),
+                ("bias", ctypes.c_void_p), ("bias_batch", ctypes.c_int), ("bias_heads", ctypes.c_int)]
 
 
 class AttnError(RuntimeError):
@@ -511,14 +512,15 @@ def backward_varlen(q, k, v, o, lse, dout, cu_seqlens_q, cu_seqlens_k, max_seqle
     return dq, dk, dv
 
 
-def make_mask(window=None, key_lengths=None, mask=None, B=1, H=1) -> AttnMask:
+def make_mask(window=None, key_lengths=None, mask=None, B=1, H=1, bias=None) -> AttnMask:
     """AttnMask from Python values: window (left, right) with -1 for an open
     side, key_lengths an int32 CUDA vector (B,), mask a bool / uint8 CUDA
-    tensor (1 or B, 1 or H, Nq, Nk).  The tensors must stay alive while the
-    calls that use the AttnMask run."""
+    tensor (1 or B, 1 or H, Nq, Nk), bias a float32 CUDA tensor of the same
+    broadcasting shape added to the scaled scores (finite or -inf).  The
+    tensors must stay alive while the calls that use the AttnMask run."""
     import torch
     wl, wr = window if window is not None else (-1, -1)
-    m = AttnMask(int(wl), int(wr), 0, 0, 1, 1)
+    m = AttnMask(int(wl), int(wr), 0, 0, 1, 1, 0, 1, 1)
     if key_lengths is not None:
         if key_lengths.dtype != torch.int32 or not key_lengths.is_cuda or not key_lengths.is_contiguous():
             raise ValueError("key_lengths must be a contiguous int32 CUDA vector")
@@ -530,6 +532,11 @@ def make_mask(window=None, key_lengths=None, mask=None, B=1, H=1) -> AttnMask:
             raise ValueError("mask must be contiguous")
         m.mask = mask.data_ptr()
         m.mask_batch, m.mask_heads = int(mask.shape[0]), int(mask.shape[1])
+    if bias is not None:
+        if bias.dim() != 4 or bias.dtype != torch.float32 or not bias.is_cuda or not bias.is_contiguous():
+            raise ValueError("bias must be a contiguous 4-D float32 CUDA tensor")
+        m.bias = bias.data_ptr()
+        m.bias_batch, m.bias_heads = int(bias.shape[0]), int(bias.shape[1])
     return m
 
 
@@ -548,14 +555,15 @@ def _masked_shapes(q, k, v):
 
 
 def forward_masked(q, k, v, scale: float | None = None, causal: bool = False, window=None, key_lengths=None,
-                   mask=None):
-    """O, lse under a sliding window / key lengths / boolean mask (see
-    include/attn.h, attn_mask_t); q (B, H, Nq, d), k, v (B, Hkv, Nk, d)."""
+                   mask=None, bias=None):
+    """O, lse under a sliding window / key lengths / boolean mask / additive
+    float32 mask (see include/attn.h, attn_mask_t); q (B, H, Nq, d), k, v
+    (B, Hkv, Nk, d)."""
     import torch
     B, H, Hkv, Nq, Nk, d = _masked_shapes(q, k, v)
     if scale is None:
         scale = 1.0 / math.sqrt(d)
-    m = make_mask(window, key_lengths, mask, B, H)
+    m = make_mask(window, key_lengths, mask, B, H, bias)
     o = torch.empty_like(q)
     lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device)
     wsb = attn_masked_workspace_size(B, H, Hkv, Nq, Nk, d, m, 0)
@@ -566,13 +574,13 @@ def forward_masked(q, k, v, scale: float | None = None, causal: bool = False, wi
 
 
 def backward_masked(q, k, v, o, lse, dout, scale: float | None = None, causal: bool = False, window=None,
-                    key_lengths=None, mask=None):
+                    key_lengths=None, mask=None, bias=None):
     """dQ, dK, dV of forward_masked with the same masks."""
     import torch
     B, H, Hkv, Nq, Nk, d = _masked_shapes(q, k, v)
     if scale is None:
         scale = 1.0 / math.sqrt(d)
-    m = make_mask(window, key_lengths, mask, B, H)
+    m = make_mask(window, key_lengths, mask, B, H, bias)
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     wsb = attn_masked_workspace_size(B, H, Hkv, Nq, Nk, d, m, 1)
     ws = torch.empty(max(wsb, 16), dtype=torch.uint8, device=q.device)

@@ -700,15 +700,21 @@ attn_status_t attn_fwd_fp8(const void* q, const void* k, const void* v, void* o,
 struct MaskGeom {
   int words, words_t, planes;
   size_t bits_bytes, bits_t_bytes, flags_bytes;
+  int bias_planes;
+  size_t bias_t_bytes;  // the additive mask's transpose (backward only)
 };
 
 static MaskGeom mask_geom(int Nq, int Nk, const attn_mask_t* m) {
-  MaskGeom g{((Nk + 127) / 128) * 4, ((Nq + 127) / 128) * 4, 0, 0, 0, 0};
+  MaskGeom g{((Nk + 127) / 128) * 4, ((Nq + 127) / 128) * 4, 0, 0, 0, 0, 0, 0};
   if (m != nullptr && m->mask != nullptr) {
     g.planes = m->mask_batch * m->mask_heads;
     g.bits_bytes = (size_t)g.planes * Nq * g.words * 4;
     g.bits_t_bytes = (size_t)g.planes * Nk * g.words_t * 4;
     g.flags_bytes = ((size_t)g.planes * (g.words_t / 4) * (g.words / 4) + 15) / 16 * 16;
+  }
+  if (m != nullptr && m->bias != nullptr) {
+    g.bias_planes = m->bias_batch * m->bias_heads;
+    g.bias_t_bytes = ((size_t)g.bias_planes * Nq * Nk * 4 + 15) / 16 * 16;
   }
   return g;
 }
@@ -727,11 +733,18 @@ static attn_status_t check_mask(int B, int H, int Nq, int Nk, const attn_mask_t*
     if ((long long)g.planes * Nq * g.words >= 0xffffffffll || (long long)g.planes * Nk * g.words_t >= 0xffffffffll)
       return ATTN_ERR_UNSUPPORTED_SHAPE;
   }
+  if (m->bias != nullptr) {
+    if ((m->bias_batch != 1 && m->bias_batch != B) || (m->bias_heads != 1 && m->bias_heads != H))
+      return ATTN_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(m->bias) & 3u) return ATTN_ERR_MISALIGNED;
+    if (m->bias_batch * m->bias_heads > 65535) return ATTN_ERR_UNSUPPORTED_SHAPE;  // planes on the grid's y
+  }
   return ATTN_OK;
 }
 
 static attn_status_t check_mask_ptrs(const attn_mask_t* m) {
-  for (const void* p : {static_cast<const void*>(m->key_lengths), static_cast<const void*>(m->mask)}) {
+  for (const void* p : {static_cast<const void*>(m->key_lengths), static_cast<const void*>(m->mask),
+                        static_cast<const void*>(m->bias)}) {
     if (p == nullptr) continue;
     cudaPointerAttributes at;
     if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
@@ -744,11 +757,17 @@ static attn_status_t check_mask_ptrs(const attn_mask_t* m) {
 }
 
 // Kernel mask arguments; the bit arrays (when there is a mask) at `bits` and
-// `bits_t` inside the caller's workspace.  Causal enters as wr = 0.
-static sdpa::MaskArgs mask_args(const attn_mask_t* m, int Nq, int Nk, int causal, uint32_t* bits, uint32_t* bits_t,
-                                uint8_t* flags) {
+// `bits_t`, and the additive mask's transpose at `bias_t` (backward), inside
+// the caller's workspace.  Causal enters as wr = 0.
+static sdpa::MaskArgs mask_args(const attn_mask_t* m, int Nq, int Nk, int causal, float scale, uint32_t* bits,
+                                uint32_t* bits_t, uint8_t* flags, float* bias_t) {
   const MaskGeom g = mask_geom(Nq, Nk, m);
   sdpa::MaskArgs a;
+  a.bias = m->bias;
+  a.bias_t = m->bias != nullptr ? bias_t : nullptr;
+  a.bias_b = m->bias != nullptr ? m->bias_batch : 1;
+  a.bias_h = m->bias != nullptr ? m->bias_heads : 1;
+  a.inv_scale = 1.f / scale;
   a.flags = m->mask != nullptr ? flags : nullptr;
   a.ftq = g.words_t / 4;
   a.ftk = g.words / 4;
@@ -771,7 +790,7 @@ size_t attn_masked_workspace_size(int B, int H, int Hkv, int Nq, int Nk, int d, 
     return 0;
   const MaskGeom g = mask_geom(Nq, Nk, mask);
   if (!backward) return g.bits_bytes + g.flags_bytes;
-  return attn_bwd_workspace_size(B, H, Hkv, Nq, d) + g.bits_bytes + g.bits_t_bytes + g.flags_bytes;
+  return attn_bwd_workspace_size(B, H, Hkv, Nq, d) + g.bits_bytes + g.bits_t_bytes + g.flags_bytes + g.bias_t_bytes;
 }
 
 attn_status_t attn_fwd_masked(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
@@ -811,7 +830,7 @@ attn_status_t attn_fwd_masked(const void* q, const void* k, const void* v, void*
   // Workspace: [row bits | tile flags].
   uint32_t* bits = static_cast<uint32_t*>(workspace);
   uint8_t* flags = static_cast<uint8_t*>(workspace) + g.bits_bytes;
-  p.mk = mask_args(mask, Nq, Nk, causal, bits, nullptr, flags);
+  p.mk = mask_args(mask, Nq, Nk, causal, scale, bits, nullptr, flags, nullptr);
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (mask->mask != nullptr &&
       sdpa::launch_mask_pack(static_cast<const uint8_t*>(mask->mask), mask->mask_batch, mask->mask_heads, Nq, Nk,
@@ -841,26 +860,32 @@ attn_status_t attn_bwd_masked_stages(const void* q, const void* k, const void* v
       !make_map_bf16(&tdq, dq, d, Nq, (long long)B * H) || !make_map_bf16(&tdk, dk, d, Nk, (long long)B * Hkv) ||
       !make_map_bf16(&tdv, dv, d, Nk, (long long)B * Hkv) || !make_map_bf16(&to, o, d, Nq, (long long)B * H))
     return ATTN_ERR_CUDA;
-  // Workspace: [row vectors | row bits | transposed bits | tile flags].
+  // Workspace: [row vectors | row bits | transposed bits | tile flags |
+  // additive mask transposed].
   const MaskGeom g = mask_geom(Nq, Nk, mask);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   uint32_t* bits = reinterpret_cast<uint32_t*>(ws + attn_bwd_workspace_size(B, H, Hkv, Nq, d));
   uint32_t* bits_t = reinterpret_cast<uint32_t*>(reinterpret_cast<uint8_t*>(bits) + g.bits_bytes);
   uint8_t* flags = reinterpret_cast<uint8_t*>(bits_t) + g.bits_t_bytes;
+  float* bias_t = reinterpret_cast<float*>(flags + g.flags_bytes);
   sdpa::BwdParams p;
   bwd_params(&p, workspace, B, H, Hkv, Nq, Nk, d, scale, causal, di);
   p.o = static_cast<const uint16_t*>(o);
   p.dout = static_cast<const uint16_t*>(dout);
   p.lse = lse;
-  p.mk = mask_args(mask, Nq, Nk, causal, bits, bits_t, flags);
+  p.mk = mask_args(mask, Nq, Nk, causal, scale, bits, bits_t, flags, bias_t);
   p.dq = static_cast<uint16_t*>(dq);  // outputs whose tiles nothing attends to are zeroed in place
   p.dk = static_cast<uint16_t*>(dk);
   p.dv = static_cast<uint16_t*>(dv);
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
-  // The mask is packed once, by the first of stages 1 and 8 that runs.
+  // The mask is packed (and the additive mask transposed) once, by the
+  // first of stages 1 and 8 that runs.
   if ((stages & (kStagePrep | kStageDqRows)) && mask->mask != nullptr &&
       sdpa::launch_mask_pack(static_cast<const uint8_t*>(mask->mask), mask->mask_batch, mask->mask_heads, Nq, Nk,
                              bits, g.words, bits_t, g.words_t, flags, st) != cudaSuccess)
+    return ATTN_ERR_LAUNCH;
+  if ((stages & (kStagePrep | kStageDqRows)) && mask->bias != nullptr &&
+      sdpa::launch_bias_transpose(mask->bias, g.bias_planes, Nq, Nk, bias_t, st) != cudaSuccess)
     return ATTN_ERR_LAUNCH;
   if ((stages & kStagePrep) && sdpa::launch_bwd_prep(p, st) != cudaSuccess) return ATTN_ERR_LAUNCH;
   if (stages & kStageDqRows) {

@@ -59,7 +59,7 @@ struct BwdTraits {
 };
 
 // MASKED: the instance that applies p.mk (causal enters as wr = 0).
-template <int D, bool CAUSAL, bool MASKED>
+template <int D, bool CAUSAL, int MASKED>
 __global__ void __launch_bounds__(384, 1)
     bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
@@ -281,6 +281,33 @@ __global__ void __launch_bounds__(384, 1)
         for (int e = 0; e < 32; ++e) {
           x[e] = __uint_as_float(ra[e]);
           x[32 + e] = __uint_as_float(rb[e]);
+        }
+      }
+      if constexpr (MASKED == 2) {
+        // The additive mask over this key row and the warpgroup's 64 query
+        // columns, from its transposed copy, added as b / scale to the
+        // unscaled scores; query rows past Nq are not read.
+        const int kk = 128 * (int)(blockIdx.x % p.nkv) + r, q0 = 128 * i + 64 * X;
+        if (kk < p.Nk) {
+          const int bb = (int)(blockIdx.x / p.nkv) / p.Hkv, hq = seq_s[5] * p.G + g;
+          const float* bt_row = p.mk.bias_t + ((size_t)bias_plane(p.mk, bb, hq) * p.Nk + (size_t)kk) * p.N + (size_t)q0;
+          const int nv = min(64, p.N - q0);
+          if ((p.N & 3) == 0) {  // the transpose sits 16-byte aligned in the workspace
+#pragma unroll
+            for (int q = 0; q < 64; q += 4) {
+              if (q < nv) {
+                const float4 b4v = __ldg(reinterpret_cast<const float4*>(bt_row + q));
+                x[q] = fmaf(b4v.x, p.mk.inv_scale, x[q]);
+                x[q + 1] = fmaf(b4v.y, p.mk.inv_scale, x[q + 1]);
+                x[q + 2] = fmaf(b4v.z, p.mk.inv_scale, x[q + 2]);
+                x[q + 3] = fmaf(b4v.w, p.mk.inv_scale, x[q + 3]);
+              }
+            }
+          } else {
+#pragma unroll
+            for (int q = 0; q < 64; ++q)
+              if (q < nv) x[q] = fmaf(__ldg(bt_row + q), p.mk.inv_scale, x[q]);
+          }
         }
       }
       // P^T[r][q] = exp2(S^T * scale * log2e - lse2[q]); masked (key > query
@@ -589,7 +616,7 @@ size_t bwd_smem_bytes(int d) {
   }
 }
 
-template <int D, bool C, bool M = false>
+template <int D, bool C, int M = 0>
 static cudaError_t launch_main_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                                  const CUtensorMap& tdo, const CUtensorMap& tdk, const CUtensorMap& tdv,
                                  const BwdParams& p, cudaStream_t stream) {
@@ -605,10 +632,14 @@ cudaError_t launch_bwd_grad(int d, bool causal, const CUtensorMap& tq, const CUt
                             const CUtensorMap& tdo, const CUtensorMap& tdk, const CUtensorMap& tdv,
                             const BwdParams& p, cudaStream_t stream, bool masked) {
   if (masked) {
+    const bool bias = p.mk.bias != nullptr;  // the instance with the additive mask
     switch (d) {
-      case 64: return launch_main_t<64, false, true>(tq, tk, tv, tdo, tdk, tdv, p, stream);
-      case 96: return launch_main_t<96, false, true>(tq, tk, tv, tdo, tdk, tdv, p, stream);
-      case 128: return launch_main_t<128, false, true>(tq, tk, tv, tdo, tdk, tdv, p, stream);
+      case 64: return bias ? launch_main_t<64, false, 2>(tq, tk, tv, tdo, tdk, tdv, p, stream)
+                      : launch_main_t<64, false, 1>(tq, tk, tv, tdo, tdk, tdv, p, stream);
+      case 96: return bias ? launch_main_t<96, false, 2>(tq, tk, tv, tdo, tdk, tdv, p, stream)
+                      : launch_main_t<96, false, 1>(tq, tk, tv, tdo, tdk, tdv, p, stream);
+      case 128: return bias ? launch_main_t<128, false, 2>(tq, tk, tv, tdo, tdk, tdv, p, stream)
+                      : launch_main_t<128, false, 1>(tq, tk, tv, tdo, tdk, tdv, p, stream);
       default: return cudaErrorInvalidValue;
     }
   }

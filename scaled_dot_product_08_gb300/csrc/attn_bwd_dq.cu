@@ -55,7 +55,7 @@ __device__ __noinline__ void no_key_vectors(const BwdParams& p, bool varlen, int
 }
 
 // MASKED: the instance that applies p.mk (causal enters as wr = 0).
-template <int D, bool CAUSAL, bool MASKED>
+template <int D, bool CAUSAL, int MASKED>
 __global__ void __launch_bounds__(384, 1)
     bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
@@ -330,6 +330,31 @@ __global__ void __launch_bounds__(384, 1)
           x[32 + e] = __uint_as_float(rb[e]);
         }
       }
+      if constexpr (MASKED == 2) {
+        // The additive mask of this row over the warpgroup's 64 keys, added
+        // as b / scale to the unscaled scores; columns past Nk are not read.
+        const int row = 128 * i + r, k0 = (seq_s[4] + jt) * 128 + 64 * X;
+        if (row < seq_s[1]) {
+          const float* br = p.mk.bias + ((size_t)bias_plane(p.mk, b, h) * p.N + (size_t)row) * p.Nk + (size_t)k0;
+          const int nv = min(64, p.Nk - k0);
+          if ((p.Nk & 3) == 0 && (reinterpret_cast<uintptr_t>(p.mk.bias) & 15) == 0) {
+#pragma unroll
+            for (int k = 0; k < 64; k += 4) {
+              if (k < nv) {
+                const float4 b4v = __ldg(reinterpret_cast<const float4*>(br + k));
+                x[k] = fmaf(b4v.x, p.mk.inv_scale, x[k]);
+                x[k + 1] = fmaf(b4v.y, p.mk.inv_scale, x[k + 1]);
+                x[k + 2] = fmaf(b4v.z, p.mk.inv_scale, x[k + 2]);
+                x[k + 3] = fmaf(b4v.w, p.mk.inv_scale, x[k + 3]);
+              }
+            }
+          } else {
+#pragma unroll
+            for (int k = 0; k < 64; ++k)
+              if (k < nv) x[k] = fmaf(__ldg(br + k), p.mk.inv_scale, x[k]);
+          }
+        }
+      }
       // P[r][k] = exp2(S * scale * log2e - lse2[r]); invisible keys (past
       // the row's causal position, or past Nk) are exactly 0.
 #pragma unroll
@@ -578,7 +603,7 @@ size_t bwd_dq_smem_bytes(int d) {
   }
 }
 
-template <int D, bool C, bool M = false>
+template <int D, bool C, int M = 0>
 static cudaError_t launch_dq_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                                const CUtensorMap& tdo, const CUtensorMap& tdq, const CUtensorMap& to,
                                const BwdParams& p, cudaStream_t stream) {
@@ -594,10 +619,14 @@ cudaError_t launch_bwd_dq(int d, bool causal, const CUtensorMap& tq, const CUten
                           const CUtensorMap& tdo, const CUtensorMap& tdq, const CUtensorMap& to, const BwdParams& p,
                           cudaStream_t stream, bool masked) {
   if (masked) {
+    const bool bias = p.mk.bias != nullptr;  // the instance with the additive mask
     switch (d) {
-      case 64: return launch_dq_t<64, false, true>(tq, tk, tv, tdo, tdq, to, p, stream);
-      case 96: return launch_dq_t<96, false, true>(tq, tk, tv, tdo, tdq, to, p, stream);
-      case 128: return launch_dq_t<128, false, true>(tq, tk, tv, tdo, tdq, to, p, stream);
+      case 64: return bias ? launch_dq_t<64, false, 2>(tq, tk, tv, tdo, tdq, to, p, stream)
+                      : launch_dq_t<64, false, 1>(tq, tk, tv, tdo, tdq, to, p, stream);
+      case 96: return bias ? launch_dq_t<96, false, 2>(tq, tk, tv, tdo, tdq, to, p, stream)
+                      : launch_dq_t<96, false, 1>(tq, tk, tv, tdo, tdq, to, p, stream);
+      case 128: return bias ? launch_dq_t<128, false, 2>(tq, tk, tv, tdo, tdq, to, p, stream)
+                      : launch_dq_t<128, false, 1>(tq, tk, tv, tdo, tdq, to, p, stream);
       default: return cudaErrorInvalidValue;
     }
   }

@@ -51,7 +51,7 @@ struct FwdTraits {
 
 // MASKED: the instance that applies p.mk (sliding window, key lengths, a
 // bit mask), with causal entering as wr = 0; CAUSAL is then false.
-template <int D, bool CAUSAL, bool MASKED>
+template <int D, bool CAUSAL, int MASKED>
 __global__ void __launch_bounds__(384, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
@@ -270,6 +270,33 @@ __global__ void __launch_bounds__(384, 1)
           x[32 + i] = __uint_as_float(rb[i]);
           x[64 + i] = __uint_as_float(rc[i]);
           x[96 + i] = __uint_as_float(rd[i]);
+        }
+      }
+      if constexpr (MASKED == 2) {
+        // The additive mask of this row over the key tile, added as b / scale
+        // to the unscaled scores (scaled below: scale x + b); -inf hides the
+        // key.  Columns past Nk are not read (the bounds below hide them).
+        if (qi * 128 + r < p.Nq) {
+          const float* br = p.mk.bias + ((size_t)bias_plane(p.mk, b, h) * p.Nq + (size_t)(qi * 128 + r)) * p.Nk +
+                            (size_t)jt * 128;
+          const int nv = min(128, p.Nk - jt * 128);
+          if ((p.Nk & 3) == 0 && (reinterpret_cast<uintptr_t>(p.mk.bias) & 15) == 0) {
+            // rows start 16-byte aligned: four columns per load
+#pragma unroll
+            for (int i = 0; i < 128; i += 4) {
+              if (i < nv) {
+                const float4 b4v = __ldg(reinterpret_cast<const float4*>(br + i));
+                x[i] = fmaf(b4v.x, p.mk.inv_scale, x[i]);
+                x[i + 1] = fmaf(b4v.y, p.mk.inv_scale, x[i + 1]);
+                x[i + 2] = fmaf(b4v.z, p.mk.inv_scale, x[i + 2]);
+                x[i + 3] = fmaf(b4v.w, p.mk.inv_scale, x[i + 3]);
+              }
+            }
+          } else {
+#pragma unroll
+            for (int i = 0; i < 128; ++i)
+              if (i < nv) x[i] = fmaf(__ldg(br + i), p.mk.inv_scale, x[i]);
+          }
         }
       }
       if (MASKED) {
@@ -573,7 +600,7 @@ size_t fwd_smem_bytes(int d) {
   }
 }
 
-template <int D, bool C, bool M = false>
+template <int D, bool C, int M = 0>
 static cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                                 const CUtensorMap& to, const FwdParams& p, cudaStream_t stream) {
   auto kern = fwd_kernel<D, C, M>;
@@ -587,10 +614,14 @@ static cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, co
 cudaError_t launch_fwd(int d, bool causal, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                        const CUtensorMap& to, const FwdParams& p, cudaStream_t stream, bool masked) {
   if (masked) {
+    const bool bias = p.mk.bias != nullptr;  // the instance with the additive mask
     switch (d) {
-      case 64: return launch_fwd_t<64, false, true>(tq, tk, tv, to, p, stream);
-      case 96: return launch_fwd_t<96, false, true>(tq, tk, tv, to, p, stream);
-      case 128: return launch_fwd_t<128, false, true>(tq, tk, tv, to, p, stream);
+      case 64: return bias ? launch_fwd_t<64, false, 2>(tq, tk, tv, to, p, stream)
+                      : launch_fwd_t<64, false, 1>(tq, tk, tv, to, p, stream);
+      case 96: return bias ? launch_fwd_t<96, false, 2>(tq, tk, tv, to, p, stream)
+                      : launch_fwd_t<96, false, 1>(tq, tk, tv, to, p, stream);
+      case 128: return bias ? launch_fwd_t<128, false, 2>(tq, tk, tv, to, p, stream)
+                      : launch_fwd_t<128, false, 1>(tq, tk, tv, to, p, stream);
       default: return cudaErrorInvalidValue;
     }
   }

@@ -123,7 +123,36 @@ __global__ void __launch_bounds__(256) mask_pack_kernel(const uint8_t* __restric
   }
 }
 
+// The additive mask's transpose, (planes, Nq, Nk) -> (planes, Nk, Nq), for
+// the dK/dV kernel, whose threads own key rows: 32 x 32 blocks through
+// shared memory (pitch 33 words: the column reads hit distinct banks).
+__global__ void __launch_bounds__(256) bias_transpose_kernel(const float* __restrict__ bias, int Nq, int Nk,
+                                                             float* __restrict__ bias_t) {
+  __shared__ float blk[32][33];
+  const int tk = (Nk + 31) / 32;
+  const int kb = (int)(blockIdx.x % tk), qb = (int)(blockIdx.x / tk);
+  const size_t plane = blockIdx.y;
+  const float* src = bias + plane * Nq * Nk;
+  float* dst = bias_t + plane * Nq * Nk;
+  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
+  for (int rr = ty; rr < 32; rr += 8) {
+    const int qi = qb * 32 + rr, kj = kb * 32 + tx;
+    if (qi < Nq && kj < Nk) blk[rr][tx] = src[(size_t)qi * Nk + kj];
+  }
+  __syncthreads();
+  for (int rr = ty; rr < 32; rr += 8) {
+    const int kj = kb * 32 + rr, qi = qb * 32 + tx;
+    if (qi < Nq && kj < Nk) dst[(size_t)kj * Nq + qi] = blk[tx][rr];
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_bias_transpose(const float* bias, int planes, int Nq, int Nk, float* bias_t, cudaStream_t stream) {
+  const unsigned blocks = (unsigned)((Nq + 31) / 32) * (unsigned)((Nk + 31) / 32);
+  bias_transpose_kernel<<<dim3(blocks, (unsigned)planes), 256, 0, stream>>>(bias, Nq, Nk, bias_t);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_mask_pack(const uint8_t* mask, int mask_b, int mask_h, int Nq, int Nk, uint32_t* bits, int words,
                              uint32_t* bits_t, int words_t, uint8_t* flags, cudaStream_t stream) {

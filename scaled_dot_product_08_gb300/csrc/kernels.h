@@ -37,6 +37,14 @@ struct MaskArgs {
   int mask_b, mask_h;
   const uint8_t* flags;
   int ftq, ftk;  // query and key tiles per plane in flags
+  // Additive mask (float32, added to the scaled scores): (bias_b, bias_h,
+  // Nq, Nk) as given, and its (bias_b * bias_h, Nk, Nq) transpose for the
+  // dK/dV kernel (backward only); inv_scale = 1 / scale, so that x + b *
+  // inv_scale, scaled, is scale x + b.
+  const float* bias;
+  const float* bias_t;
+  int bias_b, bias_h;
+  float inv_scale;
 };
 
 // Most key tiles a masked forward / dQ CTA can list for skipping (its
@@ -136,6 +144,9 @@ __device__ __forceinline__ int floor_div128(int a) { return a >= 0 ? a / 128 : -
 __device__ __forceinline__ int mask_plane(const MaskArgs& mk, int b, int h) {
   return (mk.mask_b > 1 ? b : 0) * mk.mask_h + (mk.mask_h > 1 ? h : 0);
 }
+__device__ __forceinline__ int bias_plane(const MaskArgs& mk, int b, int h) {
+  return (mk.bias_b > 1 ? b : 0) * mk.bias_h + (mk.bias_h > 1 ? h : 0);
+}
 
 // One sequence of a (possibly packed) batch as a kernel sees it.
 struct SeqView {
@@ -180,6 +191,9 @@ cudaError_t launch_bwd_grad(int d, bool causal, const CUtensorMap& tq, const CUt
 cudaError_t launch_bwd_dq(int d, bool causal, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                           const CUtensorMap& tdo, const CUtensorMap& tdq, const CUtensorMap& to, const BwdParams& p,
                           cudaStream_t stream, bool masked = false);
+// Writes the (planes, Nk, Nq) transpose of a float32 (planes, Nq, Nk)
+// additive mask (the dK/dV kernel reads it by key row).
+cudaError_t launch_bias_transpose(const float* bias, int planes, int Nq, int Nk, float* bias_t, cudaStream_t stream);
 // Packs a boolean (mask_b, mask_h, Nq, Nk) byte mask into the row and
 // transposed bit layouts of MaskArgs (bits_t may be null: row bits only).
 cudaError_t launch_mask_pack(const uint8_t* mask, int mask_b, int mask_h, int Nq, int Nk, uint32_t* bits,

@@ -91,6 +91,7 @@ class Workload:
     window: tuple[int, int] | None = None     # masked: (left, right), -1 = open
     prefix: int | None = None                 # masked: prefix-LM boolean mask with this prefix
     page_size: int | None = None              # decode: the cache kept in pages of this many tokens
+    bias_slope: float | None = None           # masked: additive (1, 1, N, N) bias -slope * |i - j|
 
     @property
     def softmax_scale(self) -> float:
@@ -124,6 +125,7 @@ WORKLOADS: dict[str, Workload] = {
     "c4f8": Workload("c4f8", 1, 32, 8, 8192, 128, True, 4, amp=0.5, kind="fp8"),
     "sw1": Workload("sw1", 1, 32, 8, 16384, 128, True, 11, with_grad=True, kind="masked", window=(4095, -1)),
     "pl1": Workload("pl1", 8, 16, 16, 4096, 128, False, 12, with_grad=True, kind="masked", prefix=1024),
+    "ab1": Workload("ab1", 8, 16, 16, 4096, 128, False, 13, with_grad=True, kind="masked", bias_slope=1 / 64),
 }
 
 
@@ -135,10 +137,21 @@ def prefix_lm_mask(N: int, prefix: int) -> np.ndarray:
     return ((j < prefix) | (j <= i))[None, None]
 
 
+def distance_bias(N: int, slope: float) -> np.ndarray:
+    """Float32 (1, 1, N, N) additive mask -slope * |i - j|: a linear
+    distance penalty shared by every head (an input of the additive-mask
+    workload; all entries finite)."""
+    i = np.arange(N)[:, None]
+    j = np.arange(N)[None, :]
+    return (-slope * np.abs(i - j)).astype(np.float32)[None, None]
+
+
 def visible_pairs(w: Workload) -> int:
     """(query, key) pairs a masked self-attention workload computes, per
     (batch, head): the exact count, by closed form."""
     N = w.N
+    if w.bias_slope is not None and w.prefix is None and w.window is None:
+        return N * (N + 1) // 2 if w.causal else N * N  # a finite bias hides no key
     if w.prefix is not None:
         P = w.prefix
         return P * P + sum(i + 1 for i in range(P, N))

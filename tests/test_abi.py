@@ -219,7 +219,8 @@ def test_varlen_rejects_bad_arguments(lib):
 def test_masked_rejects_bad_arguments(lib):
     import scaled_dot_product_08_gb300 as sdpa
     S = sdpa.Status
-    M = lambda wl=-1, wr=-1, kl=0, m=0, mb=1, mh=1: sdpa.AttnMask(wl, wr, kl, m, mb, mh)
+    M = lambda wl=-1, wr=-1, kl=0, m=0, mb=1, mh=1, bias=0, bb=1, bh=1: sdpa.AttnMask(wl, wr, kl, m, mb, mh,
+                                                                                       bias, bb, bh)
     f = lambda mask, ws=FAKE, wsb=1 << 20, causal=0: sdpa.attn_fwd_masked(
         FAKE, FAKE, FAKE, FAKE, FAKE, 2, 4, 2, 100, 300, 128, 0.1, causal, mask, ws, wsb, None)
     assert f(M(wl=-2)) == S.INVALID_ARG
@@ -237,8 +238,16 @@ def test_masked_rejects_bad_arguments(lib):
     g = lambda stages, wsb=1 << 20: sdpa.attn_bwd_masked_stages(
         FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 2, 4, 2, 100, 300, 128, 0.1, 0, M(), FAKE, wsb,
         stages, None)
-    assert g(0) == S.INVALID_ARG and g(8) == S.INVALID_ARG
+    assert g(0) == S.INVALID_ARG and g(16) == S.INVALID_ARG and g(17) == S.INVALID_ARG
     assert g(7, wsb=16) == S.WORKSPACE
+    # the additive mask: float32, 4-byte aligned, (1 or B, 1 or H, Nq, Nk)
+    assert f(M(bias=FAKE + 2)) == S.MISALIGNED
+    assert f(M(bias=FAKE, bb=3)) == S.INVALID_ARG
+    assert f(M(bias=FAKE, bh=2)) == S.INVALID_ARG
+    # its transpose (float32, Nk x Nq per plane) joins the backward's workspace only
+    assert sdpa.attn_masked_workspace_size(2, 4, 2, 100, 300, 128, M(bias=FAKE, bh=4), 0) == 0
+    assert sdpa.attn_masked_workspace_size(2, 4, 2, 100, 300, 128, M(bias=FAKE, bh=4), 1) == \
+        sdpa.attn_bwd_workspace_size(2, 4, 2, 100, 128) + 4 * 100 * 300 * 4
 
 
 def test_fp8_rejects_bad_arguments(lib):

@@ -1,5 +1,5 @@
 """Full-size parity of the workloads bench.py times beyond the first path
-(cross attention, packed varlen, masks, FP8, decode): each test makes the
+(cross attention, packed varlen, masks, the additive mask, FP8, decode): each test makes the
 same call on the same seeded inputs as the benchmark, then checks sampled
 heads, sequences or query rows against the fp64 oracle, one by one."""
 import math
@@ -122,6 +122,27 @@ def test_pl1_prefix_lm_fwd_bwd(cuda_lib):
         ref = oracle.attention_masked_backward(x["q"][sl], x["k"][sl], x["v"][sl], x["do"][sl], s, False,
                                                None, None, mask)
         check_grads([g[sl] for g in grads], ref, f"pl1 ({b},{h})")
+
+
+def test_ab1_additive_mask_fwd_bwd(cuda_lib):
+    import torch
+    from sdpa_inputs import distance_bias
+    w = workload("ab1")
+    x = make_inputs(w)
+    s = w.softmax_scale
+    bias = distance_bias(w.N, w.bias_slope)
+    tb = torch.from_numpy(bias).cuda()
+    tq, tk, tv, tdo = dev(x["q"]), dev(x["k"]), dev(x["v"]), dev(x["do"])
+    O, lse = cuda_lib.forward_masked(tq, tk, tv, s, False, None, None, None, tb)
+    grads = [host(g) for g in cuda_lib.backward_masked(tq, tk, tv, O, lse, tdo, s, False, None, None, None, tb)]
+    for (b, h) in [(0, 0), (7, 15)]:
+        sl = (slice(b, b + 1), slice(h, h + 1))
+        Or, lr = oracle.attention_masked_forward(x["q"][sl], x["k"][sl], x["v"][sl], s, False, None, None, None,
+                                                 bias)
+        check_o_lse(host(O)[sl], host(lse)[sl], Or, lr, f"ab1 ({b},{h})")
+        ref = oracle.attention_masked_backward(x["q"][sl], x["k"][sl], x["v"][sl], x["do"][sl], s, False,
+                                               None, None, None, bias)
+        check_grads([g[sl] for g in grads], ref, f"ab1 ({b},{h})")
 
 
 def test_c4f8_fp8_rows(cuda_lib):

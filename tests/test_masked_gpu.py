@@ -208,3 +208,78 @@ def test_masked_stage_orders(cuda_lib):
                                                B, H, Hkv, N, N, d, 0.1, 1, m, P(ws), wsb, bad,
                                                sp) == cuda_lib.Status.INVALID_ARG
     assert cuda_lib.attn_get_device_status(None) == cuda_lib.Status.OK
+
+
+def _bias(shape, seed, dead=0.1):
+    """Finite biases in [-4, 4) with a share of -inf entries."""
+    rng = np.random.default_rng(seed)
+    b = rng.uniform(-4.0, 4.0, shape).astype(np.float32)
+    b[rng.random(shape) < dead] = -np.inf
+    return b
+
+
+BIAS_CASES = [
+    # (B, H, Hkv, Nq, Nk, d), causal, window, key_lengths, bool mask kind, bias shape kind
+    ((2, 4, 2, 300, 300, 128), True, None, None, None, "full"),     # per (batch, head), causal
+    ((1, 4, 4, 513, 513, 64), False, None, None, None, "shared"),   # one plane for all
+    ((2, 2, 1, 260, 700, 96), True, None, None, None, "batch"),     # Nq < Nk, GQA
+    ((2, 4, 2, 384, 384, 128), True, (150, -1), [384, 200], "batch", "head"),  # with every other mask
+]
+
+
+@pytest.mark.parametrize("case", BIAS_CASES, ids=lambda c: "B%dH%dKV%dQ%dK%dd%d" % c[0] + f"_c{int(c[1])}_{c[4]}_{c[5]}")
+def test_additive_mask_matches_oracle(cuda_lib, case):
+    import torch
+    shape, causal, window, kl, kind, bkind = case
+    B, H, Hkv, Nq, Nk, d = shape
+    q, k, v, do = _problem(B, H, Hkv, Nq, Nk, d, 49000 + Nq)
+    mask = _mask(kind, B, H, Nq, Nk, 49100 + Nq)
+    bshape = {"full": (B, H, Nq, Nk), "batch": (B, 1, Nq, Nk), "head": (1, H, Nq, Nk), "shared": (1, 1, Nq, Nk)}
+    bias = _bias(bshape[bkind], 49200 + Nq)
+    s = 1 / math.sqrt(d)
+    kt = _t(np.asarray(kl, dtype=np.int32), torch.int32) if kl is not None else None
+    mt = _t(mask.astype(np.uint8), torch.uint8) if mask is not None else None
+    bt = _t(bias, torch.float32)
+    tq, tk, tv, tdo = dev(q), dev(k), dev(v), dev(do)
+    O, lse = cuda_lib.forward_masked(tq, tk, tv, s, causal, window, kt, mt, bt)
+    g = cuda_lib.backward_masked(tq, tk, tv, O, lse, tdo, s, causal, window, kt, mt, bt)
+    assert cuda_lib.attn_get_device_status(None) == cuda_lib.Status.OK
+    Or, lr = oracle.attention_masked_forward(q, k, v, s, causal, window, kl, mask, bias)
+    ref = oracle.attention_masked_backward(q, k, v, do, s, causal, window, kl, mask, bias)
+    _check_forward(host(O), host(lse), Or, lr, str(case))
+    check_grads([host(x) for x in g], ref, str(case))
+
+
+def test_additive_mask_of_zeros_and_neg_inf_is_the_boolean_mask(cuda_lib):
+    # bias = 0 where the boolean mask is True and -inf where it is False
+    # gives the boolean mask's result (up to the extra add of zero).
+    import torch
+    B, H, Hkv, N, d = 2, 2, 2, 320, 128
+    q, k, v, do = (dev(x) for x in _problem(B, H, Hkv, N, N, d, 49500))
+    mask = _mask("batch", B, H, N, N, 49501)
+    bias = np.where(mask, 0.0, -np.inf).astype(np.float32)
+    Om, lm = cuda_lib.forward_masked(q, k, v, 0.1, False, None, None, _t(mask.astype(np.uint8), torch.uint8))
+    Ob, lb = cuda_lib.forward_masked(q, k, v, 0.1, False, None, None, None, _t(bias, torch.float32))
+    # (the boolean mask also skips the tiles it hides; the bias path visits
+    # them and adds exact zeros)
+    assert np.abs(host(Om) - host(Ob)).max() <= 2 ** -8
+    assert np.abs(host(lm) - host(lb)).max() <= 1e-5
+
+
+def test_rows_whose_bias_hides_every_key(cuda_lib):
+    import torch
+    B, H, Hkv, N, d = 1, 2, 2, 200, 64
+    q, k, v, do = _problem(B, H, Hkv, N, N, d, 49600)
+    bias = _bias((1, 1, N, N), 49601, 0.0)
+    bias[0, 0, [3, 150]] = -np.inf
+    bt = _t(bias, torch.float32)
+    tq, tk, tv, tdo = dev(q), dev(k), dev(v), dev(do)
+    O, lse = cuda_lib.forward_masked(tq, tk, tv, 0.125, False, None, None, None, bt)
+    g = cuda_lib.backward_masked(tq, tk, tv, O, lse, tdo, 0.125, False, None, None, None, bt)
+    O, lse = host(O), host(lse)
+    for r in (3, 150):
+        assert np.all(O[:, :, r] == 0) and np.all(np.isneginf(lse[:, :, r])) and np.all(host(g[0])[:, :, r] == 0)
+    Or, lr = oracle.attention_masked_forward(q, k, v, 0.125, False, None, None, None, bias)
+    _check_forward(O, lse, Or, lr, "bias dead rows")
+    check_grads([host(x) for x in g], oracle.attention_masked_backward(q, k, v, do, 0.125, False, None, None, None,
+                                                                      bias), "bias dead rows")
