@@ -263,6 +263,38 @@ __global__ void __launch_bounds__(384, 1)
       int g, i;
       step_at(it, g, i);
       const float* vl = vec_g + (it & 1) * (T::VEC_BYTES / 4) + 64 * X;  // -lse2 of this half; -D at +128
+      // The additive mask over this key row and the warpgroup's 64 query
+      // columns, from its transposed copy, loaded before the waits below;
+      // added as b / scale to the unscaled scores.  Query rows past Nq are
+      // not read.
+      float bb[MASKED == 2 ? 64 : 1];
+      if constexpr (MASKED == 2) {
+#pragma unroll
+        for (int q = 0; q < 64; ++q) bb[q] = 0.f;
+        const int kk = 128 * (int)(blockIdx.x % p.nkv) + r, q0 = 128 * i + 64 * X;
+        if (kk < p.Nk) {
+          const int bb_b = (int)(blockIdx.x / p.nkv) / p.Hkv, hq = seq_s[5] * p.G + g;
+          const float* bt_row =
+              p.mk.bias_t + ((size_t)bias_plane(p.mk, bb_b, hq) * p.Nk + (size_t)kk) * p.N + (size_t)q0;
+          const int nv = min(64, p.N - q0);
+          if ((p.N & 3) == 0) {  // the transpose sits 16-byte aligned in the workspace
+#pragma unroll
+            for (int q = 0; q < 64; q += 4) {
+              if (q < nv) {
+                const float4 b4v = __ldg(reinterpret_cast<const float4*>(bt_row + q));
+                bb[q] = b4v.x;
+                bb[q + 1] = b4v.y;
+                bb[q + 2] = b4v.z;
+                bb[q + 3] = b4v.w;
+              }
+            }
+          } else {
+#pragma unroll
+            for (int q = 0; q < 64; ++q)
+              if (q < nv) bb[q] = __ldg(bt_row + q);
+          }
+        }
+      }
       // The vectors come from the bulk copy of this step: observe its barrier
       // (complete by now) before reading them.
       ok = __all_sync(0xffffffffu, wait_bounded(wc, bQf + 8u * (it & 1), (it >> 1) & 1, wait_site(0x11, it)) &&
@@ -284,31 +316,8 @@ __global__ void __launch_bounds__(384, 1)
         }
       }
       if constexpr (MASKED == 2) {
-        // The additive mask over this key row and the warpgroup's 64 query
-        // columns, from its transposed copy, added as b / scale to the
-        // unscaled scores; query rows past Nq are not read.
-        const int kk = 128 * (int)(blockIdx.x % p.nkv) + r, q0 = 128 * i + 64 * X;
-        if (kk < p.Nk) {
-          const int bb = (int)(blockIdx.x / p.nkv) / p.Hkv, hq = seq_s[5] * p.G + g;
-          const float* bt_row = p.mk.bias_t + ((size_t)bias_plane(p.mk, bb, hq) * p.Nk + (size_t)kk) * p.N + (size_t)q0;
-          const int nv = min(64, p.N - q0);
-          if ((p.N & 3) == 0) {  // the transpose sits 16-byte aligned in the workspace
 #pragma unroll
-            for (int q = 0; q < 64; q += 4) {
-              if (q < nv) {
-                const float4 b4v = __ldg(reinterpret_cast<const float4*>(bt_row + q));
-                x[q] = fmaf(b4v.x, p.mk.inv_scale, x[q]);
-                x[q + 1] = fmaf(b4v.y, p.mk.inv_scale, x[q + 1]);
-                x[q + 2] = fmaf(b4v.z, p.mk.inv_scale, x[q + 2]);
-                x[q + 3] = fmaf(b4v.w, p.mk.inv_scale, x[q + 3]);
-              }
-            }
-          } else {
-#pragma unroll
-            for (int q = 0; q < 64; ++q)
-              if (q < nv) x[q] = fmaf(__ldg(bt_row + q), p.mk.inv_scale, x[q]);
-          }
-        }
+        for (int q = 0; q < 64; ++q) x[q] = fmaf(bb[q], p.mk.inv_scale, x[q]);
       }
       // P^T[r][q] = exp2(S^T * scale * log2e - lse2[q]); masked (key > query
       // on the diagonal tile) entries and padding key rows are exactly 0.

@@ -313,6 +313,35 @@ __global__ void __launch_bounds__(384, 1)
       uint2 bt = make_uint2(~0u, ~0u);
       const int jt = MASKED ? tile_at(j) : j;  // key tile relative to jlo
       if (MASKED && rowbits != 0xffffffffu) bt = *reinterpret_cast<const uint2*>(p.mk.bits + rowbits + 4u * jt);
+      // The additive mask of this row over the warpgroup's 64 keys, loaded
+      // before the wait for S; added as b / scale to the unscaled scores.
+      // Columns past Nk are not read.
+      float bb[MASKED == 2 ? 64 : 1];
+      if constexpr (MASKED == 2) {
+#pragma unroll
+        for (int k = 0; k < 64; ++k) bb[k] = 0.f;
+        const int row = 128 * i + r, k0 = (seq_s[4] + jt) * 128 + 64 * X;
+        if (row < seq_s[1]) {
+          const float* br = p.mk.bias + ((size_t)bias_plane(p.mk, b, h) * p.N + (size_t)row) * p.Nk + (size_t)k0;
+          const int nv = min(64, p.Nk - k0);
+          if ((p.Nk & 3) == 0 && (reinterpret_cast<uintptr_t>(p.mk.bias) & 15) == 0) {
+#pragma unroll
+            for (int k = 0; k < 64; k += 4) {
+              if (k < nv) {
+                const float4 b4v = __ldg(reinterpret_cast<const float4*>(br + k));
+                bb[k] = b4v.x;
+                bb[k + 1] = b4v.y;
+                bb[k + 2] = b4v.z;
+                bb[k + 3] = b4v.w;
+              }
+            }
+          } else {
+#pragma unroll
+            for (int k = 0; k < 64; ++k)
+              if (k < nv) bb[k] = __ldg(br + k);
+          }
+        }
+      }
       ok = __all_sync(0xffffffffu, wait_bounded(wc, bS + 8u * (j & 1), (j >> 1) & 1, wait_site(0x81, j)));
       if (!ok) break;
       tc_fence_after();
@@ -331,29 +360,8 @@ __global__ void __launch_bounds__(384, 1)
         }
       }
       if constexpr (MASKED == 2) {
-        // The additive mask of this row over the warpgroup's 64 keys, added
-        // as b / scale to the unscaled scores; columns past Nk are not read.
-        const int row = 128 * i + r, k0 = (seq_s[4] + jt) * 128 + 64 * X;
-        if (row < seq_s[1]) {
-          const float* br = p.mk.bias + ((size_t)bias_plane(p.mk, b, h) * p.N + (size_t)row) * p.Nk + (size_t)k0;
-          const int nv = min(64, p.Nk - k0);
-          if ((p.Nk & 3) == 0 && (reinterpret_cast<uintptr_t>(p.mk.bias) & 15) == 0) {
 #pragma unroll
-            for (int k = 0; k < 64; k += 4) {
-              if (k < nv) {
-                const float4 b4v = __ldg(reinterpret_cast<const float4*>(br + k));
-                x[k] = fmaf(b4v.x, p.mk.inv_scale, x[k]);
-                x[k + 1] = fmaf(b4v.y, p.mk.inv_scale, x[k + 1]);
-                x[k + 2] = fmaf(b4v.z, p.mk.inv_scale, x[k + 2]);
-                x[k + 3] = fmaf(b4v.w, p.mk.inv_scale, x[k + 3]);
-              }
-            }
-          } else {
-#pragma unroll
-            for (int k = 0; k < 64; ++k)
-              if (k < nv) x[k] = fmaf(__ldg(br + k), p.mk.inv_scale, x[k]);
-          }
-        }
+        for (int k = 0; k < 64; ++k) x[k] = fmaf(bb[k], p.mk.inv_scale, x[k]);
       }
       // P[r][k] = exp2(S * scale * log2e - lse2[r]); invisible keys (past
       // the row's causal position, or past Nk) are exactly 0.

@@ -249,6 +249,37 @@ __global__ void __launch_bounds__(384, 1)
       uint4 b4 = make_uint4(~0u, ~0u, ~0u, ~0u);
       const int jt = MASKED ? tile_at(j) : j;  // absolute key tile
       if (MASKED && rowbits != 0xffffffffu) b4 = *reinterpret_cast<const uint4*>(p.mk.bits + rowbits + 4u * jt);
+      // The additive mask of this row over the key tile, loaded before the
+      // wait for S so that its latency hides behind the Q K^T MMA; added as
+      // b / scale to the unscaled scores (scaled below: scale x + b); -inf
+      // hides the key.  Columns past Nk are not read (the bounds hide them).
+      float bb[MASKED == 2 ? 128 : 1];
+      if constexpr (MASKED == 2) {
+#pragma unroll
+        for (int i = 0; i < 128; ++i) bb[i] = 0.f;
+        if (qi * 128 + r < p.Nq) {
+          const float* br = p.mk.bias + ((size_t)bias_plane(p.mk, b, h) * p.Nq + (size_t)(qi * 128 + r)) * p.Nk +
+                            (size_t)jt * 128;
+          const int nv = min(128, p.Nk - jt * 128);
+          if ((p.Nk & 3) == 0 && (reinterpret_cast<uintptr_t>(p.mk.bias) & 15) == 0) {
+            // rows start 16-byte aligned: four columns per load
+#pragma unroll
+            for (int i = 0; i < 128; i += 4) {
+              if (i < nv) {
+                const float4 b4v = __ldg(reinterpret_cast<const float4*>(br + i));
+                bb[i] = b4v.x;
+                bb[i + 1] = b4v.y;
+                bb[i + 2] = b4v.z;
+                bb[i + 3] = b4v.w;
+              }
+            }
+          } else {
+#pragma unroll
+            for (int i = 0; i < 128; ++i)
+              if (i < nv) bb[i] = __ldg(br + i);
+          }
+        }
+      }
       ok = __all_sync(0xffffffffu, wait_bounded(wc, barS, j & 1, wait_site(0x51 + s, j)));
       if (!ok) break;
       tc_fence_after();
@@ -273,31 +304,8 @@ __global__ void __launch_bounds__(384, 1)
         }
       }
       if constexpr (MASKED == 2) {
-        // The additive mask of this row over the key tile, added as b / scale
-        // to the unscaled scores (scaled below: scale x + b); -inf hides the
-        // key.  Columns past Nk are not read (the bounds below hide them).
-        if (qi * 128 + r < p.Nq) {
-          const float* br = p.mk.bias + ((size_t)bias_plane(p.mk, b, h) * p.Nq + (size_t)(qi * 128 + r)) * p.Nk +
-                            (size_t)jt * 128;
-          const int nv = min(128, p.Nk - jt * 128);
-          if ((p.Nk & 3) == 0 && (reinterpret_cast<uintptr_t>(p.mk.bias) & 15) == 0) {
-            // rows start 16-byte aligned: four columns per load
 #pragma unroll
-            for (int i = 0; i < 128; i += 4) {
-              if (i < nv) {
-                const float4 b4v = __ldg(reinterpret_cast<const float4*>(br + i));
-                x[i] = fmaf(b4v.x, p.mk.inv_scale, x[i]);
-                x[i + 1] = fmaf(b4v.y, p.mk.inv_scale, x[i + 1]);
-                x[i + 2] = fmaf(b4v.z, p.mk.inv_scale, x[i + 2]);
-                x[i + 3] = fmaf(b4v.w, p.mk.inv_scale, x[i + 3]);
-              }
-            }
-          } else {
-#pragma unroll
-            for (int i = 0; i < 128; ++i)
-              if (i < nv) x[i] = fmaf(__ldg(br + i), p.mk.inv_scale, x[i]);
-          }
-        }
+        for (int i = 0; i < 128; ++i) x[i] = fmaf(bb[i], p.mk.inv_scale, x[i]);
       }
       if (MASKED) {
         const int lim = lim0 - jt * 128, lom = lom0 - jt * 128;
