@@ -295,6 +295,19 @@ __global__ void __launch_bounds__(384, 1)
           }
         }
       }
+      // Masked instance with a boolean mask: this key row's bits over the
+      // warpgroup's 64 query columns, loaded before the waits below so that
+      // the load's latency hides behind them.
+      uint2 bt = make_uint2(~0u, ~0u);
+      if (MASKED && p.mk.bits_t != nullptr) {
+        const int kk = 128 * (int)(blockIdx.x % p.nkv) + r;
+        if (kk < p.Nk) {
+          const int hq = seq_s[5] * p.G + g;  // query head of this step
+          const uint32_t plane = (uint32_t)seq_s[7] + (p.mk.mask_h > 1 ? (uint32_t)hq : 0u);
+          const uint32_t w = (plane * (uint32_t)p.Nk + (uint32_t)kk) * (uint32_t)p.mk.words_t + 2u * X + 4u * i;
+          bt = *reinterpret_cast<const uint2*>(p.mk.bits_t + w);
+        }
+      }
       // The vectors come from the bulk copy of this step: observe its barrier
       // (complete by now) before reading them.
       ok = __all_sync(0xffffffffu, wait_bounded(wc, bQf + 8u * (it & 1), (it >> 1) & 1, wait_site(0x11, it)) &&
@@ -340,13 +353,6 @@ __global__ void __launch_bounds__(384, 1)
         const int kk = 128 * (int)(blockIdx.x % p.nkv) + r, koff = seq_s[3] - seq_s[1];
         const int qmin = (kk >= seq_s[6] ? (1 << 30) : p.mk.wr >= 0 ? kk - p.mk.wr - koff - 64 * X : -(1 << 30)) - 128 * i;
         const int qmax = (p.mk.wl >= 0 ? kk + p.mk.wl - koff - 64 * X : (1 << 30)) - 128 * i;
-        uint2 bt = make_uint2(~0u, ~0u);
-        if (p.mk.bits_t != nullptr && kk < p.Nk) {
-          const int h = seq_s[5] * p.G + g;  // query head of this step
-          const uint32_t plane = (uint32_t)seq_s[7] + (p.mk.mask_h > 1 ? (uint32_t)h : 0u);
-          const uint32_t w = (plane * (uint32_t)p.Nk + (uint32_t)kk) * (uint32_t)p.mk.words_t + 2u * X + 4u * i;
-          bt = *reinterpret_cast<const uint2*>(p.mk.bits_t + w);
-        }
         if (__any_sync(0xffffffffu, qmin > 0 || qmax < 63 || (bt.x & bt.y) != ~0u)) {
 #pragma unroll
           for (int q = 0; q < 64; ++q)
