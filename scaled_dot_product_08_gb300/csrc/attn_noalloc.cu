@@ -1,8 +1,8 @@
 // attn_noalloc.cu — attn_bwd_noalloc: the backward pass for callers that
 // cannot allocate device memory.
 //
-// attn_bwd needs a caller-supplied float32 workspace (the dQ accumulator and
-// two per-row vectors).  Some callers cannot provide one: code that runs
+// attn_bwd needs a caller-supplied float32 workspace (two per-row vectors,
+// D = rowsum(dO * O) and the logsumexp in base 2).  Some callers cannot provide one: code that runs
 // where cudaMalloc is not allowed or not wanted, such as a custom allocator
 // that must not recurse into itself, a runtime that has already handed all
 // device memory to its own pool, or a plug-in ABI that passes only tensor
@@ -66,8 +66,9 @@ attn_status_t attn_bwd_noalloc(const void* q, const void* k, const void* v, cons
   void* scratch = nullptr;
   const attn_status_t s = scratch_address(&scratch);
   if (s != ATTN_OK) return s;
-  // attn_bwd's first stage clears the dQ accumulator and rewrites both row
-  // vectors, so nothing left in the scratch by an earlier call is read.
+  // attn_bwd's first kernel (dQ) writes both row vectors of every row
+  // before the dK/dV kernel reads them, so nothing left in the scratch by an
+  // earlier call is read.
   return attn_bwd(q, k, v, o, lse, dout, dq, dk, dv, scratch, kSdpaNoallocScratchBytes, B, H, Hkv, N, d, scale,
                   causal, stream);
 }
