@@ -309,9 +309,14 @@ __global__ void __launch_bounds__(384, 1)
         }
       }
       // The vectors come from the bulk copy of this step: observe its barrier
-      // (complete by now) before reading them.
-      ok = __all_sync(0xffffffffu, wait_bounded(wc, bQf + 8u * (it & 1), (it >> 1) & 1, wait_site(0x11, it)) &&
-                                       wait_bounded(wc, bS, it & 1, wait_site(0x12, it)));
+      // (complete by now) before reading them, and read this half's -lse2
+      // while S^T is still being computed.
+      ok = __all_sync(0xffffffffu, wait_bounded(wc, bQf + 8u * (it & 1), (it >> 1) & 1, wait_site(0x11, it)));
+      if (!ok) break;
+      float4 lv[16];
+#pragma unroll
+      for (int q4 = 0; q4 < 16; ++q4) lv[q4] = *reinterpret_cast<const float4*>(vl + 4 * q4);
+      ok = __all_sync(0xffffffffu, wait_bounded(wc, bS, it & 1, wait_site(0x12, it)));
       if (!ok) break;
       tc_fence_after();
       float x[64];
@@ -336,7 +341,7 @@ __global__ void __launch_bounds__(384, 1)
       // on the diagonal tile) entries and padding key rows are exactly 0.
 #pragma unroll
       for (int q4 = 0; q4 < 16; ++q4) {
-        const float4 l4 = *reinterpret_cast<const float4*>(vl + 4 * q4);
+        const float4 l4 = lv[q4];
         const float2 t0 = ffma2(make_float2(x[4 * q4 + 0], x[4 * q4 + 1]), c2, make_float2(l4.x, l4.y));
         const float2 t1 = ffma2(make_float2(x[4 * q4 + 2], x[4 * q4 + 3]), c2, make_float2(l4.z, l4.w));
         x[4 * q4 + 0] = ex2(t0.x);
