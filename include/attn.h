@@ -471,7 +471,14 @@ attn_status_t attn_selftest_wait_timeout(unsigned int timeout_us, void* stream);
  *     process exits.
  *   - Set-up: the first call on a device looks up the array's device address
  *     with that device current; make that first call before any stream
- *     capture.
+ *     capture.  The address is kept for the life of the process, so only
+ *     the device's primary context is supported, and no cudaDeviceReset
+ *     between calls.
+ *   - Errors: arguments and the device are checked as attn_bwd checks them,
+ *     with the same status values, before the array is looked up.  After a
+ *     call whose kernels timed out (ATTN_ERR_TIMEOUT from
+ *     attn_get_device_status), dK and dV may come from an earlier call's
+ *     row vectors and must be discarded.
  *   - Sharing: all calls use the same array, which keeps the last call's
  *     contents (each call rewrites what it reads).  Calls whose work
  *     overlaps on the GPU (different streams, or different host threads

@@ -516,6 +516,19 @@ attn_status_t attn_bwd_dq_rows(const void* q, const void* k, const void* v, cons
                        stream);
 }
 
+// Everything attn_bwd checks except the workspace, the device included, in
+// the same order (attn_bwd_noalloc runs it before it looks up its scratch).
+// Internal to the library: hidden from its exported symbols.
+__attribute__((visibility("hidden"))) attn_status_t sdpa_bwd_check_args(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                                  const void* dout, void* dq, void* dk, void* dv, int B, int H, int Hkv, int N,
+                                  int d, float scale, int causal) {
+  ATTN_TRY(check_scale_flag(scale, causal));
+  ATTN_TRY(check_bwd_shape(B, H, Hkv, N, N, d, causal));
+  ATTN_TRY(check_ptrs({q, k, v, o, lse, dout, dq, dk, dv}));
+  DeviceInfo* di = nullptr;
+  return current_device(&di);
+}
+
 attn_status_t attn_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
                        const void* dout, void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes,
                        int B, int H, int Hkv, int N, int d, float scale, int causal, void* stream) {

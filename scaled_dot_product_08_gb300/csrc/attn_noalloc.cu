@@ -14,6 +14,11 @@
 // loads the library holds it until the process exits.  All calls share it:
 // two calls whose kernels overlap on the GPU (on different streams, or from
 // different host threads) race on it and give wrong results.
+//
+// The array's device address is looked up once per device and kept for the
+// life of the process, so the library supports the primary context only: a
+// cudaDeviceReset (or a non-primary driver context) makes the kept address
+// stale.
 #include <cstdint>
 #include <mutex>
 
@@ -57,18 +62,29 @@ attn_status_t scratch_address(void** out) {
 
 extern "C" {
 
+// attn_bwd's checks (arguments, then the device), in attn_api.cu.
+attn_status_t sdpa_bwd_check_args(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                                  const void* dout, void* dq, void* dk, void* dv, int B, int H, int Hkv, int N,
+                                  int d, float scale, int causal);
+
 attn_status_t attn_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, const float* lse,
                                const void* dout, void* dq, void* dk, void* dv, int B, int H, int Hkv, int N, int d,
                                float scale, int causal, void* stream) {
   const size_t need = attn_bwd_workspace_size(B, H, Hkv, N, d);
   if (need == 0) return ATTN_ERR_UNSUPPORTED_SHAPE;
   if (need > kSdpaNoallocScratchBytes) return ATTN_ERR_WORKSPACE;  // shape too large for the fixed scratch
+  // Every other invalid argument, and an unsupported device, get attn_bwd's
+  // own status before the scratch is looked up.
+  attn_status_t s = sdpa_bwd_check_args(q, k, v, o, lse, dout, dq, dk, dv, B, H, Hkv, N, d, scale, causal);
+  if (s != ATTN_OK) return s;
   void* scratch = nullptr;
-  const attn_status_t s = scratch_address(&scratch);
+  s = scratch_address(&scratch);
   if (s != ATTN_OK) return s;
   // attn_bwd's first kernel (dQ) writes both row vectors of every row
-  // before the dK/dV kernel reads them, so nothing left in the scratch by an
-  // earlier call is read.
+  // before the dK/dV kernel reads them, so a call that completes without a
+  // timeout reads nothing an earlier call left in the scratch.  After a
+  // timeout (ATTN_ERR_TIMEOUT from attn_get_device_status) some row vectors
+  // may be an earlier call's, so dK and dV of that call must be discarded.
   return attn_bwd(q, k, v, o, lse, dout, dq, dk, dv, scratch, kSdpaNoallocScratchBytes, B, H, Hkv, N, d, scale,
                   causal, stream);
 }

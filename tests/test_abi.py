@@ -95,6 +95,21 @@ def test_bwd_rejects_bad_arguments(lib):
     assert sdpa.attn_bwd(*bad, FAKE, 1 << 20, 1, 2, 2, 64, 64, 0.1, 0, None) == sdpa.Status.MISALIGNED
 
 
+def test_bwd_noalloc_checks_arguments_before_its_scratch(lib):
+    # attn_bwd_noalloc reports attn_bwd's own status for a bad argument
+    # before it looks up its scratch array (which needs a device).
+    import scaled_dot_product_08_gb300 as sdpa
+    args = [FAKE] * 9
+    assert sdpa.attn_bwd_noalloc(*args, 1, 2, 2, 64, 80, 0.1, 0, None) == sdpa.Status.UNSUPPORTED_SHAPE
+    assert sdpa.attn_bwd_noalloc(*args, 1, 2, 2, 64, 64, float("nan"), 0, None) == sdpa.Status.INVALID_ARG
+    assert sdpa.attn_bwd_noalloc(*args, 1, 2, 2, 64, 64, 0.1, 2, None) == sdpa.Status.INVALID_ARG
+    bad = list(args)
+    bad[7] = FAKE + 4
+    assert sdpa.attn_bwd_noalloc(*bad, 1, 2, 2, 64, 64, 0.1, 0, None) == sdpa.Status.MISALIGNED
+    bad[7] = 0
+    assert sdpa.attn_bwd_noalloc(*bad, 1, 2, 2, 64, 64, 0.1, 0, None) == sdpa.Status.INVALID_ARG
+
+
 def _decode_chunks(B, Hkv, Nk):
     # The documented chunk plan: whole 128-key tiles, about 1216 CTAs in all
     # (ceil(1216 / (B * Hkv)) chunks while tiles last).
