@@ -616,6 +616,13 @@ def run_ours(args, w, rank, world, local_rank):
     roof = {"kernel": dom, "bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
             "frac": achieved / peak, "peak_source": src, f"frac_of_nominal_{int(nominal)}": achieved / nominal}
     roof["traffic"] = traffic_of(dom, w.name)
+    # The whole step, and the backward, on the method's own FLOPs (forward
+    # 4*B*H*N^2*d, halved when causal; backward 2.5 x forward) over the
+    # summed kernel times: what the kernels deliver of the work the method
+    # needs, whatever they re-execute.
+    roof["frac_method_step"] = flops / (sum(per_kernel.values()) / 1e3) / 1e12 / peak
+    if w.with_grad:
+        roof["frac_method_bwd"] = f_bwd / (sum(per_kernel[n] for n in names[1:]) / 1e3) / 1e12 / peak
 
     # ---- end to end through the C ABI with pinned host buffers
     e2e = None

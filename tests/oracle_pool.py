@@ -1,0 +1,96 @@
+"""Runs the fp64 oracle over whole heads in a pool of worker processes, for
+the full-size parity tests.
+
+Every full-size comparison is element by element: each worker takes one
+(batch, head) of the inputs and of the GPU's outputs (float32 copies of the
+bf16 / fp32 results), computes that head with the oracle, and returns the
+error sums of that head; the test adds them up over every head and checks
+the tolerances on the whole tensors.  No output is sampled.
+
+The pool uses the ``spawn`` start method, so it may be created after the
+CUDA context exists (a forked child of a CUDA process can hang).  Each
+worker runs single-threaded BLAS; the pool is as wide as the host's cores
+and its free memory allow.
+"""
+from __future__ import annotations
+
+import math
+import multiprocessing as mp
+import os
+
+import numpy as np
+
+import oracle
+
+_BLAS_ENV = ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS", "BLIS_NUM_THREADS")
+
+
+def _free_bytes() -> int:
+    try:
+        return int(os.sysconf("SC_AVPHYS_PAGES")) * int(os.sysconf("SC_PAGE_SIZE"))
+    except (ValueError, OSError):
+        return 16 << 30
+
+
+def make_pool(bytes_per_worker: int):
+    """A spawn pool of single-threaded workers: one per host core, fewer if
+    the free memory cannot hold ``bytes_per_worker`` for each."""
+    cores = os.cpu_count() or 1
+    n = max(1, min(cores, int(0.6 * _free_bytes()) // max(1, bytes_per_worker)))
+    saved = {k: os.environ.get(k) for k in _BLAS_ENV}
+    for k in _BLAS_ENV:
+        os.environ[k] = "1"
+    try:
+        pool = mp.get_context("spawn").Pool(n)
+    finally:
+        for k, v in saved.items():
+            if v is None:
+                os.environ.pop(k, None)
+            else:
+                os.environ[k] = v
+    return pool, n
+
+
+def forward_head(task):
+    """Oracle forward of one head against the GPU's O and lse of that head.
+
+    task: (q (Nq, d), k (Nk, d), v (Nk, d), O (Nq, d_out), lse (Nq,), scale,
+    causal, q_offset, d_use).  Columns d_use.. of O are zero-padding columns:
+    they must be exactly 0, and the oracle runs on the first d_use columns."""
+    q, k, v, O, lse, scale, causal, q_offset, d_use = task
+    one = lambda a: np.asarray(a[None, None, :, :d_use], dtype=np.float64)
+    O_ref, lse_ref = oracle.attention_forward(one(q), one(k), one(v), scale, causal, q_offset=q_offset)
+    err = np.abs(np.asarray(O[:, :d_use], np.float64) - O_ref[0, 0])
+    lerr = np.abs(np.asarray(lse, np.float64) - lse_ref[0, 0])
+    return {
+        "finite": bool(np.all(np.isfinite(O)) and np.all(np.isfinite(lse))),
+        "pad_zero": bool(np.all(O[:, d_use:] == 0.0)),
+        "o_max": float(err.max()),
+        "o_sum": float(err.sum()),
+        "o_n": int(err.size),
+        "lse_max": float(lerr.max()),
+    }
+
+
+def backward_head(task):
+    """Oracle forward and backward of one head (H = Hkv) against the GPU's O,
+    lse, dQ, dK and dV of that head.
+
+    task: (q, k, v, do, O, lse, dq, dk, dv, scale, causal).  Returns the
+    forward errors of ``forward_head`` and, per gradient, the sums of squared
+    errors and of squared reference values (for the relative Frobenius error
+    of the whole tensor), plus the head's own relative error."""
+    q, k, v, do, O, lse, dq, dk, dv, scale, causal = task
+    out = forward_head((q, k, v, O, lse, scale, causal, 0, q.shape[1]))
+    one = lambda a: np.asarray(a[None, None], dtype=np.float64)
+    ref = oracle.attention_backward(one(q), one(k), one(v), one(do), scale, causal)
+    for name, g, r in zip(("dq", "dk", "dv"), (dq, dk, dv), ref):
+        g = np.asarray(g, np.float64)
+        r = r[0, 0]
+        e2 = float(((g - r) ** 2).sum())
+        r2 = float((r ** 2).sum())
+        out[name + "_finite"] = bool(np.all(np.isfinite(g)))
+        out[name + "_e2"] = e2
+        out[name + "_r2"] = r2
+        out[name + "_head"] = math.sqrt(e2 / r2) if r2 > 0 else math.sqrt(e2)
+    return out

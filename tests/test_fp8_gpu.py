@@ -2,12 +2,14 @@
 against the fp64 oracle on the dequantised e4m3 inputs.
 
 Tolerance (the pages give none for FP8): the kernel rounds P to e4m3 before
-the P V product, which moves each probability by up to 2^-4 of itself
-(3-bit mantissa, round to nearest).  A CPU simulation of that rounding alone
-on these shapes gives a relative Frobenius error of O of 1.0-2.4% per head;
-the bound used is twice the largest, 5e-2 per (batch, head), with a mean
-absolute error of O <= 8e-3.  lse comes from float32 scores of exact e4m3
-products, so it keeps the bf16 path's bound, 1e-3."""
+the P V product.  tests/test_fp8_tolerance.py runs that rounding alone, in an
+otherwise exact fp64 forward (tests/fp8_model.py), on these cases: the worst
+relative Frobenius error of O per head is 2.67e-2, the mean |err| 3.5e-3.
+The bounds against the oracle are about twice those, 6e-2 per (batch, head)
+and 8e-3.  Each case is also compared with that rounding model itself,
+within 5e-3 per head: the kernel rounds where the model does.  lse comes
+from float32 scores of exact e4m3 products, so it keeps the bf16 path's
+bound, 1e-3."""
 import math
 
 import numpy as np
@@ -15,12 +17,10 @@ import pytest
 
 import oracle
 from sdpa_inputs import e4m3_decode, make_random, quantize_e4m3
+from tests.fp8_model import FP8_MODEL_REL_FRO, O_MEAN_ABS_FP8, O_REL_FRO_FP8, SHAPES, p_rounding_model
 from tests.parity import LSE_MAX_ABS, host
 
 pytestmark = pytest.mark.gpu
-
-O_REL_FRO_FP8 = 5e-2
-O_MEAN_ABS_FP8 = 8e-3
 
 
 def _u8(a):
@@ -40,43 +40,36 @@ def _run(lib, shape, causal, seed, amp=1.0):
     qd, kd, vd = e4m3_decode(qb) * qs, e4m3_decode(kb) * ks, e4m3_decode(vb) * vs
     off = (Nk - Nq) if causal else 0
     Or, lr = oracle.attention_forward(qd, kd, vd, s, causal, q_offset=off)
-    return host(O), host(lse), Or, lr
+    G = H // Hkv
+    Om = np.stack([np.stack([p_rounding_model(qd[b, h], kd[b, h // G], vd[b, h // G], s, causal, off)
+                             for h in range(H)]) for b in range(B)])
+    return host(O), host(lse), Or, lr, Om
 
 
-def _check(O, lse, Or, lr, what):
+def _check(O, lse, Or, lr, Om, what):
     assert np.all(np.isfinite(O)) and np.all(np.isfinite(lse)), what
     B, H = O.shape[:2]
     for b in range(B):
         for h in range(H):
             e = np.linalg.norm(O[b, h] - Or[b, h]) / np.linalg.norm(Or[b, h])
             assert e <= O_REL_FRO_FP8, f"{what} (b={b}, h={h}): O rel Frobenius {e:.3e}"
+            em = np.linalg.norm(O[b, h] - Om[b, h]) / np.linalg.norm(Om[b, h])
+            assert em <= FP8_MODEL_REL_FRO, f"{what} (b={b}, h={h}): O against the rounding model {em:.3e}"
     assert np.abs(O - Or).mean() <= O_MEAN_ABS_FP8, what
     assert np.abs(lse - lr).max() <= LSE_MAX_ABS, f"{what}: lse err {np.abs(lse - lr).max():.3e}"
-
-
-SHAPES = [
-    # B, H, Hkv, Nq, Nk, d
-    (1, 2, 2, 512, 512, 128),
-    (2, 4, 2, 700, 700, 128),    # ragged, GQA
-    (1, 2, 1, 129, 129, 128),
-    (1, 4, 4, 256, 1024, 128),   # cross: Nq < Nk
-    (1, 2, 2, 1, 300, 128),      # one query row
-]
 
 
 @pytest.mark.parametrize("causal", [False, True])
 @pytest.mark.parametrize("shape", SHAPES, ids=lambda s: "B%dH%dKV%dQ%dK%dd%d" % s)
 def test_fp8_forward_matches_oracle(cuda_lib, shape, causal):
-    O, lse, Or, lr = _run(cuda_lib, shape, causal, 50000 + shape[3] + shape[4])
-    _check(O, lse, Or, lr, f"{shape} causal={causal}")
+    _check(*_run(cuda_lib, shape, causal, 50000 + shape[3] + shape[4]), f"{shape} causal={causal}")
 
 
 @pytest.mark.parametrize("amp", [0.25, 3.0])
 def test_fp8_forward_score_ranges(cuda_lib, amp):
     # Flat (small scores) and peaked (large scores) softmax rows.
     shape = (1, 2, 2, 384, 384, 128)
-    O, lse, Or, lr = _run(cuda_lib, shape, True, 51000, amp)
-    _check(O, lse, Or, lr, f"amp={amp}")
+    _check(*_run(cuda_lib, shape, True, 51000, amp), f"amp={amp}")
 
 
 def test_fp8_rejects_other_head_dims(cuda_lib):

@@ -147,7 +147,7 @@ def test_ab1_additive_mask_fwd_bwd(cuda_lib):
 
 def test_c4f8_fp8_rows(cuda_lib):
     import torch
-    from tests.test_fp8_gpu import O_MEAN_ABS_FP8, O_REL_FRO_FP8
+    from tests.fp8_model import FP8_MODEL_REL_FRO, O_MEAN_ABS_FP8, O_REL_FRO_FP8, p_rounding_model
     from tests.parity import LSE_MAX_ABS
     w = workload("c4f8")
     x = make_inputs(w)
@@ -156,7 +156,11 @@ def test_c4f8_fp8_rows(cuda_lib):
     O, lse = cuda_lib.forward_fp8(u8(qz[0][0]), u8(qz[1][0]), u8(qz[2][0]), qz[0][1], qz[1][1], qz[2][1],
                                   w.softmax_scale, True)
     deq = [e4m3_decode(b) * sc for b, sc in qz]
-    O_s, l_s, O_r, l_r = _rows_check(host(O), host(lse), x, w, [(0, 0), (0, 7), (0, 30)], 0, "c4f8", deq)
+    heads = [(0, 0), (0, 7), (0, 30)]
+    O_s, l_s, O_r, l_r = _rows_check(host(O), host(lse), x, w, heads, 0, "c4f8", deq)
+    O_m = np.concatenate([p_rounding_model(deq[0][b, h], deq[1][b, h // 4], deq[2][b, h // 4], w.softmax_scale, True,
+                                           0, sample_rows(w.N, seed=b * 1000 + h)) for (b, h) in heads])
+    assert np.linalg.norm(O_s - O_m) / np.linalg.norm(O_m) <= FP8_MODEL_REL_FRO
     assert np.linalg.norm(O_s - O_r) / np.linalg.norm(O_r) <= O_REL_FRO_FP8
     assert np.abs(O_s - O_r).mean() <= O_MEAN_ABS_FP8
     assert np.abs(l_s - l_r).max() <= LSE_MAX_ABS

@@ -1,5 +1,7 @@
 """GPU parity of the forward pass (attn_fwd through the C ABI) against the
-CPU fp64 oracle on the same seeded bf16 inputs."""
+CPU fp64 oracle on the same seeded bf16 inputs: small and ragged shapes,
+every element, and the invariants the oracle is pinned by.  The full-size
+workloads are compared element by element in test_fullsize_gpu.py."""
 import math
 
 import numpy as np
@@ -7,7 +9,7 @@ import pytest
 
 import oracle
 from sdpa_inputs import make_inputs, make_random, workload
-from tests.parity import LSE_MAX_ABS, check_o_lse, dev, host, sample_rows
+from tests.parity import LSE_MAX_ABS, check_o_lse, dev, host
 
 pytestmark = pytest.mark.gpu
 
@@ -48,40 +50,6 @@ def test_forward_c1_full(cuda_lib):
     O, lse = cuda_lib.forward(dev(x["q"]), dev(x["k"]), dev(x["v"]), w.softmax_scale, w.causal)
     O_ref, lse_ref = oracle.attention_forward(x["q"], x["k"], x["v"], w.softmax_scale, w.causal)
     check_o_lse(host(O), host(lse), O_ref, lse_ref, "c1")
-
-
-def _sampled_check(cuda_lib, name, heads):
-    w = workload(name)
-    x = make_inputs(w)
-    O, lse = cuda_lib.forward(dev(x["q"]), dev(x["k"]), dev(x["v"]), w.softmax_scale, w.causal)
-    O, lse = host(O), host(lse)
-    assert np.all(np.isfinite(O)) and np.all(np.isfinite(lse))
-    G = w.H // w.Hkv
-    errs, refs = [], []
-    for (b, h) in heads:
-        rows = sample_rows(w.N, seed=b * 1000 + h)
-        dd = w.d_draw or w.d
-        Or, lr = oracle.attention_forward_rows(x["q"][b, h, :, :dd], x["k"][b, h // G, :, :dd],
-                                               x["v"][b, h // G, :, :dd], rows, w.softmax_scale, w.causal)
-        if dd != w.d:  # padded head_dim: the pad columns must be exactly zero
-            assert np.all(O[b, h, :, dd:] == 0.0)
-        errs.append((O[b, h, rows, :dd], lse[b, h, rows]))
-        refs.append((Or, lr))
-    O_s = np.concatenate([e[0] for e in errs])
-    l_s = np.concatenate([e[1] for e in errs])
-    return check_o_lse(O_s, l_s, np.concatenate([r[0] for r in refs]), np.concatenate([r[1] for r in refs]), name)
-
-
-@pytest.mark.parametrize("name,heads", [
-    ("c2", [(0, 0), (1, 7), (3, 15)]),
-    ("c3", [(0, 0), (0, 50), (0, 95)]),
-    ("c3c", [(0, 0), (0, 50), (0, 95)]),
-    ("c4", [(0, 0), (0, 3), (0, 4), (0, 31)]),
-    ("c4p", [(0, 0), (0, 13), (0, 31)]),
-    ("c5", [(0, 0), (4, 9), (7, 15)]),
-])
-def test_forward_full_size_sampled_rows(cuda_lib, name, heads):
-    _sampled_check(cuda_lib, name, heads)
 
 
 # ----------------------------------------------------------------- invariants
