@@ -30,6 +30,7 @@
 // O rescale in TMEM is rare; the result is exact either way because the final
 // normalisation uses the same max as every exponent.
 #include <cmath>
+#include <type_traits>
 
 #include "kernels.h"
 #include "ptx.cuh"
@@ -242,7 +243,10 @@ __global__ void __launch_bounds__(384, 1)
     // only masked keys so far (packed batches) then gets p = 2^(-inf) = 0 for
     // them instead of 2^(-inf + inf) = NaN, and the first visible key still
     // raises the max (alpha = 2^(-1e30 - m) = 0).
-    float m = -1e30f, l = 0.f;
+    // l: sum of the fp32 p (for lse); lo: the normaliser of O, which on
+    // tiles with hidden columns adds the bf16-rounded p that the P V product
+    // uses instead (see below).
+    float m = -1e30f, l = 0.f, lo = 0.f;
     bool ok = true;
 
     for (int j = 0; j < n; ++j) {
@@ -307,10 +311,12 @@ __global__ void __launch_bounds__(384, 1)
 #pragma unroll
         for (int i = 0; i < 128; ++i) x[i] = fmaf(bb[i], p.mk.inv_scale, x[i]);
       }
+      bool edge;  // some row of the warp has hidden columns in this tile (warp-uniform)
       if (MASKED) {
         const int lim = lim0 - jt * 128, lom = lom0 - jt * 128;
         const bool all_bits = (b4.x & b4.y & b4.z & b4.w) == ~0u;
-        if (__any_sync(0xffffffffu, lim < 128 || lom > 0 || !all_bits)) {
+        edge = __any_sync(0xffffffffu, lim < 128 || lom > 0 || !all_bits);
+        if (edge) {
           const uint32_t bw[4] = {b4.x, b4.y, b4.z, b4.w};
 #pragma unroll
           for (int i = 0; i < 128; ++i)
@@ -319,7 +325,8 @@ __global__ void __launch_bounds__(384, 1)
       } else {
         // Only the diagonal and the ragged last tile have masked columns.
         const int lim = lim0 - j * 128;
-        if (__any_sync(0xffffffffu, lim < 128)) {
+        edge = __any_sync(0xffffffffu, lim < 128);
+        if (edge) {
 #pragma unroll
           for (int i = 0; i < 128; ++i)
             if (i >= lim) x[i] = -INFINITY;
@@ -362,28 +369,57 @@ __global__ void __launch_bounds__(384, 1)
       // sum runs in 4 packed partial sums.  P is published in two halves of
       // 64 keys (one barrier per half) so that the P V MMA over the first 64
       // keys runs while the second half is computed.
+      //
+      // On a tile with hidden columns (the causal diagonal, a ragged last
+      // tile, a mask edge) O's normaliser also sums the bf16-rounded p the
+      // P V product applies, so that the weights of those keys sum exactly
+      // to their share: a row whose keys all lie in such a tile (the first
+      // rows of a causal head, few keys, O of the size of single V rows) is
+      // then an exact convex combination of its V rows.  Rows with many
+      // keys average the rounding out, and interior tiles keep one sum.
       const float2 c2 = make_float2(c, c), nm2 = make_float2(-m, -m);
-      float2 sum[4];
+      float2 sum[4], sumr = make_float2(0.f, 0.f);
 #pragma unroll
       for (int k = 0; k < 4; ++k) sum[k] = make_float2(0.f, 0.f);
+      auto publish = [&](auto rounded) {
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        uint32_t pk[32];
+        for (int h = 0; h < 2; ++h) {
+          uint32_t pk[32];
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          const int i = 64 * h + 2 * e;
-          const float2 t = ffma2(make_float2(x[i], x[i + 1]), c2, nm2);
-          const float2 pp = make_float2(ex2(t.x), ex2(t.y));
-          sum[e & 3] = fadd2(sum[e & 3], pp);
-          pk[e] = pack_bf16(pp.x, pp.y);
+          for (int e = 0; e < 32; ++e) {
+            const int i = 64 * h + 2 * e;
+            const float2 t = ffma2(make_float2(x[i], x[i + 1]), c2, nm2);
+            const float2 pp = make_float2(ex2(t.x), ex2(t.y));
+            // (two partial sums on the edge path, which also carries sumr)
+            if constexpr (decltype(rounded)::value)
+              sum[e & 1] = fadd2(sum[e & 1], pp);
+            else
+              sum[e & 3] = fadd2(sum[e & 3], pp);
+            pk[e] = pack_bf16(pp.x, pp.y);
+          }
+          tmem_st32(tS + 32 * h, pk);
+          if constexpr (decltype(rounded)::value) {
+#pragma unroll
+            for (int e = 0; e < 32; ++e)
+              sumr = fadd2(sumr, make_float2(__uint_as_float(pk[e] << 16), __uint_as_float(pk[e] & 0xffff0000u)));
+          }
+          tmem_wait_st();
+          tc_fence_before();
+          mbar_arrive(barP + 8u * h);
         }
-        tmem_st32(tS + 32 * h, pk);
-        tmem_wait_st();
-        tc_fence_before();
-        mbar_arrive(barP + 8u * h);
+      };
+      if (edge) {
+        publish(std::true_type{});
+        const float2 s01 = fadd2(sum[0], sum[1]);
+        l = l * alpha + (s01.x + s01.y);
+        lo = lo * alpha + (sumr.x + sumr.y);
+      } else {
+        publish(std::false_type{});
+        const float2 s01 = fadd2(sum[0], sum[1]), s23 = fadd2(sum[2], sum[3]);
+        const float st = (s01.x + s23.x) + (s01.y + s23.y);
+        l = l * alpha + st;
+        lo = lo * alpha + st;
       }
-      const float2 s01 = fadd2(sum[0], sum[1]), s23 = fadd2(sum[2], sum[3]);
-      l = l * alpha + ((s01.x + s23.x) + (s01.y + s23.y));
     }
 
     // ------------------------------------------------------------ epilogue
@@ -391,7 +427,7 @@ __global__ void __launch_bounds__(384, 1)
     const uint32_t sOut = sQ + s * T::TILE_BYTES;  // Q tile is dead once O is final
     if (ok) {
       tc_fence_after();
-      const float inv = l > 0.f ? 1.f / l : 0.f;  // a row that saw no key: O = 0, lse = -inf
+      const float inv = lo > 0.f ? 1.f / lo : 0.f;  // a row that saw no key: O = 0, lse = -inf
 #pragma unroll
       for (int cc = 0; cc < D / 32; ++cc) {
         uint32_t o[32];

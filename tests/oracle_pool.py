@@ -55,13 +55,15 @@ def forward_head(task):
     """Oracle forward of one head against the GPU's O and lse of that head.
 
     task: (q (Nq, d), k (Nk, d), v (Nk, d), O (Nq, d_out), lse (Nq,), scale,
-    causal, q_offset, d_use).  Columns d_use.. of O are zero-padding columns:
-    they must be exactly 0, and the oracle runs on the first d_use columns."""
-    q, k, v, O, lse, scale, causal, q_offset, d_use = task
+    causal, q_offset, d_use, head).  Columns d_use.. of O are zero-padding
+    columns: they must be exactly 0, and the oracle runs on the first d_use
+    columns.  ``head`` is a label returned with the result."""
+    q, k, v, O, lse, scale, causal, q_offset, d_use, head = task
     one = lambda a: np.asarray(a[None, None, :, :d_use], dtype=np.float64)
     O_ref, lse_ref = oracle.attention_forward(one(q), one(k), one(v), scale, causal, q_offset=q_offset)
     err = np.abs(np.asarray(O[:, :d_use], np.float64) - O_ref[0, 0])
     lerr = np.abs(np.asarray(lse, np.float64) - lse_ref[0, 0])
+    at = np.unravel_index(int(np.argmax(err)), err.shape)
     return {
         "finite": bool(np.all(np.isfinite(O)) and np.all(np.isfinite(lse))),
         "pad_zero": bool(np.all(O[:, d_use:] == 0.0)),
@@ -69,6 +71,9 @@ def forward_head(task):
         "o_sum": float(err.sum()),
         "o_n": int(err.size),
         "lse_max": float(lerr.max()),
+        "head": head,
+        # where the largest O error is: (row, column, GPU value, oracle value)
+        "o_max_at": (int(at[0]), int(at[1]), float(O[at]), float(O_ref[0, 0][at])),
     }
 
 
@@ -76,12 +81,12 @@ def backward_head(task):
     """Oracle forward and backward of one head (H = Hkv) against the GPU's O,
     lse, dQ, dK and dV of that head.
 
-    task: (q, k, v, do, O, lse, dq, dk, dv, scale, causal).  Returns the
+    task: (q, k, v, do, O, lse, dq, dk, dv, scale, causal, head).  Returns the
     forward errors of ``forward_head`` and, per gradient, the sums of squared
     errors and of squared reference values (for the relative Frobenius error
     of the whole tensor), plus the head's own relative error."""
-    q, k, v, do, O, lse, dq, dk, dv, scale, causal = task
-    out = forward_head((q, k, v, O, lse, scale, causal, 0, q.shape[1]))
+    q, k, v, do, O, lse, dq, dk, dv, scale, causal, head = task
+    out = forward_head((q, k, v, O, lse, scale, causal, 0, q.shape[1], head))
     one = lambda a: np.asarray(a[None, None], dtype=np.float64)
     ref = oracle.attention_backward(one(q), one(k), one(v), one(do), scale, causal)
     for name, g, r in zip(("dq", "dk", "dv"), (dq, dk, dv), ref):
