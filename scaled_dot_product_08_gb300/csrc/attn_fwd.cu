@@ -370,13 +370,14 @@ __global__ void __launch_bounds__(384, 1)
       // 64 keys (one barrier per half) so that the P V MMA over the first 64
       // keys runs while the second half is computed.
       //
-      // On a tile with hidden columns (the causal diagonal, a ragged last
-      // tile, a mask edge) O's normaliser also sums the bf16-rounded p the
-      // P V product applies, so that the weights of those keys sum exactly
-      // to their share: a row whose keys all lie in such a tile (the first
-      // rows of a causal head, few keys, O of the size of single V rows) is
-      // then an exact convex combination of its V rows.  Rows with many
-      // keys average the rounding out, and interior tiles keep one sum.
+      // On the first tile a row visits, when it has hidden columns (the
+      // causal diagonal of the first query tile, a ragged single tile, a
+      // mask edge), O's normaliser also sums the bf16-rounded p the P V
+      // product applies, so that the weights of those keys sum exactly to
+      // their share: a row whose keys all lie in that tile (the first rows
+      // of a causal head: few keys, O of the size of single V rows) is then
+      // an exact convex combination of its V rows.  Rows with many keys
+      // average the rounding out, and every other tile keeps one sum.
       const float2 c2 = make_float2(c, c), nm2 = make_float2(-m, -m);
       float2 sum[4], sumr = make_float2(0.f, 0.f);
 #pragma unroll
@@ -408,7 +409,7 @@ __global__ void __launch_bounds__(384, 1)
           mbar_arrive(barP + 8u * h);
         }
       };
-      if (edge) {
+      if (edge && j == 0) {
         publish(std::true_type{});
         const float2 s01 = fadd2(sum[0], sum[1]);
         l = l * alpha + (s01.x + s01.y);
