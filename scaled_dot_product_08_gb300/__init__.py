@@ -23,6 +23,7 @@ __all__ = [
     "AttnError", "Status", "load", "attn_fwd", "attn_bwd", "attn_bwd_workspace_size",
     "attn_bwd_prep", "attn_bwd_grad", "attn_bwd_dq", "attn_bwd_dq_rows", "attn_bwd_noalloc",
     "attn_get_device_status", "attn_get_timeout_info", "attn_status_string", "attn_selftest_wait_timeout",
+    "attn_debug_drop_load",
     "attn_decode", "attn_decode_workspace_size", "attn_fwd_cross", "attn_bwd_cross",
     "attn_bwd_grad_cross", "attn_bwd_dq_cross", "attn_fwd_varlen", "attn_bwd_varlen",
     "attn_bwd_varlen_workspace_size", "attn_bwd_varlen_stages", "forward_varlen", "backward_varlen",
@@ -85,6 +86,8 @@ def load() -> ctypes.CDLL:
         lib.attn_bwd_grad.restype = _I
         lib.attn_bwd_dq.argtypes = [_P, _P, _P, _P, _P, _P, ctypes.c_size_t, _I, _I, _I, _I, _I, ctypes.c_float, _I, _P]
         lib.attn_bwd_dq.restype = _I
+        lib.attn_debug_drop_load.argtypes = [_I, _I, ctypes.c_uint]
+        lib.attn_debug_drop_load.restype = _I
         lib.attn_get_device_status.argtypes = [_P]
         lib.attn_get_device_status.restype = _I
         lib.attn_status_string.argtypes = [_I]
@@ -301,6 +304,10 @@ def attn_get_timeout_info(stream=None):
 
 def attn_selftest_wait_timeout(timeout_us: int, stream=None) -> int:
     return load().attn_selftest_wait_timeout(timeout_us, stream)
+
+
+def attn_debug_drop_load(kernel: int, load_index: int, limit_us: int) -> int:
+    return load().attn_debug_drop_load(kernel, load_index, limit_us)
 
 
 # ------------------------------------------------------------ torch marshalling

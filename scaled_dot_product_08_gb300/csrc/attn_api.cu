@@ -41,6 +41,21 @@ unsigned long long wait_limit_ns() {
   return lim;
 }
 
+// The dropped-load test hook (attn_debug_drop_load): armed for one launch of
+// one kernel, then cleared.  kernel: 0 forward, 1 dQ, 2 dK/dV.
+std::mutex g_debug_mu;
+int g_debug_kernel = -1, g_debug_drop1 = 0;
+unsigned long long g_debug_limit_ns = 0;
+
+// Applies (and clears) the hook when it is armed for `kernel`.
+void take_debug(int kernel, int* drop1, unsigned long long* limit_ns) {
+  std::lock_guard<std::mutex> lk(g_debug_mu);
+  if (g_debug_kernel != kernel) return;
+  *drop1 = g_debug_drop1;
+  *limit_ns = g_debug_limit_ns;
+  g_debug_kernel = -1;
+}
+
 // Written by kernels when a bounded wait gives up (0 = fine), and where the
 // first such timeout happened.
 __device__ int g_status_word;
@@ -292,6 +307,7 @@ static attn_status_t fwd_common(const void* q, const void* k, const void* v, voi
   p.status = di->status;
   p.limit_ns = wait_limit_ns();
   p.info = di->info;
+  take_debug(0, &p.debug_drop1, &p.limit_ns);
   cudaError_t e = sdpa::launch_fwd(d, causal != 0, tq, tk, tv, to, p, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return ATTN_ERR_LAUNCH;
   return ATTN_OK;
@@ -427,6 +443,7 @@ static attn_status_t bwd_grad_x(const void* q, const void* k, const void* v, con
   bwd_params(&p, workspace, B, H, Hkv, Nq, Nk, d, scale, causal, di);
   p.dk = static_cast<uint16_t*>(dk);
   p.dv = static_cast<uint16_t*>(dv);
+  take_debug(2, &p.debug_drop1, &p.limit_ns);
   cudaError_t e = sdpa::launch_bwd_grad(d, causal != 0, tq, tk, tv, tdo, tdk, tdv, p,
                                         static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;
@@ -449,6 +466,7 @@ static attn_status_t bwd_dq_x(const void* q, const void* k, const void* v, const
   sdpa::BwdParams p;
   bwd_params(&p, workspace, B, H, Hkv, Nq, Nk, d, scale, causal, di);
   p.dq = static_cast<uint16_t*>(dq);
+  take_debug(1, &p.debug_drop1, &p.limit_ns);
   cudaError_t e =
       sdpa::launch_bwd_dq(d, causal != 0, tq, tk, tv, tdo, tdq, tq, p, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;
@@ -475,6 +493,7 @@ static attn_status_t bwd_dq_rows_x(const void* q, const void* k, const void* v, 
   p.dq = static_cast<uint16_t*>(dq);
   p.lse = lse;
   p.rows_in_dq = 1;
+  take_debug(1, &p.debug_drop1, &p.limit_ns);
   cudaError_t e = sdpa::launch_bwd_dq(d, causal != 0, tq, tk, tv, tdo, tdq, to, p, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;
 }
@@ -1097,6 +1116,16 @@ attn_status_t attn_selftest_wait_timeout(unsigned int timeout_us, void* stream) 
   selftest_wait_kernel<<<1, 64, 0, static_cast<cudaStream_t>(stream)>>>(di->status, di->info,
                                                                          (unsigned long long)timeout_us * 1000ull);
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;
+}
+
+attn_status_t attn_debug_drop_load(int kernel, int load_index, unsigned int limit_us) {
+  if (kernel < 0 || kernel > 2 || load_index < 0 || load_index > (1 << 20)) return ATTN_ERR_INVALID_ARG;
+  if (limit_us < 1000u || limit_us > 60000000u) return ATTN_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> lk(g_debug_mu);
+  g_debug_kernel = kernel;
+  g_debug_drop1 = load_index + 1;
+  g_debug_limit_ns = (unsigned long long)limit_us * 1000ull;
+  return ATTN_OK;
 }
 
 }  // extern "C"

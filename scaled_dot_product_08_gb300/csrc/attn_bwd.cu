@@ -486,6 +486,8 @@ __global__ void __launch_bounds__(384, 1)
           const int bh = b * p.H + h;
           const int qplane = varlen ? h : bh;
           if (rd > 0 && !wait_bounded(wc, bQe + 8u * st, (rd - 1) & 1, wait_site(0x31, it))) break;
+          issued = it + 1;
+          if (p.debug_drop1 == it + 1 && blockIdx.x == 0) continue;  // test of the bounded waits only
           const uint32_t barq = bQf + 8u * st;
           mbar_expect_tx(barq, T::TILE_BYTES + T::VEC_BYTES);
           for (int cb = 0; cb < T::NB; ++cb)
@@ -493,7 +495,6 @@ __global__ void __launch_bounds__(384, 1)
           const size_t voff = (varlen ? (size_t)h * p.vec_stride + vseq : (size_t)bh * p.Npad) + (size_t)i * 128;
           bulk_load(sVec + st * T::VEC_BYTES, p.lse2 + voff, 512, barq);
           bulk_load(sVec + st * T::VEC_BYTES + 512, p.dvec + voff, 512, barq);
-          issued = it + 1;
         }
         // Every copy issued above has landed before the CTA may exit.
         wait_drain(bKV, 0, p.limit_ns);

@@ -487,16 +487,21 @@ __global__ void __launch_bounds__(384, 1)
           const int ks = j % T::KS, kr = j / T::KS, vs = j % T::VS, vr = j / T::VS;
           if (kr > 0 && !wait_bounded(wc, bKe + 8u * ks, (kr - 1) & 1, wait_site(0x91, j))) break;
           if (o_issued && j == 2 && !wait_bounded(wc, bOc, 0, wait_site(0x93, j))) break;
-          mbar_expect_tx(bKf + 8u * ks, T::TILE_BYTES);
-          for (int cb = 0; cb < T::NB; ++cb)
-            tma_load_3d(sK + ks * T::TILE_BYTES + cb * T::BLOCK_BYTES, &tmK, bKf + 8u * ks, cb * 64,
-                        k0 + tile_at(j) * 128, kplane);
+          // (p.debug_drop1: a test of the bounded waits skips one load in CTA 0)
+          if (!(p.debug_drop1 == 2 * j + 1 && blockIdx.x == 0)) {
+            mbar_expect_tx(bKf + 8u * ks, T::TILE_BYTES);
+            for (int cb = 0; cb < T::NB; ++cb)
+              tma_load_3d(sK + ks * T::TILE_BYTES + cb * T::BLOCK_BYTES, &tmK, bKf + 8u * ks, cb * 64,
+                          k0 + tile_at(j) * 128, kplane);
+          }
           issued = 2 * j + 1;
           if (vr > 0 && !wait_bounded(wc, bVe + 8u * vs, (vr - 1) & 1, wait_site(0x92, j))) break;
-          mbar_expect_tx(bVf + 8u * vs, T::TILE_BYTES);
-          for (int cb = 0; cb < T::NB; ++cb)
-            tma_load_3d(sV + vs * T::TILE_BYTES + cb * T::BLOCK_BYTES, &tmV, bVf + 8u * vs, cb * 64,
-                        k0 + tile_at(j) * 128, kplane);
+          if (!(p.debug_drop1 == 2 * j + 2 && blockIdx.x == 0)) {
+            mbar_expect_tx(bVf + 8u * vs, T::TILE_BYTES);
+            for (int cb = 0; cb < T::NB; ++cb)
+              tma_load_3d(sV + vs * T::TILE_BYTES + cb * T::BLOCK_BYTES, &tmV, bVf + 8u * vs, cb * 64,
+                          k0 + tile_at(j) * 128, kplane);
+          }
           issued = 2 * j + 2;
         }
         // Every copy issued above has landed before the CTA may exit.

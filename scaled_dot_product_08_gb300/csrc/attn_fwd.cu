@@ -502,6 +502,10 @@ __global__ void __launch_bounds__(384, 1)
           for (int w = 0; w < 2; ++w) {
             const int st = t % T::NSTAGE, rd = t / T::NSTAGE;
             if (rd > 0 && !(ok = wait_bounded(wc, bKVe + 8u * st, (rd - 1) & 1, wait_site(0x61, t)))) break;
+            if (p.debug_drop1 == t + 1 && blockIdx.x == 0) {  // test of the bounded waits only
+              ++t;
+              continue;
+            }
             mbar_expect_tx(bKVf + 8u * st, T::TILE_BYTES);
             const CUtensorMap* m = (w == 0) ? &tmK : &tmV;
             for (int c = 0; c < T::NB; ++c)

@@ -70,6 +70,7 @@ struct FwdParams {
   uint16_t* o;           // varlen: O base, for the rows of a sequence's last tile; FP8: O base
   MaskArgs mk;           // masked instances only
   float o_scale;         // FP8: V's dequantisation factor, applied to O
+  int debug_drop1;       // 0; n > 0 only in a test of the bounded waits: CTA 0's producer skips ring load n - 1
 };
 
 // Backward arguments.
@@ -95,6 +96,7 @@ struct BwdParams {
   uint16_t* dk;
   uint16_t* dv;
   MaskArgs mk;           // masked instances only
+  int debug_drop1;       // 0; n > 0 only in a test of the bounded waits: CTA 0's producer skips ring load n - 1
 };
 
 // Decode (split over the keys) arguments.

@@ -110,6 +110,16 @@ def test_bwd_noalloc_checks_arguments_before_its_scratch(lib):
     assert sdpa.attn_bwd_noalloc(*bad, 1, 2, 2, 64, 64, 0.1, 0, None) == sdpa.Status.INVALID_ARG
 
 
+def test_debug_drop_load_checks_its_arguments(lib):
+    # The failure-path test hook arms nothing on bad arguments (host only).
+    import scaled_dot_product_08_gb300 as sdpa
+    assert sdpa.attn_debug_drop_load(3, 0, 20000) == sdpa.Status.INVALID_ARG
+    assert sdpa.attn_debug_drop_load(-1, 0, 20000) == sdpa.Status.INVALID_ARG
+    assert sdpa.attn_debug_drop_load(0, -1, 20000) == sdpa.Status.INVALID_ARG
+    assert sdpa.attn_debug_drop_load(0, 0, 999) == sdpa.Status.INVALID_ARG
+    assert sdpa.attn_debug_drop_load(0, 0, 60000001) == sdpa.Status.INVALID_ARG
+
+
 def _decode_chunks(B, Hkv, Nk):
     # The documented chunk plan: whole 128-key tiles, about 1216 CTAs in all
     # (ceil(1216 / (B * Hkv)) chunks while tiles last).

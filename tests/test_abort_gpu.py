@@ -1,0 +1,79 @@
+"""The production kernels' failure path, without a GPU fault.
+
+attn_debug_drop_load arms one launch: the first CTA's TMA producer skips one
+ring load and every on-chip wait is limited to 20 ms.  The consumers of that
+load must give up, record ATTN_ERR_TIMEOUT with the CTA and the wait site,
+and every role of the CTA must stop and exit (each named barrier is reached
+whatever a wait returned), so that the launch ends and the context stays
+usable.  The CTAs that lost nothing complete normally, and the next normal
+call is correct.  One case per kernel: forward, dQ, dK/dV.
+"""
+import math
+
+import numpy as np
+import pytest
+
+import oracle
+from sdpa_inputs import make_random
+from tests.parity import check_grads, check_o_lse, dev, host
+
+pytestmark = pytest.mark.gpu
+
+LIMIT_US = 20000
+FWD_SITES = {0x51, 0x52, 0x53, 0x54, 0x61, 0x71, 0x72, 0x73, 0x74, 0x75, 0x76, 0x77, 0x78, 0x79, 0x7a}
+DQ_SITES = {0x81, 0x82, 0x83, 0x84, 0x85, 0x91, 0x92, 0x93} | set(range(0xa1, 0xa9))
+GRAD_SITES = {0x11, 0x12, 0x13, 0x14, 0x31, 0x32} | set(range(0x41, 0x48))
+
+
+def _inputs(B, H, N, d, seed):
+    return [make_random((B, H, N, d), seed + i) for i in range(4)]
+
+
+def _expect_timeout_in_cta0(lib, sites):
+    import torch
+    torch.cuda.synchronize()
+    st, info = lib.attn_get_timeout_info(None)
+    assert st == lib.Status.OK
+    assert lib.attn_get_device_status(None) == lib.Status.TIMEOUT
+    assert lib.attn_get_device_status(None) == lib.Status.OK  # cleared by the read
+    site = info[0] >> 16
+    assert site in sites, hex(site)
+    assert info[1] == 0  # the CTA whose load was dropped
+    assert info[3] >= LIMIT_US * 0.9
+
+
+def test_forward_dropped_load_times_out_and_recovers(cuda_lib):
+    B, H, N, d = 1, 2, 512, 128
+    q, k, v, _ = _inputs(B, H, N, d, 61000)
+    s = 1 / math.sqrt(d)
+    assert cuda_lib.attn_get_device_status(None) == cuda_lib.Status.OK
+    # CTA 0 = head 0, query tiles 2 and 3 (four key tiles, eight ring loads): drop K_1
+    assert cuda_lib.attn_debug_drop_load(0, 2, LIMIT_US) == cuda_lib.Status.OK
+    O, lse = cuda_lib.forward(dev(q), dev(k), dev(v), s, True)
+    _expect_timeout_in_cta0(cuda_lib, FWD_SITES)
+    O_ref, lse_ref = oracle.attention_forward(q, k, v, s, True)
+    O, lse = host(O), host(lse)
+    # the other CTAs (head 0 rows 0..255, all of head 1) completed normally
+    check_o_lse(O[:, 1], lse[:, 1], O_ref[:, 1], lse_ref[:, 1], "head 1 beside the dropped load")
+    check_o_lse(O[:, 0, :256], lse[:, 0, :256], O_ref[:, 0, :256], lse_ref[:, 0, :256], "head 0, first CTA")
+    # the next call is whole and correct
+    O, lse = cuda_lib.forward(dev(q), dev(k), dev(v), s, True)
+    check_o_lse(host(O), host(lse), O_ref, lse_ref, "after the timeout")
+    assert cuda_lib.attn_get_device_status(None) == cuda_lib.Status.OK
+
+
+@pytest.mark.parametrize("kernel,load,sites", [(1, 3, DQ_SITES), (2, 1, GRAD_SITES)], ids=["dq_V1", "dkdv_Q1"])
+def test_backward_dropped_load_times_out_and_recovers(cuda_lib, kernel, load, sites):
+    B, H, N, d = 1, 2, 512, 128
+    q, k, v, do = _inputs(B, H, N, d, 62000 + kernel)
+    s = 1 / math.sqrt(d)
+    tq, tk, tv, tdo = dev(q), dev(k), dev(v), dev(do)
+    O, lse = cuda_lib.forward(tq, tk, tv, s, True)
+    assert cuda_lib.attn_get_device_status(None) == cuda_lib.Status.OK
+    # dQ: CTA 0 = head 0, query tile 3, drop V_1; dK/dV: CTA 0 = head 0, key tile 0, drop Q_1
+    assert cuda_lib.attn_debug_drop_load(kernel, load, LIMIT_US) == cuda_lib.Status.OK
+    cuda_lib.backward(tq, tk, tv, O, lse, tdo, s, True)
+    _expect_timeout_in_cta0(cuda_lib, sites)
+    grads = [host(g) for g in cuda_lib.backward(tq, tk, tv, O, lse, tdo, s, True)]
+    check_grads(grads, oracle.attention_backward(q, k, v, do, s, True), "after the timeout")
+    assert cuda_lib.attn_get_device_status(None) == cuda_lib.Status.OK
