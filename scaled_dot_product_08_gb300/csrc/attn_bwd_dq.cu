@@ -521,8 +521,7 @@ __global__ void __launch_bounds__(384, 1)
     } else if (warp == 9) {
       // ------------------------------------------------------------ MMA issuer
       // Per step j: dP_{j+1} (once dP_j has been read), dQ += dS_j K_j,
-      // S_{j+2} into the S buffer dS_j occupied (MMAs from one thread run in
-      // order, so dQ has read dS_j first).
+      // S_{j+2} into the S buffer dS_j occupied.
       {
         const uint32_t leader = elect_one();
         constexpr uint32_t I_SS = idesc_bf16_f32(128, 128, false, false);  // S, dP (K-major x K-major)
@@ -543,6 +542,11 @@ __global__ void __launch_bounds__(384, 1)
         auto wait_all = [&](uint32_t bar, uint32_t parity, int site) {
           return __all_sync(0xffffffffu, wait_bounded(wc, bar, parity, site));
         };
+        // Each group's barrier checks run right after the previous group's
+        // MMAs are issued and before that group's commit: the commit returns
+        // only once its MMAs have nearly drained, so a check placed after it
+        // would leave the tensor pipe idle for its length.  No check waits on
+        // a signal that the commit it precedes would give.
         bool ok = wait_all(bQ, 0, wait_site(0xa1, 0)) && wait_all(bKf, 0, wait_site(0xa2, 0)) &&
                   wait_all(bVf, 0, wait_site(0xa3, 0));
         if (ok) {
@@ -550,28 +554,33 @@ __global__ void __launch_bounds__(384, 1)
           mma_kk(tmem, dQk, dKk0, I_SS);  // S_0
           mma_commit_p(leader, bS);
           mma_kk(tdP, dOk, dVk0, I_SS);  // dP_0
+          if (n > 1) ok = wait_all(bKf + 8u, 0, wait_site(0xa4, 1));  // for S_1
           mma_commit_p(leader, bDp);
           mma_commit_p(leader, bVe);  // V_0 consumed
-          if (n > 1) {
-            ok = wait_all(bKf + 8u, 0, wait_site(0xa4, 1));
-            if (ok) {
-              tc_fence_after();
-              mma_kk(tmem + 128, dQk, sdesc_add(dKk0, T::TILE_BYTES), I_SS);  // S_1
-              mma_commit_p(leader, bS + 8u);
-            }
+          if (ok && n > 1) {
+            tc_fence_after();
+            mma_kk(tmem + 128, dQk, sdesc_add(dKk0, T::TILE_BYTES), I_SS);  // S_1
+            // for dP_1: V_1 loaded, dP_0 read
+            ok = wait_all(bVf + 8u * (1 % T::VS), (1 / T::VS) & 1, wait_site(0xa5, 0)) &&
+                 wait_all(bDpc, 0, wait_site(0xa6, 0));
+            mma_commit_p(leader, bS + 8u);
           }
         }
         for (int j = 0; j < n && ok; ++j) {
+          // dP_{j+1} (its conditions were checked during the previous group),
+          // then dQ += dS_j K_j, then S_{j+2} into the S buffer dS_j occupied
+          // (MMAs from one thread run in order, so dQ has read dS_j first).
           if (j + 1 < n) {
             const int vs = (j + 1) % T::VS;
-            if (!(ok = wait_all(bVf + 8u * vs, ((j + 1) / T::VS) & 1, wait_site(0xa5, j)))) break;
-            if (!(ok = wait_all(bDpc, j & 1, wait_site(0xa6, j)))) break;
             tc_fence_after();
             mma_kk(tdP, dOk, sdesc_add(dVk0, vs * T::TILE_BYTES), I_SS);  // dP_{j+1}
+            ok = wait_all(bDs, j & 1, wait_site(0xa7, j));               // for dQ_j
             mma_commit_p(leader, bDp);
             mma_commit_p(leader, bVe + 8u * vs);
+          } else {
+            ok = wait_all(bDs, j & 1, wait_site(0xa7, j));
           }
-          if (!(ok = wait_all(bDs, j & 1, wait_site(0xa7, j)))) break;
+          if (!ok) break;
           tc_fence_after();
           // dQ += dS_j K_j: A = dS in TMEM (keys 64X.. of warpgroup X at
           // columns 64X.., bf16 pairs), B = K_j (MN-major, N = d)
@@ -581,12 +590,16 @@ __global__ void __launch_bounds__(384, 1)
           for (int kk = 0; kk < 8; ++kk)
             mma_ts_p(leader, tdQ, tS + 64 * (kk >> 2) + (kk & 3) * 8,
                      sdesc_add(dKmn0, ks * T::TILE_BYTES + kk * 2048), I_DQ, (j > 0 || kk > 0) ? 1u : 0u);
+          const int k2 = (j + 2) % T::KS;
+          if (j + 2 < n) ok = wait_all(bKf + 8u * k2, ((j + 2) / T::KS) & 1, wait_site(0xa8, j));  // for S_{j+2}
           mma_commit_p(leader, bKe + 8u * ks);  // K_j consumed
+          if (!ok) break;
           if (j + 2 < n) {
-            const int k2 = (j + 2) % T::KS;
-            if (!(ok = wait_all(bKf + 8u * k2, ((j + 2) / T::KS) & 1, wait_site(0xa8, j)))) break;
             tc_fence_after();
             mma_kk(tS, dQk, sdesc_add(dKk0, k2 * T::TILE_BYTES), I_SS);  // S_{j+2}
+            // for dP_{j+2}: V_{j+2} loaded, dP_{j+1} read
+            ok = wait_all(bVf + 8u * ((j + 2) % T::VS), ((j + 2) / T::VS) & 1, wait_site(0xa5, j + 1)) &&
+                 wait_all(bDpc, (j + 1) & 1, wait_site(0xa6, j + 1));
             mma_commit_p(leader, bS + 8u * (j & 1));
           }
         }
