@@ -99,3 +99,118 @@ def backward_head(task):
         out[name + "_r2"] = r2
         out[name + "_head"] = math.sqrt(e2 / r2) if r2 > 0 else math.sqrt(e2)
     return out
+
+
+def _grad_errors(out, grads, ref):
+    """Adds, per gradient, the sums of squared errors and squared reference
+    values and the unit's own relative Frobenius error to ``out``."""
+    for name, g, r in zip(("dq", "dk", "dv"), grads, ref):
+        g = np.asarray(g, np.float64)
+        r = np.asarray(r, np.float64)
+        e2 = float(((g - r) ** 2).sum())
+        r2 = float((r ** 2).sum())
+        out[name + "_finite"] = bool(np.all(np.isfinite(g)))
+        out[name + "_e2"] = e2
+        out[name + "_r2"] = r2
+        out[name + "_head"] = math.sqrt(e2 / r2) if r2 > 0 else math.sqrt(e2)
+    return out
+
+
+def _o_lse_errors(O, lse, O_ref, lse_ref, head):
+    """Forward error sums of one unit; rows that see no key must be exactly
+    O = 0, lse = -inf."""
+    O = np.asarray(O, np.float64)
+    lse = np.asarray(lse, np.float64)
+    live = np.isfinite(lse_ref)
+    err = np.abs(O - O_ref)
+    lerr = np.abs(lse[live] - lse_ref[live]) if live.any() else np.zeros(1)
+    at = np.unravel_index(int(np.argmax(err)), err.shape)
+    return {
+        "finite": bool(np.all(np.isfinite(O)) and np.all(np.isfinite(lse[live]))),
+        "dead_ok": bool(np.all(O[~live] == 0) and np.all(np.isneginf(lse[~live]))),
+        "pad_zero": True,
+        "o_max": float(err.max()),
+        "o_sum": float(err.sum()),
+        "o_n": int(err.size),
+        "lse_max": float(lerr.max()),
+        "head": head,
+        "o_max_at": (int(at[0]), int(at[1]), float(O[at]), float(O_ref[at])),
+    }
+
+
+def cross_head(task):
+    """Nq queries against Nk keys of one head (causal: query row i at
+    position Nk - Nq + i), forward and, when dO is given, backward.
+    task: (q, k, v, do or None, O, lse, dq, dk, dv (or None), scale, causal, head)."""
+    q, k, v, do, O, lse, dq, dk, dv, scale, causal, head = task
+    one = lambda a: np.asarray(a[None, None], dtype=np.float64)
+    off = k.shape[0] - q.shape[0] if causal else 0
+    O_ref, lse_ref = oracle.attention_forward(one(q), one(k), one(v), scale, causal, q_offset=off)
+    out = _o_lse_errors(O, lse, O_ref[0, 0], lse_ref[0, 0], head)
+    if do is not None:
+        ref = oracle.attention_backward(one(q), one(k), one(v), one(do), scale, causal, q_offset=off)
+        _grad_errors(out, (dq, dk, dv), [r[0, 0] for r in ref])
+    return out
+
+
+def masked_head(task):
+    """One head under a mask built here from its recipe: ("prefix", p) a
+    prefix-LM boolean mask, ("distance", slope) the additive bias
+    -slope * |i - j|; forward and, when dO is given, backward.
+    task: (q, k, v, do or None, O, lse, dq, dk, dv (or None), scale, causal, recipe, head)."""
+    from sdpa_inputs import distance_bias, prefix_lm_mask
+    q, k, v, do, O, lse, dq, dk, dv, scale, causal, recipe, head = task
+    one = lambda a: np.asarray(a[None, None], dtype=np.float64)
+    N = q.shape[0]
+    mask = prefix_lm_mask(N, recipe[1]) if recipe[0] == "prefix" else None
+    bias = distance_bias(N, recipe[1]) if recipe[0] == "distance" else None
+    O_ref, lse_ref = oracle.attention_masked_forward(one(q), one(k), one(v), scale, causal, None, None, mask, bias)
+    out = _o_lse_errors(O, lse, O_ref[0, 0], lse_ref[0, 0], head)
+    if do is not None:
+        ref = oracle.attention_masked_backward(one(q), one(k), one(v), one(do), scale, causal, None, None, mask,
+                                               bias)
+        _grad_errors(out, (dq, dk, dv), [r[0, 0] for r in ref])
+    return out
+
+
+def window_head(task):
+    """One head of a causal sliding window of wl keys to the left, every
+    query row, in blocks of 128 rows against the keys their windows reach
+    (the masked oracle aligns block row r0 + i at key position r0 + i).
+    task: (q (N, d), k, v, O, lse, scale, wl, head)."""
+    q, k, v, O, lse, scale, wl, head = task
+    N = q.shape[0]
+    O_ref = np.zeros((N, v.shape[1]))
+    lse_ref = np.zeros(N)
+    for r0 in range(0, N, 128):
+        r1 = min(N, r0 + 128)
+        k0 = max(0, r0 - wl)
+        blk = lambda a, a0, a1: np.asarray(a[None, None, a0:a1], dtype=np.float64)
+        Ob, lb = oracle.attention_masked_forward(blk(q, r0, r1), blk(k, k0, r1), blk(v, k0, r1), scale, True,
+                                                 (wl, -1))
+        O_ref[r0:r1] = Ob[0, 0]
+        lse_ref[r0:r1] = lb[0, 0]
+    return _o_lse_errors(O, lse, O_ref, lse_ref, head)
+
+
+def fp8_head(task):
+    """One head of the FP8 forward on its dequantised e4m3 inputs: errors
+    against the exact oracle and against the model of the kernel's one
+    added rounding (tests/fp8_model.py).
+    task: (q, k, v (dequantised, (N, d)), O, lse, scale, causal, q_offset, head)."""
+    from tests.fp8_model import p_rounding_model
+    q, k, v, O, lse, scale, causal, off, head = task
+    one = lambda a: np.asarray(a[None, None], dtype=np.float64)
+    O_ref, lse_ref = oracle.attention_forward(one(q), one(k), one(v), scale, causal, q_offset=off)
+    O_ref, lse_ref = O_ref[0, 0], lse_ref[0, 0]
+    O_m = p_rounding_model(q, k, v, scale, causal, off)
+    O = np.asarray(O, np.float64)
+    return {
+        "head": head,
+        "finite": bool(np.all(np.isfinite(O)) and np.all(np.isfinite(lse))),
+        "rel_fro": float(np.linalg.norm(O - O_ref) / np.linalg.norm(O_ref)),
+        "rel_fro_model": float(np.linalg.norm(O - O_m) / np.linalg.norm(O_m)),
+        "o_sum": float(np.abs(O - O_ref).sum()),
+        "o_n": int(O.size),
+        "lse_max": float(np.abs(np.asarray(lse, np.float64) - lse_ref).max()),
+    }

@@ -35,3 +35,35 @@ def test_pool_error_sums_equal_a_direct_comparison():
         assert p["o_max"] == fp["o_max"] and p["pad_zero"]
         for g in ("dq", "dk", "dv"):
             assert p[g + "_head"] < 1e-6  # float32 rounding of the oracle's own values
+
+
+def test_workers_report_zero_error_on_the_oracles_own_outputs():
+    # Each worker of the full-size tests, fed the oracle's own results as the
+    # outputs under test, reports no error; a planted error is found.
+    from sdpa_inputs import distance_bias, prefix_lm_mask, e4m3_decode, quantize_e4m3
+    from tests.oracle_pool import cross_head, fp8_head, masked_head, window_head
+    s = 0.25
+    q, k, v, do = (make_random((1, 1, n, 16), 950 + i)[0, 0] for i, n in enumerate((40, 70, 70, 40)))
+    one = lambda a: a[None, None]
+    O, lse = oracle.attention_forward(one(q), one(k), one(v), s, True, q_offset=30)
+    g = oracle.attention_backward(one(q), one(k), one(v), one(do), s, True, q_offset=30)
+    p = cross_head((q, k, v, do, O[0, 0], lse[0, 0], g[0][0, 0], g[1][0, 0], g[2][0, 0], s, True, "x"))
+    assert p["o_max"] < 1e-12 and p["lse_max"] < 1e-12 and p["dq_head"] < 1e-12 and p["dead_ok"]
+    O2 = O[0, 0].copy()
+    O2[5, 3] += 0.5
+    assert abs(cross_head((q, k, v, None, O2, lse[0, 0], None, None, None, s, True, "x"))["o_max"] - 0.5) < 1e-9
+    q, k, v, do = (make_random((1, 1, 90, 16), 960 + i)[0, 0] for i in range(4))
+    for recipe, mask, bias in ((("prefix", 20), prefix_lm_mask(90, 20), None),
+                               (("distance", 0.1), None, distance_bias(90, 0.1))):
+        O, lse = oracle.attention_masked_forward(one(q), one(k), one(v), s, False, None, None, mask, bias)
+        g = oracle.attention_masked_backward(one(q), one(k), one(v), one(do), s, False, None, None, mask, bias)
+        p = masked_head((q, k, v, do, O[0, 0], lse[0, 0], g[0][0, 0], g[1][0, 0], g[2][0, 0], s, False, recipe, 1))
+        assert p["o_max"] < 1e-12 and p["dv_head"] < 1e-12
+    q, k, v = (make_random((1, 1, 300, 16), 970 + i)[0, 0] for i in range(3))
+    O, lse = oracle.attention_masked_forward(one(q), one(k), one(v), s, True, (50, -1))
+    p = window_head((q, k, v, O[0, 0], lse[0, 0], s, 50, 2))
+    assert p["o_max"] < 1e-12 and p["lse_max"] < 1e-12
+    qd, kd, vd = (e4m3_decode(b) * sc for b, sc in (quantize_e4m3(make_random((200, 32), 980 + i)) for i in range(3)))
+    O, lse = oracle.attention_forward(one(qd), one(kd), one(vd), s, True)
+    p = fp8_head((qd, kd, vd, O[0, 0], lse[0, 0], s, True, 0, 3))
+    assert p["rel_fro"] < 1e-12 and 1e-4 < p["rel_fro_model"] < 0.1
