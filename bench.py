@@ -67,7 +67,7 @@ def workload_desc(w):
     if w.kind == "masked":
         what = (f"sliding window (left {w.window[0]}, right {w.window[1]})" if w.window is not None
                 else f"prefix-LM boolean mask (prefix {w.prefix})" if w.prefix is not None
-                else f"additive float32 mask -{w.bias_slope:g}*|i-j| shared by all heads")
+                else f"additive {'bf16' if w.bias_bf16 else 'float32'} mask -{w.bias_slope:g}*|i-j| shared by all heads")
         return (f"{w.name}: B={w.B} H={w.H} Hkv={w.Hkv} N={w.N} d={w.d} {'causal ' if w.causal else ''}{what} "
                 f"{'fwd+bwd' if w.with_grad else 'fwd'}; FLOPs count the visible (query, key) pairs")
     if w.kind == "varlen":
@@ -219,9 +219,9 @@ def _oracle_head_seconds(w, x):
     import oracle
     q, k, v, do = x
     if w.kind == "masked":
-        from sdpa_inputs import distance_bias, prefix_lm_mask
+        from sdpa_inputs import prefix_lm_mask, workload_bias
         mask = prefix_lm_mask(w.N, w.prefix) if w.prefix is not None else None
-        bias = distance_bias(w.N, w.bias_slope) if w.bias_slope is not None else None
+        bias = workload_bias(w)
         t0 = time.perf_counter()
         oracle.attention_masked_forward(q, k, v, w.softmax_scale, w.causal, w.window, None, mask, bias)
         if w.with_grad:
@@ -439,12 +439,14 @@ def run_ours(args, w, rank, world, local_rank):
         fp8 = [quantize_e4m3(x[n]) for n in ("q", "k", "v")]  # (bytes, scale) each
     mask_spec = None
     if w.kind == "masked":
-        from sdpa_inputs import distance_bias, prefix_lm_mask
+        from sdpa_inputs import prefix_lm_mask, workload_bias
         mask_t = bias_t = None
         if w.prefix is not None:
             mask_t = torch.from_numpy(prefix_lm_mask(N, w.prefix).astype("uint8")).cuda()
         if w.bias_slope is not None:
-            bias_t = torch.from_numpy(distance_bias(N, w.bias_slope)).cuda()
+            bias_t = torch.from_numpy(workload_bias(w)).cuda()
+            if w.bias_bf16:
+                bias_t = bias_t.to(torch.bfloat16)  # exact: the values are bf16 already
         mask_spec = sdpa.make_mask(w.window, None, mask_t, B, H, bias_t)
         mws_f = sdpa.attn_masked_workspace_size(B, H, Hkv, Nq, N, d, mask_spec, 0)
         mws_b = sdpa.attn_masked_workspace_size(B, H, Hkv, Nq, N, d, mask_spec, 1)

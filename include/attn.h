@@ -266,9 +266,13 @@ attn_status_t attn_fwd_fp8(const void* q, const void* k, const void* v, void* o,
  *   key_lengths  DEVICE int32 (B), 4-byte aligned, or NULL
  *   mask         DEVICE bytes (mask_batch, mask_heads, Nq, Nk), dense
  *                row-major, any alignment, or NULL
- *   bias         DEVICE float32 (bias_batch, bias_heads, Nq, Nk), dense
- *                row-major, 4-byte aligned, or NULL (bias_batch and
- *                bias_heads are then ignored)
+ *   bias         DEVICE float32 (bias_bf16 == 0) or bf16 (bias_bf16 == 1)
+ *                (bias_batch, bias_heads, Nq, Nk), dense row-major, aligned
+ *                to its element size, or NULL (bias_batch, bias_heads and
+ *                bias_bf16 are then ignored).  A bf16 bias is SDPA's float
+ *                attn_mask in the query's dtype: half the bytes to read,
+ *                the same arithmetic on the values it holds.  Any other
+ *                bias_bf16 value gives ATTN_ERR_INVALID_ARG.
  */
 typedef struct {
   int window_left;
@@ -277,9 +281,10 @@ typedef struct {
   const unsigned char* mask;
   int mask_batch;   /* 1 or B */
   int mask_heads;   /* 1 or H */
-  const float* bias;
+  const void* bias; /* float32, or bf16 when bias_bf16 */
   int bias_batch;   /* 1 or B */
   int bias_heads;   /* 1 or H */
+  int bias_bf16;    /* 0: float32 bias, 1: bf16 bias */
 } attn_mask_t;
 
 /*
@@ -437,7 +442,7 @@ attn_status_t attn_get_timeout_info(int info[4], void* stream);
 /* Human-readable name of a status code (static storage; never NULL). */
 const char* attn_status_string(attn_status_t s);
 
-/* ABI version of this header (incremented on incompatible changes). */
+/* ABI version of this header (incremented on incompatible changes; 3: attn_mask_t.bias_bf16). */
 int attn_abi_version(void);
 
 /*

@@ -51,7 +51,8 @@ class AttnMask(ctypes.Structure):
     _fields_ = [("window_left", ctypes.c_int), ("window_right", ctypes.c_int),
                 ("key_lengths", ctypes.c_void_p), ("mask", ctypes.c_void_p),
                 ("mask_batch", ctypes.c_int), ("mask_heads", ctypes.c_int),
-                ("bias", ctypes.c_void_p), ("bias_batch", ctypes.c_int), ("bias_heads", ctypes.c_int)]
+                ("bias", ctypes.c_void_p), ("bias_batch", ctypes.c_int), ("bias_heads", ctypes.c_int),
+                ("bias_bf16", ctypes.c_int)]
 
 
 class AttnError(RuntimeError):
@@ -522,12 +523,12 @@ def backward_varlen(q, k, v, o, lse, dout, cu_seqlens_q, cu_seqlens_k, max_seqle
 def make_mask(window=None, key_lengths=None, mask=None, B=1, H=1, bias=None) -> AttnMask:
     """AttnMask from Python values: window (left, right) with -1 for an open
     side, key_lengths an int32 CUDA vector (B,), mask a bool / uint8 CUDA
-    tensor (1 or B, 1 or H, Nq, Nk), bias a float32 CUDA tensor of the same
+    tensor (1 or B, 1 or H, Nq, Nk), bias a float32 or bfloat16 CUDA tensor of the same
     broadcasting shape added to the scaled scores (finite or -inf).  The
     tensors must stay alive while the calls that use the AttnMask run."""
     import torch
     wl, wr = window if window is not None else (-1, -1)
-    m = AttnMask(int(wl), int(wr), 0, 0, 1, 1, 0, 1, 1)
+    m = AttnMask(int(wl), int(wr), 0, 0, 1, 1, 0, 1, 1, 0)
     if key_lengths is not None:
         if key_lengths.dtype != torch.int32 or not key_lengths.is_cuda or not key_lengths.is_contiguous():
             raise ValueError("key_lengths must be a contiguous int32 CUDA vector")
@@ -540,9 +541,11 @@ def make_mask(window=None, key_lengths=None, mask=None, B=1, H=1, bias=None) -> 
         m.mask = mask.data_ptr()
         m.mask_batch, m.mask_heads = int(mask.shape[0]), int(mask.shape[1])
     if bias is not None:
-        if bias.dim() != 4 or bias.dtype != torch.float32 or not bias.is_cuda or not bias.is_contiguous():
-            raise ValueError("bias must be a contiguous 4-D float32 CUDA tensor")
+        if (bias.dim() != 4 or bias.dtype not in (torch.float32, torch.bfloat16) or not bias.is_cuda
+                or not bias.is_contiguous()):
+            raise ValueError("bias must be a contiguous 4-D float32 or bfloat16 CUDA tensor")
         m.bias = bias.data_ptr()
+        m.bias_bf16 = int(bias.dtype == torch.bfloat16)
         m.bias_batch, m.bias_heads = int(bias.shape[0]), int(bias.shape[1])
     return m
 

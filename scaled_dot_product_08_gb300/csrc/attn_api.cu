@@ -257,7 +257,7 @@ __global__ void selftest_wait_kernel(int* status, int* info, unsigned long long 
 
 extern "C" {
 
-int attn_abi_version(void) { return 2; }
+int attn_abi_version(void) { return 3; }
 
 const char* attn_status_string(attn_status_t s) {
   switch (s) {
@@ -746,7 +746,7 @@ static MaskGeom mask_geom(int Nq, int Nk, const attn_mask_t* m) {
   }
   if (m != nullptr && m->bias != nullptr) {
     g.bias_planes = m->bias_batch * m->bias_heads;
-    g.bias_t_bytes = ((size_t)g.bias_planes * Nq * Nk * 4 + 15) / 16 * 16;
+    g.bias_t_bytes = ((size_t)g.bias_planes * Nq * Nk * (m->bias_bf16 ? 2 : 4) + 15) / 16 * 16;
   }
   return g;
 }
@@ -768,7 +768,8 @@ static attn_status_t check_mask(int B, int H, int Nq, int Nk, const attn_mask_t*
   if (m->bias != nullptr) {
     if ((m->bias_batch != 1 && m->bias_batch != B) || (m->bias_heads != 1 && m->bias_heads != H))
       return ATTN_ERR_INVALID_ARG;
-    if (reinterpret_cast<uintptr_t>(m->bias) & 3u) return ATTN_ERR_MISALIGNED;
+    if (m->bias_bf16 != 0 && m->bias_bf16 != 1) return ATTN_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(m->bias) & (m->bias_bf16 ? 1u : 3u)) return ATTN_ERR_MISALIGNED;
     if (m->bias_batch * m->bias_heads > 65535) return ATTN_ERR_UNSUPPORTED_SHAPE;  // planes on the grid's y
   }
   return ATTN_OK;
@@ -792,13 +793,14 @@ static attn_status_t check_mask_ptrs(const attn_mask_t* m) {
 // `bits_t`, and the additive mask's transpose at `bias_t` (backward), inside
 // the caller's workspace.  Causal enters as wr = 0.
 static sdpa::MaskArgs mask_args(const attn_mask_t* m, int Nq, int Nk, int causal, float scale, uint32_t* bits,
-                                uint32_t* bits_t, uint8_t* flags, float* bias_t) {
+                                uint32_t* bits_t, uint8_t* flags, void* bias_t) {
   const MaskGeom g = mask_geom(Nq, Nk, m);
   sdpa::MaskArgs a;
   a.bias = m->bias;
   a.bias_t = m->bias != nullptr ? bias_t : nullptr;
   a.bias_b = m->bias != nullptr ? m->bias_batch : 1;
   a.bias_h = m->bias != nullptr ? m->bias_heads : 1;
+  a.bias_bf16 = m->bias != nullptr ? m->bias_bf16 : 0;
   a.inv_scale = 1.f / scale;
   a.flags = m->mask != nullptr ? flags : nullptr;
   a.ftq = g.words_t / 4;
@@ -899,7 +901,7 @@ attn_status_t attn_bwd_masked_stages(const void* q, const void* k, const void* v
   uint32_t* bits = reinterpret_cast<uint32_t*>(ws + attn_bwd_workspace_size(B, H, Hkv, Nq, d));
   uint32_t* bits_t = reinterpret_cast<uint32_t*>(reinterpret_cast<uint8_t*>(bits) + g.bits_bytes);
   uint8_t* flags = reinterpret_cast<uint8_t*>(bits_t) + g.bits_t_bytes;
-  float* bias_t = reinterpret_cast<float*>(flags + g.flags_bytes);
+  void* bias_t = flags + g.flags_bytes;
   sdpa::BwdParams p;
   bwd_params(&p, workspace, B, H, Hkv, Nq, Nk, d, scale, causal, di);
   p.o = static_cast<const uint16_t*>(o);
@@ -917,7 +919,8 @@ attn_status_t attn_bwd_masked_stages(const void* q, const void* k, const void* v
                              bits, g.words, bits_t, g.words_t, flags, st) != cudaSuccess)
     return ATTN_ERR_LAUNCH;
   if ((stages & (kStagePrep | kStageDqRows)) && mask->bias != nullptr &&
-      sdpa::launch_bias_transpose(mask->bias, g.bias_planes, Nq, Nk, bias_t, st) != cudaSuccess)
+      sdpa::launch_bias_transpose(mask->bias, mask->bias_bf16 != 0, g.bias_planes, Nq, Nk, bias_t, st) !=
+          cudaSuccess)
     return ATTN_ERR_LAUNCH;
   if ((stages & kStagePrep) && sdpa::launch_bwd_prep(p, st) != cudaSuccess) return ATTN_ERR_LAUNCH;
   if (stages & kStageDqRows) {

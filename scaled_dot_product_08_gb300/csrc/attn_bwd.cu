@@ -267,33 +267,14 @@ __global__ void __launch_bounds__(384, 1)
       // columns, from its transposed copy, loaded before the waits below;
       // added as b / scale to the unscaled scores.  Query rows past Nq are
       // not read.
-      float bb[MASKED == 2 ? 64 : 1];
-      if constexpr (MASKED == 2) {
-#pragma unroll
-        for (int q = 0; q < 64; ++q) bb[q] = 0.f;
+      float bb[MASKED >= 2 ? 64 : 1];
+      if constexpr (MASKED >= 2) {
         const int kk = 128 * (int)(blockIdx.x % p.nkv) + r, q0 = 128 * i + 64 * X;
-        if (kk < p.Nk) {
-          const int bb_b = (int)(blockIdx.x / p.nkv) / p.Hkv, hq = seq_s[5] * p.G + g;
-          const float* bt_row =
-              p.mk.bias_t + ((size_t)bias_plane(p.mk, bb_b, hq) * p.Nk + (size_t)kk) * p.N + (size_t)q0;
-          const int nv = min(64, p.N - q0);
-          if ((p.N & 3) == 0) {  // the transpose sits 16-byte aligned in the workspace
-#pragma unroll
-            for (int q = 0; q < 64; q += 4) {
-              if (q < nv) {
-                const float4 b4v = __ldg(reinterpret_cast<const float4*>(bt_row + q));
-                bb[q] = b4v.x;
-                bb[q + 1] = b4v.y;
-                bb[q + 2] = b4v.z;
-                bb[q + 3] = b4v.w;
-              }
-            }
-          } else {
-#pragma unroll
-            for (int q = 0; q < 64; ++q)
-              if (q < nv) bb[q] = __ldg(bt_row + q);
-          }
-        }
+        const int bb_b = (int)(blockIdx.x / p.nkv) / p.Hkv, hq = seq_s[5] * p.G + g;
+        // (the transpose sits 16-byte aligned in the workspace)
+        load_bias_row<64, MASKED == 3>(
+            p.mk.bias_t, ((size_t)bias_plane(p.mk, bb_b, hq) * p.Nk + (size_t)kk) * p.N + (size_t)q0,
+            kk < p.Nk ? min(64, p.N - q0) : 0, bias_rows_vec(p.mk.bias_t, p.N, MASKED == 3), bb);
       }
       // Masked instance with a boolean mask: this key row's bits over the
       // warpgroup's 64 query columns, loaded before the waits below so that
@@ -333,7 +314,7 @@ __global__ void __launch_bounds__(384, 1)
           x[32 + e] = __uint_as_float(rb[e]);
         }
       }
-      if constexpr (MASKED == 2) {
+      if constexpr (MASKED >= 2) {
 #pragma unroll
         for (int q = 0; q < 64; ++q) x[q] = fmaf(bb[q], p.mk.inv_scale, x[q]);
       }
@@ -653,13 +634,13 @@ cudaError_t launch_bwd_grad(int d, bool causal, const CUtensorMap& tq, const CUt
                             const CUtensorMap& tdo, const CUtensorMap& tdk, const CUtensorMap& tdv,
                             const BwdParams& p, cudaStream_t stream, bool masked) {
   if (masked) {
-    const bool bias = p.mk.bias != nullptr;  // the instance with the additive mask
+    const bool bias = p.mk.bias != nullptr;  // the instances with the additive mask (float32, bf16)
     switch (d) {
-      case 64: return bias ? launch_main_t<64, false, 2>(tq, tk, tv, tdo, tdk, tdv, p, stream)
+      case 64: return bias ? (p.mk.bias_bf16 ? launch_main_t<64, false, 3>(tq, tk, tv, tdo, tdk, tdv, p, stream) : launch_main_t<64, false, 2>(tq, tk, tv, tdo, tdk, tdv, p, stream))
                       : launch_main_t<64, false, 1>(tq, tk, tv, tdo, tdk, tdv, p, stream);
-      case 96: return bias ? launch_main_t<96, false, 2>(tq, tk, tv, tdo, tdk, tdv, p, stream)
+      case 96: return bias ? (p.mk.bias_bf16 ? launch_main_t<96, false, 3>(tq, tk, tv, tdo, tdk, tdv, p, stream) : launch_main_t<96, false, 2>(tq, tk, tv, tdo, tdk, tdv, p, stream))
                       : launch_main_t<96, false, 1>(tq, tk, tv, tdo, tdk, tdv, p, stream);
-      case 128: return bias ? launch_main_t<128, false, 2>(tq, tk, tv, tdo, tdk, tdv, p, stream)
+      case 128: return bias ? (p.mk.bias_bf16 ? launch_main_t<128, false, 3>(tq, tk, tv, tdo, tdk, tdv, p, stream) : launch_main_t<128, false, 2>(tq, tk, tv, tdo, tdk, tdv, p, stream))
                       : launch_main_t<128, false, 1>(tq, tk, tv, tdo, tdk, tdv, p, stream);
       default: return cudaErrorInvalidValue;
     }

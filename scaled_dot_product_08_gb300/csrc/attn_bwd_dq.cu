@@ -316,31 +316,12 @@ __global__ void __launch_bounds__(384, 1)
       // The additive mask of this row over the warpgroup's 64 keys, loaded
       // before the wait for S; added as b / scale to the unscaled scores.
       // Columns past Nk are not read.
-      float bb[MASKED == 2 ? 64 : 1];
-      if constexpr (MASKED == 2) {
-#pragma unroll
-        for (int k = 0; k < 64; ++k) bb[k] = 0.f;
+      float bb[MASKED >= 2 ? 64 : 1];
+      if constexpr (MASKED >= 2) {
         const int row = 128 * i + r, k0 = (seq_s[4] + jt) * 128 + 64 * X;
-        if (row < seq_s[1]) {
-          const float* br = p.mk.bias + ((size_t)bias_plane(p.mk, b, h) * p.N + (size_t)row) * p.Nk + (size_t)k0;
-          const int nv = min(64, p.Nk - k0);
-          if ((p.Nk & 3) == 0 && (reinterpret_cast<uintptr_t>(p.mk.bias) & 15) == 0) {
-#pragma unroll
-            for (int k = 0; k < 64; k += 4) {
-              if (k < nv) {
-                const float4 b4v = __ldg(reinterpret_cast<const float4*>(br + k));
-                bb[k] = b4v.x;
-                bb[k + 1] = b4v.y;
-                bb[k + 2] = b4v.z;
-                bb[k + 3] = b4v.w;
-              }
-            }
-          } else {
-#pragma unroll
-            for (int k = 0; k < 64; ++k)
-              if (k < nv) bb[k] = __ldg(br + k);
-          }
-        }
+        load_bias_row<64, MASKED == 3>(
+            p.mk.bias, ((size_t)bias_plane(p.mk, b, h) * p.N + (size_t)row) * p.Nk + (size_t)k0,
+            row < seq_s[1] ? min(64, p.Nk - k0) : 0, bias_rows_vec(p.mk.bias, p.Nk, MASKED == 3), bb);
       }
       ok = __all_sync(0xffffffffu, wait_bounded(wc, bS + 8u * (j & 1), (j >> 1) & 1, wait_site(0x81, j)));
       if (!ok) break;
@@ -359,7 +340,7 @@ __global__ void __launch_bounds__(384, 1)
           x[32 + e] = __uint_as_float(rb[e]);
         }
       }
-      if constexpr (MASKED == 2) {
+      if constexpr (MASKED >= 2) {
 #pragma unroll
         for (int k = 0; k < 64; ++k) x[k] = fmaf(bb[k], p.mk.inv_scale, x[k]);
       }
@@ -645,13 +626,13 @@ cudaError_t launch_bwd_dq(int d, bool causal, const CUtensorMap& tq, const CUten
                           const CUtensorMap& tdo, const CUtensorMap& tdq, const CUtensorMap& to, const BwdParams& p,
                           cudaStream_t stream, bool masked) {
   if (masked) {
-    const bool bias = p.mk.bias != nullptr;  // the instance with the additive mask
+    const bool bias = p.mk.bias != nullptr;  // the instances with the additive mask (float32, bf16)
     switch (d) {
-      case 64: return bias ? launch_dq_t<64, false, 2>(tq, tk, tv, tdo, tdq, to, p, stream)
+      case 64: return bias ? (p.mk.bias_bf16 ? launch_dq_t<64, false, 3>(tq, tk, tv, tdo, tdq, to, p, stream) : launch_dq_t<64, false, 2>(tq, tk, tv, tdo, tdq, to, p, stream))
                       : launch_dq_t<64, false, 1>(tq, tk, tv, tdo, tdq, to, p, stream);
-      case 96: return bias ? launch_dq_t<96, false, 2>(tq, tk, tv, tdo, tdq, to, p, stream)
+      case 96: return bias ? (p.mk.bias_bf16 ? launch_dq_t<96, false, 3>(tq, tk, tv, tdo, tdq, to, p, stream) : launch_dq_t<96, false, 2>(tq, tk, tv, tdo, tdq, to, p, stream))
                       : launch_dq_t<96, false, 1>(tq, tk, tv, tdo, tdq, to, p, stream);
-      case 128: return bias ? launch_dq_t<128, false, 2>(tq, tk, tv, tdo, tdq, to, p, stream)
+      case 128: return bias ? (p.mk.bias_bf16 ? launch_dq_t<128, false, 3>(tq, tk, tv, tdo, tdq, to, p, stream) : launch_dq_t<128, false, 2>(tq, tk, tv, tdo, tdq, to, p, stream))
                       : launch_dq_t<128, false, 1>(tq, tk, tv, tdo, tdq, to, p, stream);
       default: return cudaErrorInvalidValue;
     }

@@ -257,32 +257,12 @@ __global__ void __launch_bounds__(384, 1)
       // wait for S so that its latency hides behind the Q K^T MMA; added as
       // b / scale to the unscaled scores (scaled below: scale x + b); -inf
       // hides the key.  Columns past Nk are not read (the bounds hide them).
-      float bb[MASKED == 2 ? 128 : 1];
-      if constexpr (MASKED == 2) {
-#pragma unroll
-        for (int i = 0; i < 128; ++i) bb[i] = 0.f;
-        if (qi * 128 + r < p.Nq) {
-          const float* br = p.mk.bias + ((size_t)bias_plane(p.mk, b, h) * p.Nq + (size_t)(qi * 128 + r)) * p.Nk +
-                            (size_t)jt * 128;
-          const int nv = min(128, p.Nk - jt * 128);
-          if ((p.Nk & 3) == 0 && (reinterpret_cast<uintptr_t>(p.mk.bias) & 15) == 0) {
-            // rows start 16-byte aligned: four columns per load
-#pragma unroll
-            for (int i = 0; i < 128; i += 4) {
-              if (i < nv) {
-                const float4 b4v = __ldg(reinterpret_cast<const float4*>(br + i));
-                bb[i] = b4v.x;
-                bb[i + 1] = b4v.y;
-                bb[i + 2] = b4v.z;
-                bb[i + 3] = b4v.w;
-              }
-            }
-          } else {
-#pragma unroll
-            for (int i = 0; i < 128; ++i)
-              if (i < nv) bb[i] = __ldg(br + i);
-          }
-        }
+      float bb[MASKED >= 2 ? 128 : 1];
+      if constexpr (MASKED >= 2) {
+        const int row = qi * 128 + r;
+        load_bias_row<128, MASKED == 3>(
+            p.mk.bias, ((size_t)bias_plane(p.mk, b, h) * p.Nq + (size_t)row) * p.Nk + (size_t)jt * 128,
+            row < p.Nq ? min(128, p.Nk - jt * 128) : 0, bias_rows_vec(p.mk.bias, p.Nk, MASKED == 3), bb);
       }
       ok = __all_sync(0xffffffffu, wait_bounded(wc, barS, j & 1, wait_site(0x51 + s, j)));
       if (!ok) break;
@@ -307,7 +287,7 @@ __global__ void __launch_bounds__(384, 1)
           x[96 + i] = __uint_as_float(rd[i]);
         }
       }
-      if constexpr (MASKED == 2) {
+      if constexpr (MASKED >= 2) {
 #pragma unroll
         for (int i = 0; i < 128; ++i) x[i] = fmaf(bb[i], p.mk.inv_scale, x[i]);
       }
@@ -663,13 +643,13 @@ static cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, co
 cudaError_t launch_fwd(int d, bool causal, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                        const CUtensorMap& to, const FwdParams& p, cudaStream_t stream, bool masked) {
   if (masked) {
-    const bool bias = p.mk.bias != nullptr;  // the instance with the additive mask
+    const bool bias = p.mk.bias != nullptr;  // the instances with the additive mask (float32, bf16)
     switch (d) {
-      case 64: return bias ? launch_fwd_t<64, false, 2>(tq, tk, tv, to, p, stream)
+      case 64: return bias ? (p.mk.bias_bf16 ? launch_fwd_t<64, false, 3>(tq, tk, tv, to, p, stream) : launch_fwd_t<64, false, 2>(tq, tk, tv, to, p, stream))
                       : launch_fwd_t<64, false, 1>(tq, tk, tv, to, p, stream);
-      case 96: return bias ? launch_fwd_t<96, false, 2>(tq, tk, tv, to, p, stream)
+      case 96: return bias ? (p.mk.bias_bf16 ? launch_fwd_t<96, false, 3>(tq, tk, tv, to, p, stream) : launch_fwd_t<96, false, 2>(tq, tk, tv, to, p, stream))
                       : launch_fwd_t<96, false, 1>(tq, tk, tv, to, p, stream);
-      case 128: return bias ? launch_fwd_t<128, false, 2>(tq, tk, tv, to, p, stream)
+      case 128: return bias ? (p.mk.bias_bf16 ? launch_fwd_t<128, false, 3>(tq, tk, tv, to, p, stream) : launch_fwd_t<128, false, 2>(tq, tk, tv, to, p, stream))
                       : launch_fwd_t<128, false, 1>(tq, tk, tv, to, p, stream);
       default: return cudaErrorInvalidValue;
     }

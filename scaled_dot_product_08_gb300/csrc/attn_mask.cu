@@ -125,15 +125,17 @@ __global__ void __launch_bounds__(256) mask_pack_kernel(const uint8_t* __restric
 
 // The additive mask's transpose, (planes, Nq, Nk) -> (planes, Nk, Nq), for
 // the dK/dV kernel, whose threads own key rows: 32 x 32 blocks through
-// shared memory (pitch 33 words: the column reads hit distinct banks).
-__global__ void __launch_bounds__(256) bias_transpose_kernel(const float* __restrict__ bias, int Nq, int Nk,
-                                                             float* __restrict__ bias_t) {
-  __shared__ float blk[32][33];
+// shared memory (pitch 33 elements: the column reads hit distinct banks).
+// T: float (float32 mask) or uint16_t (bf16 bits, moved unchanged).
+template <typename T>
+__global__ void __launch_bounds__(256) bias_transpose_kernel(const T* __restrict__ bias, int Nq, int Nk,
+                                                             T* __restrict__ bias_t) {
+  __shared__ T blk[32][33];
   const int tk = (Nk + 31) / 32;
   const int kb = (int)(blockIdx.x % tk), qb = (int)(blockIdx.x / tk);
   const size_t plane = blockIdx.y;
-  const float* src = bias + plane * Nq * Nk;
-  float* dst = bias_t + plane * Nq * Nk;
+  const T* src = bias + plane * Nq * Nk;
+  T* dst = bias_t + plane * Nq * Nk;
   const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
   for (int rr = ty; rr < 32; rr += 8) {
     const int qi = qb * 32 + rr, kj = kb * 32 + tx;
@@ -148,9 +150,15 @@ __global__ void __launch_bounds__(256) bias_transpose_kernel(const float* __rest
 
 }  // namespace
 
-cudaError_t launch_bias_transpose(const float* bias, int planes, int Nq, int Nk, float* bias_t, cudaStream_t stream) {
+cudaError_t launch_bias_transpose(const void* bias, bool bf16, int planes, int Nq, int Nk, void* bias_t,
+                                  cudaStream_t stream) {
   const unsigned blocks = (unsigned)((Nq + 31) / 32) * (unsigned)((Nk + 31) / 32);
-  bias_transpose_kernel<<<dim3(blocks, (unsigned)planes), 256, 0, stream>>>(bias, Nq, Nk, bias_t);
+  if (bf16)
+    bias_transpose_kernel<uint16_t><<<dim3(blocks, (unsigned)planes), 256, 0, stream>>>(
+        static_cast<const uint16_t*>(bias), Nq, Nk, static_cast<uint16_t*>(bias_t));
+  else
+    bias_transpose_kernel<float><<<dim3(blocks, (unsigned)planes), 256, 0, stream>>>(
+        static_cast<const float*>(bias), Nq, Nk, static_cast<float*>(bias_t));
   return cudaGetLastError();
 }
 

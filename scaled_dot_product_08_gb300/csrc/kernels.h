@@ -37,14 +37,15 @@ struct MaskArgs {
   int mask_b, mask_h;
   const uint8_t* flags;
   int ftq, ftk;  // query and key tiles per plane in flags
-  // Additive mask (float32, added to the scaled scores): (bias_b, bias_h,
-  // Nq, Nk) as given, and its (bias_b * bias_h, Nk, Nq) transpose for the
-  // dK/dV kernel (backward only); inv_scale = 1 / scale, so that x + b *
-  // inv_scale, scaled, is scale x + b.
-  const float* bias;
-  const float* bias_t;
+  // Additive mask (float32, or bf16 when bias_bf16; added to the scaled
+  // scores): (bias_b, bias_h, Nq, Nk) as given, and its (bias_b * bias_h,
+  // Nk, Nq) transpose in the same type for the dK/dV kernel (backward only);
+  // inv_scale = 1 / scale, so that x + b * inv_scale, scaled, is scale x + b.
+  const void* bias;
+  const void* bias_t;
   int bias_b, bias_h;
   float inv_scale;
+  int bias_bf16;
 };
 
 // Most key tiles a masked forward / dQ CTA can list for skipping (its
@@ -150,6 +151,60 @@ __device__ __forceinline__ int bias_plane(const MaskArgs& mk, int b, int h) {
   return (mk.bias_b > 1 ? b : 0) * mk.bias_h + (mk.bias_h > 1 ? h : 0);
 }
 
+// n (<= CNT) consecutive values of an additive mask, element `off` of the
+// array at `base` on, as float (float32 storage, or bf16 when BF16); the
+// rest of out[] is 0.  vec: the values start 16-byte aligned and n is a
+// multiple of 16 bytes' worth (4 float32, 8 bf16), so 16-byte loads are used.
+template <int CNT, bool BF16>
+__device__ __forceinline__ void load_bias_row(const void* base, size_t off, int n, bool vec, float (&out)[CNT]) {
+#pragma unroll
+  for (int i = 0; i < CNT; ++i) out[i] = 0.f;
+  if constexpr (BF16) {
+    const uint16_t* r = static_cast<const uint16_t*>(base) + off;
+    if (vec) {
+#pragma unroll
+      for (int i = 0; i < CNT; i += 8) {
+        if (i < n) {
+          const uint4 u = __ldg(reinterpret_cast<const uint4*>(r + i));
+          const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            out[i + 2 * e] = __uint_as_float(w[e] << 16);
+            out[i + 2 * e + 1] = __uint_as_float(w[e] & 0xffff0000u);
+          }
+        }
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < CNT; ++i)
+        if (i < n) out[i] = __uint_as_float((uint32_t)__ldg(r + i) << 16);
+    }
+  } else {
+    const float* r = static_cast<const float*>(base) + off;
+    if (vec) {
+#pragma unroll
+      for (int i = 0; i < CNT; i += 4) {
+        if (i < n) {
+          const float4 v = __ldg(reinterpret_cast<const float4*>(r + i));
+          out[i] = v.x;
+          out[i + 1] = v.y;
+          out[i + 2] = v.z;
+          out[i + 3] = v.w;
+        }
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < CNT; ++i)
+        if (i < n) out[i] = __ldg(r + i);
+    }
+  }
+}
+// Whether rows of length `len` of an additive mask array at `base` start
+// 16-byte aligned (element size 2 for bf16, else 4).
+__device__ __forceinline__ bool bias_rows_vec(const void* base, int len, bool bf16) {
+  return (reinterpret_cast<uintptr_t>(base) & 15) == 0 && (len & (bf16 ? 7 : 3)) == 0;
+}
+
 // One sequence of a (possibly packed) batch as a kernel sees it.
 struct SeqView {
   int q0, nq;  // first query row in the tensor map, query rows
@@ -193,9 +248,10 @@ cudaError_t launch_bwd_grad(int d, bool causal, const CUtensorMap& tq, const CUt
 cudaError_t launch_bwd_dq(int d, bool causal, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                           const CUtensorMap& tdo, const CUtensorMap& tdq, const CUtensorMap& to, const BwdParams& p,
                           cudaStream_t stream, bool masked = false);
-// Writes the (planes, Nk, Nq) transpose of a float32 (planes, Nq, Nk)
-// additive mask (the dK/dV kernel reads it by key row).
-cudaError_t launch_bias_transpose(const float* bias, int planes, int Nq, int Nk, float* bias_t, cudaStream_t stream);
+// Writes the (planes, Nk, Nq) transpose of a (planes, Nq, Nk) additive mask,
+// float32 or bf16 (the dK/dV kernel reads it by key row).
+cudaError_t launch_bias_transpose(const void* bias, bool bf16, int planes, int Nq, int Nk, void* bias_t,
+                                  cudaStream_t stream);
 // Packs a boolean (mask_b, mask_h, Nq, Nk) byte mask into the row and
 // transposed bit layouts of MaskArgs (bits_t may be null: row bits only).
 cudaError_t launch_mask_pack(const uint8_t* mask, int mask_b, int mask_h, int Nq, int Nk, uint32_t* bits,

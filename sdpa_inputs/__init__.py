@@ -56,6 +56,9 @@ Masked workloads (attn_fwd_masked / attn_bwd_masked), forward + backward:
        (window_left 4095): the [PROF] page's window attention, n * w work
   pl1  B=8  H=16  Hkv=16 N=4096  d=128  prefix-LM boolean mask, one plane for
        all (b, h): key j visible to query i when j < 1024 or j <= i
+  ab1  B=8  H=16  Hkv=16 N=4096  d=128  additive float32 mask -|i - j| / 64,
+       one plane for all (b, h)   seed 13
+  ab1h ab1 with its mask stored in bf16 (values rounded to bf16)
 
 Every draw is numpy's PCG64 ``default_rng(seed).standard_normal(dtype=float32)``
 taken in the fixed order Q, K, V, dO, multiplied by the config's amplitude and
@@ -92,6 +95,7 @@ class Workload:
     prefix: int | None = None                 # masked: prefix-LM boolean mask with this prefix
     page_size: int | None = None              # decode: the cache kept in pages of this many tokens
     bias_slope: float | None = None           # masked: additive (1, 1, N, N) bias -slope * |i - j|
+    bias_bf16: bool = False                   # masked: that bias stored in bf16 (its values rounded to bf16)
 
     @property
     def softmax_scale(self) -> float:
@@ -126,6 +130,8 @@ WORKLOADS: dict[str, Workload] = {
     "sw1": Workload("sw1", 1, 32, 8, 16384, 128, True, 11, with_grad=True, kind="masked", window=(4095, -1)),
     "pl1": Workload("pl1", 8, 16, 16, 4096, 128, False, 12, with_grad=True, kind="masked", prefix=1024),
     "ab1": Workload("ab1", 8, 16, 16, 4096, 128, False, 13, with_grad=True, kind="masked", bias_slope=1 / 64),
+    "ab1h": Workload("ab1h", 8, 16, 16, 4096, 128, False, 13, with_grad=True, kind="masked", bias_slope=1 / 64,
+                     bias_bf16=True),
 }
 
 
@@ -144,6 +150,16 @@ def distance_bias(N: int, slope: float) -> np.ndarray:
     i = np.arange(N)[:, None]
     j = np.arange(N)[None, :]
     return (-slope * np.abs(i - j)).astype(np.float32)[None, None]
+
+
+def workload_bias(w: Workload) -> np.ndarray | None:
+    """The additive mask of a masked workload as float32 values: the
+    distance bias, rounded to bf16 (nearest even) when the workload stores it
+    in bf16; None without one."""
+    if w.bias_slope is None:
+        return None
+    b = distance_bias(w.N, w.bias_slope)
+    return round_bf16(b) if w.bias_bf16 else b
 
 
 def visible_pairs(w: Workload) -> int:

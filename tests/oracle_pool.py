@@ -155,15 +155,18 @@ def cross_head(task):
 
 def masked_head(task):
     """One head under a mask built here from its recipe: ("prefix", p) a
-    prefix-LM boolean mask, ("distance", slope) the additive bias
-    -slope * |i - j|; forward and, when dO is given, backward.
+    prefix-LM boolean mask, ("distance", slope, bf16) the additive bias
+    -slope * |i - j| (rounded to bf16 when bf16); forward and, when dO is
+    given, backward.
     task: (q, k, v, do or None, O, lse, dq, dk, dv (or None), scale, causal, recipe, head)."""
-    from sdpa_inputs import distance_bias, prefix_lm_mask
+    from sdpa_inputs import distance_bias, prefix_lm_mask, round_bf16
     q, k, v, do, O, lse, dq, dk, dv, scale, causal, recipe, head = task
     one = lambda a: np.asarray(a[None, None], dtype=np.float64)
     N = q.shape[0]
     mask = prefix_lm_mask(N, recipe[1]) if recipe[0] == "prefix" else None
     bias = distance_bias(N, recipe[1]) if recipe[0] == "distance" else None
+    if bias is not None and len(recipe) > 2 and recipe[2]:
+        bias = round_bf16(bias)
     O_ref, lse_ref = oracle.attention_masked_forward(one(q), one(k), one(v), scale, causal, None, None, mask, bias)
     out = _o_lse_errors(O, lse, O_ref[0, 0], lse_ref[0, 0], head)
     if do is not None:

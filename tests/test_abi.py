@@ -40,7 +40,7 @@ def test_status_strings(lib):
     for s in sdpa.Status:
         assert sdpa.attn_status_string(int(s)) == "ATTN_" + ("OK" if s == 0 else "ERR_" + s.name)
     assert sdpa.attn_status_string(99) == "ATTN_ERR_UNKNOWN"
-    assert lib.attn_abi_version() == 2
+    assert lib.attn_abi_version() == 3
 
 
 def test_workspace_size_formula(lib):
@@ -244,8 +244,8 @@ def test_varlen_rejects_bad_arguments(lib):
 def test_masked_rejects_bad_arguments(lib):
     import scaled_dot_product_08_gb300 as sdpa
     S = sdpa.Status
-    M = lambda wl=-1, wr=-1, kl=0, m=0, mb=1, mh=1, bias=0, bb=1, bh=1: sdpa.AttnMask(wl, wr, kl, m, mb, mh,
-                                                                                       bias, bb, bh)
+    M = lambda wl=-1, wr=-1, kl=0, m=0, mb=1, mh=1, bias=0, bb=1, bh=1, bf=0: sdpa.AttnMask(
+        wl, wr, kl, m, mb, mh, bias, bb, bh, bf)
     f = lambda mask, ws=FAKE, wsb=1 << 20, causal=0: sdpa.attn_fwd_masked(
         FAKE, FAKE, FAKE, FAKE, FAKE, 2, 4, 2, 100, 300, 128, 0.1, causal, mask, ws, wsb, None)
     assert f(M(wl=-2)) == S.INVALID_ARG
@@ -265,8 +265,13 @@ def test_masked_rejects_bad_arguments(lib):
         stages, None)
     assert g(0) == S.INVALID_ARG and g(16) == S.INVALID_ARG and g(17) == S.INVALID_ARG
     assert g(7, wsb=16) == S.WORKSPACE
-    # the additive mask: float32, 4-byte aligned, (1 or B, 1 or H, Nq, Nk)
+    # the additive mask: float32 (4-byte aligned) or bf16 (2-byte aligned), (1 or B, 1 or H, Nq, Nk)
     assert f(M(bias=FAKE + 2)) == S.MISALIGNED
+    assert f(M(bias=FAKE + 1, bf=1)) == S.MISALIGNED
+    assert f(M(bias=FAKE, bf=2)) == S.INVALID_ARG
+    for bf, size in ((0, 4), (1, 2)):  # the backward's transpose of the bias, in its own type
+        assert sdpa.attn_masked_workspace_size(2, 4, 2, 100, 300, 128, M(bias=FAKE, bb=2, bf=bf), 1) == (
+            sdpa.attn_bwd_workspace_size(2, 4, 2, 100, 128) + -(-2 * 100 * 300 * size // 16) * 16)
     assert f(M(bias=FAKE, bb=3)) == S.INVALID_ARG
     assert f(M(bias=FAKE, bh=2)) == S.INVALID_ARG
     # its transpose (float32, Nk x Nq per plane) joins the backward's workspace only

@@ -103,10 +103,10 @@ def test_sw1_sliding_window(cuda_lib):
     _check_parts("sw1", _run_pool(window_head, tasks, 7 * 128 * (wl + 128) * 8 + (1 << 28)))
 
 
-@pytest.mark.parametrize("name", ["pl1", "ab1"])
+@pytest.mark.parametrize("name", ["pl1", "ab1", "ab1h"])
 def test_masked_fwd_bwd(cuda_lib, name):
     import torch
-    from sdpa_inputs import distance_bias
+    from sdpa_inputs import workload_bias
     w = workload(name)
     x = make_inputs(w)
     s = w.softmax_scale
@@ -115,8 +115,9 @@ def test_masked_fwd_bwd(cuda_lib, name):
         recipe = ("prefix", w.prefix)
         args = (None, None, torch.from_numpy(prefix_lm_mask(w.N, w.prefix).astype(np.uint8)).cuda())
     else:
-        recipe = ("distance", w.bias_slope)
-        args = (None, None, None, torch.from_numpy(distance_bias(w.N, w.bias_slope)).cuda())
+        recipe = ("distance", w.bias_slope, w.bias_bf16)
+        tb = torch.from_numpy(workload_bias(w)).cuda()
+        args = (None, None, None, tb.to(torch.bfloat16) if w.bias_bf16 else tb)
     O, lse = cuda_lib.forward_masked(tq, tk, tv, s, w.causal, *args)
     dq, dk, dv = (_f32(g) for g in cuda_lib.backward_masked(tq, tk, tv, O, lse, tdo, s, w.causal, *args))
     O, lse = _f32(O), _f32(lse)

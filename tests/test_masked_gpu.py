@@ -8,7 +8,7 @@ import numpy as np
 import pytest
 
 import oracle
-from sdpa_inputs import make_random
+from sdpa_inputs import make_random, round_bf16
 from tests.parity import LSE_MAX_ABS, O_MAX_ABS, O_MEAN_ABS, check_grads, dev, host
 
 pytestmark = pytest.mark.gpu
@@ -227,8 +227,9 @@ BIAS_CASES = [
 ]
 
 
+@pytest.mark.parametrize("bias_dtype", ["float32", "bfloat16"])
 @pytest.mark.parametrize("case", BIAS_CASES, ids=lambda c: "B%dH%dKV%dQ%dK%dd%d" % c[0] + f"_c{int(c[1])}_{c[4]}_{c[5]}")
-def test_additive_mask_matches_oracle(cuda_lib, case):
+def test_additive_mask_matches_oracle(cuda_lib, case, bias_dtype):
     import torch
     shape, causal, window, kl, kind, bkind = case
     B, H, Hkv, Nq, Nk, d = shape
@@ -236,10 +237,12 @@ def test_additive_mask_matches_oracle(cuda_lib, case):
     mask = _mask(kind, B, H, Nq, Nk, 49100 + Nq)
     bshape = {"full": (B, H, Nq, Nk), "batch": (B, 1, Nq, Nk), "head": (1, H, Nq, Nk), "shared": (1, 1, Nq, Nk)}
     bias = _bias(bshape[bkind], 49200 + Nq)
+    if bias_dtype == "bfloat16":  # the values a bf16 bias holds (round to nearest even); -inf stays -inf
+        bias = round_bf16(bias)
     s = 1 / math.sqrt(d)
     kt = _t(np.asarray(kl, dtype=np.int32), torch.int32) if kl is not None else None
     mt = _t(mask.astype(np.uint8), torch.uint8) if mask is not None else None
-    bt = _t(bias, torch.float32)
+    bt = _t(bias, getattr(torch, bias_dtype))
     tq, tk, tv, tdo = dev(q), dev(k), dev(v), dev(do)
     O, lse = cuda_lib.forward_masked(tq, tk, tv, s, causal, window, kt, mt, bt)
     g = cuda_lib.backward_masked(tq, tk, tv, O, lse, tdo, s, causal, window, kt, mt, bt)
