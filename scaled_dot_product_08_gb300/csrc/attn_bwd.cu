@@ -105,8 +105,11 @@ __global__ void __launch_bounds__(384, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nkv = p.nkv;
-  const int bhk = blockIdx.x / nkv;           // b * Hkv + hk
-  const int j = blockIdx.x % nkv;             // key tile (0 = most causal work)
+  // Work unit (work_unit): K/V-head-major (the CTAs in flight share Q and dO
+  // in L2), the key tiles with the most causal work first; the last heads
+  // level-major, for a short tail.
+  int bhk, j;                                 // b * Hkv + hk, key tile (0 = most causal work)
+  work_unit((int)blockIdx.x, nkv, p.B * p.Hkv, p.tail, bhk, j);
   const int b = bhk / p.Hkv, hk = bhk % p.Hkv;
   const bool varlen = p.vl.cu_q != nullptr;
   // Tensor-map plane of K/V: b * Hkv + hk for the dense batch, the head for a
@@ -156,6 +159,8 @@ __global__ void __launch_bounds__(384, 1)
       seq_s[5] = hk;
       seq_s[6] = nke;
       if (MASKED) seq_s[7] = (p.mk.mask_b > 1 ? b : 0) * p.mk.mask_h;  // mask plane base of this batch element
+      seq_s[10] = j;
+      seq_s[11] = b;
     }
   }
   // Tile skipping (masked instance with tile flags): warp 0 lists the steps
@@ -269,8 +274,8 @@ __global__ void __launch_bounds__(384, 1)
       // not read.
       float bb[MASKED >= 2 ? 64 : 1];
       if constexpr (MASKED >= 2) {
-        const int kk = 128 * (int)(blockIdx.x % p.nkv) + r, q0 = 128 * i + 64 * X;
-        const int bb_b = (int)(blockIdx.x / p.nkv) / p.Hkv, hq = seq_s[5] * p.G + g;
+        const int kk = 128 * seq_s[10] + r, q0 = 128 * i + 64 * X;
+        const int bb_b = seq_s[11], hq = seq_s[5] * p.G + g;
         // (the transpose sits 16-byte aligned in the workspace)
         load_bias_row<64, MASKED == 3>(
             p.mk.bias_t, ((size_t)bias_plane(p.mk, bb_b, hq) * p.Nk + (size_t)kk) * p.N + (size_t)q0,
@@ -281,7 +286,7 @@ __global__ void __launch_bounds__(384, 1)
       // the load's latency hides behind them.
       uint2 bt = make_uint2(~0u, ~0u);
       if (MASKED && p.mk.bits_t != nullptr) {
-        const int kk = 128 * (int)(blockIdx.x % p.nkv) + r;
+        const int kk = 128 * seq_s[10] + r;
         if (kk < p.Nk) {
           const int hq = seq_s[5] * p.G + g;  // query head of this step
           const uint32_t plane = (uint32_t)seq_s[7] + (p.mk.mask_h > 1 ? (uint32_t)hq : 0u);
@@ -336,7 +341,7 @@ __global__ void __launch_bounds__(384, 1)
         // when the key is past the key length, and when its bit is clear.
         // Recomputed per step from shared memory and the indices rather than
         // held in registers across the loop.
-        const int kk = 128 * (int)(blockIdx.x % p.nkv) + r, koff = seq_s[3] - seq_s[1];
+        const int kk = 128 * seq_s[10] + r, koff = seq_s[3] - seq_s[1];
         const int qmin = (kk >= seq_s[6] ? (1 << 30) : p.mk.wr >= 0 ? kk - p.mk.wr - koff - 64 * X : -(1 << 30)) - 128 * i;
         const int qmax = (p.mk.wl >= 0 ? kk + p.mk.wl - koff - 64 * X : (1 << 30)) - 128 * i;
         if (__any_sync(0xffffffffu, qmin > 0 || qmax < 63 || (bt.x & bt.y) != ~0u)) {
@@ -429,12 +434,12 @@ __global__ void __launch_bounds__(384, 1)
     // The dense batch clips the box at Nk.  In a packed batch the rows past
     // the sequence belong to the next one, so warp 11 stores a partial tile
     // row by row (barrier 3: both warpgroups' staging is complete).
-    const int valid = seq_s[3] - 128 * (int)(blockIdx.x % p.nkv);
+    const int valid = seq_s[3] - 128 * seq_s[10];
     if (valid >= 128 || p.vl.cu_q == nullptr) {
       if (ok && r == 0) {
         for (int cb = 0; cb < T::NB; ++cb)
           tma_store_3d(X ? &tmdK : &tmdV, stage + cb * T::BLOCK_BYTES, cb * 64,
-                       seq_s[2] + 128 * (int)(blockIdx.x % p.nkv), seq_s[4]);
+                       seq_s[2] + 128 * seq_s[10], seq_s[4]);
         bulk_commit();
         bulk_wait_read_all();
       }
@@ -626,7 +631,9 @@ static cudaError_t launch_main_t(const CUtensorMap& tq, const CUtensorMap& tk, c
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, BwdTraits<D>::SMEM);
   if (e != cudaSuccess) return e;
   const unsigned grid = (unsigned)p.nkv * (unsigned)(p.B * p.Hkv);
-  kern<<<grid, BwdTraits<D>::THREADS, BwdTraits<D>::SMEM, stream>>>(tq, tk, tv, tdo, tdk, tdv, p);
+  BwdParams pc = p;
+  pc.tail = order_tail(p.nkv, p.B * p.Hkv, 1);
+  kern<<<grid, BwdTraits<D>::THREADS, BwdTraits<D>::SMEM, stream>>>(tq, tk, tv, tdo, tdk, tdv, pc);
   return cudaGetLastError();
 }
 

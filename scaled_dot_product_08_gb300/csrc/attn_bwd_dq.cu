@@ -98,10 +98,12 @@ __global__ void __launch_bounds__(384, 1)
   volatile uint16_t* const tile_list = reinterpret_cast<volatile uint16_t*>(misc + T::MISC);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // Work unit: head-major (the CTAs in flight share K/V heads in L2); within
-  // a head the longest causal walks go first.
-  const int bh = blockIdx.x / p.nq;
-  const int i = p.nq - 1 - (int)(blockIdx.x % p.nq);  // query tile
+  // Work unit (work_unit): head-major (the CTAs in flight share K/V heads in
+  // L2), the longest causal walks of a head first; the last heads
+  // level-major, for a short tail.
+  int bh, lv;
+  work_unit((int)blockIdx.x, p.nq, p.B * p.H, p.tail, bh, lv);
+  const int i = p.nq - 1 - lv;  // query tile
   const int b = bh / p.H, h = bh % p.H;
   const int bhk = b * p.Hkv + h / p.G;
   const bool varlen = p.vl.cu_q != nullptr;
@@ -618,7 +620,9 @@ static cudaError_t launch_dq_t(const CUtensorMap& tq, const CUtensorMap& tk, con
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, DqTraits<D>::SMEM);
   if (e != cudaSuccess) return e;
   const unsigned grid = (unsigned)p.nq * (unsigned)(p.B * p.H);
-  kern<<<grid, DqTraits<D>::THREADS, DqTraits<D>::SMEM, stream>>>(tq, tk, tv, tdo, tdq, to, p);
+  BwdParams pc = p;
+  pc.tail = order_tail(p.nq, p.B * p.H, p.G);
+  kern<<<grid, DqTraits<D>::THREADS, DqTraits<D>::SMEM, stream>>>(tq, tk, tv, tdo, tdq, to, pc);
   return cudaGetLastError();
 }
 

@@ -87,10 +87,11 @@ __global__ void __launch_bounds__(384, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
-  // Work unit: head-major so the CTAs in flight share few K/V heads (L2
-  // reuse); within a head the heaviest causal query tiles go first.
-  const int bh = blockIdx.x / p.n_mtiles;
-  const int mt = p.n_mtiles - 1 - (int)(blockIdx.x % p.n_mtiles);
+  // Work unit (work_unit): head-major, the heaviest causal query tiles of a
+  // head first; the last heads level-major, for a short tail.
+  int bh, lv;
+  work_unit((int)blockIdx.x, p.n_mtiles, p.B * p.H, p.tail, bh, lv);
+  const int mt = p.n_mtiles - 1 - lv;
   const int b = bh / p.H, h = bh % p.H;
   const int bhk = b * p.Hkv + h / p.G;
   // This CTA's sequence: the whole (b, h) plane, or rows of a packed batch
@@ -636,7 +637,9 @@ static cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, co
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, FwdTraits<D>::SMEM);
   if (e != cudaSuccess) return e;
   const unsigned grid = (unsigned)p.n_mtiles * (unsigned)(p.B * p.H);
-  kern<<<grid, FwdTraits<D>::THREADS, FwdTraits<D>::SMEM, stream>>>(tq, tk, tv, to, p);
+  FwdParams pc = p;
+  pc.tail = order_tail(p.n_mtiles, p.B * p.H, p.G);
+  kern<<<grid, FwdTraits<D>::THREADS, FwdTraits<D>::SMEM, stream>>>(tq, tk, tv, to, pc);
   return cudaGetLastError();
 }
 

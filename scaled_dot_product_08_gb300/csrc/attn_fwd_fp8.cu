@@ -110,9 +110,11 @@ __global__ void __launch_bounds__(384, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
-  // Work unit: head-major; within a head the heaviest causal tiles first.
-  const int bh = blockIdx.x / p.n_mtiles;
-  const int mt = p.n_mtiles - 1 - (int)(blockIdx.x % p.n_mtiles);
+  // Work unit (work_unit): head-major, the heaviest causal query tiles of a
+  // head first; the last heads level-major, for a short tail.
+  int bh, lv;
+  work_unit((int)blockIdx.x, p.n_mtiles, p.B * p.H, p.tail, bh, lv);
+  const int mt = p.n_mtiles - 1 - lv;
   const int bhk = (bh / p.H) * p.Hkv + (bh % p.H) / p.G;
   int n0 = p.nkv, n1 = p.nkv;  // key tiles visited by query tile 0 / 1
   if (CAUSAL) {  // up to the tile holding the last row's last visible key, koff + 128 qi + 127
@@ -418,7 +420,9 @@ cudaError_t launch_fp8_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, F8::SMEM);
   if (e != cudaSuccess) return e;
   const unsigned grid = (unsigned)p.n_mtiles * (unsigned)(p.B * p.H);
-  kern<<<grid, F8::THREADS, F8::SMEM, stream>>>(tq, tk, tv, p);
+  FwdParams pc = p;
+  pc.tail = order_tail(p.n_mtiles, p.B * p.H, p.G);
+  kern<<<grid, F8::THREADS, F8::SMEM, stream>>>(tq, tk, tv, pc);
   return cudaGetLastError();
 }
 

@@ -72,6 +72,7 @@ struct FwdParams {
   MaskArgs mk;           // masked instances only
   float o_scale;         // FP8: V's dequantisation factor, applied to O
   int debug_drop1;       // 0; n > 0 only in a test of the bounded waits: CTA 0's producer skips ring load n - 1
+  int tail;              // heads in the level-major tail of the CTA order (work_unit); set by the launcher
 };
 
 // Backward arguments.
@@ -98,7 +99,40 @@ struct BwdParams {
   uint16_t* dv;
   MaskArgs mk;           // masked instances only
   int debug_drop1;       // 0; n > 0 only in a test of the bounded waits: CTA 0's producer skips ring load n - 1
+  int tail;              // heads in the level-major tail of the CTA order (work_unit); set by each launcher
 };
+
+// CTA order of the forward, dQ and dK/dV launches.  A launch's CTAs cover
+// (head, level) work units, level 0 the heaviest (the longest causal walk).
+// Head-major order keeps the CTAs in flight on few heads, whose streamed
+// operands (K and V; Q and dO for dK/dV) are read once from HBM and then
+// from L2, but it ends on the heaviest unit of the last head and the other
+// SMs idle meanwhile.  So the last `tail` heads go level-major instead: all
+// their level-0 units, then all level-1 units, and so on, and the launch
+// ends on its lightest units.  tail = 1 is head-major order throughout.
+__host__ __device__ __forceinline__ void work_unit(int cta, int nlev, int nheads, int tail, int& head, int& level) {
+  const int lead = (nheads - tail) * nlev;  // CTAs of the head-major part
+  if (cta < lead) {
+    head = cta / nlev;
+    level = cta - head * nlev;
+  } else {
+    const int c = cta - lead;
+    level = c / tail;
+    head = nheads - tail + (c - level * tail);
+  }
+}
+
+// The level-major tail: whole groups of `group` heads (those that share K
+// and V), enough for about three waves of CTAs on this device's SMs, or all
+// heads.
+inline int order_tail(int nlev, int nheads, int group) {
+  int dev = 0, sms = 152;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    sms = 152;
+  int t = (3 * sms + nlev - 1) / (nlev > 0 ? nlev : 1);
+  t = (t + group - 1) / group * group;
+  return t < nheads ? (t > 0 ? t : 1) : nheads;
+}
 
 // Decode (split over the keys) arguments.
 constexpr int kDecMaxRows = 128;  // G * Nq query rows per K/V head (one 128-row MMA tile)
