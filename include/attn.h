@@ -57,7 +57,8 @@ typedef enum {
   ATTN_ERR_WORKSPACE = 5,          /* workspace missing or smaller than required  */
   ATTN_ERR_LAUNCH = 6,             /* the CUDA launch itself failed               */
   ATTN_ERR_TIMEOUT = 7,            /* a device-side wait ran out (reported by attn_get_device_status) */
-  ATTN_ERR_CUDA = 8                /* another CUDA runtime/driver error           */
+  ATTN_ERR_CUDA = 8,               /* another CUDA runtime/driver error           */
+  ATTN_ERR_CHECK = 9               /* debug build only: an in-kernel index check failed (reported by attn_get_device_status) */
 } attn_status_t;
 
 /*
@@ -424,7 +425,9 @@ attn_status_t attn_decode(const void* q, const void* k, const void* v, void* o, 
 /*
  * Synchronises `stream`, then returns (and clears) the device status word
  * that the kernels set when a bounded wait runs out: ATTN_OK or
- * ATTN_ERR_TIMEOUT; ATTN_ERR_CUDA if the synchronisation itself failed.
+ * ATTN_ERR_TIMEOUT (ATTN_ERR_INVALID_ARG for device-side offsets found out
+ * of range, ATTN_ERR_CHECK for a failed index check of the debug build);
+ * ATTN_ERR_CUDA if the synchronisation itself failed.
  */
 attn_status_t attn_get_device_status(void* stream);
 
@@ -432,7 +435,10 @@ attn_status_t attn_get_device_status(void* stream);
  * Where the first bounded wait that ran out since the last call happened,
  * for diagnosing ATTN_ERR_TIMEOUT: info[0] = (wait site << 16) | loop step,
  * info[1] = CTA index, info[2] = thread index, info[3] = microseconds waited;
- * all zero if no wait ran out.  Synchronises `stream`, then clears the record.
+ * all zero if no wait ran out.  In the debug build the first failed index
+ * check (ATTN_ERR_CHECK) fills the same record when it comes first:
+ * info[0] = check site << 16, info[3] = the offending element index
+ * (clamped to the int range).  Synchronises `stream`, then clears the record.
  * Each wait is limited to 2 s, or to SDPA08_WAIT_LIMIT_MS milliseconds
  * (1..60000) if that environment variable is set when the library is first
  * used on a device.
@@ -515,6 +521,36 @@ attn_status_t attn_bwd_noalloc(const void* q, const void* k, const void* v, cons
                                void* dq, void* dk, void* dv,
                                int B, int H, int Hkv, int N, int d, float scale, int causal,
                                void* stream);
+
+/*
+ * 1 when this library was built with the index checks of the debug build
+ * (-DATTN_DEBUG), 0 for the release build.  The pages have no counterpart:
+ * compute-sanitizer is not available on the target machines, and these
+ * checks stand in for its bounds checking.  In the debug build every plain
+ * global load and store whose element index a kernel computes (row vectors,
+ * lse, mask bits, the additive mask, packed-batch rows, decode partials,
+ * block-table entries) first checks that index against the extent implied
+ * by the call's arguments; a failed check records ATTN_ERR_CHECK
+ * (attn_get_device_status) and where it failed (attn_get_timeout_info),
+ * and the access is skipped (or, for a copy whose barrier expects its
+ * bytes, read from an in-range place), so the launch still completes and
+ * the context stays usable.  TMA copies need no check: the hardware clips
+ * them to the tensor map.
+ */
+int attn_debug_build(void);
+
+/*
+ * Test hook of the debug build (the pages have no counterpart): arms one
+ * launch, like attn_debug_drop_load, in which the first CTA computes an
+ * element index past the end of an output array, so that the index checks
+ * must catch it.  kernel 0: the forward kernel's lse store (attn_fwd and the
+ * calls built on it); 1: the dQ kernel's row-vector store into the workspace
+ * (attn_bwd's first stage; the dK/dV results of that call are then
+ * undefined).  The check records ATTN_ERR_CHECK and skips the store.
+ * Returns ATTN_ERR_INVALID_ARG for another kernel value and in the release
+ * build, where nothing is armed.
+ */
+attn_status_t attn_debug_plant_index(int kernel);
 
 #ifdef __cplusplus
 }

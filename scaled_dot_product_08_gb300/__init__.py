@@ -23,7 +23,7 @@ __all__ = [
     "AttnError", "Status", "load", "attn_fwd", "attn_bwd", "attn_bwd_workspace_size",
     "attn_bwd_prep", "attn_bwd_grad", "attn_bwd_dq", "attn_bwd_dq_rows", "attn_bwd_noalloc",
     "attn_get_device_status", "attn_get_timeout_info", "attn_status_string", "attn_selftest_wait_timeout",
-    "attn_debug_drop_load",
+    "attn_debug_drop_load", "attn_debug_build", "attn_debug_plant_index",
     "attn_decode", "attn_decode_workspace_size", "attn_fwd_cross", "attn_bwd_cross",
     "attn_bwd_grad_cross", "attn_bwd_dq_cross", "attn_fwd_varlen", "attn_bwd_varlen",
     "attn_bwd_varlen_workspace_size", "attn_bwd_varlen_stages", "forward_varlen", "backward_varlen",
@@ -44,6 +44,7 @@ class Status(enum.IntEnum):
     LAUNCH = 6
     TIMEOUT = 7
     CUDA = 8
+    CHECK = 9
 
 
 class AttnMask(ctypes.Structure):
@@ -66,13 +67,21 @@ _P = ctypes.c_void_p
 _I = ctypes.c_int
 
 
+def library_path() -> str:
+    """The library this process loads: the in-tree release build, or the file
+    that the environment variable SDPA08_LIBRARY names (e.g. the debug build,
+    _lib/libsdpa08_debug.so from build(debug=True))."""
+    return os.environ.get("SDPA08_LIBRARY") or LIB
+
+
 def load() -> ctypes.CDLL:
     """Load the in-tree shared library (raises if it has not been built)."""
     global _lib
     if _lib is None:
-        if not os.path.exists(LIB):
-            raise RuntimeError(f"CUDA library not built ({LIB} missing): run __graft_entry__.build()")
-        lib = ctypes.CDLL(LIB)
+        path = library_path()
+        if not os.path.exists(path):
+            raise RuntimeError(f"CUDA library not built ({path} missing): run __graft_entry__.build()")
+        lib = ctypes.CDLL(path)
         lib.attn_fwd.argtypes = [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, ctypes.c_float, _I, _P]
         lib.attn_fwd.restype = _I
         lib.attn_bwd_workspace_size.argtypes = [_I, _I, _I, _I, _I]
@@ -89,6 +98,10 @@ def load() -> ctypes.CDLL:
         lib.attn_bwd_dq.restype = _I
         lib.attn_debug_drop_load.argtypes = [_I, _I, ctypes.c_uint]
         lib.attn_debug_drop_load.restype = _I
+        lib.attn_debug_build.argtypes = []
+        lib.attn_debug_build.restype = _I
+        lib.attn_debug_plant_index.argtypes = [_I]
+        lib.attn_debug_plant_index.restype = _I
         lib.attn_get_device_status.argtypes = [_P]
         lib.attn_get_device_status.restype = _I
         lib.attn_status_string.argtypes = [_I]
@@ -309,6 +322,15 @@ def attn_selftest_wait_timeout(timeout_us: int, stream=None) -> int:
 
 def attn_debug_drop_load(kernel: int, load_index: int, limit_us: int) -> int:
     return load().attn_debug_drop_load(kernel, load_index, limit_us)
+
+
+def attn_debug_build() -> int:
+    """1 if the loaded library is the debug build (in-kernel index checks)."""
+    return load().attn_debug_build()
+
+
+def attn_debug_plant_index(kernel: int) -> int:
+    return load().attn_debug_plant_index(kernel)
 
 
 # ------------------------------------------------------------ torch marshalling

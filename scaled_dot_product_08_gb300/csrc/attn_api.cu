@@ -56,6 +56,18 @@ void take_debug(int kernel, int* drop1, unsigned long long* limit_ns) {
   g_debug_kernel = -1;
 }
 
+// The planted-index test hook of the debug build (attn_debug_plant_index):
+// armed for one launch of one kernel (0 forward, 1 dQ), then cleared.
+int g_plant_kernel = -1;
+
+// Sets *plant = value (and clears the hook) when it is armed for `kernel`.
+void take_plant(int kernel, int* plant, int value) {
+  std::lock_guard<std::mutex> lk(g_debug_mu);
+  if (g_plant_kernel != kernel) return;
+  *plant = value;
+  g_plant_kernel = -1;
+}
+
 // Written by kernels when a bounded wait gives up (0 = fine), and where the
 // first such timeout happened.
 __device__ int g_status_word;
@@ -270,6 +282,7 @@ const char* attn_status_string(attn_status_t s) {
     case ATTN_ERR_LAUNCH: return "ATTN_ERR_LAUNCH";
     case ATTN_ERR_TIMEOUT: return "ATTN_ERR_TIMEOUT";
     case ATTN_ERR_CUDA: return "ATTN_ERR_CUDA";
+    case ATTN_ERR_CHECK: return "ATTN_ERR_CHECK";
   }
   return "ATTN_ERR_UNKNOWN";
 }
@@ -308,6 +321,7 @@ static attn_status_t fwd_common(const void* q, const void* k, const void* v, voi
   p.limit_ns = wait_limit_ns();
   p.info = di->info;
   take_debug(0, &p.debug_drop1, &p.limit_ns);
+  take_plant(0, &p.debug_plant, 1);
   cudaError_t e = sdpa::launch_fwd(d, causal != 0, tq, tk, tv, to, p, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return ATTN_ERR_LAUNCH;
   return ATTN_OK;
@@ -494,6 +508,7 @@ static attn_status_t bwd_dq_rows_x(const void* q, const void* k, const void* v, 
   p.lse = lse;
   p.rows_in_dq = 1;
   take_debug(1, &p.debug_drop1, &p.limit_ns);
+  take_plant(1, &p.debug_plant, 2);
   cudaError_t e = sdpa::launch_bwd_dq(d, causal != 0, tq, tk, tv, tdo, tdq, to, p, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;
 }
@@ -1098,6 +1113,7 @@ attn_status_t attn_get_device_status(void* stream) {
   if (host == 0) return ATTN_OK;
   if (host == sdpa::kDevTimeout) return ATTN_ERR_TIMEOUT;
   if (host == sdpa::kDevBadSeqlens) return ATTN_ERR_INVALID_ARG;
+  if (host == sdpa::kDevCheckFailed) return ATTN_ERR_CHECK;
   return ATTN_ERR_CUDA;
 }
 
@@ -1128,6 +1144,15 @@ attn_status_t attn_debug_drop_load(int kernel, int load_index, unsigned int limi
   g_debug_kernel = kernel;
   g_debug_drop1 = load_index + 1;
   g_debug_limit_ns = (unsigned long long)limit_us * 1000ull;
+  return ATTN_OK;
+}
+
+int attn_debug_build(void) { return sdpa::kDebugChecks ? 1 : 0; }
+
+attn_status_t attn_debug_plant_index(int kernel) {
+  if (!sdpa::kDebugChecks || kernel < 0 || kernel > 1) return ATTN_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> lk(g_debug_mu);
+  g_plant_kernel = kernel;
   return ATTN_OK;
 }
 

@@ -147,7 +147,10 @@ __global__ void __launch_bounds__(384, 1)
       const uint32_t rs = varlen ? (uint32_t)(p.Hkv * D) : (uint32_t)D;
       const long long off = varlen ? ((long long)sq.k0 + 128 * j) * rs + (long long)hk * D
                                    : ((long long)bhk * p.Nk + 128 * j) * D;
-      zero_rows2_bf16<D>(p.dk + off, p.dv + off, rs, min(128, sq.nk - 128 * j));
+      const int cnt = min(128, sq.nk - 128 * j);
+      if (ATTN_IN_RANGE(varlen ? (long long)sq.k0 + 128 * j + cnt - 1 : (long long)bhk * p.Nk + 128 * j + cnt - 1,
+                        varlen ? (long long)p.vl.total_k : (long long)p.B * p.Hkv * p.Nk, p, 0x301))
+        zero_rows2_bf16<D>(p.dk + off, p.dv + off, rs, cnt);
       return;
     }
     if (threadIdx.x == 0) {
@@ -195,7 +198,10 @@ __global__ void __launch_bounds__(384, 1)
       const uint32_t rs = varlen ? (uint32_t)(p.Hkv * D) : (uint32_t)D;
       const long long off = varlen ? ((long long)seq_s[2] + 128 * j) * rs + (long long)hk * D
                                    : ((long long)bhk * p.Nk + 128 * j) * D;
-      zero_rows2_bf16<D>(p.dk + off, p.dv + off, rs, min(128, seq_s[3] - 128 * j));
+      const int cnt = min(128, seq_s[3] - 128 * j);
+      if (ATTN_IN_RANGE(varlen ? (long long)seq_s[2] + 128 * j + cnt - 1 : (long long)bhk * p.Nk + 128 * j + cnt - 1,
+                        varlen ? (long long)p.vl.total_k : (long long)p.B * p.Hkv * p.Nk, p, 0x301))
+        zero_rows2_bf16<D>(p.dk + off, p.dv + off, rs, cnt);
       return;
     }
   }
@@ -277,9 +283,10 @@ __global__ void __launch_bounds__(384, 1)
         const int kk = 128 * seq_s[10] + r, q0 = 128 * i + 64 * X;
         const int bb_b = seq_s[11], hq = seq_s[5] * p.G + g;
         // (the transpose sits 16-byte aligned in the workspace)
-        load_bias_row<64, MASKED == 3>(
-            p.mk.bias_t, ((size_t)bias_plane(p.mk, bb_b, hq) * p.Nk + (size_t)kk) * p.N + (size_t)q0,
-            kk < p.Nk ? min(64, p.N - q0) : 0, bias_rows_vec(p.mk.bias_t, p.N, MASKED == 3), bb);
+        const size_t boff = ((size_t)bias_plane(p.mk, bb_b, hq) * p.Nk + (size_t)kk) * p.N + (size_t)q0;
+        int bn = kk < p.Nk ? min(64, p.N - q0) : 0;
+        if (bn > 0 && !ATTN_IN_RANGE(boff + bn - 1, (size_t)p.mk.bias_b * p.mk.bias_h * p.Nk * p.N, p, 0x302)) bn = 0;
+        load_bias_row<64, MASKED == 3>(p.mk.bias_t, boff, bn, bias_rows_vec(p.mk.bias_t, p.N, MASKED == 3), bb);
       }
       // Masked instance with a boolean mask: this key row's bits over the
       // warpgroup's 64 query columns, loaded before the waits below so that
@@ -291,7 +298,8 @@ __global__ void __launch_bounds__(384, 1)
           const int hq = seq_s[5] * p.G + g;  // query head of this step
           const uint32_t plane = (uint32_t)seq_s[7] + (p.mk.mask_h > 1 ? (uint32_t)hq : 0u);
           const uint32_t w = (plane * (uint32_t)p.Nk + (uint32_t)kk) * (uint32_t)p.mk.words_t + 2u * X + 4u * i;
-          bt = *reinterpret_cast<const uint2*>(p.mk.bits_t + w);
+          if (ATTN_IN_RANGE((size_t)w + 1u, (size_t)p.mk.mask_b * p.mk.mask_h * p.Nk * p.mk.words_t, p, 0x303))
+            bt = *reinterpret_cast<const uint2*>(p.mk.bits_t + w);
         }
       }
       // The vectors come from the bulk copy of this step: observe its barrier
@@ -478,7 +486,9 @@ __global__ void __launch_bounds__(384, 1)
           mbar_expect_tx(barq, T::TILE_BYTES + T::VEC_BYTES);
           for (int cb = 0; cb < T::NB; ++cb)
             tma_load_3d(sQ + st * T::TILE_BYTES + cb * T::BLOCK_BYTES, &tmQ, barq, cb * 64, q0 + i * 128, qplane);
-          const size_t voff = (varlen ? (size_t)h * p.vec_stride + vseq : (size_t)bh * p.Npad) + (size_t)i * 128;
+          size_t voff = (varlen ? (size_t)h * p.vec_stride + vseq : (size_t)bh * p.Npad) + (size_t)i * 128;
+          // (a failed check reads in-range vectors instead, so that the step's barrier still completes)
+          if (!ATTN_IN_RANGE(voff + 127, vec_floats(p), p, 0x304)) voff = 0;
           bulk_load(sVec + st * T::VEC_BYTES, p.lse2 + voff, 512, barq);
           bulk_load(sVec + st * T::VEC_BYTES + 512, p.dvec + voff, 512, barq);
         }
@@ -493,7 +503,8 @@ __global__ void __launch_bounds__(384, 1)
       const int valid = seq_s[3] - 128 * j;
       if (p.vl.cu_q != nullptr && valid < 128) {
         named_bar_sync(3, 256 + 32);
-        if (*abort_flag == 0) {  // staging is complete unless a wait gave up
+        if (*abort_flag == 0 &&  // staging is complete unless a wait gave up
+            ATTN_IN_RANGE((long long)seq_s[2] + 128 * j + valid - 1, p.vl.total_k, p, 0x305)) {
           const uint32_t rs = (uint32_t)(p.Hkv * D);
           const long long off = ((long long)seq_s[2] + 128 * j) * rs + (long long)hk * D;
           store_rows_sw128<D>(sV, p.dv + off, rs, valid, lane, 32);

@@ -50,6 +50,7 @@ __device__ __noinline__ void no_key_vectors(const BwdParams& p, bool varlen, int
   if (threadIdx.x >= 128) return;
   const size_t vrow = (varlen ? (size_t)h * p.vec_stride + (size_t)varlen_vec_offset(q0, b) : (size_t)bh * p.Npad) +
                       (size_t)i * 128 + threadIdx.x;
+  if (!ATTN_IN_RANGE(vrow, vec_floats(p), p, 0x201)) return;
   p.dvec[vrow] = 0.f;
   p.lse2[vrow] = -INFINITY;
 }
@@ -140,7 +141,10 @@ __global__ void __launch_bounds__(384, 1)
       const uint32_t rs = varlen ? (uint32_t)(p.H * D) : (uint32_t)D;
       uint16_t* dst = varlen ? p.dq + ((long long)sq.q0 + 128 * i) * rs + (long long)h * D
                              : p.dq + ((long long)bh * p.N + 128 * i) * D;
-      zero_rows_bf16<D>(dst, rs, min(128, sq.nq - 128 * i));
+      if (ATTN_IN_RANGE(varlen ? (long long)sq.q0 + 128 * i + min(128, sq.nq - 128 * i) - 1
+                               : (long long)bh * p.N + 128 * i + min(128, sq.nq - 128 * i) - 1,
+                        varlen ? (long long)p.vl.total_q : (long long)p.B * p.H * p.N, p, 0x202))
+        zero_rows_bf16<D>(dst, rs, min(128, sq.nq - 128 * i));
       return;
     }
     if (threadIdx.x == 0) {
@@ -185,7 +189,10 @@ __global__ void __launch_bounds__(384, 1)
         const uint32_t rs = varlen ? (uint32_t)(p.H * D) : (uint32_t)D;
         uint16_t* dst = varlen ? p.dq + ((long long)seq_s[0] + 128 * i) * rs + (long long)h * D
                                : p.dq + ((long long)bh * p.N + 128 * i) * D;
-        zero_rows_bf16<D>(dst, rs, min(128, seq_s[1] - 128 * i));
+        if (ATTN_IN_RANGE(varlen ? (long long)seq_s[0] + 128 * i + min(128, seq_s[1] - 128 * i) - 1
+                                 : (long long)bh * p.N + 128 * i + min(128, seq_s[1] - 128 * i) - 1,
+                          varlen ? (long long)p.vl.total_q : (long long)p.B * p.H * p.N, p, 0x202))
+          zero_rows_bf16<D>(dst, rs, min(128, seq_s[1] - 128 * i));
         return;
       }
     }
@@ -235,7 +242,7 @@ __global__ void __launch_bounds__(384, 1)
     const uint32_t tdP = tmem + 256 + 64 * X + lane_off;
     const size_t vrow = (varlen ? (size_t)h * p.vec_stride + (size_t)varlen_vec_offset(seq_s[0], b)
                                 : (size_t)bh * p.Npad) + (size_t)i * 128 + r;
-    float l2, nD;  // -lse * log2(e) (-inf on padding rows: P = 0 there) and -D
+    float l2 = -INFINITY, nD = 0.f;  // -lse * log2(e) (-inf on padding rows: P = 0 there) and -D
     bool rows_ok = true;
     if (p.rows_in_dq) {
       // This kernel forms its rows' vectors itself and writes them for the
@@ -247,9 +254,11 @@ __global__ void __launch_bounds__(384, 1)
       // thread reaches the barriers below, whatever the waits return.
       const int row = 128 * i + r;
       // the row's lse first: its load overlaps the waits below
-      const float l = row < seq_s[1] ? (varlen ? p.lse[(size_t)h * p.vl.total_q + seq_s[0] + row]
-                                               : p.lse[(size_t)bh * p.N + row])
-                                     : -INFINITY;
+      const size_t lidx = varlen ? (size_t)h * p.vl.total_q + seq_s[0] + row : (size_t)bh * p.N + row;
+      const float l = (row < seq_s[1] && ATTN_IN_RANGE(lidx, varlen ? (size_t)p.H * p.vl.total_q
+                                                                      : (size_t)p.B * p.H * p.N, p, 0x203))
+                          ? p.lse[lidx]
+                          : -INFINITY;
       rows_ok = __all_sync(0xffffffffu, wait_bounded(wc, bQ, 0, wait_site(0x84, 0)) &&
                                             wait_bounded(wc, bO, 0, wait_site(0x85, 0)));
       float part = 0.f;
@@ -280,11 +289,13 @@ __global__ void __launch_bounds__(384, 1)
       asm volatile("" : "+r"(other));
       nD = row < seq_s[1] ? -(part + __uint_as_float(other)) : 0.f;
       l2 = (l == -INFINITY) ? -INFINITY : -l * 1.4426950408889634f;
-      if (X == 0 && rows_ok) {
-        p.dvec[vrow] = nD;
-        p.lse2[vrow] = l2;
+      size_t vst = vrow;
+      if (kDebugChecks && p.debug_plant == 2 && blockIdx.x == 0) vst += vec_floats(p);  // planted mistake (test of the checks)
+      if (X == 0 && rows_ok && ATTN_IN_RANGE(vst, vec_floats(p), p, 0x204)) {
+        p.dvec[vst] = nD;
+        p.lse2[vst] = l2;
       }
-    } else {
+    } else if (ATTN_IN_RANGE(vrow, vec_floats(p), p, 0x205)) {
       l2 = p.lse2[vrow];
       nD = p.dvec[vrow];
     }
@@ -314,16 +325,19 @@ __global__ void __launch_bounds__(384, 1)
       const uint32_t tS = tmem + (j & 1) * 128 + 64 * X + lane_off;
       uint2 bt = make_uint2(~0u, ~0u);
       const int jt = MASKED ? tile_at(j) : j;  // key tile relative to jlo
-      if (MASKED && rowbits != 0xffffffffu) bt = *reinterpret_cast<const uint2*>(p.mk.bits + rowbits + 4u * jt);
+      if (MASKED && rowbits != 0xffffffffu &&
+          ATTN_IN_RANGE((size_t)rowbits + 4u * jt + 1u, (size_t)p.mk.mask_b * p.mk.mask_h * p.N * p.mk.words, p, 0x206))
+        bt = *reinterpret_cast<const uint2*>(p.mk.bits + rowbits + 4u * jt);
       // The additive mask of this row over the warpgroup's 64 keys, loaded
       // before the wait for S; added as b / scale to the unscaled scores.
       // Columns past Nk are not read.
       float bb[MASKED >= 2 ? 64 : 1];
       if constexpr (MASKED >= 2) {
         const int row = 128 * i + r, k0 = (seq_s[4] + jt) * 128 + 64 * X;
-        load_bias_row<64, MASKED == 3>(
-            p.mk.bias, ((size_t)bias_plane(p.mk, b, h) * p.N + (size_t)row) * p.Nk + (size_t)k0,
-            row < seq_s[1] ? min(64, p.Nk - k0) : 0, bias_rows_vec(p.mk.bias, p.Nk, MASKED == 3), bb);
+        const size_t boff = ((size_t)bias_plane(p.mk, b, h) * p.N + (size_t)row) * p.Nk + (size_t)k0;
+        int bn = row < seq_s[1] ? min(64, p.Nk - k0) : 0;
+        if (bn > 0 && !ATTN_IN_RANGE(boff + bn - 1, (size_t)p.mk.bias_b * p.mk.bias_h * p.N * p.Nk, p, 0x207)) bn = 0;
+        load_bias_row<64, MASKED == 3>(p.mk.bias, boff, bn, bias_rows_vec(p.mk.bias, p.Nk, MASKED == 3), bb);
       }
       ok = __all_sync(0xffffffffu, wait_bounded(wc, bS + 8u * (j & 1), (j >> 1) & 1, wait_site(0x81, j)));
       if (!ok) break;
@@ -439,7 +453,8 @@ __global__ void __launch_bounds__(384, 1)
         }
       } else {
         const uint32_t rs = (uint32_t)(p.H * D);
-        store_rows_sw128<D>(sQ, p.dq + ((long long)q0 + 128 * i) * rs + (long long)h * D, rs, valid, threadIdx.x, 256);
+        if (ATTN_IN_RANGE((long long)q0 + 128 * i + valid - 1, p.vl.total_q, p, 0x208))
+          store_rows_sw128<D>(sQ, p.dq + ((long long)q0 + 128 * i) * rs + (long long)h * D, rs, valid, threadIdx.x, 256);
       }
     }
     setmaxnreg_dec<168>();

@@ -48,12 +48,13 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const BwdParams p) {
     o[it] = make_uint4(0, 0, 0, 0);
     g[it] = make_uint4(0, 0, 0, 0);
     lv[it] = -INFINITY;
-    if (i < p.N && c * 8 < p.d) {
+    if (i < p.N && c * 8 < p.d && ATTN_IN_RANGE(base + (size_t)i * p.d + 7, (size_t)p.B * p.H * p.N * p.d, p, 0x401)) {
       const size_t off = base + (size_t)i * p.d;
       o[it] = *reinterpret_cast<const uint4*>(p.o + off);
       g[it] = *reinterpret_cast<const uint4*>(p.dout + off);
     }
-    if (i < p.N && c == 0) lv[it] = p.lse[(size_t)bh * p.N + i];
+    if (i < p.N && c == 0 && ATTN_IN_RANGE((size_t)bh * p.N + i, (size_t)p.B * p.H * p.N, p, 0x402))
+      lv[it] = p.lse[(size_t)bh * p.N + i];
   }
 #pragma unroll
   for (int it = 0; it < PRE_IT; ++it) {
@@ -70,7 +71,7 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const BwdParams p) {
     for (int s = LPR / 2; s > 0; s >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, s);
     const long long row = row0 + it * RPW + sub;
     const int i = i0 + it * RPW;
-    if (c == 0 && row < rows) {
+    if (c == 0 && row < rows && ATTN_IN_RANGE(row, vec_floats(p), p, 0x403)) {
       const float l = lv[it];
       p.dvec[row] = (i < p.N) ? -dot : 0.f;
       p.lse2[row] = (l == -INFINITY) ? -INFINITY : -l * 1.4426950408889634f;
@@ -109,11 +110,12 @@ __global__ void __launch_bounds__(256) bwd_pre_varlen_kernel(const BwdParams p) 
       lv[it] = -INFINITY;
       if (i < sq.nq) {
         const size_t off = ((size_t)(sq.q0 + i) * p.H + h) * p.d + c * 8;
-        if (c * 8 < p.d) {
+        if (c * 8 < p.d && ATTN_IN_RANGE(off + 7, (size_t)p.vl.total_q * p.H * p.d, p, 0x401)) {
           o[it] = *reinterpret_cast<const uint4*>(p.o + off);
           g[it] = *reinterpret_cast<const uint4*>(p.dout + off);
         }
-        if (c == 0) lv[it] = p.lse[(size_t)h * p.vl.total_q + sq.q0 + i];
+        if (c == 0 && ATTN_IN_RANGE((size_t)h * p.vl.total_q + sq.q0 + i, (size_t)p.H * p.vl.total_q, p, 0x402))
+          lv[it] = p.lse[(size_t)h * p.vl.total_q + sq.q0 + i];
       }
     }
 #pragma unroll
@@ -129,7 +131,7 @@ __global__ void __launch_bounds__(256) bwd_pre_varlen_kernel(const BwdParams p) 
       }
 #pragma unroll
       for (int s = 8; s > 0; s >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, s);
-      if (c == 0) {
+      if (c == 0 && ATTN_IN_RANGE(vbase + k0 + 2 * it + sub, vec_floats(p), p, 0x403)) {
         const int k = k0 + 2 * it + sub;
         const float l = lv[it];
         p.dvec[vbase + k] = -dot;

@@ -225,7 +225,8 @@ __global__ void __launch_bounds__(kDecThreads, 2)
         tmem_ld32(tO + cc * 32, o);
         tmem_wait_ld();
         reg_fence(o);
-        if (live) {
+        if (live && ATTN_IN_RANGE(((long long)row * p.nsplit + split) * D + cc * 32 + 31,
+                                  (long long)p.B * p.H * p.Nq * p.nsplit * D, p, 0x501)) {
           // A row that saw no key of the chunk writes zeros, not 0 * O: a
           // chunk with no key tile at all (paged: past its sequence) never
           // ran a P V product, and its O columns hold whatever was there.
@@ -237,7 +238,7 @@ __global__ void __launch_bounds__(kDecThreads, 2)
                              : make_float4(0.f, 0.f, 0.f, 0.f);
         }
       }
-      if (live)
+      if (live && ATTN_IN_RANGE((long long)row * p.nsplit + split, (long long)p.B * p.H * p.Nq * p.nsplit, p, 0x502))
         p.lse_part[row * p.nsplit + split] = l > 0.f ? (m + log2f(l)) * 0.69314718055994531f : -INFINITY;
     }
   } else if (warp == 4) {
@@ -267,7 +268,7 @@ __global__ void __launch_bounds__(kDecThreads, 2)
           const int kp = key + piece * p.box_rows;
           const int lp = kp / p.page_size, off = kp % p.page_size;
           int page = p.num_pages;
-          if (kp < nkb) {
+          if (kp < nkb && ATTN_IN_RANGE((size_t)b * p.max_pages + lp, (size_t)p.B * p.max_pages, p, 0x503)) {
             page = p.block_table[(size_t)b * p.max_pages + lp];
             if (page < 0 || page >= p.num_pages) {
               atomicCAS(p.status, 0, kDevBadSeqlens);
@@ -376,6 +377,7 @@ __global__ void __launch_bounds__(128) decode_merge_kernel(const DecParams p) {
   __shared__ float wmax[4];
   const long long row = blockIdx.x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (!ATTN_IN_RANGE(row, (long long)p.B * p.H * p.Nq, p, 0x504)) return;  // (uniform over the block)
   const float* lp = p.lse_part + row * p.nsplit;
   float mx = -INFINITY;
   for (int s = threadIdx.x; s < p.nsplit; s += 128) mx = fmaxf(mx, lp[s]);

@@ -253,7 +253,9 @@ __global__ void __launch_bounds__(384, 1)
     for (int j = 0; j < n; ++j) {
       uint4 b4 = make_uint4(~0u, ~0u, ~0u, ~0u);
       const int jt = MASKED ? tile_at(j) : j;  // absolute key tile
-      if (MASKED && rowbits != 0xffffffffu) b4 = *reinterpret_cast<const uint4*>(p.mk.bits + rowbits + 4u * jt);
+      if (MASKED && rowbits != 0xffffffffu &&
+          ATTN_IN_RANGE((size_t)rowbits + 4u * jt + 3u, (size_t)p.mk.mask_b * p.mk.mask_h * p.Nq * p.mk.words, p, 0x101))
+        b4 = *reinterpret_cast<const uint4*>(p.mk.bits + rowbits + 4u * jt);
       // The additive mask of this row over the key tile, loaded before the
       // wait for S so that its latency hides behind the Q K^T MMA; added as
       // b / scale to the unscaled scores (scaled below: scale x + b); -inf
@@ -261,9 +263,10 @@ __global__ void __launch_bounds__(384, 1)
       float bb[MASKED >= 2 ? 128 : 1];
       if constexpr (MASKED >= 2) {
         const int row = qi * 128 + r;
-        load_bias_row<128, MASKED == 3>(
-            p.mk.bias, ((size_t)bias_plane(p.mk, b, h) * p.Nq + (size_t)row) * p.Nk + (size_t)jt * 128,
-            row < p.Nq ? min(128, p.Nk - jt * 128) : 0, bias_rows_vec(p.mk.bias, p.Nk, MASKED == 3), bb);
+        const size_t boff = ((size_t)bias_plane(p.mk, b, h) * p.Nq + (size_t)row) * p.Nk + (size_t)jt * 128;
+        int bn = row < p.Nq ? min(128, p.Nk - jt * 128) : 0;
+        if (bn > 0 && !ATTN_IN_RANGE(boff + bn - 1, (size_t)p.mk.bias_b * p.mk.bias_h * p.Nq * p.Nk, p, 0x102)) bn = 0;
+        load_bias_row<128, MASKED == 3>(p.mk.bias, boff, bn, bias_rows_vec(p.mk.bias, p.Nk, MASKED == 3), bb);
       }
       ok = __all_sync(0xffffffffu, wait_bounded(wc, barS, j & 1, wait_site(0x51 + s, j)));
       if (!ok) break;
@@ -456,8 +459,11 @@ __global__ void __launch_bounds__(384, 1)
       const int row = qi * 128 + r;
       // lse: (H, total_q) for a packed batch, (B, H, Nq) otherwise; the
       // query plane is the head there and b * H + h here.
-      const size_t lbase = packed ? (size_t)qplane * p.vl.total_q + q0 : (size_t)qplane * p.Nq;
-      if (row < nq) p.lse[lbase + row] = (m + log2f(l)) * 0.69314718055994531f;
+      size_t lbase = packed ? (size_t)qplane * p.vl.total_q + q0 : (size_t)qplane * p.Nq;
+      const size_t lsize = packed ? (size_t)p.H * p.vl.total_q : (size_t)p.B * p.H * p.Nq;
+      if (kDebugChecks && p.debug_plant == 1 && blockIdx.x == 0) lbase += lsize;  // planted mistake (test of the checks)
+      if (row < nq && ATTN_IN_RANGE(lbase + row, lsize, p, 0x103))
+        p.lse[lbase + row] = (m + log2f(l)) * 0.69314718055994531f;
     }
     setmaxnreg_dec<168>();  // one register budget again for the common teardown
   } else {
@@ -513,7 +519,8 @@ __global__ void __launch_bounds__(384, 1)
           named_bar_sync_c<3, 128 + 32>();
         else
           named_bar_sync_c<4, 128 + 32>();
-        if (*abort_flag == 0) {  // the staging is complete unless a wait gave up
+        if (*abort_flag == 0 &&  // the staging is complete unless a wait gave up
+            ATTN_IN_RANGE((long long)seq_s[0] + (2 * mt + s) * 128 + valid - 1, p.vl.total_q, p, 0x104)) {
           const uint32_t rs = (uint32_t)(p.H * D);
           store_rows_sw128<D>(sQ + s * T::TILE_BYTES,
                               p.o + ((long long)seq_s[0] + (2 * mt + s) * 128) * rs + (long long)seq_s[5] * D, rs,

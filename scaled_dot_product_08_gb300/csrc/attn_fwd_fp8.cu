@@ -271,7 +271,7 @@ __global__ void __launch_bounds__(384, 1)
         tmem_ld32(tO + cc * 32, o);
         tmem_wait_ld();
         reg_fence(o);
-        if (row < p.Nq) {
+        if (row < p.Nq && ATTN_IN_RANGE(((size_t)bh * p.Nq + row) * D + cc * 32 + 31, (size_t)p.B * p.H * p.Nq * D, p, 0x601)) {
 #pragma unroll
           for (int q4 = 0; q4 < 4; ++q4) {
             uint32_t w[4];
@@ -282,7 +282,8 @@ __global__ void __launch_bounds__(384, 1)
           }
         }
       }
-      if (row < p.Nq) p.lse[(size_t)bh * p.Nq + row] = (m + log2f(l) - 4.f) * 0.69314718055994531f;
+      if (row < p.Nq && ATTN_IN_RANGE((size_t)bh * p.Nq + row, (size_t)p.B * p.H * p.Nq, p, 0x602))
+        p.lse[(size_t)bh * p.Nq + row] = (m + log2f(l) - 4.f) * 0.69314718055994531f;
     }
     setmaxnreg_dec<168>();
   } else {

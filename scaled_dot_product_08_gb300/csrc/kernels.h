@@ -73,6 +73,7 @@ struct FwdParams {
   float o_scale;         // FP8: V's dequantisation factor, applied to O
   int debug_drop1;       // 0; n > 0 only in a test of the bounded waits: CTA 0's producer skips ring load n - 1
   int tail;              // heads in the level-major tail of the CTA order (work_unit); set by the launcher
+  int debug_plant;       // 0; 1 only in a test of the debug build's checks: CTA 0 offsets its lse store out of range
 };
 
 // Backward arguments.
@@ -100,6 +101,7 @@ struct BwdParams {
   MaskArgs mk;           // masked instances only
   int debug_drop1;       // 0; n > 0 only in a test of the bounded waits: CTA 0's producer skips ring load n - 1
   int tail;              // heads in the level-major tail of the CTA order (work_unit); set by each launcher
+  int debug_plant;       // 0; 2 only in a test of the debug build's checks: CTA 0 of the dQ kernel offsets its row-vector store out of range
 };
 
 // CTA order of the forward, dQ and dK/dV launches.  A launch's CTAs cover
@@ -160,6 +162,41 @@ struct DecParams {
 // Device status value for cu_seqlens that are out of range (a sequence longer
 // than the stated maximum, decreasing offsets, or past the packed length).
 constexpr int kDevBadSeqlens = 9;
+
+// Predicate checks of the debug build (-DATTN_DEBUG).  ATTN_IN_RANGE(i, n,
+// params, site) guards a plain global load or store whose element index i
+// a kernel computes: in the debug build it is 0 <= i < n, and a failure
+// records kDevCheckFailed in the device status word and, if it is the first
+// failure on the device, (site << 16, CTA, thread, i) in the record that
+// attn_get_timeout_info reads; the caller then skips the access.  No trap,
+// no assert: the launch completes and the context stays usable.  In the
+// release build the macro is `true` and its arguments are not evaluated.
+constexpr int kDevCheckFailed = 10;
+#ifdef ATTN_DEBUG
+__device__ __noinline__ inline bool check_failed(int* status, int* info, int site, long long i) {
+  if (atomicCAS(status, 0, kDevCheckFailed) == 0 && info != nullptr) {
+    info[0] = site << 16;
+    info[1] = (int)(blockIdx.x + gridDim.x * blockIdx.y);
+    info[2] = (int)threadIdx.x;
+    info[3] = (int)(i < -2147483647ll ? -2147483647ll : i > 2147483647ll ? 2147483647ll : i);
+  }
+  return false;
+}
+__device__ __forceinline__ bool in_range(long long i, long long n, int* status, int* info, int site) {
+  return (i >= 0 && i < n) ? true : check_failed(status, info, site, i);
+}
+#define ATTN_IN_RANGE(i, n, prm, site) \
+  ::sdpa::in_range((long long)(i), (long long)(n), (prm).status, (prm).info, (site))
+constexpr bool kDebugChecks = true;
+#else
+#define ATTN_IN_RANGE(i, n, prm, site) true
+constexpr bool kDebugChecks = false;
+#endif
+
+// Floats in each of the backward's row-vector arrays (-D, -lse2).
+__host__ __device__ inline size_t vec_floats(const BwdParams& p) {
+  return p.vl.cu_q != nullptr ? (size_t)p.H * p.vec_stride : (size_t)p.B * p.H * p.Npad;
+}
 
 // Varlen backward workspace: per head, sequence b's row vectors start at
 // float offset varlen_vec_offset(cu_q[b], b) (16-byte aligned) and span

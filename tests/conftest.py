@@ -22,3 +22,18 @@ def cuda_lib():
     import scaled_dot_product_08_gb300 as sdpa
     sdpa.load()
     return sdpa
+
+
+@pytest.fixture(autouse=True)
+def _no_failed_index_check(request):
+    """When the library under test is the debug build (SDPA08_LIBRARY names
+    it), every GPU test must end without a failed in-kernel index check."""
+    yield
+    if not os.environ.get("SDPA08_LIBRARY") or request.node.get_closest_marker("gpu") is None:
+        return
+    import scaled_dot_product_08_gb300 as sdpa
+    st = sdpa.load().attn_get_device_status(None)
+    if st == sdpa.Status.CHECK:
+        _, info = sdpa.attn_get_timeout_info(None)
+        pytest.fail(f"in-kernel index check failed: site {info[0] >> 16:#x}, CTA {info[1]}, thread {info[2]}, "
+                    f"index {info[3]}")
