@@ -224,7 +224,7 @@ attn_status_t attn_decode_paged(const void* q, const void* k_cache, const void* 
                                 int d, float scale, int causal, void* stream);
 
 /*
- * Forward with FP8 (e4m3) tensor-core products, head_dim 128.  Page "Flash
+ * Forward with FP8 (e4m3) tensor-core products, head_dim 64, 96 or 128.  Page "Flash
  * Attention原理" (§六 and FAQ Q8: FlashAttention-3 runs attention on FP8
  * tensor cores).  Q, K and V are e4m3 (1 sign, 4 exponent bits with bias 7,
  * 3 mantissa bits; no infinities) with one dequantisation factor each: the
@@ -232,11 +232,11 @@ attn_status_t attn_decode_paged(const void* q, const void* k_cache, const void* 
  * S accumulates in float32; the softmax is float32; P is rounded to e4m3 for
  * the P V product, which makes O approximate to about e4m3's precision
  * (3 mantissa bits) while lse keeps float32 accuracy.
- *   q [in]  e4m3 bytes (B, H, Nq, 128);  k, v [in] e4m3 bytes (B, Hkv, Nk, 128)
- *   o [out] bf16 (B, H, Nq, 128);  lse [out] float32 (B, H, Nq)
+ *   q [in]  e4m3 bytes (B, H, Nq, d);  k, v [in] e4m3 bytes (B, Hkv, Nk, d)
+ *   o [out] bf16 (B, H, Nq, d);  lse [out] float32 (B, H, Nq)
  *   scale   softmax scale; q_scale, k_scale, v_scale finite and > 0
- * Causal alignment and the Nq > Nk rule as attn_fwd_cross.  d != 128 gives
- * ATTN_ERR_UNSUPPORTED_SHAPE.
+ * Causal alignment and the Nq > Nk rule as attn_fwd_cross.  d outside
+ * {64, 96, 128} gives ATTN_ERR_UNSUPPORTED_SHAPE.
  */
 attn_status_t attn_fwd_fp8(const void* q, const void* k, const void* v, void* o, float* lse,
                            int B, int H, int Hkv, int Nq, int Nk, int d, float scale,

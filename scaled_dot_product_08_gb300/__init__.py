@@ -624,9 +624,9 @@ def backward_masked(q, k, v, o, lse, dout, scale: float | None = None, causal: b
 
 def forward_fp8(q8, k8, v8, q_scale: float, k_scale: float, v_scale: float, scale: float | None = None,
                 causal: bool = False):
-    """O (bf16), lse of attention on e4m3 inputs: q8 (B, H, Nq, 128), k8, v8
-    (B, Hkv, Nk, 128) uint8 CUDA tensors holding e4m3 bytes, each with its
-    dequantisation factor."""
+    """O (bf16), lse of attention on e4m3 inputs: q8 (B, H, Nq, d), k8, v8
+    (B, Hkv, Nk, d) uint8 CUDA tensors holding e4m3 bytes (d in {64, 96,
+    128}), each with its dequantisation factor."""
     import torch
     for t in (q8, k8, v8):
         if t.dim() != 4 or t.dtype != torch.uint8 or not t.is_contiguous() or not t.is_cuda:

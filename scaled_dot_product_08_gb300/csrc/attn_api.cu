@@ -162,11 +162,13 @@ bool make_map_bf16_packed(CUtensorMap* m, const void* ptr, int d, long long tota
 
 // 3-D map over a dense e4m3 (rows = B*heads, N, 128) byte tensor: box of 128
 // bytes x 128 rows x 1 head (one 128-byte swizzle block).
-bool make_map_e4m3(CUtensorMap* m, const void* ptr, int N, long long heads) {
+// e4m3 (B*heads, N, d) as planes of [N x d] bytes; boxes of 128 rows x 128
+// bytes, the bytes past d read as zeros.
+bool make_map_e4m3(CUtensorMap* m, const void* ptr, int d, int N, long long heads) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return false;
-  cuuint64_t dims[3] = {128, (cuuint64_t)N, (cuuint64_t)heads};
-  cuuint64_t strides[2] = {128, 128 * (cuuint64_t)N};
+  cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)N, (cuuint64_t)heads};
+  cuuint64_t strides[2] = {(cuuint64_t)d, (cuuint64_t)d * (cuuint64_t)N};
   cuuint32_t box[3] = {128, 128, 1};
   cuuint32_t estr[3] = {1, 1, 1};
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(ptr), dims, strides, box, estr,
@@ -705,7 +707,6 @@ attn_status_t attn_fwd_fp8(const void* q, const void* k, const void* v, void* o,
                            void* stream) {
   ATTN_TRY(check_shape(B, H, Hkv, Nq, d));
   ATTN_TRY(check_shape(B, H, Hkv, Nk, d));
-  if (d != 128) return ATTN_ERR_UNSUPPORTED_SHAPE;
   ATTN_TRY(check_scale_flag(scale, causal));
   for (float f : {q_scale, k_scale, v_scale})
     if (!std::isfinite(f) || !(f > 0.f)) return ATTN_ERR_INVALID_ARG;
@@ -715,8 +716,8 @@ attn_status_t attn_fwd_fp8(const void* q, const void* k, const void* v, void* o,
   DeviceInfo* di = nullptr;
   ATTN_TRY(current_device(&di));
   CUtensorMap tq, tk, tv;
-  if (!make_map_e4m3(&tq, q, Nq, (long long)B * H) || !make_map_e4m3(&tk, k, Nk, (long long)B * Hkv) ||
-      !make_map_e4m3(&tv, v, Nk, (long long)B * Hkv))
+  if (!make_map_e4m3(&tq, q, d, Nq, (long long)B * H) || !make_map_e4m3(&tk, k, d, Nk, (long long)B * Hkv) ||
+      !make_map_e4m3(&tv, v, d, Nk, (long long)B * Hkv))
     return ATTN_ERR_CUDA;
   sdpa::FwdParams p;
   memset(&p, 0, sizeof(p));
@@ -736,7 +737,7 @@ attn_status_t attn_fwd_fp8(const void* q, const void* k, const void* v, void* o,
   p.status = di->status;
   p.limit_ns = wait_limit_ns();
   p.info = di->info;
-  return sdpa::launch_fwd_fp8(causal != 0, tq, tk, tv, p, static_cast<cudaStream_t>(stream)) == cudaSuccess
+  return sdpa::launch_fwd_fp8(d, causal != 0, tq, tk, tv, p, static_cast<cudaStream_t>(stream)) == cudaSuccess
              ? ATTN_OK
              : ATTN_ERR_LAUNCH;
 }

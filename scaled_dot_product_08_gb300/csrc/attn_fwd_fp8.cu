@@ -1,5 +1,5 @@
 // attn_fwd_fp8.cu — forward of exact attention with FP8 (e4m3) tensor-core
-// products on sm_103a, head_dim 128.
+// products on sm_103a, head_dim 64, 96 or 128.
 //
 // Method: the forward of attn_fwd.cu (page "Flash Attention原理", §三 tiling,
 // §四 online softmax, §五 only O and the row statistic leave the chip), with
@@ -18,13 +18,16 @@
 //
 // GB300 mapping: the bf16 forward's warp roles, barriers and tensor-memory
 // plan, with e4m3 tiles of [128 rows x 128 bytes] (one 128-byte swizzle
-// block per tile, half the bf16 bytes), so the K/V ring holds 10 stages:
+// block per tile, half the bf16 bytes), so the K/V ring holds 10 stages.
+// At d = 64 / 96 a row's d bytes fill the start of its 128-byte line and the
+// TMA box fills the rest with zeros; Q K^T runs d / 32 K-steps and P V has
+// N = d, so the padding costs shared memory, not MMA work:
 //   warps 0-7  softmax (warpgroup s = query tile s of the CTA's pair)
 //   warp  8    TMA producer (Q tiles once, then K_j / V_j)
 //   warp  9    MMA issuer
 //   warps 10-11 idle
 // Tensor memory: [0,128) S0, P0 (e4m3, 4 per column) over its first 32
-// columns; [128,256) S1 / P1; [256,384) O0; [384,512) O1 (fp32).
+// columns; [128,256) S1 / P1; [256,256+d) O0; [384,384+d) O1 (fp32).
 #include <cmath>
 
 #include <cuda_fp8.h>
@@ -36,8 +39,9 @@ namespace sdpa {
 
 namespace {
 
+template <int D_>
 struct F8 {
-  static constexpr int D = 128;
+  static constexpr int D = D_;
   static constexpr int TILE_BYTES = 128 * 128;  // [128 rows x 128 e4m3]
   static constexpr int NSTAGE = 10;             // K/V ring depth
   static constexpr int KSTEPS = D / 32;         // K = 32 per e4m3 MMA
@@ -82,12 +86,11 @@ __device__ __forceinline__ uint32_t pack_e4m3x4(float a, float b, float c, float
   return lo | (hi << 16);
 }
 
-template <bool CAUSAL>
+template <int D, bool CAUSAL>
 __global__ void __launch_bounds__(384, 1)
     fwd_fp8_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                    const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
-  using T = F8;
-  constexpr int D = T::D;
+  using T = F8<D>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -414,24 +417,31 @@ __global__ void __launch_bounds__(384, 1)
   }
 }
 
-template <bool C>
+template <int D, bool C>
 cudaError_t launch_fp8_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const FwdParams& p,
                          cudaStream_t stream) {
-  auto kern = fwd_fp8_kernel<C>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, F8::SMEM);
+  using F = F8<D>;
+  auto kern = fwd_fp8_kernel<D, C>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, F::SMEM);
   if (e != cudaSuccess) return e;
   const unsigned grid = (unsigned)p.n_mtiles * (unsigned)(p.B * p.H);
   FwdParams pc = p;
   pc.tail = order_tail(p.n_mtiles, p.B * p.H, p.G);
-  kern<<<grid, F8::THREADS, F8::SMEM, stream>>>(tq, tk, tv, pc);
+  kern<<<grid, F::THREADS, F::SMEM, stream>>>(tq, tk, tv, pc);
   return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_fwd_fp8(bool causal, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+cudaError_t launch_fwd_fp8(int d, bool causal, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                            const FwdParams& p, cudaStream_t stream) {
-  return causal ? launch_fp8_t<true>(tq, tk, tv, p, stream) : launch_fp8_t<false>(tq, tk, tv, p, stream);
+  switch (d) {
+    case 64: return causal ? launch_fp8_t<64, true>(tq, tk, tv, p, stream) : launch_fp8_t<64, false>(tq, tk, tv, p, stream);
+    case 96: return causal ? launch_fp8_t<96, true>(tq, tk, tv, p, stream) : launch_fp8_t<96, false>(tq, tk, tv, p, stream);
+    case 128:
+      return causal ? launch_fp8_t<128, true>(tq, tk, tv, p, stream) : launch_fp8_t<128, false>(tq, tk, tv, p, stream);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 }  // namespace sdpa

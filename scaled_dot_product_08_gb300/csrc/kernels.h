@@ -306,9 +306,10 @@ size_t decode_smem_bytes(int d);
 cudaError_t launch_fwd(int d, bool causal, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                        const CUtensorMap& to, const FwdParams& p, cudaStream_t stream, bool masked = false);
 
-// FP8 (e4m3) forward, head_dim 128, dense (B, H, N, 128) e4m3 Q, K, V (maps
-// of bytes), O bf16 through p.o; p.scale_log2 carries q_scale * k_scale.
-cudaError_t launch_fwd_fp8(bool causal, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+// FP8 (e4m3) forward, head_dim d in {64, 96, 128}, dense (B, H, N, d) e4m3
+// Q, K, V (maps of bytes, boxes of 128 x 128 bytes zero-filled past d), O
+// bf16 through p.o; p.scale_log2 carries q_scale * k_scale.
+cudaError_t launch_fwd_fp8(int d, bool causal, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                            const FwdParams& p, cudaStream_t stream);
 
 cudaError_t launch_bwd_prep(const BwdParams& p, cudaStream_t stream);

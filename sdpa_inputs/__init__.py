@@ -48,7 +48,8 @@ backward, self-attention (the same lengths for queries and keys):
        K, V, dO use default_rng(seed + 1000) in that order.
 
 FP8 forward (attn_fwd_fp8): c4f8 is c4's draw (seed 4, x0.5) quantised per
-tensor to e4m3 (quantize_e4m3: scale = amax / 448).
+tensor to e4m3 (quantize_e4m3: scale = amax / 448); c3cf8 is c3c's draw
+(seed 3, head_dim 64, causal) quantised the same way.
 
 Masked workloads (attn_fwd_masked / attn_bwd_masked), forward + backward:
 
@@ -127,6 +128,7 @@ WORKLOADS: dict[str, Workload] = {
     "cx": Workload("cx", 8, 16, 16, 4096, 128, False, 9, with_grad=True, Nq=2048, kind="cross"),
     "vl1": Workload("vl1", 1, 16, 16, 32768, 128, True, 10, with_grad=True, kind="varlen", len_range=(128, 8192)),
     "c4f8": Workload("c4f8", 1, 32, 8, 8192, 128, True, 4, amp=0.5, kind="fp8"),
+    "c3cf8": Workload("c3cf8", 1, 96, 96, 4096, 64, True, 3, kind="fp8"),
     "sw1": Workload("sw1", 1, 32, 8, 16384, 128, True, 11, with_grad=True, kind="masked", window=(4095, -1)),
     "pl1": Workload("pl1", 8, 16, 16, 4096, 128, False, 12, with_grad=True, kind="masked", prefix=1024),
     "ab1": Workload("ab1", 8, 16, 16, 4096, 128, False, 13, with_grad=True, kind="masked", bias_slope=1 / 64),

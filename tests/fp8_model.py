@@ -31,6 +31,9 @@ SHAPES = [
     (1, 2, 1, 129, 129, 128),
     (1, 4, 4, 256, 1024, 128),   # cross: Nq < Nk
     (1, 2, 2, 1, 300, 128),      # one query row
+    (1, 2, 2, 512, 512, 64),     # head_dim 64
+    (2, 3, 1, 333, 333, 96),     # head_dim 96, ragged, GQA
+    (1, 2, 2, 200, 640, 64),     # head_dim 64, cross: Nq < Nk
 ]
 
 LOG2E = 1.0 / math.log(2.0)

@@ -285,7 +285,8 @@ def test_fp8_rejects_bad_arguments(lib):
     S = sdpa.Status
     f = lambda d=128, scale=0.1, qs=1.0, ks=1.0, vs=1.0, causal=0, Nq=100, Nk=200: sdpa.attn_fwd_fp8(
         FAKE, FAKE, FAKE, FAKE, FAKE, 1, 4, 2, Nq, Nk, d, scale, qs, ks, vs, causal, None)
-    assert f(d=64) == S.UNSUPPORTED_SHAPE
+    assert f(d=80) == S.UNSUPPORTED_SHAPE  # head_dim 64, 96 and 128 are served
+    assert f(d=256) == S.UNSUPPORTED_SHAPE
     assert f(qs=0.0) == S.INVALID_ARG
     assert f(vs=float("inf")) == S.INVALID_ARG
     assert f(ks=-1.0) == S.INVALID_ARG

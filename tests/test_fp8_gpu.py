@@ -74,6 +74,6 @@ def test_fp8_forward_score_ranges(cuda_lib, amp):
 
 def test_fp8_rejects_other_head_dims(cuda_lib):
     import torch
-    z = torch.zeros((1, 1, 16, 64), dtype=torch.uint8, device="cuda")
+    z = torch.zeros((1, 1, 16, 80), dtype=torch.uint8, device="cuda")
     with pytest.raises(cuda_lib.AttnError):
         cuda_lib.forward_fp8(z, z, z, 1.0, 1.0, 1.0)

@@ -126,10 +126,11 @@ def test_masked_fwd_bwd(cuda_lib, name):
     _check_parts(name, _run_pool(masked_head, tasks, 12 * w.N * w.N * 8), grads=True)
 
 
-def test_c4f8_fp8(cuda_lib):
+@pytest.mark.parametrize("name", ["c4f8", "c3cf8"])
+def test_fp8_full_size(cuda_lib, name):
     import torch
     from tests.fp8_model import FP8_MODEL_REL_FRO, O_MEAN_ABS_FP8, O_REL_FRO_FP8
-    w = workload("c4f8")
+    w = workload(name)
     x = make_inputs(w)
     qz = [quantize_e4m3(x[n]) for n in ("q", "k", "v")]
     u8 = lambda a: torch.from_numpy(a).cuda()
@@ -144,7 +145,7 @@ def test_c4f8_fp8(cuda_lib):
     worst, worst_m = max(p["rel_fro"] for p in parts), max(p["rel_fro_model"] for p in parts)
     mean = sum(p["o_sum"] for p in parts) / sum(p["o_n"] for p in parts)
     lmax = max(p["lse_max"] for p in parts)
-    print(f"\nc4f8: {len(parts)} heads: worst rel Frobenius {worst:.3e} (against the rounding model {worst_m:.3e}),"
+    print(f"\n{name}: {len(parts)} heads: worst rel Frobenius {worst:.3e} (against the rounding model {worst_m:.3e}),"
           f" mean |err| {mean:.3e}, lse max {lmax:.3e}", end="")
     assert all(p["finite"] for p in parts)
     assert worst <= O_REL_FRO_FP8 and worst_m <= FP8_MODEL_REL_FRO
