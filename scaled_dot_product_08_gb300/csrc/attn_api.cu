@@ -160,8 +160,6 @@ bool make_map_bf16_packed(CUtensorMap* m, const void* ptr, int d, long long tota
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// 3-D map over a dense e4m3 (rows = B*heads, N, 128) byte tensor: box of 128
-// bytes x 128 rows x 1 head (one 128-byte swizzle block).
 // e4m3 (B*heads, N, d) as planes of [N x d] bytes; boxes of 128 rows x 128
 // bytes, the bytes past d read as zeros.
 bool make_map_e4m3(CUtensorMap* m, const void* ptr, int d, int N, long long heads) {
@@ -886,7 +884,14 @@ attn_status_t attn_fwd_masked(const void* q, const void* k, const void* v, void*
       sdpa::launch_mask_pack(static_cast<const uint8_t*>(mask->mask), mask->mask_batch, mask->mask_heads, Nq, Nk,
                              bits, g.words, nullptr, 0, flags, st) != cudaSuccess)
     return ATTN_ERR_LAUNCH;
-  return sdpa::launch_fwd(d, false, tq, tk, tv, to, p, st, true) == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;
+  // A bf16 additive mask whose rows are whole 16-byte units arrives by TMA
+  // (a map over its planes of [Nq x Nk]); any other goes through per-thread loads.
+  CUtensorMap tb;
+  const bool staged = mask->bias != nullptr && mask->bias_bf16 && Nk % 8 == 0 && aligned16(mask->bias);
+  if (staged && !make_map_bf16(&tb, mask->bias, Nk, Nq, (long long)p.mk.bias_b * p.mk.bias_h)) return ATTN_ERR_CUDA;
+  return sdpa::launch_fwd(d, false, tq, tk, tv, to, p, st, true, staged ? &tb : nullptr) == cudaSuccess
+             ? ATTN_OK
+             : ATTN_ERR_LAUNCH;
 }
 
 attn_status_t attn_bwd_masked_stages(const void* q, const void* k, const void* v, const void* o, const float* lse,

@@ -37,27 +37,33 @@
 
 namespace sdpa {
 
-template <int D>
+// BT: the instance whose bf16 additive mask arrives by TMA, one [128 x 128]
+// bf16 tile (32 KB, two 128-byte swizzle blocks) per query tile, staged in
+// shared memory that fewer K/V ring stages leave free.
+template <int D, bool BT = false>
 struct FwdTraits {
   static constexpr int NB = (D + 63) / 64;           // 64-column (128-byte) blocks per row
   static constexpr int BLOCK_BYTES = 128 * 128;      // [128 rows x 128 B]
   static constexpr int TILE_BYTES = NB * BLOCK_BYTES;
-  static constexpr int NSTAGE = (D == 64) ? 8 : 5;   // K/V ring depth
+  static constexpr int NSTAGE = BT ? (D == 64 ? 7 : 3) : (D == 64 ? 8 : 5);  // K/V ring depth
+  static constexpr int BIAS_BYTES = BT ? 2 * 32768 : 0;
   static constexpr int KSTEPS = D / 16;              // K=16 steps of Q K^T
-  static constexpr int NBAR = 2 + 2 * NSTAGE + 2 + 4 + 2 + 1;
+  static constexpr int NBAR = 2 + 2 * NSTAGE + 2 + 4 + 2 + 1 + (BT ? 4 : 0);
   static constexpr int MISC = 64;                    // tmem slot, abort flag, per-CTA sequence values
-  static constexpr int SMEM = 1024 + (2 + NSTAGE) * TILE_BYTES + NBAR * 8 + MISC + 2 * kMaxTileList;
+  static constexpr int SMEM = 1024 + (2 + NSTAGE) * TILE_BYTES + BIAS_BYTES + NBAR * 8 + MISC + 2 * kMaxTileList;
   static constexpr int THREADS = 384;
 };
 
 // MASKED: the instance that applies p.mk (sliding window, key lengths, a
-// bit mask), with causal entering as wr = 0; CAUSAL is then false.
+// bit mask), with causal entering as wr = 0; CAUSAL is then false.  1: no
+// additive mask; 2: a float32 one, 3: a bf16 one, each thread loading its
+// rows from global memory; 4: a bf16 one staged by TMA (tmB, warp 10).
 template <int D, bool CAUSAL, int MASKED>
 __global__ void __launch_bounds__(384, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
-               const FwdParams p) {
-  using T = FwdTraits<D>;
+               const __grid_constant__ CUtensorMap tmB, const FwdParams p) {
+  using T = FwdTraits<D, MASKED == 4>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -65,7 +71,8 @@ __global__ void __launch_bounds__(384, 1)
 
   const uint32_t sQ = base;                          // 2 query tiles
   const uint32_t sKV = base + 2 * T::TILE_BYTES;     // K/V ring
-  const uint32_t sBar = sKV + T::NSTAGE * T::TILE_BYTES;
+  const uint32_t sBias = sKV + T::NSTAGE * T::TILE_BYTES;  // MASKED == 4: bias tiles of query tiles 0, 1
+  const uint32_t sBar = sBias + T::BIAS_BYTES;
   const uint32_t bQ = sBar;                          // q_full[2]
   const uint32_t bKVf = sBar + 8u * 2;               // kv_full[NSTAGE]
   const uint32_t bKVe = bKVf + 8u * T::NSTAGE;       // kv_empty[NSTAGE]
@@ -73,6 +80,8 @@ __global__ void __launch_bounds__(384, 1)
   const uint32_t bP = bS + 16u;                      // p_full[2][2] (tile, half of the keys)
   const uint32_t bO = bP + 32u;                      // o_full[2]
   const uint32_t bDrain = bO + 16u;
+  const uint32_t bBf = bDrain + 8u;                  // bias_full[2] (MASKED == 4)
+  const uint32_t bBe = bBf + 16u;                    // bias_empty[2] (MASKED == 4)
   uint8_t* const misc = gbase + (sBar - base) + 8 * T::NBAR;
   uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(misc);
   volatile int* const abort_flag = reinterpret_cast<volatile int*>(misc + 4);
@@ -192,6 +201,12 @@ __global__ void __launch_bounds__(384, 1)
       mbar_init(bKVe + 8u * i, 1);
     }
     mbar_init(bDrain, 1);
+    if (MASKED == 4) {
+      for (int s = 0; s < 2; ++s) {
+        mbar_init(bBf + 8u * s, 1);
+        mbar_init(bBe + 8u * s, 128);
+      }
+    }
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -260,8 +275,8 @@ __global__ void __launch_bounds__(384, 1)
       // wait for S so that its latency hides behind the Q K^T MMA; added as
       // b / scale to the unscaled scores (scaled below: scale x + b); -inf
       // hides the key.  Columns past Nk are not read (the bounds hide them).
-      float bb[MASKED >= 2 ? 128 : 1];
-      if constexpr (MASKED >= 2) {
+      float bb[MASKED == 2 || MASKED == 3 ? 128 : 1];
+      if constexpr (MASKED == 2 || MASKED == 3) {
         const int row = qi * 128 + r;
         const size_t boff = ((size_t)bias_plane(p.mk, b, h) * p.Nq + (size_t)row) * p.Nk + (size_t)jt * 128;
         int bn = row < p.Nq ? min(128, p.Nk - jt * 128) : 0;
@@ -291,9 +306,27 @@ __global__ void __launch_bounds__(384, 1)
           x[96 + i] = __uint_as_float(rd[i]);
         }
       }
-      if constexpr (MASKED >= 2) {
+      if constexpr (MASKED == 2 || MASKED == 3) {
 #pragma unroll
         for (int i = 0; i < 128; ++i) x[i] = fmaf(bb[i], p.mk.inv_scale, x[i]);
+      } else if constexpr (MASKED == 4) {
+        // This row of the staged bias tile (rows past Nq and columns past
+        // Nk read as zeros), added 8 columns at a time; the tile is then
+        // released to warp 10 for the next key tile.
+        ok = __all_sync(0xffffffffu, wait_bounded(wc, bBf + 8u * s, j & 1, wait_site(0x55 + s, j)));
+        if (!ok) break;
+        const uint32_t sb = sBias + 32768u * s;
+#pragma unroll
+        for (int ch = 0; ch < 16; ++ch) {
+          const uint4 u = ld_shared_v4u(sb + (ch >> 3) * 16384u + sw128_offset(r, ch & 7));
+          const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            x[8 * ch + 2 * e] = fmaf(__uint_as_float(w[e] << 16), p.mk.inv_scale, x[8 * ch + 2 * e]);
+            x[8 * ch + 2 * e + 1] = fmaf(__uint_as_float(w[e] & 0xffff0000u), p.mk.inv_scale, x[8 * ch + 2 * e + 1]);
+          }
+        }
+        mbar_arrive(bBe + 8u * s);
       }
       bool edge;  // some row of the warp has hidden columns in this tile (warp-uniform)
       if (MASKED) {
@@ -510,6 +543,35 @@ __global__ void __launch_bounds__(384, 1)
         }
       }
       __syncwarp();
+    } else if (MASKED == 4 && warp == 10) {
+      // ------------------------------------------------------------ bias producer
+      // The bias tile of query tile s over key tile tile_at(j), once the
+      // softmax warpgroup has read the previous one (one buffer per query
+      // tile; it reads a tile right after its scores arrive, so the next
+      // load has the rest of that step to land).  Masked calls carry no
+      // packed batch, so this warp has no partial O tile to store.
+      if (lane == 0) {
+        const int n0 = ntiles(0), n1 = ntiles(1), plane = bias_plane(p.mk, b, h);
+        tma_prefetch_desc(&tmB);
+        bool ok = true;
+        int issued[2] = {0, 0};
+        for (int j = 0; j < n1 && ok; ++j) {
+          const int jt = tile_at(j);
+          for (int s = 0; s < 2 && ok; ++s) {
+            if (j >= (s ? n1 : n0)) continue;
+            if (j > 0 && !(ok = wait_bounded(wc, bBe + 8u * s, (j - 1) & 1, wait_site(0x62 + s, j)))) break;
+            mbar_expect_tx(bBf + 8u * s, 32768);
+            for (int cb = 0; cb < 2; ++cb)
+              tma_load_3d(sBias + 32768u * s + 16384u * cb, &tmB, bBf + 8u * s, jt * 128 + 64 * cb,
+                          (2 * mt + s) * 128, plane);
+            issued[s] = j + 1;
+          }
+        }
+        // Every copy issued above has landed before the CTA may exit.
+        for (int s = 0; s < 2; ++s)
+          if (issued[s] > 0) wait_drain(bBf + 8u * s, (issued[s] - 1) & 1, p.limit_ns);
+      }
+      __syncwarp();
     } else if (warp >= 10) {
       // ------------------------------------------------------------ partial O tile (packed batch)
       const int s = warp - 10;
@@ -639,40 +701,50 @@ size_t fwd_smem_bytes(int d) {
 
 template <int D, bool C, int M = 0>
 static cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                                const CUtensorMap& to, const FwdParams& p, cudaStream_t stream) {
+                                const CUtensorMap& to, const CUtensorMap& tb, const FwdParams& p,
+                                cudaStream_t stream) {
+  using T = FwdTraits<D, M == 4>;
   auto kern = fwd_kernel<D, C, M>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, FwdTraits<D>::SMEM);
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, T::SMEM);
   if (e != cudaSuccess) return e;
   const unsigned grid = (unsigned)p.n_mtiles * (unsigned)(p.B * p.H);
   FwdParams pc = p;
   pc.tail = order_tail(p.n_mtiles, p.B * p.H, p.G);
-  kern<<<grid, FwdTraits<D>::THREADS, FwdTraits<D>::SMEM, stream>>>(tq, tk, tv, to, pc);
+  kern<<<grid, T::THREADS, T::SMEM, stream>>>(tq, tk, tv, to, tb, pc);
   return cudaGetLastError();
 }
 
 cudaError_t launch_fwd(int d, bool causal, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                       const CUtensorMap& to, const FwdParams& p, cudaStream_t stream, bool masked) {
+                       const CUtensorMap& to, const FwdParams& p, cudaStream_t stream, bool masked,
+                       const CUtensorMap* tb) {
+  const CUtensorMap& b = tb != nullptr ? *tb : to;  // (unused by the instances without a staged bias)
+#define SDPA_FWD(DD, CC, MM) launch_fwd_t<DD, CC, MM>(tq, tk, tv, to, b, p, stream)
   if (masked) {
-    const bool bias = p.mk.bias != nullptr;  // the instances with the additive mask (float32, bf16)
-    switch (d) {
-      case 64: return bias ? (p.mk.bias_bf16 ? launch_fwd_t<64, false, 3>(tq, tk, tv, to, p, stream) : launch_fwd_t<64, false, 2>(tq, tk, tv, to, p, stream))
-                      : launch_fwd_t<64, false, 1>(tq, tk, tv, to, p, stream);
-      case 96: return bias ? (p.mk.bias_bf16 ? launch_fwd_t<96, false, 3>(tq, tk, tv, to, p, stream) : launch_fwd_t<96, false, 2>(tq, tk, tv, to, p, stream))
-                      : launch_fwd_t<96, false, 1>(tq, tk, tv, to, p, stream);
-      case 128: return bias ? (p.mk.bias_bf16 ? launch_fwd_t<128, false, 3>(tq, tk, tv, to, p, stream) : launch_fwd_t<128, false, 2>(tq, tk, tv, to, p, stream))
-                      : launch_fwd_t<128, false, 1>(tq, tk, tv, to, p, stream);
+    // The additive mask: float32, bf16 loaded by each thread, or bf16 staged by TMA (tb given).
+    const int mode = p.mk.bias == nullptr ? 1 : !p.mk.bias_bf16 ? 2 : tb == nullptr ? 3 : 4;
+    switch (d * 8 + mode) {
+      case 64 * 8 + 1: return SDPA_FWD(64, false, 1);
+      case 64 * 8 + 2: return SDPA_FWD(64, false, 2);
+      case 64 * 8 + 3: return SDPA_FWD(64, false, 3);
+      case 64 * 8 + 4: return SDPA_FWD(64, false, 4);
+      case 96 * 8 + 1: return SDPA_FWD(96, false, 1);
+      case 96 * 8 + 2: return SDPA_FWD(96, false, 2);
+      case 96 * 8 + 3: return SDPA_FWD(96, false, 3);
+      case 96 * 8 + 4: return SDPA_FWD(96, false, 4);
+      case 128 * 8 + 1: return SDPA_FWD(128, false, 1);
+      case 128 * 8 + 2: return SDPA_FWD(128, false, 2);
+      case 128 * 8 + 3: return SDPA_FWD(128, false, 3);
+      case 128 * 8 + 4: return SDPA_FWD(128, false, 4);
       default: return cudaErrorInvalidValue;
     }
   }
   switch (d) {
-    case 64: return causal ? launch_fwd_t<64, true>(tq, tk, tv, to, p, stream)
-                           : launch_fwd_t<64, false>(tq, tk, tv, to, p, stream);
-    case 96: return causal ? launch_fwd_t<96, true>(tq, tk, tv, to, p, stream)
-                           : launch_fwd_t<96, false>(tq, tk, tv, to, p, stream);
-    case 128: return causal ? launch_fwd_t<128, true>(tq, tk, tv, to, p, stream)
-                            : launch_fwd_t<128, false>(tq, tk, tv, to, p, stream);
+    case 64: return causal ? SDPA_FWD(64, true, 0) : SDPA_FWD(64, false, 0);
+    case 96: return causal ? SDPA_FWD(96, true, 0) : SDPA_FWD(96, false, 0);
+    case 128: return causal ? SDPA_FWD(128, true, 0) : SDPA_FWD(128, false, 0);
     default: return cudaErrorInvalidValue;
   }
+#undef SDPA_FWD
 }
 
 }  // namespace sdpa

@@ -303,8 +303,12 @@ size_t bwd_dq_smem_bytes(int d);
 size_t decode_smem_bytes(int d);
 
 // masked: the instance that applies p.mk (causal then enters as wr = 0).
+// tb (masked, bf16 additive mask only): a map over the mask as (planes, Nq,
+// Nk) bf16 with boxes of 128 rows x 64 columns, 128-byte swizzle; given, the
+// kernel stages the mask's tiles by TMA instead of per-thread loads.
 cudaError_t launch_fwd(int d, bool causal, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                       const CUtensorMap& to, const FwdParams& p, cudaStream_t stream, bool masked = false);
+                       const CUtensorMap& to, const FwdParams& p, cudaStream_t stream, bool masked = false,
+                       const CUtensorMap* tb = nullptr);
 
 // FP8 (e4m3) forward, head_dim d in {64, 96, 128}, dense (B, H, N, d) e4m3
 // Q, K, V (maps of bytes, boxes of 128 x 128 bytes zero-filled past d), O

@@ -224,6 +224,9 @@ BIAS_CASES = [
     ((1, 4, 4, 513, 513, 64), False, None, None, None, "shared"),   # one plane for all
     ((2, 2, 1, 260, 700, 96), True, None, None, None, "batch"),     # Nq < Nk, GQA
     ((2, 4, 2, 384, 384, 128), True, (150, -1), [384, 200], "batch", "head"),  # with every other mask
+    # Nk a multiple of 8: a bf16 bias is staged by TMA (the others load it per thread)
+    ((1, 4, 4, 520, 520, 64), False, None, None, None, "shared"),   # ragged last key tile
+    ((2, 2, 1, 264, 712, 96), True, None, None, None, "batch"),     # Nq < Nk, GQA
 ]
 
 
@@ -286,3 +289,25 @@ def test_rows_whose_bias_hides_every_key(cuda_lib):
     _check_forward(O, lse, Or, lr, "bias dead rows")
     check_grads([host(x) for x in g], oracle.attention_masked_backward(q, k, v, do, 0.125, False, None, None, None,
                                                                       bias), "bias dead rows")
+
+
+@pytest.mark.parametrize("shape,causal", [((2, 4, 2, 300, 384, 128), True), ((1, 2, 2, 520, 520, 64), False)])
+def test_bf16_bias_staged_equals_loaded(cuda_lib, shape, causal):
+    """A bf16 additive mask with Nk a multiple of 8 on a 16-byte boundary is
+    staged by TMA; the same values one element into a buffer (2-byte aligned)
+    go through per-thread loads.  Both add the same values in the same order:
+    O and lse agree bit for bit."""
+    import torch
+    B, H, Hkv, Nq, Nk, d = shape
+    q, k, v, _ = _problem(B, H, Hkv, Nq, Nk, d, 49500 + Nq)
+    bias = round_bf16(_bias((1, H, Nq, Nk), 49600 + Nq))
+    s = 1 / math.sqrt(d)
+    staged = _t(bias, torch.bfloat16)
+    buf = torch.zeros(bias.size + 8, dtype=torch.bfloat16, device="cuda")
+    buf[1:1 + bias.size] = staged.reshape(-1)
+    loaded = buf[1:1 + bias.size].view(1, H, Nq, Nk)
+    assert staged.data_ptr() % 16 == 0 and loaded.data_ptr() % 16 != 0
+    tq, tk, tv = dev(q), dev(k), dev(v)
+    O1, l1 = cuda_lib.forward_masked(tq, tk, tv, s, causal, None, None, None, staged)
+    O2, l2 = cuda_lib.forward_masked(tq, tk, tv, s, causal, None, None, None, loaded)
+    assert torch.equal(O1, O2) and torch.equal(l1, l2)
