@@ -949,7 +949,13 @@ attn_status_t attn_bwd_masked_stages(const void* q, const void* k, const void* v
     pr.rows_in_dq = 1;
     if (sdpa::launch_bwd_dq(d, false, tq, tk, tv, tdo, tdq, to, pr, st, true) != cudaSuccess) return ATTN_ERR_LAUNCH;
   }
-  if ((stages & kStageGrad) && sdpa::launch_bwd_grad(d, false, tq, tk, tv, tdo, tdk, tdv, p, st, true) != cudaSuccess)
+  // A bf16 additive mask without a boolean mask reaches the dK/dV kernel by
+  // TMA when the rows of its transpose are whole 16-byte units.
+  CUtensorMap tbt;
+  const bool staged_t = mask->bias != nullptr && mask->bias_bf16 && mask->mask == nullptr && Nq % 8 == 0;
+  if (staged_t && !make_map_bf16(&tbt, bias_t, Nq, Nk, (long long)g.bias_planes)) return ATTN_ERR_CUDA;
+  if ((stages & kStageGrad) &&
+      sdpa::launch_bwd_grad(d, false, tq, tk, tv, tdo, tdk, tdv, p, st, true, staged_t ? &tbt : nullptr) != cudaSuccess)
     return ATTN_ERR_LAUNCH;
   if ((stages & kStageDq) && sdpa::launch_bwd_dq(d, false, tq, tk, tv, tdo, tdq, to, p, st, true) != cudaSuccess)
     return ATTN_ERR_LAUNCH;

@@ -30,7 +30,10 @@
 //   warp  9     MMA issuer (one elected lane issues)
 //   warp  10    TMA producer: dO_i (its own loop, so a busy dO stage never
 //               delays the next Q_i)
-//   warp  11    stores the last, partial dK / dV tile of a packed sequence
+//   warp  11    stores the last, partial dK / dV tile of a packed sequence;
+//               in the instance with a staged bf16 additive mask (masked
+//               calls carry no packed batch), loads each step's transposed
+//               mask tile by TMA instead
 // setmaxnreg: compute 200, the other warpgroup 104 registers per thread
 // (128 * (200 + 200 + 104) = 384 * 168, the launch allocation).
 // Tensor memory: [0,128) S^T / P^T, [128,256) dP^T / dS^T, [256,256+d) dK,
@@ -43,29 +46,37 @@
 namespace sdpa {
 
 // ------------------------------------------------------------------ main
-template <int D>
+// BT: the instance whose bf16 additive mask (transposed: keys x queries)
+// arrives by TMA, one [128 x 128] tile (32 KB) per step, in the space the
+// step list takes otherwise (it runs without a boolean mask, so it lists no
+// steps).
+template <int D, bool BT = false>
 struct BwdTraits {
   static constexpr int NB = (D + 63) / 64;
   static constexpr int BLOCK_BYTES = 128 * 128;
   static constexpr int TILE_BYTES = NB * BLOCK_BYTES;  // one [128 rows x d] bf16 tile
   static constexpr int KSTEPS = D / 16;
   static constexpr int VEC_BYTES = 1024;               // -lse2[128] + -D[128]
-  static constexpr int NBAR = 16;
-  // K, V, Q[2], dO[2], then vectors, barriers, misc
+  static constexpr int NBAR = BT ? 18 : 16;
+  // K, V, Q[2], dO[2], then vectors, (the mask tile,) barriers, misc
   static constexpr int TILES_BYTES = 6 * TILE_BYTES;
+  static constexpr int BIAS_BYTES = BT ? 32768 : 0;
   static constexpr int MISC = 64;                      // tmem slot, abort flag, per-CTA values
-  static constexpr int SMEM = TILES_BYTES + 2 * VEC_BYTES + NBAR * 8 + MISC + 4 * kMaxStepList;
+  static constexpr int SMEM =
+      TILES_BYTES + 2 * VEC_BYTES + BIAS_BYTES + NBAR * 8 + MISC + (BT ? 0 : 4 * kMaxStepList);
   static constexpr int THREADS = 384;
 };
 
-// MASKED: the instance that applies p.mk (causal enters as wr = 0).
+// MASKED: the instance that applies p.mk (causal enters as wr = 0); 2 / 3:
+// a float32 / bf16 additive mask loaded per thread; 4: a bf16 one staged by
+// TMA (tmB, a map over its transpose; no boolean mask).
 template <int D, bool CAUSAL, int MASKED>
 __global__ void __launch_bounds__(384, 1)
     bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
                     const __grid_constant__ CUtensorMap tmdK, const __grid_constant__ CUtensorMap tmdV,
-                    const BwdParams p) {
-  using T = BwdTraits<D>;
+                    const __grid_constant__ CUtensorMap tmB, const BwdParams p) {
+  using T = BwdTraits<D, MASKED == 4>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const uint32_t base = smem_u32(smem_raw);
   // The layout needs a 1024-byte aligned start (128-byte swizzle atoms); the
@@ -79,7 +90,8 @@ __global__ void __launch_bounds__(384, 1)
   const uint32_t sQ = sV + T::TILE_BYTES;            // [2]
   const uint32_t sdO = sQ + 2 * T::TILE_BYTES;       // [2]
   const uint32_t sVec = sdO + 2 * T::TILE_BYTES;     // [2] x {-lse2[128], -D[128]}
-  const uint32_t sBar = sVec + 2 * T::VEC_BYTES;
+  const uint32_t sBias = sVec + 2 * T::VEC_BYTES;    // MASKED == 4: the step's mask tile (1024-aligned)
+  const uint32_t sBar = sBias + T::BIAS_BYTES;
   const uint32_t bKV = sBar;          // K_j, V_j loaded
   const uint32_t bQf = bKV + 8;       // [2] Q_i + vectors loaded
   const uint32_t bQe = bQf + 16;      // [2] Q stage free (after dK_i)
@@ -91,7 +103,9 @@ __global__ void __launch_bounds__(384, 1)
   const uint32_t bDs = bDp + 8;       // dS^T in TMEM (256 arrivals)
   const uint32_t bFin = bDs + 8;      // every MMA done
   const uint32_t bDrain = bFin + 8;
-  static_assert(1 + 2 * 4 + 6 <= 16, "barrier count");
+  const uint32_t bBf = bDrain + 8;    // MASKED == 4: mask tile loaded
+  const uint32_t bBe = bBf + 8;       // MASKED == 4: mask tile read (256 arrivals)
+  static_assert(1 + 2 * 4 + 6 + (MASKED == 4 ? 2 : 0) <= T::NBAR, "barrier count");
   uint8_t* const misc = smem_raw + (sBar - base) + 8 * T::NBAR;
   uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(misc);
   volatile int* const abort_flag = reinterpret_cast<volatile int*>(misc + 4);
@@ -232,6 +246,10 @@ __global__ void __launch_bounds__(384, 1)
     mbar_init(bDs, 256);
     mbar_init(bFin, 1);
     mbar_init(bDrain, 1);
+    if (MASKED == 4) {
+      mbar_init(bBf, 1);
+      mbar_init(bBe, 256);
+    }
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -278,8 +296,8 @@ __global__ void __launch_bounds__(384, 1)
       // columns, from its transposed copy, loaded before the waits below;
       // added as b / scale to the unscaled scores.  Query rows past Nq are
       // not read.
-      float bb[MASKED >= 2 ? 64 : 1];
-      if constexpr (MASKED >= 2) {
+      float bb[MASKED == 2 || MASKED == 3 ? 64 : 1];
+      if constexpr (MASKED == 2 || MASKED == 3) {
         const int kk = 128 * seq_s[10] + r, q0 = 128 * i + 64 * X;
         const int bb_b = seq_s[11], hq = seq_s[5] * p.G + g;
         // (the transpose sits 16-byte aligned in the workspace)
@@ -327,9 +345,26 @@ __global__ void __launch_bounds__(384, 1)
           x[32 + e] = __uint_as_float(rb[e]);
         }
       }
-      if constexpr (MASKED >= 2) {
+      if constexpr (MASKED == 2 || MASKED == 3) {
 #pragma unroll
         for (int q = 0; q < 64; ++q) x[q] = fmaf(bb[q], p.mk.inv_scale, x[q]);
+      } else if constexpr (MASKED == 4) {
+        // This key row of the staged tile over the warpgroup's 64 query
+        // columns (swizzle block X; rows past Nk and columns past Nq read as
+        // zeros), then the tile is released to warp 11 for the next step.
+        ok = __all_sync(0xffffffffu, wait_bounded(wc, bBf, it & 1, wait_site(0x16, it)));
+        if (!ok) break;
+#pragma unroll
+        for (int ch = 0; ch < 8; ++ch) {
+          const uint4 u = ld_shared_v4u(sBias + 16384u * X + sw128_offset(r, ch));
+          const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            x[8 * ch + 2 * e] = fmaf(__uint_as_float(w[e] << 16), p.mk.inv_scale, x[8 * ch + 2 * e]);
+            x[8 * ch + 2 * e + 1] = fmaf(__uint_as_float(w[e] & 0xffff0000u), p.mk.inv_scale, x[8 * ch + 2 * e + 1]);
+          }
+        }
+        mbar_arrive(bBe);
       }
       // P^T[r][q] = exp2(S^T * scale * log2e - lse2[q]); masked (key > query
       // on the diagonal tile) entries and padding key rows are exactly 0.
@@ -498,6 +533,29 @@ __global__ void __launch_bounds__(384, 1)
           wait_drain(bQf + 8u * st, ((((issued - 1 - st) / 2) * 2 + st) >> 1) & 1, p.limit_ns);
       }
       __syncwarp();
+    } else if (MASKED == 4 && warp == 11) {
+      // ------------------------------------------------------------ mask tile producer
+      // Step it's tile of the transposed mask: key rows 128 j.., query
+      // columns 128 i.., plane of query head hk * G + g; loaded once both
+      // compute warpgroups have read the previous step's tile.
+      if (lane == 0) {
+        tma_prefetch_desc(&tmB);
+        bool okp = true;
+        int issued = 0;
+        for (int it = 0; it < total && okp; ++it) {
+          int g, i;
+          step_at(it, g, i);
+          if (it > 0 && !(okp = wait_bounded(wc, bBe, (it - 1) & 1, wait_site(0x33, it)))) break;
+          const int plane = bias_plane(p.mk, seq_s[11], seq_s[5] * p.G + g);
+          mbar_expect_tx(bBf, 32768);
+          for (int cb = 0; cb < 2; ++cb)
+            tma_load_3d(sBias + 16384u * cb, &tmB, bBf, 128 * i + 64 * cb, 128 * seq_s[10], plane);
+          issued = it + 1;
+        }
+        // Every copy issued above has landed before the CTA may exit.
+        if (issued > 0) wait_drain(bBf, (issued - 1) & 1, p.limit_ns);
+      }
+      __syncwarp();
     } else if (warp == 11) {
       // ------------------------------------------------------------ partial dK / dV tile (packed batch)
       const int valid = seq_s[3] - 128 * j;
@@ -637,41 +695,49 @@ size_t bwd_smem_bytes(int d) {
 template <int D, bool C, int M = 0>
 static cudaError_t launch_main_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                                  const CUtensorMap& tdo, const CUtensorMap& tdk, const CUtensorMap& tdv,
-                                 const BwdParams& p, cudaStream_t stream) {
+                                 const CUtensorMap& tb, const BwdParams& p, cudaStream_t stream) {
+  using T = BwdTraits<D, M == 4>;
   auto kern = bwd_main_kernel<D, C, M>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, BwdTraits<D>::SMEM);
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, T::SMEM);
   if (e != cudaSuccess) return e;
   const unsigned grid = (unsigned)p.nkv * (unsigned)(p.B * p.Hkv);
   BwdParams pc = p;
   pc.tail = order_tail(p.nkv, p.B * p.Hkv, 1);
-  kern<<<grid, BwdTraits<D>::THREADS, BwdTraits<D>::SMEM, stream>>>(tq, tk, tv, tdo, tdk, tdv, pc);
+  kern<<<grid, T::THREADS, T::SMEM, stream>>>(tq, tk, tv, tdo, tdk, tdv, tb, pc);
   return cudaGetLastError();
 }
 
 cudaError_t launch_bwd_grad(int d, bool causal, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                             const CUtensorMap& tdo, const CUtensorMap& tdk, const CUtensorMap& tdv,
-                            const BwdParams& p, cudaStream_t stream, bool masked) {
+                            const BwdParams& p, cudaStream_t stream, bool masked, const CUtensorMap* tbt) {
+  const CUtensorMap& b = tbt != nullptr ? *tbt : tdk;  // (unused by the instances without a staged mask tile)
+#define SDPA_MAIN(DD, CC, MM) launch_main_t<DD, CC, MM>(tq, tk, tv, tdo, tdk, tdv, b, p, stream)
   if (masked) {
-    const bool bias = p.mk.bias != nullptr;  // the instances with the additive mask (float32, bf16)
-    switch (d) {
-      case 64: return bias ? (p.mk.bias_bf16 ? launch_main_t<64, false, 3>(tq, tk, tv, tdo, tdk, tdv, p, stream) : launch_main_t<64, false, 2>(tq, tk, tv, tdo, tdk, tdv, p, stream))
-                      : launch_main_t<64, false, 1>(tq, tk, tv, tdo, tdk, tdv, p, stream);
-      case 96: return bias ? (p.mk.bias_bf16 ? launch_main_t<96, false, 3>(tq, tk, tv, tdo, tdk, tdv, p, stream) : launch_main_t<96, false, 2>(tq, tk, tv, tdo, tdk, tdv, p, stream))
-                      : launch_main_t<96, false, 1>(tq, tk, tv, tdo, tdk, tdv, p, stream);
-      case 128: return bias ? (p.mk.bias_bf16 ? launch_main_t<128, false, 3>(tq, tk, tv, tdo, tdk, tdv, p, stream) : launch_main_t<128, false, 2>(tq, tk, tv, tdo, tdk, tdv, p, stream))
-                      : launch_main_t<128, false, 1>(tq, tk, tv, tdo, tdk, tdv, p, stream);
+    // The additive mask: float32, bf16 loaded by each thread, or bf16 staged by TMA (tbt given).
+    const int mode = p.mk.bias == nullptr ? 1 : !p.mk.bias_bf16 ? 2 : tbt == nullptr ? 3 : 4;
+    switch (d * 8 + mode) {
+      case 64 * 8 + 1: return SDPA_MAIN(64, false, 1);
+      case 64 * 8 + 2: return SDPA_MAIN(64, false, 2);
+      case 64 * 8 + 3: return SDPA_MAIN(64, false, 3);
+      case 64 * 8 + 4: return SDPA_MAIN(64, false, 4);
+      case 96 * 8 + 1: return SDPA_MAIN(96, false, 1);
+      case 96 * 8 + 2: return SDPA_MAIN(96, false, 2);
+      case 96 * 8 + 3: return SDPA_MAIN(96, false, 3);
+      case 96 * 8 + 4: return SDPA_MAIN(96, false, 4);
+      case 128 * 8 + 1: return SDPA_MAIN(128, false, 1);
+      case 128 * 8 + 2: return SDPA_MAIN(128, false, 2);
+      case 128 * 8 + 3: return SDPA_MAIN(128, false, 3);
+      case 128 * 8 + 4: return SDPA_MAIN(128, false, 4);
       default: return cudaErrorInvalidValue;
     }
   }
   switch (d) {
-    case 64: return causal ? launch_main_t<64, true>(tq, tk, tv, tdo, tdk, tdv, p, stream)
-                           : launch_main_t<64, false>(tq, tk, tv, tdo, tdk, tdv, p, stream);
-    case 96: return causal ? launch_main_t<96, true>(tq, tk, tv, tdo, tdk, tdv, p, stream)
-                           : launch_main_t<96, false>(tq, tk, tv, tdo, tdk, tdv, p, stream);
-    case 128: return causal ? launch_main_t<128, true>(tq, tk, tv, tdo, tdk, tdv, p, stream)
-                            : launch_main_t<128, false>(tq, tk, tv, tdo, tdk, tdv, p, stream);
+    case 64: return causal ? SDPA_MAIN(64, true, 0) : SDPA_MAIN(64, false, 0);
+    case 96: return causal ? SDPA_MAIN(96, true, 0) : SDPA_MAIN(96, false, 0);
+    case 128: return causal ? SDPA_MAIN(128, true, 0) : SDPA_MAIN(128, false, 0);
     default: return cudaErrorInvalidValue;
   }
+#undef SDPA_MAIN
 }
 
 }  // namespace sdpa

@@ -317,9 +317,13 @@ cudaError_t launch_fwd_fp8(int d, bool causal, const CUtensorMap& tq, const CUte
                            const FwdParams& p, cudaStream_t stream);
 
 cudaError_t launch_bwd_prep(const BwdParams& p, cudaStream_t stream);
+// tbt (masked, bf16 additive mask, no boolean mask): a map over the mask's
+// transpose (planes, Nk, Nq) with boxes of 128 rows x 64 columns, 128-byte
+// swizzle; given, the dK/dV kernel stages its tiles by TMA.
 cudaError_t launch_bwd_grad(int d, bool causal, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                             const CUtensorMap& tdo, const CUtensorMap& tdk, const CUtensorMap& tdv,
-                            const BwdParams& p, cudaStream_t stream, bool masked = false);
+                            const BwdParams& p, cudaStream_t stream, bool masked = false,
+                            const CUtensorMap* tbt = nullptr);
 // `to` (a map over O laid out as Q) is read only when p.rows_in_dq is set.
 cudaError_t launch_bwd_dq(int d, bool causal, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                           const CUtensorMap& tdo, const CUtensorMap& tdq, const CUtensorMap& to, const BwdParams& p,

@@ -311,3 +311,21 @@ def test_bf16_bias_staged_equals_loaded(cuda_lib, shape, causal):
     O1, l1 = cuda_lib.forward_masked(tq, tk, tv, s, causal, None, None, None, staged)
     O2, l2 = cuda_lib.forward_masked(tq, tk, tv, s, causal, None, None, None, loaded)
     assert torch.equal(O1, O2) and torch.equal(l1, l2)
+
+
+def test_bf16_bias_staged_equals_loaded_backward(cuda_lib):
+    """The dK/dV kernel stages a bf16 additive mask by TMA unless a boolean
+    mask comes with it; an all-visible boolean mask changes no value but
+    selects per-thread loads.  dQ, dK and dV agree bit for bit."""
+    import torch
+    B, H, Hkv, Nq, Nk, d = 1, 2, 2, 384, 384, 128
+    q, k, v, do = _problem(B, H, Hkv, Nq, Nk, d, 49700)
+    bias = _t(round_bf16(_bias((1, H, Nq, Nk), 49800)), torch.bfloat16)
+    ones = _t(np.ones((1, 1, Nq, Nk), dtype=np.uint8), torch.uint8)
+    s = 1 / math.sqrt(d)
+    tq, tk, tv, tdo = dev(q), dev(k), dev(v), dev(do)
+    O, lse = cuda_lib.forward_masked(tq, tk, tv, s, True, None, None, None, bias)
+    staged = cuda_lib.backward_masked(tq, tk, tv, O, lse, tdo, s, True, None, None, None, bias)
+    loaded = cuda_lib.backward_masked(tq, tk, tv, O, lse, tdo, s, True, None, None, ones, bias)
+    for a, b, name in zip(staged, loaded, ("dQ", "dK", "dV")):
+        assert torch.equal(a, b), name
