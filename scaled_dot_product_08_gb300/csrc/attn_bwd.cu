@@ -702,7 +702,7 @@ static cudaError_t launch_main_t(const CUtensorMap& tq, const CUtensorMap& tk, c
   if (e != cudaSuccess) return e;
   const unsigned grid = (unsigned)p.nkv * (unsigned)(p.B * p.Hkv);
   BwdParams pc = p;
-  pc.tail = order_tail(p.nkv, p.B * p.Hkv, 1);
+  pc.tail = uniform_levels(C, p.vl, p.mk, M != 0) ? 1 : order_tail(p.nkv, p.B * p.Hkv, 1);
   kern<<<grid, T::THREADS, T::SMEM, stream>>>(tq, tk, tv, tdo, tdk, tdv, tb, pc);
   return cudaGetLastError();
 }

@@ -636,7 +636,7 @@ static cudaError_t launch_dq_t(const CUtensorMap& tq, const CUtensorMap& tk, con
   if (e != cudaSuccess) return e;
   const unsigned grid = (unsigned)p.nq * (unsigned)(p.B * p.H);
   BwdParams pc = p;
-  pc.tail = order_tail(p.nq, p.B * p.H, p.G);
+  pc.tail = uniform_levels(C, p.vl, p.mk, M != 0) ? 1 : order_tail(p.nq, p.B * p.H, p.G);
   kern<<<grid, DqTraits<D>::THREADS, DqTraits<D>::SMEM, stream>>>(tq, tk, tv, tdo, tdq, to, pc);
   return cudaGetLastError();
 }

@@ -709,7 +709,7 @@ static cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, co
   if (e != cudaSuccess) return e;
   const unsigned grid = (unsigned)p.n_mtiles * (unsigned)(p.B * p.H);
   FwdParams pc = p;
-  pc.tail = order_tail(p.n_mtiles, p.B * p.H, p.G);
+  pc.tail = uniform_levels(C, p.vl, p.mk, M != 0) ? 1 : order_tail(p.n_mtiles, p.B * p.H, p.G);
   kern<<<grid, T::THREADS, T::SMEM, stream>>>(tq, tk, tv, to, tb, pc);
   return cudaGetLastError();
 }

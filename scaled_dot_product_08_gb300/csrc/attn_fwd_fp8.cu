@@ -426,7 +426,7 @@ cudaError_t launch_fp8_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
   if (e != cudaSuccess) return e;
   const unsigned grid = (unsigned)p.n_mtiles * (unsigned)(p.B * p.H);
   FwdParams pc = p;
-  pc.tail = order_tail(p.n_mtiles, p.B * p.H, p.G);
+  pc.tail = !C ? 1 : order_tail(p.n_mtiles, p.B * p.H, p.G);  // (non-causal: every level alike)
   kern<<<grid, F::THREADS, F::SMEM, stream>>>(tq, tk, tv, pc);
   return cudaGetLastError();
 }

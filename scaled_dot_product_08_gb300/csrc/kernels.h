@@ -124,6 +124,14 @@ __host__ __device__ __forceinline__ void work_unit(int cta, int nlev, int nheads
   }
 }
 
+// Every level of a launch does the same work (no causal edge, window, key
+// lengths, tile mask or packed batch): the tail gains nothing there, and
+// head-major order keeps each head's CTAs together in L2.
+inline bool uniform_levels(bool causal, const VarlenArgs& vl, const MaskArgs& mk, bool masked) {
+  return !causal && vl.cu_q == nullptr &&
+         (!masked || (mk.wl < 0 && mk.wr < 0 && mk.key_len == nullptr && mk.flags == nullptr));
+}
+
 // The level-major tail: whole groups of `group` heads (those that share K
 // and V), enough for about three waves of CTAs on this device's SMs, or all
 // heads.
