@@ -465,16 +465,19 @@ attn_status_t attn_selftest_wait_timeout(unsigned int timeout_us, void* stream);
 /*
  * Test hook for the failure-detection path of the production kernels (off
  * unless called; the pages have no counterpart).  Arms one launch: the next
- * launch of `kernel` from this process (0: the forward kernel, as launched
- * by attn_fwd / attn_fwd_cross; 1: the dQ kernel, attn_bwd's first stage;
- * 2: the dK/dV kernel, its second) runs with every on-chip wait limited to
- * `limit_us` microseconds, and in its first CTA the TMA producer does not
- * issue its `load_index`-th ring load (forward: K_0, V_0, K_1, ...; dQ: the
- * same; dK/dV: the query tiles Q_i with their row vectors).  The consumers of
- * that load then wait in vain: the first wait to run out records
- * ATTN_ERR_TIMEOUT in the device status word (attn_get_device_status) and
- * where it gave up (attn_get_timeout_info), and every role of that CTA stops
- * and exits, so the context stays usable; the other CTAs complete normally.
+ * launch of `kernel` from this process (0: the launch-per-unit forward
+ * kernel, which then serves attn_fwd / attn_fwd_cross for that launch; 1:
+ * the dQ kernel, attn_bwd's first stage; 2: the dK/dV kernel, its second;
+ * 3: the persistent forward kernel, which serves attn_fwd / attn_fwd_cross
+ * otherwise) runs with every on-chip wait limited to `limit_us`
+ * microseconds, and in its first CTA (kernel 3: the CTA that takes the
+ * first work unit) the TMA producer does not issue its `load_index`-th ring
+ * load of that unit (forward: K_0, V_0, K_1, ...; dQ: the same; dK/dV: the
+ * query tiles Q_i with their row vectors).  The consumers of that load then
+ * wait in vain: the first wait to run out records ATTN_ERR_TIMEOUT in the
+ * device status word (attn_get_device_status) and where it gave up
+ * (attn_get_timeout_info), and every role of that CTA stops and exits, so
+ * the context stays usable; the other CTAs complete normally.
  * The outputs of that launch are not valid.  The hook is cleared by the
  * launch it applies to.
  *   load_index: 0 .. 2^20; limit_us: 1000 .. 60,000,000.  Other values give

@@ -321,7 +321,9 @@ static attn_status_t fwd_common(const void* q, const void* k, const void* v, voi
   p.limit_ns = wait_limit_ns();
   p.info = di->info;
   take_debug(0, &p.debug_drop1, &p.limit_ns);
+  take_debug(3, &p.debug_drop_p, &p.limit_ns);
   take_plant(0, &p.debug_plant, 1);
+  p.o = static_cast<uint16_t*>(o);  // (the persistent kernel writes O directly)
   cudaError_t e = sdpa::launch_fwd(d, causal != 0, tq, tk, tv, to, p, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return ATTN_ERR_LAUNCH;
   return ATTN_OK;
@@ -1150,7 +1152,7 @@ attn_status_t attn_selftest_wait_timeout(unsigned int timeout_us, void* stream) 
 }
 
 attn_status_t attn_debug_drop_load(int kernel, int load_index, unsigned int limit_us) {
-  if (kernel < 0 || kernel > 2 || load_index < 0 || load_index > (1 << 20)) return ATTN_ERR_INVALID_ARG;
+  if (kernel < 0 || kernel > 3 || load_index < 0 || load_index > (1 << 20)) return ATTN_ERR_INVALID_ARG;
   if (limit_us < 1000u || limit_us > 60000000u) return ATTN_ERR_INVALID_ARG;
   std::lock_guard<std::mutex> lk(g_debug_mu);
   g_debug_kernel = kernel;

@@ -74,6 +74,9 @@ struct FwdParams {
   int debug_drop1;       // 0; n > 0 only in a test of the bounded waits: CTA 0's producer skips ring load n - 1
   int tail;              // heads in the level-major tail of the CTA order (work_unit); set by the launcher
   int debug_plant;       // 0; 1 only in a test of the debug build's checks: CTA 0 offsets its lse store out of range
+  int* sched;            // persistent forward: this launch's queue (next unit, CTAs done); set by its launcher
+  int n_units;           // persistent forward: units in the launch
+  int debug_drop_p;      // 0; n > 0 only in a test of the bounded waits: the persistent forward skips unit 0's ring load n - 1
 };
 
 // Backward arguments.
@@ -314,6 +317,10 @@ size_t decode_smem_bytes(int d);
 // tb (masked, bf16 additive mask only): a map over the mask as (planes, Nq,
 // Nk) bf16 with boxes of 128 rows x 64 columns, 128-byte swizzle; given, the
 // kernel stages the mask's tiles by TMA instead of per-thread loads.
+// The dense forward (no mask, no packed batch) as a persistent kernel; O is
+// written through p.o, laid out as (B, H, Nq, d).
+cudaError_t launch_fwd_persist(int d, bool causal, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                               const FwdParams& p, cudaStream_t stream);
 cudaError_t launch_fwd(int d, bool causal, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                        const CUtensorMap& to, const FwdParams& p, cudaStream_t stream, bool masked = false,
                        const CUtensorMap* tb = nullptr);

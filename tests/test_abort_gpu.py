@@ -77,3 +77,30 @@ def test_backward_dropped_load_times_out_and_recovers(cuda_lib, kernel, load, si
     grads = [host(g) for g in cuda_lib.backward(tq, tk, tv, O, lse, tdo, s, True)]
     check_grads(grads, oracle.attention_backward(q, k, v, do, s, True), "after the timeout")
     assert cuda_lib.attn_get_device_status(None) == cuda_lib.Status.OK
+
+
+PERSIST_SITES = {0x51, 0x52, 0x53, 0x54, 0x5a, 0x61, 0x64, 0x65, 0x66} | set(range(0x71, 0x7b))
+
+
+def test_persistent_forward_dropped_load_times_out_and_recovers(cuda_lib):
+    # The persistent forward (attn_fwd's dense calls): the CTA that takes the
+    # first work unit (head 0, query tiles 2 and 3) skips that unit's K_1.
+    # Which CTA that is depends on the queue, so only the status, the site
+    # and the next call are checked.
+    import torch
+    B, H, N, d = 1, 2, 512, 128
+    q, k, v, _ = _inputs(B, H, N, d, 63000)
+    s = 1 / math.sqrt(d)
+    assert cuda_lib.attn_get_device_status(None) == cuda_lib.Status.OK
+    assert cuda_lib.attn_debug_drop_load(3, 2, LIMIT_US) == cuda_lib.Status.OK
+    cuda_lib.forward(dev(q), dev(k), dev(v), s, True)
+    torch.cuda.synchronize()
+    st, info = cuda_lib.attn_get_timeout_info(None)
+    assert st == cuda_lib.Status.OK
+    assert cuda_lib.attn_get_device_status(None) == cuda_lib.Status.TIMEOUT
+    assert info[0] >> 16 in PERSIST_SITES, hex(info[0] >> 16)
+    assert info[3] >= LIMIT_US * 0.9
+    O_ref, lse_ref = oracle.attention_forward(q, k, v, s, True)
+    O, lse = cuda_lib.forward(dev(q), dev(k), dev(v), s, True)
+    check_o_lse(host(O), host(lse), O_ref, lse_ref, "after the timeout")
+    assert cuda_lib.attn_get_device_status(None) == cuda_lib.Status.OK
