@@ -710,6 +710,11 @@ static cudaError_t launch_main_t(const CUtensorMap& tq, const CUtensorMap& tk, c
 cudaError_t launch_bwd_grad(int d, bool causal, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                             const CUtensorMap& tdo, const CUtensorMap& tdk, const CUtensorMap& tdv,
                             const BwdParams& p, cudaStream_t stream, bool masked, const CUtensorMap* tbt) {
+  // A dense call goes to the persistent kernel (attn_bwd_persist.cu), except
+  // a launch armed by the dropped-load test hook, whose checks expect this
+  // kernel's fixed CTA-to-unit mapping.
+  if (!masked && p.vl.cu_q == nullptr && p.debug_drop1 == 0 && p.dk != nullptr && p.dv != nullptr)
+    return launch_bwd_grad_persist(d, causal, tq, tk, tv, tdo, p, stream);
   const CUtensorMap& b = tbt != nullptr ? *tbt : tdk;  // (unused by the instances without a staged mask tile)
 #define SDPA_MAIN(DD, CC, MM) launch_main_t<DD, CC, MM>(tq, tk, tv, tdo, tdk, tdv, b, p, stream)
   if (masked) {
