@@ -460,6 +460,7 @@ static attn_status_t bwd_grad_x(const void* q, const void* k, const void* v, con
   p.dk = static_cast<uint16_t*>(dk);
   p.dv = static_cast<uint16_t*>(dv);
   take_debug(2, &p.debug_drop1, &p.limit_ns);
+  take_debug(4, &p.debug_drop_p, &p.limit_ns);
   cudaError_t e = sdpa::launch_bwd_grad(d, causal != 0, tq, tk, tv, tdo, tdk, tdv, p,
                                         static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;
@@ -1152,7 +1153,7 @@ attn_status_t attn_selftest_wait_timeout(unsigned int timeout_us, void* stream) 
 }
 
 attn_status_t attn_debug_drop_load(int kernel, int load_index, unsigned int limit_us) {
-  if (kernel < 0 || kernel > 3 || load_index < 0 || load_index > (1 << 20)) return ATTN_ERR_INVALID_ARG;
+  if (kernel < 0 || kernel > 4 || load_index < 0 || load_index > (1 << 20)) return ATTN_ERR_INVALID_ARG;
   if (limit_us < 1000u || limit_us > 60000000u) return ATTN_ERR_INVALID_ARG;
   std::lock_guard<std::mutex> lk(g_debug_mu);
   g_debug_kernel = kernel;

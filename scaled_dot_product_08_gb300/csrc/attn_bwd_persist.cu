@@ -347,6 +347,10 @@ __global__ void __launch_bounds__(384, 1)
             const int g = it / x.ni, i = x.i0 + it % x.ni;
             const int bh = b * p.H + hk * p.G + g;
             if (rd > 0 && !(ok = wait_bounded(wc, bQe + 8u * st, (rd - 1) & 1, wait_site(0x31, it)))) break;
+            if (u == 0 && p.debug_drop_p == it + 1) {  // test of the bounded waits only
+              ++gq;
+              continue;
+            }
             const uint32_t barq = bQf + 8u * st;
             mbar_expect_tx(barq, T::TILE_BYTES + T::VEC_BYTES);
             for (int cb = 0; cb < T::NB; ++cb)

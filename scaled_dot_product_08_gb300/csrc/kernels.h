@@ -107,6 +107,7 @@ struct BwdParams {
   int debug_plant;       // 0; 2 only in a test of the debug build's checks: CTA 0 of the dQ kernel offsets its row-vector store out of range
   int* sched;            // persistent dK/dV kernel: this launch's queue (next unit, CTAs done); set by its launcher
   int n_units;           // persistent dK/dV kernel: units in the launch
+  int debug_drop_p;      // 0; n > 0 only in a test of the bounded waits: the persistent dK/dV kernel skips unit 0's Q load n - 1
 };
 
 // CTA order of the forward, dQ and dK/dV launches.  A launch's CTAs cover

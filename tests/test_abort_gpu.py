@@ -104,3 +104,29 @@ def test_persistent_forward_dropped_load_times_out_and_recovers(cuda_lib):
     O, lse = cuda_lib.forward(dev(q), dev(k), dev(v), s, True)
     check_o_lse(host(O), host(lse), O_ref, lse_ref, "after the timeout")
     assert cuda_lib.attn_get_device_status(None) == cuda_lib.Status.OK
+
+
+PERSIST_GRAD_SITES = {0x11, 0x12, 0x13, 0x14, 0x1a, 0x31, 0x32, 0x34, 0x35} | set(range(0x41, 0x49))
+
+
+def test_persistent_dkdv_dropped_load_times_out_and_recovers(cuda_lib):
+    # The persistent dK/dV kernel (attn_bwd's dense second stage): the CTA
+    # that takes the first work unit skips that unit's Q_1 load.
+    import torch
+    B, H, N, d = 1, 2, 512, 128
+    q, k, v, do = _inputs(B, H, N, d, 64000)
+    s = 1 / math.sqrt(d)
+    tq, tk, tv, tdo = dev(q), dev(k), dev(v), dev(do)
+    O, lse = cuda_lib.forward(tq, tk, tv, s, True)
+    assert cuda_lib.attn_get_device_status(None) == cuda_lib.Status.OK
+    assert cuda_lib.attn_debug_drop_load(4, 1, LIMIT_US) == cuda_lib.Status.OK
+    cuda_lib.backward(tq, tk, tv, O, lse, tdo, s, True)
+    torch.cuda.synchronize()
+    st, info = cuda_lib.attn_get_timeout_info(None)
+    assert st == cuda_lib.Status.OK
+    assert cuda_lib.attn_get_device_status(None) == cuda_lib.Status.TIMEOUT
+    assert info[0] >> 16 in PERSIST_GRAD_SITES, hex(info[0] >> 16)
+    assert info[3] >= LIMIT_US * 0.9
+    grads = [host(g) for g in cuda_lib.backward(tq, tk, tv, O, lse, tdo, s, True)]
+    check_grads(grads, oracle.attention_backward(q, k, v, do, s, True), "after the timeout")
+    assert cuda_lib.attn_get_device_status(None) == cuda_lib.Status.OK
