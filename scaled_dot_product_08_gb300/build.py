@@ -28,6 +28,7 @@ DEBUG_LIB = os.path.join(LIBDIR, "libsdpa08_debug.so")
 INCLUDE = os.path.join(os.path.dirname(PKG), "include")
 
 SOURCES = ["attn_api.cu", "attn_fwd.cu", "attn_fwd_persist.cu", "attn_fwd_fp8.cu", "attn_bwd.cu", "attn_bwd_persist.cu", "attn_bwd_prep.cu", "attn_bwd_dq.cu",
+           "attn_bwd_dq_persist.cu",
            "attn_decode.cu", "attn_mask.cu", "attn_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",

@@ -42,7 +42,8 @@ unsigned long long wait_limit_ns() {
 }
 
 // The dropped-load test hook (attn_debug_drop_load): armed for one launch of
-// one kernel, then cleared.  kernel: 0 forward, 1 dQ, 2 dK/dV.
+// one kernel, then cleared.  kernel: 0 forward, 1 dQ, 2 dK/dV, and the
+// persistent kernels 3 forward, 4 dK/dV, 5 dQ.
 std::mutex g_debug_mu;
 int g_debug_kernel = -1, g_debug_drop1 = 0;
 unsigned long long g_debug_limit_ns = 0;
@@ -484,6 +485,7 @@ static attn_status_t bwd_dq_x(const void* q, const void* k, const void* v, const
   bwd_params(&p, workspace, B, H, Hkv, Nq, Nk, d, scale, causal, di);
   p.dq = static_cast<uint16_t*>(dq);
   take_debug(1, &p.debug_drop1, &p.limit_ns);
+  take_debug(5, &p.debug_drop_p, &p.limit_ns);
   cudaError_t e =
       sdpa::launch_bwd_dq(d, causal != 0, tq, tk, tv, tdo, tdq, tq, p, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;
@@ -509,8 +511,11 @@ static attn_status_t bwd_dq_rows_x(const void* q, const void* k, const void* v, 
   bwd_params(&p, workspace, B, H, Hkv, Nq, Nk, d, scale, causal, di);
   p.dq = static_cast<uint16_t*>(dq);
   p.lse = lse;
+  p.o = static_cast<const uint16_t*>(o);  // (the persistent kernel reads O and dO rows directly)
+  p.dout = static_cast<const uint16_t*>(dout);
   p.rows_in_dq = 1;
   take_debug(1, &p.debug_drop1, &p.limit_ns);
+  take_debug(5, &p.debug_drop_p, &p.limit_ns);
   take_plant(1, &p.debug_plant, 2);
   cudaError_t e = sdpa::launch_bwd_dq(d, causal != 0, tq, tk, tv, tdo, tdq, to, p, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;
@@ -1153,7 +1158,7 @@ attn_status_t attn_selftest_wait_timeout(unsigned int timeout_us, void* stream) 
 }
 
 attn_status_t attn_debug_drop_load(int kernel, int load_index, unsigned int limit_us) {
-  if (kernel < 0 || kernel > 4 || load_index < 0 || load_index > (1 << 20)) return ATTN_ERR_INVALID_ARG;
+  if (kernel < 0 || kernel > 5 || load_index < 0 || load_index > (1 << 20)) return ATTN_ERR_INVALID_ARG;
   if (limit_us < 1000u || limit_us > 60000000u) return ATTN_ERR_INVALID_ARG;
   std::lock_guard<std::mutex> lk(g_debug_mu);
   g_debug_kernel = kernel;

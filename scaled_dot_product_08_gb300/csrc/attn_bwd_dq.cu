@@ -656,6 +656,11 @@ cudaError_t launch_bwd_dq(int d, bool causal, const CUtensorMap& tq, const CUten
       default: return cudaErrorInvalidValue;
     }
   }
+  // The dense batch runs the persistent kernel; launches armed by the test
+  // hooks of this kernel keep it (their tests expect its CTA mapping).
+  if (p.vl.cu_q == nullptr && p.debug_drop1 == 0 && p.debug_plant == 0 && p.dq != nullptr &&
+      (!p.rows_in_dq || (p.o != nullptr && p.dout != nullptr && p.lse != nullptr)))
+    return launch_bwd_dq_persist(d, causal, tq, tk, tv, tdo, p, stream);
   switch (d) {
     case 64: return causal ? launch_dq_t<64, true>(tq, tk, tv, tdo, tdq, to, p, stream)
                            : launch_dq_t<64, false>(tq, tk, tv, tdo, tdq, to, p, stream);

@@ -1,0 +1,678 @@
+// attn_bwd_dq_persist.cu — the dQ kernel of the dense backward (no mask, no
+// packed batch) as a persistent kernel on sm_103a.
+//
+// Method and arithmetic: those of attn_bwd_dq.cu's bwd_dq_kernel (page
+// "Flash Attention原理", §五: P recomputed from lse, dP = dO V^T,
+// dS = P (dP - D), dQ = scale dS K, and the row vectors D = rowsum(dO * O)
+// and lse in base 2), unchanged, so the two kernels give the same bits.
+// What differs is the schedule: one CTA per SM takes the (head, query tile)
+// units of bwd_dq_kernel, in the same order (work_unit), from a queue until
+// none is left, instead of one CTA per unit paying its launch, barrier and
+// tensor-memory setup, the wait for its first tiles and its epilogue while
+// the tensor core idles (about 6 us of a 22 us unit at C5).
+//
+// GB300 mapping: bwd_dq_kernel's roles (warps 0-7 compute, warp 8 the TMA
+// producer, warp 9 the MMA issuer), with these differences:
+//   * warps 10-11 take the units from the queue and pass each one on through
+//     a two-entry ring in shared memory, with the unit's row vectors (-lse2,
+//     -D for its 128 query rows), which they form from lse, O and dO in
+//     global memory (or copy from the workspace, when an earlier stage formed
+//     them) while the units before it run; they also write the vectors to
+//     the workspace for the dK/dV kernel, and ask L2 for the unit's Q and dO
+//     tiles ahead of the producer's loads;
+//   * the K and V rings and every per-step barrier run on across units; Q
+//     and dO have empty barriers, committed after the unit's last S and last
+//     dP products, so the next unit's tiles load while the current unit's
+//     last steps run;
+//   * dQ leaves from registers straight to global memory, and the next
+//     unit's first products (S_0, dP_0, S_1) run during that epilogue.
+#include <atomic>
+#include <cmath>
+
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace sdpa {
+
+namespace {
+
+template <int D>
+struct PQTraits {
+  static constexpr int NB = (D + 63) / 64;
+  static constexpr int BLOCK_BYTES = 128 * 128;
+  static constexpr int TILE_BYTES = NB * BLOCK_BYTES;  // one [128 rows x d] bf16 tile
+  static constexpr int KSTEPS = D / 16;
+  static constexpr int KS = 3, VS = 2;                 // K and V ring slots
+  static constexpr int VEC_BYTES = 1024;               // -lse2[128], -D[128]
+  // q_full q_empty do_full do_empty k_full[3] k_empty[3] v_full[2] v_empty[2]
+  // s[2] dp dp_copied ds fin unit_full[2] unit_vec[2] unit_empty[2] drain
+  static constexpr int NBAR = 4 + 6 + 4 + 2 + 4 + 6 + 1;
+  static constexpr int TILES_BYTES = (2 + KS + VS) * TILE_BYTES;  // Q, dO, K[3], V[2]
+  static constexpr int MISC = 32;                                 // tmem slot, abort flag, unit ring, stop flag
+  static constexpr int SMEM = TILES_BYTES + 2 * VEC_BYTES + NBAR * 8 + MISC;
+  static constexpr int THREADS = 384;
+};
+static_assert(PQTraits<128>::SMEM <= 227 * 1024, "shared memory");
+
+// Arrivals on unit_empty: every thread that reads a ring entry (the compute
+// warpgroups, the MMA warp and the producer warp).
+constexpr int kDqUnitReaders = 256 + 32 + 32;
+// Named barrier of the two vector warps (ids 0, 15 and the compute
+// warpgroups' are taken elsewhere).
+constexpr uint32_t kVecBarrier = 5;
+
+// Asks L2 for a box of a tensor map (no shared memory written, no barrier).
+__device__ __forceinline__ void tma_prefetch_l2_3d(const CUtensorMap* m, int c0, int c1, int c2) {
+  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
+                   reinterpret_cast<uint64_t>(m)),
+               "r"(c0), "r"(c1), "r"(c2)
+               : "memory");
+}
+
+}  // namespace
+
+template <int D, bool CAUSAL>
+__global__ void __launch_bounds__(384, 1)
+    bwd_dq_persist_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                          const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
+                          const BwdParams p) {
+  using T = PQTraits<D>;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  const uint32_t base = smem_u32(smem_raw);
+  if (base & 1023u) {  // the layout needs a 1024-byte aligned start (128-byte swizzle atoms)
+    if (threadIdx.x == 0) atomicCAS(p.status, 0, kDevMisaligned);
+    return;
+  }
+  const uint32_t sQ = base;                          // Q_i
+  const uint32_t sdO = sQ + T::TILE_BYTES;           // dO_i
+  const uint32_t sK = sdO + T::TILE_BYTES;           // [KS] K_j
+  const uint32_t sV = sK + T::KS * T::TILE_BYTES;    // [VS] V_j
+  const uint32_t sVec = sV + T::VS * T::TILE_BYTES;  // [2] x {-lse2[128], -D[128]}
+  const uint32_t sBar = sVec + 2 * T::VEC_BYTES;
+  const uint32_t bQf = sBar;            // Q_i loaded
+  const uint32_t bQe = bQf + 8;         // Q stage free (after the unit's last S)
+  const uint32_t bOf = bQe + 8;         // dO_i loaded
+  const uint32_t bOe = bOf + 8;         // dO stage free (after the unit's last dP)
+  const uint32_t bKf = bOe + 8;         // [KS] K slot full
+  const uint32_t bKe = bKf + 8 * T::KS; // [KS] K slot free (after dQ += dS K_j)
+  const uint32_t bVf = bKe + 8 * T::KS; // [VS] V slot full
+  const uint32_t bVe = bVf + 8 * T::VS; // [VS] V slot free (after dP_j)
+  const uint32_t bS = bVe + 8 * T::VS;  // [2] S_j ready in buffer j & 1
+  const uint32_t bDp = bS + 16;         // dP_j ready
+  const uint32_t bDpc = bDp + 8;        // dP_j copied out of TMEM (256 arrivals)
+  const uint32_t bDs = bDpc + 8;        // dS_j in TMEM (256 arrivals)
+  const uint32_t bFin = bDs + 8;        // every MMA of the unit done
+  const uint32_t bUf = bFin + 8;        // [2] unit ring entry written
+  const uint32_t bUv = bUf + 16;        // [2] its row vectors written (64 arrivals)
+  const uint32_t bUe = bUv + 16;        // [2] unit ring entry read
+  const uint32_t bDrain = bUe + 16;
+  static_assert(4 + 2 * T::KS + 2 * T::VS + 2 + 4 + 6 + 1 == T::NBAR, "barrier count");
+  uint8_t* const misc = smem_raw + (sBar - base) + 8 * T::NBAR;
+  uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(misc);
+  volatile int* const abort_flag = reinterpret_cast<volatile int*>(misc + 4);
+  volatile int* const unit_ring = reinterpret_cast<volatile int*>(misc + 8);  // [2]
+  volatile int* const vec_stop = reinterpret_cast<volatile int*>(misc + 16);  // the vector warps stop
+  float* const vec_s = reinterpret_cast<float*>(smem_raw + (sVec - base));
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // A unit's head, query tile and key tiles visited (causal: up to the tile
+  // holding the last row's last visible key, query row r at position
+  // koff + r).
+  auto unit_of = [&](int u, int& bh, int& i, int& n) {
+    int lv;
+    work_unit(u, p.nq, p.B * p.H, p.tail, bh, lv);
+    i = p.nq - 1 - lv;
+    n = CAUSAL ? min(p.nkv, (p.koff + i * 128 + 127) / 128 + 1) : p.nkv;
+  };
+
+  if (threadIdx.x == 0) {
+    mbar_init(bQf, 1);
+    mbar_init(bQe, 1);
+    mbar_init(bOf, 1);
+    mbar_init(bOe, 1);
+    for (int s = 0; s < T::KS; ++s) {
+      mbar_init(bKf + 8u * s, 1);
+      mbar_init(bKe + 8u * s, 1);
+    }
+    for (int s = 0; s < T::VS; ++s) {
+      mbar_init(bVf + 8u * s, 1);
+      mbar_init(bVe + 8u * s, 1);
+    }
+    mbar_init(bS, 1);
+    mbar_init(bS + 8u, 1);
+    mbar_init(bDp, 1);
+    mbar_init(bDpc, 256);
+    mbar_init(bDs, 256);
+    mbar_init(bFin, 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(bUf + 8u * s, 1);
+      mbar_init(bUv + 8u * s, 64);
+      mbar_init(bUe + 8u * s, kDqUnitReaders);
+    }
+    mbar_init(bDrain, 1);
+    *abort_flag = 0;
+    *vec_stop = 0;
+    fence_mbar_init();
+  }
+  if (warp == 9) {
+    tmem_alloc(smem_u32(tmem_slot), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
+  const WaitCtx wc{abort_flag, p.status, p.limit_ns, p.info};
+  // The k-th unit this CTA takes, as read from the ring by the producer or
+  // the MMA warp (-1: none left, or the vector warps stopped).
+  auto next_unit = [&](int k, bool& ok) -> int {
+    const int e = k & 1;
+    ok = __all_sync(0xffffffffu, wait_bounded(wc, bUf + 8u * e, (k >> 1) & 1, wait_site(0xb0, k)));
+    const int u = ok ? unit_ring[e] : -1;
+    mbar_arrive(bUe + 8u * e);
+    return u;
+  };
+
+  if (warp < 8) {
+    setmaxnreg_inc<200>();
+    reg_split_sync(384);
+    // ------------------------------------------------------------ compute
+    // Warpgroup X takes key columns [64X, 64X + 64) of each 128 x 128
+    // (queries x keys) tile, one thread per query row; the body is
+    // bwd_dq_kernel's for the dense batch.
+    const int X = warp >> 2;
+    const int r = threadIdx.x & 127;  // query row within the tile == TMEM lane
+    const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+    const uint32_t tdP = tmem + 256 + 64 * X + lane_off;
+    const float2 c2 = make_float2(p.scale_log2, p.scale_log2);
+    uint32_t gs = 0;  // steps over all units so far
+    int kf = 0;       // units with steps so far
+    bool ok = true;
+    for (int k = 0; ok; ++k) {
+      // The unit and this row's vectors (-lse2, -D) from ring entry k & 1.
+      const int e = k & 1;
+      ok = __all_sync(0xffffffffu, wait_bounded(wc, bUf + 8u * e, (k >> 1) & 1, wait_site(0xb1, k)));
+      const int u = ok ? unit_ring[e] : -1;
+      float l2 = -INFINITY, nD = 0.f;
+      if (u >= 0) {
+        ok = __all_sync(0xffffffffu, wait_bounded(wc, bUv + 8u * e, (k >> 1) & 1, wait_site(0xb2, k)));
+        if (ok) {
+          l2 = vec_s[e * 256 + r];
+          nD = vec_s[e * 256 + 128 + r];
+        }
+      }
+      mbar_arrive(bUe + 8u * e);
+      if (u < 0 || !ok) break;
+      int bh, i, n;
+      unit_of(u, bh, i, n);
+      const int row = 128 * i + r;
+      uint16_t* const dqrow = p.dq + ((size_t)bh * p.N + row) * D;
+      const bool row_ok =
+          row < p.N && ATTN_IN_RANGE(((size_t)bh * p.N + row) * D + D - 1, (size_t)p.B * p.H * p.N * D, p, 0x209);
+      if (n <= 0) {
+        // No row of the tile sees a key: dQ = 0 (the vector warps wrote the
+        // rows' vectors).
+        if (row_ok)
+          for (int c8 = X * (D / 16); c8 < (X + 1) * (D / 16); ++c8)
+            *reinterpret_cast<uint4*>(dqrow + 8 * c8) = make_uint4(0, 0, 0, 0);
+        continue;
+      }
+      const float2 l22 = make_float2(l2, l2), nD2 = make_float2(nD, nD);
+      // Key columns at or past lim0 - 128 j of key tile j are invisible to
+      // row r: keys past Nk, and for causal rows keys past position
+      // koff + 128 i + r.
+      const int lim0 = (CAUSAL ? min(p.Nk, p.koff + 128 * i + r + 1) : p.Nk) - 64 * X;
+      for (int j = 0; j < n; ++j, ++gs) {
+        const uint32_t tS = tmem + (gs & 1) * 128 + 64 * X + lane_off;
+        ok = __all_sync(0xffffffffu, wait_bounded(wc, bS + 8u * (gs & 1), (gs >> 1) & 1, wait_site(0xb3, j)));
+        if (!ok) break;
+        tc_fence_after();
+        float x[64];
+        {
+          uint32_t ra[32], rb[32];
+          tmem_ld32(tS + 0, ra);
+          tmem_ld32(tS + 32, rb);
+          tmem_wait_ld();
+          reg_fence(ra);
+          reg_fence(rb);
+#pragma unroll
+          for (int q = 0; q < 32; ++q) {
+            x[q] = __uint_as_float(ra[q]);
+            x[32 + q] = __uint_as_float(rb[q]);
+          }
+        }
+        // P[r][k] = exp2(S * scale * log2e - lse2[r]); invisible keys (past
+        // the row's causal position, or past Nk) are exactly 0.
+#pragma unroll
+        for (int q = 0; q < 32; ++q) {
+          const float2 t = ffma2(make_float2(x[2 * q], x[2 * q + 1]), c2, l22);
+          x[2 * q] = ex2(t.x);
+          x[2 * q + 1] = ex2(t.y);
+        }
+        {
+          const int lim = lim0 - 128 * j;
+          if (__any_sync(0xffffffffu, lim < 64)) {
+#pragma unroll
+            for (int q = 0; q < 64; ++q)
+              if (q >= lim) x[q] = 0.f;
+          }
+        }
+        ok = __all_sync(0xffffffffu, wait_bounded(wc, bDp, gs & 1, wait_site(0xb4, j)));
+        if (!ok) break;
+        tc_fence_after();
+        // dS[r][k] = P * (dP - D) -> bf16 pairs over this warpgroup's S columns
+        uint32_t w[32];
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          uint32_t g[32];
+          tmem_ld32(tdP + 32 * hh, g);
+          tmem_wait_ld();
+          reg_fence(g);
+#pragma unroll
+          for (int q = 0; q < 16; ++q) {
+            const int c = 32 * hh + 2 * q;
+            const float2 ds = fmul2(make_float2(x[c], x[c + 1]),
+                                    fadd2(make_float2(__uint_as_float(g[2 * q]), __uint_as_float(g[2 * q + 1])), nD2));
+            w[16 * hh + q] = pack_bf16(ds.x, ds.y);
+          }
+        }
+        tc_fence_before();
+        mbar_arrive(bDpc);  // the dP columns may be overwritten
+        tmem_st32(tS, w);
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(bDs);
+      }
+      if (!ok) break;
+      // ---------------------------------------------------------- dQ out
+      // dQ_i = scale * (sum_j dS K_j) -> bf16 -> this row of dQ, from
+      // registers; warpgroup X takes the 32-column groups cc with
+      // cc % 2 == X.  The next unit's first dQ product, which overwrites the
+      // accumulator, waits for this warpgroup's next dS, published after
+      // these loads.
+      ok = __all_sync(0xffffffffu, wait_bounded(wc, bFin, kf & 1, wait_site(0xb5, k)));
+      if (!ok) break;
+      ++kf;
+      tc_fence_after();
+      const uint32_t tQd = tmem + 384 + lane_off;
+      const float2 s2 = make_float2(p.scale, p.scale);
+#pragma unroll
+      for (int cc = X; cc < D / 32; cc += 2) {
+        uint32_t o[32];
+        tmem_ld32(tQd + cc * 32, o);
+        tmem_wait_ld();
+        reg_fence(o);
+        if (row_ok) {
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4) {
+            uint32_t ww[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              const float2 t =
+                  fmul2(make_float2(__uint_as_float(o[q4 * 8 + 2 * q]), __uint_as_float(o[q4 * 8 + 2 * q + 1])), s2);
+              ww[q] = pack_bf16(t.x, t.y);
+            }
+            *reinterpret_cast<uint4*>(dqrow + cc * 32 + q4 * 8) = make_uint4(ww[0], ww[1], ww[2], ww[3]);
+          }
+        }
+      }
+    }
+    setmaxnreg_dec<168>();
+  } else {
+    setmaxnreg_dec<104>();
+    reg_split_sync(384);
+    if (warp == 8) {
+      // ------------------------------------------------------------ producer: Q, dO, K, V
+      // Per unit, in the order the MMA warp consumes them: Q_i (once the
+      // previous unit's last S has read its stage), K_0, dO_i (once the
+      // previous unit's last dP has read its stage), V_0, then K_j, V_j.
+      // The K and V slots and phases follow the step count over all units.
+      bool ok = true;
+      int kq = 0, ko = 0;  // units with steps whose Q, whose dO were issued
+      uint32_t gk = 0;  // K tiles issued over all units (== steps)
+      uint32_t gv = 0;  // V tiles issued
+      if (lane == 0) {
+        tma_prefetch_desc(&tmQ);
+        tma_prefetch_desc(&tmK);
+        tma_prefetch_desc(&tmV);
+        tma_prefetch_desc(&tmdO);
+      }
+      for (int k = 0; ok; ++k) {
+        const int u = next_unit(k, ok);
+        if (u < 0) break;
+        int bh, i, n;
+        unit_of(u, bh, i, n);
+        if (n <= 0) continue;
+        if (lane == 0) {
+          const int b = bh / p.H, h = bh % p.H;
+          const int bhk = b * p.Hkv + h / p.G;
+          auto load_k = [&](int j) -> bool {
+            const uint32_t s = gk % T::KS, rd = gk / T::KS;
+            if (rd > 0 && !wait_bounded(wc, bKe + 8u * s, (rd - 1) & 1, wait_site(0xb8, j))) return false;
+            // (p.debug_drop_p: a test of the bounded waits skips one K load of unit 0)
+            if (!(u == 0 && p.debug_drop_p == j + 1)) {
+              mbar_expect_tx(bKf + 8u * s, T::TILE_BYTES);
+              for (int cb = 0; cb < T::NB; ++cb)
+                tma_load_3d(sK + s * T::TILE_BYTES + cb * T::BLOCK_BYTES, &tmK, bKf + 8u * s, cb * 64, j * 128, bhk);
+            }
+            ++gk;
+            return true;
+          };
+          auto load_v = [&](int j) -> bool {
+            const uint32_t s = gv % T::VS, rd = gv / T::VS;
+            if (rd > 0 && !wait_bounded(wc, bVe + 8u * s, (rd - 1) & 1, wait_site(0xba, j))) return false;
+            mbar_expect_tx(bVf + 8u * s, T::TILE_BYTES);
+            for (int cb = 0; cb < T::NB; ++cb)
+              tma_load_3d(sV + s * T::TILE_BYTES + cb * T::BLOCK_BYTES, &tmV, bVf + 8u * s, cb * 64, j * 128, bhk);
+            ++gv;
+            return true;
+          };
+          ok = kq == 0 || wait_bounded(wc, bQe, (kq - 1) & 1, wait_site(0xb7, k));
+          if (ok) {
+            mbar_expect_tx(bQf, T::TILE_BYTES);
+            for (int cb = 0; cb < T::NB; ++cb) tma_load_3d(sQ + cb * T::BLOCK_BYTES, &tmQ, bQf, cb * 64, i * 128, bh);
+            ++kq;
+            ok = load_k(0);
+          }
+          if (ok) ok = ko == 0 || wait_bounded(wc, bOe, (ko - 1) & 1, wait_site(0xb9, k));
+          if (ok) {
+            mbar_expect_tx(bOf, T::TILE_BYTES);
+            for (int cb = 0; cb < T::NB; ++cb) tma_load_3d(sdO + cb * T::BLOCK_BYTES, &tmdO, bOf, cb * 64, i * 128, bh);
+            ++ko;
+            ok = load_v(0);
+          }
+          for (int j = 1; j < n && ok; ++j) ok = load_k(j) && load_v(j);
+        }
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+      }
+      // Every copy issued above has landed before the CTA may exit (bounded:
+      // after an abort, or a load the test hook skipped, some never do).
+      if (lane == 0) {
+        if (kq > 0) wait_drain(bQf, (kq - 1) & 1, p.limit_ns);
+        if (ko > 0) wait_drain(bOf, (ko - 1) & 1, p.limit_ns);
+        for (uint32_t s = 0; s < T::KS && s < gk; ++s) {
+          const uint32_t last = ((gk - 1 - s) / T::KS) * T::KS + s;
+          wait_drain(bKf + 8u * s, (last / T::KS) & 1, p.limit_ns);
+        }
+        for (uint32_t s = 0; s < T::VS && s < gv; ++s) {
+          const uint32_t last = ((gv - 1 - s) / T::VS) * T::VS + s;
+          wait_drain(bVf + 8u * s, (last / T::VS) & 1, p.limit_ns);
+        }
+      }
+      __syncwarp();
+    } else if (warp == 9) {
+      // ------------------------------------------------------------ MMA issuer
+      // bwd_dq_kernel's schedule for each unit in turn; per step j:
+      // dP_{j+1} (once dP_j has been read), dQ += dS_j K_j, S_{j+2} into the
+      // S buffer dS_j occupied.  Buffers, slots and per-step barrier phases
+      // follow the step count over all units.  A unit's first products wait
+      // for its Q, dO, K_0, V_0 and for the previous unit's last dP to have
+      // been read; the S buffers they overwrite were last read by dQ
+      // products issued before them (MMAs from one thread run in order).
+      {
+        const uint32_t leader = elect_one();
+        constexpr uint32_t I_SS = idesc_bf16_f32(128, 128, false, false);  // S, dP (K-major x K-major)
+        constexpr uint32_t I_DQ = idesc_bf16_f32(128, D, false, true);     // dQ (A in TMEM, B MN-major)
+        const uint32_t tdP = tmem + 256, tdQ = tmem + 384;
+        const uint64_t dQk = sdesc_sw128(sQ, 16, 1024);                 // Q, K-major A
+        const uint64_t dOk = sdesc_sw128(sdO, 16, 1024);                // dO, K-major A
+        const uint64_t dKk0 = sdesc_sw128(sK, 16, 1024);                // K slot 0, K-major B (S)
+        const uint64_t dKmn0 = sdesc_sw128(sK, T::BLOCK_BYTES, 1024);   // K slot 0, MN-major B (dQ)
+        const uint64_t dVk0 = sdesc_sw128(sV, 16, 1024);                // V slot 0, K-major B (dP)
+        auto mma_kk = [&](uint32_t dst, uint64_t ad, uint64_t bd, uint32_t idesc) {
+#pragma unroll
+          for (int kk = 0; kk < T::KSTEPS; ++kk) {
+            const uint32_t off = (kk >> 2) * T::BLOCK_BYTES + (kk & 3) * 32;
+            mma_ss_p(leader, dst, sdesc_add(ad, off), sdesc_add(bd, off), idesc, kk > 0);
+          }
+        };
+        auto wait_all = [&](uint32_t bar, uint32_t parity, int site) {
+          return __all_sync(0xffffffffu, wait_bounded(wc, bar, parity, site));
+        };
+        // K_g and V_g (step g over all units) loaded.
+        auto k_full = [&](uint32_t g, int site) { return wait_all(bKf + 8u * (g % T::KS), (g / T::KS) & 1, site); };
+        auto v_full = [&](uint32_t g, int site) { return wait_all(bVf + 8u * (g % T::VS), (g / T::VS) & 1, site); };
+        auto s_buf = [&](uint32_t g) { return tmem + (g & 1) * 128; };
+        bool ok = true;
+        uint32_t gs = 0;  // steps over all units
+        int kq = 0;       // units with steps so far
+        for (int k = 0; ok; ++k) {
+          const int u = next_unit(k, ok);
+          if (u < 0) break;
+          int bh, i, n;
+          unit_of(u, bh, i, n);
+          if (n <= 0) continue;
+          const uint32_t g0 = gs;
+          // The unit's first products: S_0, dP_0, S_1.  (As in the loop,
+          // the checks for a group run before the previous group's commit.)
+          ok = wait_all(bQf, kq & 1, wait_site(0xbb, k)) && k_full(g0, wait_site(0xbc, 0));
+          if (!ok) break;
+          tc_fence_after();
+          mma_kk(s_buf(g0), dQk, sdesc_add(dKk0, (g0 % T::KS) * T::TILE_BYTES), I_SS);  // S_0
+          // for dP_0: dO_i and V_0 loaded, the previous unit's last dP read
+          ok = wait_all(bOf, kq & 1, wait_site(0xf0, k)) && v_full(g0, wait_site(0xbd, 0)) &&
+               (g0 == 0 || wait_all(bDpc, (g0 - 1) & 1, wait_site(0xbe, 0)));
+          mma_commit_p(leader, bS + 8u * (g0 & 1));
+          if (n == 1) mma_commit_p(leader, bQe);  // Q_i read for the last time
+          if (!ok) break;
+          tc_fence_after();
+          mma_kk(tdP, dOk, sdesc_add(dVk0, (g0 % T::VS) * T::TILE_BYTES), I_SS);  // dP_0
+          if (n > 1) ok = k_full(g0 + 1, wait_site(0xbc, 1));                  // for S_1
+          mma_commit_p(leader, bDp);
+          mma_commit_p(leader, bVe + 8u * (g0 % T::VS));  // V_0 consumed
+          if (n == 1) mma_commit_p(leader, bOe);          // dO_i read for the last time
+          if (ok && n > 1) {
+            tc_fence_after();
+            mma_kk(s_buf(g0 + 1), dQk, sdesc_add(dKk0, ((g0 + 1) % T::KS) * T::TILE_BYTES), I_SS);  // S_1
+            // for dP_1: V_1 loaded, dP_0 read
+            ok = v_full(g0 + 1, wait_site(0xbd, 1)) && wait_all(bDpc, g0 & 1, wait_site(0xbe, 1));
+            mma_commit_p(leader, bS + 8u * ((g0 + 1) & 1));
+            if (n == 2) mma_commit_p(leader, bQe);
+          }
+          for (int j = 0; j < n && ok; ++j) {
+            const uint32_t g = g0 + j;
+            if (j + 1 < n) {
+              tc_fence_after();
+              mma_kk(tdP, dOk, sdesc_add(dVk0, ((g + 1) % T::VS) * T::TILE_BYTES), I_SS);  // dP_{j+1}
+              ok = wait_all(bDs, g & 1, wait_site(0xbf, j));                            // for dQ_j
+              mma_commit_p(leader, bDp);
+              mma_commit_p(leader, bVe + 8u * ((g + 1) % T::VS));
+              if (j + 2 == n) mma_commit_p(leader, bOe);
+            } else {
+              ok = wait_all(bDs, g & 1, wait_site(0xbf, j));
+            }
+            if (!ok) break;
+            tc_fence_after();
+            // dQ += dS_j K_j: A = dS in TMEM (keys 64X.. of warpgroup X at
+            // columns 64X.., bf16 pairs), B = K_j (MN-major, N = d)
+            const uint32_t ks = g % T::KS;
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk)
+              mma_ts_p(leader, tdQ, s_buf(g) + 64 * (kk >> 2) + (kk & 3) * 8,
+                       sdesc_add(dKmn0, ks * T::TILE_BYTES + kk * 2048), I_DQ, (j > 0 || kk > 0) ? 1u : 0u);
+            if (j + 2 < n) ok = k_full(g + 2, wait_site(0xbc, j + 2));  // for S_{j+2}
+            mma_commit_p(leader, bKe + 8u * ks);                        // K_j consumed
+            if (!ok) break;
+            if (j + 2 < n) {
+              tc_fence_after();
+              mma_kk(s_buf(g), dQk, sdesc_add(dKk0, ((g + 2) % T::KS) * T::TILE_BYTES), I_SS);  // S_{j+2}
+              // for dP_{j+2}: V_{j+2} loaded, dP_{j+1} read
+              ok = v_full(g + 2, wait_site(0xbd, j + 2)) && wait_all(bDpc, (g + 1) & 1, wait_site(0xbe, j + 1));
+              mma_commit_p(leader, bS + 8u * (g & 1));
+              if (j + 3 == n) mma_commit_p(leader, bQe);
+            }
+          }
+          if (!ok) break;
+          mma_commit_p(leader, bFin);
+          gs += n;
+          ++kq;
+        }
+        mma_commit_p(leader, bDrain);  // fires once every MMA issued above has finished
+        wait_drain(bDrain, 0, p.limit_ns);
+      }
+      __syncwarp();
+    } else {
+      // ------------------------------------------------------------ warps 10-11: queue, row vectors
+      // Warp 10 takes the next unit once ring entry k & 1 is free; then both
+      // warps write that unit's row vectors into the entry.  Their barrier
+      // is reached by both warps in every round, so that a stop is seen by
+      // both.
+      const int t = (int)threadIdx.x - 320;  // 0..63
+      for (int k = 0;; ++k) {
+        const int e = k & 1;
+        if (warp == 10) {
+          const bool ok =
+              k < 2 || __all_sync(0xffffffffu, wait_bounded(wc, bUe + 8u * e, ((k - 2) >> 1) & 1, wait_site(0xb6, k)));
+          if (lane == 0) {
+            if (ok) {
+              int u = atomicAdd(p.sched, 1);
+              if (u >= p.n_units) u = -1;
+              unit_ring[e] = u;
+              mbar_arrive(bUf + 8u * e);  // (release: the entry is visible to the roles that wait for it)
+            } else {
+              *vec_stop = 1;
+            }
+          }
+        }
+        named_bar_sync(kVecBarrier, 64);
+        const int u = unit_ring[e];
+        if (*vec_stop || u < 0) break;
+        int bh, i, n;
+        unit_of(u, bh, i, n);
+        if (t == 0 && n > 0) {
+          // Q_i and dO_i into L2 ahead of the producer's loads.
+          for (int cb = 0; cb < T::NB; ++cb) {
+            tma_prefetch_l2_3d(&tmQ, cb * 64, i * 128, bh);
+            tma_prefetch_l2_3d(&tmdO, cb * 64, i * 128, bh);
+          }
+        }
+        float* const ve = vec_s + e * 256;
+        for (int rr = t; rr < 128; rr += 64) {
+          const int row = 128 * i + rr;
+          const size_t vrow = (size_t)bh * p.Npad + row;
+          float l2 = -INFINITY, nD = 0.f;  // rows that see no key: P = 0
+          if (n > 0 && p.rows_in_dq) {
+            // -lse * log2(e) and -D = -rowsum(dO * O), D as the sum of the
+            // two column halves' sums, each summed in column order (the
+            // order of bwd_dq_kernel, so that the bits agree).
+            float l = -INFINITY, part[2] = {0.f, 0.f};
+            const size_t orow = (size_t)bh * p.N + row;
+            if (row < p.N && ATTN_IN_RANGE(orow * D + D - 1, (size_t)p.B * p.H * p.N * D, p, 0x20a)) {
+              l = p.lse[orow];
+              const uint4* po = reinterpret_cast<const uint4*>(p.o + orow * D);
+              const uint4* pg = reinterpret_cast<const uint4*>(p.dout + orow * D);
+#pragma unroll
+              for (int X = 0; X < 2; ++X) {
+                uint4 a[D / 16], g[D / 16];
+#pragma unroll
+                for (int c = 0; c < D / 16; ++c) {
+                  a[c] = __ldg(po + X * (D / 16) + c);
+                  g[c] = __ldg(pg + X * (D / 16) + c);
+                }
+                float s = 0.f;
+#pragma unroll
+                for (int c = 0; c < D / 16; ++c) {
+                  const uint32_t aw[4] = {a[c].x, a[c].y, a[c].z, a[c].w}, gw[4] = {g[c].x, g[c].y, g[c].z, g[c].w};
+#pragma unroll
+                  for (int q = 0; q < 4; ++q) {
+                    const float2 af = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&aw[q]));
+                    const float2 gf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&gw[q]));
+                    s = fmaf(af.x, gf.x, s);
+                    s = fmaf(af.y, gf.y, s);
+                  }
+                }
+                part[X] = s;
+              }
+            }
+            nD = row < p.N ? -(part[0] + part[1]) : 0.f;
+            l2 = (l == -INFINITY) ? -INFINITY : -l * 1.4426950408889634f;
+          } else if (n > 0 && ATTN_IN_RANGE(vrow, vec_floats(p), p, 0x20b)) {
+            // formed by an earlier stage
+            l2 = p.lse2[vrow];
+            nD = p.dvec[vrow];
+          }
+          ve[rr] = l2;
+          ve[128 + rr] = nD;
+          if (p.rows_in_dq && ATTN_IN_RANGE(vrow, vec_floats(p), p, 0x20c)) {
+            p.dvec[vrow] = nD;
+            p.lse2[vrow] = l2;
+          }
+        }
+        mbar_arrive(bUv + 8u * e);  // (release: the vectors are visible to the compute threads)
+      }
+    }
+    setmaxnreg_inc<168>();
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 9) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+  // The last CTA to finish resets the queue for the next launch that uses
+  // this slot (every CTA's vector warps have stopped taking units by now).
+  if (threadIdx.x == 0) {
+    __threadfence();
+    if (atomicAdd(p.sched + 1, 1) == (int)gridDim.x - 1) {
+      atomicExch(p.sched, 0);
+      atomicExch(p.sched + 1, 0);
+    }
+  }
+}
+
+namespace {
+
+// Queue slots (next unit, CTAs done), one per launch in flight (see
+// attn_fwd_persist.cu).
+constexpr int kDqQueueSlots = 256;
+__device__ int g_dq_queue[kDqQueueSlots][2];
+
+int* dq_queue_slot() {
+  static std::atomic<unsigned> next{0};
+  static int* base[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  if (base[dev] == nullptr) {
+    void* a = nullptr;
+    if (cudaGetSymbolAddress(&a, g_dq_queue) != cudaSuccess) return nullptr;
+    base[dev] = static_cast<int*>(a);
+  }
+  return base[dev] + 2 * (next.fetch_add(1) % kDqQueueSlots);
+}
+
+template <int D, bool C>
+cudaError_t launch_dq_persist_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                                const CUtensorMap& tdo, const BwdParams& p, cudaStream_t stream) {
+  using T = PQTraits<D>;
+  auto kern = bwd_dq_persist_kernel<D, C>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, T::SMEM);
+  if (e != cudaSuccess) return e;
+  int dev = 0, sms = 152;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return cudaErrorInvalidValue;
+  BwdParams pc = p;
+  pc.n_units = p.nq * p.B * p.H;
+  pc.tail = uniform_levels(C, p.vl, p.mk, false) ? 1 : order_tail(p.nq, p.B * p.H, p.G);
+  pc.sched = dq_queue_slot();
+  if (pc.sched == nullptr) return cudaErrorInvalidValue;
+  const unsigned grid = (unsigned)min(pc.n_units, sms);  // one CTA per SM
+  kern<<<grid, T::THREADS, T::SMEM, stream>>>(tq, tk, tv, tdo, pc);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_bwd_dq_persist(int d, bool causal, const CUtensorMap& tq, const CUtensorMap& tk,
+                                  const CUtensorMap& tv, const CUtensorMap& tdo, const BwdParams& p,
+                                  cudaStream_t stream) {
+  switch (d) {
+    case 64: return causal ? launch_dq_persist_t<64, true>(tq, tk, tv, tdo, p, stream) : launch_dq_persist_t<64, false>(tq, tk, tv, tdo, p, stream);
+    case 96: return causal ? launch_dq_persist_t<96, true>(tq, tk, tv, tdo, p, stream) : launch_dq_persist_t<96, false>(tq, tk, tv, tdo, p, stream);
+    case 128:
+      return causal ? launch_dq_persist_t<128, true>(tq, tk, tv, tdo, p, stream) : launch_dq_persist_t<128, false>(tq, tk, tv, tdo, p, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace sdpa

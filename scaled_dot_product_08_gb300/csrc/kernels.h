@@ -105,9 +105,10 @@ struct BwdParams {
   int debug_drop1;       // 0; n > 0 only in a test of the bounded waits: CTA 0's producer skips ring load n - 1
   int tail;              // heads in the level-major tail of the CTA order (work_unit); set by each launcher
   int debug_plant;       // 0; 2 only in a test of the debug build's checks: CTA 0 of the dQ kernel offsets its row-vector store out of range
-  int* sched;            // persistent dK/dV kernel: this launch's queue (next unit, CTAs done); set by its launcher
-  int n_units;           // persistent dK/dV kernel: units in the launch
-  int debug_drop_p;      // 0; n > 0 only in a test of the bounded waits: the persistent dK/dV kernel skips unit 0's Q load n - 1
+  int* sched;            // persistent dQ and dK/dV kernels: this launch's queue (next unit, CTAs done); set by its launcher
+  int n_units;           // persistent dQ and dK/dV kernels: units in the launch
+  int debug_drop_p;      // 0; n > 0 only in a test of the bounded waits: the persistent dK/dV kernel skips unit 0's
+                         // Q load n - 1, the persistent dQ kernel its K load n - 1
 };
 
 // CTA order of the forward, dQ and dK/dV launches.  A launch's CTAs cover
@@ -340,6 +341,12 @@ cudaError_t launch_bwd_prep(const BwdParams& p, cudaStream_t stream);
 cudaError_t launch_bwd_grad_persist(int d, bool causal, const CUtensorMap& tq, const CUtensorMap& tk,
                                     const CUtensorMap& tv, const CUtensorMap& tdo, const BwdParams& p,
                                     cudaStream_t stream);
+// The dQ kernel of the dense backward (no mask, no packed batch) as a
+// persistent kernel; dQ is written through p.dq, and with p.rows_in_dq the
+// row vectors are formed from p.o, p.dout and p.lse.
+cudaError_t launch_bwd_dq_persist(int d, bool causal, const CUtensorMap& tq, const CUtensorMap& tk,
+                                  const CUtensorMap& tv, const CUtensorMap& tdo, const BwdParams& p,
+                                  cudaStream_t stream);
 // tbt (masked, bf16 additive mask, no boolean mask): a map over the mask's
 // transpose (planes, Nk, Nq) with boxes of 128 rows x 64 columns, 128-byte
 // swizzle; given, the dK/dV kernel stages its tiles by TMA.

@@ -6,7 +6,8 @@ load must give up, record ATTN_ERR_TIMEOUT with the CTA and the wait site,
 and every role of the CTA must stop and exit (each named barrier is reached
 whatever a wait returned), so that the launch ends and the context stays
 usable.  The CTAs that lost nothing complete normally, and the next normal
-call is correct.  One case per kernel: forward, dQ, dK/dV.
+call is correct.  One case per kernel: forward, dQ, dK/dV, and the
+persistent forward, dK/dV and dQ kernels.
 """
 import math
 
@@ -126,6 +127,33 @@ def test_persistent_dkdv_dropped_load_times_out_and_recovers(cuda_lib):
     assert st == cuda_lib.Status.OK
     assert cuda_lib.attn_get_device_status(None) == cuda_lib.Status.TIMEOUT
     assert info[0] >> 16 in PERSIST_GRAD_SITES, hex(info[0] >> 16)
+    assert info[3] >= LIMIT_US * 0.9
+    grads = [host(g) for g in cuda_lib.backward(tq, tk, tv, O, lse, tdo, s, True)]
+    check_grads(grads, oracle.attention_backward(q, k, v, do, s, True), "after the timeout")
+    assert cuda_lib.attn_get_device_status(None) == cuda_lib.Status.OK
+
+
+PERSIST_DQ_SITES = set(range(0xb0, 0xc0)) | {0xf0}
+
+
+def test_persistent_dq_dropped_load_times_out_and_recovers(cuda_lib):
+    # The persistent dQ kernel (attn_bwd's dense first stage): the CTA that
+    # takes the first work unit (head 0, query tile 3: four key tiles) skips
+    # that unit's K_1 load.
+    import torch
+    B, H, N, d = 1, 2, 512, 128
+    q, k, v, do = _inputs(B, H, N, d, 65000)
+    s = 1 / math.sqrt(d)
+    tq, tk, tv, tdo = dev(q), dev(k), dev(v), dev(do)
+    O, lse = cuda_lib.forward(tq, tk, tv, s, True)
+    assert cuda_lib.attn_get_device_status(None) == cuda_lib.Status.OK
+    assert cuda_lib.attn_debug_drop_load(5, 1, LIMIT_US) == cuda_lib.Status.OK
+    cuda_lib.backward(tq, tk, tv, O, lse, tdo, s, True)
+    torch.cuda.synchronize()
+    st, info = cuda_lib.attn_get_timeout_info(None)
+    assert st == cuda_lib.Status.OK
+    assert cuda_lib.attn_get_device_status(None) == cuda_lib.Status.TIMEOUT
+    assert info[0] >> 16 in PERSIST_DQ_SITES, hex(info[0] >> 16)
     assert info[3] >= LIMIT_US * 0.9
     grads = [host(g) for g in cuda_lib.backward(tq, tk, tv, O, lse, tdo, s, True)]
     check_grads(grads, oracle.attention_backward(q, k, v, do, s, True), "after the timeout")
