@@ -24,8 +24,10 @@
 //     and dO have empty barriers, committed after the unit's last S and last
 //     dP products, so the next unit's tiles load while the current unit's
 //     last steps run;
-//   * dQ leaves from registers straight to global memory, and the next
-//     unit's first products (S_0, dP_0, S_1) run during that epilogue.
+//   * dQ leaves from registers straight to global memory (each warp's rows
+//     transposed across its lanes so that a store covers whole lines), and
+//     the next unit's first products (S_0, dP_0, S_1) run during that
+//     epilogue.
 #include <atomic>
 #include <cmath>
 
@@ -205,14 +207,12 @@ __global__ void __launch_bounds__(384, 1)
       if (u < 0 || !ok) break;
       int bh, i, n;
       unit_of(u, bh, i, n);
-      const int row = 128 * i + r;
-      uint16_t* const dqrow = p.dq + ((size_t)bh * p.N + row) * D;
-      const bool row_ok =
-          row < p.N && ATTN_IN_RANGE(((size_t)bh * p.N + row) * D + D - 1, (size_t)p.B * p.H * p.N * D, p, 0x209);
       if (n <= 0) {
         // No row of the tile sees a key: dQ = 0 (the vector warps wrote the
         // rows' vectors).
-        if (row_ok)
+        const int row = 128 * i + r;
+        uint16_t* const dqrow = p.dq + ((size_t)bh * p.N + row) * D;
+        if (row < p.N && ATTN_IN_RANGE(((size_t)bh * p.N + row) * D + D - 1, (size_t)p.B * p.H * p.N * D, p, 0x209))
           for (int c8 = X * (D / 16); c8 < (X + 1) * (D / 16); ++c8)
             *reinterpret_cast<uint4*>(dqrow + 8 * c8) = make_uint4(0, 0, 0, 0);
         continue;
@@ -285,24 +285,31 @@ __global__ void __launch_bounds__(384, 1)
       }
       if (!ok) break;
       // ---------------------------------------------------------- dQ out
-      // dQ_i = scale * (sum_j dS K_j) -> bf16 -> this row of dQ, from
-      // registers; warpgroup X takes the 32-column groups cc with
-      // cc % 2 == X.  The next unit's first dQ product, which overwrites the
-      // accumulator, waits for this warpgroup's next dS, published after
-      // these loads.
+      // dQ_i = scale * (sum_j dS K_j) -> bf16 -> dQ, from registers:
+      // warpgroup X takes the 32-column groups [X GH, min(G, (X + 1) GH)),
+      // and each warp writes its 32 rows a row slice per group of lanes
+      // (store_rows_transposed), whole lines per store.  The next unit's
+      // first dQ product, which overwrites the accumulator, waits for this
+      // warpgroup's next dS, published after these loads.
       ok = __all_sync(0xffffffffu, wait_bounded(wc, bFin, kf & 1, wait_site(0xb5, k)));
       if (!ok) break;
       ++kf;
       tc_fence_after();
-      const uint32_t tQd = tmem + 384 + lane_off;
-      const float2 s2 = make_float2(p.scale, p.scale);
-#pragma unroll
-      for (int cc = X; cc < D / 32; cc += 2) {
-        uint32_t o[32];
-        tmem_ld32(tQd + cc * 32, o);
-        tmem_wait_ld();
-        reg_fence(o);
-        if (row_ok) {
+      {
+        constexpr int G = D / 32, GH = (G + 1) / 2;
+        const uint32_t tQd = tmem + 384 + lane_off;
+        const float2 s2 = make_float2(p.scale, p.scale);
+        const int wr0 = 128 * i + 32 * (warp & 3);  // the warp's first row
+        uint16_t* const wdst = p.dq + ((size_t)bh * p.N + wr0) * D;
+        int nvalid = min(32, p.N - wr0);
+        if (nvalid > 0 && !ATTN_IN_RANGE(((size_t)bh * p.N + wr0 + nvalid) * D - 1, (size_t)p.B * p.H * p.N * D, p, 0x209))
+          nvalid = 0;
+        // Columns 32 cc .. 32 cc + 31 of this thread's row as four bf16 chunks.
+        auto chunks = [&](int cc, uint4* ch) {
+          uint32_t o[32];
+          tmem_ld32(tQd + cc * 32, o);
+          tmem_wait_ld();
+          reg_fence(o);
 #pragma unroll
           for (int q4 = 0; q4 < 4; ++q4) {
             uint32_t ww[4];
@@ -312,8 +319,27 @@ __global__ void __launch_bounds__(384, 1)
                   fmul2(make_float2(__uint_as_float(o[q4 * 8 + 2 * q]), __uint_as_float(o[q4 * 8 + 2 * q + 1])), s2);
               ww[q] = pack_bf16(t.x, t.y);
             }
-            *reinterpret_cast<uint4*>(dqrow + cc * 32 + q4 * 8) = make_uint4(ww[0], ww[1], ww[2], ww[3]);
+            ch[q4] = make_uint4(ww[0], ww[1], ww[2], ww[3]);
           }
+        };
+        if (X == 0 && GH == 2) {
+          uint4 ch[8];
+          chunks(0, ch);
+          chunks(1, ch + 4);
+          store_rows_transposed<8>(ch, wdst, D, nvalid);
+        } else if (X == 0) {
+          uint4 ch[4];
+          chunks(0, ch);
+          store_rows_transposed<4>(ch, wdst, D, nvalid);
+        } else if (G - GH == 2) {
+          uint4 ch[8];
+          chunks(GH, ch);
+          chunks(GH + 1, ch + 4);
+          store_rows_transposed<8>(ch, wdst + GH * 32, D, nvalid);
+        } else {
+          uint4 ch[4];
+          chunks(GH, ch);
+          store_rows_transposed<4>(ch, wdst + GH * 32, D, nvalid);
         }
       }
     }

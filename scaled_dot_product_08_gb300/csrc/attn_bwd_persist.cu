@@ -20,7 +20,8 @@
 //   * K and V have an empty barrier, committed once the unit's last S^T and
 //     dP^T products are issued (its last step needs only dV and dK, which
 //     read neither), so the next unit's K and V load during that step;
-//   * dK and dV leave from registers straight to global memory;
+//   * dK and dV leave from registers straight to global memory, each warp's
+//     rows transposed across its lanes so that a store covers whole lines;
 //   * a unit whose keys no query sees (causal cross attention) writes zeros
 //     and takes no loads or products.
 #include <atomic>
@@ -289,25 +290,43 @@ __global__ void __launch_bounds__(384, 1)
       tc_fence_after();
       const uint32_t src = tmem + (X ? 256u : 384u) + lane_off;
       const float2 f2 = X ? make_float2(p.scale, p.scale) : make_float2(1.f, 1.f);
-#pragma unroll
-      for (int cc = 0; cc < D / 32; ++cc) {
+      // The warp's 32 key rows 128 j + 32 (warp % 4) + lane, written a row
+      // slice per group of lanes (store_rows_transposed): whole 128-byte
+      // lines per store rather than 32 separate 16-byte pieces.
+      const int wr0 = 128 * x.j + 32 * (warp & 3);
+      uint16_t* const wdst = (X ? p.dk : p.dv) + ((size_t)x.bhk * p.Nk + wr0) * D;
+      int nvalid = min(32, p.Nk - wr0);
+      if (nvalid > 0 && !ATTN_IN_RANGE(((size_t)x.bhk * p.Nk + wr0 + nvalid) * D - 1, (size_t)p.B * p.Hkv * p.Nk * D, p, 0x306))
+        nvalid = 0;
+      // Columns 32 cc .. 32 cc + 31 of this thread's row as four bf16 chunks.
+      auto chunks = [&](int cc, uint4* ch) {
         uint32_t o[32];
         tmem_ld32(src + cc * 32, o);
         tmem_wait_ld();
         reg_fence(o);
-        if (row_ok) {
 #pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4) {
-            uint32_t wq[4];
+        for (int q4 = 0; q4 < 4; ++q4) {
+          uint32_t wq[4];
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const float2 t = fmul2(make_float2(__uint_as_float(o[q4 * 8 + 2 * e]),
-                                                 __uint_as_float(o[q4 * 8 + 2 * e + 1])), f2);
-              wq[e] = pack_bf16(t.x, t.y);
-            }
-            *reinterpret_cast<uint4*>(drow + cc * 32 + q4 * 8) = make_uint4(wq[0], wq[1], wq[2], wq[3]);
+          for (int e = 0; e < 4; ++e) {
+            const float2 t = fmul2(make_float2(__uint_as_float(o[q4 * 8 + 2 * e]),
+                                               __uint_as_float(o[q4 * 8 + 2 * e + 1])), f2);
+            wq[e] = pack_bf16(t.x, t.y);
           }
+          ch[q4] = make_uint4(wq[0], wq[1], wq[2], wq[3]);
         }
+      };
+#pragma unroll
+      for (int cc = 0; cc + 1 < D / 32; cc += 2) {
+        uint4 ch[8];
+        chunks(cc, ch);
+        chunks(cc + 1, ch + 4);
+        store_rows_transposed<8>(ch, wdst + cc * 32, D, nvalid);
+      }
+      if constexpr ((D / 32) % 2 != 0) {
+        uint4 ch[4];
+        chunks(D / 32 - 1, ch);
+        store_rows_transposed<4>(ch, wdst + (D / 32 - 1) * 32, D, nvalid);
       }
     }
     setmaxnreg_dec<168>();

@@ -467,4 +467,43 @@ __device__ __forceinline__ void store_rows_sw128(uint32_t stage, uint16_t* dst, 
   }
 }
 
+// Writes 16-byte chunks that the lanes of a warp hold one row each (lane l:
+// row l of the warp's 32 rows, x[k] = columns 8k .. 8k + 7 of a slice that
+// starts at dst for row 0; row r at dst + r * stride elements) so that every
+// store instruction covers whole slices of 32 / NCH rows, rather than 32
+// pieces of 32 rows: an NCH x NCH transpose of the chunks inside each group
+// of NCH lanes (log2 NCH stages: lanes whose bit m differs swap the chunks
+// whose bit m differs from theirs), after which lane g NCH + j holds chunk j
+// of rows g NCH + s in x[s].  Rows at or past nvalid are not written.  Every
+// lane of the warp takes part.
+template <int NCH>
+__device__ __forceinline__ void store_rows_transposed(uint4 (&x)[NCH], uint16_t* dst, size_t stride, int nvalid) {
+  static_assert(NCH == 2 || NCH == 4 || NCH == 8, "chunks per row");
+  const int lane = threadIdx.x & 31, li = lane & (NCH - 1);
+#pragma unroll
+  for (int m = NCH / 2; m >= 1; m >>= 1) {
+    const bool hi = (li & m) != 0;
+#pragma unroll
+    for (int k = 0; k < NCH; ++k) {
+      if (k & m) continue;
+      const uint4 out = hi ? x[k] : x[k | m];
+      uint4 in;
+      in.x = __shfl_xor_sync(0xffffffffu, out.x, m);
+      in.y = __shfl_xor_sync(0xffffffffu, out.y, m);
+      in.z = __shfl_xor_sync(0xffffffffu, out.z, m);
+      in.w = __shfl_xor_sync(0xffffffffu, out.w, m);
+      if (hi)
+        x[k] = in;
+      else
+        x[k | m] = in;
+    }
+  }
+  const int g = lane / NCH;
+#pragma unroll
+  for (int s = 0; s < NCH; ++s) {
+    const int r = g * NCH + s;
+    if (r < nvalid) *reinterpret_cast<uint4*>(dst + (size_t)r * stride + 8 * li) = x[s];
+  }
+}
+
 }  // namespace sdpa
