@@ -13,6 +13,16 @@
 //
 // GB300 mapping: bwd_dq_kernel's roles (warps 0-7 compute, warp 8 the TMA
 // producer, warp 9 the MMA issuer), with these differences:
+//   * Q_i and dO_i go from shared memory into tensor memory once per unit
+//     (the compute threads copy their rows), and S = Q K_j^T and
+//     dP = dO V_j^T take them from there: a 128 x 128 x 16 product with both
+//     operands in shared memory reads 8 KB per 64 cycles, as much as shared
+//     memory delivers, so with the K/V tiles streaming in the products were
+//     bound by shared-memory bandwidth; with A in tensor memory they read
+//     half of that.  The tensor memory that costs is won by keeping one S
+//     buffer (released as soon as the compute threads have loaded S_j, so
+//     S_{j+1} runs during the exponentials) and writing dS_j over dP_j;
+//     per step the products run S_{j+1}, dQ_j, dP_{j+1};
 //   * warps 10-11 take the units from the queue and pass each one on through
 //     a two-entry ring in shared memory, with the unit's row vectors (-lse2,
 //     -D for its 128 query rows), which they form from lse, O and dO in
@@ -20,14 +30,13 @@
 //     them) while the units before it run; they also write the vectors to
 //     the workspace for the dK/dV kernel, and ask L2 for the unit's Q and dO
 //     tiles ahead of the producer's loads;
-//   * the K and V rings and every per-step barrier run on across units; Q
-//     and dO have empty barriers, committed after the unit's last S and last
-//     dP products, so the next unit's tiles load while the current unit's
-//     last steps run;
+//   * the K and V rings and every per-step barrier run on across units, and
+//     the shared-memory Q and dO tiles are free once copied, so the next
+//     unit's tiles load while the current unit runs;
 //   * dQ leaves from registers straight to global memory (each warp's rows
-//     transposed across its lanes so that a store covers whole lines), and
-//     the next unit's first products (S_0, dP_0, S_1) run during that
-//     epilogue.
+//     transposed across its lanes so that a store covers whole lines).
+// Tensor memory: S [0,128), dP and then dS [128,256), dQ [256,256+d),
+// Q [384,384+d/2), dO [448,448+d/2) (bf16 pairs).
 #include <atomic>
 #include <cmath>
 
@@ -46,9 +55,9 @@ struct PQTraits {
   static constexpr int KSTEPS = D / 16;
   static constexpr int KS = 3, VS = 2;                 // K and V ring slots
   static constexpr int VEC_BYTES = 1024;               // -lse2[128], -D[128]
-  // q_full q_empty do_full do_empty k_full[3] k_empty[3] v_full[2] v_empty[2]
-  // s[2] dp dp_copied ds fin unit_full[2] unit_vec[2] unit_empty[2] drain
-  static constexpr int NBAR = 4 + 6 + 4 + 2 + 4 + 6 + 1;
+  // q_full do_full staged k_full[3] k_empty[3] v_full[2] v_empty[2]
+  // s s_read dp ds fin unit_full[2] unit_vec[2] unit_empty[2] drain
+  static constexpr int NBAR = 3 + 6 + 4 + 5 + 6 + 1;
   static constexpr int TILES_BYTES = (2 + KS + VS) * TILE_BYTES;  // Q, dO, K[3], V[2]
   static constexpr int MISC = 32;                                 // tmem slot, abort flag, unit ring, stop flag
   static constexpr int SMEM = TILES_BYTES + 2 * VEC_BYTES + NBAR * 8 + MISC;
@@ -92,23 +101,22 @@ __global__ void __launch_bounds__(384, 1)
   const uint32_t sVec = sV + T::VS * T::TILE_BYTES;  // [2] x {-lse2[128], -D[128]}
   const uint32_t sBar = sVec + 2 * T::VEC_BYTES;
   const uint32_t bQf = sBar;            // Q_i loaded
-  const uint32_t bQe = bQf + 8;         // Q stage free (after the unit's last S)
-  const uint32_t bOf = bQe + 8;         // dO_i loaded
-  const uint32_t bOe = bOf + 8;         // dO stage free (after the unit's last dP)
-  const uint32_t bKf = bOe + 8;         // [KS] K slot full
+  const uint32_t bOf = bQf + 8;         // dO_i loaded
+  const uint32_t bQs = bOf + 8;         // Q_i, dO_i copied to tensor memory (256 arrivals): shared tiles free
+  const uint32_t bKf = bQs + 8;         // [KS] K slot full
   const uint32_t bKe = bKf + 8 * T::KS; // [KS] K slot free (after dQ += dS K_j)
   const uint32_t bVf = bKe + 8 * T::KS; // [VS] V slot full
   const uint32_t bVe = bVf + 8 * T::VS; // [VS] V slot free (after dP_j)
-  const uint32_t bS = bVe + 8 * T::VS;  // [2] S_j ready in buffer j & 1
-  const uint32_t bDp = bS + 16;         // dP_j ready
-  const uint32_t bDpc = bDp + 8;        // dP_j copied out of TMEM (256 arrivals)
-  const uint32_t bDs = bDpc + 8;        // dS_j in TMEM (256 arrivals)
+  const uint32_t bS = bVe + 8 * T::VS;  // S_j ready
+  const uint32_t bSr = bS + 8;          // S_j loaded by the compute threads (256 arrivals): S buffer free
+  const uint32_t bDp = bSr + 8;         // dP_j ready
+  const uint32_t bDs = bDp + 8;         // dS_j in TMEM over dP_j (256 arrivals)
   const uint32_t bFin = bDs + 8;        // every MMA of the unit done
   const uint32_t bUf = bFin + 8;        // [2] unit ring entry written
   const uint32_t bUv = bUf + 16;        // [2] its row vectors written (64 arrivals)
   const uint32_t bUe = bUv + 16;        // [2] unit ring entry read
   const uint32_t bDrain = bUe + 16;
-  static_assert(4 + 2 * T::KS + 2 * T::VS + 2 + 4 + 6 + 1 == T::NBAR, "barrier count");
+  static_assert(3 + 2 * T::KS + 2 * T::VS + 5 + 6 + 1 == T::NBAR, "barrier count");
   uint8_t* const misc = smem_raw + (sBar - base) + 8 * T::NBAR;
   uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(misc);
   volatile int* const abort_flag = reinterpret_cast<volatile int*>(misc + 4);
@@ -129,9 +137,8 @@ __global__ void __launch_bounds__(384, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(bQf, 1);
-    mbar_init(bQe, 1);
     mbar_init(bOf, 1);
-    mbar_init(bOe, 1);
+    mbar_init(bQs, 256);
     for (int s = 0; s < T::KS; ++s) {
       mbar_init(bKf + 8u * s, 1);
       mbar_init(bKe + 8u * s, 1);
@@ -141,9 +148,8 @@ __global__ void __launch_bounds__(384, 1)
       mbar_init(bVe + 8u * s, 1);
     }
     mbar_init(bS, 1);
-    mbar_init(bS + 8u, 1);
+    mbar_init(bSr, 256);
     mbar_init(bDp, 1);
-    mbar_init(bDpc, 256);
     mbar_init(bDs, 256);
     mbar_init(bFin, 1);
     for (int s = 0; s < 2; ++s) {
@@ -185,8 +191,40 @@ __global__ void __launch_bounds__(384, 1)
     const int X = warp >> 2;
     const int r = threadIdx.x & 127;  // query row within the tile == TMEM lane
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
-    const uint32_t tdP = tmem + 256 + 64 * X + lane_off;
+    const uint32_t tS = tmem + 64 * X + lane_off;          // S columns of this half
+    const uint32_t tdP = tmem + 128 + 64 * X + lane_off;   // dP columns of this half; dS pairs after
     const float2 c2 = make_float2(p.scale_log2, p.scale_log2);
+    // Row r of a [128 x D] bf16 tile in shared memory (128-byte swizzle,
+    // 64-column blocks), columns [X D/2, (X + 1) D/2), as bf16 pairs into
+    // tensor-memory columns [X D/4, (X + 1) D/4) from tcol: the A operand
+    // layout (column c holds elements 2c, 2c + 1 of the row).
+    auto stage_half = [&](uint32_t stile, uint32_t tcol) {
+      constexpr int CH = D / 16;  // 16-byte chunks in the half
+      uint32_t w[4 * CH];
+#pragma unroll
+      for (int c = 0; c < CH; ++c) {
+        const int cg = X * CH + c;
+        const uint4 v = ld_shared_v4u(stile + (uint32_t)(cg >> 3) * T::BLOCK_BYTES + sw128_offset(r, cg & 7));
+        w[4 * c] = v.x;
+        w[4 * c + 1] = v.y;
+        w[4 * c + 2] = v.z;
+        w[4 * c + 3] = v.w;
+      }
+      const uint32_t t0 = tcol + X * (D / 4) + lane_off;
+#pragma unroll
+      for (int o = 0; o + 16 <= 4 * CH; o += 16) {
+        uint32_t q[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) q[e] = w[o + e];
+        tmem_st16(t0 + o, q);
+      }
+      if constexpr ((4 * CH) % 16 != 0) {
+        uint32_t q[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) q[e] = w[4 * CH - 8 + e];
+        tmem_st8(t0 + 4 * CH - 8, q);
+      }
+    };
     uint32_t gs = 0;  // steps over all units so far
     int kf = 0;       // units with steps so far
     bool ok = true;
@@ -217,14 +255,23 @@ __global__ void __launch_bounds__(384, 1)
             *reinterpret_cast<uint4*>(dqrow + 8 * c8) = make_uint4(0, 0, 0, 0);
         continue;
       }
+      // Q_i and dO_i into tensor memory.  The unit before has finished every
+      // product (its epilogue waited for that), so their columns are free.
+      ok = __all_sync(0xffffffffu, wait_bounded(wc, bQf, kf & 1, wait_site(0xf1, k)) &&
+                                       wait_bounded(wc, bOf, kf & 1, wait_site(0xf2, k)));
+      if (!ok) break;
+      stage_half(sQ, tmem + 384);
+      stage_half(sdO, tmem + 448);
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(bQs);  // (also: the shared Q and dO tiles may be overwritten)
       const float2 l22 = make_float2(l2, l2), nD2 = make_float2(nD, nD);
       // Key columns at or past lim0 - 128 j of key tile j are invisible to
       // row r: keys past Nk, and for causal rows keys past position
       // koff + 128 i + r.
       const int lim0 = (CAUSAL ? min(p.Nk, p.koff + 128 * i + r + 1) : p.Nk) - 64 * X;
       for (int j = 0; j < n; ++j, ++gs) {
-        const uint32_t tS = tmem + (gs & 1) * 128 + 64 * X + lane_off;
-        ok = __all_sync(0xffffffffu, wait_bounded(wc, bS + 8u * (gs & 1), (gs >> 1) & 1, wait_site(0xb3, j)));
+        ok = __all_sync(0xffffffffu, wait_bounded(wc, bS, gs & 1, wait_site(0xb3, j)));
         if (!ok) break;
         tc_fence_after();
         float x[64];
@@ -241,6 +288,8 @@ __global__ void __launch_bounds__(384, 1)
             x[32 + q] = __uint_as_float(rb[q]);
           }
         }
+        tc_fence_before();
+        mbar_arrive(bSr);  // the S buffer may take S_{j+1}
         // P[r][k] = exp2(S * scale * log2e - lse2[r]); invisible keys (past
         // the row's causal position, or past Nk) are exactly 0.
 #pragma unroll
@@ -260,7 +309,8 @@ __global__ void __launch_bounds__(384, 1)
         ok = __all_sync(0xffffffffu, wait_bounded(wc, bDp, gs & 1, wait_site(0xb4, j)));
         if (!ok) break;
         tc_fence_after();
-        // dS[r][k] = P * (dP - D) -> bf16 pairs over this warpgroup's S columns
+        // dS[r][k] = P * (dP - D) -> bf16 pairs over this warpgroup's first
+        // 32 dP columns (read before they are written)
         uint32_t w[32];
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
@@ -276,9 +326,7 @@ __global__ void __launch_bounds__(384, 1)
             w[16 * hh + q] = pack_bf16(ds.x, ds.y);
           }
         }
-        tc_fence_before();
-        mbar_arrive(bDpc);  // the dP columns may be overwritten
-        tmem_st32(tS, w);
+        tmem_st32(tdP, w);
         tmem_wait_st();
         tc_fence_before();
         mbar_arrive(bDs);
@@ -289,15 +337,15 @@ __global__ void __launch_bounds__(384, 1)
       // warpgroup X takes the 32-column groups [X GH, min(G, (X + 1) GH)),
       // and each warp writes its 32 rows a row slice per group of lanes
       // (store_rows_transposed), whole lines per store.  The next unit's
-      // first dQ product, which overwrites the accumulator, waits for this
-      // warpgroup's next dS, published after these loads.
+      // products wait for its Q and dO in tensor memory, copied after these
+      // loads.
       ok = __all_sync(0xffffffffu, wait_bounded(wc, bFin, kf & 1, wait_site(0xb5, k)));
       if (!ok) break;
       ++kf;
       tc_fence_after();
       {
         constexpr int G = D / 32, GH = (G + 1) / 2;
-        const uint32_t tQd = tmem + 384 + lane_off;
+        const uint32_t tQd = tmem + 256 + lane_off;
         const float2 s2 = make_float2(p.scale, p.scale);
         const int wr0 = 128 * i + 32 * (warp & 3);  // the warp's first row
         uint16_t* const wdst = p.dq + ((size_t)bh * p.N + wr0) * D;
@@ -322,10 +370,32 @@ __global__ void __launch_bounds__(384, 1)
             ch[q4] = make_uint4(ww[0], ww[1], ww[2], ww[3]);
           }
         };
+        // Columns 32 cc .. 32 cc + 63 (two groups): both loads in flight before one wait.
+        auto chunks2 = [&](int cc, uint4 (&ch)[8]) {
+          uint32_t o0[32], o1[32];
+          tmem_ld32(tQd + cc * 32, o0);
+          tmem_ld32(tQd + cc * 32 + 32, o1);
+          tmem_wait_ld();
+          reg_fence(o0);
+          reg_fence(o1);
+          auto cvt = [&](const uint32_t (&o)[32], uint4* c) {
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) {
+              uint32_t wq[4];
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const float2 t = fmul2(make_float2(__uint_as_float(o[q4 * 8 + 2 * e]), __uint_as_float(o[q4 * 8 + 2 * e + 1])), s2);
+                wq[e] = pack_bf16(t.x, t.y);
+              }
+              c[q4] = make_uint4(wq[0], wq[1], wq[2], wq[3]);
+            }
+          };
+          cvt(o0, ch);
+          cvt(o1, ch + 4);
+        };
         if (X == 0 && GH == 2) {
           uint4 ch[8];
-          chunks(0, ch);
-          chunks(1, ch + 4);
+          chunks2(0, ch);
           store_rows_transposed<8>(ch, wdst, D, nvalid);
         } else if (X == 0) {
           uint4 ch[4];
@@ -333,8 +403,7 @@ __global__ void __launch_bounds__(384, 1)
           store_rows_transposed<4>(ch, wdst, D, nvalid);
         } else if (G - GH == 2) {
           uint4 ch[8];
-          chunks(GH, ch);
-          chunks(GH + 1, ch + 4);
+          chunks2(GH, ch);
           store_rows_transposed<8>(ch, wdst + GH * 32, D, nvalid);
         } else {
           uint4 ch[4];
@@ -349,12 +418,12 @@ __global__ void __launch_bounds__(384, 1)
     reg_split_sync(384);
     if (warp == 8) {
       // ------------------------------------------------------------ producer: Q, dO, K, V
-      // Per unit, in the order the MMA warp consumes them: Q_i (once the
-      // previous unit's last S has read its stage), K_0, dO_i (once the
-      // previous unit's last dP has read its stage), V_0, then K_j, V_j.
-      // The K and V slots and phases follow the step count over all units.
+      // Per unit: Q_i and dO_i (once the compute threads have copied the
+      // previous unit's tiles to tensor memory), then K_j, V_j in the order
+      // the MMA warp consumes them.  The K and V slots and phases follow the
+      // step count over all units.
       bool ok = true;
-      int kq = 0, ko = 0;  // units with steps whose Q, whose dO were issued
+      int kq = 0;       // units with steps whose Q and dO were issued
       uint32_t gk = 0;  // K tiles issued over all units (== steps)
       uint32_t gv = 0;  // V tiles issued
       if (lane == 0) {
@@ -374,7 +443,7 @@ __global__ void __launch_bounds__(384, 1)
           const int bhk = b * p.Hkv + h / p.G;
           auto load_k = [&](int j) -> bool {
             const uint32_t s = gk % T::KS, rd = gk / T::KS;
-            if (rd > 0 && !wait_bounded(wc, bKe + 8u * s, (rd - 1) & 1, wait_site(0xb8, j))) return false;
+            if (rd > 0 && !wait_bounded(wc, bKe + 8u * s, (rd - 1) & 1, wait_site(0xb9, j))) return false;
             // (p.debug_drop_p: a test of the bounded waits skips one K load of unit 0)
             if (!(u == 0 && p.debug_drop_p == j + 1)) {
               mbar_expect_tx(bKf + 8u * s, T::TILE_BYTES);
@@ -393,29 +462,25 @@ __global__ void __launch_bounds__(384, 1)
             ++gv;
             return true;
           };
-          ok = kq == 0 || wait_bounded(wc, bQe, (kq - 1) & 1, wait_site(0xb7, k));
+          ok = kq == 0 || wait_bounded(wc, bQs, (kq - 1) & 1, wait_site(0xb8, k));
           if (ok) {
             mbar_expect_tx(bQf, T::TILE_BYTES);
             for (int cb = 0; cb < T::NB; ++cb) tma_load_3d(sQ + cb * T::BLOCK_BYTES, &tmQ, bQf, cb * 64, i * 128, bh);
-            ++kq;
-            ok = load_k(0);
-          }
-          if (ok) ok = ko == 0 || wait_bounded(wc, bOe, (ko - 1) & 1, wait_site(0xb9, k));
-          if (ok) {
             mbar_expect_tx(bOf, T::TILE_BYTES);
             for (int cb = 0; cb < T::NB; ++cb) tma_load_3d(sdO + cb * T::BLOCK_BYTES, &tmdO, bOf, cb * 64, i * 128, bh);
-            ++ko;
-            ok = load_v(0);
+            ++kq;
           }
-          for (int j = 1; j < n && ok; ++j) ok = load_k(j) && load_v(j);
+          for (int j = 0; j < n && ok; ++j) ok = load_k(j) && load_v(j);
         }
         ok = __shfl_sync(0xffffffffu, ok, 0);
       }
       // Every copy issued above has landed before the CTA may exit (bounded:
       // after an abort, or a load the test hook skipped, some never do).
       if (lane == 0) {
-        if (kq > 0) wait_drain(bQf, (kq - 1) & 1, p.limit_ns);
-        if (ko > 0) wait_drain(bOf, (ko - 1) & 1, p.limit_ns);
+        if (kq > 0) {
+          wait_drain(bQf, (kq - 1) & 1, p.limit_ns);
+          wait_drain(bOf, (kq - 1) & 1, p.limit_ns);
+        }
         for (uint32_t s = 0; s < T::KS && s < gk; ++s) {
           const uint32_t last = ((gk - 1 - s) / T::KS) * T::KS + s;
           wait_drain(bKf + 8u * s, (last / T::KS) & 1, p.limit_ns);
@@ -428,29 +493,26 @@ __global__ void __launch_bounds__(384, 1)
       __syncwarp();
     } else if (warp == 9) {
       // ------------------------------------------------------------ MMA issuer
-      // bwd_dq_kernel's schedule for each unit in turn; per step j:
-      // dP_{j+1} (once dP_j has been read), dQ += dS_j K_j, S_{j+2} into the
-      // S buffer dS_j occupied.  Buffers, slots and per-step barrier phases
-      // follow the step count over all units.  A unit's first products wait
-      // for its Q, dO, K_0, V_0 and for the previous unit's last dP to have
-      // been read; the S buffers they overwrite were last read by dQ
-      // products issued before them (MMAs from one thread run in order).
+      // Per unit: S_0 and dP_0 once Q_i and dO_i are in tensor memory; then
+      // per step j: S_{j+1} once the compute threads have loaded S_j,
+      // dQ += dS_j K_j once dS_j is written, dP_{j+1} over dS_j (MMAs from
+      // one thread run in order, so dQ_j has read dS_j first).  Slots and
+      // per-step barrier phases follow the step count over all units.
       {
         const uint32_t leader = elect_one();
-        constexpr uint32_t I_SS = idesc_bf16_f32(128, 128, false, false);  // S, dP (K-major x K-major)
-        constexpr uint32_t I_DQ = idesc_bf16_f32(128, D, false, true);     // dQ (A in TMEM, B MN-major)
-        const uint32_t tdP = tmem + 256, tdQ = tmem + 384;
-        const uint64_t dQk = sdesc_sw128(sQ, 16, 1024);                 // Q, K-major A
-        const uint64_t dOk = sdesc_sw128(sdO, 16, 1024);                // dO, K-major A
+        constexpr uint32_t I_S = idesc_bf16_f32(128, 128, false, false);  // S, dP (A in TMEM, B K-major)
+        constexpr uint32_t I_DQ = idesc_bf16_f32(128, D, false, true);    // dQ (A in TMEM, B MN-major)
+        const uint32_t tS = tmem, tdP = tmem + 128, tdQ = tmem + 256, tQ = tmem + 384, tO = tmem + 448;
         const uint64_t dKk0 = sdesc_sw128(sK, 16, 1024);                // K slot 0, K-major B (S)
         const uint64_t dKmn0 = sdesc_sw128(sK, T::BLOCK_BYTES, 1024);   // K slot 0, MN-major B (dQ)
         const uint64_t dVk0 = sdesc_sw128(sV, 16, 1024);                // V slot 0, K-major B (dP)
-        auto mma_kk = [&](uint32_t dst, uint64_t ad, uint64_t bd, uint32_t idesc) {
+        // D (+)= A[tmem] B[smem] over d: A = Q or dO (bf16 pairs, 8 columns
+        // per 16 elements), B = a K-major K or V tile.
+        auto mma_td = [&](uint32_t dst, uint32_t a, uint64_t bd) {
 #pragma unroll
-          for (int kk = 0; kk < T::KSTEPS; ++kk) {
-            const uint32_t off = (kk >> 2) * T::BLOCK_BYTES + (kk & 3) * 32;
-            mma_ss_p(leader, dst, sdesc_add(ad, off), sdesc_add(bd, off), idesc, kk > 0);
-          }
+          for (int kk = 0; kk < T::KSTEPS; ++kk)
+            mma_ts_p(leader, dst, a + 8 * kk, sdesc_add(bd, (kk >> 2) * T::BLOCK_BYTES + (kk & 3) * 32), I_S,
+                     kk > 0 ? 1u : 0u);
         };
         auto wait_all = [&](uint32_t bar, uint32_t parity, int site) {
           return __all_sync(0xffffffffu, wait_bounded(wc, bar, parity, site));
@@ -458,7 +520,8 @@ __global__ void __launch_bounds__(384, 1)
         // K_g and V_g (step g over all units) loaded.
         auto k_full = [&](uint32_t g, int site) { return wait_all(bKf + 8u * (g % T::KS), (g / T::KS) & 1, site); };
         auto v_full = [&](uint32_t g, int site) { return wait_all(bVf + 8u * (g % T::VS), (g / T::VS) & 1, site); };
-        auto s_buf = [&](uint32_t g) { return tmem + (g & 1) * 128; };
+        auto k_tile = [&](uint32_t g) { return (g % T::KS) * T::TILE_BYTES; };
+        auto v_tile = [&](uint32_t g) { return (g % T::VS) * T::TILE_BYTES; };
         bool ok = true;
         uint32_t gs = 0;  // steps over all units
         int kq = 0;       // units with steps so far
@@ -469,63 +532,47 @@ __global__ void __launch_bounds__(384, 1)
           unit_of(u, bh, i, n);
           if (n <= 0) continue;
           const uint32_t g0 = gs;
-          // The unit's first products: S_0, dP_0, S_1.  (As in the loop,
-          // the checks for a group run before the previous group's commit.)
-          ok = wait_all(bQf, kq & 1, wait_site(0xbb, k)) && k_full(g0, wait_site(0xbc, 0));
+          // S_0 and dP_0.  (As in the loop, the checks for a product run
+          // before the commit of the one issued before it.)
+          ok = wait_all(bQs, kq & 1, wait_site(0xbb, k)) && k_full(g0, wait_site(0xbc, 0));
           if (!ok) break;
           tc_fence_after();
-          mma_kk(s_buf(g0), dQk, sdesc_add(dKk0, (g0 % T::KS) * T::TILE_BYTES), I_SS);  // S_0
-          // for dP_0: dO_i and V_0 loaded, the previous unit's last dP read
-          ok = wait_all(bOf, kq & 1, wait_site(0xf0, k)) && v_full(g0, wait_site(0xbd, 0)) &&
-               (g0 == 0 || wait_all(bDpc, (g0 - 1) & 1, wait_site(0xbe, 0)));
-          mma_commit_p(leader, bS + 8u * (g0 & 1));
-          if (n == 1) mma_commit_p(leader, bQe);  // Q_i read for the last time
+          mma_td(tS, tQ, sdesc_add(dKk0, k_tile(g0)));  // S_0
+          ok = v_full(g0, wait_site(0xbd, 0));
+          mma_commit_p(leader, bS);
           if (!ok) break;
           tc_fence_after();
-          mma_kk(tdP, dOk, sdesc_add(dVk0, (g0 % T::VS) * T::TILE_BYTES), I_SS);  // dP_0
-          if (n > 1) ok = k_full(g0 + 1, wait_site(0xbc, 1));                  // for S_1
+          mma_td(tdP, tO, sdesc_add(dVk0, v_tile(g0)));  // dP_0
+          if (n > 1) ok = wait_all(bSr, g0 & 1, wait_site(0xbe, 0)) && k_full(g0 + 1, wait_site(0xbc, 1));  // for S_1
           mma_commit_p(leader, bDp);
           mma_commit_p(leader, bVe + 8u * (g0 % T::VS));  // V_0 consumed
-          if (n == 1) mma_commit_p(leader, bOe);          // dO_i read for the last time
-          if (ok && n > 1) {
-            tc_fence_after();
-            mma_kk(s_buf(g0 + 1), dQk, sdesc_add(dKk0, ((g0 + 1) % T::KS) * T::TILE_BYTES), I_SS);  // S_1
-            // for dP_1: V_1 loaded, dP_0 read
-            ok = v_full(g0 + 1, wait_site(0xbd, 1)) && wait_all(bDpc, g0 & 1, wait_site(0xbe, 1));
-            mma_commit_p(leader, bS + 8u * ((g0 + 1) & 1));
-            if (n == 2) mma_commit_p(leader, bQe);
-          }
           for (int j = 0; j < n && ok; ++j) {
             const uint32_t g = g0 + j;
             if (j + 1 < n) {
               tc_fence_after();
-              mma_kk(tdP, dOk, sdesc_add(dVk0, ((g + 1) % T::VS) * T::TILE_BYTES), I_SS);  // dP_{j+1}
-              ok = wait_all(bDs, g & 1, wait_site(0xbf, j));                            // for dQ_j
-              mma_commit_p(leader, bDp);
-              mma_commit_p(leader, bVe + 8u * ((g + 1) % T::VS));
-              if (j + 2 == n) mma_commit_p(leader, bOe);
-            } else {
-              ok = wait_all(bDs, g & 1, wait_site(0xbf, j));
+              mma_td(tS, tQ, sdesc_add(dKk0, k_tile(g + 1)));  // S_{j+1}, over S_j (loaded)
             }
+            ok = wait_all(bDs, g & 1, wait_site(0xbf, j));  // for dQ_j
+            if (j + 1 < n) mma_commit_p(leader, bS);
             if (!ok) break;
             tc_fence_after();
             // dQ += dS_j K_j: A = dS in TMEM (keys 64X.. of warpgroup X at
-            // columns 64X.., bf16 pairs), B = K_j (MN-major, N = d)
-            const uint32_t ks = g % T::KS;
+            // dP columns 64X.., bf16 pairs), B = K_j (MN-major, N = d)
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk)
-              mma_ts_p(leader, tdQ, s_buf(g) + 64 * (kk >> 2) + (kk & 3) * 8,
-                       sdesc_add(dKmn0, ks * T::TILE_BYTES + kk * 2048), I_DQ, (j > 0 || kk > 0) ? 1u : 0u);
-            if (j + 2 < n) ok = k_full(g + 2, wait_site(0xbc, j + 2));  // for S_{j+2}
-            mma_commit_p(leader, bKe + 8u * ks);                        // K_j consumed
+              mma_ts_p(leader, tdQ, tdP + 64 * (kk >> 2) + (kk & 3) * 8,
+                       sdesc_add(dKmn0, k_tile(g) + kk * 2048), I_DQ, (j > 0 || kk > 0) ? 1u : 0u);
+            if (j + 1 < n) ok = v_full(g + 1, wait_site(0xbd, j + 1));  // for dP_{j+1}
+            mma_commit_p(leader, bKe + 8u * (g % T::KS));               // K_j consumed
             if (!ok) break;
-            if (j + 2 < n) {
+            if (j + 1 < n) {
               tc_fence_after();
-              mma_kk(s_buf(g), dQk, sdesc_add(dKk0, ((g + 2) % T::KS) * T::TILE_BYTES), I_SS);  // S_{j+2}
-              // for dP_{j+2}: V_{j+2} loaded, dP_{j+1} read
-              ok = v_full(g + 2, wait_site(0xbd, j + 2)) && wait_all(bDpc, (g + 1) & 1, wait_site(0xbe, j + 1));
-              mma_commit_p(leader, bS + 8u * (g & 1));
-              if (j + 3 == n) mma_commit_p(leader, bQe);
+              mma_td(tdP, tO, sdesc_add(dVk0, v_tile(g + 1)));  // dP_{j+1}, over dS_j (read by dQ_j)
+              // for S_{j+2}: S_{j+1} loaded, K_{j+2} loaded
+              if (j + 2 < n)
+                ok = wait_all(bSr, (g + 1) & 1, wait_site(0xbe, j + 1)) && k_full(g + 2, wait_site(0xbc, j + 2));
+              mma_commit_p(leader, bDp);
+              mma_commit_p(leader, bVe + 8u * ((g + 1) % T::VS));
             }
           }
           if (!ok) break;

@@ -316,11 +316,33 @@ __global__ void __launch_bounds__(384, 1)
           ch[q4] = make_uint4(wq[0], wq[1], wq[2], wq[3]);
         }
       };
+      // Columns 32 cc .. 32 cc + 63 (two groups): both loads in flight before one wait.
+      auto chunks2 = [&](int cc, uint4 (&ch)[8]) {
+        uint32_t o0[32], o1[32];
+        tmem_ld32(src + cc * 32, o0);
+        tmem_ld32(src + cc * 32 + 32, o1);
+        tmem_wait_ld();
+        reg_fence(o0);
+        reg_fence(o1);
+        auto cvt = [&](const uint32_t (&o)[32], uint4* c) {
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4) {
+            uint32_t wq[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float2 t = fmul2(make_float2(__uint_as_float(o[q4 * 8 + 2 * e]), __uint_as_float(o[q4 * 8 + 2 * e + 1])), f2);
+              wq[e] = pack_bf16(t.x, t.y);
+            }
+            c[q4] = make_uint4(wq[0], wq[1], wq[2], wq[3]);
+          }
+        };
+        cvt(o0, ch);
+        cvt(o1, ch + 4);
+      };
 #pragma unroll
       for (int cc = 0; cc + 1 < D / 32; cc += 2) {
         uint4 ch[8];
-        chunks(cc, ch);
-        chunks(cc + 1, ch + 4);
+        chunks2(cc, ch);
         store_rows_transposed<8>(ch, wdst + cc * 32, D, nvalid);
       }
       if constexpr ((D / 32) % 2 != 0) {

@@ -133,7 +133,7 @@ def test_persistent_dkdv_dropped_load_times_out_and_recovers(cuda_lib):
     assert cuda_lib.attn_get_device_status(None) == cuda_lib.Status.OK
 
 
-PERSIST_DQ_SITES = set(range(0xb0, 0xc0)) | {0xf0}
+PERSIST_DQ_SITES = set(range(0xb0, 0xc0)) | {0xf1, 0xf2}
 
 
 def test_persistent_dq_dropped_load_times_out_and_recovers(cuda_lib):
