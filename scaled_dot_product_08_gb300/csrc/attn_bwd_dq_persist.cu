@@ -226,25 +226,51 @@ __global__ void __launch_bounds__(384, 1)
       }
     };
     uint32_t gs = 0;  // steps over all units so far
-    int kf = 0;       // units with steps so far
-    bool ok = true;
-    for (int k = 0; ok; ++k) {
-      // The unit and this row's vectors (-lse2, -D) from ring entry k & 1.
+    int kf = 0;       // units with steps whose products are done
+    int ks = 0;       // units with steps whose Q and dO were copied
+    // A unit as read from ring entry k & 1, with this row's vectors.
+    struct CUnit {
+      int u, bh, i, n;
+      float l2, nD;  // -lse * log2(e) (-inf on padding rows: P = 0 there) and -D
+    };
+    auto take = [&](int k, CUnit& c) -> bool {
       const int e = k & 1;
-      ok = __all_sync(0xffffffffu, wait_bounded(wc, bUf + 8u * e, (k >> 1) & 1, wait_site(0xb1, k)));
-      const int u = ok ? unit_ring[e] : -1;
-      float l2 = -INFINITY, nD = 0.f;
-      if (u >= 0) {
-        ok = __all_sync(0xffffffffu, wait_bounded(wc, bUv + 8u * e, (k >> 1) & 1, wait_site(0xb2, k)));
-        if (ok) {
-          l2 = vec_s[e * 256 + r];
-          nD = vec_s[e * 256 + 128 + r];
+      bool got = __all_sync(0xffffffffu, wait_bounded(wc, bUf + 8u * e, (k >> 1) & 1, wait_site(0xb1, k)));
+      c.u = got ? unit_ring[e] : -1;
+      c.l2 = -INFINITY;
+      c.nD = 0.f;
+      if (c.u >= 0) {
+        got = __all_sync(0xffffffffu, wait_bounded(wc, bUv + 8u * e, (k >> 1) & 1, wait_site(0xb2, k)));
+        if (got) {
+          c.l2 = vec_s[e * 256 + r];
+          c.nD = vec_s[e * 256 + 128 + r];
         }
       }
       mbar_arrive(bUe + 8u * e);
-      if (u < 0 || !ok) break;
-      int bh, i, n;
-      unit_of(u, bh, i, n);
+      c.bh = c.i = c.n = 0;
+      if (c.u >= 0) unit_of(c.u, c.bh, c.i, c.n);
+      return got;
+    };
+    // Q_i and dO_i of a unit with steps into tensor memory; the unit before
+    // has finished every product (the caller waited for that), so their
+    // columns are free.  Then the next unit's tiles may load.
+    auto stage = [&](int k) -> bool {
+      if (!__all_sync(0xffffffffu, wait_bounded(wc, bQf, ks & 1, wait_site(0xf1, k)) &&
+                                       wait_bounded(wc, bOf, ks & 1, wait_site(0xf2, k))))
+        return false;
+      stage_half(sQ, tmem + 384);
+      stage_half(sdO, tmem + 448);
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(bQs);  // (also: the shared Q and dO tiles may be overwritten)
+      ++ks;
+      return true;
+    };
+    CUnit cur;
+    bool ok = take(0, cur);
+    if (ok && cur.u >= 0 && cur.n > 0) ok = stage(0);
+    for (int k = 0; ok && cur.u >= 0; ++k) {
+      const int i = cur.i, n = cur.n, bh = cur.bh;
       if (n <= 0) {
         // No row of the tile sees a key: dQ = 0 (the vector warps wrote the
         // rows' vectors).
@@ -253,19 +279,13 @@ __global__ void __launch_bounds__(384, 1)
         if (row < p.N && ATTN_IN_RANGE(((size_t)bh * p.N + row) * D + D - 1, (size_t)p.B * p.H * p.N * D, p, 0x209))
           for (int c8 = X * (D / 16); c8 < (X + 1) * (D / 16); ++c8)
             *reinterpret_cast<uint4*>(dqrow + 8 * c8) = make_uint4(0, 0, 0, 0);
+        CUnit nx;
+        ok = take(k + 1, nx);
+        if (ok && nx.u >= 0 && nx.n > 0) ok = stage(k + 1);
+        cur = nx;
         continue;
       }
-      // Q_i and dO_i into tensor memory.  The unit before has finished every
-      // product (its epilogue waited for that), so their columns are free.
-      ok = __all_sync(0xffffffffu, wait_bounded(wc, bQf, kf & 1, wait_site(0xf1, k)) &&
-                                       wait_bounded(wc, bOf, kf & 1, wait_site(0xf2, k)));
-      if (!ok) break;
-      stage_half(sQ, tmem + 384);
-      stage_half(sdO, tmem + 448);
-      tmem_wait_st();
-      tc_fence_before();
-      mbar_arrive(bQs);  // (also: the shared Q and dO tiles may be overwritten)
-      const float2 l22 = make_float2(l2, l2), nD2 = make_float2(nD, nD);
+      const float2 l22 = make_float2(cur.l2, cur.l2), nD2 = make_float2(cur.nD, cur.nD);
       // Key columns at or past lim0 - 128 j of key tile j are invisible to
       // row r: keys past Nk, and for causal rows keys past position
       // koff + 128 i + r.
@@ -333,16 +353,23 @@ __global__ void __launch_bounds__(384, 1)
       }
       if (!ok) break;
       // ---------------------------------------------------------- dQ out
-      // dQ_i = scale * (sum_j dS K_j) -> bf16 -> dQ, from registers:
-      // warpgroup X takes the 32-column groups [X GH, min(G, (X + 1) GH)),
-      // and each warp writes its 32 rows a row slice per group of lanes
-      // (store_rows_transposed), whole lines per store.  The next unit's
-      // products wait for its Q and dO in tensor memory, copied after these
-      // loads.
+      // Once every product of the unit is done: the next unit from the
+      // ring, its Q and dO into tensor memory (so that its first products
+      // run during what follows), then dQ_i = scale * (sum_j dS K_j) -> bf16
+      // -> dQ, from registers: warpgroup X takes the 32-column groups
+      // [X GH, min(G, (X + 1) GH)), and each warp writes its 32 rows a row
+      // slice per group of lanes (store_rows_transposed), whole lines per
+      // store.  The next unit's first dQ product, which overwrites the
+      // accumulator, waits for this warpgroup's next dS, published after
+      // these loads.
       ok = __all_sync(0xffffffffu, wait_bounded(wc, bFin, kf & 1, wait_site(0xb5, k)));
       if (!ok) break;
       ++kf;
       tc_fence_after();
+      CUnit nx;
+      ok = take(k + 1, nx);
+      if (ok && nx.u >= 0 && nx.n > 0) ok = stage(k + 1);
+      if (!ok) break;
       {
         constexpr int G = D / 32, GH = (G + 1) / 2;
         const uint32_t tQd = tmem + 256 + lane_off;
@@ -411,6 +438,7 @@ __global__ void __launch_bounds__(384, 1)
           store_rows_transposed<4>(ch, wdst + GH * 32, D, nvalid);
         }
       }
+      cur = nx;
     }
     setmaxnreg_dec<168>();
   } else {
