@@ -228,7 +228,11 @@ __global__ void __launch_bounds__(384, 1)
     uint32_t gs = 0;  // steps over all units so far
     int kf = 0;       // units with steps whose products are done
     int ks = 0;       // units with steps whose Q and dO were copied
-    // A unit as read from ring entry k & 1, with this row's vectors.
+    // A unit as read from ring entry k & 1, with this row's vectors.  The
+    // entry is released when the unit is done (release()), so that the
+    // vector warps run one unit ahead, not two: their reads of O and dO
+    // then come close enough to the producer's dO load for it to find dO in
+    // L2.
     struct CUnit {
       int u, bh, i, n;
       float l2, nD;  // -lse * log2(e) (-inf on padding rows: P = 0 there) and -D
@@ -246,7 +250,7 @@ __global__ void __launch_bounds__(384, 1)
           c.nD = vec_s[e * 256 + 128 + r];
         }
       }
-      mbar_arrive(bUe + 8u * e);
+      if (c.u < 0) mbar_arrive(bUe + 8u * e);
       c.bh = c.i = c.n = 0;
       if (c.u >= 0) unit_of(c.u, c.bh, c.i, c.n);
       return got;
@@ -266,6 +270,7 @@ __global__ void __launch_bounds__(384, 1)
       ++ks;
       return true;
     };
+    auto release = [&](int k) { mbar_arrive(bUe + 8u * (k & 1)); };
     CUnit cur;
     bool ok = take(0, cur);
     if (ok && cur.u >= 0 && cur.n > 0) ok = stage(0);
@@ -279,6 +284,7 @@ __global__ void __launch_bounds__(384, 1)
         if (row < p.N && ATTN_IN_RANGE(((size_t)bh * p.N + row) * D + D - 1, (size_t)p.B * p.H * p.N * D, p, 0x209))
           for (int c8 = X * (D / 16); c8 < (X + 1) * (D / 16); ++c8)
             *reinterpret_cast<uint4*>(dqrow + 8 * c8) = make_uint4(0, 0, 0, 0);
+        release(k);
         CUnit nx;
         ok = take(k + 1, nx);
         if (ok && nx.u >= 0 && nx.n > 0) ok = stage(k + 1);
@@ -438,6 +444,7 @@ __global__ void __launch_bounds__(384, 1)
           store_rows_transposed<4>(ch, wdst + GH * 32, D, nvalid);
         }
       }
+      release(k);
       cur = nx;
     }
     setmaxnreg_dec<168>();
