@@ -72,14 +72,6 @@ constexpr int kDqUnitReaders = 256 + 32 + 32;
 // warpgroups' are taken elsewhere).
 constexpr uint32_t kVecBarrier = 5;
 
-// Asks L2 for a box of a tensor map (no shared memory written, no barrier).
-__device__ __forceinline__ void tma_prefetch_l2_3d(const CUtensorMap* m, int c0, int c1, int c2) {
-  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
-                   reinterpret_cast<uint64_t>(m)),
-               "r"(c0), "r"(c1), "r"(c2)
-               : "memory");
-}
-
 }  // namespace
 
 template <int D, bool CAUSAL>
