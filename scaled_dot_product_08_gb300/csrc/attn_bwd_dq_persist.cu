@@ -27,7 +27,7 @@
 //     a two-entry ring in shared memory, with the unit's row vectors (-lse2,
 //     -D for its 128 query rows), which they form from lse, O and dO in
 //     global memory (or copy from the workspace, when an earlier stage formed
-//     them) while the units before it run; they also write the vectors to
+//     them) while the unit before it runs; they also write the vectors to
 //     the workspace for the dK/dV kernel, and ask L2 for the unit's Q and dO
 //     tiles ahead of the producer's loads;
 //   * the K and V rings and every per-step barrier run on across units, and
