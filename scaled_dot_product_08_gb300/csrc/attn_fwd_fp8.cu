@@ -267,21 +267,56 @@ __global__ void __launch_bounds__(384, 1)
       tc_fence_after();
       const int row = qi * 128 + r;
       const float inv = l > 0.f ? p.o_scale / l : 0.f;
-      uint16_t* const orow = p.o + ((size_t)bh * p.Nq + row) * D;
-#pragma unroll
-      for (int cc = 0; cc < D / 32; ++cc) {
-        uint32_t o[32];
-        tmem_ld32(tO + cc * 32, o);
-        tmem_wait_ld();
-        reg_fence(o);
-        if (row < p.Nq && ATTN_IN_RANGE(((size_t)bh * p.Nq + row) * D + cc * 32 + 31, (size_t)p.B * p.H * p.Nq * D, p, 0x601)) {
+      if constexpr (D == 128) {
+        // The warp's 32 rows, written a row slice per group of lanes
+        // (store_rows_transposed): whole lines per store.  (A/B: d = 128
+        // 285 -> 279 us on c4f8; at d = 64 the shuffles cost more than they
+        // save, 228 -> 234 us on c3cf8, so the other head dims store rows
+        // directly.)
+        const int wr0 = qi * 128 + 32 * (warp & 3);
+        uint16_t* const wdst = p.o + ((size_t)bh * p.Nq + wr0) * D;
+        int nvalid = min(32, p.Nq - wr0);
+        if (nvalid > 0 && !ATTN_IN_RANGE(((size_t)bh * p.Nq + wr0 + nvalid) * D - 1, (size_t)p.B * p.H * p.Nq * D, p, 0x601))
+          nvalid = 0;
+        // Columns 32 cc .. 32 cc + 31 of this thread's row as four bf16 chunks.
+        auto chunks = [&](int cc, uint4* ch) {
+          uint32_t o[32];
+          tmem_ld32(tO + cc * 32, o);
+          tmem_wait_ld();
+          reg_fence(o);
 #pragma unroll
           for (int q4 = 0; q4 < 4; ++q4) {
             uint32_t w[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e)
               w[e] = pack_bf16(__uint_as_float(o[q4 * 8 + 2 * e]) * inv, __uint_as_float(o[q4 * 8 + 2 * e + 1]) * inv);
-            *reinterpret_cast<uint4*>(orow + cc * 32 + q4 * 8) = make_uint4(w[0], w[1], w[2], w[3]);
+            ch[q4] = make_uint4(w[0], w[1], w[2], w[3]);
+          }
+        };
+#pragma unroll
+        for (int cc = 0; cc < D / 32; cc += 2) {
+          uint4 ch[8];
+          chunks(cc, ch);
+          chunks(cc + 1, ch + 4);
+          store_rows_transposed<8>(ch, wdst + cc * 32, D, nvalid);
+        }
+      } else {
+        uint16_t* const orow = p.o + ((size_t)bh * p.Nq + row) * D;
+#pragma unroll
+        for (int cc = 0; cc < D / 32; ++cc) {
+          uint32_t o[32];
+          tmem_ld32(tO + cc * 32, o);
+          tmem_wait_ld();
+          reg_fence(o);
+          if (row < p.Nq && ATTN_IN_RANGE(((size_t)bh * p.Nq + row) * D + cc * 32 + 31, (size_t)p.B * p.H * p.Nq * D, p, 0x601)) {
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) {
+              uint32_t w[4];
+#pragma unroll
+              for (int e = 0; e < 4; ++e)
+                w[e] = pack_bf16(__uint_as_float(o[q4 * 8 + 2 * e]) * inv, __uint_as_float(o[q4 * 8 + 2 * e + 1]) * inv);
+              *reinterpret_cast<uint4*>(orow + cc * 32 + q4 * 8) = make_uint4(w[0], w[1], w[2], w[3]);
+            }
           }
         }
       }
