@@ -123,11 +123,15 @@ def test_keys_nobody_sees_get_zero_gradients(cuda_lib):
     check_grads(g, ref, "padding keys")
 
 
-def test_plain_causal_through_the_masked_path_is_the_dense_result(cuda_lib):
+@pytest.mark.parametrize("d,N", [(128, 777), (96, 333), (64, 461)])
+def test_plain_causal_through_the_masked_path_is_the_dense_result(cuda_lib, d, N):
     # No window, no lengths, no mask: the masked instance visits the same
-    # tiles and masks the same entries as the dense causal kernels.
-    B, H, Hkv, N, d = 2, 4, 2, 777, 128
-    q, k, v, do = (dev(x) for x in _problem(B, H, Hkv, N, N, d, 45000))
+    # tiles and masks the same entries as the dense causal kernels (which
+    # are the persistent ones, so this also checks them against the
+    # launch-per-unit kernels bit for bit, epilogues of every head dim
+    # included).
+    B, H, Hkv = 2, 4, 2
+    q, k, v, do = (dev(x) for x in _problem(B, H, Hkv, N, N, d, 45000 + d))
     for causal in (False, True):
         Od, ld = cuda_lib.forward(q, k, v, 0.1, causal)
         gd = cuda_lib.backward(q, k, v, Od, ld, do, 0.1, causal)
