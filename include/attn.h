@@ -472,14 +472,15 @@ attn_status_t attn_selftest_wait_timeout(unsigned int timeout_us, void* stream);
  * otherwise; 4: the persistent dK/dV kernel, which serves the dense second
  * stage otherwise, kernel 2 being the launch-per-unit one; 5: the persistent
  * dQ kernel, which serves the dense first stage otherwise, kernel 1 being
- * the launch-per-unit one) runs with every on-chip wait limited to
- * `limit_us` microseconds, and in its first CTA (kernels 3, 4, 5: the CTA
- * that takes the first work unit) the TMA producer does not issue its
- * `load_index`-th ring load of that unit (forward: K_0, V_0, K_1, ...; dQ:
- * the same; dK/dV: the query tiles Q_i with their row vectors; persistent
- * dQ: the key tiles K_0, K_1, ...).  The consumers of that load then
- * wait in vain: the first wait to run out records ATTN_ERR_TIMEOUT in the
- * device status word (attn_get_device_status) and where it gave up
+ * the launch-per-unit one; 6: the FP8 forward, attn_fwd_fp8) runs with
+ * every on-chip wait limited to `limit_us` microseconds, and in its first
+ * CTA (kernels 3, 4, 5, and 6 at head_dim 64 / 96: the CTA that takes the
+ * first work unit) the TMA producer does not issue its `load_index`-th ring
+ * load of that unit (forward and FP8 forward: K_0, V_0, K_1, ...; dQ: the
+ * same; dK/dV: the query tiles Q_i with their row vectors; persistent dQ:
+ * the key tiles K_0, K_1, ...).  The consumers of that load then wait in
+ * vain: the first wait to run out records ATTN_ERR_TIMEOUT in the device
+ * status word (attn_get_device_status) and where it gave up
  * (attn_get_timeout_info), and every role of that CTA stops and exits, so
  * the context stays usable; the other CTAs complete normally.
  * The outputs of that launch are not valid.  The hook is cleared by the

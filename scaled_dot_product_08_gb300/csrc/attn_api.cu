@@ -43,7 +43,7 @@ unsigned long long wait_limit_ns() {
 
 // The dropped-load test hook (attn_debug_drop_load): armed for one launch of
 // one kernel, then cleared.  kernel: 0 forward, 1 dQ, 2 dK/dV, and the
-// persistent kernels 3 forward, 4 dK/dV, 5 dQ.
+// persistent kernels 3 forward, 4 dK/dV, 5 dQ; 6 the FP8 forward.
 std::mutex g_debug_mu;
 int g_debug_kernel = -1, g_debug_drop1 = 0;
 unsigned long long g_debug_limit_ns = 0;
@@ -743,6 +743,7 @@ attn_status_t attn_fwd_fp8(const void* q, const void* k, const void* v, void* o,
   p.status = di->status;
   p.limit_ns = wait_limit_ns();
   p.info = di->info;
+  take_debug(6, &p.debug_drop_p, &p.limit_ns);
   return sdpa::launch_fwd_fp8(d, causal != 0, tq, tk, tv, p, static_cast<cudaStream_t>(stream)) == cudaSuccess
              ? ATTN_OK
              : ATTN_ERR_LAUNCH;
@@ -1158,7 +1159,7 @@ attn_status_t attn_selftest_wait_timeout(unsigned int timeout_us, void* stream) 
 }
 
 attn_status_t attn_debug_drop_load(int kernel, int load_index, unsigned int limit_us) {
-  if (kernel < 0 || kernel > 5 || load_index < 0 || load_index > (1 << 20)) return ATTN_ERR_INVALID_ARG;
+  if (kernel < 0 || kernel > 6 || load_index < 0 || load_index > (1 << 20)) return ATTN_ERR_INVALID_ARG;
   if (limit_us < 1000u || limit_us > 60000000u) return ATTN_ERR_INVALID_ARG;
   std::lock_guard<std::mutex> lk(g_debug_mu);
   g_debug_kernel = kernel;

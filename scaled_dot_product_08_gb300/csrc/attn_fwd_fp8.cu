@@ -359,6 +359,10 @@ __global__ void __launch_bounds__(384, 1)
           for (int w = 0; w < 2; ++w) {
             const int st = t % T::NSTAGE, rd = t / T::NSTAGE;
             if (rd > 0 && !(ok = wait_bounded(wc, bKVe + 8u * st, (rd - 1) & 1, wait_site(0xd1, t)))) break;
+            if (blockIdx.x == 0 && p.debug_drop_p == t + 1) {  // test of the bounded waits only
+              ++t;
+              continue;
+            }
             mbar_expect_tx(bKVf + 8u * st, T::TILE_BYTES);
             tma_load_3d(sKV + st * T::TILE_BYTES, (w == 0) ? &tmK : &tmV, bKVf + 8u * st, 0, j * 128, bhk);
             ++t;
@@ -736,6 +740,10 @@ __global__ void __launch_bounds__(384, 1)
             for (int w = 0; w < 2; ++w) {
               const int st = t % T::NSTAGE, rd = t / T::NSTAGE;
               if (rd > 0 && !(ok = wait_bounded(wc, bKVe + 8u * st, (rd - 1) & 1, wait_site(0xd1, t)))) break;
+              if (u == 0 && p.debug_drop_p == 2 * j + w + 1) {  // test of the bounded waits only
+                ++t;
+                continue;
+              }
               mbar_expect_tx(bKVf + 8u * st, T::TILE_BYTES);
               tma_load_3d(sKV + st * T::TILE_BYTES, (w == 0) ? &tmK : &tmV, bKVf + 8u * st, 0, j * 128, bhk);
               ++t;

@@ -77,6 +77,7 @@ struct FwdParams {
   int* sched;            // persistent forward: this launch's queue (next unit, CTAs done); set by its launcher
   int n_units;           // persistent forward: units in the launch
   int debug_drop_p;      // 0; n > 0 only in a test of the bounded waits: the persistent forward skips unit 0's ring load n - 1
+                         // (the FP8 forward: the same, or CTA 0's, for the one-CTA-per-unit kernel)
 };
 
 // Backward arguments.

@@ -113,7 +113,7 @@ def test_bwd_noalloc_checks_arguments_before_its_scratch(lib):
 def test_debug_drop_load_checks_its_arguments(lib):
     # The failure-path test hook arms nothing on bad arguments (host only).
     import scaled_dot_product_08_gb300 as sdpa
-    assert sdpa.attn_debug_drop_load(6, 0, 20000) == sdpa.Status.INVALID_ARG
+    assert sdpa.attn_debug_drop_load(7, 0, 20000) == sdpa.Status.INVALID_ARG
     assert sdpa.attn_debug_drop_load(-1, 0, 20000) == sdpa.Status.INVALID_ARG
     assert sdpa.attn_debug_drop_load(0, -1, 20000) == sdpa.Status.INVALID_ARG
     assert sdpa.attn_debug_drop_load(0, 0, 999) == sdpa.Status.INVALID_ARG

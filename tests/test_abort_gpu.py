@@ -6,8 +6,9 @@ load must give up, record ATTN_ERR_TIMEOUT with the CTA and the wait site,
 and every role of the CTA must stop and exit (each named barrier is reached
 whatever a wait returned), so that the launch ends and the context stays
 usable.  The CTAs that lost nothing complete normally, and the next normal
-call is correct.  One case per kernel: forward, dQ, dK/dV, and the
-persistent forward, dK/dV and dQ kernels.
+call is correct.  One case per kernel: forward, dQ, dK/dV, the
+persistent forward, dK/dV and dQ kernels, and the FP8 forward (both
+schedules).
 """
 import math
 
@@ -157,4 +158,36 @@ def test_persistent_dq_dropped_load_times_out_and_recovers(cuda_lib):
     assert info[3] >= LIMIT_US * 0.9
     grads = [host(g) for g in cuda_lib.backward(tq, tk, tv, O, lse, tdo, s, True)]
     check_grads(grads, oracle.attention_backward(q, k, v, do, s, True), "after the timeout")
+    assert cuda_lib.attn_get_device_status(None) == cuda_lib.Status.OK
+
+
+FP8_SITES = set(range(0xc1, 0xc6)) | set(range(0xd1, 0xd5)) | set(range(0xe1, 0xeb))
+
+
+@pytest.mark.parametrize("d", [128, 64], ids=["d128_per_unit", "d64_persistent"])
+def test_fp8_forward_dropped_load_times_out_and_recovers(cuda_lib, d):
+    # The FP8 forward (one CTA per unit at d = 128, persistent at d = 64):
+    # the first CTA's producer skips K_1.  The next call equals a call made
+    # before the hook was armed, bit for bit.
+    import torch
+    from sdpa_inputs import quantize_e4m3
+    B, H, N = 1, 2, 512
+    q, k, v, _ = _inputs(B, H, N, d, 66000 + d)
+    (q8, qs), (k8, ks), (v8, vs) = (quantize_e4m3(x) for x in (q, k, v))
+    t8 = [torch.from_numpy(np.ascontiguousarray(x)).cuda() for x in (q8, k8, v8)]
+    s = 1 / math.sqrt(d)
+    O_ref, lse_ref = cuda_lib.forward_fp8(*t8, qs, ks, vs, s, True)
+    torch.cuda.synchronize()
+    assert cuda_lib.attn_get_device_status(None) == cuda_lib.Status.OK
+    assert cuda_lib.attn_debug_drop_load(6, 2, LIMIT_US) == cuda_lib.Status.OK
+    cuda_lib.forward_fp8(*t8, qs, ks, vs, s, True)
+    torch.cuda.synchronize()
+    st, info = cuda_lib.attn_get_timeout_info(None)
+    assert st == cuda_lib.Status.OK
+    assert cuda_lib.attn_get_device_status(None) == cuda_lib.Status.TIMEOUT
+    assert info[0] >> 16 in FP8_SITES, hex(info[0] >> 16)
+    assert info[3] >= LIMIT_US * 0.9
+    O, lse = cuda_lib.forward_fp8(*t8, qs, ks, vs, s, True)
+    torch.cuda.synchronize()
+    assert torch.equal(O, O_ref) and torch.equal(lse, lse_ref)
     assert cuda_lib.attn_get_device_status(None) == cuda_lib.Status.OK
