@@ -20,8 +20,9 @@
 //   * K and V have an empty barrier, committed once the unit's last S^T and
 //     dP^T products are issued (its last step needs only dV and dK, which
 //     read neither), so the next unit's K and V load during that step;
-//   * dK and dV leave from registers straight to global memory, each warp's
-//     rows transposed across its lanes so that a store covers whole lines;
+//   * dK and dV leave from registers to global memory, each warp's rows
+//     transposed through a 4 KB shared-memory scratch of its own so that a
+//     store covers whole lines;
 //   * a unit whose keys no query sees (causal cross attention) writes zeros
 //     and takes no loads or products.
 #include <atomic>
@@ -46,9 +47,12 @@ struct PBTraits {
   static constexpr int NBAR = 2 + 8 + 5 + 4 + 1;
   static constexpr int TILES_BYTES = 6 * TILE_BYTES;  // K, V, Q[2], dO[2]
   static constexpr int MISC = 32;                      // tmem slot, abort flag, unit ring
-  static constexpr int SMEM = TILES_BYTES + 2 * VEC_BYTES + NBAR * 8 + MISC;
+  static constexpr int SCRATCH_BYTES = 8 * 4096;      // a 4 KB epilogue scratch per compute warp
+  static constexpr int SMEM = TILES_BYTES + SCRATCH_BYTES + 2 * VEC_BYTES + NBAR * 8 + MISC;
   static constexpr int THREADS = 384;
 };
+
+static_assert(PBTraits<128>::SMEM <= 227 * 1024, "shared memory");
 
 // Arrivals on unit_empty: every thread that reads a ring entry (the compute
 // warpgroups, the MMA warp and the dO producer warp).
@@ -72,7 +76,8 @@ __global__ void __launch_bounds__(384, 1)
   const uint32_t sV = sK + T::TILE_BYTES;
   const uint32_t sQ = sV + T::TILE_BYTES;            // [2]
   const uint32_t sdO = sQ + 2 * T::TILE_BYTES;       // [2]
-  const uint32_t sVec = sdO + 2 * T::TILE_BYTES;     // [2] x {-lse2[128], -D[128]}
+  const uint32_t sScr = sdO + 2 * T::TILE_BYTES;     // [8] epilogue scratch, one per compute warp
+  const uint32_t sVec = sScr + T::SCRATCH_BYTES;     // [2] x {-lse2[128], -D[128]}
   const uint32_t sBar = sVec + 2 * T::VEC_BYTES;
   const uint32_t bKV = sBar;          // K, V of the unit loaded
   const uint32_t bKVe = bKV + 8;      // K, V no longer read
@@ -291,10 +296,12 @@ __global__ void __launch_bounds__(384, 1)
       const uint32_t src = tmem + (X ? 256u : 384u) + lane_off;
       const float2 f2 = X ? make_float2(p.scale, p.scale) : make_float2(1.f, 1.f);
       // The warp's 32 key rows 128 j + 32 (warp % 4) + lane, written a row
-      // slice per group of lanes (store_rows_transposed): whole 128-byte
-      // lines per store rather than 32 separate 16-byte pieces.
+      // slice per group of lanes through the warp's shared-memory scratch
+      // (store_rows_staged): whole 128-byte lines per store rather than 32
+      // separate 16-byte pieces.
       const int wr0 = 128 * x.j + 32 * (warp & 3);
       uint16_t* const wdst = (X ? p.dk : p.dv) + ((size_t)x.bhk * p.Nk + wr0) * D;
+      const uint32_t scr = sScr + (uint32_t)warp * 4096u;  // this warp's scratch
       int nvalid = min(32, p.Nk - wr0);
       if (nvalid > 0 && !ATTN_IN_RANGE(((size_t)x.bhk * p.Nk + wr0 + nvalid) * D - 1, (size_t)p.B * p.Hkv * p.Nk * D, p, 0x306))
         nvalid = 0;
@@ -343,12 +350,12 @@ __global__ void __launch_bounds__(384, 1)
       for (int cc = 0; cc + 1 < D / 32; cc += 2) {
         uint4 ch[8];
         chunks2(cc, ch);
-        store_rows_transposed<8>(ch, wdst + cc * 32, D, nvalid);
+        store_rows_staged<8>(ch, scr, wdst + cc * 32, D, nvalid);
       }
       if constexpr ((D / 32) % 2 != 0) {
         uint4 ch[4];
         chunks(D / 32 - 1, ch);
-        store_rows_transposed<4>(ch, wdst + (D / 32 - 1) * 32, D, nvalid);
+        store_rows_staged<4>(ch, scr, wdst + (D / 32 - 1) * 32, D, nvalid);
       }
     }
     setmaxnreg_dec<168>();

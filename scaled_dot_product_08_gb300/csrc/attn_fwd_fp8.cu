@@ -59,7 +59,8 @@ struct F8 {
   // persistent kernel's set; the one-CTA-per-unit kernel uses a subset)
   static constexpr int NBAR = 2 + 2 + 2 * NSTAGE + 2 + 4 + 2 + 2 + 2 + 1;
   static constexpr int MISC = 32;  // tmem slot, abort flag, unit ring
-  static constexpr int SMEM = 1024 + (2 + NSTAGE) * TILE_BYTES + NBAR * 8 + MISC;
+  static constexpr int SCRATCH_BYTES = D == 128 ? 8 * 4096 : 0;  // epilogue scratch, one 4 KB per softmax warp
+  static constexpr int SMEM = 1024 + (2 + NSTAGE) * TILE_BYTES + SCRATCH_BYTES + NBAR * 8 + MISC;
   static constexpr int THREADS = 384;
 };
 
@@ -114,7 +115,8 @@ __global__ void __launch_bounds__(384, 1)
 
   const uint32_t sQ = base;                          // 2 query tiles
   const uint32_t sKV = base + 2 * T::TILE_BYTES;     // K/V ring
-  const uint32_t sBar = sKV + T::NSTAGE * T::TILE_BYTES;
+  const uint32_t sScr = sKV + T::NSTAGE * T::TILE_BYTES;  // d = 128: epilogue scratch, 4 KB per softmax warp
+  const uint32_t sBar = sScr + T::SCRATCH_BYTES;
   const uint32_t bQ = sBar;                          // q_full[2]
   const uint32_t bKVf = sBar + 8u * 2;               // kv_full[NSTAGE]
   const uint32_t bKVe = bKVf + 8u * T::NSTAGE;       // kv_empty[NSTAGE]
@@ -285,9 +287,10 @@ __global__ void __launch_bounds__(384, 1)
       const float inv = l > 0.f ? p.o_scale / l : 0.f;
       if constexpr (D == 128) {
         // The warp's 32 rows, written a row slice per group of lanes
-        // (store_rows_transposed): whole lines per store.  (A/B: d = 128
-        // 285 -> 279 us on c4f8; at d = 64 the shuffles cost more than they
-        // save, 228 -> 234 us on c3cf8, so the other head dims store rows
+        // through the warp's shared-memory scratch (store_rows_staged):
+        // whole lines per store.  (A/B with a shuffle transpose: d = 128
+        // 285 -> 279 us on c4f8; at d = 64 it cost more than it saved,
+        // 228 -> 234 us on c3cf8, so the other head dims store rows
         // directly.)
         const int wr0 = qi * 128 + 32 * (warp & 3);
         uint16_t* const wdst = p.o + ((size_t)bh * p.Nq + wr0) * D;
@@ -314,7 +317,7 @@ __global__ void __launch_bounds__(384, 1)
           uint4 ch[8];
           chunks(cc, ch);
           chunks(cc + 1, ch + 4);
-          store_rows_transposed<8>(ch, wdst + cc * 32, D, nvalid);
+          store_rows_staged<8>(ch, sScr + (uint32_t)warp * 4096u, wdst + cc * 32, D, nvalid);
         }
       } else {
         uint16_t* const orow = p.o + ((size_t)bh * p.Nq + row) * D;

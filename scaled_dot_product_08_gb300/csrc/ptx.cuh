@@ -479,6 +479,34 @@ __device__ __forceinline__ void store_rows_sw128(uint32_t stage, uint16_t* dst, 
   }
 }
 
+// The same store through a per-warp 4 KB shared-memory scratch instead of
+// shuffles: each lane writes its row's NCH chunks at a 128-byte pitch (chunk
+// c of row l at slot c ^ (l % 8), so that a warp's writes of one chunk fall
+// on all banks), then reads back chunk L % NCH of row (32 / NCH) s + L / NCH
+// for s = 0 .. NCH - 1 and stores it: each store instruction again covers
+// 32 / NCH whole row slices.  Costs 2 NCH shared-memory accesses per lane
+// where the shuffle transpose costs about 24 NCH instructions.  Rows at or
+// past nvalid are not written.  Every lane of the warp takes part; the
+// scratch is free again when it returns.
+template <int NCH>
+__device__ __forceinline__ void store_rows_staged(const uint4 (&x)[NCH], uint32_t scr, uint16_t* dst, size_t stride,
+                                                  int nvalid) {
+  static_assert(NCH == 4 || NCH == 8, "chunks per row");
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int c = 0; c < NCH; ++c)
+    st_shared_v4(scr + (uint32_t)lane * 128u + ((uint32_t)(c ^ (lane & 7)) << 4), x[c].x, x[c].y, x[c].z, x[c].w);
+  __syncwarp();
+  const int c = lane % NCH;
+#pragma unroll
+  for (int s = 0; s < NCH; ++s) {
+    const int r = (32 / NCH) * s + lane / NCH;
+    const uint4 v = ld_shared_v4u(scr + (uint32_t)r * 128u + ((uint32_t)(c ^ (r & 7)) << 4));
+    if (r < nvalid) *reinterpret_cast<uint4*>(dst + (size_t)r * stride + 8 * c) = v;
+  }
+  __syncwarp();
+}
+
 // Writes 16-byte chunks that the lanes of a warp hold one row each (lane l:
 // row l of the warp's 32 rows, x[k] = columns 8k .. 8k + 7 of a slice that
 // starts at dst for row 0; row r at dst + r * stride elements) so that every
