@@ -625,7 +625,9 @@ __global__ void __launch_bounds__(384, 1)
               k < 2 || __all_sync(0xffffffffu, wait_bounded(wc, bUe + 8u * e, ((k - 2) >> 1) & 1, wait_site(0xb6, k)));
           if (lane == 0) {
             if (ok) {
-              int u = atomicAdd(p.sched, 1);
+              // CTA b's first unit is unit b (no queue round trip before the first
+              // loads); the counter hands out the rest, from gridDim.x on.
+              int u = k == 0 ? (int)blockIdx.x : (int)gridDim.x + atomicAdd(p.sched, 1);
               if (u >= p.n_units) u = -1;
               unit_ring[e] = u;
               mbar_arrive(bUf + 8u * e);  // (release: the entry is visible to the roles that wait for it)

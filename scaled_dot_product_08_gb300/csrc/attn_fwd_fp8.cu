@@ -722,7 +722,9 @@ __global__ void __launch_bounds__(384, 1)
         int nq = 0;  // units whose Q tiles were issued
         for (int k = 0; ok; ++k) {
           const int e = k & 1;
-          int u = atomicAdd(p.sched, 1);
+          // CTA b's first unit is unit b (no queue round trip before the first
+          // loads); the counter hands out the rest, from gridDim.x on.
+          int u = k == 0 ? (int)blockIdx.x : (int)gridDim.x + atomicAdd(p.sched, 1);
           if (u >= p.n_units) u = -1;
           if (k >= 2 && !(ok = wait_bounded(wc, bUe + 8u * e, ((k - 2) >> 1) & 1, wait_site(0xd2, k)))) break;
           unit_ring[e] = u;
